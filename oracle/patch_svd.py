@@ -1,0 +1,26 @@
+"""Patch formation by truncated SVD (oracle; test infrastructure only).
+
+Kamera (gist.science/pt/paper/2606.23581, section 2, patch bullet) forms the
+rank-m patch once: a conditioned pass over [A, B] gives KV(B|A), the deficit
+Delta = KV(B|A) - KV(B|empty) is decomposed by an SVD, and the top-m factors
+are kept.  The model pass is out of scope here; given a Delta, this module
+returns the factors.  Reading: Delta is taken in the destination frame,
+Delta = KV(B|A) - R(delta) KV(B|empty), so that adding U_m V_m^T after the
+relocation reproduces KV(B|A); singular values are folded into U.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def svd_patch(delta_kv: np.ndarray, m: int):
+    """(U_m [T][m], W_m [D][m]) with U_m W_m^T the best rank-m approximation of
+    delta_kv in Frobenius norm; singular values are folded into U_m."""
+    u, s, vt = np.linalg.svd(np.asarray(delta_kv, dtype=np.float64), full_matrices=False)
+    return u[:, :m] * s[None, :m], vt[:m].T
+
+
+def eckart_young_tail(delta_kv: np.ndarray, m: int) -> float:
+    """Sum of the squared singular values beyond the first m."""
+    s = np.linalg.svd(np.asarray(delta_kv, dtype=np.float64), compute_uv=False)
+    return float(np.sum(s[m:] ** 2))
