@@ -1,0 +1,408 @@
+"""Benchmark of the KV relocation + rank-m patch path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+One step = one pass of the whole operator over one workload: every chunk,
+every layer, K and V (one kernel launch through the C ABI).  The default
+workload is the Qwen2.5-VL-7B-shaped GQA video segment (28 layers, 4 KV heads x
+128, one 4096-token chunk, rank-32 patch, 16-token pages through a shuffled
+block table); --config picks another of the five measured workloads.
+
+Prints one JSON line: tokens/s (chunk tokens per second, all layers, K and V),
+the dominant kernel's roofline (algorithmic bytes / mean launch time against
+the measured HBM copy bandwidth), an end-to-end figure through the C ABI with
+host buffers (inputs copied in and results copied out every step), the fp64
+oracle timed on the host cores, and the SM clocks sampled during the timed
+region.  Under torchrun each rank runs its own replica of the workload (the
+path shards into independent chunks; there is no exchange step): weak scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "relocated+patched KV tokens/s and HBM GB/s (fraction of GB300 roofline), 1 GPU"
+KERNEL_SOURCES = ["position_invariant_kv_gb300/csrc/kvrp_kernel.cu", "position_invariant_kv_gb300/csrc/kvrp_plan.h",
+                  "position_invariant_kv_gb300/csrc/kvrp_host.cpp"]
+L2_BYTES = 129 * 2 ** 20
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel, if
+    it was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "relocate_kernel_dram.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    ent = d.get("per_launch", {}).get(workload)
+    return None if ent is None else ent.get("dram_bytes")
+
+
+def workload_text(wl) -> str:
+    chunks = len(wl.chunks)
+    ranks = sorted({c.rank for c in wl.chunks})
+    dst = "paged 16-token pages via shuffled block table" if wl.paged else "contiguous"
+    if wl.family == "mla":
+        shape = f"MLA rows {wl.kv_lora_dim}+{wl.rope_dim}"
+    else:
+        shape = f"{wl.n_heads} KV heads x {wl.head_dim}"
+    return (f"{wl.name}: {wl.n_layers} layers, {shape}, {chunks} chunk(s), {wl.n_chunk_tokens} tokens, "
+            f"rank {'/'.join(map(str, ranks))}, theta {wl.theta:g}, {dst}")
+
+
+# --------------------------------------------------------------------------- #
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        mhz.sort()
+        return {"sm_mhz": mhz[len(mhz) // 2] if mhz else None, "sm_max_mhz": mx, "samples": len(mhz),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- #
+# CPU baseline: the fp64 oracle on a bounded sample, in a fresh process
+# --------------------------------------------------------------------------- #
+class OracleSampler:
+    """The fp64 oracle, as it stands, on rows of one (layer, tensor) slice of
+    the workload's first chunk; a step over n rows stands for n / (layers x
+    tensors) chunk tokens."""
+
+    def __init__(self, cfg: int):
+        import workloads as W
+        from oracle import operator_rows, round_to_bf16_bits, row_layout
+        self._op, self._round = operator_rows, round_to_bf16_bits
+        wl = W.config(cfg)
+        c = wl.chunks[0]
+        self.wl = wl
+        self.slice_wl = W.Workload(wl.name, wl.family, 1, wl.n_heads, wl.head_dim, wl.kv_lora_dim, wl.rope_dim,
+                                   wl.theta, c.n_tokens, wl.num_pages, wl.paged,
+                                   [W.Chunk(0, c.n_tokens, c.delta, c.rank, 0, 0)], wl.block_tables, wl.seed,
+                                   "numpy")
+        self.host = W.host_inputs(self.slice_wl)
+        self.layouts = {n: row_layout(wl.family, n, n_heads=wl.n_heads, head_dim=wl.head_dim,
+                                      kv_lora_dim=wl.kv_lora_dim, rope_dim=wl.rope_dim) for n in wl.tensors}
+        self.delta, self.theta, self.rank = c.delta, wl.theta, c.rank
+        self.n_tokens = c.n_tokens
+        self.layer_tensors = wl.n_layers * len(wl.tensors)
+        self.i = 0
+
+    def step(self, n_rows: int) -> float:
+        """Seconds of oracle time for n_rows rows (cycling through the slice)."""
+        import numpy as np
+        toks = (self.i + np.arange(n_rows)) % self.n_tokens
+        self.i = int(toks[-1] + 1)
+        name = self.wl.tensors[self.i % len(self.wl.tensors)]
+        x = self.host["rows"][name][0, toks]
+        u = self.host["u"][name][0][0, toks] if self.rank else None
+        w = self.host["w"][name][0][0] if self.rank else None
+        t0 = time.perf_counter()
+        self._round(self._op(x, u, w, self.delta, self.theta, self.layouts[name]))
+        return time.perf_counter() - t0
+
+    def tokens(self, n_rows: int) -> float:
+        return n_rows / self.layer_tensors
+
+
+def cpu_baseline_worker(cfg: int, budget_s: float) -> dict:
+    """Times the oracle on whole (layer, tensor) slices until the budget is spent."""
+    o = OracleSampler(cfg)
+    elapsed, rows = 0.0, 0
+    while elapsed < budget_s:
+        elapsed += o.step(o.n_tokens)
+        rows += o.n_tokens
+    return {"value": o.tokens(rows) / elapsed, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows // o.n_tokens} (layer, tensor) slices of {o.n_tokens} rows of {o.wl.name} "
+                      f"(fp64 NumPy, one thread, {elapsed:.1f} s); one chunk token = "
+                      f"{o.layer_tensors} such rows"}
+
+
+def run_cpu_baseline(cfg: int, budget_s: float) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-worker",
+                          "--config", str(cfg), "--budget", str(budget_s)],
+                         capture_output=True, text=True, env=env, timeout=900)
+    if res.returncode != 0:
+        tail = res.stderr.strip().splitlines()[-1] if res.stderr.strip() else "no output"
+        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": "failed: " + tail}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+# --------------------------------------------------------------------------- #
+# our arm
+# --------------------------------------------------------------------------- #
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def bench_ours(args) -> dict:
+    import torch
+    import harness
+    import workloads as W
+    import position_invariant_kv_gb300 as kvrp
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from position_invariant_kv_gb300.build import build
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        torch.distributed.barrier()
+    kvrp.lib()
+
+    wl = W.config(args.config)
+    dwl = harness.DeviceWorkload(wl, f"cuda:{local}")
+    stream = torch.cuda.current_stream()
+    nbytes = wl.algorithmic_bytes()
+    tokens = wl.n_chunk_tokens
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up
+    for _ in range(args.warmup):
+        dwl.run(stream=stream)
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            starts[i].record(stream)
+            dwl.run(stream=stream)
+            ends[i].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = sorted(s.elapsed_time(e) for s, e in zip(starts, ends))
+    mean_launch_ms = sum(launch_ms) / len(launch_ms)
+    status = dwl.status_value()
+
+    ms_t = torch.tensor([total_ms], device=f"cuda:{local}")
+    if world > 1:
+        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(ms_t.item())
+    ms_per_step = total_ms / args.steps
+    value = tokens * world / (total_ms / 1e3 / args.steps)
+
+    # end to end through the C ABI with host buffers: copy the step's inputs in
+    # from pinned memory, run, copy the destination pools out, every step
+    e2e = bench_e2e(dwl, wl, args, stream)
+
+    peaks = measured_peaks()
+    achieved = nbytes["total"] / (mean_launch_ms / 1e3) / 1e9
+    traffic = profiled_traffic(wl.name)
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_text(wl), "tokens_per_step": tokens,
+                   "algorithmic_bytes_per_step": nbytes["total"],
+                   "l2": f"inputs larger than L2 ({nbytes['total'] / 1e6:.0f} MB moved per step vs 129 MB L2)"
+                   if nbytes["total"] > 2 * L2_BYTES else "L2-resident workload (smaller than L2)",
+                   "parallelism": f"replicas x{world}"},
+        "hbm_gbs": nbytes["total"] / (ms_per_step / 1e3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "kernel": "relocate_kernel", "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
+                     if peaks["source"] == "measured" else "fallback 6.8 TB/s",
+                     "mean_launch_us": mean_launch_ms * 1e3, "median_launch_us": launch_ms[len(launch_ms) // 2] * 1e3},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "device_status": status,
+        "patch_tflops": wl.patch_flops() / (mean_launch_ms / 1e3) / 1e12,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = run_cpu_baseline(args.config, args.budget)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return out if rank == 0 else None
+
+
+def bench_e2e(dwl, wl, args, stream) -> dict:
+    import torch
+    host_in, dev_in = [], []
+    for n in wl.tensors:
+        dev_in.append(dwl.rows[n])
+        for t in dwl.u[n] + dwl.w[n]:
+            if t is not None:
+                dev_in.append(t)
+    if dwl.block_tables is not None:
+        dev_in.append(dwl.block_tables)
+    for t in dev_in:
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        host_in.append(h)
+    host_out = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in dwl.pools.values()]
+    bi = sum(t.numel() * t.element_size() for t in host_in)
+    bo = sum(t.numel() * t.element_size() for t in host_out)
+    steps = max(3, min(args.e2e_steps, args.steps))
+
+    def one():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        dwl.run(stream=stream)
+        for h, p in zip(host_out, dwl.pools.values()):
+            h.copy_(p, non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return {"value": wl.n_chunk_tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": bi,
+            "d2h_bytes_per_step": bo, "ms_per_step": dt * 1e3, "steps": steps}
+
+
+# --------------------------------------------------------------------------- #
+# reference arm: the oracle on the host cores
+# --------------------------------------------------------------------------- #
+def bench_reference(args) -> dict:
+    """The oracle timed on the host cores: each step evaluates a bounded number
+    of rows, sized so the whole run stays within about two minutes."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    o = OracleSampler(args.config)
+    probe = o.step(256)
+    rows_per_s = 256 / max(probe, 1e-6)
+    per_step = max(8, min(o.n_tokens, int(rows_per_s * 100.0 / (args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        o.step(per_step)
+    secs = 0.0
+    for _ in range(args.steps):
+        secs += o.step(per_step)
+    value = o.tokens(per_step * args.steps) / secs
+    sample = (f"{per_step} rows per step of one (layer, tensor) slice of {o.wl.name}, fp64 NumPy, one thread; "
+              f"one chunk token = {o.layer_tensors} rows")
+    return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload_text(o.wl), "tokens_per_step": o.tokens(per_step)},
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.cpu_baseline_worker:
+        print(json.dumps(cpu_baseline_worker(args.config, args.budget)))
+        return
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+            os.environ[k] = "1"
+    out = bench_reference(args) if args.impl == "reference" else bench_ours(args)
+    if out is not None:
+        print(json.dumps(out))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * kvrp.h -- C ABI of the GB300 KV relocation + rank-m patch library (libkvrp.so).
+ *
+ * The operator (Kamera, gist.science/pt/paper/2606.23581, section 2 "O Operador
+ * Kamera"; the Korean summary gist.science/ko/paper/2606.23581 section 2 states
+ * the same) reuses a chunk B that was cached on its own, KV(B|empty), at a new
+ * position after a new antecedent A:
+ *
+ *     KV^(B|A) = R(delta) . KV(B|empty) + U_m V_m^T
+ *
+ *   R(delta)   exact RoPE re-rotation of the cached keys by the position shift
+ *              delta (new position - old position), rotate-half convention:
+ *              feature i of a rotated head pairs with feature i + d/2 and the
+ *              pair turns by delta * theta^(-2i/d).  Values are not rotated
+ *              (GQA/MHA); for MLA only the 64-dim k_rope is turned and c_KV is
+ *              reused byte for byte (section 2, family bullets).
+ *   U_m V_m^T  rank-m conditioning patch, added after the rotation, to K and
+ *              to V (each tensor has its own factor pair), or to the whole
+ *              576-wide MLA row (one pair).
+ *
+ * The result is rounded to bf16 and written straight into a paged KV cache:
+ * token t of a chunk lands at position q = dst_start + t of its sequence,
+ * physical page block_table[q / 16], slot q % 16.
+ *
+ * Conventions shared by every entry point
+ *   - bf16 data is passed as raw pointers (uint16 bit patterns).  Rows are
+ *     dense: a token row of one tensor is D contiguous bf16 values, with
+ *     D = n_kv_heads * head_dim (GQA/MHA) or kv_lora_dim + rope_dim (MLA).
+ *   - Canonical source of one tensor: [n_layers][n_tokens][D]; layer l starts
+ *     at src + l * src_layer_stride (elements).
+ *   - Patch factors of one tensor: U_m [n_layers][n_tokens][rank] (token-major)
+ *     and V_m [n_layers][D][rank] (feature-major); layer strides in elements.
+ *     Singular values are expected to be folded into U_m.
+ *   - Destination pool of one tensor: layer l at base + l * layer_stride,
+ *     laid out [num_pages][16][D].  A NULL block_table means a contiguous
+ *     destination (identity table: position q is row q of the layer).
+ *   - Every device pointer is owned by the caller, must be 16-byte aligned
+ *     (block tables: 4-byte aligned) and must stay valid until the stream work
+ *     is done.  Strides and dst_start are in elements; strides must be
+ *     multiples of 8 elements.
+ *   - rank must be 0 or a multiple of 16 up to 128; head_dim must be 64 or
+ *     128; MLA rope_dim must be 64 and kv_lora_dim a multiple of 64.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *     Host-detected problems are returned as kvrp_status before anything is
+ *     enqueued.  Problems only the device can see are OR-ed into *d_status
+ *     (optional, device memory, read it after synchronising):
+ *     KVRP_DEV_BAD_PAGE: a block-table entry was outside [0, num_pages); the
+ *     rows of that page were skipped.  KVRP_DEV_TIMEOUT: an internal pipeline
+ *     wait gave up (it is bounded); the output is incomplete.
+ *   - Destination slots written by one call must not overlap (a bijective
+ *     block table); overlapping slots give an unspecified winner.  Source and
+ *     destination must not overlap.
+ *   - Thread safety: calls may come from several host threads.
+ */
+#ifndef KVRP_H
+#define KVRP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* kvrp_stream_t;
+
+typedef enum kvrp_status {
+  KVRP_OK = 0,
+  KVRP_ERR_INVALID_ARG = 1,   /* a NULL pointer, a size or stride out of range      */
+  KVRP_ERR_ALIGNMENT = 2,     /* a pointer or stride breaks the 16-byte rule        */
+  KVRP_ERR_UNSUPPORTED = 3,   /* head_dim / rank / rope_dim outside the kernel's set */
+  KVRP_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed               */
+  KVRP_ERR_WORKSPACE = 5      /* the batch workspace is missing or too small        */
+} kvrp_status;
+
+#define KVRP_DEV_BAD_PAGE 0x1u
+#define KVRP_DEV_TIMEOUT 0x2u
+
+/* One destination pool (one tensor). */
+typedef struct kvrp_dst {
+  void* base;                 /* bf16 pool; layer l at base + l * layer_stride          */
+  int64_t layer_stride;       /* elements between layers (>= num_pages * 16 * D)        */
+  const int32_t* block_table; /* device int32, one entry per logical page of the
+                                 sequence (>= ceil((dst_start + n_tokens) / 16)); NULL
+                                 = contiguous                                            */
+  int32_t num_pages;          /* physical pages per layer                               */
+  int32_t page_size;          /* tokens per page; must be 16                            */
+  int64_t dst_start;          /* sequence position of the chunk's first token (>= 0)    */
+} kvrp_dst;
+
+/*
+ * kv_relocate_patch -- one GQA/MHA chunk, all layers, K and V, one launch.
+ *   K gets R(delta) + U_K V_K^T; V gets V + U_V V_V^T (section 2, GQA bullet:
+ *   relocate the full keys by re-applying RoPE, patch both K and V; the MHA
+ *   bullet is the same with n_kv_heads = query heads).
+ *   k_src, v_src  canonical K and V, [n_layers][n_tokens][D] at src_layer_stride.
+ *   rank          m; 0 = relocation only (V is then copied byte for byte).
+ *   uk, vk        U_m [L][T][m] and V_m [L][D][m] of the K patch (NULL iff rank 0).
+ *   uv, vv        the same for the V patch.
+ *   rope_theta    RoPE base (theta_i = rope_theta^(-2i/head_dim)).
+ *   delta         position shift, new minus old.
+ */
+kvrp_status kv_relocate_patch(
+    const void* k_src, const void* v_src, int64_t src_layer_stride,
+    int32_t n_layers, int32_t n_tokens, int32_t n_kv_heads, int32_t head_dim,
+    int64_t delta, double rope_theta, int32_t rank,
+    const void* uk, const void* vk, const void* uv, const void* vv,
+    int64_t u_layer_stride, int64_t v_layer_stride,
+    const kvrp_dst* k_dst, const kvrp_dst* v_dst,
+    uint32_t* d_status, kvrp_stream_t stream);
+
+/*
+ * kv_relocate_patch_mla -- one MLA chunk, all layers, one launch (section 2,
+ * MLA bullet: only the decoupled 64-dim k_rope is relocated, c_KV is reused
+ * byte for byte, the patch goes to both channels).
+ *   src   rows [n_layers][n_tokens][kv_lora_dim + rope_dim] = c_KV ++ k_rope.
+ *   u, v  U_m [L][T][m] and V_m [L][kv_lora_dim + rope_dim][m] (NULL iff rank 0).
+ *   With rank 0 the c_KV part of every row is copied bit for bit.
+ */
+kvrp_status kv_relocate_patch_mla(
+    const void* src, int64_t src_layer_stride, int32_t n_layers, int32_t n_tokens,
+    int32_t kv_lora_dim, int32_t rope_dim, int64_t delta, double rope_theta,
+    int32_t rank, const void* u, const void* v,
+    int64_t u_layer_stride, int64_t v_layer_stride,
+    const kvrp_dst* dst, uint32_t* d_status, kvrp_stream_t stream);
+
+/* One chunk of a batch: its own source, shift, patch and destination. */
+typedef struct kvrp_chunk {
+  const void* k_src;          /* [n_layers][n_tokens][D] at src_layer_stride            */
+  const void* v_src;
+  int64_t src_layer_stride;
+  int32_t n_tokens;
+  int32_t rank;               /* 0 = relocation only                                    */
+  int64_t delta;
+  const void* uk;             /* K patch U_m [L][T][m]; NULL iff rank 0                 */
+  const void* vk;             /* K patch V_m [L][D][m]                                  */
+  const void* uv;             /* V patch U_m                                            */
+  const void* vv;             /* V patch V_m                                            */
+  int64_t u_layer_stride;
+  int64_t v_layer_stride;
+  kvrp_dst k_dst;
+  kvrp_dst v_dst;
+} kvrp_chunk;
+
+/*
+ * kv_relocate_batch -- many GQA/MHA chunks, each with its own delta and patch,
+ * in ONE kernel launch (section 3, the three window operations: reorder under
+ * an orbit patch, sliding-window survival with R(delta) alone, recall of an
+ * evicted chunk with a fresh patch).
+ *   chunks      host array of n_chunks descriptors (read before the call returns).
+ *   workspace   device scratch of at least kv_relocate_batch_workspace_size(n_chunks)
+ *               bytes, 256-byte aligned, owned by the caller.  The call writes the
+ *               launch's descriptors there with one host-to-device copy on `stream`;
+ *               do not reuse it for another purpose until the stream work is done.
+ *               Two batch calls may share one workspace only on the same stream.
+ */
+size_t kv_relocate_batch_workspace_size(int32_t n_chunks);
+
+kvrp_status kv_relocate_batch(
+    const kvrp_chunk* chunks, int32_t n_chunks,
+    int32_t n_layers, int32_t n_kv_heads, int32_t head_dim, double rope_theta,
+    void* workspace, size_t workspace_bytes,
+    uint32_t* d_status, kvrp_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kvrp_status_string(kvrp_status status);
+
+/* Text of the last error seen by this host thread (static per thread). */
+const char* kvrp_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t kvrp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVRP_H */

@@ -1,0 +1,24 @@
+"""Python binding of libkvrp, the GB300 KV relocation + rank-m patch library.
+
+Argument marshalling only: every step of the operator runs in the library's
+CUDA kernel.  Names mirror the C ABI in include/kvrp.h:
+
+    kv_relocate_patch        GQA/MHA chunk, all layers, K and V
+    kv_relocate_patch_mla    MLA chunk (c_KV ++ k_rope rows)
+    kv_relocate_batch        many GQA/MHA chunks, each with its own delta and patch
+    kv_relocate_batch_workspace_size
+
+Tensors may be passed as torch CUDA tensors (their data_ptr is used) or as raw
+device addresses (int).  Streams default to torch's current stream.  A status
+other than KVRP_OK raises KvrpError.  There is no CPU fallback: importing the
+package fails when libkvrp.so has not been built.
+"""
+from __future__ import annotations
+
+from ._abi import (  # noqa: F401
+    KVRP_DEV_BAD_PAGE, KVRP_DEV_TIMEOUT, KVRP_OK, KVRP_ERR_INVALID_ARG, KVRP_ERR_ALIGNMENT,
+    KVRP_ERR_UNSUPPORTED, KVRP_ERR_CUDA, KVRP_ERR_WORKSPACE,
+    Dst, Chunk, KvrpError, lib, lib_path,
+    kv_relocate_patch, kv_relocate_patch_mla, kv_relocate_batch, kv_relocate_batch_workspace_size,
+    kvrp_status_string, kvrp_version, EXPORTED_SYMBOLS,
+)

@@ -1,0 +1,200 @@
+"""ctypes declarations of include/kvrp.h and thin wrappers with the same names."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+lib_path = os.path.join(_HERE, "libkvrp.so")
+
+KVRP_OK = 0
+KVRP_ERR_INVALID_ARG = 1
+KVRP_ERR_ALIGNMENT = 2
+KVRP_ERR_UNSUPPORTED = 3
+KVRP_ERR_CUDA = 4
+KVRP_ERR_WORKSPACE = 5
+KVRP_DEV_BAD_PAGE = 0x1
+KVRP_DEV_TIMEOUT = 0x2
+
+EXPORTED_SYMBOLS = (
+    "kv_relocate_patch", "kv_relocate_patch_mla", "kv_relocate_batch",
+    "kv_relocate_batch_workspace_size", "kvrp_status_string", "kvrp_last_error", "kvrp_version",
+)
+
+
+class kvrp_dst(C.Structure):
+    _fields_ = [("base", C.c_void_p), ("layer_stride", C.c_int64), ("block_table", C.c_void_p),
+                ("num_pages", C.c_int32), ("page_size", C.c_int32), ("dst_start", C.c_int64)]
+
+
+class kvrp_chunk(C.Structure):
+    _fields_ = [("k_src", C.c_void_p), ("v_src", C.c_void_p), ("src_layer_stride", C.c_int64),
+                ("n_tokens", C.c_int32), ("rank", C.c_int32), ("delta", C.c_int64),
+                ("uk", C.c_void_p), ("vk", C.c_void_p), ("uv", C.c_void_p), ("vv", C.c_void_p),
+                ("u_layer_stride", C.c_int64), ("v_layer_stride", C.c_int64),
+                ("k_dst", kvrp_dst), ("v_dst", kvrp_dst)]
+
+
+def _load_library():
+    if not os.path.exists(lib_path):
+        raise ImportError(
+            f"libkvrp.so is not built ({lib_path}); run `python -m position_invariant_kv_gb300.build` "
+            "(there is no fallback implementation)")
+    L = C.CDLL(lib_path)
+    st = C.c_int
+    L.kv_relocate_patch.restype = st
+    L.kv_relocate_patch.argtypes = [
+        C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+        C.c_int64, C.c_double, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+        C.c_int64, C.c_int64, C.POINTER(kvrp_dst), C.POINTER(kvrp_dst), C.c_void_p, C.c_void_p]
+    L.kv_relocate_patch_mla.restype = st
+    L.kv_relocate_patch_mla.argtypes = [
+        C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_double,
+        C.c_int32, C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.POINTER(kvrp_dst), C.c_void_p,
+        C.c_void_p]
+    L.kv_relocate_batch_workspace_size.restype = C.c_size_t
+    L.kv_relocate_batch_workspace_size.argtypes = [C.c_int32]
+    L.kv_relocate_batch.restype = st
+    L.kv_relocate_batch.argtypes = [
+        C.POINTER(kvrp_chunk), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double,
+        C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
+    L.kvrp_status_string.restype = C.c_char_p
+    L.kvrp_status_string.argtypes = [C.c_int]
+    L.kvrp_last_error.restype = C.c_char_p
+    L.kvrp_last_error.argtypes = []
+    L.kvrp_version.restype = C.c_int32
+    L.kvrp_version.argtypes = []
+    return L
+
+
+_LIB = None
+
+
+def lib():
+    """The loaded libkvrp.so.  Raises ImportError when it has not been built:
+    there is no other implementation to fall back to."""
+    global _LIB
+    if _LIB is None:
+        _LIB = _load_library()
+    return _LIB
+
+
+class KvrpError(RuntimeError):
+    def __init__(self, status: int):
+        self.status = status
+        msg = lib().kvrp_status_string(status).decode()
+        detail = lib().kvrp_last_error().decode()
+        super().__init__(f"{msg}: {detail}" if detail else msg)
+
+
+def kvrp_status_string(status: int) -> str:
+    return lib().kvrp_status_string(status).decode()
+
+
+def kvrp_version() -> int:
+    return int(lib().kvrp_version())
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _check(status: int):
+    if status != KVRP_OK:
+        raise KvrpError(status)
+
+
+@dataclass
+class Dst:
+    """One destination pool: layer l at base + l * layer_stride elements, laid
+    out [num_pages][16][D]; block_table None means contiguous rows."""
+    base: object
+    num_pages: int
+    layer_stride: int = 0
+    block_table: object = None
+    dst_start: int = 0
+    page_size: int = 16
+
+    def c(self) -> kvrp_dst:
+        return kvrp_dst(_ptr(self.base), int(self.layer_stride), _ptr(self.block_table),
+                        int(self.num_pages), int(self.page_size), int(self.dst_start))
+
+
+@dataclass
+class Chunk:
+    """One chunk of kv_relocate_batch (fields as in struct kvrp_chunk)."""
+    k_src: object
+    v_src: object
+    n_tokens: int
+    delta: int
+    k_dst: Dst
+    v_dst: Dst
+    rank: int = 0
+    uk: object = None
+    vk: object = None
+    uv: object = None
+    vv: object = None
+    src_layer_stride: int = 0
+    u_layer_stride: int = 0
+    v_layer_stride: int = 0
+
+    def c(self) -> kvrp_chunk:
+        return kvrp_chunk(_ptr(self.k_src), _ptr(self.v_src), int(self.src_layer_stride),
+                          int(self.n_tokens), int(self.rank), int(self.delta),
+                          _ptr(self.uk), _ptr(self.vk), _ptr(self.uv), _ptr(self.vv),
+                          int(self.u_layer_stride), int(self.v_layer_stride),
+                          self.k_dst.c(), self.v_dst.c())
+
+
+def kv_relocate_patch(k_src, v_src, *, n_layers: int, n_tokens: int, n_kv_heads: int, head_dim: int,
+                      delta: int, rope_theta: float, k_dst: Dst, v_dst: Dst, rank: int = 0,
+                      uk=None, vk=None, uv=None, vv=None, src_layer_stride: int = 0,
+                      u_layer_stride: int = 0, v_layer_stride: int = 0, d_status=None,
+                      stream=None) -> None:
+    kd, vd = k_dst.c(), v_dst.c()
+    _check(lib().kv_relocate_patch(
+        _ptr(k_src), _ptr(v_src), int(src_layer_stride), int(n_layers), int(n_tokens), int(n_kv_heads),
+        int(head_dim), int(delta), float(rope_theta), int(rank), _ptr(uk), _ptr(vk), _ptr(uv), _ptr(vv),
+        int(u_layer_stride), int(v_layer_stride), C.byref(kd), C.byref(vd), _ptr(d_status),
+        _stream(stream)))
+
+
+def kv_relocate_patch_mla(src, *, n_layers: int, n_tokens: int, kv_lora_dim: int, rope_dim: int,
+                          delta: int, rope_theta: float, dst: Dst, rank: int = 0, u=None, v=None,
+                          src_layer_stride: int = 0, u_layer_stride: int = 0, v_layer_stride: int = 0,
+                          d_status=None, stream=None) -> None:
+    d = dst.c()
+    _check(lib().kv_relocate_patch_mla(
+        _ptr(src), int(src_layer_stride), int(n_layers), int(n_tokens), int(kv_lora_dim), int(rope_dim),
+        int(delta), float(rope_theta), int(rank), _ptr(u), _ptr(v), int(u_layer_stride),
+        int(v_layer_stride), C.byref(d), _ptr(d_status), _stream(stream)))
+
+
+def kv_relocate_batch_workspace_size(n_chunks: int) -> int:
+    return int(lib().kv_relocate_batch_workspace_size(int(n_chunks)))
+
+
+def kv_relocate_batch(chunks: Sequence[Chunk], *, n_layers: int, n_kv_heads: int, head_dim: int,
+                      rope_theta: float, workspace, workspace_bytes: Optional[int] = None,
+                      d_status=None, stream=None) -> None:
+    arr = (kvrp_chunk * max(1, len(chunks)))(*[c.c() for c in chunks])
+    if workspace_bytes is None:
+        workspace_bytes = int(workspace.numel() * workspace.element_size())
+    _check(lib().kv_relocate_batch(
+        arr, len(chunks), int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
+        _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))

@@ -1,0 +1,617 @@
+// Host side of libkvrp: argument checks, per-chunk phase tables, TMA tensor
+// maps, the launch plan, and the three public entry points of kvrp.h.
+//
+// Operator: Kamera, gist.science/pt/paper/2606.23581, section 2 "O Operador
+// Kamera" (KV^(B|A) = R(delta) KV(B|empty) + U_m V_m^T; GQA/MHA/MLA bullets)
+// and section 3 (reorder, sliding-window survival and recall as many chunks
+// with their own delta and patch, served here by kv_relocate_batch).
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kvrp.h"
+#include "kvrp_plan.h"
+
+namespace kvrp {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+kvrp_status fail(kvrp_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+kvrp_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVRP_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// Per-device state: SM count, shared-memory limit, driver entry point.
+// ---------------------------------------------------------------------------
+struct DeviceInfo {
+  int sms = 0;
+  int smem_optin = 0;
+  int prepared_smem = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_dev;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+kvrp_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(KVRP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  DeviceInfo& d = g_dev[dev];
+  if (d.sms == 0) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(smem)");
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3) {
+      d.sms = 0;
+      return fail(KVRP_ERR_UNSUPPORTED, "libkvrp is built for sm_103a; device %d is sm_%d%d", dev, major,
+                  minor);
+    }
+  }
+  *out = &d;
+  return KVRP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Phase tables: phi_i = delta * theta^(-2i/d) in fp64; cos and sin split into a
+// 16-significant-bit head (so that a bf16 times the head is exact in fp32) and
+// an fp32 tail holding the rest of the fp64 value.
+// ---------------------------------------------------------------------------
+float head16(double v) {
+  if (v == 0.0) return 0.0f;
+  int e = 0;
+  const double m = std::frexp(v, &e);
+  return static_cast<float>(std::ldexp(std::nearbyint(std::ldexp(m, 16)), e - 16));
+}
+
+void phase_table(int64_t delta, double theta, int rot_dim, float4* tab) {
+  for (int i = 0; i < kTablePairs; ++i) tab[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < rot_dim / 2; ++i) {
+    const double inv = std::pow(theta, -2.0 * i / rot_dim);
+    const double phi = static_cast<double>(delta) * inv;
+    const double c = std::cos(phi), s = std::sin(phi);
+    const float ch = head16(c), sh = head16(s);
+    tab[i] = make_float4(ch, sh, static_cast<float>(c - ch), static_cast<float>(s - sh));
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Chunk descriptions common to every entry point.
+// ---------------------------------------------------------------------------
+struct TensorIn {
+  const void* src;
+  const void* u;
+  const void* w;
+  kvrp_dst dst;
+  int rot_kind;
+  int rot_from;
+};
+struct ChunkIn {
+  TensorIn t[2];
+  int n_tensors;
+  int64_t src_layer_stride, u_layer_stride, w_layer_stride;
+  int32_t n_tokens, rank;
+  int64_t delta;
+};
+struct Shape {
+  int n_layers;
+  int D;
+  int rot_dim;   // 0 when nothing turns
+  double theta;
+};
+
+kvrp_status check_dst(const kvrp_dst* d, const char* name, int64_t n_tokens, const Shape& sh) {
+  if (!d) return fail(KVRP_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!d->base) return fail(KVRP_ERR_INVALID_ARG, "%s.base is NULL", name);
+  if (!aligned16(d->base)) return fail(KVRP_ERR_ALIGNMENT, "%s.base is not 16-byte aligned", name);
+  if (d->page_size != kPage) return fail(KVRP_ERR_UNSUPPORTED, "%s.page_size must be 16", name);
+  if (d->num_pages <= 0 || (int64_t)d->num_pages * kPage > (1ll << 31) - 1)
+    return fail(KVRP_ERR_INVALID_ARG, "%s.num_pages out of range", name);
+  if (d->dst_start < 0) return fail(KVRP_ERR_INVALID_ARG, "%s.dst_start is negative", name);
+  const int64_t pool = (int64_t)d->num_pages * kPage * sh.D;
+  if (sh.n_layers > 1 && d->layer_stride < pool)
+    return fail(KVRP_ERR_INVALID_ARG, "%s.layer_stride smaller than one layer's pool", name);
+  if (d->layer_stride % 8 != 0) return fail(KVRP_ERR_ALIGNMENT, "%s.layer_stride not a multiple of 8", name);
+  if (d->block_table) {
+    if (reinterpret_cast<uintptr_t>(d->block_table) & 3u)
+      return fail(KVRP_ERR_ALIGNMENT, "%s.block_table is not 4-byte aligned", name);
+  } else if (d->dst_start + n_tokens > (int64_t)d->num_pages * kPage) {
+    return fail(KVRP_ERR_INVALID_ARG, "%s: contiguous destination too small for the chunk", name);
+  }
+  return KVRP_OK;
+}
+
+kvrp_status check_chunk(const ChunkIn& c, const Shape& sh) {
+  if (c.n_tokens < 0) return fail(KVRP_ERR_INVALID_ARG, "n_tokens is negative");
+  if (c.rank < 0 || c.rank > kMaxRank || c.rank % 16 != 0)
+    return fail(KVRP_ERR_UNSUPPORTED, "rank must be 0 or a multiple of 16 up to %d (got %d)", kMaxRank, c.rank);
+  if (c.n_tokens > (1 << 30)) return fail(KVRP_ERR_INVALID_ARG, "n_tokens too large");
+  const int64_t rows = c.n_tokens;
+  if (sh.n_layers > 1 && c.src_layer_stride < rows * sh.D)
+    return fail(KVRP_ERR_INVALID_ARG, "src_layer_stride smaller than one layer of rows");
+  if (c.src_layer_stride % 8 != 0) return fail(KVRP_ERR_ALIGNMENT, "src_layer_stride not a multiple of 8");
+  if (c.rank > 0) {
+    if (sh.n_layers > 1 && c.u_layer_stride < rows * c.rank)
+      return fail(KVRP_ERR_INVALID_ARG, "u_layer_stride smaller than one layer of U_m");
+    if (sh.n_layers > 1 && c.w_layer_stride < (int64_t)sh.D * c.rank)
+      return fail(KVRP_ERR_INVALID_ARG, "v_layer_stride smaller than one layer of V_m");
+    if (c.u_layer_stride % 8 != 0 || c.w_layer_stride % 8 != 0)
+      return fail(KVRP_ERR_ALIGNMENT, "factor layer strides must be multiples of 8");
+  }
+  static const char* names[2][3] = {{"k source", "K patch U_m", "K patch V_m"},
+                                    {"v source", "V patch U_m", "V patch V_m"}};
+  for (int t = 0; t < c.n_tensors; ++t) {
+    const TensorIn& ti = c.t[t];
+    if (!ti.src) return fail(KVRP_ERR_INVALID_ARG, "%s is NULL", names[t][0]);
+    if (!aligned16(ti.src)) return fail(KVRP_ERR_ALIGNMENT, "%s is not 16-byte aligned", names[t][0]);
+    if (c.rank > 0) {
+      if (!ti.u || !ti.w) return fail(KVRP_ERR_INVALID_ARG, "rank > 0 needs both patch factors");
+      if (!aligned16(ti.u) || !aligned16(ti.w))
+        return fail(KVRP_ERR_ALIGNMENT, "patch factors must be 16-byte aligned");
+    } else if (ti.u || ti.w) {
+      return fail(KVRP_ERR_INVALID_ARG, "patch factors given with rank 0");
+    }
+    kvrp_status st = check_dst(&ti.dst, t == 0 ? "k_dst" : "v_dst", c.n_tokens, sh);
+    if (st != KVRP_OK) return st;
+  }
+  return KVRP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Plan builder
+// ---------------------------------------------------------------------------
+struct MapKey {
+  const void* base;
+  uint64_t dims[3];
+  uint64_t strides[2];
+  uint32_t box[3];
+  int swz;
+  bool operator<(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) < 0; }
+};
+
+class PlanBuilder {
+ public:
+  explicit PlanBuilder(const Shape& sh) : sh_(sh) {}
+
+  kvrp_status map(const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1_elems,
+                  uint64_t s2_elems, uint32_t b0, uint32_t b1, CUtensorMapSwizzle swz, int32_t* idx) {
+    MapKey k;
+    std::memset(&k, 0, sizeof(k));
+    k.base = base;
+    k.dims[0] = d0; k.dims[1] = d1; k.dims[2] = d2;
+    k.strides[0] = s1_elems * 2; k.strides[1] = s2_elems * 2;
+    k.box[0] = b0; k.box[1] = b1; k.box[2] = 1;
+    k.swz = static_cast<int>(swz);
+    auto found = map_index_.find(k);
+    if (found != map_index_.end()) {
+      *idx = found->second;
+      return KVRP_OK;
+    }
+    CUtensorMap m;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), k.dims,
+                                k.strides, k.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(KVRP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for dims %llu x %llu x %llu",
+                  (int)r, (unsigned long long)d0, (unsigned long long)d1, (unsigned long long)d2);
+    *idx = static_cast<int32_t>(maps_.size());
+    maps_.push_back(m);
+    map_index_[k] = *idx;
+    return KVRP_OK;
+  }
+
+  int32_t table(int64_t delta) {
+    auto f = tab_index_.find(delta);
+    if (f != tab_index_.end()) return f->second;
+    const int32_t idx = static_cast<int32_t>(tabs_.size() / kTablePairs);
+    tabs_.resize(tabs_.size() + kTablePairs);
+    phase_table(delta, sh_.theta, sh_.rot_dim, &tabs_[idx * kTablePairs]);
+    tab_index_[delta] = idx;
+    return idx;
+  }
+
+  kvrp_status add(const ChunkIn& c) {
+    ChunkRec r;
+    std::memset(&r, 0, sizeof(r));
+    r.n_tokens = c.n_tokens;
+    r.rank = c.rank;
+    r.n_tensors = c.n_tensors;
+    r.table = -1;
+    bool any_rot = false;
+    const uint64_t L = static_cast<uint64_t>(sh_.n_layers);
+    const uint64_t T = static_cast<uint64_t>(std::max(c.n_tokens, 1));
+    for (int t = 0; t < c.n_tensors; ++t) {
+      const TensorIn& ti = c.t[t];
+      TensorRec& tr = r.t[t];
+      tr.map_x = tr.map_u = tr.map_w = tr.map_dst = -1;
+      tr.block_table = ti.dst.block_table;
+      tr.dst = static_cast<uint16_t*>(ti.dst.base);
+      tr.dst_layer_stride = ti.dst.layer_stride;
+      tr.dst_start = ti.dst.dst_start;
+      tr.num_pages = ti.dst.num_pages;
+      tr.rot_kind = ti.rot_kind;
+      tr.rot_from = ti.rot_from;
+      any_rot |= ti.rot_kind != kRotNone;
+      const int lead = static_cast<int>(ti.dst.dst_start % kPage);
+      tr.n_tblk = c.n_tokens > 0 ? (lead + c.n_tokens + kTileRows - 1) / kTileRows : 0;
+      tr.item_count = 0;  // filled by finish()
+      if (c.n_tokens == 0) continue;
+      const uint64_t sls = c.src_layer_stride ? c.src_layer_stride : T * sh_.D;
+      kvrp_status st = map(ti.src, sh_.D, T, L, sh_.D, sls, kBoxCols, kTileRows,
+                           CU_TENSOR_MAP_SWIZZLE_128B, &tr.map_x);
+      if (st != KVRP_OK) return st;
+      const uint64_t rows = static_cast<uint64_t>(ti.dst.num_pages) * kPage;
+      const uint64_t dls = ti.dst.layer_stride ? ti.dst.layer_stride : rows * sh_.D;
+      st = map(ti.dst.base, sh_.D, rows, L, sh_.D, dls, kBoxCols, kPage, CU_TENSOR_MAP_SWIZZLE_128B,
+               &tr.map_dst);
+      if (st != KVRP_OK) return st;
+      if (c.rank > 0) {
+        const uint64_t m = static_cast<uint64_t>(c.rank);
+        const uint64_t uls = c.u_layer_stride ? c.u_layer_stride : T * m;
+        const uint64_t wls = c.w_layer_stride ? c.w_layer_stride : (uint64_t)sh_.D * m;
+        st = map(ti.u, m, T, L, m, uls, 16, kTileRows, CU_TENSOR_MAP_SWIZZLE_32B, &tr.map_u);
+        if (st != KVRP_OK) return st;
+        st = map(ti.w, m, sh_.D, L, m, wls, 16, kBoxCols, CU_TENSOR_MAP_SWIZZLE_32B, &tr.map_w);
+        if (st != KVRP_OK) return st;
+      }
+    }
+    if (any_rot && c.n_tokens > 0) r.table = table(c.delta);
+    m_max_ = std::max(m_max_, c.rank);
+    chunks_.push_back(r);
+    return KVRP_OK;
+  }
+
+  // Chooses the item granularity and pipeline depth and serialises the plan.
+  kvrp_status finish(int sms, int smem_optin, uint32_t* status, std::vector<unsigned char>* out,
+                     int* grid, int* smem_bytes) {
+    PlanHdr h;
+    std::memset(&h, 0, sizeof(h));
+    h.n_chunks = static_cast<int32_t>(chunks_.size());
+    h.D = sh_.D;
+    h.n_layers = sh_.n_layers;
+    h.n_sub = (sh_.D + kSubCols - 1) / kSubCols;
+    h.m_max = m_max_;
+    h.status = status;
+    // item granularity: whole rows unless that leaves SMs idle
+    int64_t tiles = 0;
+    for (const ChunkRec& r : chunks_)
+      for (int t = 0; t < r.n_tensors; ++t) tiles += (int64_t)r.t[t].n_tblk * sh_.n_layers;
+    int spi = h.n_sub;
+    while (spi > 1 && tiles * ((h.n_sub + spi - 1) / spi) < 2ll * sms) spi = (spi + 1) / 2;
+    h.subs_per_item = spi;
+    h.n_sg = (h.n_sub + spi - 1) / spi;
+    std::vector<int32_t> ibeg;
+    int64_t items = 0;
+    for (ChunkRec& r : chunks_) {
+      ibeg.push_back(static_cast<int32_t>(items));
+      for (int t = 0; t < r.n_tensors; ++t) {
+        const int64_t n = (int64_t)r.t[t].n_tblk * sh_.n_layers * h.n_sg;
+        r.t[t].item_count = static_cast<int32_t>(n);
+        items += n;
+      }
+    }
+    if (items > (1ll << 31) - 1) return fail(KVRP_ERR_INVALID_ARG, "too many tiles in one launch");
+    ibeg.push_back(static_cast<int32_t>(items));
+    h.n_items = static_cast<int32_t>(items);
+    // pipeline depth from the shared-memory budget (and TMEM: 128 columns a stage)
+    const int budget = smem_optin - 1024;
+    int stages = 0;
+    for (int s = (m_max_ > 0 ? 4 : 6); s >= 2; --s) {
+      if ((int)smem_layout(m_max_, s).total <= budget) {
+        stages = s;
+        break;
+      }
+    }
+    if (stages == 0) return fail(KVRP_ERR_UNSUPPORTED, "rank %d does not fit in shared memory", m_max_);
+    h.stages = stages;
+    h.tmem_cols = 0;
+    if (m_max_ > 0) {
+      h.tmem_cols = 32;
+      while (h.tmem_cols < stages * kSubCols) h.tmem_cols *= 2;
+    }
+    auto align = [](size_t v) { return (v + 127) & ~static_cast<size_t>(127); };
+    size_t off = align(sizeof(PlanHdr));
+    h.off_maps = static_cast<uint32_t>(off);
+    off = align(off + maps_.size() * sizeof(CUtensorMap));
+    h.off_tabs = static_cast<uint32_t>(off);
+    off = align(off + tabs_.size() * sizeof(float4));
+    h.off_chunks = static_cast<uint32_t>(off);
+    off = align(off + chunks_.size() * sizeof(ChunkRec));
+    h.off_ibeg = static_cast<uint32_t>(off);
+    off = align(off + ibeg.size() * sizeof(int32_t));
+    h.total_bytes = static_cast<uint32_t>(off);
+    out->assign(off, 0);
+    std::memcpy(out->data(), &h, sizeof(h));
+    if (!maps_.empty()) std::memcpy(out->data() + h.off_maps, maps_.data(), maps_.size() * sizeof(CUtensorMap));
+    if (!tabs_.empty()) std::memcpy(out->data() + h.off_tabs, tabs_.data(), tabs_.size() * sizeof(float4));
+    std::memcpy(out->data() + h.off_chunks, chunks_.data(), chunks_.size() * sizeof(ChunkRec));
+    std::memcpy(out->data() + h.off_ibeg, ibeg.data(), ibeg.size() * sizeof(int32_t));
+    *grid = static_cast<int>(std::min<int64_t>(items, sms));
+    *smem_bytes = static_cast<int>(smem_layout(m_max_, stages).total) + 1024;
+    return KVRP_OK;
+  }
+
+  // Upper bound of the serialised size for n chunks of up to two tensors.
+  static size_t bound(int64_t n) {
+    auto align = [](size_t v) { return (v + 127) & ~static_cast<size_t>(127); };
+    size_t off = align(sizeof(PlanHdr));
+    off = align(off + (size_t)n * 8 * sizeof(CUtensorMap));
+    off = align(off + (size_t)n * kTablePairs * sizeof(float4));
+    off = align(off + (size_t)n * sizeof(ChunkRec));
+    off = align(off + (size_t)(n + 1) * sizeof(int32_t));
+    return off;
+  }
+
+ private:
+  Shape sh_;
+  int m_max_ = 0;
+  std::vector<CUtensorMap> maps_;
+  std::map<MapKey, int32_t> map_index_;
+  std::vector<float4> tabs_;
+  std::map<int64_t, int32_t> tab_index_;
+  std::vector<ChunkRec> chunks_;
+};
+
+// Builds the plan for `chunks` and launches it: as a kernel parameter when it
+// fits, otherwise through `workspace` (device) with one host-to-device copy.
+kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d_status, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream);
+
+// Pinned staging for batch plans: a small ring per device, so consecutive
+// calls never overwrite a buffer whose copy is still queued.
+struct Staging {
+  struct Slot {
+    void* host = nullptr;
+    size_t cap = 0;
+    cudaEvent_t done = nullptr;
+    bool pending = false;
+  };
+  Slot slot[4];
+  int next = 0;
+};
+std::map<int, Staging> g_staging;
+
+kvrp_status stage_and_copy(const std::vector<unsigned char>& bytes, void* dst, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  Staging& sg = g_staging[dev];
+  Staging::Slot& s = sg.slot[sg.next];
+  sg.next = (sg.next + 1) % 4;
+  if (s.pending) {
+    e = cudaEventSynchronize(s.done);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize(staging)");
+    s.pending = false;
+  }
+  if (!s.done) {
+    e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
+  }
+  if (s.cap < bytes.size()) {
+    if (s.host) cudaFreeHost(s.host);
+    s.host = nullptr;
+    s.cap = 0;
+    const size_t cap = std::max<size_t>(bytes.size(), 64 * 1024);
+    e = cudaHostAlloc(&s.host, cap, cudaHostAllocDefault);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(staging)");
+    s.cap = cap;
+  }
+  std::memcpy(s.host, bytes.data(), bytes.size());
+  e = cudaMemcpyAsync(dst, s.host, bytes.size(), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan)");
+  e = cudaEventRecord(s.done, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");
+  s.pending = true;
+  return KVRP_OK;
+}
+
+kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d_status, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
+  DeviceInfo* di = nullptr;
+  kvrp_status st = device_info(&di);
+  if (st != KVRP_OK) return st;
+  PlanBuilder pb(sh);
+  for (const ChunkIn& c : chunks) {
+    st = pb.add(c);
+    if (st != KVRP_OK) return st;
+  }
+  std::vector<unsigned char> bytes;
+  int grid = 0, smem = 0;
+  st = pb.finish(di->sms, di->smem_optin, d_status, &bytes, &grid, &smem);
+  if (st != KVRP_OK) return st;
+  if (grid == 0) return KVRP_OK;  // nothing to move
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (di->prepared_smem < smem) {
+      const cudaError_t e = prepare_kernel(di->smem_optin);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+      di->prepared_smem = di->smem_optin;
+    }
+  }
+  cudaError_t e;
+  if (workspace == nullptr) {
+    if (bytes.size() > (size_t)kParamPlanBytes)
+      return fail(KVRP_ERR_INVALID_ARG, "internal: single-chunk plan exceeds the parameter block");
+    std::vector<unsigned char> padded(kParamPlanBytes, 0);
+    std::memcpy(padded.data(), bytes.data(), bytes.size());
+    e = launch_relocate(padded.data(), nullptr, grid, smem, stream);
+  } else {
+    if (bytes.size() > workspace_bytes)
+      return fail(KVRP_ERR_WORKSPACE, "workspace holds %zu bytes, the plan needs %zu", workspace_bytes,
+                  bytes.size());
+    st = stage_and_copy(bytes, workspace, stream);
+    if (st != KVRP_OK) return st;
+    e = launch_relocate(nullptr, workspace, grid, smem, stream);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return KVRP_OK;
+}
+
+TensorIn tensor_in(const void* src, const void* u, const void* w, const kvrp_dst* d, int rot_kind,
+                   int rot_from) {
+  TensorIn t;
+  t.src = src;
+  t.u = u;
+  t.w = w;
+  t.dst = d ? *d : kvrp_dst{};
+  t.rot_kind = rot_kind;
+  t.rot_from = rot_from;
+  return t;
+}
+
+}  // namespace
+}  // namespace kvrp
+
+using namespace kvrp;
+
+extern "C" {
+
+kvrp_status kv_relocate_patch(const void* k_src, const void* v_src, int64_t src_layer_stride,
+                              int32_t n_layers, int32_t n_tokens, int32_t n_kv_heads, int32_t head_dim,
+                              int64_t delta, double rope_theta, int32_t rank, const void* uk,
+                              const void* vk, const void* uv, const void* vv, int64_t u_layer_stride,
+                              int64_t v_layer_stride, const kvrp_dst* k_dst, const kvrp_dst* v_dst,
+                              uint32_t* d_status, kvrp_stream_t stream) {
+  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
+  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  if (!k_dst || !v_dst) return fail(KVRP_ERR_INVALID_ARG, "k_dst and v_dst are required");
+  const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
+  ChunkIn c;
+  c.n_tensors = 2;
+  c.t[0] = tensor_in(k_src, uk, vk, k_dst, head_dim == 128 ? kRotHalf128 : kRotHalf64, 0);
+  c.t[1] = tensor_in(v_src, uv, vv, v_dst, kRotNone, 0);
+  c.src_layer_stride = src_layer_stride;
+  c.u_layer_stride = u_layer_stride;
+  c.w_layer_stride = v_layer_stride;
+  c.n_tokens = n_tokens;
+  c.rank = rank;
+  c.delta = delta;
+  kvrp_status st = check_chunk(c, sh);
+  if (st != KVRP_OK) return st;
+  return run(sh, {c}, d_status, nullptr, 0, stream);
+}
+
+kvrp_status kv_relocate_patch_mla(const void* src, int64_t src_layer_stride, int32_t n_layers,
+                                  int32_t n_tokens, int32_t kv_lora_dim, int32_t rope_dim, int64_t delta,
+                                  double rope_theta, int32_t rank, const void* u, const void* v,
+                                  int64_t u_layer_stride, int64_t v_layer_stride, const kvrp_dst* dst,
+                                  uint32_t* d_status, kvrp_stream_t stream) {
+  if (n_layers <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers must be > 0");
+  if (rope_dim != 64) return fail(KVRP_ERR_UNSUPPORTED, "rope_dim must be 64");
+  if (kv_lora_dim < 0 || kv_lora_dim % 64 != 0 || kv_lora_dim > 65536 - 64)
+    return fail(KVRP_ERR_UNSUPPORTED, "kv_lora_dim must be a multiple of 64");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if (!dst) return fail(KVRP_ERR_INVALID_ARG, "dst is required");
+  const Shape sh{n_layers, kv_lora_dim + rope_dim, rope_dim, rope_theta};
+  ChunkIn c;
+  c.n_tensors = 1;
+  c.t[0] = tensor_in(src, u, v, dst, kRotHalf64, kv_lora_dim);
+  c.t[1] = tensor_in(nullptr, nullptr, nullptr, nullptr, kRotNone, 0);
+  c.src_layer_stride = src_layer_stride;
+  c.u_layer_stride = u_layer_stride;
+  c.w_layer_stride = v_layer_stride;
+  c.n_tokens = n_tokens;
+  c.rank = rank;
+  c.delta = delta;
+  kvrp_status st = check_chunk(c, sh);
+  if (st != KVRP_OK) return st;
+  return run(sh, {c}, d_status, nullptr, 0, stream);
+}
+
+size_t kv_relocate_batch_workspace_size(int32_t n_chunks) {
+  if (n_chunks <= 0) return 0;
+  return PlanBuilder::bound(n_chunks);
+}
+
+kvrp_status kv_relocate_batch(const kvrp_chunk* chunks, int32_t n_chunks, int32_t n_layers, int32_t n_kv_heads,
+                              int32_t head_dim, double rope_theta, void* workspace, size_t workspace_bytes,
+                              uint32_t* d_status, kvrp_stream_t stream) {
+  if (n_chunks < 0 || (n_chunks > 0 && !chunks)) return fail(KVRP_ERR_INVALID_ARG, "bad chunk array");
+  if (n_chunks == 0) return KVRP_OK;
+  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
+  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  if (!workspace) return fail(KVRP_ERR_WORKSPACE, "kv_relocate_batch needs a device workspace");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(KVRP_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
+  std::vector<ChunkIn> in(n_chunks);
+  for (int i = 0; i < n_chunks; ++i) {
+    const kvrp_chunk& k = chunks[i];
+    ChunkIn& c = in[i];
+    c.n_tensors = 2;
+    c.t[0] = tensor_in(k.k_src, k.uk, k.vk, &k.k_dst, head_dim == 128 ? kRotHalf128 : kRotHalf64, 0);
+    c.t[1] = tensor_in(k.v_src, k.uv, k.vv, &k.v_dst, kRotNone, 0);
+    c.src_layer_stride = k.src_layer_stride;
+    c.u_layer_stride = k.u_layer_stride;
+    c.w_layer_stride = k.v_layer_stride;
+    c.n_tokens = k.n_tokens;
+    c.rank = k.rank;
+    c.delta = k.delta;
+    kvrp_status st = check_chunk(c, sh);
+    if (st != KVRP_OK) {
+      std::string msg = "chunk " + std::to_string(i) + ": " + g_last_error;
+      std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg.c_str());
+      return st;
+    }
+  }
+  if (workspace_bytes < PlanBuilder::bound(n_chunks))
+    return fail(KVRP_ERR_WORKSPACE, "workspace smaller than kv_relocate_batch_workspace_size(%d)", n_chunks);
+  return run(sh, in, d_status, workspace, workspace_bytes, stream);
+}
+
+const char* kvrp_status_string(kvrp_status status) {
+  switch (status) {
+    case KVRP_OK: return "KVRP_OK";
+    case KVRP_ERR_INVALID_ARG: return "KVRP_ERR_INVALID_ARG";
+    case KVRP_ERR_ALIGNMENT: return "KVRP_ERR_ALIGNMENT";
+    case KVRP_ERR_UNSUPPORTED: return "KVRP_ERR_UNSUPPORTED";
+    case KVRP_ERR_CUDA: return "KVRP_ERR_CUDA";
+    case KVRP_ERR_WORKSPACE: return "KVRP_ERR_WORKSPACE";
+  }
+  return "KVRP_ERR_UNKNOWN";
+}
+
+const char* kvrp_last_error(void) { return g_last_error; }
+
+int32_t kvrp_version(void) { return 100; }
+
+}  // extern "C"

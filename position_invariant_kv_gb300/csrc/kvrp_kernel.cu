@@ -1,0 +1,680 @@
+// Relocation + rank-m patch kernel for GB300 (sm_103a).
+//
+// Computes, for every token row of every (chunk, tensor, layer) in a plan,
+//     out = RN_bf16( R(delta) x + U_m V_m^T )
+// and writes the row into its 16-token destination page (Kamera,
+// gist.science/pt/paper/2606.23581, section 2 "O Operador Kamera": relocation
+// by an exact RoPE re-rotation, then the rank-m conditioning patch).
+//
+// One persistent CTA per SM walks a list of items.  An item is a 128-token
+// tile of one (chunk, tensor, layer), split into 128-feature sub-tiles.
+// Warp roles:
+//   warp 0      TMA producer: U tile per item, X sub-tile + V_m slice per stage
+//   warp 1      TMEM owner and tcgen05.mma issuer: P = U V_m^T into TMEM (fp32)
+//   warps 2..9  epilogue: one token row per thread, R(delta) in fp32 registers
+//               with a split (16-bit head + fp32 tail) phase table, + P from
+//               TMEM, round to bf16 in place in shared memory; then TMA stores
+//               of whole destination pages and plain stores for edge rows.
+// X and the destination pages move through 128B-swizzled shared memory, so the
+// row-per-thread epilogue reads and writes without bank conflicts.
+// Every wait is bounded; a stuck pipeline sets KVRP_DEV_TIMEOUT and the CTA
+// drains its copies, frees its TMEM and returns.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kvrp.h"
+#include "kvrp_plan.h"
+
+namespace kvrp {
+
+struct alignas(64) ParamPlan {
+  unsigned char bytes[kParamPlanBytes];
+};
+
+namespace dev {
+
+constexpr long long kTimeoutCycles = 1ll << 31;   // ~1 s at GB300 clocks
+
+// --------------------------------------------------------------------------
+// PTX wrappers
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase of `bar` with the given parity.  Gives up when
+// another role has flagged an abort or after ~1 s (then flags one itself).
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      *abort_flag = 1;
+      if (status) atomicOr(status, KVRP_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int c0,
+                                            int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+               ::"l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Two TMEM reads of N consecutive fp32 columns each (this warp's 32 lanes),
+// completed (tcgen05.wait::ld) inside the same asm statement.
+#define KVRP_R8(a, o) "=r"(a[o + 0]), "=r"(a[o + 1]), "=r"(a[o + 2]), "=r"(a[o + 3]), \
+                      "=r"(a[o + 4]), "=r"(a[o + 5]), "=r"(a[o + 6]), "=r"(a[o + 7])
+__device__ __forceinline__ void tmem_ld_2x16(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                             uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : KVRP_R8(a, 0), KVRP_R8(a, 8), KVRP_R8(b, 0), KVRP_R8(b, 8)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld_2x32(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                             uint32_t (&b)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : KVRP_R8(a, 0), KVRP_R8(a, 8), KVRP_R8(a, 16), KVRP_R8(a, 24),
+        KVRP_R8(b, 0), KVRP_R8(b, 8), KVRP_R8(b, 16), KVRP_R8(b, 24)
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+#undef KVRP_R8
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void stg128(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Named barrier over the epilogue warps that also ORs a predicate across them.
+__device__ __forceinline__ bool epi_bar_or(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "n"(32 * kEpilogueWarps)
+      : "memory");
+  return out != 0;
+}
+
+// Shared-memory matrix descriptor: K-major operand staged by a 32-byte
+// swizzled TMA box (rows of 16 bf16 = 32 B, 8-row atoms 256 B apart).
+__device__ __forceinline__ uint64_t desc_k_sw32(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)1 << 16;                      // leading byte offset (unused: K fits the atom)
+  d |= (uint64_t)(256 >> 4) << 32;             // stride byte offset: next 8-row atom
+  d |= (uint64_t)1 << 46;                      // descriptor version (tcgen05)
+  d |= (uint64_t)6 << 61;                      // layout: 32-byte swizzle
+  return d;
+}
+// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M = 128.
+__device__ __forceinline__ uint32_t idesc_bf16_f32(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// --------------------------------------------------------------------------
+// Plan access
+// --------------------------------------------------------------------------
+struct Item {
+  const ChunkRec* c;
+  const TensorRec* t;
+  int tensor, layer, tblk, s0, s1;
+  int t0;          // token index of tile row 0 (may be negative)
+  int64_t q0;      // destination position of tile row 0
+};
+
+__device__ __forceinline__ Item decode_item(const unsigned char* plan, const PlanHdr& h, int item) {
+  const int32_t* ibeg = reinterpret_cast<const int32_t*>(plan + h.off_ibeg);
+  int lo = 0, hi = h.n_chunks - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ibeg[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  Item it;
+  it.c = reinterpret_cast<const ChunkRec*>(plan + h.off_chunks) + lo;
+  int local = item - ibeg[lo];
+  it.tensor = 0;
+  if (local >= it.c->t[0].item_count) {
+    it.tensor = 1;
+    local -= it.c->t[0].item_count;
+  }
+  it.t = &it.c->t[it.tensor];
+  const int sg = local % h.n_sg;
+  const int rest = local / h.n_sg;
+  it.tblk = rest % it.t->n_tblk;
+  it.layer = rest / it.t->n_tblk;
+  it.s0 = sg * h.subs_per_item;
+  it.s1 = min(it.s0 + h.subs_per_item, h.n_sub);
+  const int lead = (int)(it.t->dst_start % kPage);
+  it.t0 = it.tblk * kTileRows - lead;
+  it.q0 = it.t->dst_start - lead + (int64_t)it.tblk * kTileRows;
+  return it;
+}
+
+__device__ __forceinline__ const CUtensorMap* plan_map(const unsigned char* plan, const PlanHdr& h,
+                                                       int idx) {
+  return reinterpret_cast<const CUtensorMap*>(plan + h.off_maps) + idx;
+}
+
+// --------------------------------------------------------------------------
+// Epilogue arithmetic on one thread's share of a sub-tile row
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Address of 16-byte chunk k (0..15) of tile row r inside a 128B-swizzled X sub-tile.
+__device__ __forceinline__ uint32_t x_chunk_addr(uint32_t xbase, int r, int k) {
+  return xbase + ((uint32_t)(k >> 3) << 14) + ((uint32_t)r << 7) + ((uint32_t)((k & 7) ^ (r & 7)) << 4);
+}
+
+// Rotate one pair of elements: lower element xl, upper element xh, split table
+// entry (head cos, head sin, tail cos, tail sin).  The heads carry 16
+// significant bits, so xh*S and xl*C are exact in fp32 for bf16 x.
+__device__ __forceinline__ void turn_pair(float xl, float xh, float4 e, float& yl, float& yh) {
+  const float a = xh * e.y;
+  const float b = fmaf(xl, e.x, -a);
+  const float tl = fmaf(xl, e.z, -(xh * e.w));
+  const float a2 = xl * e.y;
+  const float b2 = fmaf(xh, e.x, a2);
+  const float th = fmaf(xh, e.z, xl * e.w);
+  yl = b + tl;
+  yh = b2 + th;
+}
+__device__ __forceinline__ void turn_pair_patch(float xl, float xh, float4 e, float pl, float ph,
+                                                float& yl, float& yh) {
+  const float a = xh * e.y;
+  const float b = fmaf(xl, e.x, -a);
+  const float tl = fmaf(xl, e.z, -(xh * e.w));
+  const float a2 = xl * e.y;
+  const float b2 = fmaf(xh, e.x, a2);
+  const float th = fmaf(xh, e.z, xl * e.w);
+  yl = b + (tl + pl);
+  yh = b2 + (th + ph);
+}
+
+// N = columns per part (32 or 16).  The thread owns two parts of N columns
+// starting at a0 and a1; with ROT, element j of part a pairs with element j
+// of part b and uses table entry tab0 + j.
+template <int N, bool ROT, bool PATCH>
+__device__ __forceinline__ void epilogue_part(uint32_t xbase, int row, int a0, int a1,
+                                              const float4* __restrict__ tab, int tab0,
+                                              uint32_t tm_a, uint32_t tm_b) {
+  uint32_t pa[32], pb[32];
+  if constexpr (PATCH) {
+    if constexpr (N == 32) tmem_ld_2x32(tm_a, tm_b, pa, pb);
+    else tmem_ld_2x16(tm_a, tm_b, pa, pb);
+  }
+#pragma unroll
+  for (int k = 0; k < N / 8; ++k) {
+    const uint32_t addr_a = x_chunk_addr(xbase, row, (a0 >> 3) + k);
+    const uint32_t addr_b = x_chunk_addr(xbase, row, (a1 >> 3) + k);
+    const uint4 va = lds128(addr_a);
+    const uint4 vb = lds128(addr_b);
+    const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+    const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+    uint32_t oa[4], ob[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      float xl0 = bf_lo(wa[w]), xl1 = bf_hi(wa[w]);
+      float xh0 = bf_lo(wb[w]), xh1 = bf_hi(wb[w]);
+      float yl0, yl1, yh0, yh1;
+      if constexpr (ROT) {
+        const float4 e0 = tab[tab0 + 8 * k + 2 * w];
+        const float4 e1 = tab[tab0 + 8 * k + 2 * w + 1];
+        if constexpr (PATCH) {
+          turn_pair_patch(xl0, xh0, e0, __uint_as_float(pa[8 * k + 2 * w]),
+                          __uint_as_float(pb[8 * k + 2 * w]), yl0, yh0);
+          turn_pair_patch(xl1, xh1, e1, __uint_as_float(pa[8 * k + 2 * w + 1]),
+                          __uint_as_float(pb[8 * k + 2 * w + 1]), yl1, yh1);
+        } else {
+          turn_pair(xl0, xh0, e0, yl0, yh0);
+          turn_pair(xl1, xh1, e1, yl1, yh1);
+        }
+      } else {
+        yl0 = xl0 + __uint_as_float(pa[8 * k + 2 * w]);
+        yl1 = xl1 + __uint_as_float(pa[8 * k + 2 * w + 1]);
+        yh0 = xh0 + __uint_as_float(pb[8 * k + 2 * w]);
+        yh1 = xh1 + __uint_as_float(pb[8 * k + 2 * w + 1]);
+      }
+      oa[w] = pack_bf2(yl0, yl1);
+      ob[w] = pack_bf2(yh0, yh1);
+    }
+    sts128(addr_a, make_uint4(oa[0], oa[1], oa[2], oa[3]));
+    sts128(addr_b, make_uint4(ob[0], ob[1], ob[2], ob[3]));
+  }
+}
+
+// --------------------------------------------------------------------------
+// The kernel
+// --------------------------------------------------------------------------
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t full(int s) const { return base + 8u * s; }
+  __device__ uint32_t empty(int s) const { return base + 8u * (8 + s); }
+  __device__ uint32_t acc_full(int s) const { return base + 8u * (16 + s); }
+  __device__ uint32_t acc_empty(int s) const { return base + 8u * (24 + s); }
+  __device__ uint32_t u_full(int b) const { return base + 8u * (32 + b); }
+  __device__ uint32_t u_empty(int b) const { return base + 8u * (34 + b); }
+  __device__ uint32_t drain() const { return base + 8u * 36; }
+};
+
+template <bool kParamPlan>
+__global__ void __launch_bounds__(kThreads, 1)
+    relocate_kernel(const __grid_constant__ ParamPlan pp, const unsigned char* __restrict__ gplan) {
+  const unsigned char* plan = kParamPlan ? pp.bytes : gplan;
+  const PlanHdr h = *reinterpret_cast<const PlanHdr*>(plan);
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const SmemLayout L = smem_layout(h.m_max, h.stages);
+  const uint32_t sbase = smem_u32(smem);
+  const Bars bars{sbase};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 520);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int S = h.stages;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bars.full(s), 1);
+      mbar_init(bars.empty(s), kEpilogueWarps);
+      mbar_init(bars.acc_full(s), 1);
+      mbar_init(bars.acc_empty(s), kEpilogueWarps);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bars.u_full(b), 1);
+      mbar_init(bars.u_empty(b), 1);
+    }
+    mbar_init(bars.drain(), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1 && h.tmem_cols > 0) tmem_alloc(smem_u32(tmem_slot), (uint32_t)h.tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = h.tmem_cols > 0 ? *tmem_slot : 0u;
+
+  const uint32_t u_buf0 = sbase + L.u_off;
+  auto u_buf = [&](int b) { return u_buf0 + (uint32_t)b * L.u_bytes; };
+  auto x_buf = [&](int s) { return sbase + L.stage_off + (uint32_t)s * L.stage_bytes; };
+  auto w_buf = [&](int s) { return x_buf(s) + L.x_bytes; };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      uint32_t it = 0, uit = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
+        const Item I = decode_item(plan, h, item);
+        const int m = I.c->rank;
+        const int nkb = m >> 4;
+        if (m > 0) {
+          const int ub = uit & 1;
+          ok = wait_phase(bars.u_empty(ub), ((uit >> 1) & 1) ^ 1, abort_flag, h.status);
+          if (!ok) break;
+          const CUtensorMap* mu = plan_map(plan, h, I.t->map_u);
+          mbar_expect_tx(bars.u_full(ub), (uint32_t)nkb * (kTileRows * 32));
+          for (int k = 0; k < nkb; ++k)
+            tma_load_3d(u_buf(ub) + (uint32_t)k * (kTileRows * 32), mu, bars.u_full(ub), 16 * k, I.t0,
+                        I.layer);
+          ++uit;
+        }
+        const CUtensorMap* mx = plan_map(plan, h, I.t->map_x);
+        const CUtensorMap* mw = m > 0 ? plan_map(plan, h, I.t->map_w) : nullptr;
+        for (int s = I.s0; s < I.s1; ++s, ++it) {
+          const int st = (int)(it % (uint32_t)S);
+          ok = wait_phase(bars.empty(st), ((it / S) & 1) ^ 1, abort_flag, h.status);
+          if (!ok) break;
+          const int width = min(kSubCols, h.D - kSubCols * s);
+          const int nbox = width / kBoxCols;
+          uint32_t bytes = (uint32_t)nbox * (kTileRows * kBoxCols * 2);
+          if (m > 0) bytes += (uint32_t)nkb * (uint32_t)width * 32u;
+          mbar_expect_tx(bars.full(st), bytes);
+          for (int j = 0; j < nbox; ++j)
+            tma_load_3d(x_buf(st) + (uint32_t)j * (kTileRows * kBoxCols * 2), mx, bars.full(st),
+                        kSubCols * s + kBoxCols * j, I.t0, I.layer);
+          for (int k = 0; k < nkb; ++k)
+            for (int j = 0; j < nbox; ++j)
+              tma_load_3d(w_buf(st) + (uint32_t)k * (uint32_t)width * 32u + (uint32_t)j * (kBoxCols * 32),
+                          mw, bars.full(st), 16 * k, kSubCols * s + kBoxCols * j, I.layer);
+        }
+      }
+      // Let every copy this CTA started land before the CTA can exit.
+      const uint32_t first = it > (uint32_t)S ? it - (uint32_t)S : 0u;
+      for (uint32_t j = first; j < it; ++j) {
+        volatile int no_abort = 0;
+        wait_phase(bars.full((int)(j % (uint32_t)S)), (j / S) & 1, &no_abort, nullptr);
+      }
+      const uint32_t ufirst = uit > 2u ? uit - 2u : 0u;
+      for (uint32_t j = ufirst; j < uit; ++j) {
+        volatile int no_abort = 0;
+        wait_phase(bars.u_full((int)(j & 1)), (j >> 1) & 1, &no_abort, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0 && h.tmem_cols > 0) {
+      uint32_t it = 0, uit = 0, accpar = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
+        const Item I = decode_item(plan, h, item);
+        const int m = I.c->rank;
+        if (m == 0) {
+          it += (uint32_t)(I.s1 - I.s0);
+          continue;
+        }
+        const int nkb = m >> 4;
+        const int ub = uit & 1;
+        ok = wait_phase(bars.u_full(ub), (uit >> 1) & 1, abort_flag, h.status);
+        if (!ok) break;
+        for (int s = I.s0; s < I.s1; ++s, ++it) {
+          const int st = (int)(it % (uint32_t)S);
+          ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
+          if (!ok) break;
+          ok = wait_phase(bars.acc_empty(st), ((accpar >> st) & 1) ^ 1, abort_flag, h.status);
+          if (!ok) break;
+          tc_fence_after();
+          const int width = min(kSubCols, h.D - kSubCols * s);
+          const uint32_t idesc = idesc_bf16_f32(width);
+          const uint32_t d_tmem = tmem_base + (uint32_t)st * kSubCols;
+          for (int k = 0; k < nkb; ++k) {
+            const uint64_t ad = desc_k_sw32(u_buf(ub) + (uint32_t)k * (kTileRows * 32));
+            const uint64_t bd = desc_k_sw32(w_buf(st) + (uint32_t)k * (uint32_t)width * 32u);
+            mma_bf16(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+          }
+          mma_commit(bars.acc_full(st));
+          issued = true;
+          accpar ^= 1u << st;
+        }
+        if (!ok) break;
+        mma_commit(bars.u_empty(ub));
+        ++uit;
+      }
+      if (issued) {
+        // every MMA this thread issued has completed once `drain` flips
+        mma_commit(bars.drain());
+        volatile int no_abort = 0;
+        wait_phase(bars.drain(), 0, &no_abort, nullptr);
+      }
+    }
+  } else {
+    // --------------------------------------------------------------- epilogue
+    const int ew = warp - 2;                 // 0..7
+    const int quarter = warp & 3;            // TMEM lanes this warp may read
+    const int half = ew >> 2;                // which share of the columns
+    const int row = quarter * 32 + lane;     // tile row (token) of this thread
+    const int etid = ew * 32 + lane;         // 0..255
+    const bool store_thread = (ew == 0 && lane == 0);
+    uint32_t it = 0, accpar = 0;
+    int prev_st = -1;
+    for (int item = blockIdx.x; item < h.n_items; item += gridDim.x) {
+      const Item I = decode_item(plan, h, item);
+      const int m = I.c->rank;
+      const TensorRec& T = *I.t;
+      const int n_tok = I.c->n_tokens;
+      const float4* tab =
+          I.c->table >= 0 ? reinterpret_cast<const float4*>(plan + h.off_tabs) + I.c->table * kTablePairs
+                          : nullptr;
+      const CUtensorMap* md = plan_map(plan, h, T.map_dst);
+      // valid tile rows [r_lo, r_hi)
+      const int r_lo = max(0, -I.t0);
+      const int r_hi = min(kTileRows, n_tok - I.t0);
+      bool aborted = false;
+      for (int s = I.s0; s < I.s1; ++s, ++it) {
+        const int st = (int)(it % (uint32_t)S);
+        bool ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
+        if (ok && m > 0) {
+          ok = wait_phase(bars.acc_full(st), (accpar >> st) & 1, abort_flag, h.status);
+          tc_fence_after();
+        }
+        ok = __all_sync(0xffffffffu, ok);     // TMEM loads below are warp-collective
+        const int width = min(kSubCols, h.D - kSubCols * s);
+        const uint32_t xb = x_buf(st);
+        if (ok) {
+          // which columns this warp owns, and whether they turn
+          int a0, a1;
+          bool rot;
+          if (width == kSubCols) {
+            if (T.rot_kind == kRotHalf128) {
+              a0 = 32 * half;
+              a1 = 64 + 32 * half;
+              rot = true;
+            } else {
+              a0 = 64 * half;
+              a1 = a0 + 32;
+              rot = T.rot_kind == kRotHalf64 && kSubCols * s + 64 * half >= T.rot_from;
+            }
+          } else {
+            a0 = 16 * half;
+            a1 = a0 + 32;
+            rot = T.rot_kind == kRotHalf64 && kSubCols * s >= T.rot_from;
+          }
+          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)st * kSubCols;
+          const int tab0 = a0 & 63;
+          if (width == kSubCols) {
+            if (m > 0) {
+              if (rot) epilogue_part<32, true, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
+              else epilogue_part<32, false, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
+            } else if (rot) {
+              epilogue_part<32, true, false>(xb, row, a0, a1, tab, tab0, 0, 0);
+            }
+          } else {
+            if (m > 0) {
+              if (rot) epilogue_part<16, true, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
+              else epilogue_part<16, false, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
+            } else if (rot) {
+              epilogue_part<16, true, false>(xb, row, a0, a1, tab, tab0, 0, 0);
+            }
+          }
+        }
+        if (m > 0) {
+          // release this stage's accumulator to the MMA issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && ok) mbar_arrive(bars.acc_empty(st));
+          accpar ^= 1u << st;
+        }
+        fence_proxy_async_smem();
+        aborted = epi_bar_or(!ok || *abort_flag);
+        if (aborted) break;
+
+        // ---- stores: whole pages by TMA, edge rows by plain 16-byte stores
+        const int nbox = width / kBoxCols;
+        const int pfull_lo = (r_lo + kPage - 1) / kPage;      // first whole page
+        const int pfull_hi = r_hi / kPage;                    // one past the last whole page
+        // edge rows: [r_lo, min(r_hi, 16*pfull_lo)) and [max(16*pfull_hi, head_end), r_hi)
+        const int e0_lo = r_lo, e0_hi = min(r_hi, kPage * pfull_lo);
+        const int e1_lo = max(kPage * max(pfull_hi, pfull_lo), e0_hi), e1_hi = r_hi;
+        const int n0 = max(0, e0_hi - e0_lo), n1 = max(0, e1_hi - e1_lo);
+        const int cpr = width / 8;                            // 16-byte chunks per row
+        for (int idx = etid; idx < (n0 + n1) * cpr; idx += 32 * kEpilogueWarps) {
+          const int rr = idx / cpr;
+          const int k = idx % cpr;
+          const int r = rr < n0 ? e0_lo + rr : e1_lo + (rr - n0);
+          const int64_t q = I.q0 + r;
+          int64_t page = q / kPage;
+          if (T.block_table) page = T.block_table[q / kPage];
+          if (page < 0 || page >= T.num_pages) {
+            if (h.status) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
+            continue;
+          }
+          const int64_t off = (int64_t)I.layer * T.dst_layer_stride +
+                              (page * kPage + q % kPage) * (int64_t)h.D + kSubCols * s + 8 * k;
+          stg128(T.dst + off, lds128(x_chunk_addr(xb, r, k)));
+        }
+        __syncwarp();
+        if (store_thread) {
+          for (int p = pfull_lo; p < pfull_hi; ++p) {
+            const int64_t lp = (I.q0 + kPage * p) / kPage;
+            int64_t page = T.block_table ? (int64_t)T.block_table[lp] : lp;
+            if (page < 0 || page >= T.num_pages) {
+              if (h.status) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
+              continue;
+            }
+            for (int j = 0; j < nbox; ++j)
+              tma_store_3d(md, xb + (uint32_t)j * (kTileRows * kBoxCols * 2) + (uint32_t)p * (kPage * 128),
+                           kSubCols * s + kBoxCols * j, (int)(page * kPage), I.layer);
+          }
+          bulk_commit();
+          if (prev_st >= 0) {
+            bulk_wait_read_1();
+            mbar_arrive(bars.empty(prev_st));
+          }
+          prev_st = st;
+        } else if (lane == 0) {
+          mbar_arrive(bars.empty(st));
+        }
+      }
+      if (aborted) break;
+    }
+    if (store_thread) {
+      bulk_wait_read_0();
+      if (prev_st >= 0) mbar_arrive(bars.empty(prev_st));
+      bulk_wait_0();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1 && h.tmem_cols > 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, (uint32_t)h.tmem_cols);
+  }
+}
+
+}  // namespace dev
+
+cudaError_t prepare_kernel(int smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(dev::relocate_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(dev::relocate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              smem_bytes);
+}
+
+cudaError_t launch_relocate(const void* param_plan, const void* dev_plan, int grid, int smem_bytes,
+                            cudaStream_t stream) {
+  ParamPlan pp;
+  if (param_plan) {
+    memcpy(pp.bytes, param_plan, kParamPlanBytes);
+    dev::relocate_kernel<true><<<grid, kThreads, smem_bytes, stream>>>(pp, nullptr);
+  } else {
+    dev::relocate_kernel<false><<<grid, kThreads, smem_bytes, stream>>>(
+        pp, static_cast<const unsigned char*>(dev_plan));
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kvrp

@@ -1,0 +1,101 @@
+// Launch plan shared by the host side (kvrp_host.cpp) and the kernel
+// (kvrp_kernel.cu).  A plan is one byte blob: a header, the TMA tensor maps,
+// the per-chunk phase tables, the chunk records and the item prefix sums.
+// Small plans (one chunk) travel as a __grid_constant__ kernel parameter;
+// batch plans are copied into a caller-provided device workspace.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvrp {
+
+constexpr int kPage = 16;           // tokens per destination page
+constexpr int kTileRows = 128;      // tokens per tile (TMEM lanes / MMA M)
+constexpr int kSubCols = 128;       // features per sub-tile (MMA N)
+constexpr int kBoxCols = 64;        // features per 128-byte swizzled TMA box
+constexpr int kMaxRank = 128;
+constexpr int kTablePairs = 64;     // phase-table entries (head_dim / 2 <= 64)
+constexpr int kParamPlanBytes = 3072;
+constexpr int kEpilogueWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpilogueWarps;   // producer, MMA, epilogue warps
+
+// Rotation kinds of one tensor.
+enum RotKind : int32_t {
+  kRotNone = 0,     // values, MLA at rank 0 ... : nothing turns
+  kRotHalf128 = 1,  // heads of 128: feature i pairs with i + 64 inside each sub-tile
+  kRotHalf64 = 2,   // heads of 64 (or MLA k_rope): i pairs with i + 32 inside each
+                    // 64-wide box whose first feature is >= rot_from
+};
+
+struct TensorRec {             // one (chunk, tensor)
+  int32_t map_x, map_u, map_w, map_dst;   // plan map indices; -1 when unused
+  const int32_t* block_table;             // NULL = contiguous destination
+  uint16_t* dst;                          // pool base (bf16 bits)
+  int64_t dst_layer_stride;               // elements
+  int64_t dst_start;
+  int32_t num_pages;
+  int32_t rot_kind;
+  int32_t rot_from;                       // first rotated feature (kRotHalf64)
+  int32_t n_tblk;                         // token tiles of this tensor
+  int32_t item_count;                     // items of this tensor (all layers)
+  int32_t pad_;
+};
+
+struct ChunkRec {
+  TensorRec t[2];
+  int32_t n_tokens;
+  int32_t rank;
+  int32_t n_tensors;
+  int32_t table;                          // phase-table index; -1 when no tensor turns
+};
+
+struct PlanHdr {
+  int32_t n_chunks;
+  int32_t n_items;
+  int32_t D;                              // row width (features)
+  int32_t n_layers;
+  int32_t n_sub;                          // sub-tiles per row: ceil(D / 128)
+  int32_t subs_per_item;
+  int32_t n_sg;                           // sub-tile groups per tile
+  int32_t stages;                         // pipeline depth
+  int32_t m_max;                          // largest rank in the plan (multiple of 16)
+  int32_t tmem_cols;                      // allocated TMEM columns (0 = none)
+  uint32_t off_maps, off_tabs, off_chunks, off_ibeg;
+  uint32_t total_bytes;
+  uint32_t* status;                       // optional device status word
+};
+static_assert(sizeof(PlanHdr) <= 128, "header must fit in 128 bytes");
+
+// Shared-memory carve-up for a given rank bound and depth.
+struct SmemLayout {
+  uint32_t u_off, u_bytes;        // two U buffers
+  uint32_t stage_off, stage_bytes;
+  uint32_t x_bytes, w_bytes;      // inside a stage: X sub-tile, then W slice
+  uint32_t total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int m_max, int stages) {
+  SmemLayout s;
+  const uint32_t kb = (uint32_t)(m_max / 16);
+  s.u_off = 1024;                                  // barriers live in the first 1 KB
+  s.u_bytes = kb * (kTileRows * 32);               // one U buffer
+  s.x_bytes = kTileRows * kSubCols * 2;            // 32 KB
+  s.w_bytes = kb * (kSubCols * 32);
+  s.stage_bytes = s.x_bytes + s.w_bytes;
+  s.stage_off = s.u_off + 2 * s.u_bytes;
+  s.total = s.stage_off + (uint32_t)stages * s.stage_bytes;
+  return s;
+}
+
+// Launches the relocation kernel.  Exactly one of param_plan / dev_plan is used:
+// param_plan (host bytes, <= kParamPlanBytes) travels as a kernel parameter,
+// dev_plan points at a plan already resident in device memory.
+cudaError_t launch_relocate(const void* param_plan, const void* dev_plan, int grid,
+                            int smem_bytes, cudaStream_t stream);
+
+// Per-device one-time kernel setup (dynamic shared-memory opt-in).
+cudaError_t prepare_kernel(int smem_bytes);
+
+}  // namespace kvrp

@@ -1,0 +1,116 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/kvrp.h declares, and rejects bad arguments with the documented status
+codes before touching CUDA."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvrp():
+    from position_invariant_kv_gb300.build import build
+    build()
+    import position_invariant_kv_gb300 as m
+    m.lib()
+    return m
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "kvrp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(kvrp):
+    declared = header_functions()
+    assert set(declared) == set(kvrp.EXPORTED_SYMBOLS), declared
+    lib = C.CDLL(kvrp.lib_path)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(kvrp):
+    assert kvrp.kvrp_status_string(0) == "KVRP_OK"
+    assert kvrp.kvrp_status_string(5) == "KVRP_ERR_WORKSPACE"
+    assert kvrp.kvrp_version() >= 100
+
+
+def _dst(**kw):
+    d = dict(base=0x10000, num_pages=16, layer_stride=16 * 16 * 256)
+    d.update(kw)
+    return d
+
+
+def _call(kvrp, **over):
+    args = dict(k_src=0x20000, v_src=0x30000, n_layers=1, n_tokens=100, n_kv_heads=2, head_dim=128,
+                delta=5, rope_theta=1e4, rank=0)
+    kd = over.pop("k_dst", _dst())
+    vd = over.pop("v_dst", _dst(base=0x40000))
+    args.update(over)
+    k, v = args.pop("k_src"), args.pop("v_src")
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_patch(k, v, k_dst=kvrp.Dst(**kd), v_dst=kvrp.Dst(**vd), stream=0, **args)
+    return e.value.status
+
+
+def test_rejects_bad_arguments_before_cuda(kvrp):
+    assert _call(kvrp, k_src=0) == kvrp.KVRP_ERR_INVALID_ARG
+    assert _call(kvrp, k_src=0x20008) == kvrp.KVRP_ERR_ALIGNMENT
+    assert _call(kvrp, head_dim=96) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert _call(kvrp, rank=8, uk=0x50000, vk=0x60000, uv=0x70000, vv=0x80000) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert _call(kvrp, rank=16) == kvrp.KVRP_ERR_INVALID_ARG            # factors missing
+    assert _call(kvrp, rank=0, uk=0x50000) == kvrp.KVRP_ERR_INVALID_ARG  # factors without rank
+    assert _call(kvrp, n_tokens=-1) == kvrp.KVRP_ERR_INVALID_ARG
+    assert _call(kvrp, n_layers=0) == kvrp.KVRP_ERR_INVALID_ARG
+    assert _call(kvrp, rope_theta=-1.0) == kvrp.KVRP_ERR_INVALID_ARG
+    assert _call(kvrp, k_dst=_dst(page_size=32)) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert _call(kvrp, k_dst=_dst(num_pages=2)) == kvrp.KVRP_ERR_INVALID_ARG   # contiguous too small
+    assert _call(kvrp, k_dst=_dst(dst_start=-3)) == kvrp.KVRP_ERR_INVALID_ARG
+    assert _call(kvrp, k_dst=_dst(block_table=0x1002)) == kvrp.KVRP_ERR_ALIGNMENT
+    assert _call(kvrp, n_layers=2, src_layer_stride=10) == kvrp.KVRP_ERR_INVALID_ARG
+    assert _call(kvrp, n_layers=2, src_layer_stride=100 * 256 + 4) == kvrp.KVRP_ERR_ALIGNMENT
+
+
+def test_mla_and_batch_argument_checks(kvrp):
+    d = kvrp.Dst(base=0x10000, num_pages=16, layer_stride=16 * 16 * 576)
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_patch_mla(0x20000, n_layers=1, n_tokens=10, kv_lora_dim=512, rope_dim=32,
+                                   delta=1, rope_theta=1e4, dst=d, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_UNSUPPORTED
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_patch_mla(0x20000, n_layers=1, n_tokens=10, kv_lora_dim=500, rope_dim=64,
+                                   delta=1, rope_theta=1e4, dst=d, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_UNSUPPORTED
+    ch = kvrp.Chunk(k_src=0x20000, v_src=0x30000, n_tokens=10, delta=3,
+                    k_dst=kvrp.Dst(base=0x10000, num_pages=4), v_dst=kvrp.Dst(base=0x40000, num_pages=4))
+    ws = kvrp.kv_relocate_batch_workspace_size(2)
+    assert ws > 0 and kvrp.kv_relocate_batch_workspace_size(0) == 0
+    with pytest.raises(kvrp.KvrpError) as e:   # no workspace
+        kvrp.kv_relocate_batch([ch, ch], n_layers=1, n_kv_heads=2, head_dim=128, rope_theta=1e4,
+                               workspace=0, workspace_bytes=0, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_WORKSPACE
+    with pytest.raises(kvrp.KvrpError) as e:   # workspace too small
+        kvrp.kv_relocate_batch([ch, ch], n_layers=1, n_kv_heads=2, head_dim=128, rope_theta=1e4,
+                               workspace=0x100000, workspace_bytes=ws - 1, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_WORKSPACE
+    bad = kvrp.Chunk(k_src=0x20000, v_src=0, n_tokens=10, delta=3,
+                     k_dst=kvrp.Dst(base=0x10000, num_pages=4), v_dst=kvrp.Dst(base=0x40000, num_pages=4))
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_batch([ch, bad], n_layers=1, n_kv_heads=2, head_dim=128, rope_theta=1e4,
+                               workspace=0x100000, workspace_bytes=ws, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_INVALID_ARG and "chunk 1" in str(e.value)
+
+
+def test_no_gpu_means_cuda_error_not_fallback(kvrp):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_patch(0x20000, 0x30000, n_layers=1, n_tokens=100, n_kv_heads=2, head_dim=128,
+                               delta=5, rope_theta=1e4, k_dst=kvrp.Dst(**_dst()),
+                               v_dst=kvrp.Dst(**_dst(base=0x40000)), stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_CUDA

@@ -1,0 +1,185 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, element
+by element, on host-drawn workloads that span several tiles and ragged tails.
+
+Bar (the parity rule of oracle.compare): every element within 1 bf16 ulp of
+the oracle rounded to bf16; with a patch (rank > 0) an element may exceed that
+only as a counted mismatch inside the conditioning bound, never as a
+violation; without a patch every element must be within 1 ulp; values (GQA V)
+and MLA c_KV without a patch must be bit-identical to the source; slots that
+no token targets must keep their sentinel bits (exact page placement)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from position_invariant_kv_gb300.build import build
+    build()
+    import position_invariant_kv_gb300 as kvrp
+    kvrp.lib()
+
+
+def assert_parity(reports, strict=False, limit_frac=1e-5):
+    for name, r in reports.items():
+        assert r["violations"] == 0, (name, r)
+        if strict:
+            assert r["max_ulp"] <= 1, (name, r)
+        else:
+            assert r["mismatches"] <= limit_frac * r["n"] + 2, (name, r)
+
+
+def test_config0_single_chunk_contiguous():
+    from gpu_util import run_and_compare
+    wl = W.config(0)
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps)
+    assert dwl.status_value() == 0
+
+
+@pytest.mark.parametrize("spec", [
+    # (n_layers, n_heads, head_dim, T, delta, rank, dst_start, paged, extra_pages)
+    (2, 2, 128, 200, 37, 0, 5, True, 3),          # relocation only, unaligned start, ragged tail
+    (3, 4, 128, 300, -20000, 32, 0, True, 5),     # c1-like patch
+    (2, 4, 64, 129, 65536, 16, 17, True, 1),      # head_dim 64, one row past a tile
+    (1, 2, 128, 130, -7, 128, 3, True, 0),        # largest rank (two pipeline stages)
+    (2, 1, 128, 1, 1, 64, 15, True, 2),           # a single token in the last slot of a page
+    (2, 3, 128, 256, 999, 48, 0, False, 1),       # contiguous, whole tiles, rank 48
+    (1, 2, 128, 77, -123, 0, 3, False, 0),        # contiguous with an offset
+    (2, 8, 128, 513, 32768, 64, 31, True, 4),     # several tiles, rank 64, D = 1024
+], ids=lambda s: "L{}H{}d{}T{}m{}s{}{}".format(s[0], s[1], s[2], s[3], s[5], s[6], "p" if s[7] else "c"))
+def test_gqa_small(spec):
+    from gpu_util import run_and_compare
+    L, H, d, T, delta, m, start, paged, extra = spec
+    wl = W.small_gqa(seed=100 + T + m, n_layers=L, n_heads=H, head_dim=d,
+                     chunks_spec=((T, delta, m, 0),), dst_starts=[start], paged=paged, extra_pages=extra)
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps, strict=(m == 0))
+    if m == 0:
+        assert np.array_equal(got["v"], want["v"])     # values copied byte for byte
+    assert dwl.status_value() == 0
+
+
+@pytest.mark.parametrize("rank,start,T", [(32, 0, 150), (0, 7, 150), (16, 9, 300)])
+def test_mla_small(rank, start, T):
+    from gpu_util import run_and_compare
+    wl = W.small_mla(seed=300 + rank, n_layers=2, n_tokens=T, delta=-40000, rank=rank, dst_start=start,
+                     extra_pages=2)
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps, strict=(rank == 0))
+    if rank == 0:
+        # c_KV bytes reused unchanged
+        assert np.array_equal(got["kv"][..., :512], want["kv"][..., :512])
+    assert dwl.status_value() == 0
+
+
+def test_batch_mixed_ranks_and_sequences():
+    from gpu_util import run_and_compare
+    spec = ((300, -2048, 0, 0), (150, 5000, 64, 0), (77, 0, 16, 1), (1, -1, 0, 1), (200, 31337, 32, 2),
+            (256, -1024, 0, 2))
+    wl = W.small_gqa(seed=400, n_layers=3, n_heads=2, head_dim=128, chunks_spec=spec, extra_pages=7,
+                     dst_starts=[0, 300, 3, 80, 16, 216])
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps)
+    assert dwl.status_value() == 0
+
+
+def test_batch_runs_twice_identically():
+    spec = ((100, 7, 32, 0), (90, -9, 0, 0))
+    wl = W.small_gqa(seed=401, n_layers=2, chunks_spec=spec)
+    import harness
+    dwl = harness.DeviceWorkload(wl)
+    dwl.run()
+    first = dwl.pools_host()
+    dwl.reset_pools()
+    dwl.run()
+    second = dwl.pools_host()
+    for n in wl.tensors:
+        assert np.array_equal(first[n], second[n])
+
+
+def test_patch_alone_and_strong_patch():
+    """Canonical rows all zero: the output is RN(U V^T) alone; then factors at
+    std 1 so that the patch dominates the rotation."""
+    from gpu_util import run_and_compare
+    wl = W.small_gqa(seed=500, n_layers=2, n_heads=2, head_dim=128, chunks_spec=((160, 77, 32, 0),))
+    host = W.host_inputs(wl)
+    for n in wl.tensors:
+        host["rows"][n][:] = 0
+    reps, *_ = run_and_compare(wl, host=host)
+    print(reps)
+    assert_parity(reps)
+    host = W.host_inputs(wl)
+    rng = np.random.default_rng(501)
+    for n in wl.tensors:
+        f = rng.standard_normal(host["u"][n][0].shape).astype(np.float32)
+        host["u"][n][0] = W._f32_to_bf16_bits(f)
+        f = rng.standard_normal(host["w"][n][0].shape).astype(np.float32)
+        host["w"][n][0] = W._f32_to_bf16_bits(f)
+    reps, *_ = run_and_compare(wl, host=host)
+    print(reps)
+    assert_parity(reps)
+
+
+def test_empty_chunk_is_a_no_op():
+    import harness
+    wl = W.small_gqa(seed=600, chunks_spec=((16, 5, 16, 0),))
+    host = W.host_inputs(wl)
+    wl.chunks[0] = W.Chunk(0, 0, 5, 16, 0, 0)
+    dwl = harness.DeviceWorkload(wl, host=host)
+    dwl.run()
+    torch.cuda.synchronize()
+    for p in dwl.pools_host().values():
+        assert np.all(p == 0xFFFF)
+
+
+def test_bad_page_is_skipped_and_flagged():
+    import harness
+    from gpu_util import run_and_compare  # noqa: F401
+    from oracle import run_workload
+    wl = W.small_gqa(seed=700, n_layers=2, chunks_spec=((64, 3, 16, 0),), extra_pages=2)
+    host = W.host_inputs(wl)
+    good_pages = wl.block_tables.copy()
+    wl.block_tables = wl.block_tables.copy()
+    wl.block_tables[0, 1] = wl.num_pages + 5        # out of range: page skipped, status bit set
+    dwl = harness.DeviceWorkload(wl, host=host)
+    dwl.run()
+    torch.cuda.synchronize()
+    import position_invariant_kv_gb300 as kvrp
+    assert dwl.status_value() & kvrp.KVRP_DEV_BAD_PAGE
+    got = dwl.pools_host()
+    wl.block_tables = good_pages
+    want, _, _ = run_workload(wl, host)
+    skipped = good_pages[0, 1]
+    for n in wl.tensors:
+        g, w_ = got[n].copy(), want[n].copy()
+        assert np.all(g[:, skipped] == 0xFFFF)
+        g[:, skipped] = w_[:, skipped]
+        from oracle import ulp_distance
+        assert ulp_distance(g, w_).max() <= 1
+
+
+def test_other_stream():
+    import harness
+    from oracle import run_workload, ulp_distance
+    wl = W.small_gqa(seed=800, n_layers=2, chunks_spec=((140, 11, 16, 0),))
+    dwl = harness.DeviceWorkload(wl)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        dwl.run(stream=s)
+    s.synchronize()
+    got = dwl.pools_host()
+    want, _, _ = run_workload(wl, dwl.host)
+    for n in wl.tensors:
+        assert ulp_distance(got[n], want[n]).max() <= 1
