@@ -331,7 +331,7 @@ class PlanBuilder {
     // pipeline depth from the shared-memory budget (and TMEM: 128 columns a stage)
     const int budget = smem_optin - 1024;
     int stages = 0;
-    for (int s = (m_max_ > 0 ? 4 : 6); s >= 2; --s) {
+    for (int s = kMaxStages; s >= 2; --s) {
       if ((int)smem_layout(m_max_, s).total <= budget) {
         stages = s;
         break;
@@ -340,10 +340,7 @@ class PlanBuilder {
     if (stages == 0) return fail(KVRP_ERR_UNSUPPORTED, "rank %d does not fit in shared memory", m_max_);
     h.stages = stages;
     h.tmem_cols = 0;
-    if (m_max_ > 0) {
-      h.tmem_cols = 32;
-      while (h.tmem_cols < stages * kSubCols) h.tmem_cols *= 2;
-    }
+    if (m_max_ > 0) h.tmem_cols = kAccSlots * kSubCols;   // 512 columns: the whole TMEM of the SM
     auto align = [](size_t v) { return (v + 127) & ~static_cast<size_t>(127); };
     size_t off = align(sizeof(PlanHdr));
     h.off_maps = static_cast<uint32_t>(off);

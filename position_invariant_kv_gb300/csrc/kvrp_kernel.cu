@@ -184,20 +184,6 @@ __device__ __forceinline__ void stg128(void* p, uint4 v) {
                : "memory");
 }
 
-// Named barrier over the epilogue warps that also ORs a predicate across them.
-__device__ __forceinline__ bool epi_bar_or(bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "barrier.cta.red.or.pred q, 1, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred), "n"(32 * kEpilogueWarps)
-      : "memory");
-  return out != 0;
-}
-
 // Shared-memory matrix descriptor: K-major operand staged by a 32-byte
 // swizzled TMA box (rows of 16 bf16 = 32 B, 8-row atoms 256 B apart).
 __device__ __forceinline__ uint64_t desc_k_sw32(uint32_t saddr) {
@@ -353,16 +339,35 @@ __device__ __forceinline__ void epilogue_part(uint32_t xbase, int row, int a0, i
 // --------------------------------------------------------------------------
 // The kernel
 // --------------------------------------------------------------------------
+// mbarriers: per shared-memory stage (X sub-tile + V_m slice) full/empty,
+// per TMEM accumulator slot full/empty, per U buffer full/empty, and one
+// drain barrier for the MMA issuer's last commit.
 struct Bars {
   uint32_t base;
   __device__ uint32_t full(int s) const { return base + 8u * s; }
-  __device__ uint32_t empty(int s) const { return base + 8u * (8 + s); }
-  __device__ uint32_t acc_full(int s) const { return base + 8u * (16 + s); }
-  __device__ uint32_t acc_empty(int s) const { return base + 8u * (24 + s); }
-  __device__ uint32_t u_full(int b) const { return base + 8u * (32 + b); }
-  __device__ uint32_t u_empty(int b) const { return base + 8u * (34 + b); }
-  __device__ uint32_t drain() const { return base + 8u * 36; }
+  __device__ uint32_t empty(int s) const { return base + 8u * (kMaxStages + s); }
+  __device__ uint32_t acc_full(int a) const { return base + 8u * (2 * kMaxStages + a); }
+  __device__ uint32_t acc_empty(int a) const { return base + 8u * (2 * kMaxStages + kAccSlots + a); }
+  __device__ uint32_t u_full(int b) const { return base + 8u * (2 * kMaxStages + 2 * kAccSlots + b); }
+  __device__ uint32_t u_empty(int b) const { return base + 8u * (2 * kMaxStages + 2 * kAccSlots + 2 + b); }
+  __device__ uint32_t drain() const { return base + 8u * (2 * kMaxStages + 2 * kAccSlots + 4); }
 };
+static_assert(8 * (2 * kMaxStages + 2 * kAccSlots + 5) <= 512, "barriers must fit below the TMEM slot");
+
+// Named barrier over the two epilogue warps that share a TMEM lane quarter
+// (ids 1..4), ORing a predicate across them.
+__device__ __forceinline__ bool pair_bar_or(int id, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, 64, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id)
+      : "memory");
+  return out != 0;
+}
 
 template <bool kParamPlan>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -387,8 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(bars.full(s), 1);
       mbar_init(bars.empty(s), kEpilogueWarps);
-      mbar_init(bars.acc_full(s), 1);
-      mbar_init(bars.acc_empty(s), kEpilogueWarps);
+    }
+    for (int a = 0; a < kAccSlots; ++a) {
+      mbar_init(bars.acc_full(a), 1);
+      mbar_init(bars.acc_empty(a), kEpilogueWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.u_full(b), 1);
@@ -464,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0 && h.tmem_cols > 0) {
-      uint32_t it = 0, uit = 0, accpar = 0;
+      uint32_t it = 0, uit = 0, ait = 0;
       bool ok = true;
       bool issued = false;
       for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
@@ -478,24 +485,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ub = uit & 1;
         ok = wait_phase(bars.u_full(ub), (uit >> 1) & 1, abort_flag, h.status);
         if (!ok) break;
-        for (int s = I.s0; s < I.s1; ++s, ++it) {
+        for (int s = I.s0; s < I.s1; ++s, ++it, ++ait) {
           const int st = (int)(it % (uint32_t)S);
+          const int a = (int)(ait % kAccSlots);
           ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
           if (!ok) break;
-          ok = wait_phase(bars.acc_empty(st), ((accpar >> st) & 1) ^ 1, abort_flag, h.status);
+          ok = wait_phase(bars.acc_empty(a), ((ait / kAccSlots) & 1) ^ 1, abort_flag, h.status);
           if (!ok) break;
           tc_fence_after();
           const int width = min(kSubCols, h.D - kSubCols * s);
           const uint32_t idesc = idesc_bf16_f32(width);
-          const uint32_t d_tmem = tmem_base + (uint32_t)st * kSubCols;
+          const uint32_t d_tmem = tmem_base + (uint32_t)a * kSubCols;
           for (int k = 0; k < nkb; ++k) {
             const uint64_t ad = desc_k_sw32(u_buf(ub) + (uint32_t)k * (kTileRows * 32));
             const uint64_t bd = desc_k_sw32(w_buf(st) + (uint32_t)k * (uint32_t)width * 32u);
             mma_bf16(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
           }
-          mma_commit(bars.acc_full(st));
+          mma_commit(bars.acc_full(a));
           issued = true;
-          accpar ^= 1u << st;
         }
         if (!ok) break;
         mma_commit(bars.u_empty(ub));
@@ -510,14 +517,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------------- epilogue
+    // Two warps share each TMEM lane quarter (32 tile rows) and split the
+    // columns; each pair syncs on its own named barrier, and the first row of
+    // every 16-row page issues that page's TMA stores.
     const int ew = warp - 2;                 // 0..7
     const int quarter = warp & 3;            // TMEM lanes this warp may read
     const int half = ew >> 2;                // which share of the columns
     const int row = quarter * 32 + lane;     // tile row (token) of this thread
-    const int etid = ew * 32 + lane;         // 0..255
-    const bool store_thread = (ew == 0 && lane == 0);
-    uint32_t it = 0, accpar = 0;
-    int prev_st = -1;
+    const int pair_id = 1 + quarter;
+    const bool leader = ((row & (kPage - 1)) == 0) && half == 0;
+    uint32_t it = 0, ait = 0;
     for (int item = blockIdx.x; item < h.n_items; item += gridDim.x) {
       const Item I = decode_item(plan, h, item);
       const int m = I.c->rank;
@@ -527,40 +536,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           I.c->table >= 0 ? reinterpret_cast<const float4*>(plan + h.off_tabs) + I.c->table * kTablePairs
                           : nullptr;
       const CUtensorMap* md = plan_map(plan, h, T.map_dst);
-      // valid tile rows [r_lo, r_hi)
+      // valid tile rows [r_lo, r_hi); this thread's row and its destination page
       const int r_lo = max(0, -I.t0);
       const int r_hi = min(kTileRows, n_tok - I.t0);
+      const bool valid = row >= r_lo && row < r_hi;
+      const int pg_row = row & ~(kPage - 1);
+      const bool whole_page = pg_row >= r_lo && pg_row + kPage <= r_hi;
+      int64_t page = -1;
+      if (valid) {
+        const int64_t lp = (I.q0 + row) / kPage;
+        page = T.block_table ? (int64_t)__ldg(T.block_table + lp) : lp;   // used at store time
+      }
       bool aborted = false;
       for (int s = I.s0; s < I.s1; ++s, ++it) {
         const int st = (int)(it % (uint32_t)S);
+        const int acc = (int)(ait % kAccSlots);
         bool ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
         if (ok && m > 0) {
-          ok = wait_phase(bars.acc_full(st), (accpar >> st) & 1, abort_flag, h.status);
+          ok = wait_phase(bars.acc_full(acc), (ait / kAccSlots) & 1, abort_flag, h.status);
           tc_fence_after();
         }
         ok = __all_sync(0xffffffffu, ok);     // TMEM loads below are warp-collective
         const int width = min(kSubCols, h.D - kSubCols * s);
         const uint32_t xb = x_buf(st);
-        if (ok) {
-          // which columns this warp owns, and whether they turn
-          int a0, a1;
-          bool rot;
-          if (width == kSubCols) {
-            if (T.rot_kind == kRotHalf128) {
-              a0 = 32 * half;
-              a1 = 64 + 32 * half;
-              rot = true;
-            } else {
-              a0 = 64 * half;
-              a1 = a0 + 32;
-              rot = T.rot_kind == kRotHalf64 && kSubCols * s + 64 * half >= T.rot_from;
-            }
+        // which columns this warp owns, and whether they turn
+        int a0, a1;
+        bool rot;
+        if (width == kSubCols) {
+          if (T.rot_kind == kRotHalf128) {
+            a0 = 32 * half;
+            a1 = 64 + 32 * half;
+            rot = true;
           } else {
-            a0 = 16 * half;
+            a0 = 64 * half;
             a1 = a0 + 32;
-            rot = T.rot_kind == kRotHalf64 && kSubCols * s >= T.rot_from;
+            rot = T.rot_kind == kRotHalf64 && kSubCols * s + 64 * half >= T.rot_from;
           }
-          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)st * kSubCols;
+        } else {
+          a0 = 16 * half;
+          a1 = a0 + 32;
+          rot = T.rot_kind == kRotHalf64 && kSubCols * s >= T.rot_from;
+        }
+        const int nchunk = (width == kSubCols ? 32 : 16) / 8;
+        if (ok) {
+          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kSubCols;
           const int tab0 = a0 & 63;
           if (width == kSubCols) {
             if (m > 0) {
@@ -579,70 +598,47 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (m > 0) {
-          // release this stage's accumulator to the MMA issuer
+          // release this accumulator slot to the MMA issuer
           tc_fence_before();
           __syncwarp();
-          if (lane == 0 && ok) mbar_arrive(bars.acc_empty(st));
-          accpar ^= 1u << st;
+          if (lane == 0 && ok) mbar_arrive(bars.acc_empty(acc));
+          ++ait;
         }
         fence_proxy_async_smem();
-        aborted = epi_bar_or(!ok || *abort_flag);
+        aborted = pair_bar_or(pair_id, !ok || *abort_flag);
         if (aborted) break;
 
-        // ---- stores: whole pages by TMA, edge rows by plain 16-byte stores
-        const int nbox = width / kBoxCols;
-        const int pfull_lo = (r_lo + kPage - 1) / kPage;      // first whole page
-        const int pfull_hi = r_hi / kPage;                    // one past the last whole page
-        // edge rows: [r_lo, min(r_hi, 16*pfull_lo)) and [max(16*pfull_hi, head_end), r_hi)
-        const int e0_lo = r_lo, e0_hi = min(r_hi, kPage * pfull_lo);
-        const int e1_lo = max(kPage * max(pfull_hi, pfull_lo), e0_hi), e1_hi = r_hi;
-        const int n0 = max(0, e0_hi - e0_lo), n1 = max(0, e1_hi - e1_lo);
-        const int cpr = width / 8;                            // 16-byte chunks per row
-        for (int idx = etid; idx < (n0 + n1) * cpr; idx += 32 * kEpilogueWarps) {
-          const int rr = idx / cpr;
-          const int k = idx % cpr;
-          const int r = rr < n0 ? e0_lo + rr : e1_lo + (rr - n0);
-          const int64_t q = I.q0 + r;
-          int64_t page = q / kPage;
-          if (T.block_table) page = T.block_table[q / kPage];
-          if (page < 0 || page >= T.num_pages) {
-            if (h.status) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
-            continue;
+        // ---- stores: whole pages by TMA (issued by the page's first row),
+        //      rows of partly covered pages by their owner threads
+        if (valid) {
+          const bool page_ok = page >= 0 && page < T.num_pages;
+          if (!page_ok) {
+            if (h.status && (leader || !whole_page)) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
+          } else if (whole_page) {
+            if (leader) {
+              const int nbox = width / kBoxCols;
+              for (int j = 0; j < nbox; ++j)
+                tma_store_3d(md, xb + (uint32_t)j * (kTileRows * kBoxCols * 2) + (uint32_t)pg_row * 128u,
+                             kSubCols * s + kBoxCols * j, (int)(page * kPage), I.layer);
+              bulk_commit();
+              bulk_wait_read_0();
+            }
+          } else {
+            uint16_t* dst_row = T.dst + (int64_t)I.layer * T.dst_layer_stride +
+                                (page * kPage + (I.q0 + row) % kPage) * (int64_t)h.D + kSubCols * s;
+            for (int k = 0; k < nchunk; ++k) {
+              const int c0 = (a0 >> 3) + k, c1 = (a1 >> 3) + k;
+              stg128(dst_row + 8 * c0, lds128(x_chunk_addr(xb, row, c0)));
+              stg128(dst_row + 8 * c1, lds128(x_chunk_addr(xb, row, c1)));
+            }
           }
-          const int64_t off = (int64_t)I.layer * T.dst_layer_stride +
-                              (page * kPage + q % kPage) * (int64_t)h.D + kSubCols * s + 8 * k;
-          stg128(T.dst + off, lds128(x_chunk_addr(xb, r, k)));
         }
         __syncwarp();
-        if (store_thread) {
-          for (int p = pfull_lo; p < pfull_hi; ++p) {
-            const int64_t lp = (I.q0 + kPage * p) / kPage;
-            int64_t page = T.block_table ? (int64_t)T.block_table[lp] : lp;
-            if (page < 0 || page >= T.num_pages) {
-              if (h.status) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
-              continue;
-            }
-            for (int j = 0; j < nbox; ++j)
-              tma_store_3d(md, xb + (uint32_t)j * (kTileRows * kBoxCols * 2) + (uint32_t)p * (kPage * 128),
-                           kSubCols * s + kBoxCols * j, (int)(page * kPage), I.layer);
-          }
-          bulk_commit();
-          if (prev_st >= 0) {
-            bulk_wait_read_1();
-            mbar_arrive(bars.empty(prev_st));
-          }
-          prev_st = st;
-        } else if (lane == 0) {
-          mbar_arrive(bars.empty(st));
-        }
+        if (lane == 0) mbar_arrive(bars.empty(st));
       }
       if (aborted) break;
     }
-    if (store_thread) {
-      bulk_wait_read_0();
-      if (prev_st >= 0) mbar_arrive(bars.empty(prev_st));
-      bulk_wait_0();
-    }
+    bulk_wait_0();   // this thread's page stores are complete before the CTA exits
   }
 
   tc_fence_before();

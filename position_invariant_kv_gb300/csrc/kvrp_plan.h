@@ -19,6 +19,8 @@ constexpr int kMaxRank = 128;
 constexpr int kTablePairs = 64;     // phase-table entries (head_dim / 2 <= 64)
 constexpr int kParamPlanBytes = 3072;
 constexpr int kEpilogueWarps = 8;
+constexpr int kMaxStages = 8;       // shared-memory pipeline depth bound
+constexpr int kAccSlots = 4;        // TMEM accumulators of 128 fp32 columns
 constexpr int kThreads = 64 + 32 * kEpilogueWarps;   // producer, MMA, epilogue warps
 
 // Rotation kinds of one tensor.
