@@ -118,6 +118,14 @@ class DeviceWorkload:
                                    rope_theta=wl.theta, workspace=self.workspace, d_status=self.status,
                                    stream=stream)
 
+    def batch_chunks(self) -> list:
+        """The workload's chunks as kv_relocate_batch descriptors."""
+        return [kvrp.Chunk(k_src=a["srcs"][0], v_src=a["srcs"][1], n_tokens=a["n_tokens"], delta=a["delta"],
+                           k_dst=a["dst"][0], v_dst=a["dst"][1], rank=a["rank"], uk=a["u"][0], vk=a["w"][0],
+                           uv=a["u"][1], vv=a["w"][1], src_layer_stride=a["src_layer_stride"],
+                           u_layer_stride=a["u_layer_stride"], v_layer_stride=a["w_layer_stride"])
+                for a in self._chunks]
+
     def pools_host(self) -> dict:
         return {n: p.view(torch.int16).cpu().numpy().view(np.uint16) for n, p in self.pools.items()}
 

@@ -163,6 +163,36 @@ kvrp_status kv_relocate_batch(
     void* workspace, size_t workspace_bytes,
     uint32_t* d_status, kvrp_stream_t stream);
 
+/*
+ * kv_relocate_batch_noalloc -- kv_relocate_batch for callers that cannot
+ * allocate device memory.  The pages have no counterpart of this call; it
+ * exists for integration.  Some callers own no device allocator at all: a
+ * plugin inside a host engine that hands out only its own tensors, or a
+ * serving process whose memory pool reserved all of the GPU up front, so that
+ * an extra cudaMalloc either fails or breaks the pool's accounting; others
+ * cannot afford the device-wide synchronisation an allocation may cause.
+ * This call takes the same chunks and does the same work in the same single
+ * kernel launch, but keeps the launch's descriptors in a fixed array inside
+ * the library instead of a caller workspace.  It calls no cudaMalloc,
+ * cudaFree, cudaHostAlloc or other allocating routine.
+ *   Limits: at most KVRP_NOALLOC_MAX_CHUNKS chunks; more is rejected with
+ *   KVRP_ERR_INVALID_ARG before any work.  The array (about 0.55 MB) lives on
+ *   every GPU that loads the library, until the process exits.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   with cudaGetSymbolAddress (the device must be current); make that first
+ *   call before any stream capture.
+ *   Sharing: every call on a device uses the same array, and each call
+ *   rewrites the part its kernel reads.  Calls on one stream are ordered and
+ *   safe; calls that can overlap on the GPU (different streams, or several
+ *   host threads) race on the array and must not be issued.
+ */
+#define KVRP_NOALLOC_MAX_CHUNKS 256
+
+kvrp_status kv_relocate_batch_noalloc(
+    const kvrp_chunk* chunks, int32_t n_chunks,
+    int32_t n_layers, int32_t n_kv_heads, int32_t head_dim, double rope_theta,
+    uint32_t* d_status, kvrp_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvrp_status_string(kvrp_status status);
 

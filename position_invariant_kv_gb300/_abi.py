@@ -20,8 +20,10 @@ KVRP_DEV_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = (
     "kv_relocate_patch", "kv_relocate_patch_mla", "kv_relocate_batch",
-    "kv_relocate_batch_workspace_size", "kvrp_status_string", "kvrp_last_error", "kvrp_version",
+    "kv_relocate_batch_workspace_size", "kv_relocate_batch_noalloc", "kvrp_status_string",
+    "kvrp_last_error", "kvrp_version",
 )
+KVRP_NOALLOC_MAX_CHUNKS = 256
 
 
 class kvrp_dst(C.Structure):
@@ -60,6 +62,10 @@ def _load_library():
     L.kv_relocate_batch.argtypes = [
         C.POINTER(kvrp_chunk), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double,
         C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
+    L.kv_relocate_batch_noalloc.restype = st
+    L.kv_relocate_batch_noalloc.argtypes = [
+        C.POINTER(kvrp_chunk), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double, C.c_void_p,
+        C.c_void_p]
     L.kvrp_status_string.restype = C.c_char_p
     L.kvrp_status_string.argtypes = [C.c_int]
     L.kvrp_last_error.restype = C.c_char_p
@@ -198,3 +204,15 @@ def kv_relocate_batch(chunks: Sequence[Chunk], *, n_layers: int, n_kv_heads: int
     _check(lib().kv_relocate_batch(
         arr, len(chunks), int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
         _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))
+
+
+def kv_relocate_batch_noalloc(chunks: Sequence[Chunk], *, n_layers: int, n_kv_heads: int, head_dim: int,
+                              rope_theta: float, d_status=None, stream=None) -> None:
+    """kv_relocate_batch without a workspace, for callers that cannot allocate
+    device memory: the launch descriptors go to a fixed array inside the
+    library (at most KVRP_NOALLOC_MAX_CHUNKS chunks; calls that can overlap on
+    the GPU must not be issued, as they share that array)."""
+    arr = (kvrp_chunk * max(1, len(chunks)))(*[c.c() for c in chunks])
+    _check(lib().kv_relocate_batch_noalloc(
+        arr, len(chunks), int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
+        _ptr(d_status), _stream(stream)))

@@ -492,6 +492,46 @@ TensorIn tensor_in(const void* src, const void* u, const void* w, const kvrp_dst
   return t;
 }
 
+// The allocation-free batch path: same plan and kernel as kv_relocate_batch,
+// but the plan goes to the library's fixed device array.  The copy reads a
+// pageable host buffer, which the runtime stages before cudaMemcpyAsync
+// returns, so nothing is allocated on the device or pinned on the host here.
+kvrp_status run_noalloc(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d_status,
+                        cudaStream_t stream) {
+  DeviceInfo* di = nullptr;
+  kvrp_status st = device_info(&di);
+  if (st != KVRP_OK) return st;
+  PlanBuilder pb(sh);
+  for (const ChunkIn& c : chunks) {
+    st = pb.add(c);
+    if (st != KVRP_OK) return st;
+  }
+  std::vector<unsigned char> bytes;
+  int grid = 0, smem = 0;
+  st = pb.finish(di->sms, di->smem_optin, d_status, &bytes, &grid, &smem);
+  if (st != KVRP_OK) return st;
+  if (grid == 0) return KVRP_OK;
+  if (bytes.size() > noalloc_scratch_bytes())
+    return fail(KVRP_ERR_WORKSPACE, "plan of %zu bytes exceeds the fixed %zu-byte device array", bytes.size(),
+                noalloc_scratch_bytes());
+  void* scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(fixed plan array)");
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (di->prepared_smem < smem) {
+      e = prepare_kernel(di->smem_optin);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+      di->prepared_smem = di->smem_optin;
+    }
+  }
+  e = cudaMemcpyAsync(scratch, bytes.data(), bytes.size(), cudaMemcpyHostToDevice, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan to fixed array)");
+  e = launch_relocate(nullptr, scratch, grid, smem, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return KVRP_OK;
+}
+
 }  // namespace
 }  // namespace kvrp
 
@@ -593,6 +633,42 @@ kvrp_status kv_relocate_batch(const kvrp_chunk* chunks, int32_t n_chunks, int32_
   if (workspace_bytes < PlanBuilder::bound(n_chunks))
     return fail(KVRP_ERR_WORKSPACE, "workspace smaller than kv_relocate_batch_workspace_size(%d)", n_chunks);
   return run(sh, in, d_status, workspace, workspace_bytes, stream);
+}
+
+kvrp_status kv_relocate_batch_noalloc(const kvrp_chunk* chunks, int32_t n_chunks, int32_t n_layers,
+                                      int32_t n_kv_heads, int32_t head_dim, double rope_theta,
+                                      uint32_t* d_status, kvrp_stream_t stream) {
+  if (n_chunks < 0 || (n_chunks > 0 && !chunks)) return fail(KVRP_ERR_INVALID_ARG, "bad chunk array");
+  if (n_chunks > KVRP_NOALLOC_MAX_CHUNKS)
+    return fail(KVRP_ERR_INVALID_ARG, "kv_relocate_batch_noalloc takes at most %d chunks (got %d)",
+                KVRP_NOALLOC_MAX_CHUNKS, n_chunks);
+  if (n_chunks == 0) return KVRP_OK;
+  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
+  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
+  std::vector<ChunkIn> in(n_chunks);
+  for (int i = 0; i < n_chunks; ++i) {
+    const kvrp_chunk& k = chunks[i];
+    ChunkIn& c = in[i];
+    c.n_tensors = 2;
+    c.t[0] = tensor_in(k.k_src, k.uk, k.vk, &k.k_dst, head_dim == 128 ? kRotHalf128 : kRotHalf64, 0);
+    c.t[1] = tensor_in(k.v_src, k.uv, k.vv, &k.v_dst, kRotNone, 0);
+    c.src_layer_stride = k.src_layer_stride;
+    c.u_layer_stride = k.u_layer_stride;
+    c.w_layer_stride = k.v_layer_stride;
+    c.n_tokens = k.n_tokens;
+    c.rank = k.rank;
+    c.delta = k.delta;
+    kvrp_status st = check_chunk(c, sh);
+    if (st != KVRP_OK) {
+      std::string msg = "chunk " + std::to_string(i) + ": " + g_last_error;
+      std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg.c_str());
+      return st;
+    }
+  }
+  return run_noalloc(sh, in, d_status, stream);
 }
 
 const char* kvrp_status_string(kvrp_status status) {

@@ -22,6 +22,9 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <map>
+#include <mutex>
+
 #include "kvrp.h"
 #include "kvrp_plan.h"
 
@@ -651,6 +654,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 }  // namespace dev
+
+// ---------------------------------------------------------------------------
+// Allocation-free batch path.  The launch plan of kv_relocate_batch_noalloc
+// lives in this fixed device array instead of a caller-provided workspace, so
+// that callers who cannot allocate device memory can still run a batch.  Every
+// GPU that loads the library holds the array until the process exits; all
+// calls on a device share it.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t align128(size_t v) { return (v + 127) & ~static_cast<size_t>(127); }
+constexpr size_t kNoAllocScratchBytes =
+    align128(align128(align128(align128(align128(sizeof(PlanHdr)) +
+                                        (size_t)kNoAllocMaxChunks * 8 * sizeof(CUtensorMap)) +
+                               (size_t)kNoAllocMaxChunks * kTablePairs * sizeof(float4)) +
+                      (size_t)kNoAllocMaxChunks * sizeof(ChunkRec)) +
+             (size_t)(kNoAllocMaxChunks + 1) * sizeof(int32_t));
+
+static __device__ __align__(256) unsigned char g_noalloc_plan[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_ptr;   // device ordinal -> device address of g_noalloc_plan
+}  // namespace
+
+size_t noalloc_scratch_bytes() { return kNoAllocScratchBytes; }
+
+cudaError_t noalloc_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  auto found = g_noalloc_ptr.find(dev);
+  if (found != g_noalloc_ptr.end()) {
+    *ptr = found->second;
+    return cudaSuccess;
+  }
+  // In host code g_noalloc_plan names a host-side stand-in, not device
+  // memory: the device address must come from the runtime, per device, with
+  // that device current.
+  void* p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_noalloc_plan);
+  if (e != cudaSuccess) return e;
+  g_noalloc_ptr[dev] = p;
+  *ptr = p;
+  return cudaSuccess;
+}
 
 cudaError_t prepare_kernel(int smem_bytes) {
   cudaError_t e = cudaFuncSetAttribute(dev::relocate_kernel<true>,

@@ -100,4 +100,11 @@ cudaError_t launch_relocate(const void* param_plan, const void* dev_plan, int gr
 // Per-device one-time kernel setup (dynamic shared-memory opt-in).
 cudaError_t prepare_kernel(int smem_bytes);
 
+// Allocation-free batch path: the largest batch its fixed device array holds,
+// the array's size, and its device address on the current device (looked up
+// once per device with cudaGetSymbolAddress).
+constexpr int kNoAllocMaxChunks = 256;
+size_t noalloc_scratch_bytes();
+cudaError_t noalloc_scratch(void** ptr);
+
 }  // namespace kvrp
