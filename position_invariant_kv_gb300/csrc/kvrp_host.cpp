@@ -330,17 +330,24 @@ class PlanBuilder {
     h.n_items = static_cast<int32_t>(items);
     // pipeline depth from the shared-memory budget (and TMEM: 128 columns a stage)
     const int budget = smem_optin - 1024;
-    int stages = 0;
-    for (int s = kMaxStages; s >= 2; --s) {
-      if ((int)smem_layout(m_max_, s).total <= budget) {
-        stages = s;
-        break;
+    int stages = 0, u_bufs = 0;
+    for (int ub = 2; ub >= 1 && stages == 0; --ub) {
+      for (int s = kMaxStages - kMaxStages % kEpiGroups; s >= kEpiGroups; s -= kEpiGroups) {
+        if ((int)smem_layout(m_max_, s, ub).total <= budget) {
+          stages = s;
+          u_bufs = ub;
+          break;
+        }
       }
     }
     if (stages == 0) return fail(KVRP_ERR_UNSUPPORTED, "rank %d does not fit in shared memory", m_max_);
     h.stages = stages;
+    h.u_bufs = u_bufs;
     h.tmem_cols = 0;
-    if (m_max_ > 0) h.tmem_cols = kAccSlots * kSubCols;   // 512 columns: the whole TMEM of the SM
+    if (m_max_ > 0) {
+      h.tmem_cols = 32;
+      while (h.tmem_cols < kAccSlots * kSubCols) h.tmem_cols *= 2;
+    }
     auto align = [](size_t v) { return (v + 127) & ~static_cast<size_t>(127); };
     size_t off = align(sizeof(PlanHdr));
     h.off_maps = static_cast<uint32_t>(off);
@@ -359,7 +366,7 @@ class PlanBuilder {
     std::memcpy(out->data() + h.off_chunks, chunks_.data(), chunks_.size() * sizeof(ChunkRec));
     std::memcpy(out->data() + h.off_ibeg, ibeg.data(), ibeg.size() * sizeof(int32_t));
     *grid = static_cast<int>(std::min<int64_t>(items, sms));
-    *smem_bytes = static_cast<int>(smem_layout(m_max_, stages).total) + 1024;
+    *smem_bytes = static_cast<int>(smem_layout(m_max_, stages, u_bufs).total) + 1024;
     return KVRP_OK;
   }
 

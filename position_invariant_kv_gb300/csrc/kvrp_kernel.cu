@@ -144,26 +144,13 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // completed (tcgen05.wait::ld) inside the same asm statement.
 #define KVRP_R8(a, o) "=r"(a[o + 0]), "=r"(a[o + 1]), "=r"(a[o + 2]), "=r"(a[o + 3]), \
                       "=r"(a[o + 4]), "=r"(a[o + 5]), "=r"(a[o + 6]), "=r"(a[o + 7])
-__device__ __forceinline__ void tmem_ld_2x16(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
-                                             uint32_t (&b)[32]) {
+__device__ __forceinline__ void tmem_ld_2x16(uint32_t ta, uint32_t tb, uint32_t (&a)[16],
+                                             uint32_t (&b)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
       "tcgen05.wait::ld.sync.aligned;"
       : KVRP_R8(a, 0), KVRP_R8(a, 8), KVRP_R8(b, 0), KVRP_R8(b, 8)
-      : "r"(ta), "r"(tb)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld_2x32(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
-                                             uint32_t (&b)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : KVRP_R8(a, 0), KVRP_R8(a, 8), KVRP_R8(a, 16), KVRP_R8(a, 24),
-        KVRP_R8(b, 0), KVRP_R8(b, 8), KVRP_R8(b, 16), KVRP_R8(b, 24)
       : "r"(ta), "r"(tb)
       : "memory");
 }
@@ -289,53 +276,53 @@ __device__ __forceinline__ void turn_pair_patch(float xl, float xh, float4 e, fl
 
 // N = columns per part (32 or 16).  The thread owns two parts of N columns
 // starting at a0 and a1; with ROT, element j of part a pairs with element j
-// of part b and uses table entry tab0 + j.
+// of part b and uses table entry tab0 + j.  Accumulators are read in rounds of
+// 16 columns per part to keep register use low.
 template <int N, bool ROT, bool PATCH>
 __device__ __forceinline__ void epilogue_part(uint32_t xbase, int row, int a0, int a1,
                                               const float4* __restrict__ tab, int tab0,
                                               uint32_t tm_a, uint32_t tm_b) {
-  uint32_t pa[32], pb[32];
-  if constexpr (PATCH) {
-    if constexpr (N == 32) tmem_ld_2x32(tm_a, tm_b, pa, pb);
-    else tmem_ld_2x16(tm_a, tm_b, pa, pb);
-  }
 #pragma unroll
-  for (int k = 0; k < N / 8; ++k) {
-    const uint32_t addr_a = x_chunk_addr(xbase, row, (a0 >> 3) + k);
-    const uint32_t addr_b = x_chunk_addr(xbase, row, (a1 >> 3) + k);
-    const uint4 va = lds128(addr_a);
-    const uint4 vb = lds128(addr_b);
-    const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
-    const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
-    uint32_t oa[4], ob[4];
+  for (int r0 = 0; r0 < N; r0 += 16) {
+    uint32_t pa[16], pb[16];
+    if constexpr (PATCH) tmem_ld_2x16(tm_a + r0, tm_b + r0, pa, pb);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      float xl0 = bf_lo(wa[w]), xl1 = bf_hi(wa[w]);
-      float xh0 = bf_lo(wb[w]), xh1 = bf_hi(wb[w]);
-      float yl0, yl1, yh0, yh1;
-      if constexpr (ROT) {
-        const float4 e0 = tab[tab0 + 8 * k + 2 * w];
-        const float4 e1 = tab[tab0 + 8 * k + 2 * w + 1];
-        if constexpr (PATCH) {
-          turn_pair_patch(xl0, xh0, e0, __uint_as_float(pa[8 * k + 2 * w]),
-                          __uint_as_float(pb[8 * k + 2 * w]), yl0, yh0);
-          turn_pair_patch(xl1, xh1, e1, __uint_as_float(pa[8 * k + 2 * w + 1]),
-                          __uint_as_float(pb[8 * k + 2 * w + 1]), yl1, yh1);
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t addr_a = x_chunk_addr(xbase, row, ((a0 + r0) >> 3) + k);
+      const uint32_t addr_b = x_chunk_addr(xbase, row, ((a1 + r0) >> 3) + k);
+      const uint4 va = lds128(addr_a);
+      const uint4 vb = lds128(addr_b);
+      const uint32_t wa[4] = {va.x, va.y, va.z, va.w};
+      const uint32_t wb[4] = {vb.x, vb.y, vb.z, vb.w};
+      uint32_t oa[4], ob[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int e = 8 * k + 2 * w;
+        float xl0 = bf_lo(wa[w]), xl1 = bf_hi(wa[w]);
+        float xh0 = bf_lo(wb[w]), xh1 = bf_hi(wb[w]);
+        float yl0, yl1, yh0, yh1;
+        if constexpr (ROT) {
+          const float4 e0 = tab[tab0 + r0 + e];
+          const float4 e1 = tab[tab0 + r0 + e + 1];
+          if constexpr (PATCH) {
+            turn_pair_patch(xl0, xh0, e0, __uint_as_float(pa[e]), __uint_as_float(pb[e]), yl0, yh0);
+            turn_pair_patch(xl1, xh1, e1, __uint_as_float(pa[e + 1]), __uint_as_float(pb[e + 1]), yl1, yh1);
+          } else {
+            turn_pair(xl0, xh0, e0, yl0, yh0);
+            turn_pair(xl1, xh1, e1, yl1, yh1);
+          }
         } else {
-          turn_pair(xl0, xh0, e0, yl0, yh0);
-          turn_pair(xl1, xh1, e1, yl1, yh1);
+          yl0 = xl0 + __uint_as_float(pa[e]);
+          yl1 = xl1 + __uint_as_float(pa[e + 1]);
+          yh0 = xh0 + __uint_as_float(pb[e]);
+          yh1 = xh1 + __uint_as_float(pb[e + 1]);
         }
-      } else {
-        yl0 = xl0 + __uint_as_float(pa[8 * k + 2 * w]);
-        yl1 = xl1 + __uint_as_float(pa[8 * k + 2 * w + 1]);
-        yh0 = xh0 + __uint_as_float(pb[8 * k + 2 * w]);
-        yh1 = xh1 + __uint_as_float(pb[8 * k + 2 * w + 1]);
+        oa[w] = pack_bf2(yl0, yl1);
+        ob[w] = pack_bf2(yh0, yh1);
       }
-      oa[w] = pack_bf2(yl0, yl1);
-      ob[w] = pack_bf2(yh0, yh1);
+      sts128(addr_a, make_uint4(oa[0], oa[1], oa[2], oa[3]));
+      sts128(addr_b, make_uint4(ob[0], ob[1], ob[2], ob[3]));
     }
-    sts128(addr_a, make_uint4(oa[0], oa[1], oa[2], oa[3]));
-    sts128(addr_b, make_uint4(ob[0], ob[1], ob[2], ob[3]));
   }
 }
 
@@ -357,21 +344,6 @@ struct Bars {
 };
 static_assert(8 * (2 * kMaxStages + 2 * kAccSlots + 5) <= 512, "barriers must fit below the TMEM slot");
 
-// Named barrier over the two epilogue warps that share a TMEM lane quarter
-// (ids 1..4), ORing a predicate across them.
-__device__ __forceinline__ bool pair_bar_or(int id, bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "barrier.cta.red.or.pred q, %2, 64, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred), "r"(id)
-      : "memory");
-  return out != 0;
-}
-
 template <bool kParamPlan>
 __global__ void __launch_bounds__(kThreads, 1)
     relocate_kernel(const __grid_constant__ ParamPlan pp, const unsigned char* __restrict__ gplan) {
@@ -381,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout(h.m_max, h.stages);
+  const SmemLayout L = smem_layout(h.m_max, h.stages, h.u_bufs);
+  const uint32_t NU = (uint32_t)h.u_bufs;
   const uint32_t sbase = smem_u32(smem);
   const Bars bars{sbase};
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 512);
@@ -394,11 +367,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bars.full(s), 1);
-      mbar_init(bars.empty(s), kEpilogueWarps);
+      // released by the owning group's warps and, when there is an MMA issuer, by it
+      mbar_init(bars.empty(s), kGroupWarps + (h.tmem_cols > 0 ? 1 : 0));
     }
     for (int a = 0; a < kAccSlots; ++a) {
       mbar_init(bars.acc_full(a), 1);
-      mbar_init(bars.acc_empty(a), kEpilogueWarps);
+      mbar_init(bars.acc_empty(a), kGroupWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bars.u_full(b), 1);
@@ -429,8 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = I.c->rank;
         const int nkb = m >> 4;
         if (m > 0) {
-          const int ub = uit & 1;
-          ok = wait_phase(bars.u_empty(ub), ((uit >> 1) & 1) ^ 1, abort_flag, h.status);
+          const int ub = (int)(uit % NU);
+          ok = wait_phase(bars.u_empty(ub), ((uit / NU) & 1) ^ 1, abort_flag, h.status);
           if (!ok) break;
           const CUtensorMap* mu = plan_map(plan, h, I.t->map_u);
           mbar_expect_tx(bars.u_full(ub), (uint32_t)nkb * (kTileRows * 32));
@@ -465,51 +439,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         volatile int no_abort = 0;
         wait_phase(bars.full((int)(j % (uint32_t)S)), (j / S) & 1, &no_abort, nullptr);
       }
-      const uint32_t ufirst = uit > 2u ? uit - 2u : 0u;
+      const uint32_t ufirst = uit > NU ? uit - NU : 0u;
       for (uint32_t j = ufirst; j < uit; ++j) {
         volatile int no_abort = 0;
-        wait_phase(bars.u_full((int)(j & 1)), (j >> 1) & 1, &no_abort, nullptr);
+        wait_phase(bars.u_full((int)(j % NU)), (j / NU) & 1, &no_abort, nullptr);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0 && h.tmem_cols > 0) {
-      uint32_t it = 0, uit = 0, ait = 0;
+      uint32_t it = 0, uit = 0;
+      uint32_t gcnt[kEpiGroups] = {};   // patched sub-tiles issued into each group's slot
       bool ok = true;
       bool issued = false;
       for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
         const Item I = decode_item(plan, h, item);
         const int m = I.c->rank;
-        if (m == 0) {
-          it += (uint32_t)(I.s1 - I.s0);
-          continue;
-        }
         const int nkb = m >> 4;
-        const int ub = uit & 1;
-        ok = wait_phase(bars.u_full(ub), (uit >> 1) & 1, abort_flag, h.status);
-        if (!ok) break;
-        for (int s = I.s0; s < I.s1; ++s, ++it, ++ait) {
+        const int ub = (int)(uit % NU);
+        if (m > 0) {
+          ok = wait_phase(bars.u_full(ub), (uit / NU) & 1, abort_flag, h.status);
+          if (!ok) break;
+        }
+        for (int s = I.s0; s < I.s1; ++s, ++it) {
           const int st = (int)(it % (uint32_t)S);
-          const int a = (int)(ait % kAccSlots);
+          // observe every stage use, patched or not, and take part in its release
           ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
           if (!ok) break;
-          ok = wait_phase(bars.acc_empty(a), ((ait / kAccSlots) & 1) ^ 1, abort_flag, h.status);
-          if (!ok) break;
-          tc_fence_after();
-          const int width = min(kSubCols, h.D - kSubCols * s);
-          const uint32_t idesc = idesc_bf16_f32(width);
-          const uint32_t d_tmem = tmem_base + (uint32_t)a * kSubCols;
-          for (int k = 0; k < nkb; ++k) {
-            const uint64_t ad = desc_k_sw32(u_buf(ub) + (uint32_t)k * (kTileRows * 32));
-            const uint64_t bd = desc_k_sw32(w_buf(st) + (uint32_t)k * (uint32_t)width * 32u);
-            mma_bf16(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+          if (m > 0) {
+            const int a = (int)(it % kEpiGroups);     // the slot of the group that owns this stage
+            ok = wait_phase(bars.acc_empty(a), (gcnt[a] & 1) ^ 1, abort_flag, h.status);
+            if (!ok) break;
+            tc_fence_after();
+            const int width = min(kSubCols, h.D - kSubCols * s);
+            const uint32_t idesc = idesc_bf16_f32(width);
+            const uint32_t d_tmem = tmem_base + (uint32_t)a * kSubCols;
+            for (int k = 0; k < nkb; ++k) {
+              const uint64_t ad = desc_k_sw32(u_buf(ub) + (uint32_t)k * (kTileRows * 32));
+              const uint64_t bd = desc_k_sw32(w_buf(st) + (uint32_t)k * (uint32_t)width * 32u);
+              mma_bf16(d_tmem, ad, bd, idesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(bars.acc_full(a));
+            issued = true;
+            ++gcnt[a];
           }
-          mma_commit(bars.acc_full(a));
-          issued = true;
+          // the group releases the stage only after acc_full, i.e. after these MMAs read it
+          mbar_arrive(bars.empty(st));
         }
         if (!ok) break;
-        mma_commit(bars.u_empty(ub));
-        ++uit;
+        if (m > 0) {
+          mma_commit(bars.u_empty(ub));
+          ++uit;
+        }
       }
       if (issued) {
         // every MMA this thread issued has completed once `drain` flips
@@ -520,17 +501,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------------- epilogue
-    // Two warps share each TMEM lane quarter (32 tile rows) and split the
-    // columns; each pair syncs on its own named barrier, and the first row of
-    // every 16-row page issues that page's TMA stores.
+    // Two groups of four warps take sub-tiles in turn (group g owns the stages
+    // s with s % 2 == g, so it sees every phase of them).  Each warp owns the
+    // 32 tile rows of its TMEM lane quarter across all columns, so it needs no
+    // other warp: it turns, patches and rounds its rows in shared memory, then
+    // lanes 0 and 16 store the warp's two 16-row pages by TMA.
     const int ew = warp - 2;                 // 0..7
+    const int group = ew / kGroupWarps;      // which sub-tiles this warp serves
     const int quarter = warp & 3;            // TMEM lanes this warp may read
-    const int half = ew >> 2;                // which share of the columns
     const int row = quarter * 32 + lane;     // tile row (token) of this thread
-    const int pair_id = 1 + quarter;
-    const bool leader = ((row & (kPage - 1)) == 0) && half == 0;
-    uint32_t it = 0, ait = 0;
-    for (int item = blockIdx.x; item < h.n_items; item += gridDim.x) {
+    const bool leader = (lane & (kPage - 1)) == 0;
+    uint32_t it = 0;
+    uint32_t gait = 0;                       // patched sub-tiles this group has taken
+    const uint32_t tslot = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)group * kSubCols;
+    bool aborted = false;
+    for (int item = blockIdx.x; !aborted && item < h.n_items; item += gridDim.x) {
       const Item I = decode_item(plan, h, item);
       const int m = I.c->rank;
       const TensorRec& T = *I.t;
@@ -550,53 +535,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t lp = (I.q0 + row) / kPage;
         page = T.block_table ? (int64_t)__ldg(T.block_table + lp) : lp;   // used at store time
       }
-      bool aborted = false;
       for (int s = I.s0; s < I.s1; ++s, ++it) {
+        if ((int)(it % kEpiGroups) != group) continue;   // another group's sub-tile
         const int st = (int)(it % (uint32_t)S);
-        const int acc = (int)(ait % kAccSlots);
         bool ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
         if (ok && m > 0) {
-          ok = wait_phase(bars.acc_full(acc), (ait / kAccSlots) & 1, abort_flag, h.status);
+          ok = wait_phase(bars.acc_full(group), gait & 1, abort_flag, h.status);
           tc_fence_after();
         }
         ok = __all_sync(0xffffffffu, ok);     // TMEM loads below are warp-collective
+        if (!ok) {
+          aborted = true;
+          break;
+        }
         const int width = min(kSubCols, h.D - kSubCols * s);
         const uint32_t xb = x_buf(st);
-        // which columns this warp owns, and whether they turn
-        int a0, a1;
-        bool rot;
-        if (width == kSubCols) {
-          if (T.rot_kind == kRotHalf128) {
-            a0 = 32 * half;
-            a1 = 64 + 32 * half;
-            rot = true;
-          } else {
-            a0 = 64 * half;
-            a1 = a0 + 32;
-            rot = T.rot_kind == kRotHalf64 && kSubCols * s + 64 * half >= T.rot_from;
-          }
+        const uint32_t tcol = tslot;
+        if (width == kSubCols && T.rot_kind == kRotHalf128) {
+          // one head of 128: column j pairs with j + 64
+          if (m > 0) epilogue_part<64, true, true>(xb, row, 0, 64, tab, 0, tcol, tcol + 64);
+          else epilogue_part<64, true, false>(xb, row, 0, 64, tab, 0, 0, 0);
         } else {
-          a0 = 16 * half;
-          a1 = a0 + 32;
-          rot = T.rot_kind == kRotHalf64 && kSubCols * s >= T.rot_from;
-        }
-        const int nchunk = (width == kSubCols ? 32 : 16) / 8;
-        if (ok) {
-          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)acc * kSubCols;
-          const int tab0 = a0 & 63;
-          if (width == kSubCols) {
+          // each 64-wide box on its own: turned (pairs j, j + 32) or not
+          for (int b = 0; b < width / kBoxCols; ++b) {
+            const int a0 = kBoxCols * b;
+            const bool rot = T.rot_kind == kRotHalf64 && kSubCols * s + a0 >= T.rot_from;
             if (m > 0) {
-              if (rot) epilogue_part<32, true, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
-              else epilogue_part<32, false, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
+              if (rot) epilogue_part<32, true, true>(xb, row, a0, a0 + 32, tab, 0, tcol + a0, tcol + a0 + 32);
+              else epilogue_part<32, false, true>(xb, row, a0, a0 + 32, tab, 0, tcol + a0, tcol + a0 + 32);
             } else if (rot) {
-              epilogue_part<32, true, false>(xb, row, a0, a1, tab, tab0, 0, 0);
-            }
-          } else {
-            if (m > 0) {
-              if (rot) epilogue_part<16, true, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
-              else epilogue_part<16, false, true>(xb, row, a0, a1, tab, tab0, tcol + a0, tcol + a1);
-            } else if (rot) {
-              epilogue_part<16, true, false>(xb, row, a0, a1, tab, tab0, 0, 0);
+              epilogue_part<32, true, false>(xb, row, a0, a0 + 32, tab, 0, 0, 0);
             }
           }
         }
@@ -604,23 +572,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           // release this accumulator slot to the MMA issuer
           tc_fence_before();
           __syncwarp();
-          if (lane == 0 && ok) mbar_arrive(bars.acc_empty(acc));
-          ++ait;
+          if (lane == 0) mbar_arrive(bars.acc_empty(group));
+          ++gait;
         }
         fence_proxy_async_smem();
-        aborted = pair_bar_or(pair_id, !ok || *abort_flag);
-        if (aborted) break;
+        __syncwarp();
 
         // ---- stores: whole pages by TMA (issued by the page's first row),
-        //      rows of partly covered pages by their owner threads
+        //      rows of partly covered pages by their own threads
         if (valid) {
           const bool page_ok = page >= 0 && page < T.num_pages;
           if (!page_ok) {
             if (h.status && (leader || !whole_page)) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
           } else if (whole_page) {
             if (leader) {
-              const int nbox = width / kBoxCols;
-              for (int j = 0; j < nbox; ++j)
+              for (int j = 0; j < width / kBoxCols; ++j)
                 tma_store_3d(md, xb + (uint32_t)j * (kTileRows * kBoxCols * 2) + (uint32_t)pg_row * 128u,
                              kSubCols * s + kBoxCols * j, (int)(page * kPage), I.layer);
               bulk_commit();
@@ -629,17 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             uint16_t* dst_row = T.dst + (int64_t)I.layer * T.dst_layer_stride +
                                 (page * kPage + (I.q0 + row) % kPage) * (int64_t)h.D + kSubCols * s;
-            for (int k = 0; k < nchunk; ++k) {
-              const int c0 = (a0 >> 3) + k, c1 = (a1 >> 3) + k;
-              stg128(dst_row + 8 * c0, lds128(x_chunk_addr(xb, row, c0)));
-              stg128(dst_row + 8 * c1, lds128(x_chunk_addr(xb, row, c1)));
-            }
+            for (int c = 0; c < width / 8; ++c) stg128(dst_row + 8 * c, lds128(x_chunk_addr(xb, row, c)));
           }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.empty(st));
       }
-      if (aborted) break;
     }
     bulk_wait_0();   // this thread's page stores are complete before the CTA exits
   }

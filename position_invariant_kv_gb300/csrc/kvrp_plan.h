@@ -18,9 +18,16 @@ constexpr int kBoxCols = 64;        // features per 128-byte swizzled TMA box
 constexpr int kMaxRank = 128;
 constexpr int kTablePairs = 64;     // phase-table entries (head_dim / 2 <= 64)
 constexpr int kParamPlanBytes = 3072;
-constexpr int kEpilogueWarps = 8;
+constexpr int kGroupWarps = 4;      // epilogue warps that share one sub-tile (one per TMEM lane quarter)
+constexpr int kEpiGroups = 2;       // epilogue groups, taking sub-tiles in turn
+constexpr int kEpilogueWarps = kGroupWarps * kEpiGroups;
+// Every mbarrier waiter must see each phase it waits on in order, or a phase
+// two uses old could pass for the current one.  Hence: stage s belongs to
+// epilogue group s % kEpiGroups (the depth is a multiple of kEpiGroups), each
+// group owns one TMEM accumulator slot, and the MMA issuer observes every
+// stage use (its arrival is part of the stage's release).
+constexpr int kAccSlots = kEpiGroups;
 constexpr int kMaxStages = 8;       // shared-memory pipeline depth bound
-constexpr int kAccSlots = 4;        // TMEM accumulators of 128 fp32 columns
 constexpr int kThreads = 64 + 32 * kEpilogueWarps;   // producer, MMA, epilogue warps
 
 // Rotation kinds of one tensor.
@@ -64,6 +71,7 @@ struct PlanHdr {
   int32_t stages;                         // pipeline depth
   int32_t m_max;                          // largest rank in the plan (multiple of 16)
   int32_t tmem_cols;                      // allocated TMEM columns (0 = none)
+  int32_t u_bufs;                         // U tile buffers (2, or 1 at the largest ranks)
   uint32_t off_maps, off_tabs, off_chunks, off_ibeg;
   uint32_t total_bytes;
   uint32_t* status;                       // optional device status word
@@ -72,13 +80,13 @@ static_assert(sizeof(PlanHdr) <= 128, "header must fit in 128 bytes");
 
 // Shared-memory carve-up for a given rank bound and depth.
 struct SmemLayout {
-  uint32_t u_off, u_bytes;        // two U buffers
+  uint32_t u_off, u_bytes;        // U buffers
   uint32_t stage_off, stage_bytes;
   uint32_t x_bytes, w_bytes;      // inside a stage: X sub-tile, then W slice
   uint32_t total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int m_max, int stages) {
+__host__ __device__ inline SmemLayout smem_layout(int m_max, int stages, int u_bufs) {
   SmemLayout s;
   const uint32_t kb = (uint32_t)(m_max / 16);
   s.u_off = 1024;                                  // barriers live in the first 1 KB
@@ -86,7 +94,7 @@ __host__ __device__ inline SmemLayout smem_layout(int m_max, int stages) {
   s.x_bytes = kTileRows * kSubCols * 2;            // 32 KB
   s.w_bytes = kb * (kSubCols * 32);
   s.stage_bytes = s.x_bytes + s.w_bytes;
-  s.stage_off = s.u_off + 2 * s.u_bytes;
+  s.stage_off = s.u_off + (uint32_t)u_bufs * s.u_bytes;
   s.total = s.stage_off + (uint32_t)stages * s.stage_bytes;
   return s;
 }
