@@ -235,6 +235,8 @@ def bench_ours(args) -> dict:
     kvrp.lib()
 
     wl = W.config(args.config)
+    if args.layers:
+        wl.n_layers = min(wl.n_layers, args.layers)   # a smaller copy of the workload for profiler captures
     dwl = harness.DeviceWorkload(wl, f"cuda:{local}")
     stream = torch.cuda.current_stream()
     nbytes = wl.algorithmic_bytes()
@@ -387,6 +389,7 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling captures)")
     ap.add_argument("--budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)

@@ -98,14 +98,23 @@ float head16(double v) {
   return static_cast<float>(std::ldexp(std::nearbyint(std::ldexp(m, 16)), e - 16));
 }
 
+// Layout, two pairs per float4 so the kernel can use packed fp32x2 math:
+//   tab[2j]     = {C_2j,  C_2j+1,  S_2j,  S_2j+1}    (16-bit heads)
+//   tab[2j + 1] = {Cl_2j, Cl_2j+1, Sl_2j, Sl_2j+1}   (fp32 tails)
 void phase_table(int64_t delta, double theta, int rot_dim, float4* tab) {
-  for (int i = 0; i < kTablePairs; ++i) tab[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float head_c[kTablePairs] = {}, head_s[kTablePairs] = {}, tail_c[kTablePairs] = {}, tail_s[kTablePairs] = {};
   for (int i = 0; i < rot_dim / 2; ++i) {
     const double inv = std::pow(theta, -2.0 * i / rot_dim);
     const double phi = static_cast<double>(delta) * inv;
     const double c = std::cos(phi), s = std::sin(phi);
-    const float ch = head16(c), sh = head16(s);
-    tab[i] = make_float4(ch, sh, static_cast<float>(c - ch), static_cast<float>(s - sh));
+    head_c[i] = head16(c);
+    head_s[i] = head16(s);
+    tail_c[i] = static_cast<float>(c - head_c[i]);
+    tail_s[i] = static_cast<float>(s - head_s[i]);
+  }
+  for (int j = 0; j < kTablePairs / 2; ++j) {
+    tab[2 * j] = make_float4(head_c[2 * j], head_c[2 * j + 1], head_s[2 * j], head_s[2 * j + 1]);
+    tab[2 * j + 1] = make_float4(tail_c[2 * j], tail_c[2 * j + 1], tail_s[2 * j], tail_s[2 * j + 1]);
   }
 }
 

@@ -249,29 +249,36 @@ __device__ __forceinline__ uint32_t x_chunk_addr(uint32_t xbase, int r, int k) {
   return xbase + ((uint32_t)(k >> 3) << 14) + ((uint32_t)r << 7) + ((uint32_t)((k & 7) ^ (r & 7)) << 4);
 }
 
-// Rotate one pair of elements: lower element xl, upper element xh, split table
-// entry (head cos, head sin, tail cos, tail sin).  The heads carry 16
-// significant bits, so xh*S and xl*C are exact in fp32 for bf16 x.
-__device__ __forceinline__ void turn_pair(float xl, float xh, float4 e, float& yl, float& yh) {
-  const float a = xh * e.y;
-  const float b = fmaf(xl, e.x, -a);
-  const float tl = fmaf(xl, e.z, -(xh * e.w));
-  const float a2 = xl * e.y;
-  const float b2 = fmaf(xh, e.x, a2);
-  const float th = fmaf(xh, e.z, xl * e.w);
-  yl = b + tl;
-  yh = b2 + th;
+// Rotate two neighbouring pairs at once with packed fp32x2 arithmetic.  xl /
+// xh hold the lower / upper elements of pairs (i, i+1); `head` holds their
+// 16-significant-bit cos and sin heads {C_i, C_i+1, S_i, S_i+1}, `tail` the
+// fp32 remainders {Cl_i, Cl_i+1, Sl_i, Sl_i+1}.  Because a bf16 value times a
+// 16-bit head is exact in fp32, x_l*C - x_h*S is formed with one rounding;
+// the tails add the rest of the fp64 cos/sin.  Every packed operation rounds
+// each lane exactly like its scalar counterpart.
+__device__ __forceinline__ float2 neg2(float2 v) { return make_float2(-v.x, -v.y); }
+
+__device__ __forceinline__ void turn2(float2 xl, float2 xh, float4 head, float4 tail, float2& yl,
+                                      float2& yh) {
+  const float2 C = make_float2(head.x, head.y), S = make_float2(head.z, head.w);
+  const float2 Cl = make_float2(tail.x, tail.y), Sl = make_float2(tail.z, tail.w);
+  const float2 b = __ffma2_rn(xl, C, neg2(__fmul2_rn(xh, S)));
+  const float2 tl = __ffma2_rn(xl, Cl, neg2(__fmul2_rn(xh, Sl)));
+  const float2 b2 = __ffma2_rn(xh, C, __fmul2_rn(xl, S));
+  const float2 th = __ffma2_rn(xh, Cl, __fmul2_rn(xl, Sl));
+  yl = __fadd2_rn(b, tl);
+  yh = __fadd2_rn(b2, th);
 }
-__device__ __forceinline__ void turn_pair_patch(float xl, float xh, float4 e, float pl, float ph,
-                                                float& yl, float& yh) {
-  const float a = xh * e.y;
-  const float b = fmaf(xl, e.x, -a);
-  const float tl = fmaf(xl, e.z, -(xh * e.w));
-  const float a2 = xl * e.y;
-  const float b2 = fmaf(xh, e.x, a2);
-  const float th = fmaf(xh, e.z, xl * e.w);
-  yl = b + (tl + pl);
-  yh = b2 + (th + ph);
+__device__ __forceinline__ void turn2_patch(float2 xl, float2 xh, float4 head, float4 tail, float2 pl,
+                                            float2 ph, float2& yl, float2& yh) {
+  const float2 C = make_float2(head.x, head.y), S = make_float2(head.z, head.w);
+  const float2 Cl = make_float2(tail.x, tail.y), Sl = make_float2(tail.z, tail.w);
+  const float2 b = __ffma2_rn(xl, C, neg2(__fmul2_rn(xh, S)));
+  const float2 tl = __ffma2_rn(xl, Cl, neg2(__fmul2_rn(xh, Sl)));
+  const float2 b2 = __ffma2_rn(xh, C, __fmul2_rn(xl, S));
+  const float2 th = __ffma2_rn(xh, Cl, __fmul2_rn(xl, Sl));
+  yl = __fadd2_rn(b, __fadd2_rn(tl, pl));
+  yh = __fadd2_rn(b2, __fadd2_rn(th, ph));
 }
 
 // N = columns per part (32 or 16).  The thread owns two parts of N columns
@@ -297,28 +304,25 @@ __device__ __forceinline__ void epilogue_part(uint32_t xbase, int row, int a0, i
       uint32_t oa[4], ob[4];
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
-        const int e = 8 * k + 2 * w;
-        float xl0 = bf_lo(wa[w]), xl1 = bf_hi(wa[w]);
-        float xh0 = bf_lo(wb[w]), xh1 = bf_hi(wb[w]);
-        float yl0, yl1, yh0, yh1;
+        const int e = 8 * k + 2 * w;        // elements e, e + 1 of both parts
+        const float2 xl = make_float2(bf_lo(wa[w]), bf_hi(wa[w]));
+        const float2 xh = make_float2(bf_lo(wb[w]), bf_hi(wb[w]));
+        float2 yl, yh;
         if constexpr (ROT) {
-          const float4 e0 = tab[tab0 + r0 + e];
-          const float4 e1 = tab[tab0 + r0 + e + 1];
+          const float4 head = tab[tab0 + r0 + e];       // table entries are stored two pairs at a time
+          const float4 tail = tab[tab0 + r0 + e + 1];
           if constexpr (PATCH) {
-            turn_pair_patch(xl0, xh0, e0, __uint_as_float(pa[e]), __uint_as_float(pb[e]), yl0, yh0);
-            turn_pair_patch(xl1, xh1, e1, __uint_as_float(pa[e + 1]), __uint_as_float(pb[e + 1]), yl1, yh1);
+            turn2_patch(xl, xh, head, tail, make_float2(__uint_as_float(pa[e]), __uint_as_float(pa[e + 1])),
+                        make_float2(__uint_as_float(pb[e]), __uint_as_float(pb[e + 1])), yl, yh);
           } else {
-            turn_pair(xl0, xh0, e0, yl0, yh0);
-            turn_pair(xl1, xh1, e1, yl1, yh1);
+            turn2(xl, xh, head, tail, yl, yh);
           }
         } else {
-          yl0 = xl0 + __uint_as_float(pa[e]);
-          yl1 = xl1 + __uint_as_float(pa[e + 1]);
-          yh0 = xh0 + __uint_as_float(pb[e]);
-          yh1 = xh1 + __uint_as_float(pb[e + 1]);
+          yl = __fadd2_rn(xl, make_float2(__uint_as_float(pa[e]), __uint_as_float(pa[e + 1])));
+          yh = __fadd2_rn(xh, make_float2(__uint_as_float(pb[e]), __uint_as_float(pb[e + 1])));
         }
-        oa[w] = pack_bf2(yl0, yl1);
-        ob[w] = pack_bf2(yh0, yh1);
+        oa[w] = pack_bf2(yl.x, yl.y);
+        ob[w] = pack_bf2(yh.x, yh.y);
       }
       sts128(addr_a, make_uint4(oa[0], oa[1], oa[2], oa[3]));
       sts128(addr_b, make_uint4(ob[0], ob[1], ob[2], ob[3]));
@@ -387,6 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = h.tmem_cols > 0 ? *tmem_slot : 0u;
+  // Programmatic dependent launch: the set-up above may overlap the previous
+  // kernel on this stream; nothing global is touched before it has finished.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const uint32_t u_buf0 = sbase + L.u_off;
   auto u_buf = [&](int b) { return u_buf0 + (uint32_t)b * L.u_bytes; };
@@ -673,8 +681,21 @@ cudaError_t launch_relocate(const void* param_plan, const void* dev_plan, int gr
                             cudaStream_t stream) {
   ParamPlan pp;
   if (param_plan) {
+    // Single-chunk plans travel in the parameter block; such a launch may start
+    // its set-up while the previous kernel on the stream drains.
     memcpy(pp.bytes, param_plan, kParamPlanBytes);
-    dev::relocate_kernel<true><<<grid, kThreads, smem_bytes, stream>>>(pp, nullptr);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const unsigned char* none = nullptr;
+    return cudaLaunchKernelEx(&cfg, dev::relocate_kernel<true>, pp, none);
   } else {
     dev::relocate_kernel<false><<<grid, kThreads, smem_bytes, stream>>>(
         pp, static_cast<const unsigned char*>(dev_plan));
