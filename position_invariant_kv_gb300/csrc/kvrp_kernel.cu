@@ -163,10 +163,13 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "r"(addr));
   return v;
 }
+// No "memory" clobber: the shared-memory loads and stores of the epilogue are
+// volatile asm, so they keep their order among themselves, while ordinary
+// loads (the phase table) may be scheduled across them.  The proxy fence that
+// precedes every TMA store carries the clobber.
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
+               "r"(v.w));
 }
 __device__ __forceinline__ void stg128(void* p, uint4 v) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
