@@ -209,6 +209,23 @@ def run_cpu_baseline(cfg: int, budget_s: float) -> dict:
 # --------------------------------------------------------------------------- #
 # our arm
 # --------------------------------------------------------------------------- #
+def max_over_ranks(value: float, device) -> float:
+    """The largest of each rank's value (the slowest rank's time); identity on one rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, total_ms: float, steps: int) -> float:
+    """Whole-job tokens/s: every rank moves its own replica each step, and the
+    job's step time is the slowest rank's."""
+    return tokens_per_rank * world / (total_ms / 1e3 / steps)
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -271,12 +288,9 @@ def bench_ours(args) -> dict:
     mean_launch_ms = sum(launch_ms) / len(launch_ms)
     status = dwl.status_value()
 
-    ms_t = torch.tensor([total_ms], device=f"cuda:{local}")
-    if world > 1:
-        torch.distributed.all_reduce(ms_t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(ms_t.item())
+    total_ms = max_over_ranks(total_ms, f"cuda:{local}")
     ms_per_step = total_ms / args.steps
-    value = tokens * world / (total_ms / 1e3 / args.steps)
+    value = job_throughput(tokens, world, total_ms, args.steps)
 
     # end to end through the C ABI with host buffers: copy the step's inputs in
     # from pinned memory, run, copy the destination pools out, every step
