@@ -348,8 +348,9 @@ struct Bars {
   __device__ uint32_t u_full(int b) const { return base + 8u * (2 * kMaxStages + 2 * kAccSlots + b); }
   __device__ uint32_t u_empty(int b) const { return base + 8u * (2 * kMaxStages + 2 * kAccSlots + 2 + b); }
   __device__ uint32_t drain() const { return base + 8u * (2 * kMaxStages + 2 * kAccSlots + 4); }
+  __device__ uint32_t computed(int s) const { return base + 8u * (2 * kMaxStages + 2 * kAccSlots + 5 + s); }
 };
-static_assert(8 * (2 * kMaxStages + 2 * kAccSlots + 5) <= 512, "barriers must fit below the TMEM slot");
+static_assert(8 * (3 * kMaxStages + 2 * kAccSlots + 5) <= 512, "barriers must fit below the TMEM slot");
 
 template <bool kParamPlan>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -374,8 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(bars.full(s), 1);
-      // released by the owning group's warps and, when there is an MMA issuer, by it
-      mbar_init(bars.empty(s), kGroupWarps + (h.tmem_cols > 0 ? 1 : 0));
+      // released by the owning group's store warp and, when there is an MMA issuer, by it
+      mbar_init(bars.empty(s), 1 + (h.tmem_cols > 0 ? 1 : 0));
+      mbar_init(bars.computed(s), kGroupWarps);   // the group's rows are final in shared memory
     }
     for (int a = 0; a < kAccSlots; ++a) {
       mbar_init(bars.acc_full(a), 1);
@@ -510,6 +512,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         wait_phase(bars.drain(), 0, &no_abort, nullptr);
       }
     }
+  } else if (warp >= 2 + kEpilogueWarps) {
+    // ------------------------------------------------------------ page stores
+    // One warp per epilogue group.  When the group's rows of a stage are final
+    // it stores every whole 16-row page of the tile by TMA (lane p: page p),
+    // waits until those stores have read shared memory, and releases the stage.
+    const int group = warp - 2 - kEpilogueWarps;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
+      const Item I = decode_item(plan, h, item);
+      const TensorRec& T = *I.t;
+      const CUtensorMap* md = plan_map(plan, h, T.map_dst);
+      const int r_lo = max(0, -I.t0);
+      const int r_hi = min(kTileRows, I.c->n_tokens - I.t0);
+      const int p = lane;                                   // page of the tile this lane stores
+      const bool whole = p < kTileRows / kPage && kPage * p >= r_lo && kPage * p + kPage <= r_hi;
+      int64_t page = -1;
+      if (whole) {
+        const int64_t lp = (I.q0 + kPage * p) / kPage;
+        page = T.block_table ? (int64_t)__ldg(T.block_table + lp) : lp;
+      }
+      for (int s = I.s0; s < I.s1; ++s, ++it) {
+        if ((int)(it % kEpiGroups) != group) continue;   // another group's sub-tile
+        const int st = (int)(it % (uint32_t)S);
+        ok = wait_phase(bars.computed(st), (it / S) & 1, abort_flag, h.status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        if (whole) {
+          if (page < 0 || page >= T.num_pages) {
+            if (h.status) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
+          } else {
+            const int width = min(kSubCols, h.D - kSubCols * s);
+            const uint32_t xb = x_buf(st);
+            for (int j = 0; j < width / kBoxCols; ++j)
+              tma_store_3d(md, xb + (uint32_t)j * (kTileRows * kBoxCols * 2) + (uint32_t)p * (kPage * 128u),
+                           kSubCols * s + kBoxCols * j, (int)(page * kPage), I.layer);
+            bulk_commit();
+            bulk_wait_read_0();
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.empty(st));
+      }
+    }
+    bulk_wait_0();   // this warp's page stores are complete before the CTA exits
   } else {
     // --------------------------------------------------------------- epilogue
     // Two groups of four warps take sub-tiles in turn (group g owns the stages
@@ -521,7 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int group = ew / kGroupWarps;      // which sub-tiles this warp serves
     const int quarter = warp & 3;            // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;     // tile row (token) of this thread
-    const bool leader = (lane & (kPage - 1)) == 0;
     uint32_t it = 0;
     uint32_t gait = 0;                       // patched sub-tiles this group has taken
     const uint32_t tslot = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)group * kSubCols;
@@ -589,20 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
 
-        // ---- stores: whole pages by TMA (issued by the page's first row),
-        //      rows of partly covered pages by their own threads
-        if (valid) {
-          const bool page_ok = page >= 0 && page < T.num_pages;
-          if (!page_ok) {
-            if (h.status && (leader || !whole_page)) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
-          } else if (whole_page) {
-            if (leader) {
-              for (int j = 0; j < width / kBoxCols; ++j)
-                tma_store_3d(md, xb + (uint32_t)j * (kTileRows * kBoxCols * 2) + (uint32_t)pg_row * 128u,
-                             kSubCols * s + kBoxCols * j, (int)(page * kPage), I.layer);
-              bulk_commit();
-              bulk_wait_read_0();
-            }
+        // ---- rows of partly covered pages go out now, by their own threads;
+        //      whole pages are left to the group's store warp
+        if (valid && !whole_page) {
+          if (page < 0 || page >= T.num_pages) {
+            if (h.status) atomicOr(h.status, KVRP_DEV_BAD_PAGE);
           } else {
             uint16_t* dst_row = T.dst + (int64_t)I.layer * T.dst_layer_stride +
                                 (page * kPage + (I.q0 + row) % kPage) * (int64_t)h.D + kSubCols * s;
@@ -610,10 +647,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.empty(st));
+        if (lane == 0) mbar_arrive(bars.computed(st));
       }
     }
-    bulk_wait_0();   // this thread's page stores are complete before the CTA exits
   }
 
   tc_fence_before();

@@ -28,7 +28,8 @@ constexpr int kEpilogueWarps = kGroupWarps * kEpiGroups;
 // stage use (its arrival is part of the stage's release).
 constexpr int kAccSlots = kEpiGroups;
 constexpr int kMaxStages = 8;       // shared-memory pipeline depth bound
-constexpr int kThreads = 64 + 32 * kEpilogueWarps;   // producer, MMA, epilogue warps
+// warps: producer, MMA issuer, epilogue groups, then one page-store warp per group
+constexpr int kThreads = 64 + 32 * kEpilogueWarps + 32 * kEpiGroups;
 
 // Rotation kinds of one tensor.
 enum RotKind : int32_t {

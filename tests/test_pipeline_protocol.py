@@ -1,8 +1,9 @@
 """A randomised model of the relocation kernel's mbarrier protocol.
 
 The kernel's roles (one TMA producer, one MMA issuer, two epilogue groups of
-four warps) hand shared-memory stages, TMEM accumulator slots and U buffers to
-each other through mbarriers whose waits test only the parity of a phase.
+four warps, one page-store warp per group) hand shared-memory stages, TMEM
+accumulator slots and U buffers to each other through mbarriers whose waits
+test only the parity of a phase.
 Such a wait is correct only if the waiter never falls two phases behind the
 barrier.  The kernel keeps that invariant by construction: stage s belongs to
 epilogue group s % 2, each group owns one accumulator slot, and the MMA issuer
@@ -52,7 +53,9 @@ def simulate(seed, items, S, groups=2, n_u=2, old_protocol=False):
     tmem = any(m for m, _ in items)
     slots = 4 if old_protocol else groups
     full = [Bar(1) for _ in range(S)]
-    empty = [Bar(4 + (1 if (tmem and not old_protocol) else 0)) for _ in range(S)]
+    # released by the group's store warp (old protocol: by the four epilogue warps) and the MMA issuer
+    empty = [Bar((4 if old_protocol else 1) + (1 if (tmem and not old_protocol) else 0)) for _ in range(S)]
+    computed = [Bar(4) for _ in range(S)]
     acc_full, acc_empty = [Bar(1) for _ in range(slots)], [Bar(4) for _ in range(slots)]
     u_full, u_empty = [Bar(1) for _ in range(n_u)], [Bar(1) for _ in range(n_u)]
     events, clock = [], [0]
@@ -134,11 +137,29 @@ def simulate(seed, items, S, groups=2, n_u=2, old_protocol=False):
                     gait += 1
                 for _ in range(rnd.randint(0, 5)):
                     yield
+                (empty if old_protocol else computed)[st].arrive()
+                it += 1
+                yield
+
+    def store_warp(g):
+        it = 0
+        for m, nsub in items:
+            for _ in range(nsub):
+                if it % groups != g:
+                    it += 1
+                    continue
+                st = it % S
+                while not computed[st].try_wait(it // S):
+                    yield
+                for _ in range(rnd.randint(0, 5)):
+                    yield
                 empty[st].arrive()
                 it += 1
                 yield
 
     roles = [producer()] + ([mma()] if tmem else []) + [epilogue_warp(g) for g in range(groups) for _ in range(4)]
+    if not old_protocol:
+        roles += [store_warp(g) for g in range(groups)]
     live, steps = list(roles), 0
     while live or events:
         steps += 1
