@@ -51,6 +51,7 @@ class DeviceWorkload:
             nbytes = kvrp.kv_relocate_batch_workspace_size(len(wl.chunks))
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         self._chunks = self._chunk_args()
+        self._batch_array = None
 
     def reset_pools(self):
         for p in self.pools.values():
@@ -109,14 +110,11 @@ class DeviceWorkload:
                 u_layer_stride=a["u_layer_stride"], v_layer_stride=a["w_layer_stride"],
                 d_status=self.status, stream=stream)
         else:
-            chunks = [kvrp.Chunk(k_src=a["srcs"][0], v_src=a["srcs"][1], n_tokens=a["n_tokens"],
-                                 delta=a["delta"], k_dst=a["dst"][0], v_dst=a["dst"][1], rank=a["rank"],
-                                 uk=a["u"][0], vk=a["w"][0], uv=a["u"][1], vv=a["w"][1],
-                                 src_layer_stride=a["src_layer_stride"], u_layer_stride=a["u_layer_stride"],
-                                 v_layer_stride=a["w_layer_stride"]) for a in self._chunks]
-            kvrp.kv_relocate_batch(chunks, n_layers=wl.n_layers, n_kv_heads=wl.n_heads, head_dim=wl.head_dim,
-                                   rope_theta=wl.theta, workspace=self.workspace, d_status=self.status,
-                                   stream=stream)
+            if self._batch_array is None:            # the chunks do not change: marshal them once
+                self._batch_array = kvrp.chunk_array(self.batch_chunks())
+            kvrp.kv_relocate_batch(self._batch_array, n_layers=wl.n_layers, n_kv_heads=wl.n_heads,
+                                   head_dim=wl.head_dim, rope_theta=wl.theta, workspace=self.workspace,
+                                   d_status=self.status, stream=stream)
 
     def batch_chunks(self) -> list:
         """The workload's chunks as kv_relocate_batch descriptors."""

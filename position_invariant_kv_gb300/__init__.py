@@ -21,5 +21,5 @@ from ._abi import (  # noqa: F401
     Dst, Chunk, KvrpError, lib, lib_path,
     kv_relocate_patch, kv_relocate_patch_mla, kv_relocate_batch, kv_relocate_batch_workspace_size,
     kvrp_status_string, kvrp_version, EXPORTED_SYMBOLS,
-    kv_relocate_batch_noalloc, KVRP_NOALLOC_MAX_CHUNKS,
+    kv_relocate_batch_noalloc, KVRP_NOALLOC_MAX_CHUNKS, chunk_array,
 )

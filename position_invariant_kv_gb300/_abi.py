@@ -195,24 +195,37 @@ def kv_relocate_batch_workspace_size(n_chunks: int) -> int:
     return int(lib().kv_relocate_batch_workspace_size(int(n_chunks)))
 
 
-def kv_relocate_batch(chunks: Sequence[Chunk], *, n_layers: int, n_kv_heads: int, head_dim: int,
+def chunk_array(chunks: Sequence[Chunk]):
+    """The ctypes array of struct kvrp_chunk for a list of chunks.  Build it once
+    and pass it to the batch calls when the same chunks are relocated again."""
+    return (kvrp_chunk * max(1, len(chunks)))(*[c.c() for c in chunks])
+
+
+def _as_array(chunks):
+    if isinstance(chunks, C.Array):
+        return chunks, len(chunks)
+    return chunk_array(chunks), len(chunks)
+
+
+def kv_relocate_batch(chunks, *, n_layers: int, n_kv_heads: int, head_dim: int,
                       rope_theta: float, workspace, workspace_bytes: Optional[int] = None,
                       d_status=None, stream=None) -> None:
-    arr = (kvrp_chunk * max(1, len(chunks)))(*[c.c() for c in chunks])
+    """chunks: a list of Chunk, or an array made by chunk_array()."""
+    arr, n = _as_array(chunks)
     if workspace_bytes is None:
         workspace_bytes = int(workspace.numel() * workspace.element_size())
     _check(lib().kv_relocate_batch(
-        arr, len(chunks), int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
+        arr, n, int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
         _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))
 
 
-def kv_relocate_batch_noalloc(chunks: Sequence[Chunk], *, n_layers: int, n_kv_heads: int, head_dim: int,
+def kv_relocate_batch_noalloc(chunks, *, n_layers: int, n_kv_heads: int, head_dim: int,
                               rope_theta: float, d_status=None, stream=None) -> None:
     """kv_relocate_batch without a workspace, for callers that cannot allocate
     device memory: the launch descriptors go to a fixed array inside the
     library (at most KVRP_NOALLOC_MAX_CHUNKS chunks; calls that can overlap on
     the GPU must not be issued, as they share that array)."""
-    arr = (kvrp_chunk * max(1, len(chunks)))(*[c.c() for c in chunks])
+    arr, n = _as_array(chunks)
     _check(lib().kv_relocate_batch_noalloc(
-        arr, len(chunks), int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
+        arr, n, int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
         _ptr(d_status), _stream(stream)))

@@ -17,6 +17,7 @@
 #include <map>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "kvrp.h"
@@ -212,6 +213,46 @@ struct MapKey {
   bool operator<(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) < 0; }
 };
 
+// Process-wide caches of encoded tensor maps and phase tables.  A serving
+// loop relocates into the same pools from the same canonical stores again and
+// again; encoding a map costs about a microsecond, and a batch needs hundreds.
+// The key holds every encoding parameter, so a hit is always the descriptor
+// the driver would produce.  Both caches are bounded and simply start over
+// when full.
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+struct MapKeyEq {
+  bool operator()(const MapKey& a, const MapKey& b) const { return std::memcmp(&a, &b, sizeof(MapKey)) == 0; }
+};
+struct TableKey {
+  int64_t delta;
+  double theta;
+  int64_t rot_dim;
+  bool operator==(const TableKey& o) const {
+    return delta == o.delta && std::memcmp(&theta, &o.theta, sizeof(double)) == 0 && rot_dim == o.rot_dim;
+  }
+};
+struct TableKeyHash {
+  size_t operator()(const TableKey& k) const {
+    uint64_t t;
+    std::memcpy(&t, &k.theta, sizeof(t));
+    return static_cast<size_t>((uint64_t)k.delta * 0x9E3779B97F4A7C15ull ^ t ^ ((uint64_t)k.rot_dim << 40));
+  }
+};
+struct CachedTable {
+  float4 v[kTablePairs];
+};
+constexpr size_t kCacheMaxEntries = 16384;
+std::mutex g_cache_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash, MapKeyEq> g_map_cache;
+std::unordered_map<TableKey, CachedTable, TableKeyHash> g_table_cache;
+
 class PlanBuilder {
  public:
   explicit PlanBuilder(const Shape& sh) : sh_(sh) {}
@@ -231,13 +272,27 @@ class PlanBuilder {
       return KVRP_OK;
     }
     CUtensorMap m;
-    const cuuint32_t estr[3] = {1, 1, 1};
-    const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), k.dims,
-                                k.strides, k.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS)
-      return fail(KVRP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for dims %llu x %llu x %llu",
-                  (int)r, (unsigned long long)d0, (unsigned long long)d1, (unsigned long long)d2);
+    bool cached = false;
+    {
+      std::lock_guard<std::mutex> lk(g_cache_mu);
+      auto hit = g_map_cache.find(k);
+      if (hit != g_map_cache.end()) {
+        m = hit->second;
+        cached = true;
+      }
+    }
+    if (!cached) {
+      const cuuint32_t estr[3] = {1, 1, 1};
+      const CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), k.dims,
+                                  k.strides, k.box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS)
+        return fail(KVRP_ERR_INVALID_ARG, "cuTensorMapEncodeTiled failed (%d) for dims %llu x %llu x %llu",
+                    (int)r, (unsigned long long)d0, (unsigned long long)d1, (unsigned long long)d2);
+      std::lock_guard<std::mutex> lk(g_cache_mu);
+      if (g_map_cache.size() >= kCacheMaxEntries) g_map_cache.clear();
+      g_map_cache.emplace(k, m);
+    }
     *idx = static_cast<int32_t>(maps_.size());
     maps_.push_back(m);
     map_index_[k] = *idx;
@@ -249,7 +304,24 @@ class PlanBuilder {
     if (f != tab_index_.end()) return f->second;
     const int32_t idx = static_cast<int32_t>(tabs_.size() / kTablePairs);
     tabs_.resize(tabs_.size() + kTablePairs);
-    phase_table(delta, sh_.theta, sh_.rot_dim, &tabs_[idx * kTablePairs]);
+    const TableKey key{delta, sh_.theta, sh_.rot_dim};
+    bool cached = false;
+    {
+      std::lock_guard<std::mutex> lk(g_cache_mu);
+      auto hit = g_table_cache.find(key);
+      if (hit != g_table_cache.end()) {
+        std::memcpy(&tabs_[idx * kTablePairs], hit->second.v, sizeof(CachedTable));
+        cached = true;
+      }
+    }
+    if (!cached) {
+      phase_table(delta, sh_.theta, sh_.rot_dim, &tabs_[idx * kTablePairs]);
+      CachedTable t;
+      std::memcpy(t.v, &tabs_[idx * kTablePairs], sizeof(CachedTable));
+      std::lock_guard<std::mutex> lk(g_cache_mu);
+      if (g_table_cache.size() >= kCacheMaxEntries) g_table_cache.clear();
+      g_table_cache.emplace(key, t);
+    }
     tab_index_[delta] = idx;
     return idx;
   }
