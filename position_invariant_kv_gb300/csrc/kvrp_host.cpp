@@ -350,7 +350,6 @@ class PlanBuilder {
       any_rot |= ti.rot_kind != kRotNone;
       const int lead = static_cast<int>(ti.dst.dst_start % kPage);
       tr.n_tblk = c.n_tokens > 0 ? (lead + c.n_tokens + kTileRows - 1) / kTileRows : 0;
-      tr.item_count = 0;  // filled by finish()
       if (c.n_tokens == 0) continue;
       const uint64_t sls = c.src_layer_stride ? c.src_layer_stride : T * sh_.D;
       kvrp_status st = map(ti.src, sh_.D, T, L, sh_.D, sls, kBoxCols, kTileRows,
@@ -396,18 +395,24 @@ class PlanBuilder {
     while (spi > 1 && tiles * ((h.n_sub + spi - 1) / spi) < 2ll * sms) spi = (spi + 1) / 2;
     h.subs_per_item = spi;
     h.n_sg = (h.n_sub + spi - 1) / spi;
-    std::vector<int32_t> ibeg;
+    // tile prefix sums per tensor; items enumerate (tensor, layer, tile, group)
+    h.n_tensors = chunks_.empty() ? 0 : chunks_[0].n_tensors;
+    std::vector<int32_t> tbeg;
     int64_t items = 0;
-    for (ChunkRec& r : chunks_) {
-      ibeg.push_back(static_cast<int32_t>(items));
-      for (int t = 0; t < r.n_tensors; ++t) {
-        const int64_t n = (int64_t)r.t[t].n_tblk * sh_.n_layers * h.n_sg;
-        r.t[t].item_count = static_cast<int32_t>(n);
-        items += n;
+    for (int t = 0; t < h.n_tensors; ++t) {
+      int64_t tiles_t = 0;
+      for (const ChunkRec& r : chunks_) {
+        tbeg.push_back(static_cast<int32_t>(tiles_t));
+        tiles_t += r.t[t].n_tblk;
       }
+      tbeg.push_back(static_cast<int32_t>(tiles_t));
+      if (tiles_t > (1ll << 30)) return fail(KVRP_ERR_INVALID_ARG, "too many tiles in one launch");
+      h.tiles[t] = static_cast<int32_t>(tiles_t);
+      const int64_t n = tiles_t * sh_.n_layers * h.n_sg;
+      if (t == 0) h.items0 = static_cast<int32_t>(std::min<int64_t>(n, INT32_MAX));
+      items += n;
     }
     if (items > (1ll << 31) - 1) return fail(KVRP_ERR_INVALID_ARG, "too many tiles in one launch");
-    ibeg.push_back(static_cast<int32_t>(items));
     h.n_items = static_cast<int32_t>(items);
     // pipeline depth from the shared-memory budget (and TMEM: 128 columns a stage)
     const int budget = smem_optin - 1024;
@@ -437,15 +442,15 @@ class PlanBuilder {
     off = align(off + tabs_.size() * sizeof(float4));
     h.off_chunks = static_cast<uint32_t>(off);
     off = align(off + chunks_.size() * sizeof(ChunkRec));
-    h.off_ibeg = static_cast<uint32_t>(off);
-    off = align(off + ibeg.size() * sizeof(int32_t));
+    h.off_tbeg = static_cast<uint32_t>(off);
+    off = align(off + tbeg.size() * sizeof(int32_t));
     h.total_bytes = static_cast<uint32_t>(off);
     out->assign(off, 0);
     std::memcpy(out->data(), &h, sizeof(h));
     if (!maps_.empty()) std::memcpy(out->data() + h.off_maps, maps_.data(), maps_.size() * sizeof(CUtensorMap));
     if (!tabs_.empty()) std::memcpy(out->data() + h.off_tabs, tabs_.data(), tabs_.size() * sizeof(float4));
     std::memcpy(out->data() + h.off_chunks, chunks_.data(), chunks_.size() * sizeof(ChunkRec));
-    std::memcpy(out->data() + h.off_ibeg, ibeg.data(), ibeg.size() * sizeof(int32_t));
+    if (!tbeg.empty()) std::memcpy(out->data() + h.off_tbeg, tbeg.data(), tbeg.size() * sizeof(int32_t));
     *grid = static_cast<int>(std::min<int64_t>(items, sms));
     *smem_bytes = static_cast<int>(smem_layout(m_max_, stages, u_bufs).total) + 1024;
     return KVRP_OK;
@@ -458,7 +463,7 @@ class PlanBuilder {
     off = align(off + (size_t)n * 8 * sizeof(CUtensorMap));
     off = align(off + (size_t)n * kTablePairs * sizeof(float4));
     off = align(off + (size_t)n * sizeof(ChunkRec));
-    off = align(off + (size_t)(n + 1) * sizeof(int32_t));
+    off = align(off + (size_t)2 * (n + 1) * sizeof(int32_t));
     return off;
   }
 

@@ -205,25 +205,24 @@ struct Item {
 };
 
 __device__ __forceinline__ Item decode_item(const unsigned char* plan, const PlanHdr& h, int item) {
-  const int32_t* ibeg = reinterpret_cast<const int32_t*>(plan + h.off_ibeg);
+  Item it;
+  it.tensor = item >= h.items0 ? 1 : 0;
+  const int local = item - (it.tensor ? h.items0 : 0);
+  const int sg = local % h.n_sg;
+  const int rest = local / h.n_sg;
+  const int tiles = it.tensor ? h.tiles[1] : h.tiles[0];   // a select keeps the header in registers
+  const int tile = rest % tiles;
+  it.layer = rest / tiles;
+  // the chunk holding this tile: last prefix-sum entry <= tile
+  const int32_t* tbeg = reinterpret_cast<const int32_t*>(plan + h.off_tbeg) + it.tensor * (h.n_chunks + 1);
   int lo = 0, hi = h.n_chunks - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (ibeg[mid] <= item) lo = mid; else hi = mid - 1;
+    if (tbeg[mid] <= tile) lo = mid; else hi = mid - 1;
   }
-  Item it;
   it.c = reinterpret_cast<const ChunkRec*>(plan + h.off_chunks) + lo;
-  int local = item - ibeg[lo];
-  it.tensor = 0;
-  if (local >= it.c->t[0].item_count) {
-    it.tensor = 1;
-    local -= it.c->t[0].item_count;
-  }
   it.t = &it.c->t[it.tensor];
-  const int sg = local % h.n_sg;
-  const int rest = local / h.n_sg;
-  it.tblk = rest % it.t->n_tblk;
-  it.layer = rest / it.t->n_tblk;
+  it.tblk = tile - tbeg[lo];
   it.s0 = sg * h.subs_per_item;
   it.s1 = min(it.s0 + h.subs_per_item, h.n_sub);
   const int lead = (int)(it.t->dst_start % kPage);

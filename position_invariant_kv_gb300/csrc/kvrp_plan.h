@@ -1,6 +1,6 @@
 // Launch plan shared by the host side (kvrp_host.cpp) and the kernel
 // (kvrp_kernel.cu).  A plan is one byte blob: a header, the TMA tensor maps,
-// the per-chunk phase tables, the chunk records and the item prefix sums.
+// the per-chunk phase tables, the chunk records and per-tensor tile prefix sums.
 // Small plans (one chunk) travel as a __grid_constant__ kernel parameter;
 // batch plans are copied into a caller-provided device workspace.
 #pragma once
@@ -52,8 +52,7 @@ struct TensorRec {             // one (chunk, tensor)
   int32_t rot_kind;
   int32_t rot_from;                       // first rotated feature (kRotHalf64)
   int32_t n_tblk;                         // token tiles of this tensor
-  int32_t item_count;                     // items of this tensor (all layers)
-  int32_t pad_;
+  int32_t pad_[2];
 };
 
 struct ChunkRec {
@@ -76,7 +75,12 @@ struct PlanHdr {
   int32_t m_max;                          // largest rank in the plan (multiple of 16)
   int32_t tmem_cols;                      // allocated TMEM columns (0 = none)
   int32_t u_bufs;                         // U tile buffers (2, or 1 at the largest ranks)
-  uint32_t off_maps, off_tabs, off_chunks, off_ibeg;
+  int32_t n_tensors;                      // tensors per chunk (GQA/MHA: K and V; MLA: 1)
+  int32_t tiles[2];                       // token tiles over all chunks, per tensor
+  int32_t items0;                         // items of tensor 0 (all layers)
+  // Items run tensor-major, then layer, then chunk, then tile, then sub-tile
+  // group: CTAs working side by side stream neighbouring chunks of one layer.
+  uint32_t off_maps, off_tabs, off_chunks, off_tbeg;   // off_tbeg: int32 [n_tensors][n_chunks + 1] tile prefix sums
   uint32_t total_bytes;
   uint32_t* status;                       // optional device status word
 };
