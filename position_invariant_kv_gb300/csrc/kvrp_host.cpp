@@ -416,19 +416,30 @@ class PlanBuilder {
     h.n_items = static_cast<int32_t>(items);
     // pipeline depth from the shared-memory budget (and TMEM: 128 columns a stage)
     const int budget = smem_optin - 1024;
-    int stages = 0, u_bufs = 0;
-    for (int ub = 2; ub >= 1 && stages == 0; --ub) {
-      for (int s = kMaxStages - kMaxStages % kEpiGroups; s >= kEpiGroups; s -= kEpiGroups) {
-        if ((int)smem_layout(m_max_, s, ub).total <= budget) {
-          stages = s;
-          u_bufs = ub;
-          break;
+    const int n_tables = static_cast<int>(tabs_.size() / kTablePairs);
+    // Preference order: deeper pipeline, double-buffered U, then tables in
+    // shared memory (one fixed copy, or one per stage), else global tables.
+    int stages = 0, u_bufs = 0, tab_mode = kTabGlobal;
+    const int modes_multi[2] = {kTabStaged, kTabGlobal};
+    const int modes_single[1] = {kTabFixed};
+    const int* modes = n_tables <= 1 ? modes_single : modes_multi;
+    const int n_modes = n_tables <= 1 ? 1 : 2;
+    for (int s = kMaxStages - kMaxStages % kEpiGroups; s >= kEpiGroups && stages == 0; s -= kEpiGroups) {
+      for (int ub = 2; ub >= 1 && stages == 0; --ub) {
+        for (int mi = 0; mi < n_modes && stages == 0; ++mi) {
+          if ((int)smem_layout(m_max_, s, ub, modes[mi]).total <= budget) {
+            stages = s;
+            u_bufs = ub;
+            tab_mode = modes[mi];
+          }
         }
       }
     }
     if (stages == 0) return fail(KVRP_ERR_UNSUPPORTED, "rank %d does not fit in shared memory", m_max_);
     h.stages = stages;
     h.u_bufs = u_bufs;
+    h.n_tables = n_tables;
+    h.tab_mode = tab_mode;
     h.tmem_cols = 0;
     if (m_max_ > 0) {
       h.tmem_cols = 32;
@@ -452,7 +463,7 @@ class PlanBuilder {
     std::memcpy(out->data() + h.off_chunks, chunks_.data(), chunks_.size() * sizeof(ChunkRec));
     if (!tbeg.empty()) std::memcpy(out->data() + h.off_tbeg, tbeg.data(), tbeg.size() * sizeof(int32_t));
     *grid = static_cast<int>(std::min<int64_t>(items, sms));
-    *smem_bytes = static_cast<int>(smem_layout(m_max_, stages, u_bufs).total) + 1024;
+    *smem_bytes = static_cast<int>(smem_layout(m_max_, stages, u_bufs, tab_mode).total) + 1024;
     return KVRP_OK;
   }
 

@@ -98,6 +98,14 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int 
                ::"l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(src)
                : "memory");
 }
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_1() {
   asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
@@ -288,8 +296,7 @@ __device__ __forceinline__ void turn2_patch(float2 xl, float2 xh, float4 head, f
 // of part b and uses table entry tab0 + j.  Accumulators are read in rounds of
 // 16 columns per part to keep register use low.
 template <int N, bool ROT, bool PATCH>
-__device__ __forceinline__ void epilogue_part(uint32_t xbase, int row, int a0, int a1,
-                                              const float4* __restrict__ tab, int tab0,
+__device__ __forceinline__ void epilogue_part(uint32_t xbase, int row, int a0, int a1, const float4* tab, int tab0,
                                               uint32_t tm_a, uint32_t tm_b) {
 #pragma unroll
   for (int r0 = 0; r0 < N; r0 += 16) {
@@ -311,7 +318,9 @@ __device__ __forceinline__ void epilogue_part(uint32_t xbase, int row, int a0, i
         const float2 xh = make_float2(bf_lo(wb[w]), bf_hi(wb[w]));
         float2 yl, yh;
         if constexpr (ROT) {
-          const float4 head = tab[tab0 + r0 + e];       // table entries are stored two pairs at a time
+          // table entries are stored two pairs at a time; all lanes read the same
+          // entry (a broadcast), from shared or global memory through one pointer
+          const float4 head = tab[tab0 + r0 + e];
           const float4 tail = tab[tab0 + r0 + e + 1];
           if constexpr (PATCH) {
             turn2_patch(xl, xh, head, tail, make_float2(__uint_as_float(pa[e]), __uint_as_float(pa[e + 1])),
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const SmemLayout L = smem_layout(h.m_max, h.stages, h.u_bufs);
+  const SmemLayout L = smem_layout(h.m_max, h.stages, h.u_bufs, h.tab_mode);
   const uint32_t NU = (uint32_t)h.u_bufs;
   const uint32_t sbase = smem_u32(smem);
   const Bars bars{sbase};
@@ -391,6 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1 && h.tmem_cols > 0) tmem_alloc(smem_u32(tmem_slot), (uint32_t)h.tmem_cols);
+  if (h.tab_mode == kTabFixed && h.n_tables == 1 && threadIdx.x < kTablePairs) {
+    // a plan with one phase table keeps it in shared memory for the whole launch
+    const float4 v = reinterpret_cast<const float4*>(plan + h.off_tabs)[threadIdx.x];
+    reinterpret_cast<float4*>(smem + L.tab_off)[threadIdx.x] = v;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -404,6 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto u_buf = [&](int b) { return u_buf0 + (uint32_t)b * L.u_bytes; };
   auto x_buf = [&](int s) { return sbase + L.stage_off + (uint32_t)s * L.stage_bytes; };
   auto w_buf = [&](int s) { return x_buf(s) + L.x_bytes; };
+  // shared-memory table slot of a stage (kTabStaged), or the fixed copy (kTabFixed)
+  auto tab_buf = [&](int s) { return sbase + L.tab_off + (h.tab_mode == kTabStaged ? (uint32_t)s * kTableBytes : 0u); };
+  const float4* tab_smem = reinterpret_cast<const float4*>(smem + L.tab_off);
+  const float4* tab_glob = reinterpret_cast<const float4*>(plan + h.off_tabs);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -414,6 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item I = decode_item(plan, h, item);
         const int m = I.c->rank;
         const int nkb = m >> 4;
+        if (h.tab_mode == kTabGlobal && item + (int)gridDim.x < h.n_items) {
+          // warm L1 with the next item's phase table for the epilogue
+          const Item N = decode_item(plan, h, item + (int)gridDim.x);
+          if (N.c->table >= 0 && N.t->rot_kind != kRotNone) {
+            const unsigned char* tp = plan + h.off_tabs + (size_t)N.c->table * kTableBytes;
+            for (int l = 0; l < kTableBytes; l += 128) prefetch_l1(tp + l);
+          }
+        }
         if (m > 0) {
           const int ub = (int)(uit % NU);
           ok = wait_phase(bars.u_empty(ub), ((uit / NU) & 1) ^ 1, abort_flag, h.status);
@@ -435,7 +461,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nbox = width / kBoxCols;
           uint32_t bytes = (uint32_t)nbox * (kTileRows * kBoxCols * 2);
           if (m > 0) bytes += (uint32_t)nkb * (uint32_t)width * 32u;
+          const bool copy_tab = h.tab_mode == kTabStaged && I.t->rot_kind != kRotNone;
+          if (copy_tab) bytes += kTableBytes;
           mbar_expect_tx(bars.full(st), bytes);
+          if (copy_tab)
+            bulk_load(tab_buf(st), plan + h.off_tabs + (size_t)I.c->table * kTableBytes, kTableBytes,
+                      bars.full(st));
           for (int j = 0; j < nbox; ++j)
             tma_load_3d(x_buf(st) + (uint32_t)j * (kTileRows * kBoxCols * 2), mx, bars.full(st),
                         kSubCols * s + kBoxCols * j, I.t0, I.layer);
@@ -576,10 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m = I.c->rank;
       const TensorRec& T = *I.t;
       const int n_tok = I.c->n_tokens;
-      const float4* tab =
-          I.c->table >= 0 ? reinterpret_cast<const float4*>(plan + h.off_tabs) + I.c->table * kTablePairs
-                          : nullptr;
-      const CUtensorMap* md = plan_map(plan, h, T.map_dst);
       // valid tile rows [r_lo, r_hi); this thread's row and its destination page
       const int r_lo = max(0, -I.t0);
       const int r_hi = min(kTileRows, n_tok - I.t0);
@@ -606,6 +633,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int width = min(kSubCols, h.D - kSubCols * s);
         const uint32_t xb = x_buf(st);
+        const float4* tab = h.tab_mode == kTabGlobal
+                                ? (I.c->table >= 0 ? tab_glob + (size_t)I.c->table * kTablePairs : tab_glob)
+                                : tab_smem + (h.tab_mode == kTabStaged ? st * kTablePairs : 0);
         const uint32_t tcol = tslot;
         if (width == kSubCols && T.rot_kind == kRotHalf128) {
           // one head of 128: column j pairs with j + 64

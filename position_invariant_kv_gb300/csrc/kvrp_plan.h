@@ -75,6 +75,8 @@ struct PlanHdr {
   int32_t m_max;                          // largest rank in the plan (multiple of 16)
   int32_t tmem_cols;                      // allocated TMEM columns (0 = none)
   int32_t u_bufs;                         // U tile buffers (2, or 1 at the largest ranks)
+  int32_t n_tables;                       // distinct phase tables in the plan
+  int32_t tab_mode;                       // where the epilogue reads tables: kTab* below
   int32_t n_tensors;                      // tensors per chunk (GQA/MHA: K and V; MLA: 1)
   int32_t tiles[2];                       // token tiles over all chunks, per tensor
   int32_t items0;                         // items of tensor 0 (all layers)
@@ -87,14 +89,25 @@ struct PlanHdr {
 static_assert(sizeof(PlanHdr) <= 128, "header must fit in 128 bytes");
 
 // Shared-memory carve-up for a given rank bound and depth.
+constexpr int kTableBytes = kTablePairs * 16;   // one phase table: 64 float4
+
+// Where the epilogue reads phase tables from.
+enum TabMode : int32_t {
+  kTabFixed = 0,     // the plan's only table, copied to shared memory once per launch
+  kTabStaged = 1,    // one table per pipeline stage, copied with the stage's data
+  kTabGlobal = 2,    // read from the plan in global memory; the producer prefetches
+                     // the next item's table into L1 (when shared memory is full)
+};
+
 struct SmemLayout {
   uint32_t u_off, u_bytes;        // U buffers
   uint32_t stage_off, stage_bytes;
   uint32_t x_bytes, w_bytes;      // inside a stage: X sub-tile, then W slice
+  uint32_t tab_off;               // phase-table slots (see TabMode)
   uint32_t total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int m_max, int stages, int u_bufs) {
+__host__ __device__ inline SmemLayout smem_layout(int m_max, int stages, int u_bufs, int tab_mode) {
   SmemLayout s;
   const uint32_t kb = (uint32_t)(m_max / 16);
   s.u_off = 1024;                                  // barriers live in the first 1 KB
@@ -103,7 +116,9 @@ __host__ __device__ inline SmemLayout smem_layout(int m_max, int stages, int u_b
   s.w_bytes = kb * (kSubCols * 32);
   s.stage_bytes = s.x_bytes + s.w_bytes;
   s.stage_off = s.u_off + (uint32_t)u_bufs * s.u_bytes;
-  s.total = s.stage_off + (uint32_t)stages * s.stage_bytes;
+  s.tab_off = s.stage_off + (uint32_t)stages * s.stage_bytes;
+  const uint32_t n_tab = tab_mode == kTabFixed ? 1u : tab_mode == kTabStaged ? (uint32_t)stages : 0u;
+  s.total = s.tab_off + n_tab * kTableBytes;
   return s;
 }
 
