@@ -13,6 +13,10 @@ Readings of points the pages leave open (each is listed in the design doc):
     theta_i = theta_base ** (-2 i / d), i = 0 .. d/2 - 1, all in fp64.
   * delta is the new position minus the old one, one value per chunk, so
     R(delta) . RoPE(k, p) = RoPE(k, p + delta).
+  * M-RoPE (the multimodal RoPE of Qwen-VL-style models, whose image KV is
+    re-rotated by M-RoPE in the composable-KV summary, section 4): the
+    frequency pairs form consecutive temporal / height / width sections and
+    delta is a (d_t, d_h, d_w) tuple, pair i turning by its section's shift.
   * The patch is added after the rotation and is not itself rotated (the
     reuse equation read literally).
   * K and V each carry their own factor pair (U [T][m], W [D][m]); MLA carries
@@ -56,10 +60,33 @@ def rope_absolute(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     return _turn(x, phi)
 
 
-def relocate(x: np.ndarray, delta, theta: float) -> np.ndarray:
-    """R(delta) applied to rows whose last axis is one rotated head."""
+def pair_shifts(delta, n_pairs: int, sections=None) -> np.ndarray:
+    """Position shift seen by each frequency pair.  Plain RoPE: every pair
+    shifts by delta.  M-RoPE (multimodal RoPE of Qwen-VL-style models): the
+    frequency pairs are split into consecutive (temporal, height, width)
+    sections, and pair i shifts by the component of delta = (d_t, d_h, d_w)
+    that owns its section."""
+    if sections is None:
+        return np.full(n_pairs, np.float64(delta))
+    assert sum(sections) == n_pairs, "sections must cover every frequency pair"
+    return np.repeat(np.asarray(delta, dtype=np.float64), np.asarray(sections))
+
+
+def relocate(x: np.ndarray, delta, theta: float, sections=None) -> np.ndarray:
+    """R(delta) applied to rows whose last axis is one rotated head; with
+    M-RoPE sections, delta is the (t, h, w) shift tuple."""
     x = np.asarray(x, dtype=np.float64)
-    phi = np.float64(delta) * inv_freq(x.shape[-1], theta)
+    d = x.shape[-1]
+    phi = pair_shifts(delta, d // 2, sections) * inv_freq(d, theta)
+    return _turn(x, phi)
+
+
+def mrope_absolute(x: np.ndarray, pos_thw: np.ndarray, theta: float, sections) -> np.ndarray:
+    """M-RoPE of rows x [n][d] at 3-component positions pos_thw [n][3] (the
+    encoding a multimodal model applies at prefill).  Used only to pin R(delta)."""
+    x = np.asarray(x, dtype=np.float64)
+    pos = np.repeat(np.asarray(pos_thw, dtype=np.float64), np.asarray(sections), axis=1)
+    phi = pos * inv_freq(x.shape[-1], theta)[None, :]
     return _turn(x, phi)
 
 
@@ -85,12 +112,12 @@ def _layout_of(wl, tensor):
                       kv_lora_dim=wl.kv_lora_dim, rope_dim=wl.rope_dim)
 
 
-def apply_relocation(x: np.ndarray, delta, theta: float, layout) -> np.ndarray:
+def apply_relocation(x: np.ndarray, delta, theta: float, layout, sections=None) -> np.ndarray:
     """R(delta) on rows [n][D] following a row layout."""
     y = np.array(x, dtype=np.float64, copy=True)
     for start, width, rotated in layout:
         if rotated:
-            y[:, start:start + width] = relocate(y[:, start:start + width], delta, theta)
+            y[:, start:start + width] = relocate(y[:, start:start + width], delta, theta, sections)
     return y
 
 
@@ -110,15 +137,15 @@ def patch_product(u_bits, w_bits) -> np.ndarray:
 # The operator on a block of rows
 # --------------------------------------------------------------------------- #
 
-def operator_rows(x_bits, u_bits, w_bits, delta, theta, layout) -> np.ndarray:
+def operator_rows(x_bits, u_bits, w_bits, delta, theta, layout, sections=None) -> np.ndarray:
     """fp64 value of R(delta) x + U W^T for rows x [n][D] (bf16 bits)."""
-    y = apply_relocation(bf16_bits_to_f64(x_bits), delta, theta, layout)
+    y = apply_relocation(bf16_bits_to_f64(x_bits), delta, theta, layout, sections)
     if u_bits is not None:
         y = y + patch_product(u_bits, w_bits)
     return y
 
 
-def conditioning(x_bits, u_bits, w_bits, delta, theta, layout) -> np.ndarray:
+def conditioning(x_bits, u_bits, w_bits, delta, theta, layout, sections=None) -> np.ndarray:
     """Sum of magnitudes of the terms that make up each output element:
     |x_i cos| + |x_j sin| for a rotated element (|x| otherwise) plus
     sum_r |U_tr W_fr|.  Rounding errors of any evaluation order are bounded by
@@ -129,7 +156,7 @@ def conditioning(x_bits, u_bits, w_bits, delta, theta, layout) -> np.ndarray:
         if not rotated:
             continue
         h = width // 2
-        phi = np.float64(delta) * inv_freq(width, theta)
+        phi = pair_shifts(delta, h, sections) * inv_freq(width, theta)
         c, sn = np.abs(np.cos(phi)), np.abs(np.sin(phi))
         x1 = x[:, start:start + h]
         x2 = x[:, start + h:start + width]
@@ -172,8 +199,9 @@ def chunk_layer_rows(wl, inputs, ci: int, tensor: str, layer: int, tokens=None):
         u = inputs["u"][tensor][ci][layer, tok]
         w = inputs["w"][tensor][ci][layer]
     lay = _layout_of(wl, tensor)
-    ref = operator_rows(x, u, w, c.delta, wl.theta, lay)
-    cond = conditioning(x, u, w, c.delta, wl.theta, lay)
+    sec = getattr(wl, "mrope_sections", None)
+    ref = operator_rows(x, u, w, c.delta, wl.theta, lay, sec)
+    cond = conditioning(x, u, w, c.delta, wl.theta, lay, sec)
     return ref, cond
 
 

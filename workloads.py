@@ -46,7 +46,7 @@ class Chunk:
 
     src_row0: int    # first row of the chunk in the canonical store (per layer)
     n_tokens: int
-    delta: int       # RoPE position shift (new position - old position)
+    delta: object    # RoPE position shift (new - old); a (t, h, w) tuple under M-RoPE
     rank: int        # patch rank m (0 = relocation only)
     seq: int         # block-table row (paged destinations); 0 for contiguous
     dst_start: int   # first destination position of the chunk in its sequence
@@ -69,6 +69,7 @@ class Workload:
     block_tables: Optional[np.ndarray] = None   # int32 [n_seq][pages_per_seq]
     seed: int = 0
     backend: str = "numpy"
+    mrope_sections: Optional[tuple] = None   # (t, h, w) frequency-pair counts under M-RoPE
 
     @property
     def row_width(self) -> int:
@@ -161,11 +162,22 @@ def config(i: int, seed: Optional[int] = None) -> Workload:
                 chunks.append(Chunk((r * S + s) * T, T, delta, rank, r, s * T))
         return Workload("c4_window_survive_recall", "gqa", 28, 4, 128, 0, 128, 1e6, R * S * T,
                         R * pages_per_req, True, chunks, bt, seed, "torch")
+    if i == 5:
+        # Qwen2.5-VL-shaped video segment under M-RoPE: 28 layers, 4 KV heads x 128,
+        # frequency sections (16, 24, 24); the segment moves by a temporal shift and
+        # a spatial base shift drawn independently
+        dt = int(rng.integers(-32768, 32768, endpoint=True))
+        ds = int(rng.integers(-32768, 32768, endpoint=True))
+        bt = _perm_pages(rng, 4096 // PAGE)[None, :]
+        return Workload("c5_qwen25vl_mrope", "gqa", 28, 4, 128, 0, 128, 1e6, 4096, 4096 // PAGE,
+                        True, [Chunk(0, 4096, (dt, ds, ds), 32, 0, 0)], bt, seed, "numpy",
+                        mrope_sections=(16, 24, 24))
     raise ValueError(f"no workload {i}")
 
 
 def small_gqa(*, seed: int, n_layers=2, n_heads=2, head_dim=128, chunks_spec=((200, 37, 16, 0),),
-              paged=True, theta=1e6, extra_pages=0, dst_starts=None, name="small_gqa") -> Workload:
+              paged=True, theta=1e6, extra_pages=0, dst_starts=None, name="small_gqa",
+              mrope_sections=None) -> Workload:
     """A host-sized GQA workload.  chunks_spec: (n_tokens, delta, rank, seq) per chunk.
     Destinations are packed one after another in each sequence unless dst_starts
     is given; pools get ``extra_pages`` unused pages so placement is checked."""
@@ -186,7 +198,7 @@ def small_gqa(*, seed: int, n_layers=2, n_heads=2, head_dim=128, chunks_spec=((2
         num_pages = pages_per_seq + extra_pages
         bt = None
     return Workload(name, "gqa", n_layers, n_heads, head_dim, 0, head_dim, theta, row, num_pages,
-                    paged, chunks, bt, seed, "numpy")
+                    paged, chunks, bt, seed, "numpy", mrope_sections=mrope_sections)
 
 
 def small_mla(*, seed: int, n_layers=2, n_tokens=150, delta=-999, rank=32, paged=True,
