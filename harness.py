@@ -100,6 +100,16 @@ class DeviceWorkload:
                 rank=a["rank"], u=a["u"][0], v=a["w"][0], src_layer_stride=a["src_layer_stride"],
                 u_layer_stride=a["u_layer_stride"], v_layer_stride=a["w_layer_stride"],
                 d_status=self.status, stream=stream)
+        elif len(wl.chunks) == 1 and wl.mrope_sections is not None:
+            a = self._chunks[0]
+            kvrp.kv_relocate_patch_mrope(
+                a["srcs"][0], a["srcs"][1], n_layers=wl.n_layers, n_tokens=a["n_tokens"],
+                n_kv_heads=wl.n_heads, head_dim=wl.head_dim, delta_thw=a["delta"],
+                mrope_section=wl.mrope_sections, rope_theta=wl.theta,
+                k_dst=a["dst"][0], v_dst=a["dst"][1], rank=a["rank"], uk=a["u"][0], vk=a["w"][0],
+                uv=a["u"][1], vv=a["w"][1], src_layer_stride=a["src_layer_stride"],
+                u_layer_stride=a["u_layer_stride"], v_layer_stride=a["w_layer_stride"],
+                d_status=self.status, stream=stream)
         elif len(wl.chunks) == 1:
             a = self._chunks[0]
             kvrp.kv_relocate_patch(

@@ -111,6 +111,28 @@ kvrp_status kv_relocate_patch(
     uint32_t* d_status, kvrp_stream_t stream);
 
 /*
+ * kv_relocate_patch_mrope -- kv_relocate_patch under M-RoPE, the multimodal
+ * RoPE of Qwen-VL-style models, which re-rotate image and video KV with it
+ * (gist.science/pt/paper/2606.17107, section 4: transplanted image KV is
+ * re-rotated with M-RoPE).  The head_dim / 2 frequency pairs form three
+ * consecutive sections -- temporal, height, width -- of mrope_section[0..2]
+ * pairs (Qwen2.5-VL with head_dim 128: {16, 24, 24}); pair i turns by
+ * delta_thw[s] * theta^(-2i/head_dim), s being the section holding i.
+ *   delta_thw      host array: the (temporal, height, width) position shift.
+ *   mrope_section  host array: frequency pairs per section, summing to head_dim / 2.
+ *   Everything else as kv_relocate_patch.  Equal shifts give plain RoPE.
+ */
+kvrp_status kv_relocate_patch_mrope(
+    const void* k_src, const void* v_src, int64_t src_layer_stride,
+    int32_t n_layers, int32_t n_tokens, int32_t n_kv_heads, int32_t head_dim,
+    const int64_t delta_thw[3], const int32_t mrope_section[3],
+    double rope_theta, int32_t rank,
+    const void* uk, const void* vk, const void* uv, const void* vv,
+    int64_t u_layer_stride, int64_t v_layer_stride,
+    const kvrp_dst* k_dst, const kvrp_dst* v_dst,
+    uint32_t* d_status, kvrp_stream_t stream);
+
+/*
  * kv_relocate_patch_mla -- one MLA chunk, all layers, one launch (section 2,
  * MLA bullet: only the decoupled 64-dim k_rope is relocated, c_KV is reused
  * byte for byte, the patch goes to both channels).

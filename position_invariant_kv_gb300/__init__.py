@@ -4,6 +4,7 @@ Argument marshalling only: every step of the operator runs in the library's
 CUDA kernel.  Names mirror the C ABI in include/kvrp.h:
 
     kv_relocate_patch        GQA/MHA chunk, all layers, K and V
+    kv_relocate_patch_mrope  the same under M-RoPE (per-section temporal/height/width shifts)
     kv_relocate_patch_mla    MLA chunk (c_KV ++ k_rope rows)
     kv_relocate_batch        many GQA/MHA chunks, each with its own delta and patch
     kv_relocate_batch_workspace_size
@@ -19,7 +20,7 @@ from ._abi import (  # noqa: F401
     KVRP_DEV_BAD_PAGE, KVRP_DEV_TIMEOUT, KVRP_OK, KVRP_ERR_INVALID_ARG, KVRP_ERR_ALIGNMENT,
     KVRP_ERR_UNSUPPORTED, KVRP_ERR_CUDA, KVRP_ERR_WORKSPACE,
     Dst, Chunk, KvrpError, lib, lib_path,
-    kv_relocate_patch, kv_relocate_patch_mla, kv_relocate_batch, kv_relocate_batch_workspace_size,
+    kv_relocate_patch, kv_relocate_patch_mrope, kv_relocate_patch_mla, kv_relocate_batch, kv_relocate_batch_workspace_size,
     kvrp_status_string, kvrp_version, EXPORTED_SYMBOLS,
     kv_relocate_batch_noalloc, KVRP_NOALLOC_MAX_CHUNKS, chunk_array,
 )

@@ -19,7 +19,7 @@ KVRP_DEV_BAD_PAGE = 0x1
 KVRP_DEV_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = (
-    "kv_relocate_patch", "kv_relocate_patch_mla", "kv_relocate_batch",
+    "kv_relocate_patch", "kv_relocate_patch_mrope", "kv_relocate_patch_mla", "kv_relocate_batch",
     "kv_relocate_batch_workspace_size", "kv_relocate_batch_noalloc", "kvrp_status_string",
     "kvrp_last_error", "kvrp_version",
 )
@@ -51,6 +51,12 @@ def _load_library():
         C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
         C.c_int64, C.c_double, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
         C.c_int64, C.c_int64, C.POINTER(kvrp_dst), C.POINTER(kvrp_dst), C.c_void_p, C.c_void_p]
+    L.kv_relocate_patch_mrope.restype = st
+    L.kv_relocate_patch_mrope.argtypes = [
+        C.c_void_p, C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+        C.POINTER(C.c_int64), C.POINTER(C.c_int32), C.c_double, C.c_int32, C.c_void_p, C.c_void_p,
+        C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.POINTER(kvrp_dst), C.POINTER(kvrp_dst), C.c_void_p,
+        C.c_void_p]
     L.kv_relocate_patch_mla.restype = st
     L.kv_relocate_patch_mla.argtypes = [
         C.c_void_p, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int64, C.c_double,
@@ -178,6 +184,20 @@ def kv_relocate_patch(k_src, v_src, *, n_layers: int, n_tokens: int, n_kv_heads:
         int(head_dim), int(delta), float(rope_theta), int(rank), _ptr(uk), _ptr(vk), _ptr(uv), _ptr(vv),
         int(u_layer_stride), int(v_layer_stride), C.byref(kd), C.byref(vd), _ptr(d_status),
         _stream(stream)))
+
+
+def kv_relocate_patch_mrope(k_src, v_src, *, n_layers: int, n_tokens: int, n_kv_heads: int, head_dim: int,
+                            delta_thw, mrope_section, rope_theta: float, k_dst: Dst, v_dst: Dst, rank: int = 0,
+                            uk=None, vk=None, uv=None, vv=None, src_layer_stride: int = 0,
+                            u_layer_stride: int = 0, v_layer_stride: int = 0, d_status=None,
+                            stream=None) -> None:
+    kd, vd = k_dst.c(), v_dst.c()
+    d3 = (C.c_int64 * 3)(*[int(v) for v in delta_thw])
+    s3 = (C.c_int32 * 3)(*[int(v) for v in mrope_section])
+    _check(lib().kv_relocate_patch_mrope(
+        _ptr(k_src), _ptr(v_src), int(src_layer_stride), int(n_layers), int(n_tokens), int(n_kv_heads),
+        int(head_dim), d3, s3, float(rope_theta), int(rank), _ptr(uk), _ptr(vk), _ptr(uv), _ptr(vv),
+        int(u_layer_stride), int(v_layer_stride), C.byref(kd), C.byref(vd), _ptr(d_status), _stream(stream)))
 
 
 def kv_relocate_patch_mla(src, *, n_layers: int, n_tokens: int, kv_lora_dim: int, rope_dim: int,

@@ -102,11 +102,16 @@ float head16(double v) {
 // Layout, two pairs per float4 so the kernel can use packed fp32x2 math:
 //   tab[2j]     = {C_2j,  C_2j+1,  S_2j,  S_2j+1}    (16-bit heads)
 //   tab[2j + 1] = {Cl_2j, Cl_2j+1, Sl_2j, Sl_2j+1}   (fp32 tails)
-void phase_table(int64_t delta, double theta, int rot_dim, float4* tab) {
+// Frequency pair i turns by the shift of the section that holds it: plain
+// RoPE has one section covering every pair; M-RoPE (multimodal RoPE of
+// Qwen-VL-style models) has consecutive temporal / height / width sections.
+void phase_table(const int64_t delta[3], const int32_t sections[3], double theta, int rot_dim, float4* tab) {
   float head_c[kTablePairs] = {}, head_s[kTablePairs] = {}, tail_c[kTablePairs] = {}, tail_s[kTablePairs] = {};
+  int sec = 0, sec_end = sections[0];
   for (int i = 0; i < rot_dim / 2; ++i) {
+    while (i >= sec_end && sec < 2) sec_end += sections[++sec];
     const double inv = std::pow(theta, -2.0 * i / rot_dim);
-    const double phi = static_cast<double>(delta) * inv;
+    const double phi = static_cast<double>(delta[sec]) * inv;
     const double c = std::cos(phi), s = std::sin(phi);
     head_c[i] = head16(c);
     head_s[i] = head16(s);
@@ -135,7 +140,8 @@ struct ChunkIn {
   int n_tensors;
   int64_t src_layer_stride, u_layer_stride, w_layer_stride;
   int32_t n_tokens, rank;
-  int64_t delta;
+  int64_t delta[3];           // plain RoPE: {delta, 0, 0}
+  int32_t sections[3];        // frequency pairs per section; plain RoPE: {rot_dim / 2, 0, 0}
 };
 struct Shape {
   int n_layers;
@@ -230,21 +236,33 @@ struct MapKeyHash {
 struct MapKeyEq {
   bool operator()(const MapKey& a, const MapKey& b) const { return std::memcmp(&a, &b, sizeof(MapKey)) == 0; }
 };
-struct TableKey {
-  int64_t delta;
+struct TableKey {             // zero-filled before use, so it compares and hashes as bytes
+  int64_t delta[3];
+  int32_t sections[3];
+  int32_t rot_dim;
   double theta;
-  int64_t rot_dim;
-  bool operator==(const TableKey& o) const {
-    return delta == o.delta && std::memcmp(&theta, &o.theta, sizeof(double)) == 0 && rot_dim == o.rot_dim;
-  }
+  bool operator==(const TableKey& o) const { return std::memcmp(this, &o, sizeof(TableKey)) == 0; }
+  bool operator<(const TableKey& o) const { return std::memcmp(this, &o, sizeof(TableKey)) < 0; }
 };
 struct TableKeyHash {
   size_t operator()(const TableKey& k) const {
-    uint64_t t;
-    std::memcpy(&t, &k.theta, sizeof(t));
-    return static_cast<size_t>((uint64_t)k.delta * 0x9E3779B97F4A7C15ull ^ t ^ ((uint64_t)k.rot_dim << 40));
+    const unsigned char* p = reinterpret_cast<const unsigned char*>(&k);
+    uint64_t h = 1469598103934665603ull;
+    for (size_t i = 0; i < sizeof(TableKey); ++i) h = (h ^ p[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
   }
 };
+TableKey table_key(const int64_t delta[3], const int32_t sections[3], int rot_dim, double theta) {
+  TableKey k;
+  std::memset(&k, 0, sizeof(k));
+  for (int i = 0; i < 3; ++i) {
+    k.delta[i] = delta[i];
+    k.sections[i] = sections[i];
+  }
+  k.rot_dim = rot_dim;
+  k.theta = theta;
+  return k;
+}
 struct CachedTable {
   float4 v[kTablePairs];
 };
@@ -299,12 +317,12 @@ class PlanBuilder {
     return KVRP_OK;
   }
 
-  int32_t table(int64_t delta) {
-    auto f = tab_index_.find(delta);
+  int32_t table(const int64_t delta[3], const int32_t sections[3]) {
+    const TableKey key = table_key(delta, sections, sh_.rot_dim, sh_.theta);
+    auto f = tab_index_.find(key);
     if (f != tab_index_.end()) return f->second;
     const int32_t idx = static_cast<int32_t>(tabs_.size() / kTablePairs);
     tabs_.resize(tabs_.size() + kTablePairs);
-    const TableKey key{delta, sh_.theta, sh_.rot_dim};
     bool cached = false;
     {
       std::lock_guard<std::mutex> lk(g_cache_mu);
@@ -315,14 +333,14 @@ class PlanBuilder {
       }
     }
     if (!cached) {
-      phase_table(delta, sh_.theta, sh_.rot_dim, &tabs_[idx * kTablePairs]);
+      phase_table(delta, sections, sh_.theta, sh_.rot_dim, &tabs_[idx * kTablePairs]);
       CachedTable t;
       std::memcpy(t.v, &tabs_[idx * kTablePairs], sizeof(CachedTable));
       std::lock_guard<std::mutex> lk(g_cache_mu);
       if (g_table_cache.size() >= kCacheMaxEntries) g_table_cache.clear();
       g_table_cache.emplace(key, t);
     }
-    tab_index_[delta] = idx;
+    tab_index_[key] = idx;
     return idx;
   }
 
@@ -370,7 +388,7 @@ class PlanBuilder {
         if (st != KVRP_OK) return st;
       }
     }
-    if (any_rot && c.n_tokens > 0) r.table = table(c.delta);
+    if (any_rot && c.n_tokens > 0) r.table = table(c.delta, c.sections);
     m_max_ = std::max(m_max_, c.rank);
     chunks_.push_back(r);
     return KVRP_OK;
@@ -484,7 +502,7 @@ class PlanBuilder {
   std::vector<CUtensorMap> maps_;
   std::map<MapKey, int32_t> map_index_;
   std::vector<float4> tabs_;
-  std::map<int64_t, int32_t> tab_index_;
+  std::map<TableKey, int32_t> tab_index_;
   std::vector<ChunkRec> chunks_;
 };
 
@@ -584,6 +602,13 @@ kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d
   return KVRP_OK;
 }
 
+void set_plain_shift(ChunkIn* c, int64_t delta, int rot_dim) {
+  c->delta[0] = delta;
+  c->delta[1] = c->delta[2] = 0;
+  c->sections[0] = rot_dim / 2;
+  c->sections[1] = c->sections[2] = 0;
+}
+
 TensorIn tensor_in(const void* src, const void* u, const void* w, const kvrp_dst* d, int rot_kind,
                    int rot_from) {
   TensorIn t;
@@ -664,7 +689,47 @@ kvrp_status kv_relocate_patch(const void* k_src, const void* v_src, int64_t src_
   c.w_layer_stride = v_layer_stride;
   c.n_tokens = n_tokens;
   c.rank = rank;
-  c.delta = delta;
+  set_plain_shift(&c, delta, head_dim);
+  kvrp_status st = check_chunk(c, sh);
+  if (st != KVRP_OK) return st;
+  return run(sh, {c}, d_status, nullptr, 0, stream);
+}
+
+kvrp_status kv_relocate_patch_mrope(const void* k_src, const void* v_src, int64_t src_layer_stride,
+                                    int32_t n_layers, int32_t n_tokens, int32_t n_kv_heads, int32_t head_dim,
+                                    const int64_t delta_thw[3], const int32_t mrope_section[3],
+                                    double rope_theta, int32_t rank, const void* uk, const void* vk,
+                                    const void* uv, const void* vv, int64_t u_layer_stride,
+                                    int64_t v_layer_stride, const kvrp_dst* k_dst, const kvrp_dst* v_dst,
+                                    uint32_t* d_status, kvrp_stream_t stream) {
+  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
+  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  if (!k_dst || !v_dst) return fail(KVRP_ERR_INVALID_ARG, "k_dst and v_dst are required");
+  if (!delta_thw || !mrope_section) return fail(KVRP_ERR_INVALID_ARG, "delta_thw and mrope_section are required");
+  int64_t pairs = 0;
+  for (int i = 0; i < 3; ++i) {
+    if (mrope_section[i] < 0) return fail(KVRP_ERR_INVALID_ARG, "mrope_section entries must be >= 0");
+    pairs += mrope_section[i];
+  }
+  if (pairs != head_dim / 2)
+    return fail(KVRP_ERR_INVALID_ARG, "mrope_section must sum to head_dim / 2 = %d (got %lld)", head_dim / 2,
+                (long long)pairs);
+  const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
+  ChunkIn c;
+  c.n_tensors = 2;
+  c.t[0] = tensor_in(k_src, uk, vk, k_dst, head_dim == 128 ? kRotHalf128 : kRotHalf64, 0);
+  c.t[1] = tensor_in(v_src, uv, vv, v_dst, kRotNone, 0);
+  c.src_layer_stride = src_layer_stride;
+  c.u_layer_stride = u_layer_stride;
+  c.w_layer_stride = v_layer_stride;
+  c.n_tokens = n_tokens;
+  c.rank = rank;
+  for (int i = 0; i < 3; ++i) {
+    c.delta[i] = delta_thw[i];
+    c.sections[i] = mrope_section[i];
+  }
   kvrp_status st = check_chunk(c, sh);
   if (st != KVRP_OK) return st;
   return run(sh, {c}, d_status, nullptr, 0, stream);
@@ -691,7 +756,7 @@ kvrp_status kv_relocate_patch_mla(const void* src, int64_t src_layer_stride, int
   c.w_layer_stride = v_layer_stride;
   c.n_tokens = n_tokens;
   c.rank = rank;
-  c.delta = delta;
+  set_plain_shift(&c, delta, rope_dim);
   kvrp_status st = check_chunk(c, sh);
   if (st != KVRP_OK) return st;
   return run(sh, {c}, d_status, nullptr, 0, stream);
@@ -726,7 +791,7 @@ kvrp_status kv_relocate_batch(const kvrp_chunk* chunks, int32_t n_chunks, int32_
     c.w_layer_stride = k.v_layer_stride;
     c.n_tokens = k.n_tokens;
     c.rank = k.rank;
-    c.delta = k.delta;
+    set_plain_shift(&c, k.delta, head_dim);
     kvrp_status st = check_chunk(c, sh);
     if (st != KVRP_OK) {
       std::string msg = "chunk " + std::to_string(i) + ": " + g_last_error;
@@ -764,7 +829,7 @@ kvrp_status kv_relocate_batch_noalloc(const kvrp_chunk* chunks, int32_t n_chunks
     c.w_layer_stride = k.v_layer_stride;
     c.n_tokens = k.n_tokens;
     c.rank = k.rank;
-    c.delta = k.delta;
+    set_plain_shift(&c, k.delta, head_dim);
     kvrp_status st = check_chunk(c, sh);
     if (st != KVRP_OK) {
       std::string msg = "chunk " + std::to_string(i) + ": " + g_last_error;

@@ -75,8 +75,9 @@ def sampled_compare(wl, dwl, n_rows=48, seed=0):
             w = bits(dwl.w[name][ci][l])
         lay = row_layout(wl.family, name, n_heads=wl.n_heads, head_dim=wl.head_dim,
                          kv_lora_dim=wl.kv_lora_dim, rope_dim=wl.rope_dim)
-        ref = operator_rows(x, u, w, c.delta, wl.theta, lay)
-        cond = conditioning(x, u, w, c.delta, wl.theta, lay)
+        sec = wl.mrope_sections
+        ref = operator_rows(x, u, w, c.delta, wl.theta, lay, sec)
+        cond = conditioning(x, u, w, c.delta, wl.theta, lay, sec)
         q = c.dst_start + toks
         page = wl.block_tables[c.seq][q // 16] if wl.paged else q // 16
         pool = dwl.pools[name]

@@ -114,3 +114,18 @@ def test_no_gpu_means_cuda_error_not_fallback(kvrp):
                                delta=5, rope_theta=1e4, k_dst=kvrp.Dst(**_dst()),
                                v_dst=kvrp.Dst(**_dst(base=0x40000)), stream=0)
     assert e.value.status == kvrp.KVRP_ERR_CUDA
+
+
+def test_mrope_argument_checks(kvrp):
+    kd, vd = kvrp.Dst(**_dst()), kvrp.Dst(**_dst(base=0x40000))
+    base = dict(n_layers=1, n_tokens=100, n_kv_heads=2, head_dim=128, rope_theta=1e4, k_dst=kd, v_dst=vd, stream=0)
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_patch_mrope(0x20000, 0x30000, delta_thw=(1, 2, 3), mrope_section=(16, 24, 20), **base)
+    assert e.value.status == kvrp.KVRP_ERR_INVALID_ARG and "sum" in str(e.value)
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_patch_mrope(0x20000, 0x30000, delta_thw=(1, 2, 3), mrope_section=(-1, 33, 32), **base)
+    assert e.value.status == kvrp.KVRP_ERR_INVALID_ARG
+    with pytest.raises(kvrp.KvrpError) as e:     # well-formed: fails only for want of a GPU
+        kvrp.kv_relocate_patch_mrope(0x20000, 0x30000, delta_thw=(1, 2, 3), mrope_section=(16, 24, 24), **base)
+    import torch
+    assert e.value.status == (kvrp.KVRP_ERR_CUDA if not torch.cuda.is_available() else e.value.status)

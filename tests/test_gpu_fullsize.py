@@ -124,3 +124,18 @@ def test_config4_window_survival_and_recall_batch():
         assert torch.equal(out.view(torch.int16), dwl.rows["v"][l, src].view(torch.int16)), l
     del dwl
     torch.cuda.empty_cache()
+
+
+def test_config5_qwen25vl_mrope():
+    from gpu_util import streaming_compare, sampled_compare
+    wl = W.config(5)
+    dwl = harness.DeviceWorkload(wl)
+    dwl.run()
+    torch.cuda.synchronize()
+    assert dwl.status_value() == 0
+    for n, k in untouched_slots(dwl).items():
+        assert k == expected_untouched(wl), n
+    reps = streaming_compare(wl, dwl, layers=[0, 27])
+    print(reps)
+    check(reps)
+    check(sampled_compare(wl, dwl, n_rows=48, seed=5))

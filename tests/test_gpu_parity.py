@@ -183,3 +183,20 @@ def test_other_stream():
     want, _, _ = run_workload(wl, dwl.host)
     for n in wl.tensors:
         assert ulp_distance(got[n], want[n]).max() <= 1
+
+
+@pytest.mark.parametrize("head_dim,sections,delta,rank,T", [
+    (128, (16, 24, 24), (-4537, 20000, 20000), 32, 300),   # Qwen2.5-VL layout, spatial base shift
+    (128, (16, 24, 24), (12, -30000, 777), 0, 129),        # three different shifts, no patch
+    (64, (8, 12, 12), (5, 6, 7), 16, 200),
+    (64, (0, 16, 16), (99999, -3, 4), 0, 77),               # an empty temporal section
+])
+def test_mrope_small(head_dim, sections, delta, rank, T):
+    from gpu_util import run_and_compare
+    wl = W.small_gqa(seed=950 + T, n_layers=2, n_heads=3, head_dim=head_dim,
+                     chunks_spec=((T, delta, rank, 0),), dst_starts=[9], extra_pages=2,
+                     mrope_sections=sections)
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps, strict=(rank == 0))
+    assert dwl.status_value() == 0
