@@ -215,6 +215,62 @@ kvrp_status kv_relocate_batch_noalloc(
     int32_t n_layers, int32_t n_kv_heads, int32_t head_dim, double rope_theta,
     uint32_t* d_status, kvrp_stream_t stream);
 
+/*
+ * Patch formation -- the rank-m factors of the conditioning deficit (Kamera,
+ * section 2, patch bullet: computed once, at compile time or on first reuse,
+ * from one conditioned pass over [A, B] followed by an SVD that keeps the
+ * top-m factors).  The conditioned pass itself belongs to the model and is
+ * the caller's: this call takes its output KV(B|A) together with the
+ * canonical KV(B|empty) of the same tensor and forms
+ *     Delta = KV(B|A) - R(delta) KV(B|empty)      (the destination frame)
+ * per layer, then factors U_m [T][m] (singular values folded in) and
+ * V_m [D][m] in bf16 such that U_m V_m^T approximates Delta, ready for
+ * kv_relocate_patch / _mla / _batch.  The factorisation is a randomized range
+ * finder with `power_iters` power iterations, Cholesky-QR orthonormalisation
+ * and an fp64 Jacobi eigensolver on the small projected problem.
+ *   conditioned, canonical  device bf16 [n_layers][n_tokens][row_width], rows
+ *               dense; layer l at base + l * *_layer_stride elements (0: dense
+ *               layers).  Only read.
+ *   rope_kind   KVRP_ROPE_HEADS: every head of rot_dim features turns (keys;
+ *               row_width a multiple of rot_dim);
+ *               KVRP_ROPE_NONE: nothing turns (values; rot_dim, delta, theta unused);
+ *               KVRP_ROPE_MLA_TAIL: the last rot_dim features turn (MLA k_rope).
+ *               rot_dim: a multiple of 4, at most 128.
+ *   delta, rope_theta  the position shift and the RoPE base, as in kv_relocate_patch.
+ *   rank, oversample  m >= 1 and the range finder's extra columns p >= 0;
+ *               m + p <= 96, m <= min(n_tokens, row_width).
+ *   power_iters 0..8 subspace iterations (1-2 suffice for decaying spectra).
+ *   omega       device fp32 [row_width][m + p], row-major: the caller's Gaussian
+ *               test matrix (N(0, 1) entries), shared by all layers; only read.
+ *   u_out, v_out  device bf16 U_m [L][T][m] and V_m [L][row_width][m],
+ *               row-major, layer strides u/v_layer_stride elements (0: dense);
+ *               V_m has orthonormal columns, U_m = Delta V_m.
+ *   workspace   device scratch of at least kv_patch_form_workspace_size(...)
+ *               bytes, owned by the caller, busy until the call's work on
+ *               `stream` completes (no two overlapping calls may share it).
+ * Base pointers must be 16-byte aligned.  Precision: Delta and the tall products in
+ * fp32, the small k x k problems in fp64, factors rounded once to bf16.
+ * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (sizes beyond the limits above)
+ * and WORKSPACE are returned before any CUDA work is queued; CUDA if a launch
+ * fails.  Asynchronous on `stream`; the result is an approximation of the
+ * truncated SVD whose quality grows with p and power_iters.
+ */
+#define KVRP_ROPE_NONE 0
+#define KVRP_ROPE_HEADS 1
+#define KVRP_ROPE_MLA_TAIL 2
+
+size_t kv_patch_form_workspace_size(int32_t n_layers, int32_t n_tokens, int32_t row_width,
+                                    int32_t rank, int32_t oversample);
+
+kvrp_status kv_patch_form(
+    const void* conditioned, const void* canonical,
+    int64_t cond_layer_stride, int64_t canon_layer_stride,
+    int32_t n_layers, int32_t n_tokens, int32_t row_width,
+    int32_t rope_kind, int32_t rot_dim, int64_t delta, double rope_theta,
+    int32_t rank, int32_t oversample, int32_t power_iters, const float* omega,
+    void* u_out, void* v_out, int64_t u_layer_stride, int64_t v_layer_stride,
+    void* workspace, size_t workspace_bytes, kvrp_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvrp_status_string(kvrp_status status);
 

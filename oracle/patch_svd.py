@@ -24,3 +24,13 @@ def eckart_young_tail(delta_kv: np.ndarray, m: int) -> float:
     """Sum of the squared singular values beyond the first m."""
     s = np.linalg.svd(np.asarray(delta_kv, dtype=np.float64), compute_uv=False)
     return float(np.sum(s[m:] ** 2))
+
+
+def conditioning_deficit(cond_rows: np.ndarray, canon_rows: np.ndarray, delta, theta: float, layout,
+                         sections=None) -> np.ndarray:
+    """Delta = KV(B|A) - R(delta) KV(B|empty) for rows [n][D] given in fp64
+    (already decoded from bf16): the matrix whose top-m factors make the patch.
+    R(delta) follows the row layout (keys: every head turned; values: none;
+    MLA: only k_rope turned), exactly as the reuse operator applies it."""
+    from .kamera import apply_relocation
+    return np.asarray(cond_rows, dtype=np.float64) - apply_relocation(canon_rows, delta, theta, layout, sections)

@@ -24,7 +24,6 @@
 #include "kvrp_plan.h"
 
 namespace kvrp {
-namespace {
 
 thread_local char g_last_error[512] = "";
 
@@ -41,6 +40,8 @@ kvrp_status cuda_fail(cudaError_t e, const char* what) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+namespace {
 
 // ---------------------------------------------------------------------------
 // Per-device state: SM count, shared-memory limit, driver entry point.
@@ -87,6 +88,8 @@ kvrp_status device_info(DeviceInfo** out) {
   return KVRP_OK;
 }
 
+}  // namespace
+
 // ---------------------------------------------------------------------------
 // Phase tables: phi_i = delta * theta^(-2i/d) in fp64; cos and sin split into a
 // 16-significant-bit head (so that a bf16 times the head is exact in fp32) and
@@ -123,6 +126,8 @@ void phase_table(const int64_t delta[3], const int32_t sections[3], double theta
     tab[2 * j + 1] = make_float4(tail_c[2 * j], tail_c[2 * j + 1], tail_s[2 * j], tail_s[2 * j + 1]);
   }
 }
+
+namespace {
 
 // ---------------------------------------------------------------------------
 // Chunk descriptions common to every entry point.
@@ -510,6 +515,19 @@ class PlanBuilder {
 // fits, otherwise through `workspace` (device) with one host-to-device copy.
 kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d_status, void* workspace,
                 size_t workspace_bytes, cudaStream_t stream);
+
+}  // namespace
+
+kvrp_status current_device_sms(int* sms, int* smem_optin) {
+  DeviceInfo* di = nullptr;
+  const kvrp_status st = device_info(&di);
+  if (st != KVRP_OK) return st;
+  *sms = di->sms;
+  *smem_optin = di->smem_optin;
+  return KVRP_OK;
+}
+
+namespace {
 
 // Pinned staging for batch plans: a small ring per device, so consecutive
 // calls never overwrite a buffer whose copy is still queued.

@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kvrp.h"
+
 namespace kvrp {
 
 constexpr int kPage = 16;           // tokens per destination page
@@ -127,6 +129,15 @@ __host__ __device__ inline SmemLayout smem_layout(int m_max, int stages, int u_b
 // dev_plan points at a plan already resident in device memory.
 cudaError_t launch_relocate(const void* param_plan, const void* dev_plan, int grid,
                             int smem_bytes, cudaStream_t stream);
+
+// Host helpers shared by the library's translation units.
+kvrp_status fail(kvrp_status st, const char* fmt, ...);
+bool aligned16(const void* p);
+// Split phase table of one shift: sections = frequency pairs per (t, h, w)
+// section (plain RoPE: {rot_dim / 2, 0, 0}); layout as the kernel reads it.
+void phase_table(const int64_t delta[3], const int32_t sections[3], double theta, int rot_dim, float4* tab);
+// SM count and shared-memory opt-in limit of the current device (checks sm_103).
+kvrp_status current_device_sms(int* sms, int* smem_optin);
 
 // Per-device one-time kernel setup (dynamic shared-memory opt-in).
 cudaError_t prepare_kernel(int smem_bytes);

@@ -129,3 +129,36 @@ def test_mrope_argument_checks(kvrp):
         kvrp.kv_relocate_patch_mrope(0x20000, 0x30000, delta_thw=(1, 2, 3), mrope_section=(16, 24, 24), **base)
     import torch
     assert e.value.status == (kvrp.KVRP_ERR_CUDA if not torch.cuda.is_available() else e.value.status)
+
+
+def test_patch_form_argument_checks(kvrp):
+    def status(**over):
+        args = dict(conditioned=0x20000, canonical=0x30000, n_layers=2, n_tokens=100, row_width=256,
+                    rope_kind=kvrp.KVRP_ROPE_HEADS, rot_dim=128, delta=5, rope_theta=1e4, rank=16, oversample=8,
+                    power_iters=2, omega=0x50000, u_out=0x60000, v_out=0x70000, workspace=0x100000,
+                    workspace_bytes=1 << 30, cond_layer_stride=100 * 256, canon_layer_stride=100 * 256,
+                    u_layer_stride=100 * 16, v_layer_stride=256 * 16, stream=0)
+        args.update(over)
+        c, x = args.pop("conditioned"), args.pop("canonical")
+        with pytest.raises(kvrp.KvrpError) as e:
+            kvrp.kv_patch_form(c, x, **args)
+        return e.value.status
+
+    assert status(conditioned=0) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(omega=0x50004) == kvrp.KVRP_ERR_ALIGNMENT
+    assert status(rank=64, oversample=40) == kvrp.KVRP_ERR_UNSUPPORTED      # rank + oversample > 96
+    assert status(rank=0) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert status(rot_dim=96) == kvrp.KVRP_ERR_INVALID_ARG                   # 256 is not a multiple of 96
+    assert status(rot_dim=130) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert status(rope_kind=7) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(rope_kind=kvrp.KVRP_ROPE_MLA_TAIL, row_width=64, rot_dim=64) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(power_iters=9) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(cond_layer_stride=10) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(v_layer_stride=10) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(workspace_bytes=1024) == kvrp.KVRP_ERR_WORKSPACE
+    need = kvrp.kv_patch_form_workspace_size(2, 100, 256, 16, 8)
+    assert need >= 4 * 2 * 100 * 256                                          # at least the fp32 deficit
+    assert kvrp.kv_patch_form_workspace_size(0, 100, 256, 16, 8) == 0
+    import torch
+    if not torch.cuda.is_available():                                         # well-formed: no GPU, no fallback
+        assert status(workspace_bytes=need) == kvrp.KVRP_ERR_CUDA

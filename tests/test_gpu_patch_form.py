@@ -1,0 +1,187 @@
+"""GPU patch formation (kv_patch_form) against the fp64 oracle.
+
+The deficit Delta = KV(B|A) - R(delta) KV(B|empty) of synthetic caches is
+factored on the GPU; the oracle computes Delta in fp64 from the same bf16
+inputs and its exact truncated SVD (Kamera, gist.science/pt/paper/2606.23581,
+section 2, patch bullet: top-m factors from an SVD).  A randomized range
+finder is not the exact SVD, so parity is stated through the Eckart-Young
+residual ||Delta - U_m V_m^T||_F^2: the GPU factors, rounded to bf16, must
+come within a few percent of the oracle's exact factors rounded the same way.
+An end-to-end case then uses the formed factors in kv_relocate_patch and
+checks that the reuse operator recovers KV(B|A) from the canonical cache."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from position_invariant_kv_gb300.build import build
+    build()
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def layout_of(kind, D, rot_dim):
+    from oracle import row_layout
+    if kind == "heads":
+        return row_layout("gqa", "k", n_heads=D // rot_dim, head_dim=rot_dim)
+    if kind == "mla":
+        return row_layout("mla", "k", kv_lora_dim=D - rot_dim, rope_dim=rot_dim)
+    return row_layout("gqa", "v", n_heads=1, head_dim=D)
+
+
+def make_case(seed, L, T, D, kind, rot_dim, delta, theta, true_rank, noise=1e-3, scale=0.05):
+    """bf16 canonical and conditioned caches whose deficit is low rank + noise:
+    cond = bf16(R(delta) canon + sum_i s_i a_i b_i^T + noise), s_i decaying."""
+    from oracle import bf16_bits_to_f64, round_to_bf16_bits
+    from oracle.kamera import apply_relocation
+    rng = np.random.default_rng(seed)
+    canon = round_to_bf16_bits(rng.standard_normal((L, T, D)) * rng.lognormal(0, 0.5, (L, 1, D)))
+    cond = np.empty_like(canon)
+    lay = layout_of(kind, D, rot_dim)
+    for l in range(L):
+        y = apply_relocation(bf16_bits_to_f64(canon[l]), delta, theta, lay)
+        u0 = np.linalg.qr(rng.standard_normal((T, true_rank)))[0]
+        v0 = np.linalg.qr(rng.standard_normal((D, true_rank)))[0]
+        s0 = 3.0 * np.sqrt(T) * 10.0 ** (-np.arange(true_rank) / 12)
+        deficit = (u0 * s0) @ v0.T * scale + noise * rng.standard_normal((T, D))
+        cond[l] = round_to_bf16_bits(y + deficit)
+    return canon, cond
+
+
+def oracle_delta(canon, cond, kind, rot_dim, delta, theta):
+    """fp64 deficit per layer from the oracle."""
+    from oracle import bf16_bits_to_f64, conditioning_deficit
+    lay = layout_of(kind, canon.shape[-1], rot_dim)
+    return np.stack([conditioning_deficit(bf16_bits_to_f64(cond[l]), bf16_bits_to_f64(canon[l]), delta, theta, lay)
+                     for l in range(canon.shape[0])])
+
+
+def form_on_gpu(canon, cond, kind, rot_dim, delta, theta, m, p, q, seed=0):
+    import position_invariant_kv_gb300 as kvrp
+    L, T, D = canon.shape
+    k = m + p
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    omega = torch.randn((D, k), generator=g, device="cuda", dtype=torch.float32)
+    u = torch.empty((L, T, m), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((L, D, m), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(kvrp.kv_patch_form_workspace_size(L, T, D, m, p), dtype=torch.uint8, device="cuda")
+    rope = {"heads": kvrp.KVRP_ROPE_HEADS, "none": kvrp.KVRP_ROPE_NONE, "mla": kvrp.KVRP_ROPE_MLA_TAIL}[kind]
+    kvrp.kv_patch_form(_dev(cond), _dev(canon), n_layers=L, n_tokens=T, row_width=D, rope_kind=rope,
+                       rot_dim=rot_dim, delta=delta, rope_theta=theta, rank=m, oversample=p, power_iters=q,
+                       omega=omega, u_out=u, v_out=v, workspace=ws,
+                       cond_layer_stride=T * D, canon_layer_stride=T * D)
+    torch.cuda.synchronize()
+    return _bits(u), _bits(v)
+
+
+def residuals(delta_f64, u_bits, v_bits, m):
+    from oracle import bf16_bits_to_f64, round_to_bf16_bits, svd_patch, eckart_young_tail
+    out = []
+    for l in range(delta_f64.shape[0]):
+        dl = delta_f64[l]
+        got = np.sum((dl - bf16_bits_to_f64(u_bits[l]) @ bf16_bits_to_f64(v_bits[l]).T) ** 2)
+        uo, vo = svd_patch(dl, m)
+        ref = np.sum((dl - bf16_bits_to_f64(round_to_bf16_bits(uo)) @ bf16_bits_to_f64(round_to_bf16_bits(vo)).T) ** 2)
+        out.append((got, ref, eckart_young_tail(dl, m), np.sum(dl ** 2)))
+    return out
+
+
+@pytest.mark.parametrize("kind,L,T,D,rot,m,p,q,true_rank", [
+    ("heads", 2, 300, 256, 128, 16, 8, 2, 12),     # keys of 2 heads x 128, ragged token count
+    ("none", 2, 257, 512, 0, 32, 16, 2, 40),       # values, truncation below the true rank
+    ("mla", 1, 200, 576, 64, 32, 16, 1, 24),       # MLA row, k_rope turned
+    ("heads", 1, 96, 128, 64, 48, 48, 2, 30),      # head_dim 64, widest range finder (96 columns)
+    ("heads", 2, 101, 200, 100, 16, 8, 2, 10),     # layer size not a multiple of 64 elements
+    ("none", 3, 1000, 1024, 0, 32, 16, 2, 48),     # split-K products (1000 tokens), 3 layers
+])
+def test_patch_form_matches_exact_svd(kind, L, T, D, rot, m, p, q, true_rank):
+    delta, theta = 4321, 1e6
+    canon, cond = make_case(11 + T, L, T, D, kind, rot, delta, theta, true_rank)
+    u, v = form_on_gpu(canon, cond, kind, rot, delta, theta, m, p, q)
+    dl = oracle_delta(canon, cond, kind, rot, delta, theta)
+    for got, ref, tail, total in residuals(dl, u, v, m):
+        print(f"residual gpu {got:.4e} exact-bf16 {ref:.4e} tail {tail:.4e} total {total:.4e}")
+        assert got <= 1.05 * ref + 1e-9 * total, (got, ref, tail)
+        assert got < 0.1 * total           # the patch removes most of the deficit
+
+
+def test_formed_patch_recovers_the_conditioned_cache():
+    """End to end: form U_m V_m^T for K and V from (KV(B|A), KV(B|empty)), then
+    reuse the canonical cache through kv_relocate_patch with those factors.
+    The result must be as close to KV(B|A) as the oracle's operator with the
+    exact SVD factors (both rounded to bf16), and far closer than blind reuse."""
+    import position_invariant_kv_gb300 as kvrp
+    from oracle import bf16_bits_to_f64, operator_rows, round_to_bf16_bits, svd_patch
+    L, T, H, d, m = 2, 384, 2, 128, 16
+    D = H * d
+    delta, theta = -777, 1e6
+    cases = {"k": ("heads", d, 21), "v": ("none", 0, 22)}
+    data = {}
+    for n, (kind, rot, seed) in cases.items():
+        canon, cond = make_case(seed, L, T, D, kind, rot, delta, theta, 10, scale=0.2)
+        u, v = form_on_gpu(canon, cond, kind, rot, delta, theta, m, 16, 2, seed=seed)
+        data[n] = (canon, cond, u, v)
+    pools = {n: torch.empty((L, T // 16, 16, D), dtype=torch.bfloat16, device="cuda") for n in "kv"}
+    dsts = {n: kvrp.Dst(base=pools[n], num_pages=T // 16, layer_stride=T * D) for n in "kv"}
+    kvrp.kv_relocate_patch(_dev(data["k"][0]), _dev(data["v"][0]), n_layers=L, n_tokens=T, n_kv_heads=H,
+                           head_dim=d, delta=delta, rope_theta=theta, k_dst=dsts["k"], v_dst=dsts["v"], rank=m,
+                           uk=_dev(data["k"][2]), vk=_dev(data["k"][3]), uv=_dev(data["v"][2]),
+                           vv=_dev(data["v"][3]), src_layer_stride=T * D, u_layer_stride=T * m,
+                           v_layer_stride=D * m)
+    torch.cuda.synchronize()
+    for n, (kind, rot, _) in cases.items():
+        canon, cond, _, _ = data[n]
+        got = bf16_bits_to_f64(_bits(pools[n]).reshape(L, T, D))
+        want = bf16_bits_to_f64(cond)
+        blind = oracle_delta(canon, cond, kind, rot, delta, theta)
+        lay = layout_of(kind, D, rot)
+        for l in range(L):
+            uo, vo = svd_patch(blind[l], m)
+            ref = bf16_bits_to_f64(round_to_bf16_bits(operator_rows(
+                canon[l], round_to_bf16_bits(uo), round_to_bf16_bits(vo), delta, theta, lay)))
+            e_gpu = np.linalg.norm(got[l] - want[l])
+            e_ref = np.linalg.norm(ref - want[l])
+            e_blind = np.linalg.norm(blind[l])
+            print(n, l, "error: formed patch", e_gpu, "exact SVD", e_ref, "blind reuse", e_blind)
+            assert e_gpu <= 1.03 * e_ref
+            assert e_gpu < 0.1 * e_blind
+
+
+def test_patch_form_rejects_bad_arguments():
+    import position_invariant_kv_gb300 as kvrp
+    x = torch.zeros((1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    om = torch.zeros((128, 200), device="cuda")
+    u = torch.empty((1, 64, 100), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((1, 128, 100), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvrp.KvrpError) as e:     # rank + oversample beyond the solver's 96 columns
+        kvrp.kv_patch_form(x, x, n_layers=1, n_tokens=64, row_width=128, rope_kind=kvrp.KVRP_ROPE_HEADS,
+                           rot_dim=128, delta=1, rope_theta=1e4, rank=64, oversample=40, power_iters=1,
+                           omega=om, u_out=u, v_out=v, workspace=ws)
+    assert e.value.status == kvrp.KVRP_ERR_UNSUPPORTED
+    with pytest.raises(kvrp.KvrpError) as e:     # workspace too small
+        kvrp.kv_patch_form(x, x, n_layers=1, n_tokens=64, row_width=128, rope_kind=kvrp.KVRP_ROPE_HEADS,
+                           rot_dim=128, delta=1, rope_theta=1e4, rank=16, oversample=8, power_iters=1,
+                           omega=om, u_out=u, v_out=v, workspace=ws, workspace_bytes=64)
+    assert e.value.status == kvrp.KVRP_ERR_WORKSPACE
+
+
+def test_zero_deficit_gives_a_zero_patch():
+    """KV(B|A) equal to the relocated canonical cache: the deficit is (almost)
+    zero and so is the patch."""
+    from oracle import bf16_bits_to_f64
+    canon, cond = make_case(31, 1, 128, 256, "none", 0, 0, 1e4, 4, noise=0.0)
+    u, v = form_on_gpu(canon, canon, "none", 0, 0, 1e4, 16, 8, 1)
+    assert np.max(np.abs(bf16_bits_to_f64(u)[0] @ bf16_bits_to_f64(v)[0].T)) < 1e-6
