@@ -235,7 +235,7 @@ kvrp_status kv_relocate_batch_noalloc(
  *               row_width a multiple of rot_dim);
  *               KVRP_ROPE_NONE: nothing turns (values; rot_dim, delta, theta unused);
  *               KVRP_ROPE_MLA_TAIL: the last rot_dim features turn (MLA k_rope).
- *               rot_dim: a multiple of 4, at most 128.
+ *               rot_dim: a multiple of 4, at most 128.  row_width: a multiple of 4.
  *   delta, rope_theta  the position shift and the RoPE base, as in kv_relocate_patch.
  *   rank, oversample  m >= 1 and the range finder's extra columns p >= 0;
  *               m + p <= 96, m <= min(n_tokens, row_width).
@@ -248,8 +248,13 @@ kvrp_status kv_relocate_batch_noalloc(
  *   workspace   device scratch of at least kv_patch_form_workspace_size(...)
  *               bytes, owned by the caller, busy until the call's work on
  *               `stream` completes (no two overlapping calls may share it).
- * Base pointers must be 16-byte aligned.  Precision: Delta and the tall products in
- * fp32, the small k x k problems in fp64, factors rounded once to bf16.
+ *   d_status    optional device word; KVRP_DEV_TIMEOUT is OR-ed in if a
+ *               pipeline wait of the tensor-core passes gave up (results invalid).
+ * Base pointers must be 16-byte aligned.  Precision: Delta is stored in bf16
+ * (rows and transposed rows), the passes over it are bf16 x bf16 tensor-core
+ * products accumulated in fp32; Gram matrices, the k x k solves (shifted
+ * Cholesky QR, Jacobi) and the small products run in fp32; factors are rounded
+ * once to bf16.
  * Errors: INVALID_ARG, ALIGNMENT, UNSUPPORTED (sizes beyond the limits above)
  * and WORKSPACE are returned before any CUDA work is queued; CUDA if a launch
  * fails.  Asynchronous on `stream`; the result is an approximation of the
@@ -269,7 +274,28 @@ kvrp_status kv_patch_form(
     int32_t rope_kind, int32_t rot_dim, int64_t delta, double rope_theta,
     int32_t rank, int32_t oversample, int32_t power_iters, const float* omega,
     void* u_out, void* v_out, int64_t u_layer_stride, int64_t v_layer_stride,
-    void* workspace, size_t workspace_bytes, kvrp_stream_t stream);
+    void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream);
+
+/*
+ * Orbit patch (Kamera, section 3, reordering bullet: one patch, averaged over
+ * the orderings of a cached set, serves every ordering).  Same as
+ * kv_patch_form, with n_orbit conditioned caches KV(B|A_pi), each in its own
+ * destination frame delta_pi, and the deficit averaged before the factorisation:
+ *     Delta = (1/n) sum_pi [KV(B|A_pi) - R(delta_pi) KV(B|empty)].
+ *   conditioned  host array of n_orbit device pointers (bf16, layout and
+ *                layer stride as `conditioned` of kv_patch_form), only read.
+ *   deltas       host array of the n_orbit position shifts.
+ *   n_orbit      1..64 (UNSUPPORTED beyond).  n_orbit = 1 is kv_patch_form.
+ * Other arguments, errors and precision as kv_patch_form.
+ */
+kvrp_status kv_patch_form_orbit(
+    const void* const* conditioned, const int64_t* deltas, int32_t n_orbit,
+    const void* canonical, int64_t cond_layer_stride, int64_t canon_layer_stride,
+    int32_t n_layers, int32_t n_tokens, int32_t row_width,
+    int32_t rope_kind, int32_t rot_dim, double rope_theta,
+    int32_t rank, int32_t oversample, int32_t power_iters, const float* omega,
+    void* u_out, void* v_out, int64_t u_layer_stride, int64_t v_layer_stride,
+    void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* kvrp_status_string(kvrp_status status);

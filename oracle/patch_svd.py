@@ -34,3 +34,17 @@ def conditioning_deficit(cond_rows: np.ndarray, canon_rows: np.ndarray, delta, t
     MLA: only k_rope turned), exactly as the reuse operator applies it."""
     from .kamera import apply_relocation
     return np.asarray(cond_rows, dtype=np.float64) - apply_relocation(canon_rows, delta, theta, layout, sections)
+
+
+def orbit_deficit(cond_rows_list, canon_rows: np.ndarray, deltas, theta: float, layout,
+                  sections=None) -> np.ndarray:
+    """Deficit of the orbit patch (Kamera, section 3, reordering bullet: one
+    patch averaged over the orderings of a cached set): the mean over the
+    orderings pi of KV(B|A_pi) - R(delta_pi) KV(B|empty), each deficit taken in
+    its own destination frame delta_pi."""
+    if len(cond_rows_list) != len(deltas) or not len(deltas):
+        raise ValueError("one delta per conditioned cache, at least one")
+    total = np.zeros(np.shape(canon_rows), dtype=np.float64)
+    for cond_rows, delta in zip(cond_rows_list, deltas):
+        total += conditioning_deficit(cond_rows, canon_rows, delta, theta, layout, sections)
+    return total / len(deltas)

@@ -21,7 +21,7 @@ KVRP_DEV_TIMEOUT = 0x2
 EXPORTED_SYMBOLS = (
     "kv_relocate_patch", "kv_relocate_patch_mrope", "kv_relocate_patch_mla", "kv_relocate_batch",
     "kv_relocate_batch_workspace_size", "kv_relocate_batch_noalloc", "kv_patch_form_workspace_size",
-    "kv_patch_form", "kvrp_status_string",
+    "kv_patch_form", "kv_patch_form_orbit", "kvrp_status_string",
     "kvrp_last_error", "kvrp_version",
 )
 KVRP_NOALLOC_MAX_CHUNKS = 256
@@ -82,7 +82,12 @@ def _load_library():
     L.kv_patch_form.argtypes = [
         C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_int32,
         C.c_int64, C.c_double, C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p,
-        C.c_int64, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p]
+        C.c_int64, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
+    L.kv_patch_form_orbit.restype = st
+    L.kv_patch_form_orbit.argtypes = [
+        C.POINTER(C.c_void_p), C.POINTER(C.c_int64), C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_int32,
+        C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
+        C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
     L.kvrp_status_string.restype = C.c_char_p
     L.kvrp_status_string.argtypes = [C.c_int]
     L.kvrp_last_error.restype = C.c_char_p
@@ -271,7 +276,7 @@ def kv_patch_form(conditioned, canonical, *, n_layers: int, n_tokens: int, row_w
                   rot_dim: int, delta: int, rope_theta: float, rank: int, oversample: int, power_iters: int,
                   omega, u_out, v_out, workspace, cond_layer_stride: int = 0, canon_layer_stride: int = 0,
                   u_layer_stride: int = 0, v_layer_stride: int = 0, workspace_bytes: Optional[int] = None,
-                  stream=None) -> None:
+                  d_status=None, stream=None) -> None:
     """Rank-m factors of Delta = conditioned - R(delta) canonical, per layer (bf16 U_m, V_m)."""
     if workspace_bytes is None:
         workspace_bytes = int(workspace.numel() * workspace.element_size())
@@ -279,4 +284,24 @@ def kv_patch_form(conditioned, canonical, *, n_layers: int, n_tokens: int, row_w
         _ptr(conditioned), _ptr(canonical), int(cond_layer_stride), int(canon_layer_stride), int(n_layers),
         int(n_tokens), int(row_width), int(rope_kind), int(rot_dim), int(delta), float(rope_theta), int(rank),
         int(oversample), int(power_iters), _ptr(omega), _ptr(u_out), _ptr(v_out), int(u_layer_stride),
-        int(v_layer_stride), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+        int(v_layer_stride), _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))
+
+
+def kv_patch_form_orbit(conditioned, deltas, canonical, *, n_layers: int, n_tokens: int, row_width: int,
+                        rope_kind: int, rot_dim: int, rope_theta: float, rank: int, oversample: int,
+                        power_iters: int, omega, u_out, v_out, workspace, cond_layer_stride: int = 0,
+                        canon_layer_stride: int = 0, u_layer_stride: int = 0, v_layer_stride: int = 0,
+                        workspace_bytes: Optional[int] = None, d_status=None, stream=None) -> None:
+    """Orbit patch: factors of mean_pi [conditioned_pi - R(delta_pi) canonical], per layer."""
+    n = len(conditioned)
+    if len(deltas) != n:
+        raise ValueError("one delta per conditioned cache")
+    ptrs = (C.c_void_p * max(n, 1))(*[_ptr(c) for c in conditioned])
+    ds = (C.c_int64 * max(n, 1))(*[int(d) for d in deltas])
+    if workspace_bytes is None:
+        workspace_bytes = int(workspace.numel() * workspace.element_size())
+    _check(lib().kv_patch_form_orbit(
+        ptrs, ds, n, _ptr(canonical), int(cond_layer_stride), int(canon_layer_stride), int(n_layers),
+        int(n_tokens), int(row_width), int(rope_kind), int(rot_dim), float(rope_theta), int(rank),
+        int(oversample), int(power_iters), _ptr(omega), _ptr(u_out), _ptr(v_out), int(u_layer_stride),
+        int(v_layer_stride), _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))

@@ -5,26 +5,41 @@
 // top-m factors of the deficit come from an SVD.  Here the deficit is taken in
 // the destination frame, Delta = KV(B|A) - R(delta) KV(B|empty), so that
 // R(delta) KV(B|empty) + U_m V_m^T reproduces KV(B|A) up to the truncation.
-// Singular values are folded into U_m, and the factors land in bf16 in the
-// layout kv_relocate_patch reads.
+// The orbit patch (same page, section 3, reordering bullet) averages the
+// deficit over the orderings pi of a cached set before the factorisation:
+//   Delta = mean_pi [KV(B|A_pi) - R(delta_pi) KV(B|empty)]
+//         = mean_pi KV(B|A_pi) - Rbar KV(B|empty),
+// Rbar being the mean of the rotations, itself a per-pair 2x2 matrix of the
+// rotate-half form (mean cosine, mean sine), so the canonical cache is read once.
 //
-// Method (all in this file's kernels, every layer of a call batched):
-//   1. Delta in fp32 from the two bf16 caches (R(delta) with the split table);
-//   2. randomized range finder: Y = Delta Omega (Omega: caller's Gaussian test
-//      matrix), q power iterations Y <- Delta orth(Delta^T orth(Y));
-//   3. Q = orth(Y) by two rounds of Cholesky QR (Gram in fp32, factor in fp64);
-//   4. B = Q^T Delta and C = B B^T;
-//   5. C = U_B Lambda U_B^T by parallel cyclic Jacobi in fp64 (one CTA);
-//   6. V_m = B^T U_B[:, :m] with unit columns, U_m = Delta V_m (singular
-//      values land in U_m).
-// The tall products are tiled fp32 CUDA-core GEMMs: patch formation runs once
-// per chunk, off the relocation hot path.
+// Method (every layer of a call batched in each launch):
+//   1. Delta from the bf16 caches, stored in bf16 twice: rows [T][D] and
+//      transposed [D][T], so that every product below reads a K-major operand;
+//   2. randomized range finder: Y = Delta Omega (Omega: the caller's Gaussian
+//      test matrix), q subspace iterations Y <- Delta orth(Delta^T orth(Y));
+//   3. Q = orth(Y);  B^T = Delta^T Q;  C = B B^T (k x k);
+//   4. C = U_B Lambda U_B^T by parallel cyclic Jacobi; W = U_B[:, :m] Lambda_m^(-1/2);
+//   5. V_m = orth(B^T W) (orthonormal right factors), U_m = Delta V_m.
+// orth() is shifted Cholesky QR: X <- X R^-1 with R^T R = X^T X + s I, the
+// shift s a small multiple of trace(X^T X) (one round inside the subspace
+// iterations, two for the final basis).
+//
+// The passes over Delta (steps 2, 3 and 5: 2q + 3 of them) are the bulk of the
+// work: tall-skinny products with k <= 96 columns, run on the tensor cores by
+// pass_kernel (TMA-staged bf16 tiles, tcgen05.mma into a TMEM accumulator,
+// fp32 results).  The skinny operands are rounded to bf16 for these products;
+// everything else -- the Gram matrices, the k x k solves, the small
+// right-multiplies -- stays in fp32 on the CUDA cores (tall_kernel and the
+// one-CTA-per-layer solvers).
+#include <cudaTypedefs.h>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <cmath>
-#include <vector>
+#include <mutex>
 
 #include "kvrp.h"
 #include "kvrp_plan.h"
@@ -32,436 +47,1042 @@
 namespace kvrp {
 namespace pf {
 
-constexpr int kMaxK = 96;            // rank + oversampling bound (Jacobi works in shared memory)
-constexpr int kJacobiSweeps = 20;
-constexpr double kCholShift = 1e-6;  // Cholesky QR shift, relative to trace(G) (fp32 Gram)
+constexpr int kMaxK = 96;          // rank + oversampling bound (k x k solves live in shared memory)
+constexpr int kMaxOrbit = 64;      // conditioned caches averaged by one call
+constexpr int kJacobiSweeps = 3;   // the top-m subspace has settled by then (V_m is re-orthonormalised)
+constexpr int kThreads = 256;
+constexpr int kTile = 128;         // output rows per CTA (tall_kernel, pass_kernel)
+constexpr int kStep = 32;          // tall_kernel: contraction step per pipeline stage
+constexpr int kStages = 3;         // tall_kernel pipeline depth
+constexpr int kPassStages = 3;     // pass_kernel pipeline depth
+constexpr int kPassK = 64;         // pass_kernel: contraction per stage (one 128-byte swizzle row of bf16)
+constexpr int kPassThreads = 192;  // producer warp, MMA warp, four epilogue warps
+constexpr int kDeltaTokens = 64;   // tokens per delta_kernel tile
+constexpr float kShiftFirst = 1e-5f;    // Cholesky QR shift / trace: a basis of unknown conditioning
+constexpr float kShiftSecond = 1e-7f;   // a basis already close to orthonormal
+constexpr long long kTimeoutCycles = 1ll << 31;   // bounded waits: ~1 s
 
 struct TableParam {
   float4 v[kTablePairs];
 };
 
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+__device__ __forceinline__ uint16_t f_to_bf16(float v) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(v);
+  return *reinterpret_cast<const uint16_t*>(&b);
+}
+
 // ---------------------------------------------------------------------------
-// 1. Delta = conditioned - R(delta) canonical, fp32
+// 1. Delta = mean_pi cond_pi - Rbar canonical, written as bf16 rows [T][Dp]
+//    and bf16 transposed rows [D][Tp].  A CTA takes 64 tokens of one layer and
+//    one segment of the row (a rotated head, the rotated MLA tail, or up to 128
+//    unrotated features), staged in shared memory for the transposed write.
 // ---------------------------------------------------------------------------
 struct DeltaArgs {
-  const uint16_t* cond;
+  const uint16_t* cond[kMaxOrbit];
   const uint16_t* canon;
-  int64_t cond_stride, canon_stride;   // elements between layers
-  float* out;                          // layer l at out + l * out_stride, rows [T][D]
-  int64_t out_stride;
-  int T, D;
-  int rope_kind;                       // KVRP_ROPE_*
-  int rot_dim;                         // rotated head width (heads) or tail width (MLA)
+  uint16_t* out;       // [L][T][Dp]
+  uint16_t* out_t;     // [L][D][Tp]
+  int64_t cond_stride, canon_stride;   // elements between layers of the inputs
+  int n_cond, T, D, Dp, Tp, rope_kind, rot_dim;
+  float inv_n;
 };
 
-__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+// Segment sg of a row: unrotated features [0, plain_end) in 128-wide pieces,
+// then the rotated heads (or the rotated MLA tail).
+struct Segment {
+  int f0, W;
+  bool turns;
+};
+__host__ __device__ inline int plain_end_of(int rope_kind, int D, int rot) {
+  return rope_kind == KVRP_ROPE_MLA_TAIL ? D - rot : (rope_kind == KVRP_ROPE_NONE ? D : 0);
+}
+__host__ __device__ inline int segment_count(int rope_kind, int D, int rot) {
+  const int n_plain = (plain_end_of(rope_kind, D, rot) + 127) / 128;
+  const int n_rot = rope_kind == KVRP_ROPE_HEADS ? D / rot : (rope_kind == KVRP_ROPE_MLA_TAIL ? 1 : 0);
+  return n_plain + n_rot;
+}
+__device__ inline Segment segment_of(int sg, int rope_kind, int D, int rot) {
+  const int pe = plain_end_of(rope_kind, D, rot);
+  const int n_plain = (pe + 127) / 128;
+  Segment s;
+  s.turns = sg >= n_plain;
+  s.f0 = s.turns ? pe + (sg - n_plain) * rot : sg * 128;
+  s.W = s.turns ? rot : min(128, pe - s.f0);
+  return s;
+}
 
-__global__ void __launch_bounds__(256) delta_kernel(DeltaArgs a, const __grid_constant__ TableParam tab) {
-  const int t = blockIdx.x;
-  const int l = blockIdx.y;
-  const uint16_t* c = a.cond + (int64_t)l * a.cond_stride + (int64_t)t * a.D;
-  const uint16_t* x = a.canon + (int64_t)l * a.canon_stride + (int64_t)t * a.D;
-  float* o = a.out + (int64_t)l * a.out_stride + (int64_t)t * a.D;
-  const int half = a.rot_dim / 2;
-  const int rot_from = a.rope_kind == KVRP_ROPE_MLA_TAIL ? a.D - a.rot_dim : 0;
-  for (int f = threadIdx.x; f < a.D / 2; f += blockDim.x) {
-    // f indexes a pair of output elements (e0, e1) and, when they turn, the pair index i
-    int e0, e1, i = -1;
-    if (a.rope_kind == KVRP_ROPE_HEADS) {
-      const int h = f / half;
-      i = f % half;
-      e0 = h * a.rot_dim + i;
-      e1 = e0 + half;
-    } else if (a.rope_kind == KVRP_ROPE_MLA_TAIL && 2 * f >= rot_from) {
-      i = f - rot_from / 2;
-      e0 = rot_from + i;
-      e1 = e0 + half;
-    } else {
-      e0 = 2 * f;
-      e1 = e0 + 1;
+constexpr int kDeltaUnroll = 8;   // work units per thread per batch of loads
+
+__global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__ DeltaArgs a,
+                                                          const __grid_constant__ TableParam tab) {
+  __shared__ float4 tb[kTablePairs];
+  __shared__ float tile[128][kDeltaTokens + 1];
+  for (int i = threadIdx.x; i < kTablePairs; i += blockDim.x) tb[i] = tab.v[i];
+  const int l = blockIdx.z;
+  const int t0 = blockIdx.x * kDeltaTokens;
+  const Segment sg = segment_of(blockIdx.y, a.rope_kind, a.D, a.rot_dim);
+  uint16_t* out = a.out + (int64_t)l * a.T * a.Dp;
+  uint16_t* out_t = a.out_t + (int64_t)l * a.D * a.Tp;
+  __syncthreads();
+  const int upt = sg.W / 4;                           // work units per token
+  const int half = sg.W / 2;
+  const int n_units = kDeltaTokens * upt;
+  for (int u0 = 0; u0 < n_units; u0 += kDeltaUnroll * kThreads) {
+    // batch of units: issue every load first, then compute
+    float2 x0[kDeltaUnroll], x1[kDeltaUnroll], c0[kDeltaUnroll], c1[kDeltaUnroll];
+    int e0s[kDeltaUnroll], e1s[kDeltaUnroll], tls[kDeltaUnroll];
+#pragma unroll
+    for (int b = 0; b < kDeltaUnroll; ++b) {
+      const int u = u0 + b * kThreads + threadIdx.x;
+      const int tl = u / upt, w = u - (u / upt) * upt;
+      const bool live = u < n_units && t0 + tl < a.T;
+      const int e0 = sg.turns ? 2 * w : 4 * w;
+      const int e1 = sg.turns ? 2 * w + half : 4 * w + 2;
+      e0s[b] = e0; e1s[b] = e1; tls[b] = live ? tl : -1;
+      x0[b] = x1[b] = c0[b] = c1[b] = make_float2(0.f, 0.f);
+      if (!live) continue;
+      const int64_t row = (int64_t)(t0 + tl) * a.D + sg.f0;
+      const uint16_t* x = a.canon + (int64_t)l * a.canon_stride + row;
+      x0[b] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(x + e0));   // (x_i, x_i+1)
+      x1[b] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(x + e1));   // their partners
+      for (int p = 0; p < a.n_cond; ++p) {
+        const uint16_t* c = a.cond[p] + (int64_t)l * a.cond_stride + row;
+        const float2 v0 = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(c + e0));
+        const float2 v1 = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(c + e1));
+        c0[b].x += v0.x; c0[b].y += v0.y; c1[b].x += v1.x; c1[b].y += v1.y;
+      }
     }
-    const float x0 = bf16f(x[e0]), x1 = bf16f(x[e1]);
-    float y0 = x0, y1 = x1;
-    if (i >= 0) {
-      const float4 hd = tab.v[2 * (i >> 1)];
-      const float4 tl = tab.v[2 * (i >> 1) + 1];
-      const float C = (i & 1) ? hd.y : hd.x, S = (i & 1) ? hd.w : hd.z;
-      const float Cl = (i & 1) ? tl.y : tl.x, Sl = (i & 1) ? tl.w : tl.z;
-      y0 = fmaf(x0, C, -(x1 * S)) + fmaf(x0, Cl, -(x1 * Sl));
-      y1 = fmaf(x1, C, x0 * S) + fmaf(x1, Cl, x0 * Sl);
+#pragma unroll
+    for (int b = 0; b < kDeltaUnroll; ++b) {
+      const int tl = tls[b];
+      if (tl < 0) continue;
+      const int e0 = e0s[b], e1 = e1s[b];
+      float2 y0 = x0[b], y1 = x1[b];
+      if (sg.turns) {
+        const float4 hd = tb[e0], tl4 = tb[e0 + 1];   // pairs i, i+1 (i = e0): {C_i, C_i+1, S_i, S_i+1}, then tails
+        y0.x = fmaf(x0[b].x, hd.x, -(x1[b].x * hd.z)) + fmaf(x0[b].x, tl4.x, -(x1[b].x * tl4.z));
+        y0.y = fmaf(x0[b].y, hd.y, -(x1[b].y * hd.w)) + fmaf(x0[b].y, tl4.y, -(x1[b].y * tl4.w));
+        y1.x = fmaf(x1[b].x, hd.x, x0[b].x * hd.z) + fmaf(x1[b].x, tl4.x, x0[b].x * tl4.z);
+        y1.y = fmaf(x1[b].y, hd.y, x0[b].y * hd.w) + fmaf(x1[b].y, tl4.y, x0[b].y * tl4.w);
+      }
+      const float d00 = c0[b].x * a.inv_n - y0.x, d01 = c0[b].y * a.inv_n - y0.y;
+      const float d10 = c1[b].x * a.inv_n - y1.x, d11 = c1[b].y * a.inv_n - y1.y;
+      uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
+      *reinterpret_cast<uint32_t*>(o + e0) = f2_to_bf16x2(d00, d01);
+      *reinterpret_cast<uint32_t*>(o + e1) = f2_to_bf16x2(d10, d11);
+      tile[e0][tl] = d00; tile[e0 + 1][tl] = d01; tile[e1][tl] = d10; tile[e1 + 1][tl] = d11;
     }
-    o[e0] = bf16f(c[e0]) - y0;
-    o[e1] = bf16f(c[e1]) - y1;
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < sg.W * (kDeltaTokens / 2); it += blockDim.x) {   // transposed rows
+    const int f = it / (kDeltaTokens / 2), tp = 2 * (it - (it / (kDeltaTokens / 2)) * (kDeltaTokens / 2));
+    const int t = t0 + tp;
+    if (t >= a.T) continue;
+    // a token past T lands in the row's padding (Tp >= T + 1), never read back
+    *reinterpret_cast<uint32_t*>(out_t + (int64_t)(sg.f0 + f) * a.Tp + t) = f2_to_bf16x2(tile[f][tp], tile[f][tp + 1]);
   }
 }
 
 // ---------------------------------------------------------------------------
-// 2. Batched fp32 GEMM, C = op(A) op(B), 64 x 64 tiles, optional split-K
+// PTX wrappers (mbarrier, TMA, tcgen05)
 // ---------------------------------------------------------------------------
-struct GemmArgs {
-  const float* A;
-  const float* B;
-  float* C;
-  int M, N, K;
-  int lda, ldb, ldc;
-  int64_t sA, sB, sC;   // batch strides (elements); 0 shares a matrix across the batch
-  int tA, tB;           // A stored [K][M] / B stored [N][K]
-  int splits;           // > 1: partial products are added into a zeroed C
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `bar` with the given parity: gives up when
+// another role has flagged an abort or after ~1 s (then flags one itself).
+__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      *abort_flag = 1;
+      if (status) atomicOr(status, KVRP_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+// 16 consecutive fp32 TMEM columns of this warp's 32 lanes, completed in the same statement
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Shared-memory matrix descriptor: K-major operand staged by a 128-byte
+// swizzled TMA box (rows of 64 bf16 = 128 B, 8-row atoms 1024 B apart).
+__device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address
+  d |= (uint64_t)1 << 16;                      // leading byte offset (unused: K stays inside the atom)
+  d |= (uint64_t)(1024 >> 4) << 32;            // stride byte offset: next 8-row atom
+  d |= (uint64_t)1 << 46;                      // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;                      // layout: 128-byte swizzle
+  return d;
+}
+// Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16_f32(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------
+// 2. pass_kernel: out[l][r][c] = sum_k A[l][r][k] B[l][c][k] for r < M, c < kp,
+//    A and B bf16 K-major (tensor maps with 128-byte swizzled boxes {64, 128}
+//    and {64, kp}), fp32 out [L][M][kp].  One CTA per (128-row tile, layer):
+//    warp 0 streams the stages with TMA, warp 1 owns the TMEM accumulator and
+//    issues tcgen05.mma (M 128, N kp, K 16), warps 2-5 drain TMEM to global.
+//    Every wait is bounded; a timeout sets KVRP_DEV_TIMEOUT in *status.
+// ---------------------------------------------------------------------------
+struct PassArgs {
+  float* out;
+  int64_t sO;         // out layer stride (elements)
+  int M, K, kp;
+  int b_layered;      // B has one matrix per layer (else layer 0 for all)
+  uint32_t* status;
 };
 
-__global__ void __launch_bounds__(256) gemm_f32(GemmArgs g) {
-  const int z = blockIdx.z / g.splits;
-  const int split = blockIdx.z % g.splits;
-  const float* A = g.A + z * g.sA;
-  const float* B = g.B + z * g.sB;
-  float* C = g.C + z * g.sC;
-  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-  const int kchunk = ((g.K + g.splits - 1) / g.splits + 15) / 16 * 16;
-  const int kb = split * kchunk;
-  const int ke = min(g.K, kb + kchunk);
-  __shared__ float As[16][68];
-  __shared__ float Bs[16][68];
-  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
-  float acc[4][4] = {};
-  for (int k0 = kb; k0 < ke; k0 += 16) {
-    for (int e = threadIdx.x; e < 1024; e += 256) {
-      int mm, kk;
-      if (g.tA) { mm = e & 63; kk = e >> 6; } else { kk = e & 15; mm = e >> 4; }
-      const int gm = m0 + mm, gk = k0 + kk;
-      float v = 0.f;
-      if (gm < g.M && gk < ke) v = g.tA ? A[(int64_t)gk * g.lda + gm] : A[(int64_t)gm * g.lda + gk];
-      As[kk][mm] = v;
-      int nn, kk2;
-      if (g.tB) { kk2 = e & 15; nn = e >> 4; } else { nn = e & 63; kk2 = e >> 6; }
-      const int gn = n0 + nn, gk2 = k0 + kk2;
-      float w = 0.f;
-      if (gn < g.N && gk2 < ke) w = g.tB ? B[(int64_t)gn * g.ldb + gk2] : B[(int64_t)gk2 * g.ldb + gn];
-      Bs[kk2][nn] = w;
+__global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_constant__ CUtensorMap map_a,
+                                                                const __grid_constant__ CUtensorMap map_b,
+                                                                PassArgs a) {
+  extern __shared__ __align__(1024) uint8_t smp[];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  const uint32_t base = (smem_u32(smp) + 1023u) & ~1023u;
+  const uint32_t a_bytes = kTile * kPassK * 2;                 // 16 KiB
+  const uint32_t b_bytes = (uint32_t)a.kp * kPassK * 2;        // kp rows of 128 B (a multiple of 1 KiB)
+  const uint32_t stage_bytes = a_bytes + b_bytes;
+  const uint32_t bars = base + kPassStages * stage_bytes;
+  auto full = [&](int s) { return bars + 8u * s; };
+  auto empty = [&](int s) { return bars + 8u * (kPassStages + s); };
+  const uint32_t acc_bar = bars + 16u * kPassStages;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ncols = a.kp <= 32 ? 32u : a.kp <= 64 ? 64u : 128u;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPassStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
     }
-    __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
+    mbar_init(acc_bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const int l = blockIdx.y;
+  const int m0 = blockIdx.x * kTile;
+  const int nk = (a.K + kPassK - 1) / kPassK;
+  volatile int* abort_p = &abort_flag;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      const int lb = a.b_layered ? l : 0;
+      int issued = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        const int st = kb % kPassStages;
+        if (kb >= kPassStages && !wait_phase(empty(st), ((kb / kPassStages) - 1) & 1, abort_p, a.status)) break;
+        const uint32_t sa = base + st * stage_bytes;
+        mbar_expect_tx(full(st), stage_bytes);
+        tma_load_3d(sa, &map_a, full(st), kb * kPassK, m0, l);
+        tma_load_3d(sa + a_bytes, &map_b, full(st), kb * kPassK, 0, lb);
+        ++issued;
+      }
+      // every issued copy must land before the CTA may exit
+      for (int kb = max(0, issued - kPassStages); kb < issued; ++kb)
+        wait_phase(full(kb % kPassStages), (kb / kPassStages) & 1, abort_p, a.status);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(a.kp);
+      for (int kb = 0; kb < nk; ++kb) {
+        const int st = kb % kPassStages;
+        if (!wait_phase(full(st), (kb / kPassStages) & 1, abort_p, a.status)) break;
+        tc_fence_after();
+        const uint32_t sa = base + st * stage_bytes;
+#pragma unroll
+        for (int j = 0; j < kPassK / 16; ++j)
+          mma_bf16(tmem, desc_k_sw128(sa + 32u * j), desc_k_sw128(sa + a_bytes + 32u * j), idesc,
+                   (kb | j) != 0 ? 1u : 0u);
+        mma_commit(empty(st));   // the stage is free once these MMAs have read it
+      }
+      mma_commit(acc_bar);       // arrives when every MMA issued above has completed
+      wait_phase(acc_bar, 0, abort_p, a.status);
+    }
+  } else {
+    // tcgen05.ld is warp-collective: the whole warp loads or none of it
+    const bool ok = __all_sync(0xffffffffu, wait_phase(acc_bar, 0, abort_p, a.status));
+    tc_fence_after();
+    const int quarter = warp & 3;              // TMEM lanes this warp may read
+    const int row = quarter * 32 + lane;
+    if (ok && nk > 0) {
+      float* o = a.out + (int64_t)l * a.sO + (int64_t)(m0 + row) * a.kp;
+      for (int c0 = 0; c0 < a.kp; c0 += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+        if (m0 + row < a.M) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(o + c0 + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. tall_kernel: out[r][c] = sum_s A(r, s) X[s][c] for c < 8 CN, fp32 on the
+//    CUDA cores, batched over layers (blockIdx.z).  Rows mode: A(r, s) =
+//    A[r * lda + s]; cols mode: A(r, s) = A[s * lda + r] (the product with A
+//    transposed).  X is [S][ldx].  One CTA owns 128 output rows and one slice
+//    of the contraction; several slices (blockIdx.y) add into a zeroed output
+//    with float2 atomics.  With out_t set (one slice only) the result is
+//    written instead as bf16 transposed rows out_t[c][r].
+// ---------------------------------------------------------------------------
+struct TallArgs {
+  const float* A;
+  const float* X;
+  float* out;
+  uint16_t* out_t;
+  int64_t sA, sX, sO, sT;  // per-layer strides (elements); sX = 0 shares X
+  int lda, ldx, ldo, ldt;
+  int R, S;                // output rows; contraction length
+  int s_per_split;         // multiple of kStep
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// rows mode: A tile [128 rows][32 s], row pitch 36; cols mode: [32 s][128 r], pitch 132
+__host__ __device__ constexpr int a_pitch(bool cols) { return cols ? kTile + 4 : kStep + 4; }
+__host__ __device__ constexpr int a_floats(bool cols) { return cols ? kStep * a_pitch(true) : kTile * a_pitch(false); }
+constexpr size_t tall_smem_bytes(int cn, bool cols) {
+  return sizeof(float) * kStages * (a_floats(cols) + kStep * 8 * cn);
+}
+
+template <int CN, bool kCols>
+__global__ void __launch_bounds__(kThreads, 2) tall_kernel(TallArgs g) {
+  constexpr int KP = 8 * CN;                        // columns of X and out
+  constexpr int AP = a_pitch(kCols);
+  constexpr int AF = a_floats(kCols);
+  constexpr int XF = kStep * KP;
+  extern __shared__ __align__(16) float sm[];
+  const int l = blockIdx.z;
+  const float* A = g.A + (int64_t)l * g.sA;
+  const float* X = g.X + (int64_t)l * g.sX;
+  const int r0 = blockIdx.x * kTile;
+  const int s_begin = blockIdx.y * g.s_per_split;
+  const int s_end = min(g.S, s_begin + g.s_per_split);
+  const int n_steps = s_end > s_begin ? (s_end - s_begin + kStep - 1) / kStep : 0;
+  const int tid = threadIdx.x;
+  const int cg = tid & 7, rg = tid >> 3;
+
+  auto load = [&](int slot, int step) {
+    float* As = sm + slot * (AF + XF);
+    float* Xs = As + AF;
+    const int s0 = s_begin + step * kStep;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {                   // 1024 16-byte chunks of A
+      const int ch = tid + j * kThreads;
+      if (!kCols) {
+        const int row = ch >> 3, s4 = (ch & 7) * 4;
+        const bool ok = r0 + row < g.R && s0 + s4 < s_end;
+        cp_async16(As + row * AP + s4, ok ? A + (int64_t)(r0 + row) * g.lda + s0 + s4 : A, ok);
+      } else {
+        const int s = ch >> 5, r4 = (ch & 31) * 4;
+        const bool ok = s0 + s < s_end && r0 + r4 < g.R;
+        cp_async16(As + s * AP + r4, ok ? A + (int64_t)(s0 + s) * g.lda + r0 + r4 : A, ok);
+      }
+    }
+    for (int ch = tid; ch < kStep * KP / 4; ch += kThreads) {   // X rows s0 .. s0+31
+      const int s = ch / (KP / 4), c4 = (ch % (KP / 4)) * 4;
+      const bool ok = s0 + s < s_end;
+      cp_async16(Xs + s * KP + c4, ok ? X + (int64_t)(s0 + s) * g.ldx + c4 : X, ok);
+    }
+  };
+
+  float2 acc[4][CN / 2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < CN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
+
+#pragma unroll
+  for (int st = 0; st < kStages - 1; ++st) {
+    if (st < n_steps) load(st, st);
+    cp_async_commit();
+  }
+  for (int it = 0; it < n_steps; ++it) {
+    cp_async_wait<kStages - 2>();
+    __syncthreads();
+    if (it + kStages - 1 < n_steps) load((it + kStages - 1) % kStages, it + kStages - 1);
+    cp_async_commit();
+    const float* As = sm + (it % kStages) * (AF + XF);
+    const float* Xs = As + AF;
+    if (!kCols) {
+      // thread rows rg + 32 i: per warp quarter four rows one apart -> distinct bank groups
+#pragma unroll
+      for (int s4 = 0; s4 < kStep; s4 += 4) {
+        float4 av[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4*>(As + (rg + 32 * i) * AP + s4);
+#pragma unroll
+        for (int ss = 0; ss < 4; ++ss) {
+          float2 x[CN / 2];
+#pragma unroll
+          for (int j = 0; j < CN / 2; ++j)
+            x[j] = *reinterpret_cast<const float2*>(Xs + (s4 + ss) * KP + cg * CN + 2 * j);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float v = ss == 0 ? av[i].x : ss == 1 ? av[i].y : ss == 2 ? av[i].z : av[i].w;
+            const float2 v2 = make_float2(v, v);
+#pragma unroll
+            for (int j = 0; j < CN / 2; ++j) acc[i][j] = __ffma2_rn(v2, x[j], acc[i][j]);
+          }
+        }
+      }
+    } else {
+      // thread rows 4 rg + i: one float4 of A per contraction index
+#pragma unroll 8
+      for (int s = 0; s < kStep; ++s) {
+        const float4 av = *reinterpret_cast<const float4*>(As + s * AP + 4 * rg);
+        float2 x[CN / 2];
+#pragma unroll
+        for (int j = 0; j < CN / 2; ++j) x[j] = *reinterpret_cast<const float2*>(Xs + s * KP + cg * CN + 2 * j);
+        const float a4[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 v2 = make_float2(a4[i], a4[i]);
+#pragma unroll
+          for (int j = 0; j < CN / 2; ++j) acc[i][j] = __ffma2_rn(v2, x[j], acc[i][j]);
+        }
+      }
+    }
+  }
+  cp_async_wait<0>();
+  const bool split = gridDim.y > 1;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int gm = m0 + ty * 4 + i;
-    if (gm >= g.M) continue;
+    const int r = r0 + (kCols ? 4 * rg + i : rg + 32 * i);
+    if (r >= g.R) continue;
+    if (g.out_t) {
+      uint16_t* ot = g.out_t + (int64_t)l * g.sT + r;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int gn = n0 + tx * 4 + j;
-      if (gn >= g.N) continue;
-      if (g.splits > 1) atomicAdd(&C[(int64_t)gm * g.ldc + gn], acc[i][j]);
-      else C[(int64_t)gm * g.ldc + gn] = acc[i][j];
+      for (int j = 0; j < CN / 2; ++j) {
+        ot[(int64_t)(cg * CN + 2 * j) * g.ldt] = f_to_bf16(acc[i][j].x);
+        ot[(int64_t)(cg * CN + 2 * j + 1) * g.ldt] = f_to_bf16(acc[i][j].y);
+      }
+    } else {
+      float* o = g.out + (int64_t)l * g.sO + (int64_t)r * g.ldo + cg * CN;
+#pragma unroll
+      for (int j = 0; j < CN / 2; ++j) {
+        if (split) atomicAdd(reinterpret_cast<float2*>(o + 2 * j), acc[i][j]);
+        else *reinterpret_cast<float2*>(o + 2 * j) = acc[i][j];
+      }
     }
   }
 }
 
+// Sum of one value per thread over the CTA (blockDim.x == kThreads); `scratch`
+// holds kThreads / 32 floats.  Every thread gets the total.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) t += scratch[w];
+  __syncthreads();
+  return t;
+}
+
 // ---------------------------------------------------------------------------
-// 3. Cholesky QR step: from the Gram matrix G = X^T X (k x k), R^-1 with
-//    G = R^T R (R upper), in fp64.  One CTA per batch entry.
+// 4. Shifted Cholesky of a Gram matrix and the inverse of its factor, fp32,
+//    one CTA per layer:  R^T R = G + s I (s = rel * trace G), out = R^-1,
+//    zero outside the leading k x k block.
+//    Factorisation: right-looking, one barrier per column j; threads form a
+//    16 x 16 grid over the trailing block and load everything they need for
+//    the step before they store (no load waits behind a store).  Row j of R
+//    goes to Rt (transposed), which nothing reads during the factorisation.
+//    Inverse: row i of X = R^-1 solves x R = e_i by forward substitution,
+//    x_j = (delta_ij - sum_{l<j} x_l R_lj) / R_jj, one thread per row; all
+//    threads walk j together, so R_lj = Rt[j][l] is a broadcast read.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) chol_inverse_kernel(const float* G, float* Rinv, int k) {
-  extern __shared__ double sm[];
-  double* R = sm;              // k x k
-  double* X = sm + k * k;      // k x k
-  __shared__ double shift;
-  const float* g = G + (int64_t)blockIdx.x * k * k;
-  float* out = Rinv + (int64_t)blockIdx.x * k * k;
-  for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
-    const int i = e / k, j = e % k;
-    R[e] = 0.5 * ((double)g[i * k + j] + (double)g[j * k + i]);
-  }
+template <int KP>
+__global__ void __launch_bounds__(kThreads) chol_inverse_kernel(const float* G, int64_t sG, float* Rinv, int64_t sR,
+                                                                 int k, float rel) {
+  constexpr int kp = KP;
+  constexpr int kCholSpan = KP / 16;    // rows (and columns) of the trailing block per thread
+  extern __shared__ __align__(16) float smc[];
+  constexpr int P = kp + 1;
+  float* A = smc;              // trailing matrix
+  float* Rt = smc + kp * P;    // R transposed: Rt[c][j] = R[j][c]
+  float* X = smc + 2 * kp * P; // R^-1, one row per thread
+  __shared__ float scratch[kThreads / 32];
+  __shared__ float rdiag[kMaxK];
+  const float* g = G + (int64_t)blockIdx.x * sG;
+  float* out = Rinv + (int64_t)blockIdx.x * sR;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float tr = 0.f;
+  for (int i = ty; i < kp; i += 16)
+    for (int j = tx; j < kp; j += 16) {
+      const float v = (i < k && j < k) ? 0.5f * (g[i * kp + j] + g[j * kp + i]) : 0.f;
+      A[i * P + j] = v;
+      Rt[i * P + j] = 0.f;
+      if (i == j) tr += v;
+    }
+  tr = block_sum(tr, scratch);
+  const float shift = tr > 0.f ? rel * tr : 1e-30f;
+  if (tid < k) A[tid * P + tid] += shift;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    double tr = 0.0;
-    for (int i = 0; i < k; ++i) tr += R[i * k + i];
-    // Shifted Cholesky QR: G + s I with s well above the fp32 rounding of G keeps
-    // the factorisation defined for a rank-deficient X; directions of X far
-    // below sqrt(s) are damped instead of amplified, and the second round
-    // restores orthonormality on the directions that carry signal.
-    shift = tr > 0.0 ? kCholShift * tr : 1e-30;
-  }
-  __syncthreads();
-  if (threadIdx.x < k) R[threadIdx.x * k + threadIdx.x] += shift;
-  __syncthreads();
-  // right-looking Cholesky, row j of R per step
   for (int j = 0; j < k; ++j) {
-    if (threadIdx.x == 0) {
-      double d = R[j * k + j];
-      for (int i = 0; i < j; ++i) d -= R[i * k + j] * R[i * k + j];
-      R[j * k + j] = sqrt(d > shift ? d : shift);
+    const float d = fmaxf(A[j * P + j], shift);   // row j of A is final after the previous step
+    const float rs = rsqrtf(d);                   // 1 / R_jj
+    const float inv2 = rs * rs;
+    if (tid < k - j) {
+      const float v = tid == 0 ? d * rs : A[j * P + j + tid] * rs;
+      Rt[(j + tid) * P + j] = v;
+      if (tid == 0) rdiag[j] = rs;
     }
-    __syncthreads();
-    for (int c = j + 1 + threadIdx.x; c < k; c += blockDim.x) {
-      double v = R[j * k + c];
-      for (int i = 0; i < j; ++i) v -= R[i * k + j] * R[i * k + c];
-      R[j * k + c] = v / R[j * k + j];
+    float ajr[kCholSpan], ajc[kCholSpan], old[kCholSpan][kCholSpan];
+#pragma unroll
+    for (int a = 0; a < kCholSpan; ++a) {
+      const int r = j + 1 + ty + 16 * a, c = j + 1 + tx + 16 * a;
+      ajr[a] = r < k ? A[j * P + r] * inv2 : 0.f;
+      ajc[a] = c < k ? A[j * P + c] : 0.f;
     }
+#pragma unroll
+    for (int a = 0; a < kCholSpan; ++a)
+#pragma unroll
+      for (int b = 0; b < kCholSpan; ++b) {
+        const int r = j + 1 + ty + 16 * a, c = j + 1 + tx + 16 * b;
+        old[a][b] = (r < k && c < k && c >= r) ? A[r * P + c] : 0.f;
+      }
+#pragma unroll
+    for (int a = 0; a < kCholSpan; ++a)
+#pragma unroll
+      for (int b = 0; b < kCholSpan; ++b) {
+        const int r = j + 1 + ty + 16 * a, c = j + 1 + tx + 16 * b;
+        if (r < k && c < k && c >= r) A[r * P + c] = old[a][b] - ajr[a] * ajc[b];
+      }
     __syncthreads();
   }
-  // X = R^-1 (upper triangular), one column per thread, back substitution
-  for (int c = threadIdx.x; c < k; c += blockDim.x) {
-    for (int i = k - 1; i >= 0; --i) {
-      double v = (i == c) ? 1.0 : 0.0;
-      if (i > c) v = 0.0;
-      else
-        for (int j = i + 1; j <= c; ++j) v -= R[i * k + j] * X[j * k + c];
-      X[i * k + c] = (i > c) ? 0.0 : v / R[i * k + i];
+  if (tid < kp) {
+    const int i = tid;
+    float* xi = X + i * P;
+    for (int j = 0; j < kp; ++j) {
+      float s4[4] = {(i == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
+      const float* rj = Rt + j * P;
+      int l = 0;
+      for (; l + 3 < j; l += 4) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) s4[u] = fmaf(-xi[l + u], rj[l + u], s4[u]);
+      }
+      for (; l < j; ++l) s4[0] = fmaf(-xi[l], rj[l], s4[0]);
+      xi[j] = (i < k && j < k && j >= i) ? ((s4[0] + s4[1]) + (s4[2] + s4[3])) * rdiag[j] : 0.f;
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < k * k; e += blockDim.x) out[e] = (float)X[e];
+  for (int i = ty; i < kp; i += 16)
+    for (int j = tx; j < kp; j += 16) out[i * kp + j] = X[i * P + j];
 }
 
 // ---------------------------------------------------------------------------
 // 5. Symmetric eigenproblem C = U L U^T by parallel cyclic Jacobi (round-robin
-//    pairing: n/2 disjoint rotations per step), fp64, one CTA per entry.
-//    Writes the eigenvectors of the m largest eigenvalues, W = U[:, top m]
-//    (k x m, descending).
+//    pairing: n/2 disjoint rotations per step), fp32, one CTA per layer.  A
+//    step applies A <- J^T A J as independent 2 x 2 blocks (rows of one pair
+//    against columns of another; blocks on or above the diagonal, mirrored),
+//    so each thread updates whole blocks with no barrier between the row and
+//    column halves of the rotations.  Writes W [kp][kp]: column r < m is the
+//    eigenvector of the r-th largest eigenvalue scaled by lambda^(-1/2) (zero
+//    where lambda vanishes); other columns zero.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) jacobi_kernel(const float* Cm, float* W, int k, int m) {
-  extern __shared__ double sm[];
-  double* A = sm;                 // k x k
-  double* V = sm + k * k;         // k x k
-  __shared__ double cs_c[kMaxK / 2 + 1], cs_s[kMaxK / 2 + 1];
-  __shared__ int pp[kMaxK / 2 + 1], qq[kMaxK / 2 + 1];
-  __shared__ int idx[kMaxK + 1];
+__global__ void __launch_bounds__(kThreads) jacobi_kernel(const float* Cm, int64_t sC, float* W, int64_t sW, int k,
+                                                           int kp, int m) {
+  extern __shared__ __align__(16) float smj[];
+  const int P = kp + 1;
+  float* A = smj;
+  float* V = smj + kp * P;
+  __shared__ int4 rot[kMaxK / 2];      // {p, q, cos, sin} of each pair of the step
   __shared__ int order[kMaxK];
-  __shared__ double red[256];
-  __shared__ int done;
-  __shared__ double floor_abs;
-  const float* c = Cm + (int64_t)blockIdx.x * k * k;
-  float* w = W + (int64_t)blockIdx.x * k * m;
-  const int n2 = k + (k & 1);
-  for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
-    const int i = e / k, j = e % k;
-    A[e] = 0.5 * ((double)c[i * k + j] + (double)c[j * k + i]);
-    V[e] = (i == j) ? 1.0 : 0.0;
+  __shared__ float scratch[kThreads / 32];
+  __shared__ int rotated;
+  const float* c = Cm + (int64_t)blockIdx.x * sC;
+  float* w = W + (int64_t)blockIdx.x * sW;
+  const int tid = threadIdx.x;
+  float ss = 0.f;
+  for (int e = tid; e < kp * kp; e += kThreads) {
+    const int i = e / kp, j = e - (e / kp) * kp;
+    const float v = (i < k && j < k) ? 0.5f * (c[i * kp + j] + c[j * kp + i]) : 0.f;
+    A[i * P + j] = v;
+    V[i * P + j] = i == j ? 1.f : 0.f;
+    ss += v * v;
   }
-  for (int i = threadIdx.x; i < n2; i += blockDim.x) idx[i] = i;
-  __syncthreads();
-  {  // entries below 1e-15 ||C||_F are rounding noise of the fp32 input
-    double ss = 0.0;
-    for (int e = threadIdx.x; e < k * k; e += blockDim.x) ss += A[e] * A[e];
-    red[threadIdx.x] = ss;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      double t = 0.0;
-      for (int i = 0; i < blockDim.x; ++i) t += red[i];
-      floor_abs = 1e-15 * sqrt(t);
-    }
-    __syncthreads();
+  // entries below floor_abs are rounding noise of the fp32 input
+  const float floor_abs = 1e-6f * sqrtf(block_sum(ss, scratch));
+  const int n2 = k + (k & 1);      // index k (< kp when k is odd) is a dummy that never turns
+  const int np = n2 / 2;
+  // this thread's 2 x 2 blocks (t1 <= t2), the same at every step
+  constexpr int kMaxBlk = ((kMaxK / 2) * (kMaxK / 2 + 1) / 2 + kThreads - 1) / kThreads;
+  int blk[kMaxBlk];
+  int nb = 0;
+  {
+    int idx = 0;
+    for (int t1 = 0; t1 < np; ++t1)
+      for (int t2 = t1; t2 < np; ++t2, ++idx)
+        if (idx % kThreads == tid && nb < kMaxBlk) blk[nb++] = (t1 << 8) | t2;
   }
+  // eigenvector rows: thread -> row vj, pairs vh, vh + H, ...
+  const int H = max(1, kThreads / k);
+  const int vj = tid % k, vh = tid / k;
   for (int sweep = 0; sweep < kJacobiSweeps; ++sweep) {
-    // stop once every off-diagonal entry is negligible next to its diagonal pair
-    double mx = 0.0;
-    for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
-      const int i = e / k, j = e % k;
-      if (i == j || fabs(A[e]) <= floor_abs) continue;
-      const double r = fabs(A[e]) / sqrt(fabs(A[i * k + i] * A[j * k + j]) + 1e-300);
-      mx = r > mx ? r : mx;
-    }
-    red[threadIdx.x] = mx;
+    if (tid == 0) rotated = 0;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      double r = 0.0;
-      for (int t = 0; t < blockDim.x; ++t) r = red[t] > r ? red[t] : r;
-      done = r <= 1e-14;
-    }
-    __syncthreads();
-    if (done) break;
     for (int step = 0; step < n2 - 1; ++step) {
-      const int np = n2 / 2;
-      if (threadIdx.x < np) {
-        int p = idx[threadIdx.x], q = idx[n2 - 1 - threadIdx.x];
-        if (p > q) { const int t = p; p = q; q = t; }
-        double cc = 1.0, ss = 0.0;
+      if (tid < np) {
+        // circle method: player n2-1 stays, the others move one seat per step
+        int p = tid == 0 ? n2 - 1 : (step + tid) % (n2 - 1);
+        int q = tid == 0 ? step : (step - tid + n2 - 1) % (n2 - 1);
+        if (p > q) { const int x = p; p = q; q = x; }
+        float cc = 1.f, s = 0.f;
         if (q < k) {
-          const double apq = A[p * k + q];
-          if (fabs(apq) > floor_abs && fabs(apq) > 1e-16 * sqrt(fabs(A[p * k + p] * A[q * k + q]))) {
-            const double th = (A[q * k + q] - A[p * k + p]) / (2.0 * apq);
-            const double t = fabs(th) < 1e150 ? ((th >= 0 ? 1.0 : -1.0) / (fabs(th) + sqrt(th * th + 1.0))) : 0.5 / th;
-            cc = 1.0 / sqrt(t * t + 1.0);
-            ss = t * cc;
+          const float apq = A[p * P + q];
+          const float app = A[p * P + p], aqq = A[q * P + q];
+          // Any angle gives an exact orthogonal update, so approximate reciprocals
+          // and square roots only affect how fast the sweep converges.
+          // |a_pq| below 1e-4 sqrt(a_pp a_qq) moves an eigenvector by ~1e-4: the
+          // orthonormalisation of B^T W that follows absorbs that
+          if (fabsf(apq) > floor_abs && apq * apq > 1e-8f * fabsf(app * aqq)) {
+            const float th = __fdividef(aqq - app, 2.f * apq);
+            const float r2 = fmaf(th, th, 1.f);
+            const float tt = copysignf(__frcp_rn(fabsf(th) + r2 * rsqrtf(r2)), th);
+            cc = rsqrtf(fmaf(tt, tt, 1.f));
+            s = tt * cc;
+            if (s != 0.f) rotated = 1;
           }
         }
-        pp[threadIdx.x] = p;
-        qq[threadIdx.x] = q;
-        cs_c[threadIdx.x] = cc;
-        cs_s[threadIdx.x] = ss;
+        rot[tid] = make_int4(p, q, __float_as_int(cc), __float_as_int(s));
       }
       __syncthreads();
-      for (int e = threadIdx.x; e < np * k; e += blockDim.x) {   // rows p, q
-        const int t = e / k, j = e % k;
-        const int p = pp[t], q = qq[t];
-        if (q >= k) continue;
-        const double cc = cs_c[t], ss = cs_s[t];
-        const double ap = A[p * k + j], aq = A[q * k + j];
-        A[p * k + j] = cc * ap - ss * aq;
-        A[q * k + j] = ss * ap + cc * aq;
+#pragma unroll
+      for (int u = 0; u < kMaxBlk; ++u) {
+        if (u >= nb) break;
+        const int t1 = blk[u] >> 8, t2 = blk[u] & 0xFF;
+        const int4 r1 = rot[t1], r2 = rot[t2];
+        const float s1 = __int_as_float(r1.w), s2 = __int_as_float(r2.w);
+        if (s1 == 0.f && s2 == 0.f) continue;
+        const float c1 = __int_as_float(r1.z), c2 = __int_as_float(r2.z);
+        const int p1 = r1.x, q1 = r1.y, p2 = r2.x, q2 = r2.y;
+        const float a = A[p1 * P + p2], b = A[p1 * P + q2], cq = A[q1 * P + p2], d = A[q1 * P + q2];
+        // rows: [p1; q1] <- [c1 -s1; s1 c1] [p1; q1]
+        const float ra = c1 * a - s1 * cq, rb = c1 * b - s1 * d;
+        const float rc = s1 * a + c1 * cq, rd = s1 * b + c1 * d;
+        // columns: [p2 q2] <- [p2 q2] [c2 s2; -s2 c2]
+        float na = c2 * ra - s2 * rb, nb2 = s2 * ra + c2 * rb;
+        float nc = c2 * rc - s2 * rd, nd = s2 * rc + c2 * rd;
+        if (t1 == t2) {
+          if (s1 != 0.f) { nb2 = 0.f; nc = 0.f; }   // the rotation annihilates a_pq
+          A[p1 * P + p2] = na; A[p1 * P + q2] = nb2; A[q1 * P + p2] = nc; A[q1 * P + q2] = nd;
+        } else {
+          A[p1 * P + p2] = na; A[p1 * P + q2] = nb2; A[q1 * P + p2] = nc; A[q1 * P + q2] = nd;
+          A[p2 * P + p1] = na; A[q2 * P + p1] = nb2; A[p2 * P + q1] = nc; A[q2 * P + q1] = nd;
+        }
       }
-      __syncthreads();
-      for (int e = threadIdx.x; e < np * k; e += blockDim.x) {   // columns p, q and eigenvectors
-        const int t = e / k, j = e % k;
-        const int p = pp[t], q = qq[t];
-        if (q >= k) continue;
-        const double cc = cs_c[t], ss = cs_s[t];
-        const double ap = A[j * k + p], aq = A[j * k + q];
-        A[j * k + p] = cc * ap - ss * aq;
-        A[j * k + q] = ss * ap + cc * aq;
-        const double vp = V[j * k + p], vq = V[j * k + q];
-        V[j * k + p] = cc * vp - ss * vq;
-        V[j * k + q] = ss * vp + cc * vq;
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {   // next round of the tournament: keep idx[0], rotate the rest
-        const int last = idx[n2 - 1];
-        for (int i = n2 - 1; i > 1; --i) idx[i] = idx[i - 1];
-        idx[1] = last;
+      if (vh < H) {   // V <- V J on row vj
+        for (int t = vh; t < np; t += H) {
+          const int4 r = rot[t];
+          const float s = __int_as_float(r.w);
+          if (s == 0.f) continue;
+          const float cc = __int_as_float(r.z);
+          const float vp = V[vj * P + r.x], vq = V[vj * P + r.y];
+          V[vj * P + r.x] = cc * vp - s * vq;
+          V[vj * P + r.y] = s * vp + cc * vq;
+        }
       }
       __syncthreads();
     }
+    if (!rotated) break;
+    __syncthreads();
   }
-  if (threadIdx.x == 0) {   // indices of the m largest eigenvalues, descending
-    for (int j = 0; j < k; ++j) order[j] = j;
-    for (int a = 0; a < m; ++a) {
-      int best = a;
-      for (int b = a + 1; b < k; ++b)
-        if (A[order[b] * k + order[b]] > A[order[best] * k + order[best]]) best = b;
-      const int t = order[a]; order[a] = order[best]; order[best] = t;
+  // descending order by rank counting (ties by index)
+  if (tid < k) {
+    const float li = A[tid * P + tid];
+    int rank = 0;
+    for (int j = 0; j < k; ++j) {
+      const float lj = A[j * P + j];
+      rank += (lj > li) || (lj == li && j < tid);
     }
+    order[rank] = tid;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < k * m; e += blockDim.x) {
-    const int i = e / m, j = e % m;
-    w[i * m + j] = (float)V[i * k + order[j]];
-  }
-}
-
-// ---------------------------------------------------------------------------
-// 6a. V_m = B^T U_B has columns of norm sqrt(lambda_j); scale each to unit
-//     length from its own computed norm (not from lambda, whose fp32 rounding
-//     can be far off for a vanishing eigenvalue).  A zero column stays zero.
-//     One CTA per layer.
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) normalise_columns_kernel(float* Vm, int64_t stride, int rows, int m) {
-  __shared__ double part[256];
-  __shared__ float scale[kMaxK];
-  float* v = Vm + (int64_t)blockIdx.x * stride;
-  for (int j = 0; j < m; ++j) {
-    double ss = 0.0;
-    for (int r = threadIdx.x; r < rows; r += blockDim.x) ss += (double)v[(int64_t)r * m + j] * v[(int64_t)r * m + j];
-    part[threadIdx.x] = ss;
-    __syncthreads();
-    for (int h = blockDim.x / 2; h > 0; h >>= 1) {
-      if (threadIdx.x < h) part[threadIdx.x] += part[threadIdx.x + h];
-      __syncthreads();
+  const float lmax = fmaxf(A[order[0] * P + order[0]], 0.f);
+  for (int e = tid; e < kp * kp; e += kThreads) {
+    const int i = e / kp, r = e - (e / kp) * kp;
+    float v = 0.f;
+    if (i < k && r < m && r < k) {
+      const int o = order[r];
+      const float lam = A[o * P + o];
+      if (lam > 1e-10f * lmax && lam > 0.f) v = V[i * P + o] * rsqrtf(lam);
     }
-    if (threadIdx.x == 0) scale[j] = part[0] > 0.0 ? (float)(1.0 / sqrt(part[0])) : 0.f;
-    __syncthreads();
+    w[e] = v;
   }
-  for (int64_t e = threadIdx.x; e < (int64_t)rows * m; e += blockDim.x) v[e] *= scale[e % m];
 }
 
 // ---------------------------------------------------------------------------
-// 6. fp32 -> bf16 factors in the caller's layout
+// 6. Small helpers: Omega^T in bf16, the caller's factors in bf16
 // ---------------------------------------------------------------------------
-__global__ void to_bf16_kernel(const float* src, int64_t src_stride, uint16_t* dst, int64_t dst_stride,
-                               int64_t n_per_layer) {
+// dst [kp][Dp] bf16 = Omega^T, zero beyond the k columns of Omega [D][k]
+__global__ void omega_t_kernel(const float* src, int D, int k, uint16_t* dst, int kp, int Dp) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < kp * D; e += gridDim.x * blockDim.x) {
+    const int c = e / D, f = e - (e / D) * D;
+    dst[(int64_t)c * Dp + f] = f_to_bf16(c < k ? src[(int64_t)f * k + c] : 0.f);
+  }
+}
+// u_out[l][t][c] = bf16(U[l][t][c]) for c < m, from fp32 [L][T][kp]
+__global__ void u_out_kernel(const float* src, int64_t src_stride, int kp, uint16_t* dst, int64_t dst_stride, int rows,
+                             int m) {
   const int l = blockIdx.y;
-  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n_per_layer;
-       e += (int64_t)gridDim.x * blockDim.x) {
-    const __nv_bfloat16 b = __float2bfloat16_rn(src[l * src_stride + e]);
-    dst[l * dst_stride + e] = *reinterpret_cast<const uint16_t*>(&b);
+  const int64_t n = (int64_t)rows * m;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = e / m;
+    const int c = (int)(e - r * m);
+    dst[l * dst_stride + e] = f_to_bf16(src[l * src_stride + r * kp + c]);
+  }
+}
+// v_out[l][f][c] = V^T[l][c][f] for c < m, from bf16 [L][kp][ld]
+__global__ void v_out_kernel(const uint16_t* src, int64_t src_stride, int ld, uint16_t* dst, int64_t dst_stride, int D,
+                             int m) {
+  const int l = blockIdx.y;
+  const int64_t n = (int64_t)D * m;
+  for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t f = e / m;
+    const int c = (int)(e - f * m);
+    dst[l * dst_stride + e] = src[l * src_stride + (int64_t)c * ld + f];
   }
 }
 
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
+int64_t round8(int64_t v) { return (v + 7) / 8 * 8; }
+int pad16(int k) { return (k + 15) / 16 * 16; }
+
 struct Buffers {
-  float *delta, *y, *y2, *z, *z2, *b, *g, *rinv, *c, *w, *vf, *uf;
-  int64_t s_delta, s_tk, s_dk, s_kd, s_kk, s_km, s_dm, s_tm;
+  uint16_t *delta, *delta_t, *st_t, *st_d, *omega_t;   // bf16
+  float *y, *y2, *z, *z2, *g, *rinv, *w;               // fp32
+  int64_t Dp, Tp, s_delta, s_delta_t, s_st_t, s_st_d, s_tk, s_dk, s_kk;
   size_t bytes;
 };
 
-size_t round64(size_t v) { return (v + 63) / 64 * 64; }
-
-Buffers layout(float* base, int L, int T, int D, int k, int m) {
+Buffers layout(uint8_t* base, int L, int T, int D, int kp) {
   Buffers b;
-  b.s_delta = (int64_t)round64((size_t)T * D);
-  b.s_tk = (int64_t)round64((size_t)T * k);
-  b.s_dk = (int64_t)round64((size_t)D * k);
-  b.s_kd = (int64_t)round64((size_t)k * D);
-  b.s_kk = (int64_t)round64((size_t)k * k);
-  b.s_km = (int64_t)round64((size_t)k * m);
-  b.s_dm = (int64_t)round64((size_t)D * m);
-  b.s_tm = (int64_t)round64((size_t)T * m);
-  float* p = base;
-  auto take = [&](int64_t stride) {
-    float* q = p;
-    p += stride * L;
-    return q;
+  b.Dp = round8(D);
+  b.Tp = round8(T + 1);   // room for the odd-token pad of the transposed writes
+  b.s_delta = (int64_t)T * b.Dp;
+  b.s_delta_t = (int64_t)D * b.Tp;
+  b.s_st_t = (int64_t)kp * b.Tp;
+  b.s_st_d = (int64_t)kp * b.Dp;
+  b.s_tk = (int64_t)T * kp;
+  b.s_dk = (int64_t)D * kp;
+  b.s_kk = (int64_t)kp * kp;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = (off + bytes + 1023) / 1024 * 1024;
+    return base + o;
   };
-  b.delta = take(b.s_delta);
-  b.y = take(b.s_tk);
-  b.y2 = take(b.s_tk);
-  b.z = take(b.s_dk);
-  b.z2 = take(b.s_dk);
-  b.b = take(b.s_kd);
-  b.g = take(b.s_kk);
-  b.rinv = take(b.s_kk);
-  b.c = take(b.s_kk);
-  b.w = take(b.s_km);
-  b.vf = take(b.s_dm);
-  b.uf = take(b.s_tm);
-  b.bytes = (size_t)(p - base) * sizeof(float);
+  b.delta = reinterpret_cast<uint16_t*>(take(2 * (size_t)b.s_delta * L));
+  b.delta_t = reinterpret_cast<uint16_t*>(take(2 * (size_t)b.s_delta_t * L));
+  b.st_t = reinterpret_cast<uint16_t*>(take(2 * (size_t)b.s_st_t * L));
+  b.st_d = reinterpret_cast<uint16_t*>(take(2 * (size_t)b.s_st_d * L));
+  b.omega_t = reinterpret_cast<uint16_t*>(take(2 * (size_t)b.s_st_d));
+  b.y = reinterpret_cast<float*>(take(4 * (size_t)b.s_tk * L));
+  b.y2 = reinterpret_cast<float*>(take(4 * (size_t)b.s_tk * L));
+  b.z = reinterpret_cast<float*>(take(4 * (size_t)b.s_dk * L));
+  b.z2 = reinterpret_cast<float*>(take(4 * (size_t)b.s_dk * L));
+  b.g = reinterpret_cast<float*>(take(4 * (size_t)b.s_kk * L));
+  b.rinv = reinterpret_cast<float*>(take(4 * (size_t)b.s_kk * L));
+  b.w = reinterpret_cast<float*>(take(4 * (size_t)b.s_kk * L));
+  b.bytes = off;
   return b;
 }
 
-cudaError_t gemm(cudaStream_t st, int L, const float* A, int64_t sA, int lda, int tA, const float* B, int64_t sB,
-                 int ldb, int tB, float* C, int64_t sC, int ldc, int M, int N, int K, int splits) {
-  GemmArgs g{A, B, C, M, N, K, lda, ldb, ldc, sA, sB, sC, tA, tB, splits};
-  if (splits > 1) {
-    for (int l = 0; l < L; ++l) {   // split-K partials are added into zeros
-      const cudaError_t e = cudaMemsetAsync(C + l * sC, 0, sizeof(float) * (size_t)M * ldc, st);
-      if (e != cudaSuccess) return e;
+// 16-significant-bit head of a value (its fp32 tail is value - head)
+float head16(double v) {
+  if (v == 0.0) return 0.0f;
+  int e = 0;
+  const double m = std::frexp(v, &e);
+  return static_cast<float>(std::ldexp(std::nearbyint(std::ldexp(m, 16)), e - 16));
+}
+
+// Mean rotation over the orbit: pair i holds (mean cos(delta_pi theta_i), mean sin(...)),
+// computed in fp64 and laid out like the relocation tables (two pairs per
+// float4: heads {C_i, C_i+1, S_i, S_i+1}, then the fp32 tails).
+void mean_table(const int64_t* deltas, int n, double theta, int rot_dim, float4* tab) {
+  float hc[kTablePairs] = {}, hs[kTablePairs] = {}, tc[kTablePairs] = {}, ts[kTablePairs] = {};
+  for (int i = 0; i < rot_dim / 2; ++i) {
+    const double inv = std::pow(theta, -2.0 * i / rot_dim);
+    double c = 0.0, s = 0.0;
+    for (int p = 0; p < n; ++p) {
+      const double phi = static_cast<double>(deltas[p]) * inv;
+      c += std::cos(phi);
+      s += std::sin(phi);
+    }
+    c /= n;
+    s /= n;
+    hc[i] = head16(c);
+    hs[i] = head16(s);
+    tc[i] = static_cast<float>(c - hc[i]);
+    ts[i] = static_cast<float>(s - hs[i]);
+  }
+  for (int j = 0; j < kTablePairs / 2; ++j) {
+    tab[2 * j] = make_float4(hc[2 * j], hc[2 * j + 1], hs[2 * j], hs[2 * j + 1]);
+    tab[2 * j + 1] = make_float4(tc[2 * j], tc[2 * j + 1], ts[2 * j], ts[2 * j + 1]);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// bf16 [layers][rows][K] with row pitch `ld` elements, boxes {64, box_rows}, 128-byte swizzle
+bool encode_kmajor(CUtensorMap* map, const uint16_t* base, int K, int rows, int layers, int64_t ld,
+                   int64_t layer_stride, int box_rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)layers};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld * 2, (cuuint64_t)layer_stride * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kPassK, (cuuint32_t)box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t pass_smem_bytes(int kp) { return 1024 + (size_t)kPassStages * (kTile * kPassK * 2 + kp * kPassK * 2) + 64; }
+
+class Runner {
+ public:
+  Runner(cudaStream_t st, int L, int kp, int sms, uint32_t* status)
+      : st_(st), L_(L), kp_(kp), sms_(sms), status_(status) {}
+  cudaError_t err = cudaSuccess;
+  bool map_fail = false;
+
+  // out[L][M][kp] fp32 = A[L][M][K] B[Lb][kp][K]^T on the tensor cores
+  void pass(const uint16_t* A, int64_t a_ld, int64_t a_stride, const uint16_t* B, int64_t b_ld, int64_t b_stride,
+            bool b_layered, float* out, int64_t sO, int M, int K) {
+    if (err != cudaSuccess || map_fail) return;
+    CUtensorMap ma, mb;
+    if (!encode_kmajor(&ma, A, K, M, L_, a_ld, a_stride, kTile) ||
+        !encode_kmajor(&mb, B, K, kp_, b_layered ? L_ : 1, b_ld, b_stride, kp_)) {
+      map_fail = true;
+      return;
+    }
+    PassArgs pa{out, sO, M, K, kp_, b_layered ? 1 : 0, status_};
+    pass_kernel<<<dim3((M + kTile - 1) / kTile, L_), kPassThreads, pass_smem_bytes(kp_), st_>>>(ma, mb, pa);
+    err = cudaGetLastError();
+  }
+
+  // out[L][R][kp] = A(R x S) X(S x kp) on the CUDA cores; cols: A is stored
+  // [S][lda] and read transposed.  out_t: bf16 transposed output instead.
+  void tall(bool cols, const float* A, int64_t sA, int lda, const float* X, int64_t sX, int ldx, float* out,
+            int64_t sO, int R, int S, uint16_t* out_t = nullptr, int64_t sT = 0, int ldt = 0) {
+    if (err != cudaSuccess) return;
+    const int tiles = (R + kTile - 1) / kTile;
+    // Contraction slices per output tile: each slice keeps >= 4 steps, and the
+    // CTA count should fill whole waves of the resident slots (2 per SM).
+    const int cap = 2 * sms_;
+    const int max_splits = out_t ? 1 : std::max(1, (S + 4 * kStep - 1) / (4 * kStep));
+    int splits = 1, per = S;
+    double best = -1.0;
+    for (int sp = 1; sp <= max_splits; ++sp) {
+      const int pr = ((S + sp - 1) / sp + kStep - 1) / kStep * kStep;
+      const int n = (S + pr - 1) / pr;
+      if (n != sp) continue;
+      const int64_t total = (int64_t)tiles * L_ * n;
+      const int64_t waves = (total + cap - 1) / cap;
+      // fraction of slot-time used, with a small preference for fewer atomics
+      const double score = (double)total / (double)(waves * cap) - 0.002 * n;
+      if (score > best + 1e-9) { best = score; splits = n; per = pr; }
+    }
+    if (splits > 1) {
+      err = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)(sO * (L_ - 1) + (int64_t)R * kp_), st_);
+      if (err != cudaSuccess) return;
+    }
+    TallArgs g{A, X, out, out_t, sA, sX, sO, sT, lda, ldx, kp_, ldt, R, S, per};
+    dim3 grid(tiles, splits, L_);
+    switch (kp_ / 8) {
+      case 2: launch<2>(cols, grid, g); break;
+      case 4: launch<4>(cols, grid, g); break;
+      case 6: launch<6>(cols, grid, g); break;
+      case 8: launch<8>(cols, grid, g); break;
+      case 10: launch<10>(cols, grid, g); break;
+      case 12: launch<12>(cols, grid, g); break;
+      default: err = cudaErrorInvalidValue;
     }
   }
-  dim3 grid((N + 63) / 64, (M + 63) / 64, L * splits);
-  gemm_f32<<<grid, 256, 0, st>>>(g);
-  return cudaGetLastError();
-}
 
-int splits_for(int K) { return K >= 2048 ? 16 : K >= 512 ? 4 : 1; }
-
-// X [rows x k] (batched) <- X R^-1, twice (Cholesky QR2); tmp is a buffer of X's shape.
-cudaError_t orthonormalise(cudaStream_t st, int L, float* X, float* tmp, int64_t sX, int rows, int k, float* g,
-                           float* rinv, int64_t s_kk) {
-  for (int round = 0; round < 2; ++round) {
-    cudaError_t e = gemm(st, L, X, sX, k, 1, X, sX, k, 0, g, s_kk, k, k, k, rows, splits_for(rows));
-    if (e != cudaSuccess) return e;
-    chol_inverse_kernel<<<L, 256, 2 * sizeof(double) * k * k, st>>>(g, rinv, k);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    e = gemm(st, L, X, sX, k, 0, rinv, s_kk, k, 0, tmp, sX, k, rows, k, k, 1);
-    if (e != cudaSuccess) return e;
-    e = cudaMemcpyAsync(X, tmp, sizeof(float) * (size_t)sX * L, cudaMemcpyDeviceToDevice, st);
-    if (e != cudaSuccess) return e;
+  // X [L][R][kp] <- orth(X) by rounds of shifted Cholesky QR (the first with
+  // shift `first`, later ones kShiftSecond); tmp has X's shape.  With out_t
+  // set, the last round writes bf16 X^T [kp][ldt] there instead of X.
+  void orth(float*& X, float*& tmp, int64_t sX, int R, int k, int rounds, float first, float* g, float* rinv,
+            uint16_t* out_t = nullptr, int64_t sT = 0, int ldt = 0) {
+    const int64_t skk = (int64_t)kp_ * kp_;
+    for (int r = 0; r < rounds && err == cudaSuccess; ++r) {
+      tall(true, X, sX, kp_, X, sX, kp_, g, skk, kp_, R);                      // G = X^T X
+      if (err != cudaSuccess) return;
+      chol(g, rinv, k, r == 0 ? first : kShiftSecond);
+      if (r == rounds - 1 && out_t) {
+        tall(false, X, sX, kp_, rinv, skk, kp_, nullptr, 0, R, kp_, out_t, sT, ldt);   // (X R^-1)^T in bf16
+      } else {
+        tall(false, X, sX, kp_, rinv, skk, kp_, tmp, sX, R, kp_);                     // X R^-1
+        std::swap(X, tmp);
+      }
+    }
   }
-  return cudaSuccess;
-}
+
+  size_t chol_smem() const { return sizeof(float) * 3 * (size_t)kp_ * (kp_ + 1); }
+
+  void chol(const float* g, float* rinv, int k, float rel) {
+    if (err != cudaSuccess) return;
+    const int64_t skk = (int64_t)kp_ * kp_;
+    switch (kp_) {
+      case 16: chol_inverse_kernel<16><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
+      case 32: chol_inverse_kernel<32><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
+      case 48: chol_inverse_kernel<48><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
+      case 64: chol_inverse_kernel<64><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
+      case 80: chol_inverse_kernel<80><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
+      case 96: chol_inverse_kernel<96><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
+      default: err = cudaErrorInvalidValue; return;
+    }
+    err = cudaGetLastError();
+  }
+  size_t jacobi_smem() const { return sizeof(float) * 2 * (size_t)kp_ * (kp_ + 1); }
+
+  static cudaError_t configure() {
+    cudaError_t e = cudaSuccess;
+    const int chol = (int)(sizeof(float) * 3 * kMaxK * (kMaxK + 1));
+    const int jac = (int)(sizeof(float) * 2 * kMaxK * (kMaxK + 1));
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, jac);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem_bytes(kMaxK));
+    if (e == cudaSuccess) e = set_tall<2>();
+    if (e == cudaSuccess) e = set_tall<4>();
+    if (e == cudaSuccess) e = set_tall<6>();
+    if (e == cudaSuccess) e = set_tall<8>();
+    if (e == cudaSuccess) e = set_tall<10>();
+    if (e == cudaSuccess) e = set_tall<12>();
+    return e;
+  }
+
+ private:
+  template <int CN>
+  static cudaError_t set_tall() {
+    cudaError_t e = cudaFuncSetAttribute(tall_kernel<CN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)tall_smem_bytes(CN, false));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tall_kernel<CN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)tall_smem_bytes(CN, true));
+    return e;
+  }
+  template <int CN>
+  void launch(bool cols, dim3 grid, const TallArgs& g) {
+    if (cols) tall_kernel<CN, true><<<grid, kThreads, tall_smem_bytes(CN, true), st_>>>(g);
+    else tall_kernel<CN, false><<<grid, kThreads, tall_smem_bytes(CN, false), st_>>>(g);
+    err = cudaGetLastError();
+  }
+  cudaStream_t st_;
+  int L_, kp_, sms_;
+  uint32_t* status_;
+};
 
 }  // namespace pf
 }  // namespace kvrp
@@ -473,23 +1094,31 @@ extern "C" {
 size_t kv_patch_form_workspace_size(int32_t n_layers, int32_t n_tokens, int32_t row_width, int32_t rank,
                                     int32_t oversample) {
   if (n_layers <= 0 || n_tokens <= 0 || row_width <= 0 || rank <= 0 || oversample < 0) return 0;
-  const int k = rank + oversample;
-  return pf::layout(nullptr, n_layers, n_tokens, row_width, k, rank).bytes + 256;
+  return pf::layout(nullptr, n_layers, n_tokens, row_width, pf::pad16(rank + oversample)).bytes + 1024;
 }
 
-kvrp_status kv_patch_form(const void* conditioned, const void* canonical, int64_t cond_layer_stride,
-                          int64_t canon_layer_stride, int32_t n_layers, int32_t n_tokens, int32_t row_width,
-                          int32_t rope_kind, int32_t rot_dim, int64_t delta, double rope_theta, int32_t rank,
-                          int32_t oversample, int32_t power_iters, const float* omega, void* u_out, void* v_out,
-                          int64_t u_layer_stride, int64_t v_layer_stride, void* workspace, size_t workspace_bytes,
-                          kvrp_stream_t stream) {
-  if (!conditioned || !canonical || !omega || !u_out || !v_out)
+kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* deltas, int32_t n_orbit,
+                                const void* canonical, int64_t cond_layer_stride, int64_t canon_layer_stride,
+                                int32_t n_layers, int32_t n_tokens, int32_t row_width, int32_t rope_kind,
+                                int32_t rot_dim, double rope_theta, int32_t rank, int32_t oversample,
+                                int32_t power_iters, const float* omega, void* u_out, void* v_out,
+                                int64_t u_layer_stride, int64_t v_layer_stride, void* workspace,
+                                size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream) {
+  if (!conditioned || !deltas || !canonical || !omega || !u_out || !v_out)
     return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: NULL pointer argument");
-  if (!aligned16(conditioned) || !aligned16(canonical) || !aligned16(omega) || !aligned16(u_out) ||
-      !aligned16(v_out))
+  if (n_orbit <= 0 || n_orbit > pf::kMaxOrbit)
+    return fail(KVRP_ERR_UNSUPPORTED, "kv_patch_form_orbit: 1 <= n_orbit <= %d", pf::kMaxOrbit);
+  for (int p = 0; p < n_orbit; ++p) {
+    if (!conditioned[p]) return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: conditioned cache %d is NULL", p);
+    if (!aligned16(conditioned[p]))
+      return fail(KVRP_ERR_ALIGNMENT, "kv_patch_form: conditioned cache %d is not 16-byte aligned", p);
+  }
+  if (!aligned16(canonical) || !aligned16(omega) || !aligned16(u_out) || !aligned16(v_out))
     return fail(KVRP_ERR_ALIGNMENT, "kv_patch_form: pointers must be 16-byte aligned");
-  if (n_layers <= 0 || n_tokens <= 0 || row_width <= 0 || row_width % 2)
-    return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: n_layers, n_tokens > 0 and an even row_width are required");
+  if (n_layers <= 0 || n_tokens <= 0 || row_width <= 0)
+    return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: n_layers, n_tokens, row_width must be > 0");
+  if (row_width % 4) return fail(KVRP_ERR_UNSUPPORTED, "kv_patch_form: row_width must be a multiple of 4");
+  if (n_layers > 65535) return fail(KVRP_ERR_UNSUPPORTED, "kv_patch_form: at most 65535 layers");
   if (rope_kind != KVRP_ROPE_NONE && rope_kind != KVRP_ROPE_HEADS && rope_kind != KVRP_ROPE_MLA_TAIL)
     return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: unknown rope_kind %d", rope_kind);
   if (rope_kind != KVRP_ROPE_NONE) {
@@ -497,7 +1126,7 @@ kvrp_status kv_patch_form(const void* conditioned, const void* canonical, int64_
       return fail(KVRP_ERR_UNSUPPORTED, "kv_patch_form: rot_dim must be a multiple of 4 up to 128");
     if (rope_kind == KVRP_ROPE_HEADS && row_width % rot_dim)
       return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: row_width must be a multiple of rot_dim");
-    if (rope_kind == KVRP_ROPE_MLA_TAIL && (row_width <= rot_dim || (row_width - rot_dim) % 2))
+    if (rope_kind == KVRP_ROPE_MLA_TAIL && row_width <= rot_dim)
       return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: the rotated tail must fit the row");
     if (!(rope_theta > 0.0) || !std::isfinite(rope_theta))
       return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: rope_theta must be > 0");
@@ -517,77 +1146,95 @@ kvrp_status kv_patch_form(const void* conditioned, const void* canonical, int64_
     return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: layer strides smaller than one layer");
   if (n_layers > 1 && (u_layer_stride < (int64_t)n_tokens * rank || v_layer_stride < (int64_t)row_width * rank))
     return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: factor layer strides smaller than one layer");
+  if (cond_layer_stride % 2 || canon_layer_stride % 2)
+    return fail(KVRP_ERR_ALIGNMENT, "kv_patch_form: cache layer strides must be even");
   const size_t need = kv_patch_form_workspace_size(n_layers, n_tokens, row_width, rank, oversample);
   if (!workspace || workspace_bytes < need)
     return fail(KVRP_ERR_WORKSPACE, "kv_patch_form: workspace of %zu bytes needed", need);
   int sms = 0, smem = 0;
   kvrp_status st0 = current_device_sms(&sms, &smem);
   if (st0 != KVRP_OK) return st0;
+  cudaError_t e = pf::Runner::configure();
+  if (e != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_patch_form: %s", cudaGetErrorString(e));
+  if (!pf::encoder()) return fail(KVRP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
 
   cudaStream_t st = stream;
-  const int L = n_layers, T = n_tokens, D = row_width, m = rank;
-  float* base = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
-  const pf::Buffers b = pf::layout(base, L, T, D, k, m);
+  const int L = n_layers, T = n_tokens, D = row_width, m = rank, kp = pf::pad16(k);
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(workspace) + 1023) & ~uintptr_t(1023));
+  const pf::Buffers b = pf::layout(base, L, T, D, kp);
+
+  // 1. Delta, rows and transposed rows, bf16
+  pf::DeltaArgs da = {};
+  for (int p = 0; p < n_orbit; ++p) da.cond[p] = static_cast<const uint16_t*>(conditioned[p]);
+  da.canon = static_cast<const uint16_t*>(canonical);
+  da.out = b.delta;
+  da.out_t = b.delta_t;
+  da.cond_stride = cond_layer_stride;
+  da.canon_stride = canon_layer_stride;
+  da.n_cond = n_orbit;
+  da.T = T;
+  da.D = D;
+  da.Dp = (int)b.Dp;
+  da.Tp = (int)b.Tp;
+  da.rope_kind = rope_kind;
+  da.rot_dim = rope_kind == KVRP_ROPE_NONE ? 4 : rot_dim;
+  da.inv_n = 1.0f / (float)n_orbit;
   pf::TableParam tab = {};
-  const int64_t d3[3] = {delta, 0, 0};
-  const int32_t s3[3] = {rot_dim / 2, 0, 0};
-  if (rope_kind != KVRP_ROPE_NONE) phase_table(d3, s3, rope_theta, rot_dim, tab.v);
-
-  cudaError_t e = cudaSuccess;
-  // the kernels of steps 3 and 5 keep k x k fp64 matrices in shared memory
-  e = cudaFuncSetAttribute(pf::chol_inverse_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           2 * (int)sizeof(double) * pf::kMaxK * pf::kMaxK);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(pf::jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             2 * (int)sizeof(double) * pf::kMaxK * pf::kMaxK);
-  if (e != cudaSuccess) return fail(KVRP_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-  // Gram-type matrices are used densely (leading dimension k)
-  const int64_t s_kk = (int64_t)k * k;
-  float* g = b.g;
-  float* rinv = b.rinv;
-  float* cmat = b.c;
-
-  // 1. Delta
-  pf::DeltaArgs da{static_cast<const uint16_t*>(conditioned), static_cast<const uint16_t*>(canonical),
-                   cond_layer_stride, canon_layer_stride, b.delta, b.s_delta, T, D, rope_kind, rot_dim};
-  pf::delta_kernel<<<dim3(T, L), 256, 0, st>>>(da, tab);
+  if (rope_kind != KVRP_ROPE_NONE) pf::mean_table(deltas, n_orbit, rope_theta, rot_dim, tab.v);
+  pf::delta_kernel<<<dim3((T + pf::kDeltaTokens - 1) / pf::kDeltaTokens, pf::segment_count(rope_kind, D, da.rot_dim), L),
+                     pf::kThreads, 0, st>>>(da, tab);
   e = cudaGetLastError();
-  // 2. range finder with power iterations
-  if (e == cudaSuccess) e = pf::gemm(st, L, b.delta, b.s_delta, D, 0, omega, 0, k, 0, b.y, b.s_tk, k, T, k, D, 1);
-  for (int it = 0; it < power_iters && e == cudaSuccess; ++it) {
-    e = pf::orthonormalise(st, L, b.y, b.y2, b.s_tk, T, k, g, rinv, s_kk);
-    if (e == cudaSuccess)
-      e = pf::gemm(st, L, b.delta, b.s_delta, D, 1, b.y, b.s_tk, k, 0, b.z, b.s_dk, k, D, k, T, pf::splits_for(T));
-    if (e == cudaSuccess) e = pf::orthonormalise(st, L, b.z, b.z2, b.s_dk, D, k, g, rinv, s_kk);
-    if (e == cudaSuccess) e = pf::gemm(st, L, b.delta, b.s_delta, D, 0, b.z, b.s_dk, k, 0, b.y, b.s_tk, k, T, k, D, 1);
-  }
-  // 3. Q = orth(Y)
-  if (e == cudaSuccess) e = pf::orthonormalise(st, L, b.y, b.y2, b.s_tk, T, k, g, rinv, s_kk);
-  // 4. B = Q^T Delta  (k x D), C = B B^T  (k x k)
-  if (e == cudaSuccess)
-    e = pf::gemm(st, L, b.y, b.s_tk, k, 1, b.delta, b.s_delta, D, 0, b.b, b.s_kd, D, k, D, T, pf::splits_for(T));
-  if (e == cudaSuccess) e = pf::gemm(st, L, b.b, b.s_kd, D, 0, b.b, b.s_kd, D, 1, cmat, s_kk, k, k, k, D, pf::splits_for(D));
-  // 5. eigenvectors of the m largest eigenvalues, W = U_B[:, :m]
   if (e == cudaSuccess) {
-    pf::jacobi_kernel<<<L, 256, 2 * sizeof(double) * k * k, st>>>(cmat, b.w, k, m);
-    e = cudaGetLastError();
-  }
-  // 6. V_m = B^T W normalised (D x m), U_m = Delta V_m (T x m)
-  if (e == cudaSuccess) e = pf::gemm(st, L, b.b, b.s_kd, D, 1, b.w, (int64_t)k * m, m, 0, b.vf, b.s_dm, m, D, m, k, 1);
-  if (e == cudaSuccess) {
-    pf::normalise_columns_kernel<<<L, 256, 0, st>>>(b.vf, b.s_dm, D, m);
-    e = cudaGetLastError();
-  }
-  if (e == cudaSuccess) e = pf::gemm(st, L, b.delta, b.s_delta, D, 0, b.vf, b.s_dm, m, 0, b.uf, b.s_tm, m, T, m, D, 1);
-  if (e == cudaSuccess) {
-    pf::to_bf16_kernel<<<dim3(64, L), 256, 0, st>>>(b.uf, b.s_tm, static_cast<uint16_t*>(u_out),
-                                                    u_layer_stride, (int64_t)T * m);
-    pf::to_bf16_kernel<<<dim3(64, L), 256, 0, st>>>(b.vf, b.s_dm, static_cast<uint16_t*>(v_out),
-                                                    v_layer_stride, (int64_t)D * m);
+    pf::omega_t_kernel<<<std::max(1, std::min(sms, (D * kp + 255) / 256)), 256, 0, st>>>(omega, D, k, b.omega_t, kp,
+                                                                                         (int)b.Dp);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_patch_form: %s", cudaGetErrorString(e));
+
+  pf::Runner run(st, L, kp, sms, d_status);
+  float *y = b.y, *y2 = b.y2, *z = b.z, *z2 = b.z2;
+  // 2. range finder with subspace iterations (tensor-core passes over Delta and Delta^T)
+  run.pass(b.delta, b.Dp, b.s_delta, b.omega_t, b.Dp, b.s_st_d, false, y, b.s_tk, T, D);           // Y = Delta Omega
+  for (int it = 0; it < power_iters; ++it) {
+    run.orth(y, y2, b.s_tk, T, k, 1, pf::kShiftFirst, b.g, b.rinv, b.st_t, b.s_st_t, (int)b.Tp);     // Q^T
+    run.pass(b.delta_t, b.Tp, b.s_delta_t, b.st_t, b.Tp, b.s_st_t, true, z, b.s_dk, D, T);          // Z = Delta^T Q
+    run.orth(z, z2, b.s_dk, D, k, 1, pf::kShiftFirst, b.g, b.rinv, b.st_d, b.s_st_d, (int)b.Dp);     // Zq^T
+    run.pass(b.delta, b.Dp, b.s_delta, b.st_d, b.Dp, b.s_st_d, true, y, b.s_tk, T, D);              // Y = Delta Zq
+  }
+  // 3. Q = orth(Y); B^T = Delta^T Q; C = B B^T
+  run.orth(y, y2, b.s_tk, T, k, 2, pf::kShiftFirst, b.g, b.rinv, b.st_t, b.s_st_t, (int)b.Tp);
+  run.pass(b.delta_t, b.Tp, b.s_delta_t, b.st_t, b.Tp, b.s_st_t, true, z, b.s_dk, D, T);
+  run.tall(true, z, b.s_dk, kp, z, b.s_dk, kp, b.g, b.s_kk, kp, D);
+  // 4. eigenvectors of the m largest eigenvalues, scaled by lambda^-1/2
+  if (run.err == cudaSuccess && !run.map_fail) {
+    pf::jacobi_kernel<<<L, pf::kThreads, run.jacobi_smem(), st>>>(b.g, b.s_kk, b.w, b.s_kk, k, kp, m);
+    run.err = cudaGetLastError();
+  }
+  // 5. V_m = orth(B^T W) (columns already near unit length) as bf16 V^T; U_m = Delta V_m
+  run.tall(false, z, b.s_dk, kp, b.w, b.s_kk, kp, z2, b.s_dk, D, kp);
+  run.orth(z2, z, b.s_dk, D, m, 1, pf::kShiftSecond, b.g, b.rinv, b.st_d, b.s_st_d, (int)b.Dp);
+  run.pass(b.delta, b.Dp, b.s_delta, b.st_d, b.Dp, b.s_st_d, true, y2, b.s_tk, T, D);
+  if (run.err == cudaSuccess && !run.map_fail) {
+    pf::u_out_kernel<<<dim3(64, L), 256, 0, st>>>(y2, b.s_tk, kp, static_cast<uint16_t*>(u_out), u_layer_stride, T, m);
+    pf::v_out_kernel<<<dim3(64, L), 256, 0, st>>>(b.st_d, b.s_st_d, (int)b.Dp, static_cast<uint16_t*>(v_out),
+                                                  v_layer_stride, D, m);
+    run.err = cudaGetLastError();
+  }
+  if (run.map_fail) return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: cuTensorMapEncodeTiled rejected a workspace map");
+  if (run.err != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_patch_form: %s", cudaGetErrorString(run.err));
   return KVRP_OK;
+}
+
+kvrp_status kv_patch_form(const void* conditioned, const void* canonical, int64_t cond_layer_stride,
+                          int64_t canon_layer_stride, int32_t n_layers, int32_t n_tokens, int32_t row_width,
+                          int32_t rope_kind, int32_t rot_dim, int64_t delta, double rope_theta, int32_t rank,
+                          int32_t oversample, int32_t power_iters, const float* omega, void* u_out, void* v_out,
+                          int64_t u_layer_stride, int64_t v_layer_stride, void* workspace, size_t workspace_bytes,
+                          uint32_t* d_status, kvrp_stream_t stream) {
+  const void* one[1] = {conditioned};
+  return kv_patch_form_orbit(one, &delta, 1, canonical, cond_layer_stride, canon_layer_stride, n_layers, n_tokens,
+                             row_width, rope_kind, rot_dim, rope_theta, rank, oversample, power_iters, omega, u_out,
+                             v_out, u_layer_stride, v_layer_stride, workspace, workspace_bytes, d_status, stream);
 }
 
 }  // extern "C"

@@ -162,3 +162,24 @@ def test_patch_form_argument_checks(kvrp):
     import torch
     if not torch.cuda.is_available():                                         # well-formed: no GPU, no fallback
         assert status(workspace_bytes=need) == kvrp.KVRP_ERR_CUDA
+
+
+def test_patch_form_orbit_argument_checks(kvrp):
+    def status(conds, deltas, **over):
+        args = dict(n_layers=1, n_tokens=100, row_width=256, rope_kind=kvrp.KVRP_ROPE_HEADS, rot_dim=128,
+                    rope_theta=1e4, rank=16, oversample=8, power_iters=1, omega=0x50000, u_out=0x60000,
+                    v_out=0x70000, workspace=0x100000, workspace_bytes=1 << 30, stream=0)
+        args.update(over)
+        with pytest.raises(kvrp.KvrpError) as e:
+            kvrp.kv_patch_form_orbit(conds, deltas, 0x30000, **args)
+        return e.value.status
+
+    assert status([], []) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert status([0x20000] * 65, list(range(65))) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert status([0x20000, 0], [1, 2]) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status([0x20000, 0x20008], [1, 2]) == kvrp.KVRP_ERR_ALIGNMENT
+    assert status([0x20000], [1], row_width=254, rope_kind=kvrp.KVRP_ROPE_NONE) == kvrp.KVRP_ERR_UNSUPPORTED
+    with pytest.raises(ValueError):
+        kvrp.kv_patch_form_orbit([0x20000], [1, 2], 0x30000, n_layers=1, n_tokens=100, row_width=256,
+                                 rope_kind=0, rot_dim=0, rope_theta=1e4, rank=16, oversample=8, power_iters=1,
+                                 omega=0x50000, u_out=0x60000, v_out=0x70000, workspace=0x100000)

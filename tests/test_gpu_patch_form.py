@@ -185,3 +185,70 @@ def test_zero_deficit_gives_a_zero_patch():
     canon, cond = make_case(31, 1, 128, 256, "none", 0, 0, 1e4, 4, noise=0.0)
     u, v = form_on_gpu(canon, canon, "none", 0, 0, 1e4, 16, 8, 1)
     assert np.max(np.abs(bf16_bits_to_f64(u)[0] @ bf16_bits_to_f64(v)[0].T)) < 1e-6
+
+
+def make_orbit_case(seed, L, T, D, kind, rot_dim, deltas, theta, shared_rank=8, own_rank=4, noise=1e-3):
+    """Canonical cache and one conditioned cache per ordering pi:
+    cond_pi = bf16(R(delta_pi) canon + S + P_pi + noise), S shared by every
+    ordering, P_pi its own low-rank term."""
+    from oracle import bf16_bits_to_f64, round_to_bf16_bits
+    from oracle.kamera import apply_relocation
+    rng = np.random.default_rng(seed)
+    canon = round_to_bf16_bits(rng.standard_normal((L, T, D)))
+    lay = layout_of(kind, D, rot_dim)
+
+    def low_rank(r, scale):
+        return (np.linalg.qr(rng.standard_normal((T, r)))[0] * scale * np.sqrt(T)) @ \
+            np.linalg.qr(rng.standard_normal((D, r)))[0].T
+
+    shared = [low_rank(shared_rank, 0.3 * 0.8 ** np.arange(shared_rank)) for _ in range(L)]
+    conds = []
+    for dl in deltas:
+        c = np.empty_like(canon)
+        for l in range(L):
+            y = apply_relocation(bf16_bits_to_f64(canon[l]), dl, theta, lay)
+            c[l] = round_to_bf16_bits(y + shared[l] + low_rank(own_rank, 0.1 * np.ones(own_rank))
+                                      + noise * rng.standard_normal((T, D)))
+        conds.append(c)
+    return canon, conds
+
+
+@pytest.mark.parametrize("kind,D,rot", [("heads", 256, 128), ("mla", 576, 64)])
+def test_orbit_patch_matches_exact_svd_of_the_mean_deficit(kind, D, rot):
+    """kv_patch_form_orbit factors mean_pi [KV(B|A_pi) - R(delta_pi) KV(B|empty)];
+    its residual against the oracle's mean deficit is within a few percent of
+    the exact truncated SVD's (Kamera section 3, reordering bullet)."""
+    import position_invariant_kv_gb300 as kvrp
+    from oracle import bf16_bits_to_f64, orbit_deficit
+    L, T, m, p, theta = 2, 320, 16, 16, 1e6
+    deltas = [0, 300, -1200, 5000, 77]
+    canon, conds = make_orbit_case(51, L, T, D, kind, rot, deltas, theta)
+    g = torch.Generator(device="cuda").manual_seed(5)
+    omega = torch.randn((D, m + p), generator=g, device="cuda", dtype=torch.float32)
+    u = torch.empty((L, T, m), dtype=torch.bfloat16, device="cuda")
+    v = torch.empty((L, D, m), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(kvrp.kv_patch_form_workspace_size(L, T, D, m, p), dtype=torch.uint8, device="cuda")
+    rope = kvrp.KVRP_ROPE_HEADS if kind == "heads" else kvrp.KVRP_ROPE_MLA_TAIL
+    cond_dev = [_dev(c) for c in conds]
+    kvrp.kv_patch_form_orbit(cond_dev, deltas, _dev(canon), n_layers=L, n_tokens=T, row_width=D, rope_kind=rope,
+                             rot_dim=rot, rope_theta=theta, rank=m, oversample=p, power_iters=2, omega=omega,
+                             u_out=u, v_out=v, workspace=ws)
+    torch.cuda.synchronize()
+    lay = layout_of(kind, D, rot)
+    dl = np.stack([orbit_deficit([bf16_bits_to_f64(c[l]) for c in conds], bf16_bits_to_f64(canon[l]), deltas,
+                                 theta, lay) for l in range(L)])
+    for got, ref, tail, total in residuals(dl, _bits(u), _bits(v), m):
+        print(f"orbit residual gpu {got:.4e} exact-bf16 {ref:.4e} tail {tail:.4e} total {total:.4e}")
+        assert got <= 1.05 * ref + 1e-9 * total
+        assert got < 0.1 * total
+    # the plain entry point is the orbit of one ordering
+    u1 = torch.empty_like(u)
+    v1 = torch.empty_like(v)
+    kvrp.kv_patch_form(cond_dev[2], _dev(canon), n_layers=L, n_tokens=T, row_width=D, rope_kind=rope, rot_dim=rot,
+                       delta=deltas[2], rope_theta=theta, rank=m, oversample=p, power_iters=2, omega=omega,
+                       u_out=u1, v_out=v1, workspace=ws)
+    torch.cuda.synchronize()
+    d2 = np.stack([orbit_deficit([bf16_bits_to_f64(conds[2][l])], bf16_bits_to_f64(canon[l]), [deltas[2]], theta,
+                                 lay) for l in range(L)])
+    for got, ref, tail, total in residuals(d2, _bits(u1), _bits(v1), m):
+        assert got <= 1.05 * ref + 1e-9 * total

@@ -83,3 +83,44 @@ def test_inverse_frequencies_used_by_the_deficit():
     d1 = conditioning_deficit(np.array([[np.cos(3.0), np.sin(3.0)]]), x, 3, 1e4, row_layout("gqa", "k", n_heads=1, head_dim=2))
     assert np.max(np.abs(d1)) < 1e-15
     assert inv_freq(2, 1e4)[0] == 1.0
+
+
+# --------------------------------------------------------------------------- #
+# Orbit patch: the deficit averaged over orderings
+# --------------------------------------------------------------------------- #
+
+def test_orbit_deficit_hand_example():
+    """d = 2, theta_0 = 1, two orderings with shifts +1 and -1, x = (1, 0).
+    The conditioned caches are the shifted x plus (0.5, 0) and (0.25, 0.5):
+    the mean deficit is (0.375, 0.25).  With zero conditioned caches the
+    deficit is -Rbar x where Rbar averages the two rotations: mean cos = cos 1,
+    mean sin = 0, so -Rbar x = (-cos 1, 0) = (-0.5403023058681398, 0)."""
+    from oracle import orbit_deficit
+    lay = row_layout("gqa", "k", n_heads=1, head_dim=2)
+    x = np.array([[1.0, 0.0]])
+    c1, s1 = 0.5403023058681398, 0.8414709848078965
+    conds = [np.array([[c1 + 0.5, s1]]), np.array([[c1 + 0.25, -s1 + 0.5]])]
+    d = orbit_deficit(conds, x, [1, -1], 1e4, lay)
+    assert np.allclose(d, [[0.375, 0.25]], atol=1e-15, rtol=0)
+    z = orbit_deficit([np.zeros((1, 2)), np.zeros((1, 2))], x, [1, -1], 1e4, lay)
+    assert np.allclose(z, [[-c1, 0.0]], atol=1e-15, rtol=0)
+
+
+def test_orbit_of_pure_shifts_is_zero_and_planted_terms_average():
+    from oracle import orbit_deficit
+    rng = np.random.default_rng(44)
+    T, H, d, theta = 40, 2, 64, 1e6
+    pos = np.arange(T) + 77
+    deltas = [0, 1500, -700, 4096]
+    raw, canon = _keys(rng, T, H, d, pos, theta)
+    lay = row_layout("gqa", "k", n_heads=H, head_dim=d)
+    shifted = [_keys(rng, T, H, d, pos + dl, theta, raw)[1] for dl in deltas]
+    assert np.max(np.abs(orbit_deficit(shifted, canon, deltas, theta, lay))) < 1e-9
+    planted = [rng.standard_normal((T, H * d)) for _ in deltas]
+    got = orbit_deficit([s + p for s, p in zip(shifted, planted)], canon, deltas, theta, lay)
+    assert np.allclose(got, sum(planted) / len(planted), atol=1e-9, rtol=0)
+    # a single ordering is the plain deficit
+    one = orbit_deficit([shifted[1] + planted[1]], canon, [deltas[1]], theta, lay)
+    assert np.allclose(one, planted[1], atol=1e-9, rtol=0)
+    with pytest.raises(ValueError):
+        orbit_deficit([canon], canon, [1, 2], theta, lay)
