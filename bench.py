@@ -395,6 +395,157 @@ def bench_reference(args) -> dict:
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# --------------------------------------------------------------------------- #
+# patch formation (and the orbit patch): the factors of one chunk's deficit
+# --------------------------------------------------------------------------- #
+PATCH_METRIC = "patch formation: chunk tokens/s (rank-m K and V factors of one chunk, all layers)"
+
+
+def patch_form_setup(wl, orbit: int, device):
+    """Seeded synthetic caches of the workload's first chunk: canonical K and V
+    rows and `orbit` conditioned copies (canonical plus a conditioning term)."""
+    import torch
+    c = wl.chunks[0]
+    L, T, D = wl.n_layers, c.n_tokens, wl.row_width
+    g = torch.Generator(device=device).manual_seed(wl.seed + 101)
+    canon = {n: torch.randn((L, T, D), generator=g, device=device).to(torch.bfloat16) for n in wl.tensors}
+    cond = {n: [(canon[n].float() + 0.1 * torch.randn((L, T, D), generator=g, device=device)).to(torch.bfloat16)
+                for _ in range(orbit)] for n in wl.tensors}
+    deltas = [int(c.delta) + 977 * i for i in range(orbit)]
+    return canon, cond, deltas
+
+
+def patch_bytes(L, T, D, m, p, q, orbit) -> int:
+    """Bytes this method moves per tensor: read the caches (bf16), write the
+    deficit twice (bf16 rows and transposed rows), 2q + 3 tensor-core passes
+    over it (bf16), and the small fp32 / bf16 operands and factors."""
+    kp = (m + p + 15) // 16 * 16
+    n = L * T * D
+    skinny = L * (T + D) * kp * 4
+    return n * 2 * (1 + orbit) + n * 4 + (2 * q + 3) * n * 2 + (2 * q + 3) * 3 * skinny + L * (T + D) * m * 2
+
+
+def bench_patch_form(args) -> dict:
+    import torch
+    import workloads as W
+    import position_invariant_kv_gb300 as kvrp
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    from position_invariant_kv_gb300.build import build
+    build()
+    kvrp.lib()
+    wl = W.config(args.config)
+    if args.layers:
+        wl.n_layers = min(wl.n_layers, args.layers)
+    device = f"cuda:{local}"
+    c = wl.chunks[0]
+    L, T, D = wl.n_layers, c.n_tokens, wl.row_width
+    m = c.rank if c.rank else 32
+    p, q, orbit = args.oversample, args.power_iters, args.orbit
+    canon, cond, deltas = patch_form_setup(wl, orbit, device)
+    g = torch.Generator(device=device).manual_seed(wl.seed + 202)
+    omega = torch.randn((D, m + p), generator=g, device=device)
+    ws = torch.empty(kvrp.kv_patch_form_workspace_size(L, T, D, m, p), dtype=torch.uint8, device=device)
+    fac = {n: (torch.empty((L, T, m), dtype=torch.bfloat16, device=device),
+               torch.empty((L, D, m), dtype=torch.bfloat16, device=device)) for n in wl.tensors}
+    d_status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    if wl.family == "mla":
+        kinds = {"kv": (kvrp.KVRP_ROPE_MLA_TAIL, wl.rope_dim)}
+    else:
+        kinds = {"k": (kvrp.KVRP_ROPE_HEADS, wl.head_dim), "v": (kvrp.KVRP_ROPE_NONE, 0)}
+
+    def step():
+        for n in wl.tensors:
+            kind, rot = kinds[n]
+            kvrp.kv_patch_form_orbit(cond[n], deltas, canon[n], n_layers=L, n_tokens=T, row_width=D, rope_kind=kind,
+                                     rot_dim=rot, rope_theta=wl.theta, rank=m, oversample=p, power_iters=q,
+                                     omega=omega, u_out=fac[n][0], v_out=fac[n][1], workspace=ws,
+                                     d_status=d_status, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    steps = args.steps
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / steps
+    nb = patch_bytes(L, T, D, m, p, q, orbit) * len(wl.tensors)
+    peaks = measured_peaks()
+    achieved = nb / (ms / 1e3) / 1e9
+    out = {
+        "metric": PATCH_METRIC, "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "row": "patch_form",
+        "config": {"workload": f"{wl.name} first chunk: {L} layers x {T} tokens x {D} features, tensors "
+                               f"{'/'.join(wl.tensors)}, rank {m}, oversample {p}, {q} subspace iterations, "
+                               f"orbit of {orbit} ordering(s)",
+                   "tokens_per_step": T, "method_bytes_per_step": nb,
+                   "l2": f"inputs larger than L2 ({nb / 1e6:.0f} MB moved per step vs 129 MB L2)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "kv_patch_form_orbit, whole call (delta, tensor-core passes, k x k solves)",
+                     "peak_source": peaks["source"]},
+        "gpu_launches": None,
+        "clocks": clocks.summary(),
+        "device_status": int(d_status.item()),
+    }
+    if not args.no_cpu_baseline:
+        out["cpu_baseline"] = run_patch_cpu_baseline(args.config, args.budget)
+    return out
+
+
+def patch_cpu_worker(cfg: int, budget_s: float) -> dict:
+    """The oracle's patch formation (fp64 deficit + exact truncated SVD) on
+    whole (layer, tensor) slices of the chunk until the budget is spent."""
+    import numpy as np
+    import workloads as W
+    from oracle import conditioning_deficit, row_layout, svd_patch
+    wl = W.config(cfg)
+    c = wl.chunks[0]
+    T, D = c.n_tokens, wl.row_width
+    m = c.rank if c.rank else 32
+    rng = np.random.default_rng(wl.seed + 303)
+    elapsed, n = 0.0, 0
+    while elapsed < budget_s:
+        name = wl.tensors[n % len(wl.tensors)]
+        lay = row_layout(wl.family, name, n_heads=wl.n_heads, head_dim=wl.head_dim, kv_lora_dim=wl.kv_lora_dim,
+                         rope_dim=wl.rope_dim)
+        canon = rng.standard_normal((T, D))
+        cond = canon + 0.1 * rng.standard_normal((T, D))
+        t0 = time.perf_counter()
+        svd_patch(conditioning_deficit(cond, canon, c.delta, wl.theta, lay), m)
+        elapsed += time.perf_counter() - t0
+        n += 1
+    slices = wl.n_layers * len(wl.tensors)
+    return {"value": T * n / slices / elapsed, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} (layer, tensor) slices of {T} x {D} ({wl.name}; fp64 deficit and exact SVD, NumPy, "
+                      f"one thread, {elapsed:.1f} s); one chunk = {slices} slices"}
+
+
+def run_patch_cpu_baseline(cfg: int, budget_s: float) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-worker", "--row",
+                          "patch_form", "--config", str(cfg), "--budget", str(budget_s)],
+                         capture_output=True, text=True, env=env, timeout=900)
+    if res.returncode != 0:
+        tail = res.stderr.strip().splitlines()[-1] if res.stderr.strip() else "no output"
+        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": "failed: " + tail}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -407,15 +558,36 @@ def main():
     ap.add_argument("--budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--row", choices=["relocate", "patch_form"], default="relocate",
+                    help="relocate: the reuse operator (the headline); patch_form: forming the patch factors")
+    ap.add_argument("--orbit", type=int, default=1, help="patch_form: conditioned caches averaged (orbit patch)")
+    ap.add_argument("--oversample", type=int, default=16, help="patch_form: range-finder oversampling")
+    ap.add_argument("--power-iters", type=int, default=2, help="patch_form: subspace iterations")
     args = ap.parse_args()
     if args.cpu_baseline_worker:
-        print(json.dumps(cpu_baseline_worker(args.config, args.budget)))
+        worker = patch_cpu_worker if args.row == "patch_form" else cpu_baseline_worker
+        print(json.dumps(worker(args.config, args.budget)))
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[k] = "1"
+    if args.row == "patch_form":
+        if args.impl == "reference":
+            rank, world, _ = dist_env()
+            if rank != 0:
+                return
+            cb = patch_cpu_worker(args.config, args.budget)
+            out = {"metric": PATCH_METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": world, "impl": "reference",
+                   "higher_is_better": True, "dtype": "f64", "data": "synthetic", "row": "patch_form",
+                   "config": {"workload": cb["sample"]}, "cpu_baseline": cb,
+                   "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        else:
+            out = bench_patch_form(args)
+        if out is not None:
+            print(json.dumps(out))
+        return
     out = bench_reference(args) if args.impl == "reference" else bench_ours(args)
     if out is not None:
         print(json.dumps(out))

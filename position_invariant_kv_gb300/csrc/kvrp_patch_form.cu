@@ -29,8 +29,8 @@
 // pass_kernel (TMA-staged bf16 tiles, tcgen05.mma into a TMEM accumulator,
 // fp32 results).  The skinny operands are rounded to bf16 for these products;
 // everything else -- the Gram matrices, the k x k solves, the small
-// right-multiplies -- stays in fp32 on the CUDA cores (tall_kernel and the
-// one-CTA-per-layer solvers).
+// right-multiplies -- stays in fp32 on the CUDA cores (gram_kernel,
+// apply_kernel and the one-CTA-per-layer solvers).
 #include <cudaTypedefs.h>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -51,9 +51,7 @@ constexpr int kMaxK = 96;          // rank + oversampling bound (k x k solves li
 constexpr int kMaxOrbit = 64;      // conditioned caches averaged by one call
 constexpr int kJacobiSweeps = 3;   // the top-m subspace has settled by then (V_m is re-orthonormalised)
 constexpr int kThreads = 256;
-constexpr int kTile = 128;         // output rows per CTA (tall_kernel, pass_kernel)
-constexpr int kStep = 32;          // tall_kernel: contraction step per pipeline stage
-constexpr int kStages = 3;         // tall_kernel pipeline depth
+constexpr int kTile = 128;         // output rows per pass_kernel CTA
 constexpr int kPassStages = 3;     // pass_kernel pipeline depth
 constexpr int kPassK = 64;         // pass_kernel: contraction per stage (one 128-byte swizzle row of bf16)
 constexpr int kPassThreads = 192;  // producer warp, MMA warp, four epilogue warps
@@ -118,7 +116,20 @@ __device__ inline Segment segment_of(int sg, int rope_kind, int D, int rot) {
   return s;
 }
 
-constexpr int kDeltaUnroll = 8;   // work units per thread per batch of loads
+constexpr int kDeltaUnroll = 8;   // narrow path: work units per thread per batch of loads
+
+__device__ __forceinline__ void bf16x8_to_f(const uint4 w, float (&v)[8]) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(u[i] << 16);
+    v[2 * i + 1] = __uint_as_float(u[i] & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ uint4 f_to_bf16x8(const float (&v)[8]) {
+  return make_uint4(f2_to_bf16x2(v[0], v[1]), f2_to_bf16x2(v[2], v[3]), f2_to_bf16x2(v[4], v[5]),
+                    f2_to_bf16x2(v[6], v[7]));
+}
 
 __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__ DeltaArgs a,
                                                           const __grid_constant__ TableParam tab) {
@@ -130,63 +141,121 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__
   const Segment sg = segment_of(blockIdx.y, a.rope_kind, a.D, a.rot_dim);
   uint16_t* out = a.out + (int64_t)l * a.T * a.Dp;
   uint16_t* out_t = a.out_t + (int64_t)l * a.D * a.Tp;
+  const uint16_t* canon = a.canon + (int64_t)l * a.canon_stride;
   __syncthreads();
-  const int upt = sg.W / 4;                           // work units per token
   const int half = sg.W / 2;
-  const int n_units = kDeltaTokens * upt;
-  for (int u0 = 0; u0 < n_units; u0 += kDeltaUnroll * kThreads) {
-    // batch of units: issue every load first, then compute
-    float2 x0[kDeltaUnroll], x1[kDeltaUnroll], c0[kDeltaUnroll], c1[kDeltaUnroll];
-    int e0s[kDeltaUnroll], e1s[kDeltaUnroll], tls[kDeltaUnroll];
-#pragma unroll
-    for (int b = 0; b < kDeltaUnroll; ++b) {
-      const int u = u0 + b * kThreads + threadIdx.x;
+  // Wide path: a unit is 8 frequency pairs (elements [e0, e0+8) and their
+  // partners [e0+half, ...)), or 16 consecutive unrotated elements, moved as
+  // 16-byte vectors.  It needs half (or W) to be a multiple of 8 (16) and the
+  // row start 16-byte aligned.
+  const bool wide = (sg.turns ? half % 8 == 0 : sg.W % 16 == 0) && a.D % 8 == 0 && sg.f0 % 8 == 0 &&
+                    a.canon_stride % 8 == 0 && a.cond_stride % 8 == 0;
+  if (wide) {
+    const int upt = sg.W / 16;
+    const int n_units = kDeltaTokens * upt;
+    for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
       const int tl = u / upt, w = u - (u / upt) * upt;
-      const bool live = u < n_units && t0 + tl < a.T;
-      const int e0 = sg.turns ? 2 * w : 4 * w;
-      const int e1 = sg.turns ? 2 * w + half : 4 * w + 2;
-      e0s[b] = e0; e1s[b] = e1; tls[b] = live ? tl : -1;
-      x0[b] = x1[b] = c0[b] = c1[b] = make_float2(0.f, 0.f);
-      if (!live) continue;
-      const int64_t row = (int64_t)(t0 + tl) * a.D + sg.f0;
-      const uint16_t* x = a.canon + (int64_t)l * a.canon_stride + row;
-      x0[b] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(x + e0));   // (x_i, x_i+1)
-      x1[b] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(x + e1));   // their partners
+      const int t = t0 + tl;
+      if (t >= a.T) continue;
+      const int e0 = sg.turns ? 8 * w : 16 * w;
+      const int e1 = sg.turns ? 8 * w + half : 16 * w + 8;
+      const int64_t row = (int64_t)t * a.D + sg.f0;
+      float x0[8], x1[8], c0[8] = {}, c1[8] = {};
+      bf16x8_to_f(*reinterpret_cast<const uint4*>(canon + row + e0), x0);
+      bf16x8_to_f(*reinterpret_cast<const uint4*>(canon + row + e1), x1);
       for (int p = 0; p < a.n_cond; ++p) {
         const uint16_t* c = a.cond[p] + (int64_t)l * a.cond_stride + row;
-        const float2 v0 = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(c + e0));
-        const float2 v1 = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(c + e1));
-        c0[b].x += v0.x; c0[b].y += v0.y; c1[b].x += v1.x; c1[b].y += v1.y;
-      }
-    }
+        float v0[8], v1[8];
+        bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e0), v0);
+        bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e1), v1);
 #pragma unroll
-    for (int b = 0; b < kDeltaUnroll; ++b) {
-      const int tl = tls[b];
-      if (tl < 0) continue;
-      const int e0 = e0s[b], e1 = e1s[b];
-      float2 y0 = x0[b], y1 = x1[b];
-      if (sg.turns) {
-        const float4 hd = tb[e0], tl4 = tb[e0 + 1];   // pairs i, i+1 (i = e0): {C_i, C_i+1, S_i, S_i+1}, then tails
-        y0.x = fmaf(x0[b].x, hd.x, -(x1[b].x * hd.z)) + fmaf(x0[b].x, tl4.x, -(x1[b].x * tl4.z));
-        y0.y = fmaf(x0[b].y, hd.y, -(x1[b].y * hd.w)) + fmaf(x0[b].y, tl4.y, -(x1[b].y * tl4.w));
-        y1.x = fmaf(x1[b].x, hd.x, x0[b].x * hd.z) + fmaf(x1[b].x, tl4.x, x0[b].x * tl4.z);
-        y1.y = fmaf(x1[b].y, hd.y, x0[b].y * hd.w) + fmaf(x1[b].y, tl4.y, x0[b].y * tl4.w);
+        for (int i = 0; i < 8; ++i) { c0[i] += v0[i]; c1[i] += v1[i]; }
       }
-      const float d00 = c0[b].x * a.inv_n - y0.x, d01 = c0[b].y * a.inv_n - y0.y;
-      const float d10 = c1[b].x * a.inv_n - y1.x, d11 = c1[b].y * a.inv_n - y1.y;
-      uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
-      *reinterpret_cast<uint32_t*>(o + e0) = f2_to_bf16x2(d00, d01);
-      *reinterpret_cast<uint32_t*>(o + e1) = f2_to_bf16x2(d10, d11);
-      tile[e0][tl] = d00; tile[e0 + 1][tl] = d01; tile[e1][tl] = d10; tile[e1 + 1][tl] = d11;
+      float d0[8], d1[8];
+      if (sg.turns) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {   // pairs e0 + 2q, e0 + 2q + 1
+          const float4 hd = tb[e0 + 2 * q], tl4 = tb[e0 + 2 * q + 1];
+          const float a0 = x0[2 * q], a1 = x0[2 * q + 1], b0 = x1[2 * q], b1 = x1[2 * q + 1];
+          const float y00 = fmaf(a0, hd.x, -(b0 * hd.z)) + fmaf(a0, tl4.x, -(b0 * tl4.z));
+          const float y01 = fmaf(a1, hd.y, -(b1 * hd.w)) + fmaf(a1, tl4.y, -(b1 * tl4.w));
+          const float y10 = fmaf(b0, hd.x, a0 * hd.z) + fmaf(b0, tl4.x, a0 * tl4.z);
+          const float y11 = fmaf(b1, hd.y, a1 * hd.w) + fmaf(b1, tl4.y, a1 * tl4.w);
+          d0[2 * q] = c0[2 * q] * a.inv_n - y00;
+          d0[2 * q + 1] = c0[2 * q + 1] * a.inv_n - y01;
+          d1[2 * q] = c1[2 * q] * a.inv_n - y10;
+          d1[2 * q + 1] = c1[2 * q + 1] * a.inv_n - y11;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { d0[i] = c0[i] * a.inv_n - x0[i]; d1[i] = c1[i] * a.inv_n - x1[i]; }
+      }
+      uint16_t* o = out + (int64_t)t * a.Dp + sg.f0;
+      *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0);
+      *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { tile[e0 + i][tl] = d0[i]; tile[e1 + i][tl] = d1[i]; }
+    }
+  } else {
+    const int upt = sg.W / 4;                           // two pairs (or four elements) per unit
+    const int n_units = kDeltaTokens * upt;
+    for (int u0 = 0; u0 < n_units; u0 += kDeltaUnroll * kThreads) {
+      // batch of units: issue every load first, then compute
+      float2 x0[kDeltaUnroll], x1[kDeltaUnroll], c0[kDeltaUnroll], c1[kDeltaUnroll];
+      int e0s[kDeltaUnroll], e1s[kDeltaUnroll], tls[kDeltaUnroll];
+#pragma unroll
+      for (int b = 0; b < kDeltaUnroll; ++b) {
+        const int u = u0 + b * kThreads + threadIdx.x;
+        const int tl = u / upt, w = u - (u / upt) * upt;
+        const bool live = u < n_units && t0 + tl < a.T;
+        const int e0 = sg.turns ? 2 * w : 4 * w;
+        const int e1 = sg.turns ? 2 * w + half : 4 * w + 2;
+        e0s[b] = e0; e1s[b] = e1; tls[b] = live ? tl : -1;
+        x0[b] = x1[b] = c0[b] = c1[b] = make_float2(0.f, 0.f);
+        if (!live) continue;
+        const int64_t row = (int64_t)(t0 + tl) * a.D + sg.f0;
+        x0[b] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(canon + row + e0));   // (x_i, x_i+1)
+        x1[b] = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(canon + row + e1));   // their partners
+        for (int p = 0; p < a.n_cond; ++p) {
+          const uint16_t* c = a.cond[p] + (int64_t)l * a.cond_stride + row;
+          const float2 v0 = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(c + e0));
+          const float2 v1 = bf16x2_to_f2(*reinterpret_cast<const uint32_t*>(c + e1));
+          c0[b].x += v0.x; c0[b].y += v0.y; c1[b].x += v1.x; c1[b].y += v1.y;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kDeltaUnroll; ++b) {
+        const int tl = tls[b];
+        if (tl < 0) continue;
+        const int e0 = e0s[b], e1 = e1s[b];
+        float2 y0 = x0[b], y1 = x1[b];
+        if (sg.turns) {
+          const float4 hd = tb[e0], tl4 = tb[e0 + 1];   // pairs i, i+1 (i = e0): {C_i, C_i+1, S_i, S_i+1}, then tails
+          y0.x = fmaf(x0[b].x, hd.x, -(x1[b].x * hd.z)) + fmaf(x0[b].x, tl4.x, -(x1[b].x * tl4.z));
+          y0.y = fmaf(x0[b].y, hd.y, -(x1[b].y * hd.w)) + fmaf(x0[b].y, tl4.y, -(x1[b].y * tl4.w));
+          y1.x = fmaf(x1[b].x, hd.x, x0[b].x * hd.z) + fmaf(x1[b].x, tl4.x, x0[b].x * tl4.z);
+          y1.y = fmaf(x1[b].y, hd.y, x0[b].y * hd.w) + fmaf(x1[b].y, tl4.y, x0[b].y * tl4.w);
+        }
+        const float d00 = c0[b].x * a.inv_n - y0.x, d01 = c0[b].y * a.inv_n - y0.y;
+        const float d10 = c1[b].x * a.inv_n - y1.x, d11 = c1[b].y * a.inv_n - y1.y;
+        uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
+        *reinterpret_cast<uint32_t*>(o + e0) = f2_to_bf16x2(d00, d01);
+        *reinterpret_cast<uint32_t*>(o + e1) = f2_to_bf16x2(d10, d11);
+        tile[e0][tl] = d00; tile[e0 + 1][tl] = d01; tile[e1][tl] = d10; tile[e1 + 1][tl] = d11;
+      }
     }
   }
   __syncthreads();
-  for (int it = threadIdx.x; it < sg.W * (kDeltaTokens / 2); it += blockDim.x) {   // transposed rows
-    const int f = it / (kDeltaTokens / 2), tp = 2 * (it - (it / (kDeltaTokens / 2)) * (kDeltaTokens / 2));
-    const int t = t0 + tp;
+  // transposed rows: 8 tokens (16 bytes) per store; tokens past T land in the
+  // row padding (Tp rounds T + 1 up to a multiple of 8) and are never read back
+  for (int it = threadIdx.x; it < sg.W * (kDeltaTokens / 8); it += blockDim.x) {
+    const int f = it / (kDeltaTokens / 8), t8 = 8 * (it - (it / (kDeltaTokens / 8)) * (kDeltaTokens / 8));
+    const int t = t0 + t8;
     if (t >= a.T) continue;
-    // a token past T lands in the row's padding (Tp >= T + 1), never read back
-    *reinterpret_cast<uint32_t*>(out_t + (int64_t)(sg.f0 + f) * a.Tp + t) = f2_to_bf16x2(tile[f][tp], tile[f][tp + 1]);
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = tile[f][t8 + i];
+    *reinterpret_cast<uint4*>(out_t + (int64_t)(sg.f0 + f) * a.Tp + t) = f_to_bf16x8(v);
   }
 }
 
@@ -291,6 +360,7 @@ struct PassArgs {
   int64_t sO;         // out layer stride (elements)
   int M, K, kp;
   int b_layered;      // B has one matrix per layer (else layer 0 for all)
+  int kb_per_split;   // contraction blocks of 64 per slice (blockIdx.y); slices add into a zeroed out
   uint32_t* status;
 };
 
@@ -329,9 +399,11 @@ __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const int l = blockIdx.y;
+  const int l = blockIdx.z;
   const int m0 = blockIdx.x * kTile;
-  const int nk = (a.K + kPassK - 1) / kPassK;
+  const int kb0 = blockIdx.y * a.kb_per_split;
+  const int nk = max(0, min((a.K + kPassK - 1) / kPassK - kb0, a.kb_per_split));
+  const bool split = gridDim.y > 1;
   volatile int* abort_p = &abort_flag;
 
   if (warp == 0) {
@@ -343,8 +415,8 @@ __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_cons
         if (kb >= kPassStages && !wait_phase(empty(st), ((kb / kPassStages) - 1) & 1, abort_p, a.status)) break;
         const uint32_t sa = base + st * stage_bytes;
         mbar_expect_tx(full(st), stage_bytes);
-        tma_load_3d(sa, &map_a, full(st), kb * kPassK, m0, l);
-        tma_load_3d(sa + a_bytes, &map_b, full(st), kb * kPassK, 0, lb);
+        tma_load_3d(sa, &map_a, full(st), (kb0 + kb) * kPassK, m0, l);
+        tma_load_3d(sa + a_bytes, &map_b, full(st), (kb0 + kb) * kPassK, 0, lb);
         ++issued;
       }
       // every issued copy must land before the CTA may exit
@@ -381,8 +453,11 @@ __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_cons
         tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
         if (m0 + row < a.M) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(o + c0 + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int q = 0; q < 4; ++q) {
+            const float4 f4 = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            if (split) atomicAdd(reinterpret_cast<float4*>(o + c0 + 4 * q), f4);
+            else *reinterpret_cast<float4*>(o + c0 + 4 * q) = f4;
+          }
         }
       }
     }
@@ -396,25 +471,16 @@ __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
-// 3. tall_kernel: out[r][c] = sum_s A(r, s) X[s][c] for c < 8 CN, fp32 on the
-//    CUDA cores, batched over layers (blockIdx.z).  Rows mode: A(r, s) =
-//    A[r * lda + s]; cols mode: A(r, s) = A[s * lda + r] (the product with A
-//    transposed).  X is [S][ldx].  One CTA owns 128 output rows and one slice
-//    of the contraction; several slices (blockIdx.y) add into a zeroed output
-//    with float2 atomics.  With out_t set (one slice only) the result is
-//    written instead as bf16 transposed rows out_t[c][r].
+// 3. Skinny fp32 products on the CUDA cores (the k x k side of the method).
+//    gram_kernel:  G[l] += X[l]^T X[l] over a slice of rows, X [R][KP] fp32;
+//                  threads form a 16 x 16 grid over G, rows stream through
+//                  shared memory in double-buffered chunks of 64 (cp.async);
+//                  slices add into a zeroed G.
+//    apply_kernel: out[l][r] = X[l][r] M[l] (M KP x KP), one thread per row,
+//                  M read from shared memory as broadcast float4 rows; with
+//                  `upper` M is upper triangular and its zero half is skipped.
+//                  Output fp32 rows [R][KP], or bf16 transposed rows [KP][ldt].
 // ---------------------------------------------------------------------------
-struct TallArgs {
-  const float* A;
-  const float* X;
-  float* out;
-  uint16_t* out_t;
-  int64_t sA, sX, sO, sT;  // per-layer strides (elements); sX = 0 shares X
-  int lda, ldx, ldo, ldt;
-  int R, S;                // output rows; contraction length
-  int s_per_split;         // multiple of kStep
-};
-
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(valid ? 16 : 0)
@@ -424,133 +490,97 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-// rows mode: A tile [128 rows][32 s], row pitch 36; cols mode: [32 s][128 r], pitch 132
-__host__ __device__ constexpr int a_pitch(bool cols) { return cols ? kTile + 4 : kStep + 4; }
-__host__ __device__ constexpr int a_floats(bool cols) { return cols ? kStep * a_pitch(true) : kTile * a_pitch(false); }
-constexpr size_t tall_smem_bytes(int cn, bool cols) {
-  return sizeof(float) * kStages * (a_floats(cols) + kStep * 8 * cn);
+constexpr int kGramRows = 512;    // rows per CTA
+constexpr int kGramChunk = 64;    // rows per shared-memory stage
+
+template <int KP>
+__global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t sX, float* G, int64_t sG, int R) {
+  constexpr int S = KP / 16;
+  __shared__ __align__(16) float xs[2][kGramChunk][KP];
+  const int l = blockIdx.y;
+  const float* x = X + (int64_t)l * sX;
+  const int r0 = blockIdx.x * kGramRows;
+  const int r1 = min(R, r0 + kGramRows);
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  auto load = [&](int buf, int c0) {
+    for (int ch = tid; ch < kGramChunk * KP / 4; ch += kThreads) {
+      const int r = ch / (KP / 4), c4 = (ch - r * (KP / 4)) * 4;
+      const bool ok = c0 + r < r1;
+      cp_async16(&xs[buf][r][c4], ok ? x + (int64_t)(c0 + r) * KP + c4 : x, ok);
+    }
+    cp_async_commit();
+  };
+  float acc[S][S] = {};
+  const int n_chunks = (r1 - r0 + kGramChunk - 1) / kGramChunk;
+  if (n_chunks > 0) load(0, r0);
+  for (int c = 0; c < n_chunks; ++c) {
+    if (c + 1 < n_chunks) {
+      load((c + 1) & 1, r0 + (c + 1) * kGramChunk);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const float(*xb)[KP] = xs[c & 1];
+#pragma unroll 4
+    for (int r = 0; r < kGramChunk; ++r) {
+      float a[S], b[S];
+#pragma unroll
+      for (int i = 0; i < S; ++i) { a[i] = xb[r][ty + 16 * i]; b[i] = xb[r][tx + 16 * i]; }
+#pragma unroll
+      for (int i = 0; i < S; ++i)
+#pragma unroll
+        for (int j = 0; j < S; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  float* g = G + (int64_t)l * sG;
+#pragma unroll
+  for (int i = 0; i < S; ++i)
+#pragma unroll
+    for (int j = 0; j < S; ++j) atomicAdd(&g[(ty + 16 * i) * KP + tx + 16 * j], acc[i][j]);
 }
 
-template <int CN, bool kCols>
-__global__ void __launch_bounds__(kThreads, 2) tall_kernel(TallArgs g) {
-  constexpr int KP = 8 * CN;                        // columns of X and out
-  constexpr int AP = a_pitch(kCols);
-  constexpr int AF = a_floats(kCols);
-  constexpr int XF = kStep * KP;
-  extern __shared__ __align__(16) float sm[];
-  const int l = blockIdx.z;
-  const float* A = g.A + (int64_t)l * g.sA;
-  const float* X = g.X + (int64_t)l * g.sX;
-  const int r0 = blockIdx.x * kTile;
-  const int s_begin = blockIdx.y * g.s_per_split;
-  const int s_end = min(g.S, s_begin + g.s_per_split);
-  const int n_steps = s_end > s_begin ? (s_end - s_begin + kStep - 1) / kStep : 0;
-  const int tid = threadIdx.x;
-  const int cg = tid & 7, rg = tid >> 3;
-
-  auto load = [&](int slot, int step) {
-    float* As = sm + slot * (AF + XF);
-    float* Xs = As + AF;
-    const int s0 = s_begin + step * kStep;
+template <int KP>
+__global__ void __launch_bounds__(128) apply_kernel(const float* X, int64_t sX, const float* M, int64_t sM, float* out,
+                                                    int64_t sO, uint16_t* out_t, int64_t sT, int ldt, int R, int upper) {
+  __shared__ __align__(16) float ms[KP][KP];
+  const int l = blockIdx.y;
+  const float* m = M + (int64_t)l * sM;
+  for (int e = threadIdx.x; e < KP * KP / 4; e += blockDim.x)
+    reinterpret_cast<float4*>(&ms[0][0])[e] = reinterpret_cast<const float4*>(m)[e];
+  __syncthreads();
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  const float* x = X + (int64_t)l * sX + (int64_t)r * KP;
+  float xv[KP], o[KP];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {                   // 1024 16-byte chunks of A
-      const int ch = tid + j * kThreads;
-      if (!kCols) {
-        const int row = ch >> 3, s4 = (ch & 7) * 4;
-        const bool ok = r0 + row < g.R && s0 + s4 < s_end;
-        cp_async16(As + row * AP + s4, ok ? A + (int64_t)(r0 + row) * g.lda + s0 + s4 : A, ok);
-      } else {
-        const int s = ch >> 5, r4 = (ch & 31) * 4;
-        const bool ok = s0 + s < s_end && r0 + r4 < g.R;
-        cp_async16(As + s * AP + r4, ok ? A + (int64_t)(s0 + s) * g.lda + r0 + r4 : A, ok);
-      }
-    }
-    for (int ch = tid; ch < kStep * KP / 4; ch += kThreads) {   // X rows s0 .. s0+31
-      const int s = ch / (KP / 4), c4 = (ch % (KP / 4)) * 4;
-      const bool ok = s0 + s < s_end;
-      cp_async16(Xs + s * KP + c4, ok ? X + (int64_t)(s0 + s) * g.ldx + c4 : X, ok);
-    }
-  };
-
-  float2 acc[4][CN / 2];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < CN / 2; ++j) acc[i][j] = make_float2(0.f, 0.f);
-
-#pragma unroll
-  for (int st = 0; st < kStages - 1; ++st) {
-    if (st < n_steps) load(st, st);
-    cp_async_commit();
+  for (int i = 0; i < KP; i += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(x + i);
+    xv[i] = v.x; xv[i + 1] = v.y; xv[i + 2] = v.z; xv[i + 3] = v.w;
   }
-  for (int it = 0; it < n_steps; ++it) {
-    cp_async_wait<kStages - 2>();
-    __syncthreads();
-    if (it + kStages - 1 < n_steps) load((it + kStages - 1) % kStages, it + kStages - 1);
-    cp_async_commit();
-    const float* As = sm + (it % kStages) * (AF + XF);
-    const float* Xs = As + AF;
-    if (!kCols) {
-      // thread rows rg + 32 i: per warp quarter four rows one apart -> distinct bank groups
 #pragma unroll
-      for (int s4 = 0; s4 < kStep; s4 += 4) {
-        float4 av[4];
+  for (int j = 0; j < KP; ++j) o[j] = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) av[i] = *reinterpret_cast<const float4*>(As + (rg + 32 * i) * AP + s4);
+  for (int i = 0; i < KP; ++i) {
 #pragma unroll
-        for (int ss = 0; ss < 4; ++ss) {
-          float2 x[CN / 2];
-#pragma unroll
-          for (int j = 0; j < CN / 2; ++j)
-            x[j] = *reinterpret_cast<const float2*>(Xs + (s4 + ss) * KP + cg * CN + 2 * j);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float v = ss == 0 ? av[i].x : ss == 1 ? av[i].y : ss == 2 ? av[i].z : av[i].w;
-            const float2 v2 = make_float2(v, v);
-#pragma unroll
-            for (int j = 0; j < CN / 2; ++j) acc[i][j] = __ffma2_rn(v2, x[j], acc[i][j]);
-          }
-        }
-      }
-    } else {
-      // thread rows 4 rg + i: one float4 of A per contraction index
-#pragma unroll 8
-      for (int s = 0; s < kStep; ++s) {
-        const float4 av = *reinterpret_cast<const float4*>(As + s * AP + 4 * rg);
-        float2 x[CN / 2];
-#pragma unroll
-        for (int j = 0; j < CN / 2; ++j) x[j] = *reinterpret_cast<const float2*>(Xs + s * KP + cg * CN + 2 * j);
-        const float a4[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 v2 = make_float2(a4[i], a4[i]);
-#pragma unroll
-          for (int j = 0; j < CN / 2; ++j) acc[i][j] = __ffma2_rn(v2, x[j], acc[i][j]);
-        }
-      }
+    for (int j4 = 0; j4 < KP; j4 += 4) {
+      if (upper && j4 + 3 < i) continue;   // an upper-triangular M has zeros left of its diagonal
+      const float4 mv = *reinterpret_cast<const float4*>(&ms[i][j4]);
+      o[j4] = fmaf(xv[i], mv.x, o[j4]);
+      o[j4 + 1] = fmaf(xv[i], mv.y, o[j4 + 1]);
+      o[j4 + 2] = fmaf(xv[i], mv.z, o[j4 + 2]);
+      o[j4 + 3] = fmaf(xv[i], mv.w, o[j4 + 3]);
     }
   }
-  cp_async_wait<0>();
-  const bool split = gridDim.y > 1;
+  if (out_t) {
+    uint16_t* ot = out_t + (int64_t)l * sT + r;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int r = r0 + (kCols ? 4 * rg + i : rg + 32 * i);
-    if (r >= g.R) continue;
-    if (g.out_t) {
-      uint16_t* ot = g.out_t + (int64_t)l * g.sT + r;
+    for (int j = 0; j < KP; ++j) ot[(int64_t)j * ldt] = f_to_bf16(o[j]);
+  } else {
+    float* op = out + (int64_t)l * sO + (int64_t)r * KP;
 #pragma unroll
-      for (int j = 0; j < CN / 2; ++j) {
-        ot[(int64_t)(cg * CN + 2 * j) * g.ldt] = f_to_bf16(acc[i][j].x);
-        ot[(int64_t)(cg * CN + 2 * j + 1) * g.ldt] = f_to_bf16(acc[i][j].y);
-      }
-    } else {
-      float* o = g.out + (int64_t)l * g.sO + (int64_t)r * g.ldo + cg * CN;
-#pragma unroll
-      for (int j = 0; j < CN / 2; ++j) {
-        if (split) atomicAdd(reinterpret_cast<float2*>(o + 2 * j), acc[i][j]);
-        else *reinterpret_cast<float2*>(o + 2 * j) = acc[i][j];
-      }
-    }
+    for (int j = 0; j < KP; j += 4) *reinterpret_cast<float4*>(op + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
   }
 }
 
@@ -960,48 +990,67 @@ class Runner {
       map_fail = true;
       return;
     }
-    PassArgs pa{out, sO, M, K, kp_, b_layered ? 1 : 0, status_};
-    pass_kernel<<<dim3((M + kTile - 1) / kTile, L_), kPassThreads, pass_smem_bytes(kp_), st_>>>(ma, mb, pa);
-    err = cudaGetLastError();
-  }
-
-  // out[L][R][kp] = A(R x S) X(S x kp) on the CUDA cores; cols: A is stored
-  // [S][lda] and read transposed.  out_t: bf16 transposed output instead.
-  void tall(bool cols, const float* A, int64_t sA, int lda, const float* X, int64_t sX, int ldx, float* out,
-            int64_t sO, int R, int S, uint16_t* out_t = nullptr, int64_t sT = 0, int ldt = 0) {
-    if (err != cudaSuccess) return;
-    const int tiles = (R + kTile - 1) / kTile;
-    // Contraction slices per output tile: each slice keeps >= 4 steps, and the
-    // CTA count should fill whole waves of the resident slots (2 per SM).
+    // Contraction slices: when tiles x layers cannot fill the resident CTA
+    // slots (2 per SM), split K, each slice keeping >= 8 blocks of 64.
+    const int tiles = (M + kTile - 1) / kTile;
+    const int nkb = (K + kPassK - 1) / kPassK;
     const int cap = 2 * sms_;
-    const int max_splits = out_t ? 1 : std::max(1, (S + 4 * kStep - 1) / (4 * kStep));
-    int splits = 1, per = S;
+    int splits = 1, per = nkb;
     double best = -1.0;
-    for (int sp = 1; sp <= max_splits; ++sp) {
-      const int pr = ((S + sp - 1) / sp + kStep - 1) / kStep * kStep;
-      const int n = (S + pr - 1) / pr;
+    for (int sp = 1; sp <= std::max(1, nkb / 8); ++sp) {
+      const int pr = (nkb + sp - 1) / sp;
+      const int n = (nkb + pr - 1) / pr;
       if (n != sp) continue;
       const int64_t total = (int64_t)tiles * L_ * n;
       const int64_t waves = (total + cap - 1) / cap;
-      // fraction of slot-time used, with a small preference for fewer atomics
-      const double score = (double)total / (double)(waves * cap) - 0.002 * n;
+      const double score = (double)total / (double)(waves * cap) - 0.01 * n;
       if (score > best + 1e-9) { best = score; splits = n; per = pr; }
     }
     if (splits > 1) {
-      err = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)(sO * (L_ - 1) + (int64_t)R * kp_), st_);
+      err = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)(sO * (L_ - 1) + (int64_t)M * kp_), st_);
       if (err != cudaSuccess) return;
     }
-    TallArgs g{A, X, out, out_t, sA, sX, sO, sT, lda, ldx, kp_, ldt, R, S, per};
-    dim3 grid(tiles, splits, L_);
-    switch (kp_ / 8) {
-      case 2: launch<2>(cols, grid, g); break;
-      case 4: launch<4>(cols, grid, g); break;
-      case 6: launch<6>(cols, grid, g); break;
-      case 8: launch<8>(cols, grid, g); break;
-      case 10: launch<10>(cols, grid, g); break;
-      case 12: launch<12>(cols, grid, g); break;
-      default: err = cudaErrorInvalidValue;
+    PassArgs pa{out, sO, M, K, kp_, b_layered ? 1 : 0, per, status_};
+    pass_kernel<<<dim3(tiles, splits, L_), kPassThreads, pass_smem_bytes(kp_), st_>>>(ma, mb, pa);
+    err = cudaGetLastError();
+  }
+
+  // G[L][kp][kp] = X^T X for X [L][R][kp]
+  void gram(const float* X, int64_t sX, float* G, int R) {
+    if (err != cudaSuccess) return;
+    const int64_t skk = (int64_t)kp_ * kp_;
+    err = cudaMemsetAsync(G, 0, sizeof(float) * (size_t)(skk * L_), st_);
+    if (err != cudaSuccess) return;
+    const dim3 grid((R + kGramRows - 1) / kGramRows, L_);
+    switch (kp_) {
+      case 16: gram_kernel<16><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
+      case 32: gram_kernel<32><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
+      case 48: gram_kernel<48><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
+      case 64: gram_kernel<64><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
+      case 80: gram_kernel<80><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
+      case 96: gram_kernel<96><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
+      default: err = cudaErrorInvalidValue; return;
     }
+    err = cudaGetLastError();
+  }
+
+  // out[L][R][kp] = X[L][R][kp] M[L][kp][kp] (fp32 rows), or bf16 transposed rows into out_t
+  void apply(const float* X, int64_t sX, const float* M, float* out, int64_t sO, int R, bool upper,
+             uint16_t* out_t = nullptr, int64_t sT = 0, int ldt = 0) {
+    if (err != cudaSuccess) return;
+    const int64_t skk = (int64_t)kp_ * kp_;
+    const dim3 grid((R + 127) / 128, L_);
+    const int up = upper ? 1 : 0;
+    switch (kp_) {
+      case 16: apply_kernel<16><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 32: apply_kernel<32><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 48: apply_kernel<48><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 64: apply_kernel<64><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 80: apply_kernel<80><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 96: apply_kernel<96><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      default: err = cudaErrorInvalidValue; return;
+    }
+    err = cudaGetLastError();
   }
 
   // X [L][R][kp] <- orth(X) by rounds of shifted Cholesky QR (the first with
@@ -1009,15 +1058,13 @@ class Runner {
   // set, the last round writes bf16 X^T [kp][ldt] there instead of X.
   void orth(float*& X, float*& tmp, int64_t sX, int R, int k, int rounds, float first, float* g, float* rinv,
             uint16_t* out_t = nullptr, int64_t sT = 0, int ldt = 0) {
-    const int64_t skk = (int64_t)kp_ * kp_;
     for (int r = 0; r < rounds && err == cudaSuccess; ++r) {
-      tall(true, X, sX, kp_, X, sX, kp_, g, skk, kp_, R);                      // G = X^T X
-      if (err != cudaSuccess) return;
+      gram(X, sX, g, R);                                                      // G = X^T X
       chol(g, rinv, k, r == 0 ? first : kShiftSecond);
       if (r == rounds - 1 && out_t) {
-        tall(false, X, sX, kp_, rinv, skk, kp_, nullptr, 0, R, kp_, out_t, sT, ldt);   // (X R^-1)^T in bf16
+        apply(X, sX, rinv, nullptr, 0, R, true, out_t, sT, ldt);              // (X R^-1)^T in bf16
       } else {
-        tall(false, X, sX, kp_, rinv, skk, kp_, tmp, sX, R, kp_);                     // X R^-1
+        apply(X, sX, rinv, tmp, sX, R, true);                                 // X R^-1
         std::swap(X, tmp);
       }
     }
@@ -1054,31 +1101,10 @@ class Runner {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, jac);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem_bytes(kMaxK));
-    if (e == cudaSuccess) e = set_tall<2>();
-    if (e == cudaSuccess) e = set_tall<4>();
-    if (e == cudaSuccess) e = set_tall<6>();
-    if (e == cudaSuccess) e = set_tall<8>();
-    if (e == cudaSuccess) e = set_tall<10>();
-    if (e == cudaSuccess) e = set_tall<12>();
     return e;
   }
 
  private:
-  template <int CN>
-  static cudaError_t set_tall() {
-    cudaError_t e = cudaFuncSetAttribute(tall_kernel<CN, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tall_smem_bytes(CN, false));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tall_kernel<CN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)tall_smem_bytes(CN, true));
-    return e;
-  }
-  template <int CN>
-  void launch(bool cols, dim3 grid, const TallArgs& g) {
-    if (cols) tall_kernel<CN, true><<<grid, kThreads, tall_smem_bytes(CN, true), st_>>>(g);
-    else tall_kernel<CN, false><<<grid, kThreads, tall_smem_bytes(CN, false), st_>>>(g);
-    err = cudaGetLastError();
-  }
   cudaStream_t st_;
   int L_, kp_, sms_;
   uint32_t* status_;
@@ -1204,14 +1230,14 @@ kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* d
   // 3. Q = orth(Y); B^T = Delta^T Q; C = B B^T
   run.orth(y, y2, b.s_tk, T, k, 2, pf::kShiftFirst, b.g, b.rinv, b.st_t, b.s_st_t, (int)b.Tp);
   run.pass(b.delta_t, b.Tp, b.s_delta_t, b.st_t, b.Tp, b.s_st_t, true, z, b.s_dk, D, T);
-  run.tall(true, z, b.s_dk, kp, z, b.s_dk, kp, b.g, b.s_kk, kp, D);
+  run.gram(z, b.s_dk, b.g, D);
   // 4. eigenvectors of the m largest eigenvalues, scaled by lambda^-1/2
   if (run.err == cudaSuccess && !run.map_fail) {
     pf::jacobi_kernel<<<L, pf::kThreads, run.jacobi_smem(), st>>>(b.g, b.s_kk, b.w, b.s_kk, k, kp, m);
     run.err = cudaGetLastError();
   }
   // 5. V_m = orth(B^T W) (columns already near unit length) as bf16 V^T; U_m = Delta V_m
-  run.tall(false, z, b.s_dk, kp, b.w, b.s_kk, kp, z2, b.s_dk, D, kp);
+  run.apply(z, b.s_dk, b.w, z2, b.s_dk, D, false);
   run.orth(z2, z, b.s_dk, D, m, 1, pf::kShiftSecond, b.g, b.rinv, b.st_d, b.s_st_d, (int)b.Dp);
   run.pass(b.delta, b.Dp, b.s_delta, b.st_d, b.Dp, b.s_st_d, true, y2, b.s_tk, T, D);
   if (run.err == cudaSuccess && !run.map_fail) {
