@@ -53,6 +53,22 @@ class DeviceWorkload:
         self._chunks = self._chunk_args()
         self._batch_array = None
 
+    def replica(self) -> "DeviceWorkload":
+        """A second device copy of this workload (inputs, pools, status,
+        workspace), with launch arguments pointing at the copy."""
+        r = object.__new__(DeviceWorkload)
+        r.wl, r.device, r.host = self.wl, self.device, self.host
+        r.rows = {n: t.clone() for n, t in self.rows.items()}
+        r.u = {n: [None if t is None else t.clone() for t in ts] for n, ts in self.u.items()}
+        r.w = {n: [None if t is None else t.clone() for t in ts] for n, ts in self.w.items()}
+        r.block_tables = None if self.block_tables is None else self.block_tables.clone()
+        r.pools = {n: p.clone() for n, p in self.pools.items()}
+        r.status = torch.zeros_like(self.status)
+        r.workspace = None if self.workspace is None else torch.empty_like(self.workspace)
+        r._chunks = r._chunk_args()
+        r._batch_array = None
+        return r
+
     def reset_pools(self):
         for p in self.pools.values():
             p.view(torch.int16).fill_(SENTINEL)
