@@ -33,10 +33,12 @@ from .kamera import (
     conditioning, placement, run_workload, chunk_layer_rows,
 )
 from .patch_svd import svd_patch, eckart_young_tail, conditioning_deficit, orbit_deficit
+from .attend import attention, attend_relocated, attend_conditioning, relocated_chunk
 
 __all__ = [
     "bf16_bits_to_f64", "round_to_bf16_bits", "bf16_ord", "ulp_distance", "bf16_ulp",
     "inv_freq", "rope_absolute", "mrope_absolute", "pair_shifts", "relocate", "patch_product", "row_layout", "operator_rows",
     "conditioning", "placement", "run_workload", "chunk_layer_rows",
     "svd_patch", "eckart_young_tail", "conditioning_deficit", "orbit_deficit",
+    "attention", "attend_relocated", "attend_conditioning", "relocated_chunk",
 ]
