@@ -575,6 +575,141 @@ def run_patch_cpu_baseline(cfg: int, budget_s: float) -> dict:
     return json.loads(res.stdout.strip().splitlines()[-1])
 
 
+# --------------------------------------------------------------------------- #
+# fused read: decode attention over relocated, patched chunks (no relocated cache)
+# --------------------------------------------------------------------------- #
+ATTN_METRIC = "relocated-chunk decode attention: context tokens/s (one query token per sequence, one layer)"
+ATTN_SHAPE = dict(seqs=16, chunks=4, tokens=4096, Hq=28, Hkv=4, d=128, rank=32, theta=1e6)
+
+
+def attn_text(a) -> str:
+    return (f"one layer of a Qwen2.5-VL-shaped GQA model ({a['Hq']} query / {a['Hkv']} KV heads x {a['d']}): "
+            f"{a['seqs']} sequences, each {a['chunks']} relocated chunks x {a['tokens']} tokens with rank-{a['rank']} "
+            f"K and V patches, theta {a['theta']:g}")
+
+
+def attn_bytes(a) -> int:
+    n_chunks = a["seqs"] * a["chunks"]
+    D = a["Hkv"] * a["d"]
+    per_chunk = a["tokens"] * D * 2 * 2 + a["tokens"] * a["rank"] * 2 * 2 + D * a["rank"] * 2 * 2
+    return n_chunks * per_chunk + a["seqs"] * a["Hq"] * a["d"] * 2 * 2
+
+
+def bench_attend(args) -> dict:
+    import torch
+    import position_invariant_kv_gb300 as kvrp
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    torch.cuda.set_device(local)
+    from position_invariant_kv_gb300.build import build
+    build()
+    kvrp.lib()
+    a = dict(ATTN_SHAPE)
+    dev = f"cuda:{local}"
+    g = torch.Generator(device=dev).manual_seed(4242)
+    D = a["Hkv"] * a["d"]
+    n_chunks = a["seqs"] * a["chunks"]
+
+    def rnd(*shape, std=1.0):
+        return (std * torch.randn(shape, generator=g, device=dev)).to(torch.bfloat16)
+
+    keep, chunks = [], []
+    for i in range(n_chunks):
+        t = [rnd(a["tokens"], D), rnd(a["tokens"], D), rnd(a["tokens"], a["rank"], std=0.3),
+             rnd(D, a["rank"], std=0.1), rnd(a["tokens"], a["rank"], std=0.3), rnd(D, a["rank"], std=0.1)]
+        keep += t
+        chunks.append(kvrp.AttnChunk(k=t[0], v=t[1], n_tokens=a["tokens"], delta=(i * 7919) % 65536 - 32768,
+                                     rank=a["rank"], uk=t[2], vk=t[3], uv=t[4], vv=t[5]))
+    arr = kvrp.attn_chunk_array(chunks)
+    seq_chunks = [s * a["chunks"] for s in range(a["seqs"] + 1)]
+    q = rnd(a["seqs"], a["Hq"], a["d"])
+    out = torch.empty_like(q)
+    ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([a["tokens"]] * n_chunks, a["Hq"], a["d"]),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        kvrp.kv_attend_relocated(q, arr, seq_chunks, n_q_heads=a["Hq"], n_kv_heads=a["Hkv"], head_dim=a["d"],
+                                 rope_theta=a["theta"], softmax_scale=a["d"] ** -0.5, out=out, workspace=ws,
+                                 stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / args.steps
+    nb = attn_bytes(a)
+    peaks = measured_peaks()
+    achieved = nb / (ms / 1e3) / 1e9
+    ctx = a["seqs"] * a["chunks"] * a["tokens"]
+    out_line = {
+        "metric": ATTN_METRIC, "value": ctx / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic", "row": "attend",
+        "config": {"workload": attn_text(a), "context_tokens_per_step": ctx, "algorithmic_bytes_per_step": nb,
+                   "l2": f"inputs larger than L2 ({nb / 1e6:.0f} MB read per step vs 129 MB L2)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                     "kernel": "kv_attend_relocated, whole call (table, block and combine kernels)",
+                     "peak_source": peaks["source"]},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        out_line["cpu_baseline"] = run_attn_cpu_baseline(args.budget)
+    return out_line
+
+
+def attn_cpu_worker(budget_s: float) -> dict:
+    """The fp64 oracle (materialised K^, V^ and softmax) on whole sequences of
+    the bench shape until the budget is spent."""
+    import numpy as np
+    from oracle import attend_relocated, round_to_bf16_bits
+    a = dict(ATTN_SHAPE)
+    rng = np.random.default_rng(4242)
+    D = a["Hkv"] * a["d"]
+    elapsed, n = 0.0, 0
+    while elapsed < budget_s:
+        cs = []
+        for i in range(a["chunks"]):
+            cs.append({"k": round_to_bf16_bits(rng.standard_normal((a["tokens"], D))),
+                       "v": round_to_bf16_bits(rng.standard_normal((a["tokens"], D))), "delta": 1000 * i,
+                       "uk": round_to_bf16_bits(0.3 * rng.standard_normal((a["tokens"], a["rank"]))),
+                       "vk": round_to_bf16_bits(0.1 * rng.standard_normal((D, a["rank"]))),
+                       "uv": round_to_bf16_bits(0.3 * rng.standard_normal((a["tokens"], a["rank"]))),
+                       "vv": round_to_bf16_bits(0.1 * rng.standard_normal((D, a["rank"])))})
+        q = round_to_bf16_bits(rng.standard_normal(a["Hq"] * a["d"]))
+        t0 = time.perf_counter()
+        attend_relocated(q, cs, a["Hq"], a["Hkv"], a["d"], a["theta"], a["d"] ** -0.5)
+        elapsed += time.perf_counter() - t0
+        n += 1
+    ctx = n * a["chunks"] * a["tokens"]
+    return {"value": ctx / elapsed, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} sequences of {a['chunks']} x {a['tokens']} tokens (fp64 NumPy, one thread, "
+                      f"{elapsed:.1f} s)"}
+
+
+def run_attn_cpu_baseline(budget_s: float) -> dict:
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-worker", "--row",
+                          "attend", "--budget", str(budget_s)], capture_output=True, text=True, env=env, timeout=900)
+    if res.returncode != 0:
+        tail = res.stderr.strip().splitlines()[-1] if res.stderr.strip() else "no output"
+        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": "failed: " + tail}
+    return json.loads(res.stdout.strip().splitlines()[-1])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -587,13 +722,17 @@ def main():
     ap.add_argument("--budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
-    ap.add_argument("--row", choices=["relocate", "patch_form"], default="relocate",
-                    help="relocate: the reuse operator (the headline); patch_form: forming the patch factors")
+    ap.add_argument("--row", choices=["relocate", "patch_form", "attend"], default="relocate",
+                    help="relocate: the reuse operator (the headline); patch_form: forming the patch factors; "
+                         "attend: decode attention over relocated chunks without materialising them")
     ap.add_argument("--orbit", type=int, default=1, help="patch_form: conditioned caches averaged (orbit patch)")
     ap.add_argument("--oversample", type=int, default=16, help="patch_form: range-finder oversampling")
     ap.add_argument("--power-iters", type=int, default=2, help="patch_form: subspace iterations")
     args = ap.parse_args()
     if args.cpu_baseline_worker:
+        if args.row == "attend":
+            print(json.dumps(attn_cpu_worker(args.budget)))
+            return
         worker = patch_cpu_worker if args.row == "patch_form" else cpu_baseline_worker
         print(json.dumps(worker(args.config, args.budget)))
         return
@@ -602,6 +741,21 @@ def main():
     if args.impl == "reference":
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[k] = "1"
+    if args.row == "attend":
+        if args.impl == "reference":
+            rank, world, _ = dist_env()
+            if rank != 0:
+                return
+            cb = attn_cpu_worker(args.budget)
+            out = {"metric": ATTN_METRIC, "value": cb["value"], "unit": "tokens/s", "n_gpus": world,
+                   "impl": "reference", "higher_is_better": True, "dtype": "f64", "data": "synthetic", "row": "attend",
+                   "config": {"workload": attn_text(ATTN_SHAPE)}, "cpu_baseline": cb,
+                   "e2e": {"value": cb["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        else:
+            out = bench_attend(args)
+        if out is not None:
+            print(json.dumps(out))
+        return
     if args.row == "patch_form":
         if args.impl == "reference":
             rank, world, _ = dist_env()

@@ -297,6 +297,58 @@ kvrp_status kv_patch_form_orbit(
     void* u_out, void* v_out, int64_t u_layer_stride, int64_t v_layer_stride,
     void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream);
 
+/*
+ * Decode attention over relocated, patched chunks, without writing the
+ * relocated cache (the fused read-side use of the operator of Kamera, section 2:
+ * a chunk cached as KV(B|empty) is read as K^ = R(delta) K + U_k V_k^T and
+ * V^ = V + U_v V_v^T).  For one new query token per sequence,
+ *     out[s][j] = softmax(softmax_scale * q[s][j] . K^_s) V^_s
+ * over the concatenated chunks of sequence s, query head j reading KV head
+ * j / (n_q_heads / n_kv_heads).  The query is rotated by R(-delta) once per
+ * chunk and the key patch enters as (V_k^T q) . u_k,t, so a token costs its
+ * canonical k_t, v_t and the rank-m rows u_k,t, u_v,t.
+ *   q           device bf16 [n_seqs][n_q_heads][head_dim].
+ *   chunks      host array of n_chunks (1..KVRP_ATTN_MAX_CHUNKS) kvrp_attn_chunk,
+ *               ordered by sequence: sequence s owns chunks
+ *               [seq_chunks[s], seq_chunks[s + 1]) (host array of n_seqs + 1,
+ *               from 0 to n_chunks, non-decreasing).
+ *   kvrp_attn_chunk.k, .v   device bf16 [n_tokens][n_kv_heads * head_dim] rows
+ *               of one layer; .rank 0 or a multiple of 16 up to 128; .uk, .uv
+ *               [n_tokens][rank], .vk, .vv [n_kv_heads * head_dim][rank] bf16
+ *               (all four, or none when rank is 0); .delta the shift.
+ *   head_dim    64 or 128; n_q_heads a multiple of n_kv_heads, at most 16x.
+ *   out         device bf16 [n_seqs][n_q_heads][head_dim]; a sequence with no
+ *               tokens gets zeros.
+ *   workspace   device scratch of kv_attend_relocated_workspace_size(...) bytes
+ *               (fp32 partial results and per-chunk rotation tables).
+ * Pointers 16-byte aligned.  Arithmetic fp32 on the bf16 inputs (rotation
+ * angles in fp64), output rounded once to bf16.  Errors (INVALID_ARG,
+ * ALIGNMENT, UNSUPPORTED, WORKSPACE) are returned before any CUDA work; CUDA
+ * on a launch failure.  Asynchronous on `stream`.
+ */
+#define KVRP_ATTN_MAX_CHUNKS 256
+
+typedef struct {
+  const void* k;
+  const void* v;
+  int32_t n_tokens;
+  int32_t rank;
+  int64_t delta;
+  const void* uk;
+  const void* vk;
+  const void* uv;
+  const void* vv;
+} kvrp_attn_chunk;
+
+size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk_tokens, int32_t n_q_heads,
+                                          int32_t head_dim);
+
+kvrp_status kv_attend_relocated(
+    const void* q, const kvrp_attn_chunk* chunks, int32_t n_chunks, const int32_t* seq_chunks,
+    int32_t n_seqs, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
+    double rope_theta, float softmax_scale, void* out,
+    void* workspace, size_t workspace_bytes, kvrp_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvrp_status_string(kvrp_status status);
 

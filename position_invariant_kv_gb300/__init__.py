@@ -10,6 +10,7 @@ CUDA kernel.  Names mirror the C ABI in include/kvrp.h:
     kv_relocate_batch_workspace_size
     kv_patch_form            rank-m factors of the conditioning deficit (patch formation)
     kv_patch_form_orbit      the same, deficit averaged over the orderings of a cached set
+    kv_attend_relocated      decode attention over relocated, patched chunks (never materialised)
 
 Tensors may be passed as torch CUDA tensors (their data_ptr is used) or as raw
 device addresses (int).  Streams default to torch's current stream.  A status
@@ -25,5 +26,7 @@ from ._abi import (  # noqa: F401
     kv_relocate_patch, kv_relocate_patch_mrope, kv_relocate_patch_mla, kv_relocate_batch, kv_relocate_batch_workspace_size,
     kvrp_status_string, kvrp_version, EXPORTED_SYMBOLS,
     kv_relocate_batch_noalloc, KVRP_NOALLOC_MAX_CHUNKS, chunk_array,
-    kv_patch_form, kv_patch_form_orbit, kv_patch_form_workspace_size, KVRP_ROPE_NONE, KVRP_ROPE_HEADS, KVRP_ROPE_MLA_TAIL,
+    kv_patch_form, kv_patch_form_orbit, kv_patch_form_workspace_size,
+    kv_attend_relocated, kv_attend_relocated_workspace_size, AttnChunk, attn_chunk_array, KVRP_ATTN_MAX_CHUNKS,
+    KVRP_ROPE_NONE, KVRP_ROPE_HEADS, KVRP_ROPE_MLA_TAIL,
 )

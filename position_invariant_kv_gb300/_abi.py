@@ -21,13 +21,23 @@ KVRP_DEV_TIMEOUT = 0x2
 EXPORTED_SYMBOLS = (
     "kv_relocate_patch", "kv_relocate_patch_mrope", "kv_relocate_patch_mla", "kv_relocate_batch",
     "kv_relocate_batch_workspace_size", "kv_relocate_batch_noalloc", "kv_patch_form_workspace_size",
-    "kv_patch_form", "kv_patch_form_orbit", "kvrp_status_string",
+    "kv_patch_form", "kv_patch_form_orbit", "kv_attend_relocated_workspace_size", "kv_attend_relocated",
+    "kvrp_status_string",
     "kvrp_last_error", "kvrp_version",
 )
 KVRP_NOALLOC_MAX_CHUNKS = 256
 KVRP_ROPE_NONE = 0
 KVRP_ROPE_HEADS = 1
 KVRP_ROPE_MLA_TAIL = 2
+
+
+KVRP_ATTN_MAX_CHUNKS = 256
+
+
+class kvrp_attn_chunk(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("n_tokens", C.c_int32), ("rank", C.c_int32),
+                ("delta", C.c_int64), ("uk", C.c_void_p), ("vk", C.c_void_p), ("uv", C.c_void_p),
+                ("vv", C.c_void_p)]
 
 
 class kvrp_dst(C.Structure):
@@ -88,6 +98,12 @@ def _load_library():
         C.POINTER(C.c_void_p), C.POINTER(C.c_int64), C.c_int32, C.c_void_p, C.c_int64, C.c_int64, C.c_int32,
         C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
         C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
+    L.kv_attend_relocated_workspace_size.restype = C.c_size_t
+    L.kv_attend_relocated_workspace_size.argtypes = [C.c_int32, C.POINTER(C.c_int32), C.c_int32, C.c_int32]
+    L.kv_attend_relocated.restype = st
+    L.kv_attend_relocated.argtypes = [
+        C.c_void_p, C.POINTER(kvrp_attn_chunk), C.c_int32, C.POINTER(C.c_int32), C.c_int32, C.c_int32, C.c_int32,
+        C.c_int32, C.c_double, C.c_float, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
     L.kvrp_status_string.restype = C.c_char_p
     L.kvrp_status_string.argtypes = [C.c_int]
     L.kvrp_last_error.restype = C.c_char_p
@@ -305,3 +321,48 @@ def kv_patch_form_orbit(conditioned, deltas, canonical, *, n_layers: int, n_toke
         int(n_tokens), int(row_width), int(rope_kind), int(rot_dim), float(rope_theta), int(rank),
         int(oversample), int(power_iters), _ptr(omega), _ptr(u_out), _ptr(v_out), int(u_layer_stride),
         int(v_layer_stride), _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))
+
+
+@dataclass
+class AttnChunk:
+    """One chunk of kv_attend_relocated (fields as in struct kvrp_attn_chunk)."""
+    k: object
+    v: object
+    n_tokens: int
+    delta: int = 0
+    rank: int = 0
+    uk: object = None
+    vk: object = None
+    uv: object = None
+    vv: object = None
+
+    def c(self) -> kvrp_attn_chunk:
+        return kvrp_attn_chunk(_ptr(self.k), _ptr(self.v), int(self.n_tokens), int(self.rank), int(self.delta),
+                               _ptr(self.uk), _ptr(self.vk), _ptr(self.uv), _ptr(self.vv))
+
+
+def kv_attend_relocated_workspace_size(chunk_tokens, n_q_heads: int, head_dim: int) -> int:
+    n = len(chunk_tokens)
+    arr = (C.c_int32 * max(n, 1))(*[int(t) for t in chunk_tokens])
+    return int(lib().kv_attend_relocated_workspace_size(n, arr, int(n_q_heads), int(head_dim)))
+
+
+def attn_chunk_array(chunks):
+    """ctypes array of kvrp_attn_chunk for kv_attend_relocated (reusable across calls)."""
+    arr = (kvrp_attn_chunk * max(len(chunks), 1))()
+    for i, c in enumerate(chunks):
+        arr[i] = c.c()
+    return arr, len(chunks)
+
+
+def kv_attend_relocated(q, chunks, seq_chunks, *, n_q_heads: int, n_kv_heads: int, head_dim: int, rope_theta: float,
+                        softmax_scale: float, out, workspace, workspace_bytes: Optional[int] = None,
+                        stream=None) -> None:
+    """Decode attention of one query token per sequence over relocated, patched chunks."""
+    arr, n = chunks if isinstance(chunks, tuple) else attn_chunk_array(chunks)
+    sc = (C.c_int32 * len(seq_chunks))(*[int(v) for v in seq_chunks])
+    if workspace_bytes is None:
+        workspace_bytes = int(workspace.numel() * workspace.element_size())
+    _check(lib().kv_attend_relocated(
+        _ptr(q), arr, n, sc, len(seq_chunks) - 1, int(n_q_heads), int(n_kv_heads), int(head_dim), float(rope_theta),
+        float(softmax_scale), _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream)))

@@ -2,7 +2,7 @@
 
     python -m position_invariant_kv_gb300.build [-v]
 
-One nvcc invocation, three translation units compiled in parallel, one
+One nvcc invocation, four translation units compiled in parallel, one
 -gencode (sm_103a).  The shared object lands next to this file and is
 git-ignored.
 """
@@ -16,14 +16,14 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libkvrp.so")
 SOURCES = [os.path.join(HERE, "csrc", "kvrp_kernel.cu"), os.path.join(HERE, "csrc", "kvrp_patch_form.cu"),
-           os.path.join(HERE, "csrc", "kvrp_host.cpp")]
+           os.path.join(HERE, "csrc", "kvrp_attend.cu"), os.path.join(HERE, "csrc", "kvrp_host.cpp")]
 HEADERS = [os.path.join(ROOT, "include", "kvrp.h"), os.path.join(HERE, "csrc", "kvrp_plan.h")]
 
 
 def nvcc_command(out: str = LIB, ptxas_verbose: bool = False) -> list:
     cmd = [
         "nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",
-        "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "--threads", "3",
+        "-shared", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2", "--threads", "4",
         "-I", os.path.join(ROOT, "include"), "-I", os.path.join(HERE, "csrc"),
         "-o", out,
     ]

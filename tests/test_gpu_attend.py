@@ -1,0 +1,134 @@
+"""GPU decode attention over relocated, patched chunks (kv_attend_relocated)
+against the fp64 oracle, element by element.
+
+The oracle materialises K^ = R(delta) K + U_k V_k^T and V^ = V + U_v V_v^T of
+every chunk in fp64 and evaluates softmax(scale q K^T) V^ (Kamera,
+gist.science/pt/paper/2606.23581, section 2, read side).  The kernel never
+forms K^ or V^: it rotates the query by R(-delta) and adds the rank-m terms.
+The bar: within 1 bf16 ulp of the oracle rounded once to bf16; an element off
+by more must still lie within ulp(ref) + 2^-14 * sum_t p_t |v^_t| (the fp32
+rounding of the scores and sums, bounded by that magnitude)."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from position_invariant_kv_gb300.build import build
+    build()
+
+
+def _dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def make_case(seed, seqs, Hq, Hkv, d):
+    """seqs: list of sequences, each a list of (n_tokens, rank) chunks."""
+    from oracle import round_to_bf16_bits
+    rng = np.random.default_rng(seed)
+    D = Hkv * d
+    q = round_to_bf16_bits(rng.standard_normal((len(seqs), Hq, d)))
+    chunks, seq_chunks = [], [0]
+    for s in seqs:
+        for (T, m) in s:
+            c = {"k": round_to_bf16_bits(rng.standard_normal((T, D))),
+                 "v": round_to_bf16_bits(rng.standard_normal((T, D))),
+                 "delta": int(rng.integers(-40000, 40001)), "rank": m}
+            if m:
+                c["uk"] = round_to_bf16_bits(0.3 * rng.standard_normal((T, m)))
+                c["vk"] = round_to_bf16_bits(0.1 * rng.standard_normal((D, m)))
+                c["uv"] = round_to_bf16_bits(0.3 * rng.standard_normal((T, m)))
+                c["vv"] = round_to_bf16_bits(0.1 * rng.standard_normal((D, m)))
+            chunks.append(c)
+        seq_chunks.append(len(chunks))
+    return q, chunks, seq_chunks
+
+
+def run_gpu(q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
+    import position_invariant_kv_gb300 as kvrp
+    keep = []
+    ac = []
+    for c in chunks:
+        T = c["k"].shape[0]
+        k = _dev(c["k"]) if T else torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+        v = _dev(c["v"]) if T else torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+        f = [(_dev(c[n]) if c["rank"] else None) for n in ("uk", "vk", "uv", "vv")]
+        keep += [k, v] + f
+        ac.append(kvrp.AttnChunk(k=k, v=v, n_tokens=T, delta=c["delta"], rank=c["rank"], uk=f[0], vk=f[1], uv=f[2],
+                                 vv=f[3]))
+    out = torch.empty((len(seq_chunks) - 1, Hq, d), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([c["k"].shape[0] for c in chunks], Hq, d),
+                     dtype=torch.uint8, device="cuda")
+    kvrp.kv_attend_relocated(_dev(q), ac, seq_chunks, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, rope_theta=theta,
+                             softmax_scale=scale, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    return _bits(out)
+
+
+def check(got, q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
+    from oracle import attend_conditioning, attend_relocated, bf16_bits_to_f64, bf16_ulp, round_to_bf16_bits
+    from oracle.bf16 import ulp_distance
+    worst = 0
+    for s in range(len(seq_chunks) - 1):
+        cs = [dict(c, **({} if c["rank"] else {"uk": None, "vk": None, "uv": None, "vv": None}))
+              for c in chunks[seq_chunks[s]:seq_chunks[s + 1]] if c["k"].shape[0] > 0]
+        g = got[s].reshape(-1)
+        if not cs:
+            assert np.all(bf16_bits_to_f64(g) == 0.0)
+            continue
+        ref = attend_relocated(q[s].reshape(-1), cs, Hq, Hkv, d, theta, scale)
+        cond = attend_conditioning(q[s].reshape(-1), cs, Hq, Hkv, d, theta, scale)
+        dist = ulp_distance(g, round_to_bf16_bits(ref))
+        err = np.abs(bf16_bits_to_f64(g) - ref)
+        bound = bf16_ulp(ref) + 2.0 ** -14 * cond
+        assert np.all((dist <= 1) | (err <= bound)), (s, int(dist.max()), float((err / bound).max()))
+        worst = max(worst, int(dist.max()))
+    return worst
+
+
+@pytest.mark.parametrize("seqs,Hq,Hkv,d", [
+    ([[(300, 32), (77, 0)], [(1, 0)], [(128, 16), (129, 32), (513, 16)]], 28, 4, 128),   # GQA, ragged, mixed ranks
+    ([[(200, 16), (64, 16)], [(1000, 32)]], 8, 8, 64),                                    # MHA, head_dim 64
+    ([[(260, 32)], [(17, 0), (300, 16)]], 32, 2, 128),                                    # 16 query heads per KV head
+])
+def test_attention_matches_oracle(seqs, Hq, Hkv, d):
+    theta, scale = 1e6, d ** -0.5
+    q, chunks, sc = make_case(7 + Hq, seqs, Hq, Hkv, d)
+    got = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale)
+    worst = check(got, q, chunks, sc, Hq, Hkv, d, theta, scale)
+    print("worst ulp distance", worst)
+
+
+def test_empty_sequences_and_chunks():
+    """A sequence with no chunks and one whose only chunk is empty get zeros;
+    an empty chunk between two others changes nothing."""
+    Hq, Hkv, d, theta, scale = 4, 2, 64, 1e4, 0.125
+    q, chunks, sc = make_case(91, [[(50, 16), (0, 0), (40, 0)], [], [(0, 0)]], Hq, Hkv, d)
+    got = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale)
+    check(got, q, chunks, sc, Hq, Hkv, d, theta, scale)
+
+
+def test_shift_moves_only_through_the_rotation():
+    """delta = 0 and no patch: plain attention over the canonical cache; the
+    same chunk with delta != 0 differs (the relocation is applied)."""
+    from oracle import attention, bf16_bits_to_f64, round_to_bf16_bits
+    Hq, Hkv, d = 4, 2, 128
+    q, chunks, sc = make_case(92, [[(100, 0)]], Hq, Hkv, d)
+    chunks[0]["delta"] = 0
+    got0 = run_gpu(q, chunks, sc, Hq, Hkv, d, 1e4, 0.088)
+    ref0 = attention(bf16_bits_to_f64(q[0].reshape(-1)), bf16_bits_to_f64(chunks[0]["k"]),
+                     bf16_bits_to_f64(chunks[0]["v"]), Hq, Hkv, d, 0.088)
+    from oracle.bf16 import ulp_distance
+    assert ulp_distance(got0[0].reshape(-1), round_to_bf16_bits(ref0)).max() <= 1
+    chunks[0]["delta"] = 5000
+    got1 = run_gpu(q, chunks, sc, Hq, Hkv, d, 1e4, 0.088)
+    assert np.any(got1 != got0)
