@@ -625,14 +625,15 @@ def bench_attend(args) -> dict:
     seq_chunks = [s * a["chunks"] for s in range(a["seqs"] + 1)]
     q = rnd(a["seqs"], a["Hq"], a["d"])
     out = torch.empty_like(q)
-    ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([a["tokens"]] * n_chunks, a["Hq"], a["d"]),
+    ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([a["tokens"]] * n_chunks, a["Hq"], a["Hkv"], a["d"]),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
         kvrp.kv_attend_relocated(q, arr, seq_chunks, n_q_heads=a["Hq"], n_kv_heads=a["Hkv"], head_dim=a["d"],
                                  rope_theta=a["theta"], softmax_scale=a["d"] ** -0.5, out=out, workspace=ws,
-                                 stream=stream)
+                                 d_status=status, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -645,6 +646,8 @@ def bench_attend(args) -> dict:
             step()
         t1.record(stream)
         torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"kv_attend_relocated reported device status {int(status.item()):#x}")
     ms = t0.elapsed_time(t1) / args.steps
     nb = attn_bytes(a)
     peaks = measured_peaks()

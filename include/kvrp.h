@@ -320,11 +320,17 @@ kvrp_status kv_patch_form_orbit(
  *   out         device bf16 [n_seqs][n_q_heads][head_dim]; a sequence with no
  *               tokens gets zeros.
  *   workspace   device scratch of kv_attend_relocated_workspace_size(...) bytes
- *               (fp32 partial results and per-chunk rotation tables).
+ *               (the rotated queries and fp32 partial results); the size depends
+ *               on the current device's SM count, and the call returns WORKSPACE
+ *               if it is smaller than the size for the device it runs on.
+ *   d_status    optional device word; KVRP_DEV_TIMEOUT is OR-ed in if an internal
+ *               pipeline wait gave up (the output is then undefined).
  * Pointers 16-byte aligned.  Arithmetic fp32 on the bf16 inputs (rotation
- * angles in fp64), output rounded once to bf16.  Errors (INVALID_ARG,
- * ALIGNMENT, UNSUPPORTED, WORKSPACE) are returned before any CUDA work; CUDA
- * on a launch failure.  Asynchronous on `stream`.
+ * angles in fp64; q, V_k^T q and the softmax weights enter the tensor-core
+ * products as high + low bf16 parts), output rounded once to bf16.  Errors
+ * (INVALID_ARG, ALIGNMENT, UNSUPPORTED -- also beyond 2^31 - 1 tokens in one
+ * call -- and WORKSPACE) are returned before any CUDA work; CUDA on a launch
+ * failure.  Asynchronous on `stream`.
  */
 #define KVRP_ATTN_MAX_CHUNKS 256
 
@@ -341,13 +347,13 @@ typedef struct {
 } kvrp_attn_chunk;
 
 size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk_tokens, int32_t n_q_heads,
-                                          int32_t head_dim);
+                                          int32_t n_kv_heads, int32_t head_dim);
 
 kvrp_status kv_attend_relocated(
     const void* q, const kvrp_attn_chunk* chunks, int32_t n_chunks, const int32_t* seq_chunks,
     int32_t n_seqs, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
     double rope_theta, float softmax_scale, void* out,
-    void* workspace, size_t workspace_bytes, kvrp_stream_t stream);
+    void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char* kvrp_status_string(kvrp_status status);

@@ -99,11 +99,11 @@ def _load_library():
         C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double, C.c_int32, C.c_int32, C.c_int32, C.c_void_p,
         C.c_void_p, C.c_void_p, C.c_int64, C.c_int64, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
     L.kv_attend_relocated_workspace_size.restype = C.c_size_t
-    L.kv_attend_relocated_workspace_size.argtypes = [C.c_int32, C.POINTER(C.c_int32), C.c_int32, C.c_int32]
+    L.kv_attend_relocated_workspace_size.argtypes = [C.c_int32, C.POINTER(C.c_int32), C.c_int32, C.c_int32, C.c_int32]
     L.kv_attend_relocated.restype = st
     L.kv_attend_relocated.argtypes = [
         C.c_void_p, C.POINTER(kvrp_attn_chunk), C.c_int32, C.POINTER(C.c_int32), C.c_int32, C.c_int32, C.c_int32,
-        C.c_int32, C.c_double, C.c_float, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p]
+        C.c_int32, C.c_double, C.c_float, C.c_void_p, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
     L.kvrp_status_string.restype = C.c_char_p
     L.kvrp_status_string.argtypes = [C.c_int]
     L.kvrp_last_error.restype = C.c_char_p
@@ -341,10 +341,11 @@ class AttnChunk:
                                _ptr(self.uk), _ptr(self.vk), _ptr(self.uv), _ptr(self.vv))
 
 
-def kv_attend_relocated_workspace_size(chunk_tokens, n_q_heads: int, head_dim: int) -> int:
+def kv_attend_relocated_workspace_size(chunk_tokens, n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
+    """Scratch bytes of kv_attend_relocated (depends on the current device's SM count)."""
     n = len(chunk_tokens)
     arr = (C.c_int32 * max(n, 1))(*[int(t) for t in chunk_tokens])
-    return int(lib().kv_attend_relocated_workspace_size(n, arr, int(n_q_heads), int(head_dim)))
+    return int(lib().kv_attend_relocated_workspace_size(n, arr, int(n_q_heads), int(n_kv_heads), int(head_dim)))
 
 
 def attn_chunk_array(chunks):
@@ -357,7 +358,7 @@ def attn_chunk_array(chunks):
 
 def kv_attend_relocated(q, chunks, seq_chunks, *, n_q_heads: int, n_kv_heads: int, head_dim: int, rope_theta: float,
                         softmax_scale: float, out, workspace, workspace_bytes: Optional[int] = None,
-                        stream=None) -> None:
+                        d_status=None, stream=None) -> None:
     """Decode attention of one query token per sequence over relocated, patched chunks."""
     arr, n = chunks if isinstance(chunks, tuple) else attn_chunk_array(chunks)
     sc = (C.c_int32 * len(seq_chunks))(*[int(v) for v in seq_chunks])
@@ -365,4 +366,4 @@ def kv_attend_relocated(q, chunks, seq_chunks, *, n_q_heads: int, n_kv_heads: in
         workspace_bytes = int(workspace.numel() * workspace.element_size())
     _check(lib().kv_attend_relocated(
         _ptr(q), arr, n, sc, len(seq_chunks) - 1, int(n_q_heads), int(n_kv_heads), int(head_dim), float(rope_theta),
-        float(softmax_scale), _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream)))
+        float(softmax_scale), _ptr(out), _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))

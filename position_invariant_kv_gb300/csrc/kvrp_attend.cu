@@ -14,22 +14,26 @@
 //
 // Kernels:
 //   prep_kernel    one CTA per (chunk, KV head): the rotated, scaled queries
-//                  scale * R(-delta) q (angles in fp64) and w = scale V_k,h^T q
-//                  of the group's query heads, each split into a bf16 high and
-//                  low part (their sum carries ~16 significant bits);
-//   block_kernel   one CTA per (block of up to 256 tokens of one chunk, KV
-//                  head), four warps; 64-token sub-blocks stream through a
-//                  double-buffered cp.async pipeline (one barrier each) and
-//                  every warp owns 16 tokens of each: S^T = Q K^T + W U_k^T
-//                  (query heads as the 16 rows), an online softmax in
-//                  registers, and O += P [V | U_v] with P taken straight from
-//                  the score accumulators -- all products warp-level
-//                  tensor-core MMAs (mma.sync m16n8k16 bf16 -> fp32, fragments
-//                  by ldmatrix; q, w and P enter as high + low bf16 parts,
-//                  two products each).  The four warps' (O, max, sum) merge in
-//                  shared memory into one fp32 partial per block and head;
+//                  scale * R(-delta) q (angles in fp64, shared by the group's
+//                  query heads) and w = scale V_k,h^T q, each split into a bf16
+//                  high and low part (their sum carries ~16 significant bits);
+//   block_kernel   persistent, two CTAs per SM.  The work is a sequence of
+//                  stages -- (head group, chunk, 16 * 4 / hg tokens) -- and each
+//                  CTA takes an equal contiguous share of it (stream-K), so
+//                  every SM streams the same number of bytes.  A producer warp
+//                  fills a ring of shared-memory stages with bulk copies (the
+//                  TMA engine; one copy per token row of the head group's K and
+//                  V, one per factor block of U_k and U_v, which the group's
+//                  heads share); four consumer warps, one (KV head, 16-token
+//                  slice) each, compute S = K Q^T + U_k W^T with the tokens as
+//                  the MMA's rows, an online softmax in registers, and
+//                  O^T += [V | U_v]^T P^T with P^T transposed in registers
+//                  (movmatrix) -- warp-level tensor-core MMAs (mma.sync
+//                  m16n8k16 bf16 -> fp32; q, w and P enter as high + low bf16
+//                  parts, two products each).  At a chunk or share boundary a
+//                  warp writes its (O, max, sum) as one fp32 partial;
 //   combine_kernel one CTA per (sequence, query head): merges the partials of
-//                  the sequence's blocks by their maxima, applies each chunk's
+//                  the sequence's chunks by their maxima, applies each chunk's
 //                  value patch V_v,h (P U_v) once, rounds to bf16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -42,33 +46,50 @@
 
 #include "kvrp.h"
 #include "kvrp_plan.h"
+#include "kvrp_ptx.h"
 
 namespace kvrp {
 namespace at {
 
+using namespace kvrp::ptx;
+
 constexpr int kMaxChunks = KVRP_ATTN_MAX_CHUNKS;
-constexpr int kBlock = 64;          // tokens per sub-block
-constexpr int kSubs = 4;            // sub-blocks per block_kernel CTA
-constexpr int kCta = kBlock * kSubs;
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
-constexpr int kMaxGroup = 16;       // query heads per KV head (one m16 tile)
+constexpr int kConsumers = 4;                       // consumer warps; warp kConsumers is the producer
+constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int kSlice = 16;                          // tokens per consumer warp and stage (the MMA's rows)
+constexpr int kMaxGroup = 16;                       // query heads per KV head (two n-tiles of 8)
 constexpr int kMaxRank = 128;
+constexpr int kMaxStages = 8;
+constexpr int kCtasPerSm = 2;
+constexpr int kMaxCtas = 1024;                      // bound on the block kernel's grid (workspace sizing)
+constexpr int kSmemPerSm = 228 * 1024;              // shared memory of one SM, 1 KB of it reserved per CTA
 
 struct ChunkRec {
   const uint16_t *k, *v, *uk, *vk, *uv, *vv;
-  int32_t n_tokens, rank, seq, blk0;   // blk0: first block of this chunk
+  int32_t n_tokens, rank, seq, st0;   // st0: this chunk's first stage within a head group
 };
 
 struct Params {
   const uint16_t* q;
   uint16_t* out;
-  float* partial;      // [n_blocks][Hq][d + m_max + 2]: P V, P U_v, max, sum
+  float* partial;      // [slot][slice][hg * g][d + 2]: O (value patch included), max, sum
   uint16_t* qhl;       // [n_chunks][2][Hq][d]: high, low bf16 parts of scale * R(-delta) q
   uint16_t* whl;       // [n_chunks][2][Hq][m_max]: high, low parts of scale * V_k,h^T q
-  int n_chunks, n_seqs, n_blocks, Hq, Hkv, d, g, m_max;
+  uint32_t* status;
+  int n_chunks, n_seqs, Hq, Hkv, d, g, m_max;
+  int hg;              // KV heads per head group: a power of two dividing Hkv, at most kConsumers
+  int n_hg;            // head groups (Hkv / hg)
+  int ns;              // token slices per stage (kConsumers / hg)
+  int ts;              // tokens per stage (kSlice * ns)
+  int stages;          // ring depth
+  int k_pitch;         // elements per staged K (and V) row: hg * d + 8
+  int kv_bytes;        // bytes of a stage's K (and of its V)
+  int u_bytes;         // bytes of a stage's U_k (and of its U_v): ts * m_max * 2
+  int stage_bytes;
+  int n_cta;
+  int64_t s_hg;        // stages per head group
   float scale;
-  double theta;
+  double inv_freq[64];   // theta^(-2i/d), i < d/2
   ChunkRec c[kMaxChunks];
   int64_t delta[kMaxChunks];
   int32_t seq_chunk[kMaxChunks + 1];
@@ -79,13 +100,16 @@ __device__ __forceinline__ uint16_t to_bf(float v) {
   const __nv_bfloat16 b = __float2bfloat16_rn(v);
   return *reinterpret_cast<const uint16_t*>(&b);
 }
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+__device__ __forceinline__ uint32_t pack_bf(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
+__device__ __forceinline__ uint32_t ldg32(const uint16_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
 
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint16_t vks[];   // V_k,h [d][m]
   __shared__ float2 rot[64];                         // (cos, sin) of -delta * theta^(-2i/d)
+  __shared__ float qs[kMaxGroup * 128];              // the group's queries, fp32
+  // the block kernel may launch now: its producer streams K, V and U (inputs) while
+  // this kernel prepares the queries, which its consumers wait for
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int ci = blockIdx.x, h = blockIdx.y;
   const ChunkRec& c = p.c[ci];
   const int d = p.d, half = d / 2, g = p.g, m = c.rank, Hq = p.Hq;
@@ -95,16 +119,17 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Param
   if (m > 0)
     for (int e = threadIdx.x; e < d * m / 8; e += blockDim.x)
       reinterpret_cast<uint4*>(vks)[e] = reinterpret_cast<const uint4*>(c.vk + (int64_t)h * d * m)[e];
+  for (int e = threadIdx.x; e < g * d; e += blockDim.x) qs[e] = bf(q[e]);
   if (threadIdx.x < half) {
-    const int i = threadIdx.x;
-    const double phi = -static_cast<double>(p.delta[ci]) * pow(p.theta, -2.0 * i / d);
-    rot[i] = make_float2((float)cos(phi), (float)sin(phi));
+    double sn, cs;
+    sincos(-static_cast<double>(p.delta[ci]) * p.inv_freq[threadIdx.x], &sn, &cs);
+    rot[threadIdx.x] = make_float2((float)cs, (float)sn);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < g * half; e += blockDim.x) {
     const int j = e / half, i = e - j * half;
     const float cs = rot[i].x, sn = rot[i].y;
-    const float a = bf(q[j * d + i]), b = bf(q[j * d + i + half]);
+    const float a = qs[j * d + i], b = qs[j * d + i + half];
     const float r0 = (a * cs - b * sn) * p.scale, r1 = (b * cs + a * sn) * p.scale;
     const uint16_t h0 = to_bf(r0), h1 = to_bf(r1);
     qh[j * d + i] = h0;
@@ -120,7 +145,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Param
     float a4[4] = {0.f, 0.f, 0.f, 0.f};
     for (int i = 0; i < d; i += 4) {
 #pragma unroll
-      for (int u = 0; u < 4; ++u) a4[u] = fmaf(bf(vks[(i + u) * m + r]), bf(q[j * d + i + u]), a4[u]);
+      for (int u = 0; u < 4; ++u) a4[u] = fmaf(bf(vks[(i + u) * m + r]), qs[j * d + i + u], a4[u]);
     }
     const float w = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * p.scale;
     const uint16_t hw = to_bf(w);
@@ -129,376 +154,510 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Param
   }
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(smem_u32(smem)), "l"(gmem),
-               "r"(valid ? 16 : 0)
-               : "memory");
+// --- the stage sequence ------------------------------------------------------
+// Stage f of the whole job is stage (f mod s_hg) of head group f / s_hg; inside a
+// head group the chunks follow each other, chunk c owning stages
+// [st0, st0 + ceil(n_tokens / ts)).  CTA i takes stages [begin(i), begin(i + 1)).
+__host__ __device__ __forceinline__ int64_t share_begin(int64_t total, int n_cta, int i) {
+  return (int64_t)i * total / n_cta;
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-
-// Warp-level tensor-core product D += A B, m16n8k16, bf16 inputs, fp32 accumulate.
-__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+// The CTA whose share holds stage f: the largest i with begin(i) <= f.
+__host__ __device__ __forceinline__ int share_of(int64_t total, int n_cta, int64_t f) {
+  return (int)(((f + 1) * n_cta - 1) / total);
 }
-// A fragment (16 x 16, row-major source): lane l addresses row (l & 15), column 8 (l >> 4)
-__device__ __forceinline__ void ldsm_a(uint32_t (&r)[4], const uint16_t* base, int pitch) {
-  const int l = threadIdx.x & 31;
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(base + (l & 15) * pitch + (l >> 4) * 8)));
-}
-// B fragment (16 x 8) from an [n][k] row-major source: lane l < 16 addresses row (l & 7), column 8 (l >> 3)
-__device__ __forceinline__ void ldsm_b(uint32_t (&r)[2], const uint16_t* base, int pitch) {
-  const int l = threadIdx.x & 15;
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(smem_u32(base + (l & 7) * pitch + (l >> 3) * 8)));
-}
-// B fragment (16 x 8) from a [k][n] row-major source (transposed load): lane l < 16 addresses row l
-__device__ __forceinline__ void ldsm_bt(uint32_t (&r)[2], const uint16_t* base, int pitch) {
-  const int l = threadIdx.x & 15;
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r[0]), "=r"(r[1])
-               : "r"(smem_u32(base + l * pitch)));
-}
-
-// Two B fragments (16 x 8 each, n-tiles n0 and n0 + 8) from an [n][k] row-major source
-__device__ __forceinline__ void ldsm_b2(uint32_t (&r)[4], const uint16_t* base, int pitch) {
-  const int l = threadIdx.x & 31;
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(base + ((l & 7) + ((l >> 4) << 3)) * pitch + ((l >> 3) & 1) * 8)));
-}
-// Two B fragments (n-tiles n0 and n0 + 8) from a [k][n] row-major source (transposed load)
-__device__ __forceinline__ void ldsm_bt2(uint32_t (&r)[4], const uint16_t* base, int pitch) {
-  const int l = threadIdx.x & 31;
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(base + (l & 15) * pitch + (l >> 4) * 8)));
-}
-__device__ __forceinline__ uint32_t pack_bf(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
-
-// Shared memory of block_kernel (bf16 rows padded by 16 bytes for conflict-free ldmatrix).
-struct BlockSmem {
-  int kv_pitch, u_pitch, m_pitch;
-  int k_off, v_off, uk_off, uv_off, buf_bytes;   // buffer b of a stage at (offset + b * buf_bytes)
-  int qh_off, ql_off, wh_off, wl_off;
-  int bytes;
+// Position in the stage sequence: head group, chunk, stage within the chunk,
+// and the chunk's stage count.  Decoded once per CTA, then advanced.
+struct Cursor {
+  int hg, c, k, nst;
 };
-// Staging (two buffers of K, V, U_k, U_v), then the queries and w; the warps'
-// final (O, max, sum) reuse the staging area (fp32 rows of m_pitch floats).
-__host__ __device__ inline BlockSmem block_smem(int d, int m) {
-  BlockSmem s;
-  s.kv_pitch = d + 8;
-  s.u_pitch = (m > 0 ? m : 16) + 8;
-  s.m_pitch = d + m + 8;
-  int off = 0;
-  s.k_off = off; off += kBlock * s.kv_pitch * 2;
-  s.v_off = off; off += kBlock * s.kv_pitch * 2;
-  s.uk_off = off; off += m > 0 ? kBlock * s.u_pitch * 2 : 0;
-  s.uv_off = off; off += m > 0 ? kBlock * s.u_pitch * 2 : 0;
-  s.buf_bytes = off;
-  off *= 2;
-  const int merge = kWarps * kMaxGroup * (s.m_pitch + 2) * 4;
-  off = off > merge ? off : merge;
-  s.qh_off = off; off += kMaxGroup * s.kv_pitch * 2;
-  s.ql_off = off; off += kMaxGroup * s.kv_pitch * 2;
-  s.wh_off = off; off += m > 0 ? kMaxGroup * s.u_pitch * 2 : 0;
-  s.wl_off = off; off += m > 0 ? kMaxGroup * s.u_pitch * 2 : 0;
-  s.bytes = off;
-  return s;
-}
-
-__device__ __forceinline__ int chunk_of_block(const Params& p, int blk) {
-  int lo = 0, hi = p.n_chunks - 1;   // last chunk whose blk0 <= blk
+__device__ __forceinline__ int chunk_stages(const Params& p, int ci) { return (p.c[ci].n_tokens + p.ts - 1) / p.ts; }
+__device__ __forceinline__ Cursor cursor_at(const Params& p, int64_t f) {
+  Cursor r;
+  r.hg = (int)(f / p.s_hg);
+  const int64_t rem = f - (int64_t)r.hg * p.s_hg;
+  int lo = 0, hi = p.n_chunks - 1;   // last chunk with st0 <= rem: one with tokens
   while (lo < hi) {
-    const int mid = (lo + hi + 1) / 2;
-    if (p.c[mid].blk0 <= blk) lo = mid;
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.c[mid].st0 <= rem) lo = mid;
     else hi = mid - 1;
   }
-  return lo;
+  r.c = lo;
+  r.k = (int)(rem - p.c[lo].st0);
+  r.nst = (p.c[lo].n_tokens + p.ts - 1) / p.ts;
+  return r;
+}
+// The next stage; only called while one exists.
+__device__ __forceinline__ void advance(const Params& p, Cursor& r) {
+  if (++r.k < r.nst) return;
+  r.k = 0;
+  do {
+    if (++r.c == p.n_chunks) {
+      r.c = 0;
+      ++r.hg;
+    }
+  } while (p.c[r.c].n_tokens <= 0);
+  r.nst = (p.c[r.c].n_tokens + p.ts - 1) / p.ts;
+}
+// Partial slot of (CTA i, head group hg, chunk c); distinct for every pair that shares a stage.
+__host__ __device__ __forceinline__ int64_t slot_of(int i, int hg, int c, int n_chunks) {
+  return (int64_t)i + (int64_t)hg * n_chunks + c;
 }
 
-template <int D, int UT>   // head dim; rank n-tiles the accumulators hold (rank <= 8 UT)
+// Bounded wait that ignores the abort flag: used to let this CTA's own copies land before it exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kTimeoutCycles) {
+      if (status) atomicOr(status, KVRP_DEV_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int D, int NT, int MCAP>   // head dim; n-tiles of 8 query heads; rank the accumulators hold
 __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__ Params p) {
-  constexpr int DT = D / 8, CPR = D / 8;
-  extern __shared__ __align__(16) uint8_t sm[];
-  const int blk = blockIdx.x, h = blockIdx.y;
-  const int ci = chunk_of_block(p, blk);
-  const ChunkRec& c = p.c[ci];
-  const int t0 = (blk - c.blk0) * kCta;
-  const int n_sub = (min(kCta, c.n_tokens - t0) + kBlock - 1) / kBlock;
-  const int g = p.g, m = c.rank, row = p.Hkv * D, upr = m / 8, ntu = m / 8;
-  const BlockSmem L = block_smem(D, p.m_max);
-  uint16_t* qhs = reinterpret_cast<uint16_t*>(sm + L.qh_off);
-  uint16_t* qls = reinterpret_cast<uint16_t*>(sm + L.ql_off);
-  uint16_t* whs = reinterpret_cast<uint16_t*>(sm + L.wh_off);
-  uint16_t* wls = reinterpret_cast<uint16_t*>(sm + L.wl_off);
+  constexpr int KT = D / 16;             // k-steps over the head dim (and m-tiles of the features)
+  constexpr int RT = MCAP / 16;          // k-steps over the rank (and m-tiles of the rank columns)
+  extern __shared__ __align__(128) uint8_t sm[];
+  __shared__ __align__(8) uint64_t bars[2 * kMaxStages];
+  __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gid = lane >> 2, tig = lane & 3;
+  const int cta = blockIdx.x;
+  const int64_t total = (int64_t)p.n_hg * p.s_hg;
+  const int64_t f0 = share_begin(total, p.n_cta, cta), f1 = share_begin(total, p.n_cta, cta + 1);
+  const uint32_t ring = smem_u32(sm);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
 
-  // one sub-block (64 tokens from token ts) into buffer b; rows past the chunk end are zero
-  auto stage = [&](int b, int ts) {
-    const int n = min(kBlock, c.n_tokens - ts);
-    uint16_t* ks = reinterpret_cast<uint16_t*>(sm + L.k_off + b * L.buf_bytes);
-    uint16_t* vs = reinterpret_cast<uint16_t*>(sm + L.v_off + b * L.buf_bytes);
-#pragma unroll
-    for (int e = tid; e < kBlock * CPR; e += kThreads) {
-      const int r = e / CPR, q16 = e % CPR;
-      const bool ok = r < n;
-      const int64_t off = (int64_t)(ts + r) * row + h * D + 8 * q16;
-      cp_async16(ks + r * L.kv_pitch + 8 * q16, ok ? c.k + off : c.k, ok);
-      cp_async16(vs + r * L.kv_pitch + 8 * q16, ok ? c.v + off : c.v, ok);
+  // zero the ring: rows past a chunk's end then always hold finite values
+  for (int e = tid; e < p.stages * p.stage_bytes / 16; e += kThreads)
+    reinterpret_cast<uint4*>(sm)[e] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), kConsumers);
     }
-    if (m > 0) {
-      uint16_t* uks = reinterpret_cast<uint16_t*>(sm + L.uk_off + b * L.buf_bytes);
-      uint16_t* uvs = reinterpret_cast<uint16_t*>(sm + L.uv_off + b * L.buf_bytes);
-      for (int e = tid; e < kBlock * upr; e += kThreads) {
-        const int r = e / upr, q16 = e - r * upr;
-        const bool ok = r < n;
-        const int64_t off = (int64_t)(ts + r) * m + 8 * q16;
-        cp_async16(uks + r * L.u_pitch + 8 * q16, ok ? c.uk + off : c.uk, ok);
-        cp_async16(uvs + r * L.u_pitch + 8 * q16, ok ? c.uv + off : c.uv, ok);
-      }
-    }
-    cp_async_commit();
-  };
-
-  // the queries and w of this head group (rows g..15 zero), then the first sub-block
-  const uint16_t* qsrc = p.qhl + ((int64_t)ci * 2 * p.Hq + (int64_t)h * g) * D;
-  for (int e = tid; e < 2 * kMaxGroup * CPR; e += kThreads) {
-    const int part = e / (kMaxGroup * CPR), rr = e % (kMaxGroup * CPR);
-    const int j = rr / CPR, q16 = rr % CPR;
-    const bool ok = j < g;
-    cp_async16((part ? qls : qhs) + j * L.kv_pitch + 8 * q16,
-               ok ? qsrc + (int64_t)part * p.Hq * D + (int64_t)j * D + 8 * q16 : qsrc, ok);
-  }
-  if (m > 0) {
-    const uint16_t* wsrc = p.whl + ((int64_t)ci * 2 * p.Hq + (int64_t)h * g) * p.m_max;
-    for (int e = tid; e < 2 * kMaxGroup * upr; e += kThreads) {
-      const int part = e / (kMaxGroup * upr), rr = e - part * kMaxGroup * upr;
-      const int j = rr / upr, q16 = rr - j * upr;
-      const bool ok = j < g;
-      cp_async16((part ? wls : whs) + j * L.u_pitch + 8 * q16,
-                 ok ? wsrc + (int64_t)part * p.Hq * p.m_max + (int64_t)j * p.m_max + 8 * q16 : wsrc, ok);
-    }
-  }
-  stage(0, t0);
-
-  // this warp's running state: rows gid and gid + 8 (query heads) of O = [P V | P U_v]
-  float o[DT + UT][4] = {};
-  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
-  const int tok0 = warp * 16;   // this warp's 16 tokens of each sub-block
-
-  for (int sb = 0; sb < n_sub; ++sb) {
-    const int b = sb & 1;
-    const int ts = t0 + sb * kBlock;
-    const int n = min(kBlock, c.n_tokens - ts);
-    cp_async_wait<0>();
-    __syncthreads();   // sub-block sb is visible; every warp is done with buffer b ^ 1
-    if (sb + 1 < n_sub) stage(b ^ 1, ts + kBlock);
-    if (tok0 >= n) continue;   // warp-uniform: this slice lies past the chunk end
-    const uint16_t* ks = reinterpret_cast<const uint16_t*>(sm + L.k_off + b * L.buf_bytes) + tok0 * L.kv_pitch;
-    const uint16_t* vs = reinterpret_cast<const uint16_t*>(sm + L.v_off + b * L.buf_bytes) + tok0 * L.kv_pitch;
-    const uint16_t* uks = reinterpret_cast<const uint16_t*>(sm + L.uk_off + b * L.buf_bytes) + tok0 * L.u_pitch;
-    const uint16_t* uvs = reinterpret_cast<const uint16_t*>(sm + L.uv_off + b * L.buf_bytes) + tok0 * L.u_pitch;
-
-    // S^T (16 heads x 16 tokens, two n-tiles) = Q K^T + W U_k^T
-    float s[2][4] = {};
-#pragma unroll
-    for (int k0 = 0; k0 < D; k0 += 16) {
-      uint32_t ah[4], al[4], bk[4];
-      ldsm_a(ah, qhs + k0, L.kv_pitch);
-      ldsm_a(al, qls + k0, L.kv_pitch);
-      ldsm_b2(bk, ks + k0, L.kv_pitch);
-      const uint32_t b0[2] = {bk[0], bk[1]}, b1[2] = {bk[2], bk[3]};
-      mma16816(s[0], ah, b0);
-      mma16816(s[1], ah, b1);
-      mma16816(s[0], al, b0);
-      mma16816(s[1], al, b1);
-    }
-    for (int k0 = 0; k0 < m; k0 += 16) {
-      uint32_t ah[4], al[4], bk[4];
-      ldsm_a(ah, whs + k0, L.u_pitch);
-      ldsm_a(al, wls + k0, L.u_pitch);
-      ldsm_b2(bk, uks + k0, L.u_pitch);
-      const uint32_t b0[2] = {bk[0], bk[1]}, b1[2] = {bk[2], bk[3]};
-      mma16816(s[0], ah, b0);
-      mma16816(s[1], ah, b1);
-      mma16816(s[0], al, b0);
-      mma16816(s[1], al, b1);
-    }
-
-    // online softmax over this warp's tokens: row r of the fragment is head gid + 8 r
-    float alpha[2];
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = tok0 + nt * 8 + 2 * tig + e;
-          if (t >= n) s[nt][2 * r + e] = -INFINITY;
-          mx = fmaxf(mx, s[nt][2 * r + e]);
-        }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-      const float m_new = fmaxf(mrow[r], mx);   // finite: token tok0 < n is in every quad's row
-      alpha[r] = expf(mrow[r] - m_new);         // 0 while nothing was accumulated
-      mrow[r] = m_new;
-      float sum = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float pe = expf(s[nt][2 * r + e] - m_new);
-          s[nt][2 * r + e] = pe;
-          sum += pe;
-        }
-      lrow[r] = lrow[r] * alpha[r] + sum;
-    }
-    // P (16 heads x 16 tokens) as the A operand, high and low bf16 parts
-    uint32_t ph[4], pl[4];
-#pragma unroll
-    for (int x = 0; x < 4; ++x) {
-      const float p0 = s[x >> 1][2 * (x & 1)], p1 = s[x >> 1][2 * (x & 1) + 1];
-      const uint16_t h0 = to_bf(p0), h1 = to_bf(p1);
-      ph[x] = pack_bf(h0, h1);
-      pl[x] = pack_bf(to_bf(p0 - bf(h0)), to_bf(p1 - bf(h1)));
-    }
-
-    // O = O * alpha + P [V | U_v], two n-tiles per transposed load
-#pragma unroll
-    for (int x = 0; x < DT + UT; x += 2) {
-      if (x >= DT && x - DT >= ntu) break;
-      uint32_t bv[4];
-      if (x < DT) ldsm_bt2(bv, vs + x * 8, L.kv_pitch);
-      else ldsm_bt2(bv, uvs + (x - DT) * 8, L.u_pitch);
-      const uint32_t b0[2] = {bv[0], bv[1]}, b1[2] = {bv[2], bv[3]};
-#pragma unroll
-      for (int y = 0; y < 2; ++y) {
-        o[x + y][0] *= alpha[0]; o[x + y][1] *= alpha[0];
-        o[x + y][2] *= alpha[1]; o[x + y][3] *= alpha[1];
-      }
-      mma16816(o[x], ph, b0);
-      mma16816(o[x + 1], ph, b1);
-      mma16816(o[x], pl, b0);
-      mma16816(o[x + 1], pl, b1);
-    }
-  }
-
-  // merge the four warps: each writes (O, max, sum) of its rows; then one pass over (head, column)
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 1);
-    lrow[r] += __shfl_xor_sync(0xffffffffu, lrow[r], 2);
-  }
-  __syncthreads();   // every warp is done with the staging buffers (no copy is in flight)
-  float* mo = reinterpret_cast<float*>(sm);                       // [warp][16][m_pitch]
-  float* ml = mo + kWarps * kMaxGroup * L.m_pitch;                // [warp][16][2]: max, sum
-  {
-    float* mw = mo + warp * kMaxGroup * L.m_pitch;
-#pragma unroll
-    for (int x = 0; x < DT + UT; ++x) {
-      if (x >= DT && x - DT >= ntu) break;
-      const int col = (x < DT ? x * 8 : D + (x - DT) * 8) + 2 * tig;
-      *reinterpret_cast<float2*>(mw + gid * L.m_pitch + col) = make_float2(o[x][0], o[x][1]);
-      *reinterpret_cast<float2*>(mw + (gid + 8) * L.m_pitch + col) = make_float2(o[x][2], o[x][3]);
-    }
-    if (tig == 0) {
-      ml[(warp * kMaxGroup + gid) * 2] = mrow[0];
-      ml[(warp * kMaxGroup + gid) * 2 + 1] = lrow[0];
-      ml[(warp * kMaxGroup + gid + 8) * 2] = mrow[1];
-      ml[(warp * kMaxGroup + gid + 8) * 2 + 1] = lrow[1];
-    }
+    abort_flag = 0;
+    mbar_init_fence();
   }
   __syncthreads();
-  const int pw = D + p.m_max + 2, cols = D + m;
-  float* part = p.partial + ((int64_t)blk * p.Hq + (int64_t)h * g) * pw;
-  for (int e = tid; e < g * (cols + 2); e += kThreads) {
-    const int j = e / (cols + 2), col = e - j * (cols + 2);
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, ml[(w * kMaxGroup + j) * 2]);
-    float acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float mw = ml[(w * kMaxGroup + j) * 2];
-      const float sc = mw == -INFINITY ? 0.f : expf(mw - M);
-      const float v = col < cols ? mo[(w * kMaxGroup + j) * L.m_pitch + col]
-                                 : (col == cols ? 0.f : ml[(w * kMaxGroup + j) * 2 + 1]);
-      acc = fmaf(sc, v, acc);
+  volatile int* abort_p = &abort_flag;
+  if (f0 >= f1) return;
+  Cursor r = cursor_at(p, f0);
+
+  if (warp == kConsumers) {
+    // ---------------- producer ----------------
+    const int64_t row = (int64_t)p.Hkv * D;
+    const uint32_t row_bytes = (uint32_t)p.hg * D * 2;
+    int s = 0, n_issued = 0;
+    uint32_t par = 0;
+    for (int64_t f = f0; f < f1; ++f) {
+      if (!wait_phase(empty(s), par ^ 1u, abort_p, p.status)) break;
+      const ChunkRec& c = p.c[r.c];
+      const int t0 = r.k * p.ts;
+      const int n = min(p.ts, c.n_tokens - t0);
+      const uint32_t ub = (uint32_t)n * c.rank * 2;
+      if (lane == 0) mbar_expect_tx(full(s), (uint32_t)n * 2 * row_bytes + 2 * ub);
+      __syncwarp();
+      const uint32_t st = ring + (uint32_t)s * p.stage_bytes;
+      const uint16_t* kp = c.k + (int64_t)t0 * row + (int64_t)r.hg * p.hg * D;
+      const uint16_t* vp = c.v + (kp - c.k);
+      for (int t = lane; t < n; t += 32) {
+        bulk_load(st + (uint32_t)t * p.k_pitch * 2, kp + t * row, row_bytes, full(s));
+        bulk_load(st + p.kv_bytes + (uint32_t)t * p.k_pitch * 2, vp + t * row, row_bytes, full(s));
+      }
+      if (lane == 0 && ub > 0) {
+        bulk_load(st + 2 * p.kv_bytes, c.uk + (int64_t)t0 * c.rank, ub, full(s));
+        bulk_load(st + 2 * p.kv_bytes + p.u_bytes, c.uv + (int64_t)t0 * c.rank, ub, full(s));
+      }
+      ++n_issued;
+      if (++s == p.stages) {
+        s = 0;
+        par ^= 1u;
+      }
+      if (f + 1 < f1) advance(p, r);
     }
-    if (col < cols) part[(int64_t)j * pw + col] = acc;
-    else if (col == cols) part[(int64_t)j * pw + D + p.m_max] = M;
-    else part[(int64_t)j * pw + D + p.m_max + 1] = acc;
+    // no copy of this CTA may still be landing when it exits: wait for the last phase issued on each stage
+    if (lane == 0)
+      for (int j = 0; j < p.stages && j < n_issued; ++j) {
+        if (--s < 0) {
+          s = p.stages - 1;
+          par ^= 1u;
+        }
+        drain_wait(full(s), par, p.status);
+      }
+    return;
+  }
+
+  // ---------------- consumers: warp -> (KV head hw of the group, token slice sw) ----------------
+  const int hw = warp % p.hg, sw = warp / p.hg;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int g = p.g, pw = D + 2;
+  // ldmatrix lane offsets (elements): A from [token][feature] rows; A^T (transposed load) likewise
+  const int a_row = lane & 15, a_col = (lane >> 4) * 8;
+  const int t_row = (lane & 7) + ((lane >> 4) << 3), t_col = ((lane >> 3) & 1) * 8;
+
+  float o[KT + RT][NT][4];                 // O^T: feature m-tiles, then rank m-tiles (P U_v)
+  float mcol[NT][2], lcol[NT][2];
+  uint32_t qb[KT][NT][2][2];               // B fragments of Q^T: [k-step][n-tile][high, low][b0, b1]
+  uint32_t wb[RT][NT][2][2];               // B fragments of W^T
+#pragma unroll
+  for (int mt = 0; mt < KT + RT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    mcol[nt][0] = mcol[nt][1] = -INFINITY;
+    lcol[nt][0] = lcol[nt][1] = 0.f;
+  }
+
+  // the rotated queries come from prep_kernel, which may still be running (dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int s = 0;
+  uint32_t par = 0;
+  bool seg_start = true;
+  for (int64_t f = f0; f < f1; ++f) {
+    const ChunkRec& c = p.c[r.c];
+    const int m = c.rank;
+    const int kvh = r.hg * p.hg + hw;   // this warp's KV head
+    const int head0 = kvh * g;          // its first query head
+    if (seg_start) {
+      // a new segment: this chunk's rotated query and w as B fragments (heads >= g zero)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int j = nt * 8 + gid;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const uint16_t* qs = p.qhl + (((int64_t)r.c * 2 + part) * p.Hq + head0 + j) * D + 2 * tig;
+          const uint16_t* ws = p.whl + (((int64_t)r.c * 2 + part) * p.Hq + head0 + j) * p.m_max + 2 * tig;
+#pragma unroll
+          for (int kk = 0; kk < KT; ++kk) {
+            qb[kk][nt][part][0] = j < g ? ldg32(qs + kk * 16) : 0u;
+            qb[kk][nt][part][1] = j < g ? ldg32(qs + kk * 16 + 8) : 0u;
+          }
+#pragma unroll
+          for (int kk = 0; kk < RT; ++kk) {
+            const bool ok = j < g && kk * 16 < m;
+            wb[kk][nt][part][0] = ok ? ldg32(ws + kk * 16) : 0u;
+            wb[kk][nt][part][1] = ok ? ldg32(ws + kk * 16 + 8) : 0u;
+          }
+        }
+      }
+      // the value patch rows V_v,h are used when the segment ends: start them towards L2
+      if (m > 0)
+        for (int e = lane; e < D * m / 64; e += 32)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(c.vv + (int64_t)kvh * D * m + e * 64));
+      seg_start = false;
+    }
+    if (!wait_phase(full(s), par, abort_p, p.status)) break;
+    const int nv = min(kSlice, c.n_tokens - (r.k * p.ts + sw * kSlice));   // valid tokens of this slice
+    if (nv > 0) {
+      const uint32_t st = ring + (uint32_t)s * p.stage_bytes;
+      const uint32_t kb = st + (uint32_t)((sw * kSlice) * p.k_pitch + hw * D) * 2;
+      const uint32_t vb = kb + p.kv_bytes;
+      const uint32_t ukb = st + 2 * p.kv_bytes + (uint32_t)(sw * kSlice * m) * 2;
+      const uint32_t uvb = ukb + p.u_bytes;
+
+      // S (16 tokens x 8 NT heads) = K Q^T + U_k W^T, high and low parts in separate chains
+      float sh[NT][4], sl[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < KT; ++kk) {
+        uint32_t a[4];
+        ldsm_x4(a, kb + (uint32_t)(a_row * p.k_pitch + a_col + kk * 16) * 2);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816(sh[nt], a, qb[kk][nt][0][0], qb[kk][nt][0][1]);
+          mma16816(sl[nt], a, qb[kk][nt][1][0], qb[kk][nt][1][1]);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < RT; ++kk) {
+        if (kk * 16 >= m) break;
+        uint32_t a[4];
+        ldsm_x4(a, ukb + (uint32_t)(a_row * m + a_col + kk * 16) * 2);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma16816(sh[nt], a, wb[kk][nt][0][0], wb[kk][nt][0][1]);
+          mma16816(sl[nt], a, wb[kk][nt][1][0], wb[kk][nt][1][1]);
+        }
+      }
+
+      // online softmax per head (column): rows are tokens gid (e = 0, 1) and gid + 8 (e = 2, 3)
+      float alpha[NT][2];
+      uint32_t pb[NT][2][2];   // B fragments of P^T: [n-tile][high, low][tokens 0-7, tokens 8-15]
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float sc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[e] = sh[nt][e] + sl[nt][e];
+        if (gid >= nv) sc[0] = sc[1] = -INFINITY;
+        if (gid + 8 >= nv) sc[2] = sc[3] = -INFINITY;
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          float mx = fmaxf(sc[e2], sc[e2 + 2]);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mn = fmaxf(mcol[nt][e2], mx);   // finite: token 0 of the slice is valid
+          alpha[nt][e2] = expf(mcol[nt][e2] - mn);     // 0 while nothing was accumulated
+          mcol[nt][e2] = mn;
+          sc[e2] = expf(sc[e2] - mn);
+          sc[e2 + 2] = expf(sc[e2 + 2] - mn);
+          lcol[nt][e2] = lcol[nt][e2] * alpha[nt][e2] + (sc[e2] + sc[e2 + 2]);
+        }
+        uint16_t hb[4], lb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hb[e] = to_bf(sc[e]);
+          lb[e] = to_bf(sc[e] - bf(hb[e]));
+        }
+        // (token, head) pairs in fragment layout, transposed to (head, token): the B operand
+        pb[nt][0][0] = movmatrix_trans(pack_bf(hb[0], hb[1]));
+        pb[nt][0][1] = movmatrix_trans(pack_bf(hb[2], hb[3]));
+        pb[nt][1][0] = movmatrix_trans(pack_bf(lb[0], lb[1]));
+        pb[nt][1][1] = movmatrix_trans(pack_bf(lb[2], lb[3]));
+      }
+
+      // O^T = O^T * alpha + [V | U_v]^T P^T: rows features (then rank columns), columns heads
+#pragma unroll
+      for (int mt = 0; mt < KT + RT; ++mt) {
+        if (mt >= KT && (mt - KT) * 16 >= m) break;
+        uint32_t a[4];
+        if (mt < KT) ldsm_x4_trans(a, vb + (uint32_t)(t_row * p.k_pitch + t_col + mt * 16) * 2);
+        else ldsm_x4_trans(a, uvb + (uint32_t)(t_row * m + t_col + (mt - KT) * 16) * 2);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          o[mt][nt][0] *= alpha[nt][0];
+          o[mt][nt][1] *= alpha[nt][1];
+          o[mt][nt][2] *= alpha[nt][0];
+          o[mt][nt][3] *= alpha[nt][1];
+          mma16816(o[mt][nt], a, pb[nt][0][0], pb[nt][0][1]);
+          mma16816(o[mt][nt], a, pb[nt][1][0], pb[nt][1][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));
+    if (++s == p.stages) {
+      s = 0;
+      par ^= 1u;
+    }
+
+    if (f + 1 == f1 || r.k + 1 == r.nst) {
+      // segment end.  The value patch: O^T += V_v,h (P U_v)^T, with the rank rows of O^T
+      // as the B operand (fp32 -> high + low bf16, transposed in registers) and
+      // V_v,h [d][m] rows as A, read from global memory.
+      if (m > 0) {
+        const uint16_t* vv = c.vv + (int64_t)kvh * D * m;
+#pragma unroll
+        for (int rt = 0; rt < RT; ++rt) {
+          if (rt * 16 >= m) break;
+          uint32_t ub[NT][2][2];
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const float* u = o[KT + rt][nt];
+            uint16_t hb[4], lb[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              hb[e] = to_bf(u[e]);
+              lb[e] = to_bf(u[e] - bf(hb[e]));
+            }
+            ub[nt][0][0] = movmatrix_trans(pack_bf(hb[0], hb[1]));
+            ub[nt][0][1] = movmatrix_trans(pack_bf(hb[2], hb[3]));
+            ub[nt][1][0] = movmatrix_trans(pack_bf(lb[0], lb[1]));
+            ub[nt][1][1] = movmatrix_trans(pack_bf(lb[2], lb[3]));
+          }
+#pragma unroll
+          for (int ft = 0; ft < KT; ++ft) {
+            const uint16_t* va = vv + (int64_t)(ft * 16 + gid) * m + rt * 16 + 2 * tig;
+            uint32_t a[4];
+            a[0] = ldg32(va);
+            a[1] = ldg32(va + 8 * m);
+            a[2] = ldg32(va + 8);
+            a[3] = ldg32(va + 8 * m + 8);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma16816(o[ft][nt], a, ub[nt][0][0], ub[nt][0][1]);
+              mma16816(o[ft][nt], a, ub[nt][1][0], ub[nt][1][1]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          float l = lcol[nt][e2];
+          l += __shfl_xor_sync(0xffffffffu, l, 4);
+          l += __shfl_xor_sync(0xffffffffu, l, 8);
+          l += __shfl_xor_sync(0xffffffffu, l, 16);
+          lcol[nt][e2] = l;
+        }
+      // this warp's partial (its KV head's g query heads) to slot (cta, hg, chunk), slice sw
+      float* base = p.partial + ((slot_of(cta, r.hg, r.c, p.n_chunks) * p.ns + sw) * (p.hg * g) + (int64_t)hw * g) * pw;
+#pragma unroll
+      for (int ft = 0; ft < KT; ++ft)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = nt * 8 + 2 * tig + (e & 1);
+            if (j < g) base[(int64_t)j * pw + ft * 16 + gid + (e >> 1) * 8] = o[ft][nt][e];
+          }
+      if (gid == 0)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int j = nt * 8 + 2 * tig + e2;
+            if (j < g) {
+              base[(int64_t)j * pw + D] = mcol[nt][e2];
+              base[(int64_t)j * pw + D + 1] = lcol[nt][e2];
+            }
+          }
+#pragma unroll
+      for (int mt = 0; mt < KT + RT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mcol[nt][0] = mcol[nt][1] = -INFINITY;
+        lcol[nt][0] = lcol[nt][1] = 0.f;
+      }
+      seg_start = true;
+    }
+    if (f + 1 < f1) advance(p, r);
   }
 }
 
-// One CTA per (sequence, query head); thread -> output feature.  Merges the
-// block partials by their maxima (the global maximum first, by a CTA-wide
-// reduction); each chunk's P U_v is multiplied by its V_v,h once, when the
-// chunk's last block has been merged.
-__global__ void combine_kernel(const __grid_constant__ Params p) {
-  __shared__ float pu[kMaxRank];
-  __shared__ float red[32];
-  const int s = blockIdx.x, jq = blockIdx.y;
-  const int d = p.d, pw = d + p.m_max + 2, h = jq / p.g;
-  const int c0 = p.seq_chunk[s], c1 = p.seq_chunk[s + 1];
-  const int b0 = c0 < p.n_chunks ? p.c[c0].blk0 : p.n_blocks;
-  const int b1 = c1 < p.n_chunks ? p.c[c1].blk0 : p.n_blocks;
-  const int tid = threadIdx.x, lane = tid & 31, nw = blockDim.x >> 5;
-  float M = -INFINITY;
-  for (int b = b0 + tid; b < b1; b += blockDim.x) M = fmaxf(M, p.partial[((int64_t)b * p.Hq + jq) * pw + d + p.m_max]);
+// One warp per (sequence, query head); lane -> features lane, lane + 32, ...
+// Merges the partials of the sequence's chunks by their maxima (a partial with
+// no tokens has max -inf and weight 0) and rounds to bf16.  The partials of all
+// the sequence's chunks form one list, taken in groups of 32: lane x locates
+// entry x of a group (arithmetic only), so the loads of a group are independent.
+constexpr int kCombineWarps = 4;
+template <int D>
+__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const __grid_constant__ Params p) {
+  constexpr int FL = D / 32;   // features per lane
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // the block kernel's partials
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t item = (int64_t)blockIdx.x * kCombineWarps + warp;
+  if (item >= (int64_t)p.n_seqs * p.Hq) return;
+  const int s = (int)(item / p.Hq), jq = (int)(item - (int64_t)s * p.Hq);
+  const int g = p.g, pw = D + 2;
+  const int h = jq / g, hg = h / p.hg, row = (h % p.hg) * g + jq % g;
+  const int64_t total = (int64_t)p.n_hg * p.s_hg;
+  // list entry L: its partial (null past the end); returns the list's length
+  auto locate = [&](int L, const float*& pe) {
+    int n = 0;
+    pe = nullptr;
+    for (int ci = p.seq_chunk[s]; ci < p.seq_chunk[s + 1]; ++ci) {
+      if (p.c[ci].n_tokens <= 0) continue;
+      const int64_t F0 = (int64_t)hg * p.s_hg + p.c[ci].st0;
+      const int i0 = share_of(total, p.n_cta, F0);
+      const int ne = (share_of(total, p.n_cta, F0 + (p.c[ci].n_tokens + p.ts - 1) / p.ts - 1) - i0 + 1) * p.ns;
+      if (L >= n && L < n + ne) {
+        const int e = L - n;
+        pe = p.partial + ((slot_of(i0 + e / p.ns, hg, ci, p.n_chunks) * p.ns + e % p.ns) * (p.hg * g) + row) * pw;
+      }
+      n += ne;
+    }
+    return n;
+  };
+  const float* pe;
+  const int n_list = locate(lane, pe);
+  // the first group's max and sum stay in registers; later groups reload theirs
+  float mx0 = pe ? pe[D] : -INFINITY, l0 = pe ? pe[D + 1] : 0.f;
+  float M = mx0;
+  for (int L0 = 32; L0 < n_list; L0 += 32) {
+    const float* q;
+    locate(L0 + lane, q);
+    if (q) M = fmaxf(M, q[D]);
+  }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  if (lane == 0) red[tid >> 5] = M;
-  __syncthreads();
-  M = red[0];
-  for (int w = 1; w < nw; ++w) M = fmaxf(M, red[w]);
-  const int col = tid;   // blockDim.x == d
-  float num = 0.f, den = 0.f;
-  for (int ci = c0; ci < c1; ++ci) {
-    const ChunkRec& c = p.c[ci];
-    const int cb0 = c.blk0, cb1 = c.blk0 + (c.n_tokens + kCta - 1) / kCta;
-    float pr = 0.f;   // thread r < rank: this chunk's sum of weighted P U_v, component r
-#pragma unroll 4
-    for (int b = cb0; b < cb1; ++b) {
-      const float* pb = p.partial + ((int64_t)b * p.Hq + jq) * pw;
-      const float sc = expf(pb[d + p.m_max] - M);
-      num = fmaf(sc, pb[col], num);
-      den = fmaf(sc, pb[d + p.m_max + 1], den);
-      if (tid < c.rank) pr = fmaf(sc, pb[d + tid], pr);
+  float acc[FL] = {};
+  float den = 0.f;
+  for (int L0 = 0; L0 < n_list; L0 += 32) {
+    float mx = mx0, lt = l0;
+    if (L0 > 0) {
+      locate(L0 + lane, pe);
+      mx = pe ? pe[D] : -INFINITY;
+      lt = pe ? pe[D + 1] : 0.f;
     }
-    if (c.rank > 0) {
-      __syncthreads();   // the previous chunk's reads of pu are done
-      if (tid < c.rank) pu[tid] = pr;
-      __syncthreads();
-      const uint16_t* vv = c.vv + ((int64_t)h * d + col) * c.rank;
-      float a = 0.f;
-      for (int r = 0; r < c.rank; r += 8) {
-        const uint4 w = *reinterpret_cast<const uint4*>(vv + r);
-        const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    const float wt = mx == -INFINITY ? 0.f : expf(mx - M);
+    float dl = wt * lt;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          a = fmaf(__uint_as_float(wv[u] << 16), pu[r + 2 * u], a);
-          a = fmaf(__uint_as_float(wv[u] & 0xffff0000u), pu[r + 2 * u + 1], a);
-        }
+    for (int off = 16; off > 0; off >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, off);
+    den += dl;
+    const int nx = min(32, n_list - L0);
+    const uint64_t pa = reinterpret_cast<uint64_t>(pe);
+    for (int x = 0; x < nx; x += 4) {   // four entries' loads in flight
+      float w[4], v[4][FL];
+#pragma unroll
+      for (int y = 0; y < 4; ++y) {
+        const int xy = min(x + y, nx - 1);
+        w[y] = x + y < nx ? __shfl_sync(0xffffffffu, wt, xy) : 0.f;
+        const float* py = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, pa, xy));
+#pragma unroll
+        for (int u = 0; u < FL; ++u) v[y][u] = py[lane + 32 * u];
       }
-      num += a;
+#pragma unroll
+      for (int y = 0; y < 4; ++y)
+#pragma unroll
+        for (int u = 0; u < FL; ++u) acc[u] = fmaf(w[y], v[y][u], acc[u]);
     }
   }
-  const __nv_bfloat16 o = __float2bfloat16_rn(den > 0.f ? num / den : 0.f);
-  p.out[((int64_t)s * p.Hq + jq) * d + col] = *reinterpret_cast<const uint16_t*>(&o);
+  uint16_t* out = p.out + ((int64_t)s * p.Hq + jq) * D;
+#pragma unroll
+  for (int u = 0; u < FL; ++u) out[lane + 32 * u] = to_bf(den > 0.f ? acc[u] / den : 0.f);
 }
 
-int64_t blocks_of(int32_t n_tokens) { return (n_tokens + kCta - 1) / kCta; }
+// ---- host-side planning -----------------------------------------------------
+struct Plan {
+  int hg, n_hg, ns, ts, k_pitch, kv_bytes, u_bytes, stage_bytes, stages;
+};
+Plan make_plan(int n_kv_heads, int head_dim, int m_max) {
+  Plan pl;
+  pl.hg = 1;
+  while (pl.hg * 2 <= kConsumers && n_kv_heads % (pl.hg * 2) == 0) pl.hg *= 2;
+  pl.n_hg = n_kv_heads / pl.hg;
+  pl.ns = kConsumers / pl.hg;
+  pl.ts = kSlice * pl.ns;
+  pl.k_pitch = pl.hg * head_dim + 8;   // +16 bytes: ldmatrix rows fall in distinct banks
+  pl.kv_bytes = pl.ts * pl.k_pitch * 2;
+  pl.u_bytes = pl.ts * m_max * 2;
+  pl.stage_bytes = (2 * pl.kv_bytes + 2 * pl.u_bytes + 127) / 128 * 128;
+  const int budget = kSmemPerSm / kCtasPerSm - 1024 - 256;   // per CTA: reserved and static shared memory
+  pl.stages = std::max(2, std::min(kMaxStages, budget / pl.stage_bytes));
+  return pl;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0) {
+    cudaGetLastError();
+    return kMaxCtas / kCtasPerSm;
+  }
+  return n;
+}
+
+size_t partial_bytes(int n_cta_max, int n_chunks, int Hq, int Hkv, int head_dim) {
+  const Plan pl = make_plan(Hkv, head_dim, 0);
+  const int64_t slots = n_cta_max + (int64_t)pl.n_hg * n_chunks;
+  return sizeof(float) * (size_t)slots * kConsumers * (Hq / Hkv) * (head_dim + 2);
+}
 
 }  // namespace at
 }  // namespace kvrp
@@ -508,20 +667,20 @@ using namespace kvrp;
 extern "C" {
 
 size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk_tokens, int32_t n_q_heads,
-                                          int32_t head_dim) {
-  if (n_chunks <= 0 || !chunk_tokens || n_q_heads <= 0 || head_dim <= 0) return 0;
-  int64_t blocks = 0;
-  for (int i = 0; i < n_chunks; ++i) blocks += at::blocks_of(chunk_tokens[i] > 0 ? chunk_tokens[i] : 0);
-  const size_t part = sizeof(float) * (size_t)blocks * n_q_heads * (head_dim + at::kMaxRank + 2);
-  const size_t qhl = 2 * 2 * (size_t)n_chunks * n_q_heads * head_dim;
-  const size_t whl = 2 * 2 * (size_t)n_chunks * n_q_heads * at::kMaxRank;
-  return part + qhl + whl + 1024;
+                                          int32_t n_kv_heads, int32_t head_dim) {
+  if (n_chunks <= 0 || !chunk_tokens || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads || head_dim <= 0)
+    return 0;
+  const int n_cta_max = std::min(at::kMaxCtas, at::kCtasPerSm * at::sm_count());
+  const size_t part = at::partial_bytes(n_cta_max, n_chunks, n_q_heads, n_kv_heads, head_dim);
+  const size_t qhl = (2 * 2 * (size_t)n_chunks * n_q_heads * head_dim + 255) / 256 * 256;
+  const size_t whl = (2 * 2 * (size_t)n_chunks * n_q_heads * at::kMaxRank + 255) / 256 * 256;
+  return part + qhl + whl + 256;
 }
 
 kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, int32_t n_chunks,
                                 const int32_t* seq_chunks, int32_t n_seqs, int32_t n_q_heads, int32_t n_kv_heads,
                                 int32_t head_dim, double rope_theta, float softmax_scale, void* out,
-                                void* workspace, size_t workspace_bytes, kvrp_stream_t stream) {
+                                void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream) {
   if (!q || !chunks || !seq_chunks || !out) return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: NULL argument");
   if (n_chunks <= 0 || n_chunks > at::kMaxChunks)
     return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: 1 <= n_chunks <= %d", at::kMaxChunks);
@@ -536,11 +695,12 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   if (!aligned16(q) || !aligned16(out)) return fail(KVRP_ERR_ALIGNMENT, "kv_attend_relocated: q, out not 16-byte aligned");
   if (seq_chunks[0] != 0 || seq_chunks[n_seqs] != n_chunks)
     return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: seq_chunks must run from 0 to n_chunks");
-  std::vector<int32_t> tok(n_chunks);
-  int m_max = 0;
   for (int s = 0; s < n_seqs; ++s)
     if (seq_chunks[s + 1] < seq_chunks[s])
       return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: seq_chunks must not decrease");
+  std::vector<int32_t> tok(n_chunks);
+  int m_max = 0;
+  int64_t all_tokens = 0;
   for (int i = 0; i < n_chunks; ++i) {
     const kvrp_attn_chunk& c = chunks[i];
     if (c.n_tokens < 0) return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: chunk %d: n_tokens < 0", i);
@@ -555,17 +715,22 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
       return fail(KVRP_ERR_ALIGNMENT, "kv_attend_relocated: chunk %d: pointers must be 16-byte aligned", i);
     tok[i] = c.n_tokens;
     m_max = std::max(m_max, (int)c.rank);
+    all_tokens += c.n_tokens;
   }
-  const size_t need = kv_attend_relocated_workspace_size(n_chunks, tok.data(), n_q_heads, head_dim);
+  if (all_tokens > INT32_MAX)
+    return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: at most 2^31 - 1 tokens per call");
+  const size_t need = kv_attend_relocated_workspace_size(n_chunks, tok.data(), n_q_heads, n_kv_heads, head_dim);
   if (!workspace || workspace_bytes < need)
     return fail(KVRP_ERR_WORKSPACE, "kv_attend_relocated: workspace of %zu bytes needed", need);
 
+  const at::Plan pl = at::make_plan(n_kv_heads, head_dim, m_max);
   static_assert(sizeof(at::Params) <= 32000, "kernel parameter block too large");
-  at::Params* pp = new at::Params;   // ~17 KB: off the stack
+  at::Params* pp = new at::Params;   // ~20 KB: off the stack
   std::memset(pp, 0, sizeof(at::Params));
   at::Params& p = *pp;
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
+  p.status = d_status;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
   const size_t qhl_bytes = (2 * 2 * (size_t)n_chunks * n_q_heads * head_dim + 255) / 256 * 256;
   const size_t whl_bytes = (2 * 2 * (size_t)n_chunks * n_q_heads * at::kMaxRank + 255) / 256 * 256;
@@ -578,9 +743,19 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   p.Hkv = n_kv_heads;
   p.d = head_dim;
   p.g = n_q_heads / n_kv_heads;
+  p.m_max = m_max;
+  p.hg = pl.hg;
+  p.n_hg = pl.n_hg;
+  p.ns = pl.ns;
+  p.ts = pl.ts;
+  p.stages = pl.stages;
+  p.k_pitch = pl.k_pitch;
+  p.kv_bytes = pl.kv_bytes;
+  p.u_bytes = pl.u_bytes;
+  p.stage_bytes = pl.stage_bytes;
   p.scale = softmax_scale;
-  p.theta = rope_theta;
-  int blk = 0;
+  for (int i = 0; i < head_dim / 2; ++i) p.inv_freq[i] = std::pow(rope_theta, -2.0 * i / head_dim);
+  int64_t st0 = 0;
   for (int s = 0; s < n_seqs; ++s)
     for (int i = seq_chunks[s]; i < seq_chunks[s + 1]; ++i) {
       const kvrp_attn_chunk& c = chunks[i];
@@ -594,32 +769,56 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
       r.n_tokens = c.n_tokens;
       r.rank = c.rank;
       r.seq = s;
-      r.blk0 = blk;
+      r.st0 = (int32_t)st0;
       p.delta[i] = c.delta;
-      blk += (int)at::blocks_of(c.n_tokens);
+      st0 += (c.n_tokens + pl.ts - 1) / pl.ts;
     }
-  p.n_blocks = blk;
+  p.s_hg = st0;
   for (int s = 0; s <= n_seqs; ++s) p.seq_chunk[s] = seq_chunks[s];
-  p.m_max = m_max;
 
   cudaStream_t st = stream;
-  const at::BlockSmem L = at::block_smem(head_dim, m_max);
-  void (*blk_fn)(at::Params) = head_dim == 64 ? (m_max <= 32 ? at::block_kernel<64, 4> : at::block_kernel<64, 16>)
-                                              : (m_max <= 32 ? at::block_kernel<128, 4> : at::block_kernel<128, 16>);
-  cudaError_t e = cudaFuncSetAttribute(blk_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, L.bytes);
+  void (*blk_fn)(at::Params) = nullptr;
+  const bool two = p.g > 8, big = m_max > 32;
+  if (head_dim == 64)
+    blk_fn = two ? (big ? at::block_kernel<64, 2, 128> : at::block_kernel<64, 2, 32>)
+                 : (big ? at::block_kernel<64, 1, 128> : at::block_kernel<64, 1, 32>);
+  else
+    blk_fn = two ? (big ? at::block_kernel<128, 2, 128> : at::block_kernel<128, 2, 32>)
+                 : (big ? at::block_kernel<128, 1, 128> : at::block_kernel<128, 1, 32>);
+  const int smem = pl.stages * pl.stage_bytes;
+  cudaError_t e = cudaFuncSetAttribute(blk_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int per_sm = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, blk_fn, at::kThreads, smem);
+  const int n_cta_max = std::min(at::kMaxCtas, at::kCtasPerSm * at::sm_count());
+  p.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)std::max(per_sm, 1) * at::sm_count(), (int64_t)n_cta_max,
+                                                         (int64_t)p.n_hg * p.s_hg}));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(at::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, head_dim * at::kMaxRank * 2);
   if (e == cudaSuccess) {
     at::prep_kernel<<<dim3(n_chunks, n_kv_heads), 256, (size_t)head_dim * m_max * 2, st>>>(p);
     e = cudaGetLastError();
   }
-  if (e == cudaSuccess && blk > 0) {
-    blk_fn<<<dim3(blk, n_kv_heads), at::kThreads, L.bytes, st>>>(p);
-    e = cudaGetLastError();
+  // prep -> block -> combine as programmatic dependent launches: each may start while
+  // the previous one runs, and waits (griddepcontrol.wait) before it reads that one's results
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (e == cudaSuccess && p.s_hg > 0) {
+    cfg.gridDim = dim3(p.n_cta);
+    cfg.blockDim = dim3(at::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    e = cudaLaunchKernelEx(&cfg, blk_fn, p);
   }
   if (e == cudaSuccess) {
-    at::combine_kernel<<<dim3(n_seqs, n_q_heads), head_dim, 0, st>>>(p);   // one thread per feature
-    e = cudaGetLastError();
+    const int items = n_seqs * n_q_heads;
+    cfg.gridDim = dim3((items + at::kCombineWarps - 1) / at::kCombineWarps);
+    cfg.blockDim = dim3(32 * at::kCombineWarps);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, head_dim == 64 ? at::combine_kernel<64> : at::combine_kernel<128>, p);
   }
   delete pp;
   if (e != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_attend_relocated: %s", cudaGetErrorString(e));

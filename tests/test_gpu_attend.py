@@ -32,22 +32,23 @@ def _bits(t):
 
 
 def make_case(seed, seqs, Hq, Hkv, d):
-    """seqs: list of sequences, each a list of (n_tokens, rank) chunks."""
-    from oracle import round_to_bf16_bits
+    """seqs: list of sequences, each a list of (n_tokens, rank) chunks.  Inputs
+    are seeded normal draws (fp32) rounded to bf16 (nearest even), as bits."""
     rng = np.random.default_rng(seed)
     D = Hkv * d
-    q = round_to_bf16_bits(rng.standard_normal((len(seqs), Hq, d)))
+
+    def bf16(shape, std=1.0):
+        x = torch.from_numpy((std * rng.standard_normal(shape, dtype=np.float32)).astype(np.float32))
+        return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    q = bf16((len(seqs), Hq, d))
     chunks, seq_chunks = [], [0]
     for s in seqs:
         for (T, m) in s:
-            c = {"k": round_to_bf16_bits(rng.standard_normal((T, D))),
-                 "v": round_to_bf16_bits(rng.standard_normal((T, D))),
-                 "delta": int(rng.integers(-40000, 40001)), "rank": m}
+            c = {"k": bf16((T, D)), "v": bf16((T, D)), "delta": int(rng.integers(-40000, 40001)), "rank": m}
             if m:
-                c["uk"] = round_to_bf16_bits(0.3 * rng.standard_normal((T, m)))
-                c["vk"] = round_to_bf16_bits(0.1 * rng.standard_normal((D, m)))
-                c["uv"] = round_to_bf16_bits(0.3 * rng.standard_normal((T, m)))
-                c["vv"] = round_to_bf16_bits(0.1 * rng.standard_normal((D, m)))
+                c["uk"], c["vk"] = bf16((T, m), 0.3), bf16((D, m), 0.1)
+                c["uv"], c["vv"] = bf16((T, m), 0.3), bf16((D, m), 0.1)
             chunks.append(c)
         seq_chunks.append(len(chunks))
     return q, chunks, seq_chunks
@@ -66,11 +67,13 @@ def run_gpu(q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
         ac.append(kvrp.AttnChunk(k=k, v=v, n_tokens=T, delta=c["delta"], rank=c["rank"], uk=f[0], vk=f[1], uv=f[2],
                                  vv=f[3]))
     out = torch.empty((len(seq_chunks) - 1, Hq, d), dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([c["k"].shape[0] for c in chunks], Hq, d),
+    ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([c["k"].shape[0] for c in chunks], Hq, Hkv, d),
                      dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
     kvrp.kv_attend_relocated(_dev(q), ac, seq_chunks, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, rope_theta=theta,
-                             softmax_scale=scale, out=out, workspace=ws)
+                             softmax_scale=scale, out=out, workspace=ws, d_status=status)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0
     return _bits(out)
 
 
@@ -99,6 +102,8 @@ def check(got, q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
     ([[(300, 32), (77, 0)], [(1, 0)], [(128, 16), (129, 32), (513, 16)]], 28, 4, 128),   # GQA, ragged, mixed ranks
     ([[(200, 16), (64, 16)], [(1000, 32)]], 8, 8, 64),                                    # MHA, head_dim 64
     ([[(260, 32)], [(17, 0), (300, 16)]], 32, 2, 128),                                    # 16 query heads per KV head
+    ([[(100, 48), (50, 128)], [(65, 0), (1, 128)]], 6, 3, 64),                            # odd KV heads; ranks 48, 128
+    ([[(9000, 32), (7000, 16)], [(12000, 0)]], 16, 4, 128),                               # long: several stages per CTA
 ])
 def test_attention_matches_oracle(seqs, Hq, Hkv, d):
     theta, scale = 1e6, d ** -0.5
