@@ -31,10 +31,11 @@
 //                  (movmatrix) -- warp-level tensor-core MMAs (mma.sync
 //                  m16n8k16 bf16 -> fp32; q, w and P enter as high + low bf16
 //                  parts, two products each).  At a chunk or share boundary a
-//                  warp writes its (O, max, sum) as one fp32 partial;
+//                  warp applies the value patch, O^T += V_v,h (P U_v)^T (tensor
+//                  cores; P U_v as high + low bf16 parts), and writes its
+//                  (O, max, sum) as one fp32 partial;
 //   combine_kernel one CTA per (sequence, query head): merges the partials of
-//                  the sequence's chunks by their maxima, applies each chunk's
-//                  value patch V_v,h (P U_v) once, rounds to bf16.
+//                  the sequence's chunks by their maxima, rounds to bf16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -103,27 +104,41 @@ __device__ __forceinline__ uint16_t to_bf(float v) {
 __device__ __forceinline__ uint32_t pack_bf(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
 __device__ __forceinline__ uint32_t ldg32(const uint16_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
 
+// Shared memory is kept small (V_k,h, the queries and the angle table: 14 KB
+// for d = 128, rank 32) so that the block kernel's two CTAs per SM fit beside a
+// running prep CTA.
 __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(16) uint16_t vks[];   // V_k,h [d][m]
-  __shared__ float2 rot[64];                         // (cos, sin) of -delta * theta^(-2i/d)
-  __shared__ float qs[kMaxGroup * 128];              // the group's queries, fp32
+  extern __shared__ __align__(16) uint8_t psm[];   // V_k,h [d][m + 8] bf16, then the queries [g][d] fp32
+  __shared__ float2 rot[64];                        // (cos, sin) of -delta * theta^(-2i/d)
   // the block kernel may launch now: its producer streams K, V and U (inputs) while
   // this kernel prepares the queries, which its consumers wait for
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int ci = blockIdx.x, h = blockIdx.y;
   const ChunkRec& c = p.c[ci];
-  const int d = p.d, half = d / 2, g = p.g, m = c.rank, Hq = p.Hq;
+  const int d = p.d, half = d / 2, g = p.g, m = c.rank, Hq = p.Hq, vp = m + 8;
+  uint16_t* vks = reinterpret_cast<uint16_t*>(psm);
+  float* qs = reinterpret_cast<float*>(psm + (size_t)d * (p.m_max + 8) * 2);
   const uint16_t* q = p.q + ((int64_t)c.seq * Hq + (int64_t)h * g) * d;
   uint16_t* qh = p.qhl + ((int64_t)ci * 2 * Hq + (int64_t)h * g) * d;
   uint16_t* ql = qh + (int64_t)Hq * d;
-  if (m > 0)
-    for (int e = threadIdx.x; e < d * m / 8; e += blockDim.x)
-      reinterpret_cast<uint4*>(vks)[e] = reinterpret_cast<const uint4*>(c.vk + (int64_t)h * d * m)[e];
+  if (m > 0) {
+    const uint4* src = reinterpret_cast<const uint4*>(c.vk + (int64_t)h * d * m);
+    for (int e = threadIdx.x; e < d * m / 8; e += blockDim.x) {
+      const int f = e / (m / 8), r8 = e - f * (m / 8);
+      *reinterpret_cast<uint4*>(vks + f * vp + 8 * r8) = __ldg(src + e);
+    }
+  }
   for (int e = threadIdx.x; e < g * d; e += blockDim.x) qs[e] = bf(q[e]);
   if (threadIdx.x < half) {
-    double sn, cs;
-    sincos(-static_cast<double>(p.delta[ci]) * p.inv_freq[threadIdx.x], &sn, &cs);
-    rot[threadIdx.x] = make_float2((float)cs, (float)sn);
+    // phi = -delta theta^(-2i/d) reduced to [-pi, pi] in fp64 (Cody and Waite: 2 pi as a
+    // double plus its remainder, each product fused), then sine and cosine in fp32
+    const double two_pi_hi = 6.283185307179586, two_pi_lo = 2.4492935982947064e-16;
+    const double phi = -static_cast<double>(p.delta[ci]) * p.inv_freq[threadIdx.x];
+    const double k = rint(phi * (1.0 / 6.283185307179586));
+    const double red = fma(-k, two_pi_lo, fma(-k, two_pi_hi, phi));
+    float sn, cs;
+    sincosf(static_cast<float>(red), &sn, &cs);
+    rot[threadIdx.x] = make_float2(cs, sn);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < g * half; e += blockDim.x) {
@@ -138,19 +153,32 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Param
     ql[j * d + i + half] = to_bf(r1 - bf(h1));
   }
   if (m == 0) return;
+  // W^T [m][g] = V_k,h^T Q^T on tensor cores (bf16 products, exact; fp32 sums): warp ->
+  // rank m-tiles; A = V_k,h^T by transposed ldmatrix of the [d][m] rows, B = Q^T from q
   uint16_t* wh = p.whl + ((int64_t)ci * 2 * Hq + (int64_t)h * g) * p.m_max;
   uint16_t* wl = wh + (int64_t)Hq * p.m_max;
-  for (int e = threadIdx.x; e < g * m; e += blockDim.x) {
-    const int j = e / m, r = e - j * m;
-    float a4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < d; i += 4) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) a4[u] = fmaf(bf(vks[(i + u) * m + r]), qs[j * d + i + u], a4[u]);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int t_row = (lane & 7) + ((lane >> 4) << 3), t_col = ((lane >> 3) & 1) * 8;
+  for (int t = warp; t < (m / 16) * ((g + 7) / 8); t += blockDim.x / 32) {
+    const int mt = t % (m / 16), nt = t / (m / 16), j = nt * 8 + gid;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < d; k0 += 16) {
+      uint32_t a[4];
+      ldsm_x4_trans(a, smem_u32(vks + (k0 + t_row) * vp + mt * 16 + t_col));
+      const uint32_t b0 = j < g ? ldg32(q + j * d + k0 + 2 * tig) : 0u;
+      const uint32_t b1 = j < g ? ldg32(q + j * d + k0 + 8 + 2 * tig) : 0u;
+      mma16816(acc, a, b0, b1);
     }
-    const float w = ((a4[0] + a4[1]) + (a4[2] + a4[3])) * p.scale;
-    const uint16_t hw = to_bf(w);
-    wh[j * p.m_max + r] = hw;
-    wl[j * p.m_max + r] = to_bf(w - bf(hw));
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {   // (rank mt 16 + gid + 8 (e / 2), head nt 8 + 2 tig + e % 2)
+      const int r = mt * 16 + gid + (e >> 1) * 8, jj = nt * 8 + 2 * tig + (e & 1);
+      if (jj < g) {
+        const float w = acc[e] * p.scale;
+        const uint16_t hw = to_bf(w);
+        wh[jj * p.m_max + r] = hw;
+        wl[jj * p.m_max + r] = to_bf(w - bf(hw));
+      }
+    }
   }
 }
 
@@ -161,9 +189,12 @@ __global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Param
 __host__ __device__ __forceinline__ int64_t share_begin(int64_t total, int n_cta, int i) {
   return (int64_t)i * total / n_cta;
 }
-// The CTA whose share holds stage f: the largest i with begin(i) <= f.
+// The CTA whose share holds stage f: the largest i with begin(i) <= f (32-bit division
+// when the product fits, as it does below ~2M stages).
 __host__ __device__ __forceinline__ int share_of(int64_t total, int n_cta, int64_t f) {
-  return (int)(((f + 1) * n_cta - 1) / total);
+  const int64_t num = (f + 1) * n_cta - 1;
+  if (num < 0x7fffffffLL && total < 0x7fffffffLL) return (int)((uint32_t)num / (uint32_t)total);
+  return (int)(num / total);
 }
 // Position in the stage sequence: head group, chunk, stage within the chunk,
 // and the chunk's stage count.  Decoded once per CTA, then advanced.
@@ -243,6 +274,8 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
     mbar_init_fence();
   }
   __syncthreads();
+  // the combine kernel may launch (and wait, resident) while this grid runs
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   volatile int* abort_p = &abort_flag;
   if (f0 >= f1) return;
   Cursor r = cursor_at(p, f0);
@@ -540,20 +573,23 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
   }
 }
 
-// One warp per (sequence, query head); lane -> features lane, lane + 32, ...
-// Merges the partials of the sequence's chunks by their maxima (a partial with
-// no tokens has max -inf and weight 0) and rounds to bf16.  The partials of all
-// the sequence's chunks form one list, taken in groups of 32: lane x locates
-// entry x of a group (arithmetic only), so the loads of a group are independent.
-constexpr int kCombineWarps = 4;
+// One CTA per (sequence, query head).  Merges the partials of the sequence's
+// chunks by their maxima (a partial with no tokens has max -inf and weight 0)
+// and rounds to bf16.  The partials of all the sequence's chunks form one list,
+// taken in groups of kCombineThreads: thread t locates entry t of a group
+// (arithmetic only) and loads its max and sum; the weighted features are then
+// summed with thread -> feature (d = 128) or feature and entry parity (d = 64),
+// eight entries' loads in flight.
+constexpr int kCombineThreads = 128;
 template <int D>
-__global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const __grid_constant__ Params p) {
-  constexpr int FL = D / 32;   // features per lane
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ Params p) {
+  constexpr int G = kCombineThreads / D;   // thread groups, each covering the D features
+  __shared__ const float* ent[kCombineThreads];
+  __shared__ float wts[kCombineThreads];
+  __shared__ float red[kCombineThreads / 32];
+  __shared__ float part[kCombineThreads];
   asm volatile("griddepcontrol.wait;" ::: "memory");   // the block kernel's partials
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t item = (int64_t)blockIdx.x * kCombineWarps + warp;
-  if (item >= (int64_t)p.n_seqs * p.Hq) return;
-  const int s = (int)(item / p.Hq), jq = (int)(item - (int64_t)s * p.Hq);
+  const int s = blockIdx.x, jq = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = p.g, pw = D + 2;
   const int h = jq / g, hg = h / p.hg, row = (h % p.hg) * g + jq % g;
   const int64_t total = (int64_t)p.n_hg * p.s_hg;
@@ -574,53 +610,68 @@ __global__ void __launch_bounds__(32 * kCombineWarps) combine_kernel(const __gri
     }
     return n;
   };
-  const float* pe;
-  const int n_list = locate(lane, pe);
-  // the first group's max and sum stay in registers; later groups reload theirs
-  float mx0 = pe ? pe[D] : -INFINITY, l0 = pe ? pe[D + 1] : 0.f;
+  auto block_reduce = [&](float v, bool is_max) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, off);
+      v = is_max ? fmaxf(v, o) : v + o;
+    }
+    __syncthreads();
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
+    return v;
+  };
+  // the first group's entry, max and sum stay in registers; later groups reload theirs
+  const float* pe0;
+  const int n_list = locate(tid, pe0);
+  const float mx0 = pe0 ? pe0[D] : -INFINITY, l0 = pe0 ? pe0[D + 1] : 0.f;
   float M = mx0;
-  for (int L0 = 32; L0 < n_list; L0 += 32) {
+  for (int L0 = kCombineThreads; L0 < n_list; L0 += kCombineThreads) {
     const float* q;
-    locate(L0 + lane, q);
+    locate(L0 + tid, q);
     if (q) M = fmaxf(M, q[D]);
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float acc[FL] = {};
-  float den = 0.f;
-  for (int L0 = 0; L0 < n_list; L0 += 32) {
+  M = block_reduce(M, true);
+  const int f = tid % D, grp = tid / D;
+  float acc = 0.f, den = 0.f;
+  for (int L0 = 0; L0 < n_list; L0 += kCombineThreads) {
+    const float* pe = pe0;
     float mx = mx0, lt = l0;
     if (L0 > 0) {
-      locate(L0 + lane, pe);
+      locate(L0 + tid, pe);
       mx = pe ? pe[D] : -INFINITY;
       lt = pe ? pe[D + 1] : 0.f;
     }
     const float wt = mx == -INFINITY ? 0.f : expf(mx - M);
-    float dl = wt * lt;
+    den += wt * lt;
+    __syncthreads();   // the previous group's entries have been read
+    ent[tid] = pe;
+    wts[tid] = wt;
+    __syncthreads();
+    const int nx = min(kCombineThreads, n_list - L0);
+    for (int x = grp; x < nx; x += 8 * G) {
+      float v[8], w[8];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, off);
-    den += dl;
-    const int nx = min(32, n_list - L0);
-    const uint64_t pa = reinterpret_cast<uint64_t>(pe);
-    for (int x = 0; x < nx; x += 4) {   // four entries' loads in flight
-      float w[4], v[4][FL];
-#pragma unroll
-      for (int y = 0; y < 4; ++y) {
-        const int xy = min(x + y, nx - 1);
-        w[y] = x + y < nx ? __shfl_sync(0xffffffffu, wt, xy) : 0.f;
-        const float* py = reinterpret_cast<const float*>(__shfl_sync(0xffffffffu, pa, xy));
-#pragma unroll
-        for (int u = 0; u < FL; ++u) v[y][u] = py[lane + 32 * u];
+      for (int y = 0; y < 8; ++y) {
+        const int xy = x + y * G;
+        w[y] = xy < nx ? wts[xy] : 0.f;
+        v[y] = xy < nx ? ent[xy][f] : 0.f;
       }
 #pragma unroll
-      for (int y = 0; y < 4; ++y)
-#pragma unroll
-        for (int u = 0; u < FL; ++u) acc[u] = fmaf(w[y], v[y][u], acc[u]);
+      for (int y = 0; y < 8; ++y) acc = fmaf(w[y], v[y], acc);
     }
   }
-  uint16_t* out = p.out + ((int64_t)s * p.Hq + jq) * D;
-#pragma unroll
-  for (int u = 0; u < FL; ++u) out[lane + 32 * u] = to_bf(den > 0.f ? acc[u] / den : 0.f);
+  den = block_reduce(den, false);
+  if (G > 1) {
+    part[tid] = acc;
+    __syncthreads();
+    if (grp == 0)
+      for (int k = 1; k < G; ++k) acc += part[k * D + f];
+  }
+  if (grp == 0) p.out[((int64_t)s * p.Hq + jq) * D + f] = to_bf(den > 0.f ? acc / den : 0.f);
 }
 
 // ---- host-side planning -----------------------------------------------------
@@ -792,10 +843,10 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   const int n_cta_max = std::min(at::kMaxCtas, at::kCtasPerSm * at::sm_count());
   p.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)std::max(per_sm, 1) * at::sm_count(), (int64_t)n_cta_max,
                                                          (int64_t)p.n_hg * p.s_hg}));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(at::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, head_dim * at::kMaxRank * 2);
   if (e == cudaSuccess) {
-    at::prep_kernel<<<dim3(n_chunks, n_kv_heads), 256, (size_t)head_dim * m_max * 2, st>>>(p);
+    const size_t prep_smem = (size_t)head_dim * (m_max + 8) * 2 + sizeof(float) * p.g * head_dim;
+    e = cudaFuncSetAttribute(at::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
+    if (e == cudaSuccess) at::prep_kernel<<<dim3(n_chunks, n_kv_heads), 256, prep_smem, st>>>(p);
     e = cudaGetLastError();
   }
   // prep -> block -> combine as programmatic dependent launches: each may start while
@@ -814,9 +865,8 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
     e = cudaLaunchKernelEx(&cfg, blk_fn, p);
   }
   if (e == cudaSuccess) {
-    const int items = n_seqs * n_q_heads;
-    cfg.gridDim = dim3((items + at::kCombineWarps - 1) / at::kCombineWarps);
-    cfg.blockDim = dim3(32 * at::kCombineWarps);
+    cfg.gridDim = dim3(n_seqs, n_q_heads);
+    cfg.blockDim = dim3(at::kCombineThreads);
     cfg.dynamicSmemBytes = 0;
     e = cudaLaunchKernelEx(&cfg, head_dim == 64 ? at::combine_kernel<64> : at::combine_kernel<128>, p);
   }
