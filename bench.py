@@ -37,9 +37,9 @@ KERNEL_SOURCES = ["position_invariant_kv_gb300/csrc/kvrp_kernel.cu", "position_i
 L2_BYTES = 129 * 2 ** 20
 
 
-def kernel_hash() -> str:
+def kernel_hash(sources=None) -> str:
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources or KERNEL_SOURCES:
         h.update(open(os.path.join(ROOT, p), "rb").read())
     return h.hexdigest()[:16]
 
@@ -52,14 +52,17 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profiled_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary of this kernel, if
-    it was taken on the current kernel sources."""
-    p = os.path.join(ROOT, "profiles", "relocate_kernel_dram.json")
+ATTEND_SOURCES = ["position_invariant_kv_gb300/csrc/kvrp_attend.cu", "position_invariant_kv_gb300/csrc/kvrp_ptx.h"]
+
+
+def profiled_traffic(workload: str, summary: str = "relocate_kernel_dram.json", sources=None):
+    """DRAM bytes per launch from the committed ncu summary of a kernel, if it
+    was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
-    if d.get("kernel_hash") != kernel_hash():
+    if d.get("kernel_hash") != kernel_hash(sources):
         return None
     ent = d.get("per_launch", {}).get(workload)
     return None if ent is None else ent.get("dram_bytes")
@@ -660,8 +663,10 @@ def bench_attend(args) -> dict:
         "config": {"workload": attn_text(a), "context_tokens_per_step": ctx, "algorithmic_bytes_per_step": nb,
                    "l2": f"inputs larger than L2 ({nb / 1e6:.0f} MB read per step vs 129 MB L2)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": None,
-                     "kernel": "kv_attend_relocated, whole call (table, block and combine kernels)",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic("attend", "attend_dram.json", ATTEND_SOURCES),
+                     "kernel": "kv_attend_relocated, whole call (prep, block and combine kernels); traffic is "
+                               "block_kernel's DRAM bytes per launch",
                      "peak_source": peaks["source"]},
         "gpu_launches": 3 * args.steps,
         "clocks": clocks.summary(),
