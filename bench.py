@@ -527,7 +527,9 @@ def bench_patch_form(args) -> dict:
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "kernel": "kv_patch_form_orbit, whole call (delta, tensor-core passes, k x k solves)",
                      "peak_source": peaks["source"]},
-        "gpu_launches": None,
+        # per tensor: deficit, Omega transpose, 2q + 3 passes over the deficit, 2q + 3 orthonormalisation
+        # rounds of (Gram, Cholesky, apply), the projected Gram, Jacobi, the B^T W apply, U and V writers
+        "gpu_launches": steps * len(wl.tensors) * (2 + (2 * q + 3) + 3 * (2 * q + 3) + 5),
         "clocks": clocks.summary(),
         "device_status": int(d_status.item()),
     }
