@@ -600,6 +600,31 @@ def attn_bytes(a) -> int:
     return n_chunks * per_chunk + a["seqs"] * a["Hq"] * a["d"] * 2 * 2
 
 
+def attend_workload(a, dev, seed: int = 4242):
+    """The attention row's seeded synthetic inputs on the device: (tensors kept
+    alive, AttnChunk list, q [seqs][Hq][d], seq_chunks).  bf16 N(0,1) K, V and
+    queries, U_k, U_v N(0, 0.3^2), V_k, V_v N(0, 0.1^2); chunk i shifted by
+    (7919 i mod 65536) - 32768."""
+    import torch
+    import position_invariant_kv_gb300 as kvrp
+    g = torch.Generator(device=dev).manual_seed(seed)
+    D = a["Hkv"] * a["d"]
+
+    def rnd(*shape, std=1.0):
+        return (std * torch.randn(shape, generator=g, device=dev)).to(torch.bfloat16)
+
+    keep, chunks = [], []
+    for i in range(a["seqs"] * a["chunks"]):
+        t = [rnd(a["tokens"], D), rnd(a["tokens"], D), rnd(a["tokens"], a["rank"], std=0.3),
+             rnd(D, a["rank"], std=0.1), rnd(a["tokens"], a["rank"], std=0.3), rnd(D, a["rank"], std=0.1)]
+        keep += t
+        chunks.append(kvrp.AttnChunk(k=t[0], v=t[1], n_tokens=a["tokens"], delta=(i * 7919) % 65536 - 32768,
+                                     rank=a["rank"], uk=t[2], vk=t[3], uv=t[4], vv=t[5]))
+    seq_chunks = [s * a["chunks"] for s in range(a["seqs"] + 1)]
+    q = rnd(a["seqs"], a["Hq"], a["d"])
+    return keep, chunks, q, seq_chunks
+
+
 def bench_attend(args) -> dict:
     import torch
     import position_invariant_kv_gb300 as kvrp
@@ -612,23 +637,9 @@ def bench_attend(args) -> dict:
     kvrp.lib()
     a = dict(ATTN_SHAPE)
     dev = f"cuda:{local}"
-    g = torch.Generator(device=dev).manual_seed(4242)
-    D = a["Hkv"] * a["d"]
     n_chunks = a["seqs"] * a["chunks"]
-
-    def rnd(*shape, std=1.0):
-        return (std * torch.randn(shape, generator=g, device=dev)).to(torch.bfloat16)
-
-    keep, chunks = [], []
-    for i in range(n_chunks):
-        t = [rnd(a["tokens"], D), rnd(a["tokens"], D), rnd(a["tokens"], a["rank"], std=0.3),
-             rnd(D, a["rank"], std=0.1), rnd(a["tokens"], a["rank"], std=0.3), rnd(D, a["rank"], std=0.1)]
-        keep += t
-        chunks.append(kvrp.AttnChunk(k=t[0], v=t[1], n_tokens=a["tokens"], delta=(i * 7919) % 65536 - 32768,
-                                     rank=a["rank"], uk=t[2], vk=t[3], uv=t[4], vv=t[5]))
+    keep, chunks, q, seq_chunks = attend_workload(a, dev)
     arr = kvrp.attn_chunk_array(chunks)
-    seq_chunks = [s * a["chunks"] for s in range(a["seqs"] + 1)]
-    q = rnd(a["seqs"], a["Hq"], a["d"])
     out = torch.empty_like(q)
     ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([a["tokens"]] * n_chunks, a["Hq"], a["Hkv"], a["d"]),
                      dtype=torch.uint8, device=dev)

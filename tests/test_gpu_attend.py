@@ -137,3 +137,30 @@ def test_shift_moves_only_through_the_rotation():
     chunks[0]["delta"] = 5000
     got1 = run_gpu(q, chunks, sc, Hq, Hkv, d, 1e4, 0.088)
     assert np.any(got1 != got0)
+
+
+def test_bench_workload_on_sampled_sequences():
+    """The bench's own workload and launch (16 sequences x 4 chunks x 4096 tokens,
+    28 query / 4 KV heads x 128, rank-32 K and V patches): sequences 0, 7 and 15
+    against the oracle, every output element of each."""
+    import bench
+    import position_invariant_kv_gb300 as kvrp
+    a = dict(bench.ATTN_SHAPE)
+    keep, chunks, q, sc = bench.attend_workload(a, "cuda")
+    out = torch.empty_like(q)
+    ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([c.n_tokens for c in chunks], a["Hq"], a["Hkv"], a["d"]),
+                     dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = a["d"] ** -0.5
+    kvrp.kv_attend_relocated(q, chunks, sc, n_q_heads=a["Hq"], n_kv_heads=a["Hkv"], head_dim=a["d"],
+                             rope_theta=a["theta"], softmax_scale=scale, out=out, workspace=ws, d_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = _bits(out)
+    qb = _bits(q)
+    for s in (0, 7, 15):
+        host = [{"k": _bits(c.k), "v": _bits(c.v), "delta": c.delta, "rank": c.rank, "uk": _bits(c.uk),
+                 "vk": _bits(c.vk), "uv": _bits(c.uv), "vv": _bits(c.vv)} for c in chunks[sc[s]:sc[s + 1]]]
+        sub_sc = [0, len(host)]
+        worst = check(got[s:s + 1], qb[s:s + 1], host, sub_sc, a["Hq"], a["Hkv"], a["d"], a["theta"], scale)
+        print("sequence", s, "worst ulp distance", worst)
