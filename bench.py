@@ -590,7 +590,7 @@ ATTN_SHAPE = dict(seqs=16, chunks=4, tokens=4096, Hq=28, Hkv=4, d=128, rank=32, 
 def attn_text(a) -> str:
     return (f"one layer of a Qwen2.5-VL-shaped GQA model ({a['Hq']} query / {a['Hkv']} KV heads x {a['d']}): "
             f"{a['seqs']} sequences, each {a['chunks']} relocated chunks x {a['tokens']} tokens with rank-{a['rank']} "
-            f"K and V patches, theta {a['theta']:g}")
+            f"K and V patches, theta {a['theta']:g}; canonical K, V in a shuffled 16-token paged pool")
 
 
 def attn_bytes(a) -> int:
@@ -602,24 +602,33 @@ def attn_bytes(a) -> int:
 
 def attend_workload(a, dev, seed: int = 4242):
     """The attention row's seeded synthetic inputs on the device: (tensors kept
-    alive, AttnChunk list, q [seqs][Hq][d], seq_chunks).  bf16 N(0,1) K, V and
-    queries, U_k, U_v N(0, 0.3^2), V_k, V_v N(0, 0.1^2); chunk i shifted by
+    alive, AttnChunk list, q [seqs][Hq][d], seq_chunks).  The canonical K and V
+    of all chunks sit in one paged pool per tensor ([pages][16][H_kv d], pages
+    handed out by a seeded shuffle, as a serving cache holds them); each chunk
+    reads its pages through its block table.  bf16 N(0,1) K, V and queries,
+    U_k, U_v N(0, 0.3^2), V_k, V_v N(0, 0.1^2); chunk i shifted by
     (7919 i mod 65536) - 32768."""
     import torch
     import position_invariant_kv_gb300 as kvrp
     g = torch.Generator(device=dev).manual_seed(seed)
     D = a["Hkv"] * a["d"]
+    n_chunks = a["seqs"] * a["chunks"]
+    per = (a["tokens"] + 15) // 16
+    n_pages = n_chunks * per
 
     def rnd(*shape, std=1.0):
         return (std * torch.randn(shape, generator=g, device=dev)).to(torch.bfloat16)
 
-    keep, chunks = [], []
-    for i in range(a["seqs"] * a["chunks"]):
-        t = [rnd(a["tokens"], D), rnd(a["tokens"], D), rnd(a["tokens"], a["rank"], std=0.3),
-             rnd(D, a["rank"], std=0.1), rnd(a["tokens"], a["rank"], std=0.3), rnd(D, a["rank"], std=0.1)]
+    pool_k, pool_v = rnd(n_pages, 16, D), rnd(n_pages, 16, D)
+    perm = torch.randperm(n_pages, generator=g, device=dev).to(torch.int32)
+    keep, chunks = [pool_k, pool_v, perm], []
+    for i in range(n_chunks):
+        t = [rnd(a["tokens"], a["rank"], std=0.3), rnd(D, a["rank"], std=0.1), rnd(a["tokens"], a["rank"], std=0.3),
+             rnd(D, a["rank"], std=0.1)]
         keep += t
-        chunks.append(kvrp.AttnChunk(k=t[0], v=t[1], n_tokens=a["tokens"], delta=(i * 7919) % 65536 - 32768,
-                                     rank=a["rank"], uk=t[2], vk=t[3], uv=t[4], vv=t[5]))
+        chunks.append(kvrp.AttnChunk(k=pool_k, v=pool_v, n_tokens=a["tokens"], delta=(i * 7919) % 65536 - 32768,
+                                     rank=a["rank"], uk=t[0], vk=t[1], uv=t[2], vv=t[3],
+                                     block_table=perm[i * per:(i + 1) * per], num_pages=n_pages))
     seq_chunks = [s * a["chunks"] for s in range(a["seqs"] + 1)]
     q = rnd(a["seqs"], a["Hq"], a["d"])
     return keep, chunks, q, seq_chunks

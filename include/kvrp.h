@@ -313,7 +313,11 @@ kvrp_status kv_patch_form_orbit(
  *               [seq_chunks[s], seq_chunks[s + 1]) (host array of n_seqs + 1,
  *               from 0 to n_chunks, non-decreasing).
  *   kvrp_attn_chunk.k, .v   device bf16 [n_tokens][n_kv_heads * head_dim] rows
- *               of one layer; .rank 0 or a multiple of 16 up to 128; .uk, .uv
+ *               of one layer, or, with .block_table, pools [num_pages][16][row]
+ *               in which token t of the chunk sits at page block_table[t / 16],
+ *               slot t % 16 (a paged cache; an entry outside [0, num_pages)
+ *               sets KVRP_DEV_BAD_PAGE and reads page 0 instead, the output then
+ *               being undefined); .rank 0 or a multiple of 16 up to 128; .uk, .uv
  *               [n_tokens][rank], .vk, .vv [n_kv_heads * head_dim][rank] bf16
  *               (all four, or none when rank is 0); .delta the shift.
  *   head_dim    64 or 128; n_q_heads a multiple of n_kv_heads, at most 16x.
@@ -344,6 +348,8 @@ typedef struct {
   const void* vk;
   const void* uv;
   const void* vv;
+  const int32_t* block_table;  /* device; NULL => k, v are contiguous [n_tokens][row] */
+  int32_t num_pages;           /* pages of the pool k, v point to (when block_table != NULL) */
 } kvrp_attn_chunk;
 
 size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk_tokens, int32_t n_q_heads,

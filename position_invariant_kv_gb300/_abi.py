@@ -37,7 +37,7 @@ KVRP_ATTN_MAX_CHUNKS = 256
 class kvrp_attn_chunk(C.Structure):
     _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("n_tokens", C.c_int32), ("rank", C.c_int32),
                 ("delta", C.c_int64), ("uk", C.c_void_p), ("vk", C.c_void_p), ("uv", C.c_void_p),
-                ("vv", C.c_void_p)]
+                ("vv", C.c_void_p), ("block_table", C.c_void_p), ("num_pages", C.c_int32)]
 
 
 class kvrp_dst(C.Structure):
@@ -335,10 +335,13 @@ class AttnChunk:
     vk: object = None
     uv: object = None
     vv: object = None
+    block_table: object = None   # int32 device tensor: page of each 16 tokens (None: contiguous rows)
+    num_pages: int = 0
 
     def c(self) -> kvrp_attn_chunk:
         return kvrp_attn_chunk(_ptr(self.k), _ptr(self.v), int(self.n_tokens), int(self.rank), int(self.delta),
-                               _ptr(self.uk), _ptr(self.vk), _ptr(self.uv), _ptr(self.vv))
+                               _ptr(self.uk), _ptr(self.vk), _ptr(self.uv), _ptr(self.vv),
+                               _ptr(self.block_table), int(self.num_pages))
 
 
 def kv_attend_relocated_workspace_size(chunk_tokens, n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:

@@ -23,8 +23,9 @@
 //                  every SM streams the same number of bytes.  A producer warp
 //                  fills a ring of shared-memory stages with bulk copies (the
 //                  TMA engine; one copy per token row of the head group's K and
-//                  V, one per factor block of U_k and U_v, which the group's
-//                  heads share); four consumer warps, one (KV head, 16-token
+//                  V -- contiguous rows, or rows of a paged pool through the
+//                  chunk's block table -- and one per factor block of U_k and
+//                  U_v, which the group's heads share); four consumer warps, one (KV head, 16-token
 //                  slice) each, compute S = K Q^T + U_k W^T with the tokens as
 //                  the MMA's rows, an online softmax in registers, and
 //                  O^T += [V | U_v]^T P^T with P^T transposed in registers
@@ -67,7 +68,9 @@ constexpr int kSmemPerSm = 228 * 1024;              // shared memory of one SM, 
 
 struct ChunkRec {
   const uint16_t *k, *v, *uk, *vk, *uv, *vv;
+  const int32_t* table;               // page of each 16 tokens, or null (contiguous rows)
   int32_t n_tokens, rank, seq, st0;   // st0: this chunk's first stage within a head group
+  int32_t num_pages;
 };
 
 struct Params {
@@ -295,11 +298,19 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
       if (lane == 0) mbar_expect_tx(full(s), (uint32_t)n * 2 * row_bytes + 2 * ub);
       __syncwarp();
       const uint32_t st = ring + (uint32_t)s * p.stage_bytes;
-      const uint16_t* kp = c.k + (int64_t)t0 * row + (int64_t)r.hg * p.hg * D;
-      const uint16_t* vp = c.v + (kp - c.k);
+      const int64_t col = (int64_t)r.hg * p.hg * D;
       for (int t = lane; t < n; t += 32) {
-        bulk_load(st + (uint32_t)t * p.k_pitch * 2, kp + t * row, row_bytes, full(s));
-        bulk_load(st + p.kv_bytes + (uint32_t)t * p.k_pitch * 2, vp + t * row, row_bytes, full(s));
+        int64_t tok = t0 + t;   // the row of this token: contiguous, or page table[tok / 16], slot tok % 16
+        if (c.table) {
+          int pg = __ldg(c.table + (tok >> 4));
+          if (pg < 0 || pg >= c.num_pages) {
+            if (p.status) atomicOr(p.status, KVRP_DEV_BAD_PAGE);
+            pg = 0;
+          }
+          tok = (int64_t)pg * 16 + (tok & 15);
+        }
+        bulk_load(st + (uint32_t)t * p.k_pitch * 2, c.k + tok * row + col, row_bytes, full(s));
+        bulk_load(st + p.kv_bytes + (uint32_t)t * p.k_pitch * 2, c.v + tok * row + col, row_bytes, full(s));
       }
       if (lane == 0 && ub > 0) {
         bulk_load(st + 2 * p.kv_bytes, c.uk + (int64_t)t0 * c.rank, ub, full(s));
@@ -764,6 +775,10 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
     if ((c.k && !aligned16(c.k)) || (c.v && !aligned16(c.v)) || (c.uk && !aligned16(c.uk)) || (c.uv && !aligned16(c.uv)) ||
         (c.vk && !aligned16(c.vk)) || (c.vv && !aligned16(c.vv)))
       return fail(KVRP_ERR_ALIGNMENT, "kv_attend_relocated: chunk %d: pointers must be 16-byte aligned", i);
+    if (c.block_table && c.num_pages <= 0)
+      return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: chunk %d: a block table needs num_pages > 0", i);
+    if (c.block_table && reinterpret_cast<uintptr_t>(c.block_table) % 4)
+      return fail(KVRP_ERR_ALIGNMENT, "kv_attend_relocated: chunk %d: block table not 4-byte aligned", i);
     tok[i] = c.n_tokens;
     m_max = std::max(m_max, (int)c.rank);
     all_tokens += c.n_tokens;
@@ -817,6 +832,8 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
       r.vk = static_cast<const uint16_t*>(c.vk);
       r.uv = static_cast<const uint16_t*>(c.uv);
       r.vv = static_cast<const uint16_t*>(c.vv);
+      r.table = c.block_table;
+      r.num_pages = c.block_table ? c.num_pages : 0;
       r.n_tokens = c.n_tokens;
       r.rank = c.rank;
       r.seq = s;

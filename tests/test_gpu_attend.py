@@ -54,18 +54,41 @@ def make_case(seed, seqs, Hq, Hkv, d):
     return q, chunks, seq_chunks
 
 
-def run_gpu(q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
+def paged_pool(rows, seed):
+    """rows [T][D] bf16 bits placed in a pool of 16-token pages: the chunk's pages
+    shuffled among 3 more pages than it needs, the unused ones NaN.  Returns the
+    pool [pages][16][D], the block table and the page count."""
+    T, D = rows.shape
+    need = (T + 15) // 16
+    n_pages = need + 3
+    table = np.random.default_rng(seed).permutation(n_pages)[:need].astype(np.int32)
+    pool = np.full((n_pages, 16, D), 0x7FC0, dtype=np.uint16)
+    for t in range(T):
+        pool[table[t // 16], t % 16] = rows[t]
+    return pool, table, n_pages
+
+
+def run_gpu(q, chunks, seq_chunks, Hq, Hkv, d, theta, scale, paged=False, status_ok=True):
     import position_invariant_kv_gb300 as kvrp
     keep = []
     ac = []
-    for c in chunks:
+    for i, c in enumerate(chunks):
         T = c["k"].shape[0]
-        k = _dev(c["k"]) if T else torch.empty((16,), dtype=torch.bfloat16, device="cuda")
-        v = _dev(c["v"]) if T else torch.empty((16,), dtype=torch.bfloat16, device="cuda")
         f = [(_dev(c[n]) if c["rank"] else None) for n in ("uk", "vk", "uv", "vv")]
+        if paged and T:
+            pk, table, n_pages = paged_pool(c["k"], 100 + i)
+            pv, _, _ = paged_pool(c["v"], 100 + i)
+            k, v = _dev(pk), _dev(pv)
+            tab = torch.from_numpy(c.get("table_override", table)).cuda()
+            keep += [tab]
+            extra = dict(block_table=tab, num_pages=n_pages)
+        else:
+            k = _dev(c["k"]) if T else torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+            v = _dev(c["v"]) if T else torch.empty((16,), dtype=torch.bfloat16, device="cuda")
+            extra = {}
         keep += [k, v] + f
         ac.append(kvrp.AttnChunk(k=k, v=v, n_tokens=T, delta=c["delta"], rank=c["rank"], uk=f[0], vk=f[1], uv=f[2],
-                                 vv=f[3]))
+                                 vv=f[3], **extra))
     out = torch.empty((len(seq_chunks) - 1, Hq, d), dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(kvrp.kv_attend_relocated_workspace_size([c["k"].shape[0] for c in chunks], Hq, Hkv, d),
                      dtype=torch.uint8, device="cuda")
@@ -73,8 +96,10 @@ def run_gpu(q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
     kvrp.kv_attend_relocated(_dev(q), ac, seq_chunks, n_q_heads=Hq, n_kv_heads=Hkv, head_dim=d, rope_theta=theta,
                              softmax_scale=scale, out=out, workspace=ws, d_status=status)
     torch.cuda.synchronize()
-    assert int(status.item()) == 0
-    return _bits(out)
+    if status_ok:
+        assert int(status.item()) == 0
+        return _bits(out)
+    return _bits(out), int(status.item())
 
 
 def check(got, q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
@@ -111,6 +136,25 @@ def test_attention_matches_oracle(seqs, Hq, Hkv, d):
     got = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale)
     worst = check(got, q, chunks, sc, Hq, Hkv, d, theta, scale)
     print("worst ulp distance", worst)
+    # the same chunks read from paged pools (shuffled pages, unused pages NaN): the same bits
+    paged = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale, paged=True)
+    assert np.array_equal(paged, got)
+
+
+def test_bad_page_is_flagged_not_faulted():
+    """A block-table entry outside the pool sets KVRP_DEV_BAD_PAGE; the kernel reads
+    page 0 instead of faulting, and the other sequence is untouched."""
+    import position_invariant_kv_gb300 as kvrp
+    Hq, Hkv, d, theta, scale = 8, 4, 128, 1e6, 0.088
+    q, chunks, sc = make_case(93, [[(100, 16)], [(64, 0)]], Hq, Hkv, d)
+    good = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale, paged=True)
+    _, table, n_pages = paged_pool(chunks[0]["k"], 100)
+    bad = table.copy()
+    bad[3] = n_pages + 5
+    chunks[0]["table_override"] = bad
+    got, status = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale, paged=True, status_ok=False)
+    assert status & kvrp.KVRP_DEV_BAD_PAGE
+    assert np.array_equal(got[1], good[1])
 
 
 def test_empty_sequences_and_chunks():
@@ -141,8 +185,9 @@ def test_shift_moves_only_through_the_rotation():
 
 def test_bench_workload_on_sampled_sequences():
     """The bench's own workload and launch (16 sequences x 4 chunks x 4096 tokens,
-    28 query / 4 KV heads x 128, rank-32 K and V patches): sequences 0, 7 and 15
-    against the oracle, every output element of each."""
+    28 query / 4 KV heads x 128, rank-32 K and V patches, canonical K and V in a
+    shuffled paged pool): sequences 0, 7 and 15 against the oracle, every output
+    element of each (the oracle gets each chunk's rows gathered through its table)."""
     import bench
     import position_invariant_kv_gb300 as kvrp
     a = dict(bench.ATTN_SHAPE)
@@ -158,8 +203,15 @@ def test_bench_workload_on_sampled_sequences():
     assert int(status.item()) == 0
     got = _bits(out)
     qb = _bits(q)
+    pool_k, pool_v = _bits(chunks[0].k), _bits(chunks[0].v)   # the shared paged pools [pages][16][D]
+
+    def rows(pool, c):   # the chunk's rows, gathered through its block table
+        table = c.block_table.cpu().numpy()
+        t = np.arange(c.n_tokens)
+        return pool[table[t // 16], t % 16]
+
     for s in (0, 7, 15):
-        host = [{"k": _bits(c.k), "v": _bits(c.v), "delta": c.delta, "rank": c.rank, "uk": _bits(c.uk),
+        host = [{"k": rows(pool_k, c), "v": rows(pool_v, c), "delta": c.delta, "rank": c.rank, "uk": _bits(c.uk),
                  "vk": _bits(c.vk), "uv": _bits(c.uv), "vv": _bits(c.vv)} for c in chunks[sc[s]:sc[s + 1]]]
         sub_sc = [0, len(host)]
         worst = check(got[s:s + 1], qb[s:s + 1], host, sub_sc, a["Hq"], a["Hkv"], a["d"], a["theta"], scale)
