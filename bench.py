@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "relocated+patched KV tokens/s and HBM GB/s (fraction of GB300 roofline), 1 GPU"
 KERNEL_SOURCES = ["position_invariant_kv_gb300/csrc/kvrp_kernel.cu", "position_invariant_kv_gb300/csrc/kvrp_plan.h",
-                  "position_invariant_kv_gb300/csrc/kvrp_host.cpp"]
+                  "position_invariant_kv_gb300/csrc/kvrp_host.cpp", "position_invariant_kv_gb300/csrc/kvrp_ptx.h"]
 L2_BYTES = 129 * 2 ** 20
 
 

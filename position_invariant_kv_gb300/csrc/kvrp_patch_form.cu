@@ -43,6 +43,7 @@
 
 #include "kvrp.h"
 #include "kvrp_plan.h"
+#include "kvrp_ptx.h"
 
 namespace kvrp {
 namespace pf {
@@ -58,7 +59,7 @@ constexpr int kPassThreads = 192;  // producer warp, MMA warp, four epilogue war
 constexpr int kDeltaTokens = 64;   // tokens per delta_kernel tile
 constexpr float kShiftFirst = 1e-5f;    // Cholesky QR shift / trace: a basis of unknown conditioning
 constexpr float kShiftSecond = 1e-7f;   // a basis already close to orthonormal
-constexpr long long kTimeoutCycles = 1ll << 31;   // bounded waits: ~1 s
+using namespace kvrp::ptx;   // mbarrier, TMA, tcgen05 wrappers; kTimeoutCycles bounds every wait
 
 struct TableParam {
   float4 v[kTablePairs];
@@ -259,65 +260,6 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__
   }
 }
 
-// ---------------------------------------------------------------------------
-// PTX wrappers (mbarrier, TMA, tcgen05)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of `bar` with the given parity: gives up when
-// another role has flagged an abort or after ~1 s (then flags one itself).
-__device__ __noinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
-      *abort_flag = 1;
-      if (status) atomicOr(status, KVRP_DEV_TIMEOUT);
-      return false;
-    }
-  }
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* map, uint32_t bar, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
 // 16 consecutive fp32 TMEM columns of this warp's 32 lanes, completed in the same statement
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
