@@ -183,3 +183,51 @@ def test_patch_form_orbit_argument_checks(kvrp):
         kvrp.kv_patch_form_orbit([0x20000], [1, 2], 0x30000, n_layers=1, n_tokens=100, row_width=256,
                                  rope_kind=0, rot_dim=0, rope_theta=1e4, rank=16, oversample=8, power_iters=1,
                                  omega=0x50000, u_out=0x60000, v_out=0x70000, workspace=0x100000)
+
+
+def test_attend_argument_checks(kvrp):
+    """kv_attend_relocated validates everything on the host, before any CUDA call."""
+    def chunk(**over):
+        c = dict(k=0x20000, v=0x30000, n_tokens=100, delta=5, rank=16, uk=0x40000, vk=0x50000, uv=0x60000,
+                 vv=0x70000)
+        c.update(over)
+        return kvrp.AttnChunk(**c)
+
+    def status(chunks=None, seq_chunks=None, q=0x80000, **over):
+        args = dict(n_q_heads=8, n_kv_heads=2, head_dim=128, rope_theta=1e6, softmax_scale=0.088, out=0x90000,
+                    workspace=0x100000, workspace_bytes=1 << 40, stream=0)
+        args.update(over)
+        chunks = [chunk()] if chunks is None else chunks
+        seq_chunks = [0, len(chunks)] if seq_chunks is None else seq_chunks
+        with pytest.raises(kvrp.KvrpError) as e:
+            kvrp.kv_attend_relocated(q, chunks, seq_chunks, **args)
+        return e.value.status
+
+    assert status(q=0) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(q=0x80004) == kvrp.KVRP_ERR_ALIGNMENT
+    assert status(head_dim=96) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert status(n_q_heads=7) == kvrp.KVRP_ERR_UNSUPPORTED                  # not a multiple of n_kv_heads
+    assert status(n_q_heads=64) == kvrp.KVRP_ERR_UNSUPPORTED                 # 32 query heads per KV head
+    assert status(rope_theta=0.0) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(softmax_scale=-1.0) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(chunks=[chunk(rank=24)]) == kvrp.KVRP_ERR_UNSUPPORTED      # rank not a multiple of 16
+    assert status(chunks=[chunk(rank=144)]) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert status(chunks=[chunk(uk=None)]) == kvrp.KVRP_ERR_INVALID_ARG      # rank > 0 needs all four factors
+    assert status(chunks=[chunk(n_tokens=-1)]) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(chunks=[chunk(k=None)]) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(chunks=[chunk(k=0x20008)]) == kvrp.KVRP_ERR_ALIGNMENT
+    assert status(chunks=[chunk(vv=0x70004)]) == kvrp.KVRP_ERR_ALIGNMENT
+    assert status(chunks=[chunk(block_table=0x1000, num_pages=0)]) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(chunks=[chunk(block_table=0x1002, num_pages=4)]) == kvrp.KVRP_ERR_ALIGNMENT
+    assert status(seq_chunks=[0, 0]) == kvrp.KVRP_ERR_INVALID_ARG            # must end at n_chunks
+    assert status(chunks=[chunk(), chunk()], seq_chunks=[0, 2, 1, 2]) == kvrp.KVRP_ERR_INVALID_ARG
+    assert status(chunks=[chunk()] * 257, seq_chunks=[0, 257]) == kvrp.KVRP_ERR_UNSUPPORTED
+    assert status(workspace_bytes=16) == kvrp.KVRP_ERR_WORKSPACE
+    need = kvrp.kv_attend_relocated_workspace_size([100], 8, 2, 128)
+    assert need > 0
+    assert kvrp.kv_attend_relocated_workspace_size([], 8, 2, 128) == 0
+    assert kvrp.kv_attend_relocated_workspace_size([100], 8, 3, 128) == 0     # heads not a multiple
+    import torch
+    if not torch.cuda.is_available():                                         # well-formed: no GPU, no fallback
+        assert status(workspace_bytes=need) == kvrp.KVRP_ERR_CUDA
+        assert status(workspace_bytes=need, chunks=[chunk(block_table=0x1000, num_pages=7)]) == kvrp.KVRP_ERR_CUDA
