@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
 // taken in groups of kCombineThreads: thread t locates entry t of a group
 // (arithmetic only) and loads its max and sum; the weighted features are then
 // summed with thread -> feature (d = 128) or feature and entry parity (d = 64),
-// eight entries' loads in flight.
+// up to 32 entries' loads in flight.
 constexpr int kCombineThreads = 128;
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ Params p) {
@@ -663,16 +663,16 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     wts[tid] = wt;
     __syncthreads();
     const int nx = min(kCombineThreads, n_list - L0);
-    for (int x = grp; x < nx; x += 8 * G) {
-      float v[8], w[8];
+    for (int x = grp; x < nx; x += 32 * G) {
+      float v[32], w[32];
 #pragma unroll
-      for (int y = 0; y < 8; ++y) {
+      for (int y = 0; y < 32; ++y) {
         const int xy = x + y * G;
         w[y] = xy < nx ? wts[xy] : 0.f;
         v[y] = xy < nx ? ent[xy][f] : 0.f;
       }
 #pragma unroll
-      for (int y = 0; y < 8; ++y) acc = fmaf(w[y], v[y], acc);
+      for (int y = 0; y < 32; ++y) acc = fmaf(w[y], v[y], acc);
     }
   }
   den = block_reduce(den, false);
