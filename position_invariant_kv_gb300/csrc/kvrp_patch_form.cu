@@ -415,13 +415,16 @@ __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_cons
 // ---------------------------------------------------------------------------
 // 3. Skinny fp32 products on the CUDA cores (the k x k side of the method).
 //    gram_kernel:  G[l] += X[l]^T X[l] over a slice of rows, X [R][KP] fp32;
-//                  threads form a 16 x 16 grid over G, rows stream through
-//                  shared memory in double-buffered chunks of 64 (cp.async);
+//                  row slices sized for ~4 CTAs per SM stream through shared
+//                  memory in double-buffered stages (cp.async); each value is
+//                  split once into a tf32 high part and remainder, and the
+//                  product runs on the tensor cores as three tf32 MMAs per tile;
 //                  slices add into a zeroed G.
 //    apply_kernel: out[l][r] = X[l][r] M[l] (M KP x KP), one thread per row,
 //                  M read from shared memory as broadcast float4 rows; with
-//                  `upper` M is upper triangular and its zero half is skipped.
-//                  Output fp32 rows [R][KP], or bf16 transposed rows [KP][ldt].
+//                  `solve`, M is chol_kernel's R and out = X R^-1 by
+//                  substitution.  Output fp32 rows [R][KP], or bf16 transposed
+//                  rows [KP][ldt].
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -432,60 +435,99 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
 
-constexpr int kGramRows = 512;    // rows per CTA
-constexpr int kGramChunk = 64;    // rows per shared-memory stage
 
+// fp32 -> tf32 (round to nearest, ties away), the value kept in a 32-bit register.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// D += A B, m16n8k8, tf32 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// G = X^T X on the tensor cores: each fp32 value splits into a tf32 high part and
+// a tf32 remainder, and G takes hi.hi + hi.lo + lo.hi (the lo.lo term is below
+// fp32 rounding of the sum).  Warp w owns output tiles (16 x 8) w, w + 8, ...,
+// and runs every staged row through them.
 template <int KP>
-__global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t sX, float* G, int64_t sG, int R) {
-  constexpr int S = KP / 16;
-  __shared__ __align__(16) float xs[2][kGramChunk][KP];
+__global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t sX, float* G, int64_t sG, int R,
+                                                        int rows_per_cta) {
+  constexpr int MT = KP / 16, NT = KP / 8, TILES = MT * NT, TPW = (TILES + 7) / 8;   // tiles per warp
+  constexpr int XP = KP + 8;   // staged row pitch: fragment reads fall in distinct banks
+  constexpr int CH = KP <= 48 ? 32 : 16;   // rows per stage (static shared memory < 48 KB)
+  __shared__ __align__(16) float xs[2][CH][XP];         // fp32 rows, by cp.async
+  __shared__ __align__(16) uint32_t xh[CH][XP], xl[CH][XP];   // their tf32 high parts and remainders
   const int l = blockIdx.y;
   const float* x = X + (int64_t)l * sX;
-  const int r0 = blockIdx.x * kGramRows;
-  const int r1 = min(R, r0 + kGramRows);
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int r0 = blockIdx.x * rows_per_cta;
+  const int r1 = min(R, r0 + rows_per_cta);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   auto load = [&](int buf, int c0) {
-    for (int ch = tid; ch < kGramChunk * KP / 4; ch += kThreads) {
+    for (int ch = tid; ch < CH * KP / 4; ch += kThreads) {
       const int r = ch / (KP / 4), c4 = (ch - r * (KP / 4)) * 4;
       const bool ok = c0 + r < r1;
       cp_async16(&xs[buf][r][c4], ok ? x + (int64_t)(c0 + r) * KP + c4 : x, ok);
     }
     cp_async_commit();
   };
-  float acc[S][S] = {};
-  const int n_chunks = (r1 - r0 + kGramChunk - 1) / kGramChunk;
+  float acc[TPW][4] = {};
+  const int n_chunks = (r1 - r0 + CH - 1) / CH;
   if (n_chunks > 0) load(0, r0);
   for (int c = 0; c < n_chunks; ++c) {
     if (c + 1 < n_chunks) {
-      load((c + 1) & 1, r0 + (c + 1) * kGramChunk);
+      load((c + 1) & 1, r0 + (c + 1) * CH);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
-    const float(*xb)[KP] = xs[c & 1];
-#pragma unroll 4
-    for (int r = 0; r < kGramChunk; ++r) {
-      float a[S], b[S];
-#pragma unroll
-      for (int i = 0; i < S; ++i) { a[i] = xb[r][ty + 16 * i]; b[i] = xb[r][tx + 16 * i]; }
-#pragma unroll
-      for (int i = 0; i < S; ++i)
-#pragma unroll
-        for (int j = 0; j < S; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    // split every staged value once (rows past r1 are zero)
+    for (int e = tid; e < CH * KP; e += kThreads) {
+      const int r = e / KP, k = e - r * KP;
+      const float v = xs[c & 1][r][k];
+      const uint32_t h = to_tf32(v);
+      xh[r][k] = h;
+      xl[r][k] = to_tf32(v - __uint_as_float(h));
     }
     __syncthreads();
+#pragma unroll
+    for (int k0 = 0; k0 < CH; k0 += 8) {
+#pragma unroll
+      for (int i = 0; i < TPW; ++i) {
+        const int t = warp + 8 * i;
+        if (t >= TILES) break;
+        const int m0 = (t / NT) * 16, n0 = (t % NT) * 8;
+        // A = X^T (rows m, columns k), B = X (rows k, columns n)
+        const uint32_t ah[4] = {xh[k0 + tig][m0 + gid], xh[k0 + tig][m0 + gid + 8], xh[k0 + tig + 4][m0 + gid],
+                                xh[k0 + tig + 4][m0 + gid + 8]};
+        const uint32_t al[4] = {xl[k0 + tig][m0 + gid], xl[k0 + tig][m0 + gid + 8], xl[k0 + tig + 4][m0 + gid],
+                                xl[k0 + tig + 4][m0 + gid + 8]};
+        mma_tf32(acc[i], al, xh[k0 + tig][n0 + gid], xh[k0 + tig + 4][n0 + gid]);
+        mma_tf32(acc[i], ah, xl[k0 + tig][n0 + gid], xl[k0 + tig + 4][n0 + gid]);
+        mma_tf32(acc[i], ah, xh[k0 + tig][n0 + gid], xh[k0 + tig + 4][n0 + gid]);
+      }
+    }
+    __syncthreads();   // the split arrays and this stage buffer are reused
   }
   float* g = G + (int64_t)l * sG;
 #pragma unroll
-  for (int i = 0; i < S; ++i)
+  for (int i = 0; i < TPW; ++i) {
+    const int t = warp + 8 * i;
+    if (t >= TILES) break;
+    const int m0 = (t / NT) * 16, n0 = (t % NT) * 8;
 #pragma unroll
-    for (int j = 0; j < S; ++j) atomicAdd(&g[(ty + 16 * i) * KP + tx + 16 * j], acc[i][j]);
+    for (int e = 0; e < 4; ++e) atomicAdd(&g[(m0 + gid + (e >> 1) * 8) * KP + n0 + 2 * tig + (e & 1)], acc[i][e]);
+  }
 }
 
 template <int KP>
 __global__ void __launch_bounds__(128) apply_kernel(const float* X, int64_t sX, const float* M, int64_t sM, float* out,
-                                                    int64_t sO, uint16_t* out_t, int64_t sT, int ldt, int R, int upper) {
+                                                    int64_t sO, uint16_t* out_t, int64_t sT, int ldt, int R, int solve) {
   __shared__ __align__(16) float ms[KP][KP];
   const int l = blockIdx.y;
   const float* m = M + (int64_t)l * sM;
@@ -501,18 +543,28 @@ __global__ void __launch_bounds__(128) apply_kernel(const float* X, int64_t sX, 
     const float4 v = *reinterpret_cast<const float4*>(x + i);
     xv[i] = v.x; xv[i + 1] = v.y; xv[i + 2] = v.z; xv[i + 3] = v.w;
   }
+  if (solve) {
+    // o R = x with R from chol_kernel (diagonal held as 1 / R_jj): o_j = x_j / R_jj, then
+    // x_l -= o_j R_jl for l > j (right-looking substitution: short dependency chains)
 #pragma unroll
-  for (int j = 0; j < KP; ++j) o[j] = 0.f;
+    for (int j = 0; j < KP; ++j) {
+      o[j] = xv[j] * ms[j][j];
 #pragma unroll
-  for (int i = 0; i < KP; ++i) {
+      for (int l = j + 1; l < KP; ++l) xv[l] = fmaf(-o[j], ms[j][l], xv[l]);
+    }
+  } else {
 #pragma unroll
-    for (int j4 = 0; j4 < KP; j4 += 4) {
-      if (upper && j4 + 3 < i) continue;   // an upper-triangular M has zeros left of its diagonal
-      const float4 mv = *reinterpret_cast<const float4*>(&ms[i][j4]);
-      o[j4] = fmaf(xv[i], mv.x, o[j4]);
-      o[j4 + 1] = fmaf(xv[i], mv.y, o[j4 + 1]);
-      o[j4 + 2] = fmaf(xv[i], mv.z, o[j4 + 2]);
-      o[j4 + 3] = fmaf(xv[i], mv.w, o[j4 + 3]);
+    for (int j = 0; j < KP; ++j) o[j] = 0.f;
+#pragma unroll
+    for (int i = 0; i < KP; ++i) {
+#pragma unroll
+      for (int j4 = 0; j4 < KP; j4 += 4) {
+        const float4 mv = *reinterpret_cast<const float4*>(&ms[i][j4]);
+        o[j4] = fmaf(xv[i], mv.x, o[j4]);
+        o[j4 + 1] = fmaf(xv[i], mv.y, o[j4 + 1]);
+        o[j4 + 2] = fmaf(xv[i], mv.z, o[j4 + 2]);
+        o[j4 + 3] = fmaf(xv[i], mv.w, o[j4 + 3]);
+      }
     }
   }
   if (out_t) {
@@ -541,19 +593,17 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
 }
 
 // ---------------------------------------------------------------------------
-// 4. Shifted Cholesky of a Gram matrix and the inverse of its factor, fp32,
-//    one CTA per layer:  R^T R = G + s I (s = rel * trace G), out = R^-1,
-//    zero outside the leading k x k block.
-//    Factorisation: right-looking, one barrier per column j; threads form a
-//    16 x 16 grid over the trailing block and load everything they need for
-//    the step before they store (no load waits behind a store).  Row j of R
-//    goes to Rt (transposed), which nothing reads during the factorisation.
-//    Inverse: row i of X = R^-1 solves x R = e_i by forward substitution,
-//    x_j = (delta_ij - sum_{l<j} x_l R_lj) / R_jj, one thread per row; all
-//    threads walk j together, so R_lj = Rt[j][l] is a broadcast read.
+// 4. Shifted Cholesky of a Gram matrix, fp32, one CTA per layer:
+//    R^T R = G + s I (s = rel * trace G); out = R with its diagonal stored as
+//    1 / R_jj, zero outside the leading k x k block (apply_kernel's solve mode
+//    then forms X R^-1 by substitution, so R is never inverted).
+//    Right-looking, one barrier per column j; threads form a 16 x 16 grid over
+//    the trailing block and load everything they need for the step before they
+//    store (no load waits behind a store).  Row j of R goes to Rt (transposed),
+//    which nothing reads during the factorisation.
 // ---------------------------------------------------------------------------
 template <int KP>
-__global__ void __launch_bounds__(kThreads) chol_inverse_kernel(const float* G, int64_t sG, float* Rinv, int64_t sR,
+__global__ void __launch_bounds__(kThreads) chol_kernel(const float* G, int64_t sG, float* Rf, int64_t sR,
                                                                  int k, float rel) {
   constexpr int kp = KP;
   constexpr int kCholSpan = KP / 16;    // rows (and columns) of the trailing block per thread
@@ -561,11 +611,10 @@ __global__ void __launch_bounds__(kThreads) chol_inverse_kernel(const float* G, 
   constexpr int P = kp + 1;
   float* A = smc;              // trailing matrix
   float* Rt = smc + kp * P;    // R transposed: Rt[c][j] = R[j][c]
-  float* X = smc + 2 * kp * P; // R^-1, one row per thread
   __shared__ float scratch[kThreads / 32];
   __shared__ float rdiag[kMaxK];
   const float* g = G + (int64_t)blockIdx.x * sG;
-  float* out = Rinv + (int64_t)blockIdx.x * sR;
+  float* out = Rf + (int64_t)blockIdx.x * sR;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   float tr = 0.f;
   for (int i = ty; i < kp; i += 16)
@@ -611,24 +660,11 @@ __global__ void __launch_bounds__(kThreads) chol_inverse_kernel(const float* G, 
       }
     __syncthreads();
   }
-  if (tid < kp) {
-    const int i = tid;
-    float* xi = X + i * P;
-    for (int j = 0; j < kp; ++j) {
-      float s4[4] = {(i == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};
-      const float* rj = Rt + j * P;
-      int l = 0;
-      for (; l + 3 < j; l += 4) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u) s4[u] = fmaf(-xi[l + u], rj[l + u], s4[u]);
-      }
-      for (; l < j; ++l) s4[0] = fmaf(-xi[l], rj[l], s4[0]);
-      xi[j] = (i < k && j < k && j >= i) ? ((s4[0] + s4[1]) + (s4[2] + s4[3])) * rdiag[j] : 0.f;
-    }
-  }
   __syncthreads();
+  // R row by row, its diagonal stored as 1 / R_jj (zero outside the leading k x k block)
   for (int i = ty; i < kp; i += 16)
-    for (int j = tx; j < kp; j += 16) out[i * kp + j] = X[i * P + j];
+    for (int j = tx; j < kp; j += 16)
+      out[i * kp + j] = (i < k && j < k && j >= i) ? (i == j ? rdiag[i] : Rt[j * P + i]) : 0.f;
 }
 
 // ---------------------------------------------------------------------------
@@ -813,7 +849,7 @@ int pad16(int k) { return (k + 15) / 16 * 16; }
 
 struct Buffers {
   uint16_t *delta, *delta_t, *st_t, *st_d, *omega_t;   // bf16
-  float *y, *y2, *z, *z2, *g, *rinv, *w;               // fp32
+  float *y, *y2, *z, *z2, *g, *rfac, *w;               // fp32
   int64_t Dp, Tp, s_delta, s_delta_t, s_st_t, s_st_d, s_tk, s_dk, s_kk;
   size_t bytes;
 };
@@ -845,7 +881,7 @@ Buffers layout(uint8_t* base, int L, int T, int D, int kp) {
   b.z = reinterpret_cast<float*>(take(4 * (size_t)b.s_dk * L));
   b.z2 = reinterpret_cast<float*>(take(4 * (size_t)b.s_dk * L));
   b.g = reinterpret_cast<float*>(take(4 * (size_t)b.s_kk * L));
-  b.rinv = reinterpret_cast<float*>(take(4 * (size_t)b.s_kk * L));
+  b.rfac = reinterpret_cast<float*>(take(4 * (size_t)b.s_kk * L));
   b.w = reinterpret_cast<float*>(take(4 * (size_t)b.s_kk * L));
   b.bytes = off;
   return b;
@@ -963,26 +999,29 @@ class Runner {
     const int64_t skk = (int64_t)kp_ * kp_;
     err = cudaMemsetAsync(G, 0, sizeof(float) * (size_t)(skk * L_), st_);
     if (err != cudaSuccess) return;
-    const dim3 grid((R + kGramRows - 1) / kGramRows, L_);
+    // row slices sized for about four CTAs per SM over all layers (64-row multiples, 64..512)
+    const int64_t want = ((int64_t)R * L_ + 4 * sms_ - 1) / (4 * sms_);
+    const int rows = (int)std::min<int64_t>(512, std::max<int64_t>(64, (want + 63) / 64 * 64));
+    const dim3 grid((R + rows - 1) / rows, L_);
     switch (kp_) {
-      case 16: gram_kernel<16><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
-      case 32: gram_kernel<32><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
-      case 48: gram_kernel<48><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
-      case 64: gram_kernel<64><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
-      case 80: gram_kernel<80><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
-      case 96: gram_kernel<96><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R); break;
+      case 16: gram_kernel<16><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
+      case 32: gram_kernel<32><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
+      case 48: gram_kernel<48><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
+      case 64: gram_kernel<64><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
+      case 80: gram_kernel<80><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
+      case 96: gram_kernel<96><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
       default: err = cudaErrorInvalidValue; return;
     }
     err = cudaGetLastError();
   }
 
   // out[L][R][kp] = X[L][R][kp] M[L][kp][kp] (fp32 rows), or bf16 transposed rows into out_t
-  void apply(const float* X, int64_t sX, const float* M, float* out, int64_t sO, int R, bool upper,
+  void apply(const float* X, int64_t sX, const float* M, float* out, int64_t sO, int R, bool solve,
              uint16_t* out_t = nullptr, int64_t sT = 0, int ldt = 0) {
     if (err != cudaSuccess) return;
     const int64_t skk = (int64_t)kp_ * kp_;
     const dim3 grid((R + 127) / 128, L_);
-    const int up = upper ? 1 : 0;
+    const int up = solve ? 1 : 0;
     switch (kp_) {
       case 16: apply_kernel<16><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
       case 32: apply_kernel<32><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
@@ -998,32 +1037,32 @@ class Runner {
   // X [L][R][kp] <- orth(X) by rounds of shifted Cholesky QR (the first with
   // shift `first`, later ones kShiftSecond); tmp has X's shape.  With out_t
   // set, the last round writes bf16 X^T [kp][ldt] there instead of X.
-  void orth(float*& X, float*& tmp, int64_t sX, int R, int k, int rounds, float first, float* g, float* rinv,
+  void orth(float*& X, float*& tmp, int64_t sX, int R, int k, int rounds, float first, float* g, float* rfac,
             uint16_t* out_t = nullptr, int64_t sT = 0, int ldt = 0) {
     for (int r = 0; r < rounds && err == cudaSuccess; ++r) {
       gram(X, sX, g, R);                                                      // G = X^T X
-      chol(g, rinv, k, r == 0 ? first : kShiftSecond);
+      chol(g, rfac, k, r == 0 ? first : kShiftSecond);                        // G + sI = R^T R
       if (r == rounds - 1 && out_t) {
-        apply(X, sX, rinv, nullptr, 0, R, true, out_t, sT, ldt);              // (X R^-1)^T in bf16
+        apply(X, sX, rfac, nullptr, 0, R, true, out_t, sT, ldt);              // (X R^-1)^T in bf16
       } else {
-        apply(X, sX, rinv, tmp, sX, R, true);                                 // X R^-1
+        apply(X, sX, rfac, tmp, sX, R, true);                                 // X R^-1
         std::swap(X, tmp);
       }
     }
   }
 
-  size_t chol_smem() const { return sizeof(float) * 3 * (size_t)kp_ * (kp_ + 1); }
+  size_t chol_smem() const { return sizeof(float) * 2 * (size_t)kp_ * (kp_ + 1); }
 
-  void chol(const float* g, float* rinv, int k, float rel) {
+  void chol(const float* g, float* rfac, int k, float rel) {
     if (err != cudaSuccess) return;
     const int64_t skk = (int64_t)kp_ * kp_;
     switch (kp_) {
-      case 16: chol_inverse_kernel<16><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
-      case 32: chol_inverse_kernel<32><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
-      case 48: chol_inverse_kernel<48><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
-      case 64: chol_inverse_kernel<64><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
-      case 80: chol_inverse_kernel<80><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
-      case 96: chol_inverse_kernel<96><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rinv, skk, k, rel); break;
+      case 16: chol_kernel<16><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
+      case 32: chol_kernel<32><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
+      case 48: chol_kernel<48><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
+      case 64: chol_kernel<64><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
+      case 80: chol_kernel<80><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
+      case 96: chol_kernel<96><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
       default: err = cudaErrorInvalidValue; return;
     }
     err = cudaGetLastError();
@@ -1032,14 +1071,14 @@ class Runner {
 
   static cudaError_t configure() {
     cudaError_t e = cudaSuccess;
-    const int chol = (int)(sizeof(float) * 3 * kMaxK * (kMaxK + 1));
+    const int chol = (int)(sizeof(float) * 2 * kMaxK * (kMaxK + 1));
     const int jac = (int)(sizeof(float) * 2 * kMaxK * (kMaxK + 1));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_inverse_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, jac);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem_bytes(kMaxK));
@@ -1164,13 +1203,13 @@ kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* d
   // 2. range finder with subspace iterations (tensor-core passes over Delta and Delta^T)
   run.pass(b.delta, b.Dp, b.s_delta, b.omega_t, b.Dp, b.s_st_d, false, y, b.s_tk, T, D);           // Y = Delta Omega
   for (int it = 0; it < power_iters; ++it) {
-    run.orth(y, y2, b.s_tk, T, k, 1, pf::kShiftFirst, b.g, b.rinv, b.st_t, b.s_st_t, (int)b.Tp);     // Q^T
+    run.orth(y, y2, b.s_tk, T, k, 1, pf::kShiftFirst, b.g, b.rfac, b.st_t, b.s_st_t, (int)b.Tp);     // Q^T
     run.pass(b.delta_t, b.Tp, b.s_delta_t, b.st_t, b.Tp, b.s_st_t, true, z, b.s_dk, D, T);          // Z = Delta^T Q
-    run.orth(z, z2, b.s_dk, D, k, 1, pf::kShiftFirst, b.g, b.rinv, b.st_d, b.s_st_d, (int)b.Dp);     // Zq^T
+    run.orth(z, z2, b.s_dk, D, k, 1, pf::kShiftFirst, b.g, b.rfac, b.st_d, b.s_st_d, (int)b.Dp);     // Zq^T
     run.pass(b.delta, b.Dp, b.s_delta, b.st_d, b.Dp, b.s_st_d, true, y, b.s_tk, T, D);              // Y = Delta Zq
   }
   // 3. Q = orth(Y); B^T = Delta^T Q; C = B B^T
-  run.orth(y, y2, b.s_tk, T, k, 2, pf::kShiftFirst, b.g, b.rinv, b.st_t, b.s_st_t, (int)b.Tp);
+  run.orth(y, y2, b.s_tk, T, k, 2, pf::kShiftFirst, b.g, b.rfac, b.st_t, b.s_st_t, (int)b.Tp);
   run.pass(b.delta_t, b.Tp, b.s_delta_t, b.st_t, b.Tp, b.s_st_t, true, z, b.s_dk, D, T);
   run.gram(z, b.s_dk, b.g, D);
   // 4. eigenvectors of the m largest eigenvalues, scaled by lambda^-1/2
@@ -1180,7 +1219,7 @@ kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* d
   }
   // 5. V_m = orth(B^T W) (columns already near unit length) as bf16 V^T; U_m = Delta V_m
   run.apply(z, b.s_dk, b.w, z2, b.s_dk, D, false);
-  run.orth(z2, z, b.s_dk, D, m, 1, pf::kShiftSecond, b.g, b.rinv, b.st_d, b.s_st_d, (int)b.Dp);
+  run.orth(z2, z, b.s_dk, D, m, 1, pf::kShiftSecond, b.g, b.rfac, b.st_d, b.s_st_d, (int)b.Dp);
   run.pass(b.delta, b.Dp, b.s_delta, b.st_d, b.Dp, b.s_st_d, true, y2, b.s_tk, T, D);
   if (run.err == cudaSuccess && !run.map_fail) {
     pf::u_out_kernel<<<dim3(64, L), 256, 0, st>>>(y2, b.s_tk, kp, static_cast<uint16_t*>(u_out), u_layer_stride, T, m);
