@@ -50,7 +50,7 @@ namespace pf {
 
 constexpr int kMaxK = 96;          // rank + oversampling bound (k x k solves live in shared memory)
 constexpr int kMaxOrbit = 64;      // conditioned caches averaged by one call
-constexpr int kJacobiSweeps = 3;   // the top-m subspace has settled by then (V_m is re-orthonormalised)
+constexpr int kJacobiSweeps = 2;   // the top-m subspace has settled by then (V_m is re-orthonormalised)
 constexpr int kThreads = 256;
 constexpr int kTile = 128;         // output rows per pass_kernel CTA
 constexpr int kPassStages = 3;     // pass_kernel pipeline depth
@@ -152,50 +152,82 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__
   const bool wide = (sg.turns ? half % 8 == 0 : sg.W % 16 == 0) && a.D % 8 == 0 && sg.f0 % 8 == 0 &&
                     a.canon_stride % 8 == 0 && a.cond_stride % 8 == 0;
   if (wide) {
+    // a thread's units (at most kDeltaWide of them) load everything first, then compute
+    constexpr int kDeltaWide = 4;
     const int upt = sg.W / 16;
     const int n_units = kDeltaTokens * upt;
-    for (int u = threadIdx.x; u < n_units; u += blockDim.x) {
-      const int tl = u / upt, w = u - (u / upt) * upt;
-      const int t = t0 + tl;
-      if (t >= a.T) continue;
-      const int e0 = sg.turns ? 8 * w : 16 * w;
-      const int e1 = sg.turns ? 8 * w + half : 16 * w + 8;
-      const int64_t row = (int64_t)t * a.D + sg.f0;
-      float x0[8], x1[8], c0[8] = {}, c1[8] = {};
-      bf16x8_to_f(*reinterpret_cast<const uint4*>(canon + row + e0), x0);
-      bf16x8_to_f(*reinterpret_cast<const uint4*>(canon + row + e1), x1);
-      for (int p = 0; p < a.n_cond; ++p) {
-        const uint16_t* c = a.cond[p] + (int64_t)l * a.cond_stride + row;
-        float v0[8], v1[8];
-        bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e0), v0);
-        bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e1), v1);
+    for (int u0 = 0; u0 < n_units; u0 += kDeltaWide * kThreads) {
+      uint4 xa[kDeltaWide], xb[kDeltaWide], ca[kDeltaWide], cb[kDeltaWide];
+      int tls[kDeltaWide], e0s[kDeltaWide], e1s[kDeltaWide];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { c0[i] += v0[i]; c1[i] += v1[i]; }
-      }
-      float d0[8], d1[8];
-      if (sg.turns) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {   // pairs e0 + 2q, e0 + 2q + 1
-          const float4 hd = tb[e0 + 2 * q], tl4 = tb[e0 + 2 * q + 1];
-          const float a0 = x0[2 * q], a1 = x0[2 * q + 1], b0 = x1[2 * q], b1 = x1[2 * q + 1];
-          const float y00 = fmaf(a0, hd.x, -(b0 * hd.z)) + fmaf(a0, tl4.x, -(b0 * tl4.z));
-          const float y01 = fmaf(a1, hd.y, -(b1 * hd.w)) + fmaf(a1, tl4.y, -(b1 * tl4.w));
-          const float y10 = fmaf(b0, hd.x, a0 * hd.z) + fmaf(b0, tl4.x, a0 * tl4.z);
-          const float y11 = fmaf(b1, hd.y, a1 * hd.w) + fmaf(b1, tl4.y, a1 * tl4.w);
-          d0[2 * q] = c0[2 * q] * a.inv_n - y00;
-          d0[2 * q + 1] = c0[2 * q + 1] * a.inv_n - y01;
-          d1[2 * q] = c1[2 * q] * a.inv_n - y10;
-          d1[2 * q + 1] = c1[2 * q + 1] * a.inv_n - y11;
+      for (int b = 0; b < kDeltaWide; ++b) {
+        const int u = u0 + b * kThreads + threadIdx.x;
+        const int tl = u / upt, w = u - (u / upt) * upt;
+        const int t = t0 + tl;
+        const bool live = u < n_units && t < a.T;
+        tls[b] = live ? tl : -1;
+        e0s[b] = sg.turns ? 8 * w : 16 * w;
+        e1s[b] = sg.turns ? 8 * w + half : 16 * w + 8;
+        xa[b] = xb[b] = ca[b] = cb[b] = make_uint4(0u, 0u, 0u, 0u);
+        if (!live) continue;
+        const int64_t row = (int64_t)t * a.D + sg.f0;
+        xa[b] = *reinterpret_cast<const uint4*>(canon + row + e0s[b]);
+        xb[b] = *reinterpret_cast<const uint4*>(canon + row + e1s[b]);
+        if (a.n_cond == 1) {
+          const uint16_t* c = a.cond[0] + (int64_t)l * a.cond_stride + row;
+          ca[b] = *reinterpret_cast<const uint4*>(c + e0s[b]);
+          cb[b] = *reinterpret_cast<const uint4*>(c + e1s[b]);
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) { d0[i] = c0[i] * a.inv_n - x0[i]; d1[i] = c1[i] * a.inv_n - x1[i]; }
       }
-      uint16_t* o = out + (int64_t)t * a.Dp + sg.f0;
-      *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0);
-      *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) { tile[e0 + i][tl] = d0[i]; tile[e1 + i][tl] = d1[i]; }
+      for (int b = 0; b < kDeltaWide; ++b) {
+        const int tl = tls[b];
+        if (tl < 0) continue;
+        const int e0 = e0s[b], e1 = e1s[b];
+        const int64_t row = (int64_t)(t0 + tl) * a.D + sg.f0;
+        float x0[8], x1[8], c0[8], c1[8];
+        bf16x8_to_f(xa[b], x0);
+        bf16x8_to_f(xb[b], x1);
+        if (a.n_cond == 1) {
+          bf16x8_to_f(ca[b], c0);
+          bf16x8_to_f(cb[b], c1);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) c0[i] = c1[i] = 0.f;
+          for (int p = 0; p < a.n_cond; ++p) {
+            const uint16_t* c = a.cond[p] + (int64_t)l * a.cond_stride + row;
+            float v0[8], v1[8];
+            bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e0), v0);
+            bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e1), v1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { c0[i] += v0[i]; c1[i] += v1[i]; }
+          }
+        }
+        float d0[8], d1[8];
+        if (sg.turns) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {   // pairs e0 + 2q, e0 + 2q + 1
+            const float4 hd = tb[e0 + 2 * q], tl4 = tb[e0 + 2 * q + 1];
+            const float a0 = x0[2 * q], a1 = x0[2 * q + 1], b0 = x1[2 * q], b1 = x1[2 * q + 1];
+            const float y00 = fmaf(a0, hd.x, -(b0 * hd.z)) + fmaf(a0, tl4.x, -(b0 * tl4.z));
+            const float y01 = fmaf(a1, hd.y, -(b1 * hd.w)) + fmaf(a1, tl4.y, -(b1 * tl4.w));
+            const float y10 = fmaf(b0, hd.x, a0 * hd.z) + fmaf(b0, tl4.x, a0 * tl4.z);
+            const float y11 = fmaf(b1, hd.y, a1 * hd.w) + fmaf(b1, tl4.y, a1 * tl4.w);
+            d0[2 * q] = c0[2 * q] * a.inv_n - y00;
+            d0[2 * q + 1] = c0[2 * q + 1] * a.inv_n - y01;
+            d1[2 * q] = c1[2 * q] * a.inv_n - y10;
+            d1[2 * q + 1] = c1[2 * q + 1] * a.inv_n - y11;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) { d0[i] = c0[i] * a.inv_n - x0[i]; d1[i] = c1[i] * a.inv_n - x1[i]; }
+        }
+        uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
+        *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0);
+        *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { tile[e0 + i][tl] = d0[i]; tile[e1 + i][tl] = d1[i]; }
+      }
     }
   } else {
     const int upt = sg.W / 4;                           // two pairs (or four elements) per unit
