@@ -91,6 +91,8 @@ struct DeltaArgs {
   int64_t cond_stride, canon_stride;   // elements between layers of the inputs
   int n_cond, T, D, Dp, Tp, rope_kind, rot_dim;
   float inv_n;
+  float* g_zero;        // the Gram accumulators, zeroed here for the first Gram of the call
+  int64_t g_count;      // floats (a multiple of 4)
 };
 
 // Segment sg of a row: unrotated features [0, plain_end) in 128-wide pieces,
@@ -134,9 +136,17 @@ __device__ __forceinline__ uint4 f_to_bf16x8(const float (&v)[8]) {
 
 __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__ DeltaArgs a,
                                                           const __grid_constant__ TableParam tab) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   __shared__ float4 tb[kTablePairs];
   __shared__ float tile[128][kDeltaTokens + 1];
   for (int i = threadIdx.x; i < kTablePairs; i += blockDim.x) tb[i] = tab.v[i];
+  {
+    const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    const int64_t n_threads = (int64_t)gridDim.x * gridDim.y * gridDim.z * blockDim.x;
+    for (int64_t e = cta * blockDim.x + threadIdx.x; e < a.g_count / 4; e += n_threads)
+      reinterpret_cast<float4*>(a.g_zero)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const int l = blockIdx.z;
   const int t0 = blockIdx.x * kDeltaTokens;
   const Segment sg = segment_of(blockIdx.y, a.rope_kind, a.D, a.rot_dim);
@@ -341,6 +351,8 @@ struct PassArgs {
 __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_constant__ CUtensorMap map_a,
                                                                 const __grid_constant__ CUtensorMap map_b,
                                                                 PassArgs a) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   extern __shared__ __align__(1024) uint8_t smp[];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -489,6 +501,8 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
 template <int KP>
 __global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t sX, float* G, int64_t sG, int R,
                                                         int rows_per_cta) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   constexpr int MT = KP / 16, NT = KP / 8, TILES = MT * NT, TPW = (TILES + 7) / 8;   // tiles per warp
   constexpr int XP = KP + 8;   // staged row pitch: fragment reads fall in distinct banks
   constexpr int CH = KP <= 48 ? 32 : 16;   // rows per stage (static shared memory < 48 KB)
@@ -560,6 +574,8 @@ __global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t 
 template <int KP>
 __global__ void __launch_bounds__(128) apply_kernel(const float* X, int64_t sX, const float* M, int64_t sM, float* out,
                                                     int64_t sO, uint16_t* out_t, int64_t sT, int ldt, int R, int solve) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   __shared__ __align__(16) float ms[KP][KP];
   const int l = blockIdx.y;
   const float* m = M + (int64_t)l * sM;
@@ -635,8 +651,10 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
 //    which nothing reads during the factorisation.
 // ---------------------------------------------------------------------------
 template <int KP>
-__global__ void __launch_bounds__(kThreads) chol_kernel(const float* G, int64_t sG, float* Rf, int64_t sR,
+__global__ void __launch_bounds__(kThreads) chol_kernel(float* G, int64_t sG, float* Rf, int64_t sR,
                                                                  int k, float rel) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   constexpr int kp = KP;
   constexpr int kCholSpan = KP / 16;    // rows (and columns) of the trailing block per thread
   extern __shared__ __align__(16) float smc[];
@@ -645,7 +663,7 @@ __global__ void __launch_bounds__(kThreads) chol_kernel(const float* G, int64_t 
   float* Rt = smc + kp * P;    // R transposed: Rt[c][j] = R[j][c]
   __shared__ float scratch[kThreads / 32];
   __shared__ float rdiag[kMaxK];
-  const float* g = G + (int64_t)blockIdx.x * sG;
+  float* g = G + (int64_t)blockIdx.x * sG;
   float* out = Rf + (int64_t)blockIdx.x * sR;
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   float tr = 0.f;
@@ -656,7 +674,8 @@ __global__ void __launch_bounds__(kThreads) chol_kernel(const float* G, int64_t 
       Rt[i * P + j] = 0.f;
       if (i == j) tr += v;
     }
-  tr = block_sum(tr, scratch);
+  tr = block_sum(tr, scratch);   // (its barriers: every thread has read G)
+  for (int e = tid; e < kp * kp; e += kThreads) g[e] = 0.f;   // zeroed for the next Gram
   const float shift = tr > 0.f ? rel * tr : 1e-30f;
   if (tid < k) A[tid * P + tid] += shift;
   __syncthreads();
@@ -709,8 +728,10 @@ __global__ void __launch_bounds__(kThreads) chol_kernel(const float* G, int64_t 
 //    eigenvector of the r-th largest eigenvalue scaled by lambda^(-1/2) (zero
 //    where lambda vanishes); other columns zero.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) jacobi_kernel(const float* Cm, int64_t sC, float* W, int64_t sW, int k,
+__global__ void __launch_bounds__(kThreads) jacobi_kernel(float* Cm, int64_t sC, float* W, int64_t sW, int k,
                                                            int kp, int m) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   extern __shared__ __align__(16) float smj[];
   const int P = kp + 1;
   float* A = smj;
@@ -719,7 +740,7 @@ __global__ void __launch_bounds__(kThreads) jacobi_kernel(const float* Cm, int64
   __shared__ int order[kMaxK];
   __shared__ float scratch[kThreads / 32];
   __shared__ int rotated;
-  const float* c = Cm + (int64_t)blockIdx.x * sC;
+  float* c = Cm + (int64_t)blockIdx.x * sC;
   float* w = W + (int64_t)blockIdx.x * sW;
   const int tid = threadIdx.x;
   float ss = 0.f;
@@ -731,7 +752,8 @@ __global__ void __launch_bounds__(kThreads) jacobi_kernel(const float* Cm, int64
     ss += v * v;
   }
   // entries below floor_abs are rounding noise of the fp32 input
-  const float floor_abs = 1e-6f * sqrtf(block_sum(ss, scratch));
+  const float floor_abs = 1e-6f * sqrtf(block_sum(ss, scratch));   // (its barriers: every thread has read C)
+  for (int e = tid; e < kp * kp; e += kThreads) c[e] = 0.f;           // zeroed for the next Gram
   const int n2 = k + (k & 1);      // index k (< kp when k is odd) is a dummy that never turns
   const int np = n2 / 2;
   // this thread's 2 x 2 blocks (t1 <= t2), the same at every step
@@ -845,6 +867,8 @@ __global__ void __launch_bounds__(kThreads) jacobi_kernel(const float* Cm, int64
 // ---------------------------------------------------------------------------
 // dst [kp][Dp] bf16 = Omega^T, zero beyond the k columns of Omega [D][k]
 __global__ void omega_t_kernel(const float* src, int D, int k, uint16_t* dst, int kp, int Dp) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < kp * D; e += gridDim.x * blockDim.x) {
     const int c = e / D, f = e - (e / D) * D;
     dst[(int64_t)c * Dp + f] = f_to_bf16(c < k ? src[(int64_t)f * k + c] : 0.f);
@@ -853,6 +877,8 @@ __global__ void omega_t_kernel(const float* src, int D, int k, uint16_t* dst, in
 // u_out[l][t][c] = bf16(U[l][t][c]) for c < m, from fp32 [L][T][kp]
 __global__ void u_out_kernel(const float* src, int64_t src_stride, int kp, uint16_t* dst, int64_t dst_stride, int rows,
                              int m) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   const int l = blockIdx.y;
   const int64_t n = (int64_t)rows * m;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
@@ -864,6 +890,8 @@ __global__ void u_out_kernel(const float* src, int64_t src_stride, int kp, uint1
 // v_out[l][f][c] = V^T[l][c][f] for c < m, from bf16 [L][kp][ld]
 __global__ void v_out_kernel(const uint16_t* src, int64_t src_stride, int ld, uint16_t* dst, int64_t dst_stride, int D,
                              int m) {
+  pdl_wait();               // the previous kernel's results are visible
+  pdl_launch_dependents();  // the next kernel may start launching
   const int l = blockIdx.y;
   const int64_t n = (int64_t)D * m;
   for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
@@ -983,6 +1011,24 @@ bool encode_kmajor(CUtensorMap* map, const uint16_t* base, int K, int rows, int 
 
 size_t pass_smem_bytes(int kp) { return 1024 + (size_t)kPassStages * (kTile * kPassK * 2 + kp * kPassK * 2) + 64; }
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// previous one on the stream drains, and waits for it in pdl_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 class Runner {
  public:
   Runner(cudaStream_t st, int L, int kp, int sms, uint32_t* status)
@@ -1021,27 +1067,26 @@ class Runner {
       if (err != cudaSuccess) return;
     }
     PassArgs pa{out, sO, M, K, kp_, b_layered ? 1 : 0, per, status_};
-    pass_kernel<<<dim3(tiles, splits, L_), kPassThreads, pass_smem_bytes(kp_), st_>>>(ma, mb, pa);
-    err = cudaGetLastError();
+    err = launch_pdl(pass_kernel, dim3(tiles, splits, L_), dim3(kPassThreads), pass_smem_bytes(kp_), st_, ma, mb, pa);
   }
 
   // G[L][kp][kp] = X^T X for X [L][R][kp]
   void gram(const float* X, int64_t sX, float* G, int R) {
     if (err != cudaSuccess) return;
     const int64_t skk = (int64_t)kp_ * kp_;
-    err = cudaMemsetAsync(G, 0, sizeof(float) * (size_t)(skk * L_), st_);
-    if (err != cudaSuccess) return;
+    // G is zero here: the deficit kernel clears it, and every reader of a Gram (the Cholesky
+    // and Jacobi kernels) clears it after reading
     // row slices sized for about four CTAs per SM over all layers (64-row multiples, 64..512)
     const int64_t want = ((int64_t)R * L_ + 4 * sms_ - 1) / (4 * sms_);
     const int rows = (int)std::min<int64_t>(512, std::max<int64_t>(64, (want + 63) / 64 * 64));
     const dim3 grid((R + rows - 1) / rows, L_);
     switch (kp_) {
-      case 16: gram_kernel<16><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
-      case 32: gram_kernel<32><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
-      case 48: gram_kernel<48><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
-      case 64: gram_kernel<64><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
-      case 80: gram_kernel<80><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
-      case 96: gram_kernel<96><<<grid, kThreads, 0, st_>>>(X, sX, G, skk, R, rows); break;
+      case 16: err = launch_pdl(gram_kernel<16>, dim3(grid), dim3(kThreads), 0, st_, X, sX, G, skk, R, rows); break;
+      case 32: err = launch_pdl(gram_kernel<32>, dim3(grid), dim3(kThreads), 0, st_, X, sX, G, skk, R, rows); break;
+      case 48: err = launch_pdl(gram_kernel<48>, dim3(grid), dim3(kThreads), 0, st_, X, sX, G, skk, R, rows); break;
+      case 64: err = launch_pdl(gram_kernel<64>, dim3(grid), dim3(kThreads), 0, st_, X, sX, G, skk, R, rows); break;
+      case 80: err = launch_pdl(gram_kernel<80>, dim3(grid), dim3(kThreads), 0, st_, X, sX, G, skk, R, rows); break;
+      case 96: err = launch_pdl(gram_kernel<96>, dim3(grid), dim3(kThreads), 0, st_, X, sX, G, skk, R, rows); break;
       default: err = cudaErrorInvalidValue; return;
     }
     err = cudaGetLastError();
@@ -1055,12 +1100,12 @@ class Runner {
     const dim3 grid((R + 127) / 128, L_);
     const int up = solve ? 1 : 0;
     switch (kp_) {
-      case 16: apply_kernel<16><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
-      case 32: apply_kernel<32><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
-      case 48: apply_kernel<48><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
-      case 64: apply_kernel<64><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
-      case 80: apply_kernel<80><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
-      case 96: apply_kernel<96><<<grid, 128, 0, st_>>>(X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 16: err = launch_pdl(apply_kernel<16>, dim3(grid), dim3(128), 0, st_, X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 32: err = launch_pdl(apply_kernel<32>, dim3(grid), dim3(128), 0, st_, X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 48: err = launch_pdl(apply_kernel<48>, dim3(grid), dim3(128), 0, st_, X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 64: err = launch_pdl(apply_kernel<64>, dim3(grid), dim3(128), 0, st_, X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 80: err = launch_pdl(apply_kernel<80>, dim3(grid), dim3(128), 0, st_, X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
+      case 96: err = launch_pdl(apply_kernel<96>, dim3(grid), dim3(128), 0, st_, X, sX, M, skk, out, sO, out_t, sT, ldt, R, up); break;
       default: err = cudaErrorInvalidValue; return;
     }
     err = cudaGetLastError();
@@ -1085,16 +1130,16 @@ class Runner {
 
   size_t chol_smem() const { return sizeof(float) * 2 * (size_t)kp_ * (kp_ + 1); }
 
-  void chol(const float* g, float* rfac, int k, float rel) {
+  void chol(float* g, float* rfac, int k, float rel) {
     if (err != cudaSuccess) return;
     const int64_t skk = (int64_t)kp_ * kp_;
     switch (kp_) {
-      case 16: chol_kernel<16><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
-      case 32: chol_kernel<32><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
-      case 48: chol_kernel<48><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
-      case 64: chol_kernel<64><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
-      case 80: chol_kernel<80><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
-      case 96: chol_kernel<96><<<L_, kThreads, chol_smem(), st_>>>(g, skk, rfac, skk, k, rel); break;
+      case 16: err = launch_pdl(chol_kernel<16>, dim3(L_), dim3(kThreads), chol_smem(), st_, g, skk, rfac, skk, k, rel); break;
+      case 32: err = launch_pdl(chol_kernel<32>, dim3(L_), dim3(kThreads), chol_smem(), st_, g, skk, rfac, skk, k, rel); break;
+      case 48: err = launch_pdl(chol_kernel<48>, dim3(L_), dim3(kThreads), chol_smem(), st_, g, skk, rfac, skk, k, rel); break;
+      case 64: err = launch_pdl(chol_kernel<64>, dim3(L_), dim3(kThreads), chol_smem(), st_, g, skk, rfac, skk, k, rel); break;
+      case 80: err = launch_pdl(chol_kernel<80>, dim3(L_), dim3(kThreads), chol_smem(), st_, g, skk, rfac, skk, k, rel); break;
+      case 96: err = launch_pdl(chol_kernel<96>, dim3(L_), dim3(kThreads), chol_smem(), st_, g, skk, rfac, skk, k, rel); break;
       default: err = cudaErrorInvalidValue; return;
     }
     err = cudaGetLastError();
@@ -1220,14 +1265,14 @@ kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* d
   da.inv_n = 1.0f / (float)n_orbit;
   pf::TableParam tab = {};
   if (rope_kind != KVRP_ROPE_NONE) pf::mean_table(deltas, n_orbit, rope_theta, rot_dim, tab.v);
-  pf::delta_kernel<<<dim3((T + pf::kDeltaTokens - 1) / pf::kDeltaTokens, pf::segment_count(rope_kind, D, da.rot_dim), L),
-                     pf::kThreads, 0, st>>>(da, tab);
-  e = cudaGetLastError();
-  if (e == cudaSuccess) {
-    pf::omega_t_kernel<<<std::max(1, std::min(sms, (D * kp + 255) / 256)), 256, 0, st>>>(omega, D, k, b.omega_t, kp,
-                                                                                         (int)b.Dp);
-    e = cudaGetLastError();
-  }
+  da.g_zero = b.g;
+  da.g_count = b.s_kk * L;
+  e = pf::launch_pdl(pf::delta_kernel,
+                     dim3((T + pf::kDeltaTokens - 1) / pf::kDeltaTokens, pf::segment_count(rope_kind, D, da.rot_dim), L),
+                     dim3(pf::kThreads), 0, st, da, tab);
+  if (e == cudaSuccess)
+    e = pf::launch_pdl(pf::omega_t_kernel, dim3(std::max(1, std::min(sms, (D * kp + 255) / 256))), dim3(256), 0, st,
+                       omega, D, k, b.omega_t, kp, (int)b.Dp);
   if (e != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_patch_form: %s", cudaGetErrorString(e));
 
   pf::Runner run(st, L, kp, sms, d_status);
@@ -1246,18 +1291,19 @@ kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* d
   run.gram(z, b.s_dk, b.g, D);
   // 4. eigenvectors of the m largest eigenvalues, scaled by lambda^-1/2
   if (run.err == cudaSuccess && !run.map_fail) {
-    pf::jacobi_kernel<<<L, pf::kThreads, run.jacobi_smem(), st>>>(b.g, b.s_kk, b.w, b.s_kk, k, kp, m);
-    run.err = cudaGetLastError();
+    run.err = pf::launch_pdl(pf::jacobi_kernel, dim3(L), dim3(pf::kThreads), run.jacobi_smem(), st, b.g, b.s_kk, b.w,
+                             b.s_kk, k, kp, m);
   }
   // 5. V_m = orth(B^T W) (columns already near unit length) as bf16 V^T; U_m = Delta V_m
   run.apply(z, b.s_dk, b.w, z2, b.s_dk, D, false);
   run.orth(z2, z, b.s_dk, D, m, 1, pf::kShiftSecond, b.g, b.rfac, b.st_d, b.s_st_d, (int)b.Dp);
   run.pass(b.delta, b.Dp, b.s_delta, b.st_d, b.Dp, b.s_st_d, true, y2, b.s_tk, T, D);
   if (run.err == cudaSuccess && !run.map_fail) {
-    pf::u_out_kernel<<<dim3(64, L), 256, 0, st>>>(y2, b.s_tk, kp, static_cast<uint16_t*>(u_out), u_layer_stride, T, m);
-    pf::v_out_kernel<<<dim3(64, L), 256, 0, st>>>(b.st_d, b.s_st_d, (int)b.Dp, static_cast<uint16_t*>(v_out),
-                                                  v_layer_stride, D, m);
-    run.err = cudaGetLastError();
+    run.err = pf::launch_pdl(pf::u_out_kernel, dim3(64, L), dim3(256), 0, st, (const float*)y2, b.s_tk, kp,
+                             static_cast<uint16_t*>(u_out), u_layer_stride, T, m);
+    if (run.err == cudaSuccess)
+      run.err = pf::launch_pdl(pf::v_out_kernel, dim3(64, L), dim3(256), 0, st, (const uint16_t*)b.st_d, b.s_st_d,
+                               (int)b.Dp, static_cast<uint16_t*>(v_out), v_layer_stride, D, m);
   }
   if (run.map_fail) return fail(KVRP_ERR_INVALID_ARG, "kv_patch_form: cuTensorMapEncodeTiled rejected a workspace map");
   if (run.err != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_patch_form: %s", cudaGetErrorString(run.err));
