@@ -119,7 +119,7 @@ __device__ inline Segment segment_of(int sg, int rope_kind, int D, int rot) {
   return s;
 }
 
-constexpr int kDeltaUnroll = 8;   // narrow path: work units per thread per batch of loads
+constexpr int kDeltaUnroll = 4;   // narrow path: work units per thread per batch of loads
 
 __device__ __forceinline__ void bf16x8_to_f(const uint4 w, float (&v)[8]) {
   const uint32_t u[4] = {w.x, w.y, w.z, w.w};
@@ -134,12 +134,12 @@ __device__ __forceinline__ uint4 f_to_bf16x8(const float (&v)[8]) {
                     f2_to_bf16x2(v[6], v[7]));
 }
 
-__global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__ DeltaArgs a,
+__global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constant__ DeltaArgs a,
                                                           const __grid_constant__ TableParam tab) {
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
   __shared__ float4 tb[kTablePairs];
-  __shared__ float tile[128][kDeltaTokens + 1];
+  __shared__ uint16_t tile[128][kDeltaTokens + 2];   // bf16 of the deficit, for the transposed rows
   for (int i = threadIdx.x; i < kTablePairs; i += blockDim.x) tb[i] = tab.v[i];
   {
     const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__
                     a.canon_stride % 8 == 0 && a.cond_stride % 8 == 0;
   if (wide) {
     // a thread's units (at most kDeltaWide of them) load everything first, then compute
-    constexpr int kDeltaWide = 4;
+    constexpr int kDeltaWide = 2;
     const int upt = sg.W / 16;
     const int n_units = kDeltaTokens * upt;
     for (int u0 = 0; u0 < n_units; u0 += kDeltaWide * kThreads) {
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__
         *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0);
         *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { tile[e0 + i][tl] = d0[i]; tile[e1 + i][tl] = d1[i]; }
+        for (int i = 0; i < 8; ++i) { tile[e0 + i][tl] = f_to_bf16(d0[i]); tile[e1 + i][tl] = f_to_bf16(d1[i]); }
       }
     }
   } else {
@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__
         uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
         *reinterpret_cast<uint32_t*>(o + e0) = f2_to_bf16x2(d00, d01);
         *reinterpret_cast<uint32_t*>(o + e1) = f2_to_bf16x2(d10, d11);
-        tile[e0][tl] = d00; tile[e0 + 1][tl] = d01; tile[e1][tl] = d10; tile[e1 + 1][tl] = d11;
+        tile[e0][tl] = f_to_bf16(d00); tile[e0 + 1][tl] = f_to_bf16(d01);
+        tile[e1][tl] = f_to_bf16(d10); tile[e1 + 1][tl] = f_to_bf16(d11);
       }
     }
   }
@@ -295,10 +296,11 @@ __global__ void __launch_bounds__(kThreads) delta_kernel(const __grid_constant__
     const int f = it / (kDeltaTokens / 8), t8 = 8 * (it - (it / (kDeltaTokens / 8)) * (kDeltaTokens / 8));
     const int t = t0 + t8;
     if (t >= a.T) continue;
-    float v[8];
+    uint4 w;
+    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = tile[f][t8 + i];
-    *reinterpret_cast<uint4*>(out_t + (int64_t)(sg.f0 + f) * a.Tp + t) = f_to_bf16x8(v);
+    for (int i = 0; i < 4; ++i) wp[i] = (uint32_t)tile[f][t8 + 2 * i] | ((uint32_t)tile[f][t8 + 2 * i + 1] << 16);
+    *reinterpret_cast<uint4*>(out_t + (int64_t)(sg.f0 + f) * a.Tp + t) = w;
   }
 }
 
