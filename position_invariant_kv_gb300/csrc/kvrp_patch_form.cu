@@ -599,8 +599,17 @@ __global__ void __launch_bounds__(128) apply_kernel(const float* X, int64_t sX, 
 #pragma unroll
     for (int j = 0; j < KP; ++j) {
       o[j] = xv[j] * ms[j][j];
+      const int l4 = (j + 4) & ~3;   // first 16-byte aligned column after j
 #pragma unroll
-      for (int l = j + 1; l < KP; ++l) xv[l] = fmaf(-o[j], ms[j][l], xv[l]);
+      for (int l = j + 1; l < l4 && l < KP; ++l) xv[l] = fmaf(-o[j], ms[j][l], xv[l]);
+#pragma unroll
+      for (int l = l4; l < KP; l += 4) {   // the rest of row j as broadcast float4 reads
+        const float4 mv = *reinterpret_cast<const float4*>(&ms[j][l]);
+        xv[l] = fmaf(-o[j], mv.x, xv[l]);
+        xv[l + 1] = fmaf(-o[j], mv.y, xv[l + 1]);
+        xv[l + 2] = fmaf(-o[j], mv.z, xv[l + 2]);
+        xv[l + 3] = fmaf(-o[j], mv.w, xv[l + 3]);
+      }
     }
   } else {
 #pragma unroll
