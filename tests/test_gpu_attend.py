@@ -129,6 +129,8 @@ def check(got, q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
     ([[(260, 32)], [(17, 0), (300, 16)]], 32, 2, 128),                                    # 16 query heads per KV head
     ([[(100, 48), (50, 128)], [(65, 0), (1, 128)]], 6, 3, 64),                            # odd KV heads; ranks 48, 128
     ([[(9000, 32), (7000, 16)], [(12000, 0)]], 16, 4, 128),                               # long: several stages per CTA
+    ([[(300, 64), (129, 128)], [(77, 96)]], 28, 4, 128),                                   # ranks above 32 at head_dim 128
+    ([[(200, 128), (33, 64)], [(150, 0)]], 32, 2, 128),                                    # 16 heads per KV head, rank 128
 ])
 def test_attention_matches_oracle(seqs, Hq, Hkv, d):
     theta, scale = 1e6, d ** -0.5
@@ -216,3 +218,19 @@ def test_bench_workload_on_sampled_sequences():
         sub_sc = [0, len(host)]
         worst = check(got[s:s + 1], qb[s:s + 1], host, sub_sc, a["Hq"], a["Hkv"], a["d"], a["theta"], scale)
         print("sequence", s, "worst ulp distance", worst)
+
+
+def test_many_chunks_and_sequences():
+    """200 chunks (1 to 90 tokens, mixed ranks) over 50 sequences: the parameter block
+    near its limit and partial lists that cross many CTA shares."""
+    rng = np.random.default_rng(95)
+    seqs, n = [], 0
+    while n < 200:
+        k = int(min(rng.integers(1, 8), 200 - n))
+        seqs.append([(int(rng.integers(1, 91)), int(rng.choice([0, 16, 32]))) for _ in range(k)])
+        n += k
+    Hq, Hkv, d, theta, scale = 8, 2, 128, 1e6, 128 ** -0.5
+    q, chunks, sc = make_case(96, seqs, Hq, Hkv, d)
+    got = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale)
+    worst = check(got, q, chunks, sc, Hq, Hkv, d, theta, scale)
+    print(len(seqs), "sequences, worst ulp distance", worst)
