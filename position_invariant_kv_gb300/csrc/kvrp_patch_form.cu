@@ -53,7 +53,7 @@ constexpr int kMaxOrbit = 64;      // conditioned caches averaged by one call
 constexpr int kJacobiSweeps = 2;   // the top-m subspace has settled by then (V_m is re-orthonormalised)
 constexpr int kThreads = 256;
 constexpr int kTile = 128;         // output rows per pass_kernel CTA
-constexpr int kPassStages = 3;     // pass_kernel pipeline depth
+constexpr int kPassStages = 4;     // pass_kernel pipeline depth
 constexpr int kPassK = 64;         // pass_kernel: contraction per stage (one 128-byte swizzle row of bf16)
 constexpr int kPassThreads = 192;  // producer warp, MMA warp, four epilogue warps
 constexpr int kDeltaTokens = 64;   // tokens per delta_kernel tile
@@ -346,10 +346,26 @@ struct PassArgs {
   int64_t sO;         // out layer stride (elements)
   int M, K, kp;
   int b_layered;      // B has one matrix per layer (else layer 0 for all)
-  int kb_per_split;   // contraction blocks of 64 per slice (blockIdx.y); slices add into a zeroed out
+  int kb_per_split;   // contraction blocks of 64 per slice; slices add into a zeroed out
+  int splits, layers;
   uint32_t* status;
 };
 
+// Bounded wait that ignores the abort flag: lets this CTA's own copies land before it exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kTimeoutCycles) {
+      if (status) atomicOr(status, KVRP_DEV_TIMEOUT);
+      return;
+    }
+  }
+}
+
+// Persistent: CTA i takes items i, i + gridDim.x, ... of (128-row tile, K slice,
+// layer).  The producer streams K-blocks through the stage ring without a break
+// between items; the MMA warp accumulates item j into TMEM buffer j % 2 while the
+// epilogue drains buffer (j - 1) % 2.
 __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_constant__ CUtensorMap map_a,
                                                                 const __grid_constant__ CUtensorMap map_b,
                                                                 PassArgs a) {
@@ -365,21 +381,25 @@ __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_cons
   const uint32_t bars = base + kPassStages * stage_bytes;
   auto full = [&](int s) { return bars + 8u * s; };
   auto empty = [&](int s) { return bars + 8u * (kPassStages + s); };
-  const uint32_t acc_bar = bars + 16u * kPassStages;
+  auto acc_full = [&](int b) { return bars + 8u * (2 * kPassStages + b); };
+  auto acc_empty = [&](int b) { return bars + 8u * (2 * kPassStages + 2 + b); };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t ncols = a.kp <= 32 ? 32u : a.kp <= 64 ? 64u : 128u;
+  const uint32_t ncols = a.kp <= 32 ? 32u : a.kp <= 64 ? 64u : 128u;   // one accumulator
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPassStages; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    mbar_init(acc_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 4);   // the four epilogue warps
+    }
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
-                 "r"(ncols)
+                 "r"(2 * ncols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -387,74 +407,113 @@ __global__ void __launch_bounds__(kPassThreads, 2) pass_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const int l = blockIdx.z;
-  const int m0 = blockIdx.x * kTile;
-  const int kb0 = blockIdx.y * a.kb_per_split;
-  const int nk = max(0, min((a.K + kPassK - 1) / kPassK - kb0, a.kb_per_split));
-  const bool split = gridDim.y > 1;
+  const int tiles = (a.M + kTile - 1) / kTile;
+  const int n_items = tiles * a.splits * a.layers;
+  const int nkb_all = (a.K + kPassK - 1) / kPassK;
+  const bool split = a.splits > 1;
   volatile int* abort_p = &abort_flag;
+  struct Item {
+    int m0, kb0, nk, l;
+  };
+  auto item_of = [&](int it) {
+    Item r;
+    const int t = it % tiles, rest = it / tiles;
+    r.m0 = t * kTile;
+    r.kb0 = (rest % a.splits) * a.kb_per_split;
+    r.l = rest / a.splits;
+    r.nk = max(0, min(nkb_all - r.kb0, a.kb_per_split));
+    return r;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
-      const int lb = a.b_layered ? l : 0;
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int st = kb % kPassStages;
-        if (kb >= kPassStages && !wait_phase(empty(st), ((kb / kPassStages) - 1) & 1, abort_p, a.status)) break;
-        const uint32_t sa = base + st * stage_bytes;
-        mbar_expect_tx(full(st), stage_bytes);
-        tma_load_3d(sa, &map_a, full(st), (kb0 + kb) * kPassK, m0, l);
-        tma_load_3d(sa + a_bytes, &map_b, full(st), (kb0 + kb) * kPassK, 0, lb);
-        ++issued;
+      int g = 0;   // K-blocks issued by this CTA
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+        const Item r = item_of(it);
+        const int lb = a.b_layered ? r.l : 0;
+        bool ok = true;
+        for (int kb = 0; kb < r.nk; ++kb, ++g) {
+          const int st = g % kPassStages;
+          if (g >= kPassStages && !wait_phase(empty(st), ((g / kPassStages) - 1) & 1, abort_p, a.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t sa = base + st * stage_bytes;
+          mbar_expect_tx(full(st), stage_bytes);
+          tma_load_3d(sa, &map_a, full(st), (r.kb0 + kb) * kPassK, r.m0, r.l);
+          tma_load_3d(sa + a_bytes, &map_b, full(st), (r.kb0 + kb) * kPassK, 0, lb);
+        }
+        if (!ok) break;
       }
       // every issued copy must land before the CTA may exit
-      for (int kb = max(0, issued - kPassStages); kb < issued; ++kb)
-        wait_phase(full(kb % kPassStages), (kb / kPassStages) & 1, abort_p, a.status);
+      for (int q = max(0, g - kPassStages); q < g; ++q) drain_wait(full(q % kPassStages), (q / kPassStages) & 1, a.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(a.kp);
-      for (int kb = 0; kb < nk; ++kb) {
-        const int st = kb % kPassStages;
-        if (!wait_phase(full(st), (kb / kPassStages) & 1, abort_p, a.status)) break;
+      int g = 0, j = 0;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
+        const Item r = item_of(it);
+        const int b = j & 1;
+        const uint32_t acc = tmem + (uint32_t)b * ncols;
+        // the epilogue has drained this buffer (item j - 2)
+        if (j >= 2 && !wait_phase(acc_empty(b), ((j >> 1) - 1) & 1, abort_p, a.status)) break;
         tc_fence_after();
-        const uint32_t sa = base + st * stage_bytes;
+        bool ok = true;
+        for (int kb = 0; kb < r.nk; ++kb, ++g) {
+          const int st = g % kPassStages;
+          if (!wait_phase(full(st), (g / kPassStages) & 1, abort_p, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + st * stage_bytes;
 #pragma unroll
-        for (int j = 0; j < kPassK / 16; ++j)
-          mma_bf16(tmem, desc_k_sw128(sa + 32u * j), desc_k_sw128(sa + a_bytes + 32u * j), idesc,
-                   (kb | j) != 0 ? 1u : 0u);
-        mma_commit(empty(st));   // the stage is free once these MMAs have read it
+          for (int q = 0; q < kPassK / 16; ++q)
+            mma_bf16(acc, desc_k_sw128(sa + 32u * q), desc_k_sw128(sa + a_bytes + 32u * q), idesc,
+                     (kb | q) != 0 ? 1u : 0u);
+          mma_commit(empty(st));   // the stage is free once these MMAs have read it
+        }
+        if (!ok) break;
+        mma_commit(acc_full(b));   // arrives when every MMA issued so far has completed
       }
-      mma_commit(acc_bar);       // arrives when every MMA issued above has completed
-      wait_phase(acc_bar, 0, abort_p, a.status);
     }
   } else {
-    // tcgen05.ld is warp-collective: the whole warp loads or none of it
-    const bool ok = __all_sync(0xffffffffu, wait_phase(acc_bar, 0, abort_p, a.status));
-    tc_fence_after();
     const int quarter = warp & 3;              // TMEM lanes this warp may read
     const int row = quarter * 32 + lane;
-    if (ok && nk > 0) {
-      float* o = a.out + (int64_t)l * a.sO + (int64_t)(m0 + row) * a.kp;
-      for (int c0 = 0; c0 < a.kp; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
-        if (m0 + row < a.M) {
+    int j = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
+      const Item r = item_of(it);
+      const int b = j & 1;
+      // tcgen05.ld is warp-collective: the whole warp loads or none of it
+      const bool ok = __all_sync(0xffffffffu, wait_phase(acc_full(b), (j >> 1) & 1, abort_p, a.status));
+      tc_fence_after();
+      if (ok && r.nk > 0) {
+        float* o = a.out + (int64_t)r.l * a.sO + (int64_t)(r.m0 + row) * a.kp;
+        for (int c0 = 0; c0 < a.kp; c0 += 16) {
+          float v[16];
+          tmem_ld16(tmem + (uint32_t)b * ncols + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+          if (r.m0 + row < a.M) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 f4 = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-            if (split) atomicAdd(reinterpret_cast<float4*>(o + c0 + 4 * q), f4);
-            else *reinterpret_cast<float4*>(o + c0 + 4 * q) = f4;
+            for (int q = 0; q < 4; ++q) {
+              const float4 f4 = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              if (split) atomicAdd(reinterpret_cast<float4*>(o + c0 + 4 * q), f4);
+              else *reinterpret_cast<float4*>(o + c0 + 4 * q) = f4;
+            }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(b));   // this warp is done with buffer b
+      if (!ok) break;
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(ncols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(2 * ncols) : "memory");
   }
 }
 
@@ -1020,7 +1079,7 @@ bool encode_kmajor(CUtensorMap* map, const uint16_t* base, int K, int rows, int 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t pass_smem_bytes(int kp) { return 1024 + (size_t)kPassStages * (kTile * kPassK * 2 + kp * kPassK * 2) + 64; }
+size_t pass_smem_bytes(int kp) { return 1024 + (size_t)kPassStages * (kTile * kPassK * 2 + kp * kPassK * 2) + 128; }
 
 // Launch with programmatic stream serialization: the kernel may start while the
 // previous one on the stream drains, and waits for it in pdl_wait().
@@ -1077,8 +1136,9 @@ class Runner {
       err = cudaMemsetAsync(out, 0, sizeof(float) * (size_t)(sO * (L_ - 1) + (int64_t)M * kp_), st_);
       if (err != cudaSuccess) return;
     }
-    PassArgs pa{out, sO, M, K, kp_, b_layered ? 1 : 0, per, status_};
-    err = launch_pdl(pass_kernel, dim3(tiles, splits, L_), dim3(kPassThreads), pass_smem_bytes(kp_), st_, ma, mb, pa);
+    PassArgs pa{out, sO, M, K, kp_, b_layered ? 1 : 0, per, splits, L_, status_};
+    const int items = tiles * splits * L_;
+    err = launch_pdl(pass_kernel, dim3(std::min(items, cap)), dim3(kPassThreads), pass_smem_bytes(kp_), st_, ma, mb, pa);
   }
 
   // G[L][kp][kp] = X^T X for X [L][R][kp]
