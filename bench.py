@@ -479,7 +479,6 @@ def bench_patch_form(args) -> dict:
     canon, cond, deltas = patch_form_setup(wl, orbit, device)
     g = torch.Generator(device=device).manual_seed(wl.seed + 202)
     omega = torch.randn((D, m + p), generator=g, device=device)
-    ws = torch.empty(kvrp.kv_patch_form_workspace_size(L, T, D, m, p), dtype=torch.uint8, device=device)
     fac = {n: (torch.empty((L, T, m), dtype=torch.bfloat16, device=device),
                torch.empty((L, D, m), dtype=torch.bfloat16, device=device)) for n in wl.tensors}
     d_status = torch.zeros(1, dtype=torch.int32, device=device)
@@ -488,14 +487,32 @@ def bench_patch_form(args) -> dict:
         kinds = {"kv": (kvrp.KVRP_ROPE_MLA_TAIL, wl.rope_dim)}
     else:
         kinds = {"k": (kvrp.KVRP_ROPE_HEADS, wl.head_dim), "v": (kvrp.KVRP_ROPE_NONE, 0)}
+    # The calls of a step (one per tensor, or per tensor and range of layers) each run on
+    # a stream of their own with their own workspace: one call's k x k solves (one CTA per
+    # layer) overlap another's passes over the deficit.
+    per = max(1, args.streams // len(wl.tensors))
+    bounds = [L * i // per for i in range(per + 1)]
+    jobs = [(n, bounds[i], bounds[i + 1]) for n in wl.tensors for i in range(per) if bounds[i + 1] > bounds[i]]
+    streams = [torch.cuda.Stream(device=device) for _ in jobs] if args.streams > 1 else [stream] * len(jobs)
+    wss = [torch.empty(kvrp.kv_patch_form_workspace_size(l1 - l0, T, D, m, p), dtype=torch.uint8, device=device)
+           for (_, l0, l1) in (jobs if args.streams > 1 else jobs[:1])]
+    fork = torch.cuda.Event()
+    joins = [torch.cuda.Event() for _ in jobs]
 
     def step():
-        for n in wl.tensors:
+        fork.record(stream)
+        for j, (n, l0, l1) in enumerate(jobs):
             kind, rot = kinds[n]
-            kvrp.kv_patch_form_orbit(cond[n], deltas, canon[n], n_layers=L, n_tokens=T, row_width=D, rope_kind=kind,
-                                     rot_dim=rot, rope_theta=wl.theta, rank=m, oversample=p, power_iters=q,
-                                     omega=omega, u_out=fac[n][0], v_out=fac[n][1], workspace=ws,
-                                     d_status=d_status, stream=stream)
+            s = streams[j]
+            s.wait_event(fork)
+            kvrp.kv_patch_form_orbit([c[l0:l1] for c in cond[n]], deltas, canon[n][l0:l1], n_layers=l1 - l0,
+                                     n_tokens=T, row_width=D, rope_kind=kind, rot_dim=rot, rope_theta=wl.theta,
+                                     rank=m, oversample=p, power_iters=q, omega=omega, u_out=fac[n][0][l0:l1],
+                                     v_out=fac[n][1][l0:l1], workspace=wss[min(j, len(wss) - 1)],
+                                     d_status=d_status, stream=s)
+            joins[j].record(s)
+        for e in joins:
+            stream.wait_event(e)
 
     for _ in range(args.warmup):
         step()
@@ -520,16 +537,18 @@ def bench_patch_form(args) -> dict:
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "row": "patch_form",
         "config": {"workload": f"{wl.name} first chunk: {L} layers x {T} tokens x {D} features, tensors "
                                f"{'/'.join(wl.tensors)}, rank {m}, oversample {p}, {q} subspace iterations, "
-                               f"orbit of {orbit} ordering(s)",
+                               f"orbit of {orbit} ordering(s), "
+                               f"{len(jobs)} call(s) per step ({per} layer range(s) per tensor), "
+                               f"{'each on its own stream' if args.streams > 1 else 'in turn on one stream'}",
                    "tokens_per_step": T, "method_bytes_per_step": nb,
                    "l2": f"inputs larger than L2 ({nb / 1e6:.0f} MB moved per step vs 129 MB L2)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "kernel": "kv_patch_form_orbit, whole call (delta, tensor-core passes, k x k solves)",
                      "peak_source": peaks["source"]},
-        # per tensor: deficit, Omega transpose, 2q + 3 passes over the deficit, 2q + 3 orthonormalisation
+        # per call: deficit, Omega transpose, 2q + 3 passes over the deficit, 2q + 3 orthonormalisation
         # rounds of (Gram, Cholesky, apply), the projected Gram, Jacobi, the B^T W apply, U and V writers
-        "gpu_launches": steps * len(wl.tensors) * (2 + (2 * q + 3) + 3 * (2 * q + 3) + 5),
+        "gpu_launches": steps * len(jobs) * (2 + (2 * q + 3) + 3 * (2 * q + 3) + 5),
         "clocks": clocks.summary(),
         "device_status": int(d_status.item()),
     }
@@ -758,6 +777,9 @@ def main():
     ap.add_argument("--orbit", type=int, default=1, help="patch_form: conditioned caches averaged (orbit patch)")
     ap.add_argument("--oversample", type=int, default=16, help="patch_form: range-finder oversampling")
     ap.add_argument("--power-iters", type=int, default=2, help="patch_form: subspace iterations")
+    ap.add_argument("--streams", type=int, default=4,
+                    help="patch_form: concurrent calls per step, one stream each (tensors first, then layer "
+                         "ranges of each tensor); 1 runs the tensors in turn on one stream")
     args = ap.parse_args()
     if args.cpu_baseline_worker:
         if args.row == "attend":

@@ -227,7 +227,7 @@ kvrp_status kv_relocate_batch_noalloc(
  * V_m [D][m] in bf16 such that U_m V_m^T approximates Delta, ready for
  * kv_relocate_patch / _mla / _batch.  The factorisation is a randomized range
  * finder with `power_iters` power iterations, Cholesky-QR orthonormalisation
- * and an fp64 Jacobi eigensolver on the small projected problem.
+ * and an fp32 Jacobi eigensolver on the small projected problem.
  *   conditioned, canonical  device bf16 [n_layers][n_tokens][row_width], rows
  *               dense; layer l at base + l * *_layer_stride elements (0: dense
  *               layers).  Only read.
@@ -248,6 +248,10 @@ kvrp_status kv_relocate_batch_noalloc(
  *   workspace   device scratch of at least kv_patch_form_workspace_size(...)
  *               bytes, owned by the caller, busy until the call's work on
  *               `stream` completes (no two overlapping calls may share it).
+ *               Calls with their own workspaces may run concurrently on
+ *               different streams (K and V of one chunk, say): the k x k
+ *               solves occupy one CTA per layer, so a second call's passes
+ *               fill the rest of the GPU meanwhile.
  *   d_status    optional device word; KVRP_DEV_TIMEOUT is OR-ed in if a
  *               pipeline wait of the tensor-core passes gave up (results invalid).
  * Base pointers must be 16-byte aligned.  Precision: Delta is stored in bf16

@@ -252,3 +252,53 @@ def test_orbit_patch_matches_exact_svd_of_the_mean_deficit(kind, D, rot):
                                  lay) for l in range(L)])
     for got, ref, tail, total in residuals(d2, _bits(u1), _bits(v1), m):
         assert got <= 1.05 * ref + 1e-9 * total
+
+
+def test_concurrent_calls_on_two_streams():
+    """Keys and values of one chunk formed by two calls in flight at once, each on
+    its own stream with its own workspace: both meet the residual bar, and each
+    patch U_m V_m^T agrees with the same call run alone (no state is shared
+    between calls; the Gram sums are atomic, so the bits may differ in rounding)."""
+    import position_invariant_kv_gb300 as kvrp
+    delta, theta, L, T, D, m, p, q = 2024, 1e6, 4, 640, 512, 32, 16, 2
+    cases = {"heads": make_case(71, L, T, D, "heads", 128, delta, theta, 40),
+             "none": make_case(72, L, T, D, "none", 0, delta, theta, 40)}
+    g = torch.Generator(device="cuda").manual_seed(5)
+    omega = torch.randn((D, m + p), generator=g, device="cuda", dtype=torch.float32)
+    rope = {"heads": (kvrp.KVRP_ROPE_HEADS, 128), "none": (kvrp.KVRP_ROPE_NONE, 0)}
+    dev = {n: (_dev(cond), _dev(canon)) for n, (canon, cond) in cases.items()}
+
+    def launch(n, stream, ws):
+        u = torch.empty((L, T, m), dtype=torch.bfloat16, device="cuda")
+        v = torch.empty((L, D, m), dtype=torch.bfloat16, device="cuda")
+        kvrp.kv_patch_form(dev[n][0], dev[n][1], n_layers=L, n_tokens=T, row_width=D, rope_kind=rope[n][0],
+                           rot_dim=rope[n][1], delta=delta, rope_theta=theta, rank=m, oversample=p,
+                           power_iters=q, omega=omega, u_out=u, v_out=v, workspace=ws, stream=stream)
+        return u, v
+
+    size = kvrp.kv_patch_form_workspace_size(L, T, D, m, p)
+    wss = {n: torch.empty(size, dtype=torch.uint8, device="cuda") for n in cases}
+    main = torch.cuda.current_stream()
+    alone = {}
+    for n in cases:
+        alone[n] = launch(n, main, wss[n])
+        torch.cuda.synchronize()
+    streams = {n: torch.cuda.Stream() for n in cases}
+    start = torch.cuda.Event()
+    start.record(main)
+    both = {}
+    for n in cases:
+        streams[n].wait_event(start)
+        both[n] = launch(n, streams[n], wss[n])
+    torch.cuda.synchronize()
+    for n, (canon, cond) in cases.items():
+        rot = rope[n][1]
+        dl = oracle_delta(canon, cond, n, rot, delta, theta)
+        u, v = _bits(both[n][0]), _bits(both[n][1])
+        for got, ref, tail, total in residuals(dl, u, v, m):
+            assert got <= 1.05 * ref + 1e-9 * total, (n, got, ref)
+        from oracle import bf16_bits_to_f64
+        for l in range(L):
+            pb = bf16_bits_to_f64(u[l]) @ bf16_bits_to_f64(v[l]).T
+            pa = bf16_bits_to_f64(_bits(alone[n][0])[l]) @ bf16_bits_to_f64(_bits(alone[n][1])[l]).T
+            assert np.linalg.norm(pb - pa) <= 1e-2 * np.linalg.norm(pa), (n, l)
