@@ -52,6 +52,7 @@ constexpr int kMaxK = 96;          // rank + oversampling bound (k x k solves li
 constexpr int kMaxOrbit = 64;      // conditioned caches averaged by one call
 constexpr int kJacobiSweeps = 2;   // the top-m subspace has settled by then (V_m is re-orthonormalised)
 constexpr int kThreads = 256;
+constexpr int kJacThreads = 512;   // jacobi_kernel: at most one 2 x 2 block per thread for k <= 48
 constexpr int kTile = 128;         // output rows per pass_kernel CTA
 constexpr int kPassStages = 4;     // pass_kernel pipeline depth
 constexpr int kPassK = 64;         // pass_kernel: contraction per stage (one 128-byte swizzle row of bf16)
@@ -698,6 +699,7 @@ __global__ void __launch_bounds__(128) apply_kernel(const float* X, int64_t sX, 
 
 // Sum of one value per thread over the CTA (blockDim.x == kThreads); `scratch`
 // holds kThreads / 32 floats.  Every thread gets the total.
+template <int NT = kThreads>   // threads of the CTA; scratch holds NT / 32 floats
 __device__ __forceinline__ float block_sum(float v, float* scratch) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -705,7 +707,7 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
   __syncthreads();
   float t = 0.f;
 #pragma unroll
-  for (int w = 0; w < kThreads / 32; ++w) t += scratch[w];
+  for (int w = 0; w < NT / 32; ++w) t += scratch[w];
   __syncthreads();
   return t;
 }
@@ -798,8 +800,9 @@ __global__ void __launch_bounds__(kThreads) chol_kernel(float* G, int64_t sG, fl
 //    eigenvector of the r-th largest eigenvalue scaled by lambda^(-1/2) (zero
 //    where lambda vanishes); other columns zero.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) jacobi_kernel(float* Cm, int64_t sC, float* W, int64_t sW, int k,
-                                                           int kp, int m) {
+template <int NT>   // threads per CTA
+__global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float* W, int64_t sW, int k, int kp,
+                                                    int m) {
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
   extern __shared__ __align__(16) float smj[];
@@ -808,13 +811,13 @@ __global__ void __launch_bounds__(kThreads) jacobi_kernel(float* Cm, int64_t sC,
   float* V = smj + kp * P;
   __shared__ int4 rot[kMaxK / 2];      // {p, q, cos, sin} of each pair of the step
   __shared__ int order[kMaxK];
-  __shared__ float scratch[kThreads / 32];
+  __shared__ float scratch[NT / 32];
   __shared__ int rotated;
   float* c = Cm + (int64_t)blockIdx.x * sC;
   float* w = W + (int64_t)blockIdx.x * sW;
   const int tid = threadIdx.x;
   float ss = 0.f;
-  for (int e = tid; e < kp * kp; e += kThreads) {
+  for (int e = tid; e < kp * kp; e += NT) {
     const int i = e / kp, j = e - (e / kp) * kp;
     const float v = (i < k && j < k) ? 0.5f * (c[i * kp + j] + c[j * kp + i]) : 0.f;
     A[i * P + j] = v;
@@ -822,22 +825,22 @@ __global__ void __launch_bounds__(kThreads) jacobi_kernel(float* Cm, int64_t sC,
     ss += v * v;
   }
   // entries below floor_abs are rounding noise of the fp32 input
-  const float floor_abs = 1e-6f * sqrtf(block_sum(ss, scratch));   // (its barriers: every thread has read C)
-  for (int e = tid; e < kp * kp; e += kThreads) c[e] = 0.f;           // zeroed for the next Gram
+  const float floor_abs = 1e-6f * sqrtf(block_sum<NT>(ss, scratch));   // (its barriers: every thread has read C)
+  for (int e = tid; e < kp * kp; e += NT) c[e] = 0.f;           // zeroed for the next Gram
   const int n2 = k + (k & 1);      // index k (< kp when k is odd) is a dummy that never turns
   const int np = n2 / 2;
   // this thread's 2 x 2 blocks (t1 <= t2), the same at every step
-  constexpr int kMaxBlk = ((kMaxK / 2) * (kMaxK / 2 + 1) / 2 + kThreads - 1) / kThreads;
+  constexpr int kMaxBlk = ((kMaxK / 2) * (kMaxK / 2 + 1) / 2 + NT - 1) / NT;
   int blk[kMaxBlk];
   int nb = 0;
   {
     int idx = 0;
     for (int t1 = 0; t1 < np; ++t1)
       for (int t2 = t1; t2 < np; ++t2, ++idx)
-        if (idx % kThreads == tid && nb < kMaxBlk) blk[nb++] = (t1 << 8) | t2;
+        if (idx % NT == tid && nb < kMaxBlk) blk[nb++] = (t1 << 8) | t2;
   }
   // eigenvector rows: thread -> row vj, pairs vh, vh + H, ...
-  const int H = max(1, kThreads / k);
+  const int H = max(1, NT / k);
   const int vj = tid % k, vh = tid / k;
   for (int sweep = 0; sweep < kJacobiSweeps; ++sweep) {
     if (tid == 0) rotated = 0;
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__(kThreads) jacobi_kernel(float* Cm, int64_t sC,
   }
   __syncthreads();
   const float lmax = fmaxf(A[order[0] * P + order[0]], 0.f);
-  for (int e = tid; e < kp * kp; e += kThreads) {
+  for (int e = tid; e < kp * kp; e += NT) {
     const int i = e / kp, r = e - (e / kp) * kp;
     float v = 0.f;
     if (i < k && r < m && r < k) {
@@ -1227,7 +1230,7 @@ class Runner {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(jacobi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, jac);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(jacobi_kernel<kJacThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, jac);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem_bytes(kMaxK));
     return e;
@@ -1362,8 +1365,8 @@ kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* d
   run.gram(z, b.s_dk, b.g, D);
   // 4. eigenvectors of the m largest eigenvalues, scaled by lambda^-1/2
   if (run.err == cudaSuccess && !run.map_fail) {
-    run.err = pf::launch_pdl(pf::jacobi_kernel, dim3(L), dim3(pf::kThreads), run.jacobi_smem(), st, b.g, b.s_kk, b.w,
-                             b.s_kk, k, kp, m);
+    run.err = pf::launch_pdl(pf::jacobi_kernel<pf::kJacThreads>, dim3(L), dim3(pf::kJacThreads), run.jacobi_smem(), st,
+                             b.g, b.s_kk, b.w, b.s_kk, k, kp, m);
   }
   // 5. V_m = orth(B^T W) (columns already near unit length) as bf16 V^T; U_m = Delta V_m
   run.apply(z, b.s_dk, b.w, z2, b.s_dk, D, false);

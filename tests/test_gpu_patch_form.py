@@ -257,8 +257,9 @@ def test_orbit_patch_matches_exact_svd_of_the_mean_deficit(kind, D, rot):
 def test_concurrent_calls_on_two_streams():
     """Keys and values of one chunk formed by two calls in flight at once, each on
     its own stream with its own workspace: both meet the residual bar, and each
-    patch U_m V_m^T agrees with the same call run alone (no state is shared
-    between calls; the Gram sums are atomic, so the bits may differ in rounding)."""
+    residual is that of the same call run alone.  (The Gram sums are atomic, so
+    the bits may differ in rounding; with noise-level singular values at the cut
+    the last directions of the patch are not unique, the residual is.)"""
     import position_invariant_kv_gb300 as kvrp
     delta, theta, L, T, D, m, p, q = 2024, 1e6, 4, 640, 512, 32, 16, 2
     cases = {"heads": make_case(71, L, T, D, "heads", 128, delta, theta, 40),
@@ -295,10 +296,7 @@ def test_concurrent_calls_on_two_streams():
         rot = rope[n][1]
         dl = oracle_delta(canon, cond, n, rot, delta, theta)
         u, v = _bits(both[n][0]), _bits(both[n][1])
-        for got, ref, tail, total in residuals(dl, u, v, m):
+        res_alone = residuals(dl, _bits(alone[n][0]), _bits(alone[n][1]), m)
+        for (got, ref, tail, total), (got1, _, _, _) in zip(residuals(dl, u, v, m), res_alone):
             assert got <= 1.05 * ref + 1e-9 * total, (n, got, ref)
-        from oracle import bf16_bits_to_f64
-        for l in range(L):
-            pb = bf16_bits_to_f64(u[l]) @ bf16_bits_to_f64(v[l]).T
-            pa = bf16_bits_to_f64(_bits(alone[n][0])[l]) @ bf16_bits_to_f64(_bits(alone[n][1])[l]).T
-            assert np.linalg.norm(pb - pa) <= 1e-2 * np.linalg.norm(pa), (n, l)
+            assert abs(got - got1) <= 0.02 * got1, (n, got, got1)
