@@ -499,23 +499,37 @@ def bench_patch_form(args) -> dict:
     fork = torch.cuda.Event()
     joins = [torch.cuda.Event() for _ in jobs]
 
-    def step():
+    def fork_all():
         fork.record(stream)
+        for s in set(streams):
+            if s is not stream:
+                s.wait_event(fork)
+
+    def join_all():
+        for j, s in enumerate(streams):
+            joins[j].record(s)
+            stream.wait_event(joins[j])
+
+    def step():
+        # Steps are independent chunks: each stream runs its calls back to back (its
+        # workspace and outputs are only reused in its own order) unless --join-steps
+        # makes every step wait for the previous one on all streams.
+        if args.join_steps:
+            fork_all()
         for j, (n, l0, l1) in enumerate(jobs):
             kind, rot = kinds[n]
-            s = streams[j]
-            s.wait_event(fork)
             kvrp.kv_patch_form_orbit([c[l0:l1] for c in cond[n]], deltas, canon[n][l0:l1], n_layers=l1 - l0,
                                      n_tokens=T, row_width=D, rope_kind=kind, rot_dim=rot, rope_theta=wl.theta,
                                      rank=m, oversample=p, power_iters=q, omega=omega, u_out=fac[n][0][l0:l1],
                                      v_out=fac[n][1][l0:l1], workspace=wss[min(j, len(wss) - 1)],
-                                     d_status=d_status, stream=s)
-            joins[j].record(s)
-        for e in joins:
-            stream.wait_event(e)
+                                     d_status=d_status, stream=streams[j])
+        if args.join_steps:
+            join_all()
 
+    fork_all()
     for _ in range(args.warmup):
         step()
+    join_all()
     torch.cuda.synchronize()
     steps = args.steps
     with ClockSampler(local) as clocks:
@@ -523,8 +537,10 @@ def bench_patch_form(args) -> dict:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
+        fork_all()
         for _ in range(steps):
             step()
+        join_all()
         t1.record(stream)
         torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
@@ -539,7 +555,8 @@ def bench_patch_form(args) -> dict:
                                f"{'/'.join(wl.tensors)}, rank {m}, oversample {p}, {q} subspace iterations, "
                                f"orbit of {orbit} ordering(s), "
                                f"{len(jobs)} call(s) per step ({per} layer range(s) per tensor), "
-                               f"{'each on its own stream' if args.streams > 1 else 'in turn on one stream'}",
+                               f"{'each on its own stream' if args.streams > 1 else 'in turn on one stream'}"
+                               f"{', every step joined' if args.join_steps else ''}",
                    "tokens_per_step": T, "method_bytes_per_step": nb,
                    "l2": f"inputs larger than L2 ({nb / 1e6:.0f} MB moved per step vs 129 MB L2)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -777,6 +794,8 @@ def main():
     ap.add_argument("--orbit", type=int, default=1, help="patch_form: conditioned caches averaged (orbit patch)")
     ap.add_argument("--oversample", type=int, default=16, help="patch_form: range-finder oversampling")
     ap.add_argument("--power-iters", type=int, default=2, help="patch_form: subspace iterations")
+    ap.add_argument("--join-steps", type=int, default=0,
+                    help="patch_form: 1 makes each step wait for the previous one on every stream")
     ap.add_argument("--streams", type=int, default=4,
                     help="patch_form: concurrent calls per step, one stream each (tensors first, then layer "
                          "ranges of each tensor); 1 runs the tensors in turn on one stream")
