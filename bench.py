@@ -457,6 +457,16 @@ def patch_bytes(L, T, D, m, p, q, orbit) -> int:
     return n * 2 * (1 + orbit) + n * 4 + (2 * q + 3) * n * 2 + (2 * q + 3) * 3 * skinny + L * (T + D) * m * 2
 
 
+def patch_form_jobs(tensors, n_layers: int, streams: int):
+    """The calls of one patch-formation step: (tensor, first layer, end layer)
+    for each tensor, its layers cut into max(1, streams // len(tensors)) nearly
+    equal ranges (empty ranges dropped), and that range count."""
+    per = max(1, streams // len(tensors))
+    bounds = [n_layers * i // per for i in range(per + 1)]
+    jobs = [(n, bounds[i], bounds[i + 1]) for n in tensors for i in range(per) if bounds[i + 1] > bounds[i]]
+    return jobs, per
+
+
 def bench_patch_form(args) -> dict:
     import torch
     import workloads as W
@@ -490,9 +500,7 @@ def bench_patch_form(args) -> dict:
     # The calls of a step (one per tensor, or per tensor and range of layers) each run on
     # a stream of their own with their own workspace: one call's k x k solves (one CTA per
     # layer) overlap another's passes over the deficit.
-    per = max(1, args.streams // len(wl.tensors))
-    bounds = [L * i // per for i in range(per + 1)]
-    jobs = [(n, bounds[i], bounds[i + 1]) for n in wl.tensors for i in range(per) if bounds[i + 1] > bounds[i]]
+    jobs, per = patch_form_jobs(wl.tensors, L, args.streams)
     streams = [torch.cuda.Stream(device=device) for _ in jobs] if args.streams > 1 else [stream] * len(jobs)
     wss = [torch.empty(kvrp.kv_patch_form_workspace_size(l1 - l0, T, D, m, p), dtype=torch.uint8, device=device)
            for (_, l0, l1) in (jobs if args.streams > 1 else jobs[:1])]
