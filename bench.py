@@ -526,7 +526,7 @@ def bench_patch_form(args) -> dict:
             fork_all()
         for j, (n, l0, l1) in enumerate(jobs):
             kind, rot = kinds[n]
-            kvrp.kv_patch_form_orbit([c[l0:l1] for c in cond[n]], deltas, canon[n][l0:l1], n_layers=l1 - l0,
+            kvrp.kv_patch_form_orbit([x[l0:l1] for x in cond[n]], deltas, canon[n][l0:l1], n_layers=l1 - l0,
                                      n_tokens=T, row_width=D, rope_kind=kind, rot_dim=rot, rope_theta=wl.theta,
                                      rank=m, oversample=p, power_iters=q, omega=omega, u_out=fac[n][0][l0:l1],
                                      v_out=fac[n][1][l0:l1], workspace=wss[min(j, len(wss) - 1)],
