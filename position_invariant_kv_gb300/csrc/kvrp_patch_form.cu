@@ -848,8 +848,14 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
     for (int step = 0; step < n2 - 1; ++step) {
       if (tid < np) {
         // circle method: player n2-1 stays, the others move one seat per step
-        int p = tid == 0 ? n2 - 1 : (step + tid) % (n2 - 1);
-        int q = tid == 0 ? step : (step - tid + n2 - 1) % (n2 - 1);
+        // (step + tid and step - tid + n2 - 1 lie in [0, 2 (n2 - 1)): one wrap each)
+        int p = n2 - 1, q = step;
+        if (tid > 0) {
+          p = step + tid;
+          if (p >= n2 - 1) p -= n2 - 1;
+          q = step - tid + n2 - 1;
+          if (q >= n2 - 1) q -= n2 - 1;
+        }
         if (p > q) { const int x = p; p = q; q = x; }
         float cc = 1.f, s = 0.f;
         if (q < k) {
@@ -862,7 +868,7 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
           if (fabsf(apq) > floor_abs && apq * apq > 1e-8f * fabsf(app * aqq)) {
             const float th = __fdividef(aqq - app, 2.f * apq);
             const float r2 = fmaf(th, th, 1.f);
-            const float tt = copysignf(__frcp_rn(fabsf(th) + r2 * rsqrtf(r2)), th);
+            const float tt = copysignf(__fdividef(1.f, fabsf(th) + r2 * rsqrtf(r2)), th);
             cc = rsqrtf(fmaf(tt, tt, 1.f));
             s = tt * cc;
             if (s != 0.f) rotated = 1;
