@@ -1,5 +1,5 @@
-"""Host-side arithmetic of bench.py that needs no GPU: how a patch-formation
-step is cut into concurrent calls."""
+"""Host-side parts of bench.py that need no GPU: how a patch-formation step
+is cut into concurrent calls, and the reference arm's JSON line."""
 import pytest
 
 import bench
@@ -26,3 +26,22 @@ def test_patch_form_jobs_cover_every_layer_once(tensors, L, streams):
 def test_one_stream_runs_whole_tensors():
     jobs, per = bench.patch_form_jobs(("k", "v"), 28, 1)
     assert per == 1 and jobs == [("k", 0, 28), ("v", 0, 28)]
+
+
+def test_reference_arm_line_contract():
+    """The reference arm's JSON line (the fp64 oracle on host cores) carries the
+    keys of the bench contract, names our arm's metric and workload, and marks
+    itself with impl, a cpu_baseline and an e2e without host-device bytes."""
+    class Args:
+        config, steps, warmup = 1, 2, 0
+    line = bench.bench_reference(Args())
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in line, key
+    assert line["metric"] == bench.METRIC and line["unit"] == "tokens/s" and line["higher_is_better"] is True
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["value"] > 0
+    assert line["config"]["workload"].startswith("c1_")
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
