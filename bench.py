@@ -3,17 +3,23 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
 
 One step = one pass of the whole operator over one workload: every chunk,
-every layer, K and V (one kernel launch through the C ABI).  The default
-workload is the Qwen2.5-VL-7B-shaped GQA video segment (28 layers, 4 KV heads x
-128, one 4096-token chunk, rank-32 patch, 16-token pages through a shuffled
-block table); --config picks another of the five measured workloads.
+every layer, K and V (one relocation kernel launch through the C ABI, preceded
+for a batch by the small copy launches that carry its plan).  The default
+workload is the largest: the sliding-window survival + recall batch of a
+Qwen2.5-VL-7B-shaped model (28 layers, 4 KV heads x 128; 8 requests x 32
+chunks x 1024 tokens, 224 chunks moved by R(delta) alone and 32 recalled with
+rank-64 patches; 16-token pages through shuffled block tables; one
+kv_relocate_batch launch).  --config picks another of the measured workloads
+(1: the single-chunk Qwen2.5-VL-shaped GQA video segment).
 
 Prints one JSON line: tokens/s (chunk tokens per second, all layers, K and V),
 the dominant kernel's roofline (algorithmic bytes / mean launch time against
-the measured HBM copy bandwidth), an end-to-end figure through the C ABI with
+the measured HBM copy bandwidth), a parity block on what the timed launches
+wrote (whole-output placement and byte-copy checks on the device, and sampled
+rows against the fp64 oracle), an end-to-end figure through the C ABI with
 host buffers (inputs copied in and results copied out every step), the fp64
-oracle timed on the host cores, and the SM clocks sampled during the timed
-region.  Under torchrun each rank runs its own replica of the workload (the
+oracle timed on the host cores (one core and all cores), and the SM clocks
+sampled during the timed region.  Under torchrun each rank runs its own replica of the workload (the
 path shards into independent chunks; there is no exchange step): weak scaling.
 """
 from __future__ import annotations
@@ -142,71 +148,212 @@ class ClockSampler:
 # CPU baseline: the fp64 oracle on a bounded sample, in a fresh process
 # --------------------------------------------------------------------------- #
 class OracleSampler:
-    """The fp64 oracle, as it stands, on rows of one (layer, tensor) slice of
-    the workload's first chunk; a step over n rows stands for n / (layers x
-    tensors) chunk tokens."""
+    """The fp64 oracle, as it stands, on token rows of one layer of the
+    workload: one representative chunk of each distinct rank (c4: a surviving
+    chunk at rank 0 and a recalled one at rank 64), each evaluated in
+    proportion to the workload's tokens of that kind.  A step over n rows of
+    one (layer, tensor) slice stands for n / (layers x tensors) chunk tokens."""
 
-    def __init__(self, cfg: int):
+    def __init__(self, cfg: int, seed_offset: int = 0):
         import workloads as W
         from oracle import operator_rows, round_to_bf16_bits, row_layout
         self._op, self._round = operator_rows, round_to_bf16_bits
         wl = W.config(cfg)
-        c = wl.chunks[0]
         self.wl = wl
+        kinds = {}
+        for c in wl.chunks:
+            kinds.setdefault(c.rank, [c, 0])[1] += c.n_tokens
+        chunks, row = [], 0
+        for c, _ in kinds.values():
+            chunks.append(W.Chunk(row, c.n_tokens, c.delta, c.rank, 0, row))
+            row += c.n_tokens
+        total = sum(t for _, t in kinds.values())
+        self.share = [t / total for _, t in kinds.values()]
         self.slice_wl = W.Workload(wl.name, wl.family, 1, wl.n_heads, wl.head_dim, wl.kv_lora_dim, wl.rope_dim,
-                                   wl.theta, c.n_tokens, wl.num_pages, wl.paged,
-                                   [W.Chunk(0, c.n_tokens, c.delta, c.rank, 0, 0)], wl.block_tables, wl.seed,
-                                   "numpy")
+                                   wl.theta, row, (row + W.PAGE - 1) // W.PAGE, False, chunks, None,
+                                   wl.seed + seed_offset, "numpy", mrope_sections=wl.mrope_sections)
         self.host = W.host_inputs(self.slice_wl)
         self.layouts = {n: row_layout(wl.family, n, n_heads=wl.n_heads, head_dim=wl.head_dim,
                                       kv_lora_dim=wl.kv_lora_dim, rope_dim=wl.rope_dim) for n in wl.tensors}
-        self.delta, self.theta, self.rank = c.delta, wl.theta, c.rank
-        self.n_tokens = c.n_tokens
         self.layer_tensors = wl.n_layers * len(wl.tensors)
+        self.n_tokens = max(c.n_tokens for c in chunks)
+        self.kinds = "; ".join(f"{share:.1%} of rows at rank {c.rank}" for c, share in zip(chunks, self.share))
         self.i = 0
 
-    def step(self, n_rows: int) -> float:
-        """Seconds of oracle time for n_rows rows (cycling through the slice)."""
+    def step(self, n_rows: int):
+        """(seconds of oracle time, rows evaluated) for about n_rows rows, split
+        over the chunk kinds by their share of the workload's tokens."""
         import numpy as np
-        toks = (self.i + np.arange(n_rows)) % self.n_tokens
-        self.i = int(toks[-1] + 1)
-        name = self.wl.tensors[self.i % len(self.wl.tensors)]
-        x = self.host["rows"][name][0, toks]
-        u = self.host["u"][name][0][0, toks] if self.rank else None
-        w = self.host["w"][name][0][0] if self.rank else None
-        t0 = time.perf_counter()
-        self._round(self._op(x, u, w, self.delta, self.theta, self.layouts[name]))
-        return time.perf_counter() - t0
+        secs, done = 0.0, 0
+        for ci, (c, share) in enumerate(zip(self.slice_wl.chunks, self.share)):
+            n = max(1, int(round(n_rows * share)))
+            toks = (self.i + np.arange(n)) % c.n_tokens
+            name = self.wl.tensors[self.i % len(self.wl.tensors)]
+            x = self.host["rows"][name][0, c.src_row0 + toks]
+            u = self.host["u"][name][ci][0, toks] if c.rank else None
+            w = self.host["w"][name][ci][0] if c.rank else None
+            t0 = time.perf_counter()
+            self._round(self._op(x, u, w, c.delta, self.wl.theta, self.layouts[name], self.wl.mrope_sections))
+            secs += time.perf_counter() - t0
+            done += n
+        self.i += 1 + n_rows
+        return secs, done
 
     def tokens(self, n_rows: int) -> float:
         return n_rows / self.layer_tensors
 
 
+def _oracle_rate(cfg: int, seconds: float, seed_offset: int, barrier=None, out=None):
+    """Rows/s of the oracle on one core for about `seconds` of wall time (after
+    an optional start barrier shared with the other cores' processes)."""
+    o = OracleSampler(cfg, seed_offset)
+    if barrier is not None:
+        barrier.wait()
+    t0 = time.perf_counter()
+    rows, busy = 0, 0.0
+    while time.perf_counter() - t0 < seconds:
+        s, n = o.step(o.n_tokens)
+        busy += s
+        rows += n
+    wall = time.perf_counter() - t0
+    res = (rows, wall, busy)
+    if out is not None:
+        out.put(res)
+    return res
+
+
 def cpu_baseline_worker(cfg: int, budget_s: float) -> dict:
-    """Times the oracle on whole (layer, tensor) slices until the budget is spent."""
+    """The oracle on one host core, then on every host core at once (one
+    process per core, started with spawn, all timed over the same window)."""
+    import multiprocessing as mp
     o = OracleSampler(cfg)
-    elapsed, rows = 0.0, 0
-    while elapsed < budget_s:
-        elapsed += o.step(o.n_tokens)
-        rows += o.n_tokens
-    return {"value": o.tokens(rows) / elapsed, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{rows // o.n_tokens} (layer, tensor) slices of {o.n_tokens} rows of {o.wl.name} "
-                      f"(fp64 NumPy, one thread, {elapsed:.1f} s); one chunk token = "
-                      f"{o.layer_tensors} such rows"}
+    cores = os.cpu_count() or 1
+    rows1, wall1, busy1 = _oracle_rate(cfg, budget_s / 2, 0)
+    one = o.tokens(rows1) / busy1
+    ctx = mp.get_context("spawn")
+    barrier, q = ctx.Barrier(cores), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_rate, args=(cfg, budget_s / 2, 1 + i, barrier, q)) for i in range(cores)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=600) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+    rows_all = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    every = o.tokens(rows_all) / wall
+    return {"value": every, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "single_core_value": one, "os_cpu_count": cores,
+            "sample": f"fp64 NumPy oracle on rows of one layer of {o.wl.name} ({o.kinds}); one chunk token = "
+                      f"{o.layer_tensors} such rows. value: {cores} processes, one per host core (os.cpu_count() = "
+                      f"{cores}), one BLAS thread each, {rows_all} rows in {wall:.1f} s of wall time; "
+                      f"single_core_value: one process, {rows1} rows in {busy1:.1f} s of oracle time"}
 
 
-def run_cpu_baseline(cfg: int, budget_s: float) -> dict:
+def parity_worker(path: str) -> dict:
+    """The parity rule of the oracle on output rows sampled from the device
+    (see collect_parity_sample): the report summed over every sampled row."""
+    import pickle
+    from oracle import conditioning, operator_rows, row_layout
+    from oracle.compare import parity_report
+    with open(path, "rb") as f:
+        groups = pickle.load(f)
+    total = {}
+    for g in groups:
+        lay = row_layout(g["family"], g["tensor"], n_heads=g["n_heads"], head_dim=g["head_dim"],
+                         kv_lora_dim=g["kv_lora_dim"], rope_dim=g["rope_dim"])
+        ref = operator_rows(g["x"], g["u"], g["w"], g["delta"], g["theta"], lay, g["sections"])
+        cond = conditioning(g["x"], g["u"], g["w"], g["delta"], g["theta"], lay, g["sections"])
+        r = parity_report(g["got"], ref, cond)
+        for k, v in r.items():
+            total[k] = max(total.get(k, 0), v) if k.startswith("max") else total.get(k, 0) + v
+    total["rows"] = sum(len(g["got"]) for g in groups)
+    return total
+
+
+def _worker_env() -> dict:
     env = dict(os.environ)
     for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[k] = "1"
     env["CUDA_VISIBLE_DEVICES"] = ""
-    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-worker",
-                          "--config", str(cfg), "--budget", str(budget_s)],
-                         capture_output=True, text=True, env=env, timeout=900)
+    return env
+
+
+def run_cpu_baseline(cfg: int, budget_s: float, parity_path: str = None) -> dict:
+    """Runs the CPU-baseline worker (and, given a sample file, the oracle's
+    parity check of the bench's own output) in a fresh process without a GPU."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-baseline-worker", "--config", str(cfg),
+           "--budget", str(budget_s)]
+    if parity_path:
+        cmd += ["--parity-sample", parity_path]
+    res = subprocess.run(cmd, capture_output=True, text=True, env=_worker_env(), timeout=1200)
     if res.returncode != 0:
         tail = res.stderr.strip().splitlines()[-1] if res.stderr.strip() else "no output"
         return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": "failed: " + tail}
     return json.loads(res.stdout.strip().splitlines()[-1])
+
+
+def collect_parity_sample(wl, dwl, path: str, n_groups: int = 512, per_group: int = 4, seed: int = 12345) -> int:
+    """Copies to the host, for randomly chosen (chunk, tensor, layer) groups of
+    a few tokens each, the inputs the oracle needs and the rows the device
+    wrote into the destination pools, and pickles them to `path`.  Returns the
+    number of rows.  No arithmetic of the operator happens here."""
+    import pickle
+    import numpy as np
+    import torch
+    rng = np.random.default_rng(seed)
+    dev = dwl.pools[wl.tensors[0]].device
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    groups = []
+    for _ in range(n_groups):
+        ci = int(rng.integers(len(wl.chunks)))
+        c = wl.chunks[ci]
+        name = wl.tensors[int(rng.integers(len(wl.tensors)))]
+        layer = int(rng.integers(wl.n_layers))
+        toks = np.unique(rng.integers(0, c.n_tokens, size=per_group))
+        ti = torch.as_tensor(toks, device=dev)
+        q = c.dst_start + toks
+        page = wl.block_tables[c.seq][q // 16] if wl.paged else q // 16
+        got = dwl.pools[name][layer, torch.as_tensor(page, device=dev), torch.as_tensor(q % 16, device=dev)]
+        groups.append({
+            "family": wl.family, "tensor": name, "n_heads": wl.n_heads, "head_dim": wl.head_dim,
+            "kv_lora_dim": wl.kv_lora_dim, "rope_dim": wl.rope_dim, "delta": c.delta, "theta": wl.theta,
+            "sections": wl.mrope_sections, "x": bits(dwl.rows[name][layer, c.src_row0 + ti]),
+            "u": bits(dwl.u[name][ci][layer, ti]) if c.rank else None,
+            "w": bits(dwl.w[name][ci][layer]) if c.rank else None, "got": bits(got)})
+    with open(path, "wb") as f:
+        pickle.dump(groups, f)
+    return sum(len(g["got"]) for g in groups)
+
+
+def device_properties(wl, dwl) -> dict:
+    """Checks of the whole output that hold at any size, evaluated on the
+    device one layer at a time: every slot no token targets keeps its sentinel
+    (and every targeted slot was written), and the values of unpatched GQA/MHA
+    chunks and the c_KV part of unpatched MLA rows are byte copies."""
+    import torch
+    import workloads as W
+    untouched = sum(int((p[l].view(torch.int16) == -1).all(dim=-1).sum())
+                    for p in dwl.pools.values() for l in range(wl.n_layers))
+    want_untouched = len(wl.tensors) * wl.n_layers * (wl.num_pages * W.PAGE - wl.n_chunk_tokens)
+    copies_ok, copied_rows = True, 0
+    plain = [c for c in wl.chunks if c.rank == 0]
+    if plain:
+        name = "kv" if wl.family == "mla" else "v"
+        cols = slice(0, wl.kv_lora_dim) if wl.family == "mla" else slice(None)
+        dev = dwl.pools[name].device
+        q = torch.cat([torch.arange(c.dst_start, c.dst_start + c.n_tokens) for c in plain]).to(dev)
+        seq = torch.cat([torch.full((c.n_tokens,), c.seq) for c in plain]).to(dev)
+        src = torch.cat([torch.arange(c.src_row0, c.src_row0 + c.n_tokens) for c in plain]).to(dev)
+        page = dwl.block_tables.long()[seq, q // 16] if wl.paged else q // 16
+        for l in range(wl.n_layers):
+            out = dwl.pools[name][l, page, q % 16, cols]
+            copies_ok &= bool(torch.equal(out.view(torch.int16), dwl.rows[name][l, src, cols].view(torch.int16)))
+        copied_rows = int(q.numel()) * wl.n_layers
+    return {"untouched_slots": untouched, "untouched_slots_expected": want_untouched,
+            "placement_ok": untouched == want_untouched, "byte_copy_rows": copied_rows, "byte_copies_ok": copies_ok}
 
 
 # --------------------------------------------------------------------------- #
@@ -236,7 +383,24 @@ def dist_env():
     return rank, world, local
 
 
+def bench_config(wl, world: int) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    nbytes = wl.algorithmic_bytes()
+    return {"workload": workload_text(wl), "tokens_per_step": wl.n_chunk_tokens,
+            "algorithmic_bytes_per_step": nbytes["total"],
+            "l2": f"inputs larger than L2 ({nbytes['total'] / 1e6:.0f} MB moved per step vs 129 MB L2)"
+            if nbytes["total"] > 2 * L2_BYTES else "L2-resident workload (smaller than L2)",
+            "parallelism": f"replicas x{world}"}
+
+
+def default_steps(wl, peak_gbs: float) -> int:
+    """Launches that keep the timed region near ten seconds at ~90% of peak."""
+    t = wl.algorithmic_bytes()["total"] / (0.9 * peak_gbs * 1e9)
+    return int(min(20000, max(20, 10.0 / max(t, 1e-6))))
+
+
 def bench_ours(args) -> dict:
+    import tempfile
     import torch
     import harness
     import workloads as W
@@ -261,6 +425,9 @@ def bench_ours(args) -> dict:
     stream = torch.cuda.current_stream()
     nbytes = wl.algorithmic_bytes()
     tokens = wl.n_chunk_tokens
+    peaks = measured_peaks()
+    steps = args.steps if args.steps else default_steps(wl, peaks["hbm_gbs"])
+    args.steps = steps
 
     def barrier():
         if world > 1:
@@ -269,6 +436,10 @@ def bench_ours(args) -> dict:
     # warm-up
     for _ in range(args.warmup):
         dwl.run(stream=stream)
+    torch.cuda.synchronize()
+    # the timed launches alone write the pools checked below
+    dwl.reset_pools()
+    dwl.status.zero_()
     torch.cuda.synchronize()
 
     # One event pair brackets the timed region; the launches inside it run back
@@ -280,53 +451,75 @@ def bench_ours(args) -> dict:
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             dwl.run(stream=stream)
         t1.record(stream)
         torch.cuda.synchronize()
         barrier()
     total_ms = t0.elapsed_time(t1)
-    mean_launch_ms = total_ms / args.steps      # every launch in the region is relocate_kernel
+    mean_launch_ms = total_ms / steps      # one step = the plan upload (batches) + relocate_kernel
     status = dwl.status_value()
 
     total_ms = max_over_ranks(total_ms, f"cuda:{local}")
-    ms_per_step = total_ms / args.steps
-    value = job_throughput(tokens, world, total_ms, args.steps)
+    ms_per_step = total_ms / steps
+    value = job_throughput(tokens, world, total_ms, steps)
+
+    # parity of what the timed launches wrote: properties of the whole output on
+    # the device, and sampled rows for the oracle (checked in the CPU-baseline
+    # process, the only place this script runs the oracle)
+    props = device_properties(wl, dwl)
+    parity_path = None
+    if rank == 0 and not args.no_cpu_baseline:
+        parity_path = os.path.join(tempfile.mkdtemp(prefix="kvrp_parity_"), "sample.pkl")
+        n_rows = collect_parity_sample(wl, dwl, parity_path)
 
     # end to end through the C ABI with host buffers: copy the step's inputs in
     # from pinned memory, run, copy the destination pools out, every step
     e2e = bench_e2e(dwl, wl, args, stream)
 
-    peaks = measured_peaks()
     achieved = nbytes["total"] / (mean_launch_ms / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
+    launches_per_step = 1 + (plan_pieces(wl) if len(wl.chunks) > 1 else 0)
     out = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_text(wl), "tokens_per_step": tokens,
-                   "algorithmic_bytes_per_step": nbytes["total"],
-                   "l2": f"inputs larger than L2 ({nbytes['total'] / 1e6:.0f} MB moved per step vs 129 MB L2)"
-                   if nbytes["total"] > 2 * L2_BYTES else "L2-resident workload (smaller than L2)",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(wl, world),
         "hbm_gbs": nbytes["total"] / (ms_per_step / 1e3) / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "kernel": "relocate_kernel", "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"
                      if peaks["source"] == "measured" else "fallback 6.8 TB/s",
                      "mean_launch_us": mean_launch_ms * 1e3,
-                     "launch_timing": "CUDA events around the whole timed region / launches"},
+                     "launch_timing": "CUDA events around the whole timed region / steps (a step of a batch "
+                                      "also holds its plan-upload copy kernels)"},
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": steps * launches_per_step,
         "clocks": clocks.summary(),
         "device_status": status,
         "patch_tflops": wl.patch_flops() / (mean_launch_ms / 1e3) / 1e12,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = run_cpu_baseline(args.config, args.budget)
+        cb = run_cpu_baseline(args.config, args.budget, parity_path)
+        par = cb.pop("parity", None)
+        out["cpu_baseline"] = cb
+        out["parity"] = dict(par or {"error": "parity check did not run"}, **props,
+                             of="the destination pools as the last timed launch left them (reset to a "
+                                "sentinel before the timed region)",
+                             rule="within 1 bf16 ulp of the fp64 oracle rounded once; a mismatch (> 1 ulp) "
+                                  "must stay within ulp(ref) + 2^-20 x the conditioning sum, else a violation")
+    else:
+        out["parity"] = props
     if world > 1:
         torch.distributed.destroy_process_group()
     return out if rank == 0 else None
+
+
+def plan_pieces(wl) -> int:
+    """Copy launches that carry a batch plan of this workload to the device
+    (31 KB of plan per launch)."""
+    import position_invariant_kv_gb300 as kvrp
+    return -(-kvrp.kv_relocate_batch_workspace_size(len(wl.chunks)) // (31 * 1024))
 
 
 def bench_e2e(dwl, wl, args, stream) -> dict:
@@ -407,23 +600,26 @@ def bench_reference(args) -> dict:
     if rank != 0:
         return None
     o = OracleSampler(args.config)
-    probe = o.step(256)
-    rows_per_s = 256 / max(probe, 1e-6)
+    probe, n_probe = o.step(256)
+    rows_per_s = n_probe / max(probe, 1e-6)
     per_step = max(8, min(o.n_tokens, int(rows_per_s * 100.0 / (args.steps + args.warmup))))
     for _ in range(args.warmup):
         o.step(per_step)
-    secs = 0.0
+    secs, rows = 0.0, 0
     for _ in range(args.steps):
-        secs += o.step(per_step)
-    value = o.tokens(per_step * args.steps) / secs
-    sample = (f"{per_step} rows per step of one (layer, tensor) slice of {o.wl.name}, fp64 NumPy, one thread; "
-              f"one chunk token = {o.layer_tensors} rows")
+        s_, n_ = o.step(per_step)
+        secs += s_
+        rows += n_
+    value = o.tokens(rows) / secs
+    sample = (f"{rows // args.steps} rows per step of one layer of {o.wl.name} ({o.kinds}), fp64 NumPy, one "
+              f"thread; one chunk token = {o.layer_tensors} rows")
     return {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": workload_text(o.wl), "tokens_per_step": o.tokens(per_step)},
+            "config": bench_config(o.wl, world),
             "impl": "reference",
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "os_cpu_count": os.cpu_count()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -787,15 +983,18 @@ def run_attn_cpu_baseline(budget_s: float) -> dict:
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0,
+                    help="timed steps; 0 (default) picks a count that keeps the timed region near ten seconds")
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=4,
+                    help="workload: 4 (default) is the sliding-window survival + recall batch, the largest")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling captures)")
     ap.add_argument("--budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--parity-sample", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--row", choices=["relocate", "patch_form", "attend"], default="relocate",
                     help="relocate: the reuse operator (the headline); patch_form: forming the patch factors; "
                          "attend: decode attention over relocated chunks without materialising them")
@@ -812,11 +1011,18 @@ def main():
         if args.row == "attend":
             print(json.dumps(attn_cpu_worker(args.budget)))
             return
-        worker = patch_cpu_worker if args.row == "patch_form" else cpu_baseline_worker
-        print(json.dumps(worker(args.config, args.budget)))
+        if args.row == "patch_form":
+            print(json.dumps(patch_cpu_worker(args.config, args.budget)))
+            return
+        out = cpu_baseline_worker(args.config, args.budget)
+        if args.parity_sample:
+            out["parity"] = parity_worker(args.parity_sample)
+        print(json.dumps(out))
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if not args.steps and (args.impl == "reference" or args.row != "relocate"):
+        args.steps = 20 if args.impl == "reference" else {"patch_form": 200, "attend": 2000}[args.row]
     if args.impl == "reference":
         for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
             os.environ[k] = "1"

@@ -3,9 +3,10 @@
 Shared by the GPU tests, bench.py and __graft_entry__.smoke().  It allocates
 device memory with torch (inputs, sentinel-filled destination pools, block
 tables, the batch workspace) and calls the library entry point that fits the
-workload: kv_relocate_patch for one GQA/MHA chunk, kv_relocate_patch_mla for
-MLA, kv_relocate_batch for several chunks.  No arithmetic of the operator
-happens here.
+workload: kv_relocate_patch (or _mrope) for one GQA/MHA chunk,
+kv_relocate_patch_mla for one MLA chunk, and for several chunks
+kv_relocate_batch, kv_relocate_batch_mrope or kv_relocate_batch_mla.  No
+arithmetic of the operator happens here.
 """
 from __future__ import annotations
 
@@ -47,7 +48,7 @@ class DeviceWorkload:
         self.reset_pools()
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.workspace = None
-        if wl.family == "gqa" and len(wl.chunks) > 1:
+        if len(wl.chunks) > 1:
             nbytes = kvrp.kv_relocate_batch_workspace_size(len(wl.chunks))
             self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
         self._chunks = self._chunk_args()
@@ -108,7 +109,13 @@ class DeviceWorkload:
     def run(self, stream=None):
         """One pass of the whole operator over the workload (one kernel launch)."""
         wl = self.wl
-        if wl.family == "mla":
+        if wl.family == "mla" and len(wl.chunks) > 1:
+            if self._batch_array is None:
+                self._batch_array = kvrp.mla_chunk_array(self.mla_batch_chunks())
+            kvrp.kv_relocate_batch_mla(self._batch_array, n_layers=wl.n_layers, kv_lora_dim=wl.kv_lora_dim,
+                                       rope_dim=wl.rope_dim, rope_theta=wl.theta, workspace=self.workspace,
+                                       d_status=self.status, stream=stream)
+        elif wl.family == "mla":
             a = self._chunks[0]
             kvrp.kv_relocate_patch_mla(
                 a["srcs"][0], n_layers=wl.n_layers, n_tokens=a["n_tokens"], kv_lora_dim=wl.kv_lora_dim,
@@ -135,6 +142,13 @@ class DeviceWorkload:
                 uv=a["u"][1], vv=a["w"][1], src_layer_stride=a["src_layer_stride"],
                 u_layer_stride=a["u_layer_stride"], v_layer_stride=a["w_layer_stride"],
                 d_status=self.status, stream=stream)
+        elif wl.mrope_sections is not None:
+            if self._batch_array is None:
+                self._batch_array = kvrp.chunk_array(self.batch_chunks())
+            kvrp.kv_relocate_batch_mrope(self._batch_array, [a["delta"] for a in self._chunks], n_layers=wl.n_layers,
+                                         n_kv_heads=wl.n_heads, head_dim=wl.head_dim,
+                                         mrope_section=wl.mrope_sections, rope_theta=wl.theta,
+                                         workspace=self.workspace, d_status=self.status, stream=stream)
         else:
             if self._batch_array is None:            # the chunks do not change: marshal them once
                 self._batch_array = kvrp.chunk_array(self.batch_chunks())
@@ -142,9 +156,18 @@ class DeviceWorkload:
                                    head_dim=wl.head_dim, rope_theta=wl.theta, workspace=self.workspace,
                                    d_status=self.status, stream=stream)
 
+    def mla_batch_chunks(self) -> list:
+        """The workload's chunks as kv_relocate_batch_mla descriptors."""
+        return [kvrp.MlaChunk(src=a["srcs"][0], n_tokens=a["n_tokens"], delta=a["delta"], dst=a["dst"][0],
+                              rank=a["rank"], u=a["u"][0], v=a["w"][0], src_layer_stride=a["src_layer_stride"],
+                              u_layer_stride=a["u_layer_stride"], v_layer_stride=a["w_layer_stride"])
+                for a in self._chunks]
+
     def batch_chunks(self) -> list:
-        """The workload's chunks as kv_relocate_batch descriptors."""
-        return [kvrp.Chunk(k_src=a["srcs"][0], v_src=a["srcs"][1], n_tokens=a["n_tokens"], delta=a["delta"],
+        """The workload's chunks as kv_relocate_batch descriptors (under M-RoPE
+        the .delta field is unused: the (t, h, w) shifts travel beside them)."""
+        return [kvrp.Chunk(k_src=a["srcs"][0], v_src=a["srcs"][1], n_tokens=a["n_tokens"],
+                           delta=0 if isinstance(a["delta"], tuple) else a["delta"],
                            k_dst=a["dst"][0], v_dst=a["dst"][1], rank=a["rank"], uk=a["u"][0], vk=a["w"][0],
                            uv=a["u"][1], vv=a["w"][1], src_layer_stride=a["src_layer_stride"],
                            u_layer_stride=a["u_layer_stride"], v_layer_stride=a["w_layer_stride"])

@@ -38,7 +38,8 @@
  *     (block tables: 4-byte aligned) and must stay valid until the stream work
  *     is done.  Strides and dst_start are in elements; strides must be
  *     multiples of 8 elements.
- *   - rank must be 0 or a multiple of 16 up to 128; head_dim must be 64 or
+ *   - rank must be 0 or a multiple of 8 up to 128 (the factor rows are then a
+ *     multiple of 16 bytes, as the TMA copies need); head_dim must be 64 or
  *     128; MLA rope_dim must be 64 and kv_lora_dim a multiple of 64.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
  *     Host-detected problems are returned as kvrp_status before anything is
@@ -167,21 +168,72 @@ typedef struct kvrp_chunk {
 
 /*
  * kv_relocate_batch -- many GQA/MHA chunks, each with its own delta and patch,
- * in ONE kernel launch (section 3, the three window operations: reorder under
- * an orbit patch, sliding-window survival with R(delta) alone, recall of an
- * evicted chunk with a fresh patch).
+ * in ONE relocation kernel launch (section 3, the three window operations:
+ * reorder under an orbit patch, sliding-window survival with R(delta) alone,
+ * recall of an evicted chunk with a fresh patch).
  *   chunks      host array of n_chunks descriptors (read before the call returns).
  *   workspace   device scratch of at least kv_relocate_batch_workspace_size(n_chunks)
  *               bytes, 256-byte aligned, owned by the caller.  The call writes the
- *               launch's descriptors there with one host-to-device copy on `stream`;
- *               do not reuse it for another purpose until the stream work is done.
- *               Two batch calls may share one workspace only on the same stream.
+ *               launch's descriptors there on `stream` (small copy kernels carry
+ *               them in their parameters, ahead of the relocation kernel); do not
+ *               reuse it for another purpose until the stream work is done.  Two
+ *               batch calls may share one workspace only on the same stream.
+ * The workspace size covers every batch call below (GQA/MHA, M-RoPE, MLA).
  */
 size_t kv_relocate_batch_workspace_size(int32_t n_chunks);
 
 kvrp_status kv_relocate_batch(
     const kvrp_chunk* chunks, int32_t n_chunks,
     int32_t n_layers, int32_t n_kv_heads, int32_t head_dim, double rope_theta,
+    void* workspace, size_t workspace_bytes,
+    uint32_t* d_status, kvrp_stream_t stream);
+
+/*
+ * kv_relocate_batch_mrope -- kv_relocate_batch under M-RoPE: a window of
+ * image or video chunks of a Qwen-VL-style model, each moved by its own
+ * (temporal, height, width) shift, in one launch (transplanted image KV is
+ * re-rotated with M-RoPE: gist.science/pt/paper/2606.17107, section 4; the
+ * window operations are those of Kamera, section 3).
+ *   delta_thw      host array [n_chunks][3]: chunk i turns frequency pair p by
+ *                  delta_thw[3i + s] * theta^(-2p/head_dim), s being the section
+ *                  of p; the chunks' own .delta fields are not read.
+ *   mrope_section  host array: frequency pairs per (t, h, w) section, summing to
+ *                  head_dim / 2 (Qwen2.5-VL with head_dim 128: {16, 24, 24}).
+ *   Everything else as kv_relocate_batch (same workspace size).
+ */
+kvrp_status kv_relocate_batch_mrope(
+    const kvrp_chunk* chunks, const int64_t* delta_thw, int32_t n_chunks,
+    int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+    const int32_t mrope_section[3], double rope_theta,
+    void* workspace, size_t workspace_bytes,
+    uint32_t* d_status, kvrp_stream_t stream);
+
+/* One MLA chunk of a batch: its own source rows, shift, patch and destination. */
+typedef struct kvrp_mla_chunk {
+  const void* src;            /* rows [n_layers][n_tokens][kv_lora_dim + rope_dim] = c_KV ++ k_rope */
+  int64_t src_layer_stride;
+  int32_t n_tokens;
+  int32_t rank;               /* 0 = relocation only (c_KV copied byte for byte)       */
+  int64_t delta;
+  const void* u;              /* U_m [L][T][m]; NULL iff rank 0                         */
+  const void* v;              /* V_m [L][kv_lora_dim + rope_dim][m]                     */
+  int64_t u_layer_stride;
+  int64_t v_layer_stride;
+  kvrp_dst dst;
+} kvrp_mla_chunk;
+
+/*
+ * kv_relocate_batch_mla -- many MLA chunks, each with its own delta and patch,
+ * in one launch: the window operations of Kamera section 3 (survival by
+ * R(delta) alone, recall with a fresh patch) on a DeepSeek-style cache, where
+ * only the k_rope tail of each row turns and c_KV is reused byte for byte
+ * (section 2, MLA bullet: survival needs only R(delta) for GQA and MLA alike).
+ *   Shapes and rules per chunk as kv_relocate_patch_mla; workspace as
+ *   kv_relocate_batch (kv_relocate_batch_workspace_size(n_chunks) bytes).
+ */
+kvrp_status kv_relocate_batch_mla(
+    const kvrp_mla_chunk* chunks, int32_t n_chunks, int32_t n_layers,
+    int32_t kv_lora_dim, int32_t rope_dim, double rope_theta,
     void* workspace, size_t workspace_bytes,
     uint32_t* d_status, kvrp_stream_t stream);
 
@@ -195,8 +247,9 @@ kvrp_status kv_relocate_batch(
  * cannot afford the device-wide synchronisation an allocation may cause.
  * This call takes the same chunks and does the same work in the same single
  * kernel launch, but keeps the launch's descriptors in a fixed array inside
- * the library instead of a caller workspace.  It calls no cudaMalloc,
- * cudaFree, cudaHostAlloc or other allocating routine.
+ * the library instead of a caller workspace (small copy kernels write them
+ * there from their parameters).  It calls no cudaMalloc, cudaFree,
+ * cudaHostAlloc or other allocating routine.
  *   Limits: at most KVRP_NOALLOC_MAX_CHUNKS chunks; more is rejected with
  *   KVRP_ERR_INVALID_ARG before any work.  The array (about 0.55 MB) lives on
  *   every GPU that loads the library, until the process exits.
@@ -364,6 +417,17 @@ kvrp_status kv_attend_relocated(
     int32_t n_seqs, int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim,
     double rope_theta, float softmax_scale, void* out,
     void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream);
+
+/*
+ * kvrp_test_set_wait_limit -- for tests of the failure path only.  Sets the
+ * limit, in SM clock cycles, of the relocation kernel's pipeline waits in the
+ * plans built from now on by any thread (0 restores the default of about one
+ * second).  With a limit of a few hundred cycles the waits give up almost at
+ * once: the launch then ORs KVRP_DEV_TIMEOUT into *d_status, lets its copies
+ * and tensor-core work drain, frees its TMEM and returns, leaving the output
+ * incomplete.  It never hangs the GPU, whatever the limit.
+ */
+void kvrp_test_set_wait_limit(uint32_t cycles);
 
 /* Human-readable name of a status code (static string). */
 const char* kvrp_status_string(kvrp_status status);

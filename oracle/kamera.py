@@ -7,7 +7,7 @@ composable-KV section 3.B of gist.science/pt/paper/2606.17107 ("Models take
 notes in prefill") confirms that keys are re-rotated to their new absolute
 positions while values, being position-free, are transplanted unchanged.
 
-Readings of points the pages leave open (each is listed in the design doc):
+Readings of points the pages leave open:
   * RoPE is the rotate-half convention: feature i of a rotated head pairs with
     feature i + d/2; the pair turns by phi_i = delta * theta_i with
     theta_i = theta_base ** (-2 i / d), i = 0 .. d/2 - 1, all in fp64.

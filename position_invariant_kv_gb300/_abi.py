@@ -20,7 +20,8 @@ KVRP_DEV_TIMEOUT = 0x2
 
 EXPORTED_SYMBOLS = (
     "kv_relocate_patch", "kv_relocate_patch_mrope", "kv_relocate_patch_mla", "kv_relocate_batch",
-    "kv_relocate_batch_workspace_size", "kv_relocate_batch_noalloc", "kv_patch_form_workspace_size",
+    "kv_relocate_batch_workspace_size", "kv_relocate_batch_noalloc", "kv_relocate_batch_mrope",
+    "kv_relocate_batch_mla", "kvrp_test_set_wait_limit", "kv_patch_form_workspace_size",
     "kv_patch_form", "kv_patch_form_orbit", "kv_attend_relocated_workspace_size", "kv_attend_relocated",
     "kvrp_status_string",
     "kvrp_last_error", "kvrp_version",
@@ -53,6 +54,12 @@ class kvrp_chunk(C.Structure):
                 ("k_dst", kvrp_dst), ("v_dst", kvrp_dst)]
 
 
+class kvrp_mla_chunk(C.Structure):
+    _fields_ = [("src", C.c_void_p), ("src_layer_stride", C.c_int64), ("n_tokens", C.c_int32),
+                ("rank", C.c_int32), ("delta", C.c_int64), ("u", C.c_void_p), ("v", C.c_void_p),
+                ("u_layer_stride", C.c_int64), ("v_layer_stride", C.c_int64), ("dst", kvrp_dst)]
+
+
 def _load_library():
     if not os.path.exists(lib_path):
         raise ImportError(
@@ -82,6 +89,16 @@ def _load_library():
     L.kv_relocate_batch.argtypes = [
         C.POINTER(kvrp_chunk), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double,
         C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
+    L.kv_relocate_batch_mrope.restype = st
+    L.kv_relocate_batch_mrope.argtypes = [
+        C.POINTER(kvrp_chunk), C.POINTER(C.c_int64), C.c_int32, C.c_int32, C.c_int32, C.c_int32,
+        C.POINTER(C.c_int32), C.c_double, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
+    L.kv_relocate_batch_mla.restype = st
+    L.kv_relocate_batch_mla.argtypes = [
+        C.POINTER(kvrp_mla_chunk), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double,
+        C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
+    L.kvrp_test_set_wait_limit.restype = None
+    L.kvrp_test_set_wait_limit.argtypes = [C.c_uint32]
     L.kv_relocate_batch_noalloc.restype = st
     L.kv_relocate_batch_noalloc.argtypes = [
         C.POINTER(kvrp_chunk), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double, C.c_void_p,
@@ -269,6 +286,68 @@ def kv_relocate_batch(chunks, *, n_layers: int, n_kv_heads: int, head_dim: int,
     _check(lib().kv_relocate_batch(
         arr, n, int(n_layers), int(n_kv_heads), int(head_dim), float(rope_theta),
         _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))
+
+
+def kv_relocate_batch_mrope(chunks, delta_thw, *, n_layers: int, n_kv_heads: int, head_dim: int,
+                            mrope_section, rope_theta: float, workspace, workspace_bytes: Optional[int] = None,
+                            d_status=None, stream=None) -> None:
+    """kv_relocate_batch under M-RoPE: chunk i turns by the (t, h, w) shift delta_thw[i]."""
+    arr, n = _as_array(chunks)
+    if len(delta_thw) != n:
+        raise ValueError("one (t, h, w) shift per chunk")
+    d = (C.c_int64 * max(3 * n, 3))(*[int(v) for t in delta_thw for v in t])
+    s3 = (C.c_int32 * 3)(*[int(v) for v in mrope_section])
+    if workspace_bytes is None:
+        workspace_bytes = int(workspace.numel() * workspace.element_size())
+    _check(lib().kv_relocate_batch_mrope(
+        arr, d, n, int(n_layers), int(n_kv_heads), int(head_dim), s3, float(rope_theta),
+        _ptr(workspace), int(workspace_bytes), _ptr(d_status), _stream(stream)))
+
+
+@dataclass
+class MlaChunk:
+    """One chunk of kv_relocate_batch_mla (fields as in struct kvrp_mla_chunk)."""
+    src: object
+    n_tokens: int
+    delta: int
+    dst: Dst
+    rank: int = 0
+    u: object = None
+    v: object = None
+    src_layer_stride: int = 0
+    u_layer_stride: int = 0
+    v_layer_stride: int = 0
+
+    def c(self) -> kvrp_mla_chunk:
+        return kvrp_mla_chunk(_ptr(self.src), int(self.src_layer_stride), int(self.n_tokens), int(self.rank),
+                              int(self.delta), _ptr(self.u), _ptr(self.v), int(self.u_layer_stride),
+                              int(self.v_layer_stride), self.dst.c())
+
+
+def mla_chunk_array(chunks: Sequence[MlaChunk]):
+    """The ctypes array of struct kvrp_mla_chunk for a list of MLA chunks."""
+    return (kvrp_mla_chunk * max(1, len(chunks)))(*[c.c() for c in chunks])
+
+
+def kv_relocate_batch_mla(chunks, *, n_layers: int, kv_lora_dim: int, rope_dim: int, rope_theta: float,
+                          workspace, workspace_bytes: Optional[int] = None, d_status=None, stream=None) -> None:
+    """Many MLA chunks, each with its own delta and patch, in one launch.
+    chunks: a list of MlaChunk, or an array made by mla_chunk_array()."""
+    if isinstance(chunks, C.Array):
+        arr, n = chunks, len(chunks)
+    else:
+        arr, n = mla_chunk_array(chunks), len(chunks)
+    if workspace_bytes is None:
+        workspace_bytes = int(workspace.numel() * workspace.element_size())
+    _check(lib().kv_relocate_batch_mla(
+        arr, n, int(n_layers), int(kv_lora_dim), int(rope_dim), float(rope_theta), _ptr(workspace),
+        int(workspace_bytes), _ptr(d_status), _stream(stream)))
+
+
+def kvrp_test_set_wait_limit(cycles: int) -> None:
+    """Testing hook: the relocation kernel's pipeline wait limit in cycles for
+    plans built from now on (0 = the default, about one second)."""
+    lib().kvrp_test_set_wait_limit(int(cycles))
 
 
 def kv_relocate_batch_noalloc(chunks, *, n_layers: int, n_kv_heads: int, head_dim: int,

@@ -17,7 +17,8 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libkvrp.so")
 SOURCES = [os.path.join(HERE, "csrc", "kvrp_kernel.cu"), os.path.join(HERE, "csrc", "kvrp_patch_form.cu"),
            os.path.join(HERE, "csrc", "kvrp_attend.cu"), os.path.join(HERE, "csrc", "kvrp_host.cpp")]
-HEADERS = [os.path.join(ROOT, "include", "kvrp.h"), os.path.join(HERE, "csrc", "kvrp_plan.h")]
+HEADERS = [os.path.join(ROOT, "include", "kvrp.h"), os.path.join(HERE, "csrc", "kvrp_plan.h"),
+           os.path.join(HERE, "csrc", "kvrp_ptx.h")]
 
 
 def nvcc_command(out: str = LIB, ptxas_verbose: bool = False) -> list:

@@ -51,7 +51,7 @@
 #include "kvrp_ptx.h"
 
 namespace kvrp {
-namespace at {
+namespace attn {
 
 using namespace kvrp::ptx;
 
@@ -721,7 +721,7 @@ size_t partial_bytes(int n_cta_max, int n_chunks, int Hq, int Hkv, int head_dim)
   return sizeof(float) * (size_t)slots * kConsumers * (Hq / Hkv) * (head_dim + 2);
 }
 
-}  // namespace at
+}  // namespace attn
 }  // namespace kvrp
 
 using namespace kvrp;
@@ -732,10 +732,10 @@ size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk
                                           int32_t n_kv_heads, int32_t head_dim) {
   if (n_chunks <= 0 || !chunk_tokens || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads || head_dim <= 0)
     return 0;
-  const int n_cta_max = std::min(at::kMaxCtas, at::kCtasPerSm * at::sm_count());
-  const size_t part = at::partial_bytes(n_cta_max, n_chunks, n_q_heads, n_kv_heads, head_dim);
+  const int n_cta_max = std::min(attn::kMaxCtas, attn::kCtasPerSm * attn::sm_count());
+  const size_t part = attn::partial_bytes(n_cta_max, n_chunks, n_q_heads, n_kv_heads, head_dim);
   const size_t qhl = (2 * 2 * (size_t)n_chunks * n_q_heads * head_dim + 255) / 256 * 256;
-  const size_t whl = (2 * 2 * (size_t)n_chunks * n_q_heads * at::kMaxRank + 255) / 256 * 256;
+  const size_t whl = (2 * 2 * (size_t)n_chunks * n_q_heads * attn::kMaxRank + 255) / 256 * 256;
   return part + qhl + whl + 256;
 }
 
@@ -744,14 +744,14 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
                                 int32_t head_dim, double rope_theta, float softmax_scale, void* out,
                                 void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream) {
   if (!q || !chunks || !seq_chunks || !out) return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: NULL argument");
-  if (n_chunks <= 0 || n_chunks > at::kMaxChunks)
-    return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: 1 <= n_chunks <= %d", at::kMaxChunks);
+  if (n_chunks <= 0 || n_chunks > attn::kMaxChunks)
+    return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: 1 <= n_chunks <= %d", attn::kMaxChunks);
   if (n_seqs <= 0 || n_seqs > 65535) return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: 1 <= n_seqs <= 65535");
   if (head_dim != 64 && head_dim != 128)
     return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: head_dim must be 64 or 128");
-  if (n_kv_heads <= 0 || n_q_heads <= 0 || n_q_heads % n_kv_heads || n_q_heads / n_kv_heads > at::kMaxGroup)
+  if (n_kv_heads <= 0 || n_q_heads <= 0 || n_q_heads % n_kv_heads || n_q_heads / n_kv_heads > attn::kMaxGroup)
     return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: n_q_heads must be a multiple of n_kv_heads, at most %d x",
-                at::kMaxGroup);
+                attn::kMaxGroup);
   if (!(rope_theta > 0.0) || !std::isfinite(rope_theta) || !(softmax_scale > 0.f) || !std::isfinite(softmax_scale))
     return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: rope_theta and softmax_scale must be > 0");
   if (!aligned16(q) || !aligned16(out)) return fail(KVRP_ERR_ALIGNMENT, "kv_attend_relocated: q, out not 16-byte aligned");
@@ -767,9 +767,9 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
     const kvrp_attn_chunk& c = chunks[i];
     if (c.n_tokens < 0) return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: chunk %d: n_tokens < 0", i);
     if (c.n_tokens > 0 && (!c.k || !c.v)) return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: chunk %d: NULL k/v", i);
-    if (c.rank < 0 || c.rank > at::kMaxRank || c.rank % 16)
+    if (c.rank < 0 || c.rank > attn::kMaxRank || c.rank % 16)
       return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: chunk %d: rank must be 0 or a multiple of 16 up to %d", i,
-                  at::kMaxRank);
+                  attn::kMaxRank);
     if (c.rank > 0 && (!c.uk || !c.vk || !c.uv || !c.vv))
       return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: chunk %d: rank > 0 needs all four factors", i);
     if ((c.k && !aligned16(c.k)) || (c.v && !aligned16(c.v)) || (c.uk && !aligned16(c.uk)) || (c.uv && !aligned16(c.uv)) ||
@@ -789,17 +789,17 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   if (!workspace || workspace_bytes < need)
     return fail(KVRP_ERR_WORKSPACE, "kv_attend_relocated: workspace of %zu bytes needed", need);
 
-  const at::Plan pl = at::make_plan(n_kv_heads, head_dim, m_max);
-  static_assert(sizeof(at::Params) <= 32000, "kernel parameter block too large");
-  at::Params* pp = new at::Params;   // ~20 KB: off the stack
-  std::memset(pp, 0, sizeof(at::Params));
-  at::Params& p = *pp;
+  const attn::Plan pl = attn::make_plan(n_kv_heads, head_dim, m_max);
+  static_assert(sizeof(attn::Params) <= 32000, "kernel parameter block too large");
+  attn::Params* pp = new attn::Params;   // ~20 KB: off the stack
+  std::memset(pp, 0, sizeof(attn::Params));
+  attn::Params& p = *pp;
   p.q = static_cast<const uint16_t*>(q);
   p.out = static_cast<uint16_t*>(out);
   p.status = d_status;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
   const size_t qhl_bytes = (2 * 2 * (size_t)n_chunks * n_q_heads * head_dim + 255) / 256 * 256;
-  const size_t whl_bytes = (2 * 2 * (size_t)n_chunks * n_q_heads * at::kMaxRank + 255) / 256 * 256;
+  const size_t whl_bytes = (2 * 2 * (size_t)n_chunks * n_q_heads * attn::kMaxRank + 255) / 256 * 256;
   p.qhl = reinterpret_cast<uint16_t*>(base);
   p.whl = reinterpret_cast<uint16_t*>(base + qhl_bytes);
   p.partial = reinterpret_cast<float*>(base + qhl_bytes + whl_bytes);
@@ -825,7 +825,7 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   for (int s = 0; s < n_seqs; ++s)
     for (int i = seq_chunks[s]; i < seq_chunks[s + 1]; ++i) {
       const kvrp_attn_chunk& c = chunks[i];
-      at::ChunkRec& r = p.c[i];
+      attn::ChunkRec& r = p.c[i];
       r.k = static_cast<const uint16_t*>(c.k);
       r.v = static_cast<const uint16_t*>(c.v);
       r.uk = static_cast<const uint16_t*>(c.uk);
@@ -845,25 +845,25 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   for (int s = 0; s <= n_seqs; ++s) p.seq_chunk[s] = seq_chunks[s];
 
   cudaStream_t st = stream;
-  void (*blk_fn)(at::Params) = nullptr;
+  void (*blk_fn)(attn::Params) = nullptr;
   const bool two = p.g > 8, big = m_max > 32;
   if (head_dim == 64)
-    blk_fn = two ? (big ? at::block_kernel<64, 2, 128> : at::block_kernel<64, 2, 32>)
-                 : (big ? at::block_kernel<64, 1, 128> : at::block_kernel<64, 1, 32>);
+    blk_fn = two ? (big ? attn::block_kernel<64, 2, 128> : attn::block_kernel<64, 2, 32>)
+                 : (big ? attn::block_kernel<64, 1, 128> : attn::block_kernel<64, 1, 32>);
   else
-    blk_fn = two ? (big ? at::block_kernel<128, 2, 128> : at::block_kernel<128, 2, 32>)
-                 : (big ? at::block_kernel<128, 1, 128> : at::block_kernel<128, 1, 32>);
+    blk_fn = two ? (big ? attn::block_kernel<128, 2, 128> : attn::block_kernel<128, 2, 32>)
+                 : (big ? attn::block_kernel<128, 1, 128> : attn::block_kernel<128, 1, 32>);
   const int smem = pl.stages * pl.stage_bytes;
   cudaError_t e = cudaFuncSetAttribute(blk_fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   int per_sm = 0;
-  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, blk_fn, at::kThreads, smem);
-  const int n_cta_max = std::min(at::kMaxCtas, at::kCtasPerSm * at::sm_count());
-  p.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)std::max(per_sm, 1) * at::sm_count(), (int64_t)n_cta_max,
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, blk_fn, attn::kThreads, smem);
+  const int n_cta_max = std::min(attn::kMaxCtas, attn::kCtasPerSm * attn::sm_count());
+  p.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)std::max(per_sm, 1) * attn::sm_count(), (int64_t)n_cta_max,
                                                          (int64_t)p.n_hg * p.s_hg}));
   if (e == cudaSuccess) {
     const size_t prep_smem = (size_t)head_dim * (m_max + 8) * 2 + sizeof(float) * p.g * head_dim;
-    e = cudaFuncSetAttribute(at::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
-    if (e == cudaSuccess) at::prep_kernel<<<dim3(n_chunks, n_kv_heads), 256, prep_smem, st>>>(p);
+    e = cudaFuncSetAttribute(attn::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
+    if (e == cudaSuccess) attn::prep_kernel<<<dim3(n_chunks, n_kv_heads), 256, prep_smem, st>>>(p);
     e = cudaGetLastError();
   }
   // prep -> block -> combine as programmatic dependent launches: each may start while
@@ -877,15 +877,15 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   cfg.numAttrs = 1;
   if (e == cudaSuccess && p.s_hg > 0) {
     cfg.gridDim = dim3(p.n_cta);
-    cfg.blockDim = dim3(at::kThreads);
+    cfg.blockDim = dim3(attn::kThreads);
     cfg.dynamicSmemBytes = smem;
     e = cudaLaunchKernelEx(&cfg, blk_fn, p);
   }
   if (e == cudaSuccess) {
     cfg.gridDim = dim3(n_seqs, n_q_heads);
-    cfg.blockDim = dim3(at::kCombineThreads);
+    cfg.blockDim = dim3(attn::kCombineThreads);
     cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, head_dim == 64 ? at::combine_kernel<64> : at::combine_kernel<128>, p);
+    e = cudaLaunchKernelEx(&cfg, head_dim == 64 ? attn::combine_kernel<64> : attn::combine_kernel<128>, p);
   }
   delete pp;
   if (e != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_attend_relocated: %s", cudaGetErrorString(e));

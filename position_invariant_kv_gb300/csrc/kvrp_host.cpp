@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -54,6 +55,7 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 std::map<int, DeviceInfo> g_dev;
+std::atomic<uint32_t> g_test_wait_limit{0};   // kvrp_test_set_wait_limit
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 kvrp_status device_info(DeviceInfo** out) {
@@ -178,8 +180,8 @@ kvrp_status check_dst(const kvrp_dst* d, const char* name, int64_t n_tokens, con
 
 kvrp_status check_chunk(const ChunkIn& c, const Shape& sh) {
   if (c.n_tokens < 0) return fail(KVRP_ERR_INVALID_ARG, "n_tokens is negative");
-  if (c.rank < 0 || c.rank > kMaxRank || c.rank % 16 != 0)
-    return fail(KVRP_ERR_UNSUPPORTED, "rank must be 0 or a multiple of 16 up to %d (got %d)", kMaxRank, c.rank);
+  if (c.rank < 0 || c.rank > kMaxRank || c.rank % 8 != 0)
+    return fail(KVRP_ERR_UNSUPPORTED, "rank must be 0 or a multiple of 8 up to %d (got %d)", kMaxRank, c.rank);
   if (c.n_tokens > (1 << 30)) return fail(KVRP_ERR_INVALID_ARG, "n_tokens too large");
   const int64_t rows = c.n_tokens;
   if (sh.n_layers > 1 && c.src_layer_stride < rows * sh.D)
@@ -394,7 +396,9 @@ class PlanBuilder {
       }
     }
     if (any_rot && c.n_tokens > 0) r.table = table(c.delta, c.sections);
-    m_max_ = std::max(m_max_, c.rank);
+    // shared memory and TMA boxes work in steps of 16 ranks; the boxes of a
+    // rank-8 tail reach past the factor's last column and read zeros there
+    m_max_ = std::max(m_max_, (c.rank + 15) / 16 * 16);
     chunks_.push_back(r);
     return KVRP_OK;
   }
@@ -410,6 +414,7 @@ class PlanBuilder {
     h.n_sub = (sh_.D + kSubCols - 1) / kSubCols;
     h.m_max = m_max_;
     h.status = status;
+    h.wait_cycles = test_wait_limit();
     // item granularity: whole rows unless that leaves SMs idle
     int64_t tiles = 0;
     for (const ChunkRec& r : chunks_)
@@ -490,17 +495,6 @@ class PlanBuilder {
     return KVRP_OK;
   }
 
-  // Upper bound of the serialised size for n chunks of up to two tensors.
-  static size_t bound(int64_t n) {
-    auto align = [](size_t v) { return (v + 127) & ~static_cast<size_t>(127); };
-    size_t off = align(sizeof(PlanHdr));
-    off = align(off + (size_t)n * 8 * sizeof(CUtensorMap));
-    off = align(off + (size_t)n * kTablePairs * sizeof(float4));
-    off = align(off + (size_t)n * sizeof(ChunkRec));
-    off = align(off + (size_t)2 * (n + 1) * sizeof(int32_t));
-    return off;
-  }
-
  private:
   Shape sh_;
   int m_max_ = 0;
@@ -512,11 +506,13 @@ class PlanBuilder {
 };
 
 // Builds the plan for `chunks` and launches it: as a kernel parameter when it
-// fits, otherwise through `workspace` (device) with one host-to-device copy.
+// fits, otherwise through `workspace` (device), carried there by upload_plan.
 kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d_status, void* workspace,
                 size_t workspace_bytes, cudaStream_t stream);
 
 }  // namespace
+
+uint32_t test_wait_limit() { return g_test_wait_limit.load(std::memory_order_relaxed); }
 
 kvrp_status current_device_sms(int* sms, int* smem_optin) {
   DeviceInfo* di = nullptr;
@@ -528,55 +524,6 @@ kvrp_status current_device_sms(int* sms, int* smem_optin) {
 }
 
 namespace {
-
-// Pinned staging for batch plans: a small ring per device, so consecutive
-// calls never overwrite a buffer whose copy is still queued.
-struct Staging {
-  struct Slot {
-    void* host = nullptr;
-    size_t cap = 0;
-    cudaEvent_t done = nullptr;
-    bool pending = false;
-  };
-  Slot slot[4];
-  int next = 0;
-};
-std::map<int, Staging> g_staging;
-
-kvrp_status stage_and_copy(const std::vector<unsigned char>& bytes, void* dst, cudaStream_t stream) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  std::lock_guard<std::mutex> lk(g_mu);
-  Staging& sg = g_staging[dev];
-  Staging::Slot& s = sg.slot[sg.next];
-  sg.next = (sg.next + 1) % 4;
-  if (s.pending) {
-    e = cudaEventSynchronize(s.done);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize(staging)");
-    s.pending = false;
-  }
-  if (!s.done) {
-    e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate");
-  }
-  if (s.cap < bytes.size()) {
-    if (s.host) cudaFreeHost(s.host);
-    s.host = nullptr;
-    s.cap = 0;
-    const size_t cap = std::max<size_t>(bytes.size(), 64 * 1024);
-    e = cudaHostAlloc(&s.host, cap, cudaHostAllocDefault);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(staging)");
-    s.cap = cap;
-  }
-  std::memcpy(s.host, bytes.data(), bytes.size());
-  e = cudaMemcpyAsync(dst, s.host, bytes.size(), cudaMemcpyHostToDevice, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan)");
-  e = cudaEventRecord(s.done, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord(staging)");
-  s.pending = true;
-  return KVRP_OK;
-}
 
 kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d_status, void* workspace,
                 size_t workspace_bytes, cudaStream_t stream) {
@@ -612,8 +559,8 @@ kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d
     if (bytes.size() > workspace_bytes)
       return fail(KVRP_ERR_WORKSPACE, "workspace holds %zu bytes, the plan needs %zu", workspace_bytes,
                   bytes.size());
-    st = stage_and_copy(bytes, workspace, stream);
-    if (st != KVRP_OK) return st;
+    e = upload_plan(bytes.data(), bytes.size(), workspace, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "plan upload");
     e = launch_relocate(nullptr, workspace, grid, smem, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -640,9 +587,9 @@ TensorIn tensor_in(const void* src, const void* u, const void* w, const kvrp_dst
 }
 
 // The allocation-free batch path: same plan and kernel as kv_relocate_batch,
-// but the plan goes to the library's fixed device array.  The copy reads a
-// pageable host buffer, which the runtime stages before cudaMemcpyAsync
-// returns, so nothing is allocated on the device or pinned on the host here.
+// but the plan goes to the library's fixed device array, carried there by the
+// same parameter-block copy kernels; nothing is allocated on the device or
+// pinned on the host.
 kvrp_status run_noalloc(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d_status,
                         cudaStream_t stream) {
   DeviceInfo* di = nullptr;
@@ -672,10 +619,90 @@ kvrp_status run_noalloc(const Shape& sh, const std::vector<ChunkIn>& chunks, uin
       di->prepared_smem = di->smem_optin;
     }
   }
-  e = cudaMemcpyAsync(scratch, bytes.data(), bytes.size(), cudaMemcpyHostToDevice, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(plan to fixed array)");
+  e = upload_plan(bytes.data(), bytes.size(), scratch, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "plan upload to the fixed array");
   e = launch_relocate(nullptr, scratch, grid, smem, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return KVRP_OK;
+}
+
+// Prefixes the last error with the index of the chunk it came from.
+kvrp_status chunk_error(int i, kvrp_status st) {
+  std::string msg = "chunk " + std::to_string(i) + ": " + g_last_error;
+  std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg.c_str());
+  return st;
+}
+
+kvrp_status check_gqa_shape(int32_t n_layers, int32_t n_kv_heads, int32_t head_dim, double rope_theta) {
+  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
+  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  return KVRP_OK;
+}
+
+kvrp_status check_mla_shape(int32_t n_layers, int32_t kv_lora_dim, int32_t rope_dim, double rope_theta) {
+  if (n_layers <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers must be > 0");
+  if (rope_dim != 64) return fail(KVRP_ERR_UNSUPPORTED, "rope_dim must be 64");
+  if (kv_lora_dim < 0 || kv_lora_dim % 64 != 0 || kv_lora_dim > 65536 - 64)
+    return fail(KVRP_ERR_UNSUPPORTED, "kv_lora_dim must be a multiple of 64");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  return KVRP_OK;
+}
+
+kvrp_status check_sections(const int32_t sec[3], int32_t head_dim) {
+  if (!sec) return fail(KVRP_ERR_INVALID_ARG, "mrope_section is required");
+  int64_t pairs = 0;
+  for (int i = 0; i < 3; ++i) {
+    if (sec[i] < 0) return fail(KVRP_ERR_INVALID_ARG, "mrope_section entries must be >= 0");
+    pairs += sec[i];
+  }
+  if (pairs != head_dim / 2)
+    return fail(KVRP_ERR_INVALID_ARG, "mrope_section must sum to head_dim / 2 = %d (got %lld)", head_dim / 2,
+                (long long)pairs);
+  return KVRP_OK;
+}
+
+// One GQA/MHA chunk of a batch: keys turn per head, values do not.
+ChunkIn gqa_chunk(const kvrp_chunk& k, int32_t head_dim) {
+  ChunkIn c;
+  c.n_tensors = 2;
+  c.t[0] = tensor_in(k.k_src, k.uk, k.vk, &k.k_dst, head_dim == 128 ? kRotHalf128 : kRotHalf64, 0);
+  c.t[1] = tensor_in(k.v_src, k.uv, k.vv, &k.v_dst, kRotNone, 0);
+  c.src_layer_stride = k.src_layer_stride;
+  c.u_layer_stride = k.u_layer_stride;
+  c.w_layer_stride = k.v_layer_stride;
+  c.n_tokens = k.n_tokens;
+  c.rank = k.rank;
+  set_plain_shift(&c, k.delta, head_dim);
+  return c;
+}
+
+// The checked chunk list of a GQA/MHA batch; under M-RoPE (delta_thw != NULL)
+// chunk i turns by the shifts delta_thw[3i .. 3i + 2] of the sections `sec`.
+kvrp_status gqa_batch(const kvrp_chunk* chunks, int32_t n_chunks, const Shape& sh, int32_t head_dim,
+                      const int64_t* delta_thw, const int32_t* sec, std::vector<ChunkIn>* out) {
+  out->resize(n_chunks);
+  for (int i = 0; i < n_chunks; ++i) {
+    ChunkIn& c = (*out)[i];
+    c = gqa_chunk(chunks[i], head_dim);
+    if (delta_thw) {
+      for (int j = 0; j < 3; ++j) {
+        c.delta[j] = delta_thw[3 * i + j];
+        c.sections[j] = sec[j];
+      }
+    }
+    const kvrp_status st = check_chunk(c, sh);
+    if (st != KVRP_OK) return chunk_error(i, st);
+  }
+  return KVRP_OK;
+}
+
+kvrp_status check_workspace(void* workspace, size_t workspace_bytes, int32_t n_chunks) {
+  if (!workspace) return fail(KVRP_ERR_WORKSPACE, "a batch call needs a device workspace");
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(KVRP_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  if (workspace_bytes < plan_bytes_bound(n_chunks))
+    return fail(KVRP_ERR_WORKSPACE, "workspace smaller than kv_relocate_batch_workspace_size(%d)", n_chunks);
   return KVRP_OK;
 }
 
@@ -692,10 +719,8 @@ kvrp_status kv_relocate_patch(const void* k_src, const void* v_src, int64_t src_
                               const void* vk, const void* uv, const void* vv, int64_t u_layer_stride,
                               int64_t v_layer_stride, const kvrp_dst* k_dst, const kvrp_dst* v_dst,
                               uint32_t* d_status, kvrp_stream_t stream) {
-  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
-  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
-  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  kvrp_status st = check_gqa_shape(n_layers, n_kv_heads, head_dim, rope_theta);
+  if (st != KVRP_OK) return st;
   if (!k_dst || !v_dst) return fail(KVRP_ERR_INVALID_ARG, "k_dst and v_dst are required");
   const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
   ChunkIn c;
@@ -708,7 +733,7 @@ kvrp_status kv_relocate_patch(const void* k_src, const void* v_src, int64_t src_
   c.n_tokens = n_tokens;
   c.rank = rank;
   set_plain_shift(&c, delta, head_dim);
-  kvrp_status st = check_chunk(c, sh);
+  st = check_chunk(c, sh);
   if (st != KVRP_OK) return st;
   return run(sh, {c}, d_status, nullptr, 0, stream);
 }
@@ -720,20 +745,12 @@ kvrp_status kv_relocate_patch_mrope(const void* k_src, const void* v_src, int64_
                                     const void* uv, const void* vv, int64_t u_layer_stride,
                                     int64_t v_layer_stride, const kvrp_dst* k_dst, const kvrp_dst* v_dst,
                                     uint32_t* d_status, kvrp_stream_t stream) {
-  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
-  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
-  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  kvrp_status st = check_gqa_shape(n_layers, n_kv_heads, head_dim, rope_theta);
+  if (st != KVRP_OK) return st;
   if (!k_dst || !v_dst) return fail(KVRP_ERR_INVALID_ARG, "k_dst and v_dst are required");
-  if (!delta_thw || !mrope_section) return fail(KVRP_ERR_INVALID_ARG, "delta_thw and mrope_section are required");
-  int64_t pairs = 0;
-  for (int i = 0; i < 3; ++i) {
-    if (mrope_section[i] < 0) return fail(KVRP_ERR_INVALID_ARG, "mrope_section entries must be >= 0");
-    pairs += mrope_section[i];
-  }
-  if (pairs != head_dim / 2)
-    return fail(KVRP_ERR_INVALID_ARG, "mrope_section must sum to head_dim / 2 = %d (got %lld)", head_dim / 2,
-                (long long)pairs);
+  if (!delta_thw) return fail(KVRP_ERR_INVALID_ARG, "delta_thw is required");
+  st = check_sections(mrope_section, head_dim);
+  if (st != KVRP_OK) return st;
   const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
   ChunkIn c;
   c.n_tensors = 2;
@@ -748,7 +765,7 @@ kvrp_status kv_relocate_patch_mrope(const void* k_src, const void* v_src, int64_
     c.delta[i] = delta_thw[i];
     c.sections[i] = mrope_section[i];
   }
-  kvrp_status st = check_chunk(c, sh);
+  st = check_chunk(c, sh);
   if (st != KVRP_OK) return st;
   return run(sh, {c}, d_status, nullptr, 0, stream);
 }
@@ -758,11 +775,8 @@ kvrp_status kv_relocate_patch_mla(const void* src, int64_t src_layer_stride, int
                                   double rope_theta, int32_t rank, const void* u, const void* v,
                                   int64_t u_layer_stride, int64_t v_layer_stride, const kvrp_dst* dst,
                                   uint32_t* d_status, kvrp_stream_t stream) {
-  if (n_layers <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers must be > 0");
-  if (rope_dim != 64) return fail(KVRP_ERR_UNSUPPORTED, "rope_dim must be 64");
-  if (kv_lora_dim < 0 || kv_lora_dim % 64 != 0 || kv_lora_dim > 65536 - 64)
-    return fail(KVRP_ERR_UNSUPPORTED, "kv_lora_dim must be a multiple of 64");
-  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
+  kvrp_status st = check_mla_shape(n_layers, kv_lora_dim, rope_dim, rope_theta);
+  if (st != KVRP_OK) return st;
   if (!dst) return fail(KVRP_ERR_INVALID_ARG, "dst is required");
   const Shape sh{n_layers, kv_lora_dim + rope_dim, rope_dim, rope_theta};
   ChunkIn c;
@@ -775,14 +789,14 @@ kvrp_status kv_relocate_patch_mla(const void* src, int64_t src_layer_stride, int
   c.n_tokens = n_tokens;
   c.rank = rank;
   set_plain_shift(&c, delta, rope_dim);
-  kvrp_status st = check_chunk(c, sh);
+  st = check_chunk(c, sh);
   if (st != KVRP_OK) return st;
   return run(sh, {c}, d_status, nullptr, 0, stream);
 }
 
 size_t kv_relocate_batch_workspace_size(int32_t n_chunks) {
   if (n_chunks <= 0) return 0;
-  return PlanBuilder::bound(n_chunks);
+  return plan_bytes_bound(n_chunks);
 }
 
 kvrp_status kv_relocate_batch(const kvrp_chunk* chunks, int32_t n_chunks, int32_t n_layers, int32_t n_kv_heads,
@@ -790,35 +804,62 @@ kvrp_status kv_relocate_batch(const kvrp_chunk* chunks, int32_t n_chunks, int32_
                               uint32_t* d_status, kvrp_stream_t stream) {
   if (n_chunks < 0 || (n_chunks > 0 && !chunks)) return fail(KVRP_ERR_INVALID_ARG, "bad chunk array");
   if (n_chunks == 0) return KVRP_OK;
-  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
-  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
-  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
-  if (!workspace) return fail(KVRP_ERR_WORKSPACE, "kv_relocate_batch needs a device workspace");
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(KVRP_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+  kvrp_status st = check_gqa_shape(n_layers, n_kv_heads, head_dim, rope_theta);
+  if (st != KVRP_OK) return st;
+  st = check_workspace(workspace, workspace_bytes, n_chunks);
+  if (st != KVRP_OK) return st;
   const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
+  std::vector<ChunkIn> in;
+  st = gqa_batch(chunks, n_chunks, sh, head_dim, nullptr, nullptr, &in);
+  if (st != KVRP_OK) return st;
+  return run(sh, in, d_status, workspace, workspace_bytes, stream);
+}
+
+kvrp_status kv_relocate_batch_mrope(const kvrp_chunk* chunks, const int64_t* delta_thw, int32_t n_chunks,
+                                    int32_t n_layers, int32_t n_kv_heads, int32_t head_dim,
+                                    const int32_t mrope_section[3], double rope_theta, void* workspace,
+                                    size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream) {
+  if (n_chunks < 0 || (n_chunks > 0 && (!chunks || !delta_thw))) return fail(KVRP_ERR_INVALID_ARG, "bad chunk array");
+  if (n_chunks == 0) return KVRP_OK;
+  kvrp_status st = check_gqa_shape(n_layers, n_kv_heads, head_dim, rope_theta);
+  if (st != KVRP_OK) return st;
+  st = check_sections(mrope_section, head_dim);
+  if (st != KVRP_OK) return st;
+  st = check_workspace(workspace, workspace_bytes, n_chunks);
+  if (st != KVRP_OK) return st;
+  const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
+  std::vector<ChunkIn> in;
+  st = gqa_batch(chunks, n_chunks, sh, head_dim, delta_thw, mrope_section, &in);
+  if (st != KVRP_OK) return st;
+  return run(sh, in, d_status, workspace, workspace_bytes, stream);
+}
+
+kvrp_status kv_relocate_batch_mla(const kvrp_mla_chunk* chunks, int32_t n_chunks, int32_t n_layers,
+                                  int32_t kv_lora_dim, int32_t rope_dim, double rope_theta, void* workspace,
+                                  size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream) {
+  if (n_chunks < 0 || (n_chunks > 0 && !chunks)) return fail(KVRP_ERR_INVALID_ARG, "bad chunk array");
+  if (n_chunks == 0) return KVRP_OK;
+  kvrp_status st = check_mla_shape(n_layers, kv_lora_dim, rope_dim, rope_theta);
+  if (st != KVRP_OK) return st;
+  st = check_workspace(workspace, workspace_bytes, n_chunks);
+  if (st != KVRP_OK) return st;
+  const Shape sh{n_layers, kv_lora_dim + rope_dim, rope_dim, rope_theta};
   std::vector<ChunkIn> in(n_chunks);
   for (int i = 0; i < n_chunks; ++i) {
-    const kvrp_chunk& k = chunks[i];
+    const kvrp_mla_chunk& k = chunks[i];
     ChunkIn& c = in[i];
-    c.n_tensors = 2;
-    c.t[0] = tensor_in(k.k_src, k.uk, k.vk, &k.k_dst, head_dim == 128 ? kRotHalf128 : kRotHalf64, 0);
-    c.t[1] = tensor_in(k.v_src, k.uv, k.vv, &k.v_dst, kRotNone, 0);
+    c.n_tensors = 1;
+    c.t[0] = tensor_in(k.src, k.u, k.v, &k.dst, kRotHalf64, kv_lora_dim);
+    c.t[1] = tensor_in(nullptr, nullptr, nullptr, nullptr, kRotNone, 0);
     c.src_layer_stride = k.src_layer_stride;
     c.u_layer_stride = k.u_layer_stride;
     c.w_layer_stride = k.v_layer_stride;
     c.n_tokens = k.n_tokens;
     c.rank = k.rank;
-    set_plain_shift(&c, k.delta, head_dim);
-    kvrp_status st = check_chunk(c, sh);
-    if (st != KVRP_OK) {
-      std::string msg = "chunk " + std::to_string(i) + ": " + g_last_error;
-      std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg.c_str());
-      return st;
-    }
+    set_plain_shift(&c, k.delta, rope_dim);
+    st = check_chunk(c, sh);
+    if (st != KVRP_OK) return chunk_error(i, st);
   }
-  if (workspace_bytes < PlanBuilder::bound(n_chunks))
-    return fail(KVRP_ERR_WORKSPACE, "workspace smaller than kv_relocate_batch_workspace_size(%d)", n_chunks);
   return run(sh, in, d_status, workspace, workspace_bytes, stream);
 }
 
@@ -830,33 +871,16 @@ kvrp_status kv_relocate_batch_noalloc(const kvrp_chunk* chunks, int32_t n_chunks
     return fail(KVRP_ERR_INVALID_ARG, "kv_relocate_batch_noalloc takes at most %d chunks (got %d)",
                 KVRP_NOALLOC_MAX_CHUNKS, n_chunks);
   if (n_chunks == 0) return KVRP_OK;
-  if (n_layers <= 0 || n_kv_heads <= 0) return fail(KVRP_ERR_INVALID_ARG, "n_layers and n_kv_heads must be > 0");
-  if (head_dim != 64 && head_dim != 128) return fail(KVRP_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
-  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(KVRP_ERR_INVALID_ARG, "rope_theta must be > 0");
-  if ((int64_t)n_kv_heads * head_dim > 65536) return fail(KVRP_ERR_UNSUPPORTED, "row too wide");
+  kvrp_status st = check_gqa_shape(n_layers, n_kv_heads, head_dim, rope_theta);
+  if (st != KVRP_OK) return st;
   const Shape sh{n_layers, n_kv_heads * head_dim, head_dim, rope_theta};
-  std::vector<ChunkIn> in(n_chunks);
-  for (int i = 0; i < n_chunks; ++i) {
-    const kvrp_chunk& k = chunks[i];
-    ChunkIn& c = in[i];
-    c.n_tensors = 2;
-    c.t[0] = tensor_in(k.k_src, k.uk, k.vk, &k.k_dst, head_dim == 128 ? kRotHalf128 : kRotHalf64, 0);
-    c.t[1] = tensor_in(k.v_src, k.uv, k.vv, &k.v_dst, kRotNone, 0);
-    c.src_layer_stride = k.src_layer_stride;
-    c.u_layer_stride = k.u_layer_stride;
-    c.w_layer_stride = k.v_layer_stride;
-    c.n_tokens = k.n_tokens;
-    c.rank = k.rank;
-    set_plain_shift(&c, k.delta, head_dim);
-    kvrp_status st = check_chunk(c, sh);
-    if (st != KVRP_OK) {
-      std::string msg = "chunk " + std::to_string(i) + ": " + g_last_error;
-      std::snprintf(g_last_error, sizeof(g_last_error), "%s", msg.c_str());
-      return st;
-    }
-  }
+  std::vector<ChunkIn> in;
+  st = gqa_batch(chunks, n_chunks, sh, head_dim, nullptr, nullptr, &in);
+  if (st != KVRP_OK) return st;
   return run_noalloc(sh, in, d_status, stream);
 }
+
+void kvrp_test_set_wait_limit(uint32_t cycles) { g_test_wait_limit.store(cycles, std::memory_order_relaxed); }
 
 const char* kvrp_status_string(kvrp_status status) {
   switch (status) {

@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 
@@ -270,6 +271,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = h.stages;
+  // limit of the pipeline waits below (the drains at the end keep the default:
+  // a copy or MMA in flight always completes, and must, before the CTA exits)
+  const long long wlim = h.wait_cycles ? (long long)h.wait_cycles : kTimeoutCycles;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -319,10 +323,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, uit = 0;
       bool ok = true;
+      // A plan in global memory was written by an earlier kernel: before this
+      // thread's first TMA use of each tensor map it acquires the map through
+      // the tensor-map proxy (maps in the parameter block need no fence).
+      int32_t acq_x = -1, acq_u = -1, acq_w = -1;
       for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
         const Item I = decode_item(plan, h, item);
         const int m = I.c->rank;
-        const int nkb = m >> 4;
+        const int nkb = (m + 15) >> 4;          // 16-rank MMA steps; a rank-8 tail box reads zeros
+        if (!kParamPlan) {
+          if (I.t->map_x != acq_x) tensormap_acquire(plan_map(plan, h, acq_x = I.t->map_x));
+          if (m > 0 && I.t->map_u != acq_u) tensormap_acquire(plan_map(plan, h, acq_u = I.t->map_u));
+          if (m > 0 && I.t->map_w != acq_w) tensormap_acquire(plan_map(plan, h, acq_w = I.t->map_w));
+        }
         if (h.tab_mode == kTabGlobal && item + (int)gridDim.x < h.n_items) {
           // warm L1 with the next item's phase table for the epilogue
           const Item N = decode_item(plan, h, item + (int)gridDim.x);
@@ -333,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (m > 0) {
           const int ub = (int)(uit % NU);
-          ok = wait_phase(bars.u_empty(ub), ((uit / NU) & 1) ^ 1, abort_flag, h.status);
+          ok = wait_phase(bars.u_empty(ub), ((uit / NU) & 1) ^ 1, abort_flag, h.status, wlim);
           if (!ok) break;
           const CUtensorMap* mu = plan_map(plan, h, I.t->map_u);
           mbar_expect_tx(bars.u_full(ub), (uint32_t)nkb * (kTileRows * 32));
@@ -346,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mw = m > 0 ? plan_map(plan, h, I.t->map_w) : nullptr;
         for (int s = I.s0; s < I.s1; ++s, ++it) {
           const int st = (int)(it % (uint32_t)S);
-          ok = wait_phase(bars.empty(st), ((it / S) & 1) ^ 1, abort_flag, h.status);
+          ok = wait_phase(bars.empty(st), ((it / S) & 1) ^ 1, abort_flag, h.status, wlim);
           if (!ok) break;
           const int width = min(kSubCols, h.D - kSubCols * s);
           const int nbox = width / kBoxCols;
@@ -389,20 +402,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
         const Item I = decode_item(plan, h, item);
         const int m = I.c->rank;
-        const int nkb = m >> 4;
+        const int nkb = (m + 15) >> 4;
         const int ub = (int)(uit % NU);
         if (m > 0) {
-          ok = wait_phase(bars.u_full(ub), (uit / NU) & 1, abort_flag, h.status);
+          ok = wait_phase(bars.u_full(ub), (uit / NU) & 1, abort_flag, h.status, wlim);
           if (!ok) break;
         }
         for (int s = I.s0; s < I.s1; ++s, ++it) {
           const int st = (int)(it % (uint32_t)S);
           // observe every stage use, patched or not, and take part in its release
-          ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
+          ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status, wlim);
           if (!ok) break;
           if (m > 0) {
             const int a = (int)(it % kEpiGroups);     // the slot of the group that owns this stage
-            ok = wait_phase(bars.acc_empty(a), (gcnt[a] & 1) ^ 1, abort_flag, h.status);
+            ok = wait_phase(bars.acc_empty(a), (gcnt[a] & 1) ^ 1, abort_flag, h.status, wlim);
             if (!ok) break;
             tc_fence_after();
             const int width = min(kSubCols, h.D - kSubCols * s);
@@ -441,10 +454,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int group = warp - 2 - kEpilogueWarps;
     uint32_t it = 0;
     bool ok = true;
+    int32_t acq_dst = -1;                    // last destination map this lane acquired (see the producer)
     for (int item = blockIdx.x; ok && item < h.n_items; item += gridDim.x) {
       const Item I = decode_item(plan, h, item);
       const TensorRec& T = *I.t;
       const CUtensorMap* md = plan_map(plan, h, T.map_dst);
+      if (!kParamPlan && T.map_dst != acq_dst) tensormap_acquire(plan_map(plan, h, acq_dst = T.map_dst));
       const int r_lo = max(0, -I.t0);
       const int r_hi = min(kTileRows, I.c->n_tokens - I.t0);
       const int p = lane;                                   // page of the tile this lane stores
@@ -457,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = I.s0; s < I.s1; ++s, ++it) {
         if ((int)(it % kEpiGroups) != group) continue;   // another group's sub-tile
         const int st = (int)(it % (uint32_t)S);
-        ok = wait_phase(bars.computed(st), (it / S) & 1, abort_flag, h.status);
+        ok = wait_phase(bars.computed(st), (it / S) & 1, abort_flag, h.status, wlim);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         if (whole) {
@@ -512,9 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = I.s0; s < I.s1; ++s, ++it) {
         if ((int)(it % kEpiGroups) != group) continue;   // another group's sub-tile
         const int st = (int)(it % (uint32_t)S);
-        bool ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status);
+        bool ok = wait_phase(bars.full(st), (it / S) & 1, abort_flag, h.status, wlim);
         if (ok && m > 0) {
-          ok = wait_phase(bars.acc_full(group), gait & 1, abort_flag, h.status);
+          ok = wait_phase(bars.acc_full(group), gait & 1, abort_flag, h.status, wlim);
           tc_fence_after();
         }
         ok = __all_sync(0xffffffffu, ok);     // TMEM loads below are warp-collective
@@ -591,14 +606,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // calls on a device share it.
 // ---------------------------------------------------------------------------
 namespace {
-constexpr size_t align128(size_t v) { return (v + 127) & ~static_cast<size_t>(127); }
-constexpr size_t kNoAllocScratchBytes =
-    align128(align128(align128(align128(align128(sizeof(PlanHdr)) +
-                                        (size_t)kNoAllocMaxChunks * 8 * sizeof(CUtensorMap)) +
-                               (size_t)kNoAllocMaxChunks * kTablePairs * sizeof(float4)) +
-                      (size_t)kNoAllocMaxChunks * sizeof(ChunkRec)) +
-             (size_t)(kNoAllocMaxChunks + 1) * sizeof(int32_t));
-
+// Sized for the largest plan a batch of KVRP_NOALLOC_MAX_CHUNKS chunks can
+// produce (the same bound kv_relocate_batch_workspace_size reports).
 static __device__ __align__(256) unsigned char g_noalloc_plan[kNoAllocScratchBytes];
 
 std::mutex g_noalloc_mu;
@@ -626,6 +635,40 @@ cudaError_t noalloc_scratch(void** ptr) {
   g_noalloc_ptr[dev] = p;
   *ptr = p;
   return cudaSuccess;
+}
+
+// ---------------------------------------------------------------------------
+// Plan upload.  A batch plan is carried to device memory in the parameter
+// blocks of small copy kernels (up to 31 KB each): the launch copies the bytes
+// when it is enqueued, so the host plan may be freed as soon as the call
+// returns, and no pinned staging buffer is needed.
+// ---------------------------------------------------------------------------
+namespace dev {
+constexpr uint32_t kPieceBytes = 31 * 1024;
+struct alignas(16) PlanPiece {
+  unsigned char bytes[kPieceBytes];
+};
+__global__ void __launch_bounds__(256) plan_copy_kernel(const __grid_constant__ PlanPiece piece,
+                                                         unsigned char* __restrict__ dst, uint32_t n_bytes) {
+  for (uint32_t i = threadIdx.x * 16u; i < n_bytes; i += blockDim.x * 16u)
+    *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(piece.bytes + i);
+}
+}  // namespace dev
+
+cudaError_t upload_plan(const void* host_bytes, size_t n_bytes, void* dev_plan, cudaStream_t stream) {
+  if (n_bytes % 16 != 0) return cudaErrorInvalidValue;
+  const unsigned char* src = static_cast<const unsigned char*>(host_bytes);
+  unsigned char* dst = static_cast<unsigned char*>(dev_plan);
+  dev::PlanPiece* piece = new dev::PlanPiece;   // 31 KB: off the stack
+  cudaError_t e = cudaSuccess;
+  for (size_t off = 0; off < n_bytes && e == cudaSuccess; off += dev::kPieceBytes) {
+    const uint32_t n = (uint32_t)std::min<size_t>(dev::kPieceBytes, n_bytes - off);
+    memcpy(piece->bytes, src + off, n);
+    dev::plan_copy_kernel<<<1, 256, 0, stream>>>(*piece, dst + off, n);
+    e = cudaGetLastError();
+  }
+  delete piece;
+  return e;
 }
 
 cudaError_t prepare_kernel(int smem_bytes) {

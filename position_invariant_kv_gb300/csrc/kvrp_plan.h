@@ -86,9 +86,22 @@ struct PlanHdr {
   // group: CTAs working side by side stream neighbouring chunks of one layer.
   uint32_t off_maps, off_tabs, off_chunks, off_tbeg;   // off_tbeg: int32 [n_tensors][n_chunks + 1] tile prefix sums
   uint32_t total_bytes;
+  uint32_t wait_cycles;                   // pipeline wait limit in cycles; 0 = the default (~1 s)
   uint32_t* status;                       // optional device status word
 };
 static_assert(sizeof(PlanHdr) <= 128, "header must fit in 128 bytes");
+
+// Upper bound of a serialised plan for n chunks of up to two tensors: header,
+// up to 8 tensor maps and one phase table per chunk, the chunk records and the
+// per-tensor tile prefix sums (n + 1 entries for each of two tensors).
+constexpr size_t plan_align(size_t v) { return (v + 127) & ~static_cast<size_t>(127); }
+constexpr size_t plan_bytes_bound(int64_t n) {
+  return plan_align(plan_align(plan_align(plan_align(plan_align(sizeof(PlanHdr)) +
+                                                     (size_t)n * 8 * sizeof(CUtensorMap)) +
+                                          (size_t)n * kTablePairs * 16) +
+                               (size_t)n * sizeof(ChunkRec)) +
+                    (size_t)2 * (size_t)(n + 1) * sizeof(int32_t));
+}
 
 // Shared-memory carve-up for a given rank bound and depth.
 constexpr int kTableBytes = kTablePairs * 16;   // one phase table: 64 float4
@@ -130,6 +143,11 @@ __host__ __device__ inline SmemLayout smem_layout(int m_max, int stages, int u_b
 cudaError_t launch_relocate(const void* param_plan, const void* dev_plan, int grid,
                             int smem_bytes, cudaStream_t stream);
 
+// Copies a serialised plan (host bytes, a multiple of 16) to device memory on
+// `stream` by small copy kernels whose parameter blocks carry the bytes, so no
+// host buffer has to outlive the call and nothing is staged or pinned.
+cudaError_t upload_plan(const void* host_bytes, size_t n_bytes, void* dev_plan, cudaStream_t stream);
+
 // Host helpers shared by the library's translation units.
 kvrp_status fail(kvrp_status st, const char* fmt, ...);
 bool aligned16(const void* p);
@@ -145,8 +163,13 @@ cudaError_t prepare_kernel(int smem_bytes);
 // Allocation-free batch path: the largest batch its fixed device array holds,
 // the array's size, and its device address on the current device (looked up
 // once per device with cudaGetSymbolAddress).
-constexpr int kNoAllocMaxChunks = 256;
+constexpr int kNoAllocMaxChunks = KVRP_NOALLOC_MAX_CHUNKS;
+constexpr size_t kNoAllocScratchBytes = plan_bytes_bound(kNoAllocMaxChunks);
 size_t noalloc_scratch_bytes();
 cudaError_t noalloc_scratch(void** ptr);
+
+// Wait limit (cycles) written into every relocation plan; 0 keeps the default.
+// Set only through kvrp_test_set_wait_limit, by tests of the failure path.
+uint32_t test_wait_limit();
 
 }  // namespace kvrp

@@ -38,16 +38,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait for the phase of `bar` with the given parity: gives up when
-// another warp has flagged an abort or after ~1 s (then flags one itself and
-// ORs KVRP_DEV_TIMEOUT into *status).
+// another warp has flagged an abort or after `limit` cycles (~1 s by default;
+// then flags one itself and ORs KVRP_DEV_TIMEOUT into *status).
 __device__ __noinline__ inline bool wait_phase(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                               uint32_t* status) {
+                                               uint32_t* status, long long limit = kTimeoutCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       if (status) atomicOr(status, KVRP_DEV_TIMEOUT);
       return false;
@@ -76,6 +76,12 @@ __device__ __forceinline__ void tma_store_3d(const void* map, uint32_t src, int 
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
                ::"l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(src)
                : "memory");
+}
+// Makes this thread's later TMA uses of the 128-byte tensor map at `map` (in
+// global memory, written by an earlier kernel) see its current contents rather
+// than a copy cached from before that write.
+__device__ __forceinline__ void tensormap_acquire(const void* map) {
+  asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(map) : "memory");
 }
 __device__ __forceinline__ void prefetch_l1(const void* p) { asm volatile("prefetch.global.L1 [%0];" ::"l"(p)); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

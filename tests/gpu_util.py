@@ -86,5 +86,31 @@ def sampled_compare(wl, dwl, n_rows=48, seed=0):
     return reports
 
 
+def layer_compare(wl, dwl, layer: int):
+    """Every element of one whole layer (every chunk, every tensor) against the
+    oracle, for workloads of any size: each chunk's inputs of that layer are
+    copied back from the device, the oracle evaluates them, and the rows the
+    device wrote are gathered through the block table."""
+    reports = {n: {} for n in wl.tensors}
+    for ci, c in enumerate(wl.chunks):
+        dev = dwl.rows[wl.tensors[0]].device
+        q = c.dst_start + np.arange(c.n_tokens)
+        page = wl.block_tables[c.seq][q // 16] if wl.paged else q // 16
+        pg, sl = torch.as_tensor(page, device=dev), torch.as_tensor(q % 16, device=dev)
+        for name in wl.tensors:
+            x = bits(dwl.rows[name][layer, c.src_row0:c.src_row0 + c.n_tokens])
+            u = w = None
+            if c.rank:
+                u = bits(dwl.u[name][ci][layer])
+                w = bits(dwl.w[name][ci][layer])
+            lay = row_layout(wl.family, name, n_heads=wl.n_heads, head_dim=wl.head_dim,
+                             kv_lora_dim=wl.kv_lora_dim, rope_dim=wl.rope_dim)
+            ref = operator_rows(x, u, w, c.delta, wl.theta, lay, wl.mrope_sections)
+            cond = conditioning(x, u, w, c.delta, wl.theta, lay, wl.mrope_sections)
+            g = bits(dwl.pools[name][layer, pg, sl])
+            reports[name] = merge(reports[name], parity_report(g, ref, cond))
+    return reports
+
+
 def bits(t: torch.Tensor) -> np.ndarray:
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

@@ -61,7 +61,10 @@ def test_rejects_bad_arguments_before_cuda(kvrp):
     assert _call(kvrp, k_src=0) == kvrp.KVRP_ERR_INVALID_ARG
     assert _call(kvrp, k_src=0x20008) == kvrp.KVRP_ERR_ALIGNMENT
     assert _call(kvrp, head_dim=96) == kvrp.KVRP_ERR_UNSUPPORTED
-    assert _call(kvrp, rank=8, uk=0x50000, vk=0x60000, uv=0x70000, vv=0x80000) == kvrp.KVRP_ERR_UNSUPPORTED
+    f = dict(uk=0x50000, vk=0x60000, uv=0x70000, vv=0x80000)
+    assert _call(kvrp, rank=12, **f) == kvrp.KVRP_ERR_UNSUPPORTED         # not a multiple of 8
+    assert _call(kvrp, rank=136, **f) == kvrp.KVRP_ERR_UNSUPPORTED        # above 128
+    assert _call(kvrp, rank=8, **f) == kvrp.KVRP_ERR_CUDA                 # accepted; no GPU here
     assert _call(kvrp, rank=16) == kvrp.KVRP_ERR_INVALID_ARG            # factors missing
     assert _call(kvrp, rank=0, uk=0x50000) == kvrp.KVRP_ERR_INVALID_ARG  # factors without rank
     assert _call(kvrp, n_tokens=-1) == kvrp.KVRP_ERR_INVALID_ARG
@@ -103,6 +106,36 @@ def test_mla_and_batch_argument_checks(kvrp):
         kvrp.kv_relocate_batch([ch, bad], n_layers=1, n_kv_heads=2, head_dim=128, rope_theta=1e4,
                                workspace=0x100000, workspace_bytes=ws, stream=0)
     assert e.value.status == kvrp.KVRP_ERR_INVALID_ARG and "chunk 1" in str(e.value)
+
+
+def test_mla_and_mrope_batch_argument_checks(kvrp):
+    d = kvrp.Dst(base=0x10000, num_pages=16, layer_stride=16 * 16 * 576)
+    ws = kvrp.kv_relocate_batch_workspace_size(2)
+    ch = kvrp.MlaChunk(src=0x20000, n_tokens=10, delta=-7, dst=d)
+    with pytest.raises(kvrp.KvrpError) as e:                    # rope_dim must be 64
+        kvrp.kv_relocate_batch_mla([ch, ch], n_layers=1, kv_lora_dim=512, rope_dim=32, rope_theta=1e4,
+                                   workspace=0x100000, workspace_bytes=ws, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_UNSUPPORTED
+    with pytest.raises(kvrp.KvrpError) as e:                    # workspace too small
+        kvrp.kv_relocate_batch_mla([ch, ch], n_layers=1, kv_lora_dim=512, rope_dim=64, rope_theta=1e4,
+                                   workspace=0x100000, workspace_bytes=ws - 1, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_WORKSPACE
+    bad = kvrp.MlaChunk(src=0x20000, n_tokens=10, delta=-7, dst=d, rank=16)   # rank without factors
+    with pytest.raises(kvrp.KvrpError) as e:
+        kvrp.kv_relocate_batch_mla([ch, bad], n_layers=1, kv_lora_dim=512, rope_dim=64, rope_theta=1e4,
+                                   workspace=0x100000, workspace_bytes=ws, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_INVALID_ARG and "chunk 1" in str(e.value)
+    g = kvrp.Chunk(k_src=0x20000, v_src=0x30000, n_tokens=10, delta=3,
+                   k_dst=kvrp.Dst(base=0x10000, num_pages=4), v_dst=kvrp.Dst(base=0x40000, num_pages=4))
+    with pytest.raises(kvrp.KvrpError) as e:                    # sections must cover head_dim / 2 pairs
+        kvrp.kv_relocate_batch_mrope([g, g], [(1, 2, 3), (4, 5, 6)], n_layers=1, n_kv_heads=2, head_dim=128,
+                                     mrope_section=(16, 24, 23), rope_theta=1e6, workspace=0x100000,
+                                     workspace_bytes=ws, stream=0)
+    assert e.value.status == kvrp.KVRP_ERR_INVALID_ARG
+    with pytest.raises(ValueError):                             # one shift triple per chunk
+        kvrp.kv_relocate_batch_mrope([g, g], [(1, 2, 3)], n_layers=1, n_kv_heads=2, head_dim=128,
+                                     mrope_section=(16, 24, 24), rope_theta=1e6, workspace=0x100000,
+                                     workspace_bytes=ws, stream=0)
 
 
 def test_no_gpu_means_cuda_error_not_fallback(kvrp):

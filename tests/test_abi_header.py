@@ -3,7 +3,7 @@
 Every prototype of the header is parsed and compared, argument by argument,
 with the ctypes argtypes and restype the binding declares: the same count, the
 same scalar widths (int32 / int64 / size_t / float / double), and a pointer
-wherever the header has one.  The three argument structs are compiled with the
+wherever the header has one.  The argument structs are compiled with the
 host C compiler, and their size and every field offset are compared with the
 ctypes Structures.  Nothing here needs a GPU."""
 import ctypes as C
@@ -27,7 +27,7 @@ def _prototypes():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
     out = {}
-    for m in re.finditer(r"(kvrp_status|size_t|const char\*|int32_t)\s+(k\w+)\s*\(([^;]*?)\)\s*;", text):
+    for m in re.finditer(r"(kvrp_status|size_t|const char\*|int32_t|void)\s+(k\w+)\s*\(([^;]*?)\)\s*;", text):
         ret, name, args = m.group(1), m.group(2), " ".join(m.group(3).split())
         params = [] if args in ("", "void") else [a.strip() for a in args.split(",")]
         out[name] = (ret, params)
@@ -62,11 +62,15 @@ def test_every_header_function_is_declared_alike_in_the_binding():
             if want[0] == "scalar":
                 assert C.sizeof(want[1]) == C.sizeof(got[1]), (name, i, p, t)
                 assert (want[1] in (C.c_float, C.c_double)) == (got[1] in (C.c_float, C.c_double)), (name, i, p, t)
+        if ret == "void":
+            assert fn.restype is None, name
+            continue
         rt = {"kvrp_status": C.c_int, "size_t": C.c_size_t, "const char*": C.c_char_p, "int32_t": C.c_int32}[ret]
         assert C.sizeof(fn.restype) == C.sizeof(rt) and (fn.restype is C.c_char_p) == (rt is C.c_char_p), name
 
 
-STRUCTS = {"kvrp_dst": abi.kvrp_dst, "kvrp_chunk": abi.kvrp_chunk, "kvrp_attn_chunk": abi.kvrp_attn_chunk}
+STRUCTS = {"kvrp_dst": abi.kvrp_dst, "kvrp_chunk": abi.kvrp_chunk, "kvrp_attn_chunk": abi.kvrp_attn_chunk,
+           "kvrp_mla_chunk": abi.kvrp_mla_chunk}
 
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs a host C compiler")

@@ -41,7 +41,50 @@ def test_reference_arm_line_contract():
     assert line["metric"] == bench.METRIC and line["unit"] == "tokens/s" and line["higher_is_better"] is True
     assert line["impl"] == "reference" and line["steps"] == 2 and line["value"] > 0
     assert line["config"]["workload"].startswith("c1_")
+    import workloads as W
+    assert line["config"] == bench.bench_config(W.config(1), 1)      # the same config object as our arm's
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["os_cpu_count"] >= 1
     assert line["e2e"] == {"value": line["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_oracle_sampler_weights_the_chunk_kinds_of_the_window_batch():
+    """c4 mixes 224 unpatched and 32 rank-64 chunks: the CPU baseline samples one
+    chunk of each kind, in proportion to their tokens."""
+    o = bench.OracleSampler(4)
+    ranks = [c.rank for c in o.slice_wl.chunks]
+    assert sorted(ranks) == [0, 64]
+    share = dict(zip(ranks, o.share))
+    assert share[0] == pytest.approx(224 / 256) and share[64] == pytest.approx(32 / 256)
+    secs, rows = o.step(64)
+    assert secs > 0 and rows == 56 + 8
+
+
+def test_parity_worker_reports_the_sampled_rows(tmp_path):
+    """The bench's in-run parity check: rows the oracle itself rounds pass with
+    no mismatch, and a row moved by 3 ulp counts as a mismatch and, outside the
+    conditioning bound, as a violation."""
+    import pickle
+    import numpy as np
+    import workloads as W
+    from oracle import operator_rows, round_to_bf16_bits, row_layout
+    wl = W.small_gqa(seed=5, n_layers=1, n_heads=2, head_dim=128, chunks_spec=((8, 1000, 16, 0),))
+    host = W.host_inputs(wl)
+    x, u, w = host["rows"]["k"][0], host["u"]["k"][0][0], host["w"]["k"][0][0]
+    ref = operator_rows(x, u, w, 1000, wl.theta, row_layout("gqa", "k", n_heads=2, head_dim=128))
+    got = round_to_bf16_bits(ref)
+    g = {"family": "gqa", "tensor": "k", "n_heads": 2, "head_dim": 128, "kv_lora_dim": 0, "rope_dim": 128,
+         "delta": 1000, "theta": wl.theta, "sections": None, "x": x, "u": u, "w": w, "got": got}
+    path = tmp_path / "s.pkl"
+    path.write_bytes(pickle.dumps([g]))
+    r = bench.parity_worker(str(path))
+    assert r["rows"] == 8 and r["n"] == 8 * 256 and r["mismatches"] == 0 and r["violations"] == 0
+    bad = got.copy()
+    big = np.argmax(np.abs(ref).ravel())
+    bad.ravel()[big] += 3
+    g["got"] = bad
+    path.write_bytes(pickle.dumps([g]))
+    r = bench.parity_worker(str(path))
+    assert r["mismatches"] == 1 and r["violations"] == 1 and r["max_ulp"] == 3

@@ -1,9 +1,10 @@
 """GPU parity at the full sizes of the five measured workloads, in the launch
-configuration bench.py times: sampled output rows against the fp64 oracle
-(whole layers for the Qwen2.5-VL-shaped GQA workload, whose inputs are drawn
-on the host), plus properties that hold at any size: every targeted slot is
-written and no other, values of unpatched chunks and MLA c_KV without a patch
-are byte copies, and the device status word stays clear."""
+configuration bench.py times: whole layers element by element against the
+fp64 oracle (for the device-drawn workloads the inputs of that layer are copied
+back for the oracle), sampled output rows of every layer, plus properties that
+hold at any size: every targeted slot is written and no other, values of
+unpatched chunks and MLA c_KV without a patch are byte copies, and the device
+status word stays clear.  Every report is printed with its counts."""
 import numpy as np
 import pytest
 import torch
@@ -56,7 +57,7 @@ def test_config1_qwen25vl_gqa_paged():
 
 
 def test_config2_llama2_mha_reorder_batch():
-    from gpu_util import sampled_compare
+    from gpu_util import layer_compare, sampled_compare
     wl = W.config(2)
     dwl = harness.DeviceWorkload(wl)
     dwl.run()
@@ -67,13 +68,16 @@ def test_config2_llama2_mha_reorder_batch():
     reps = sampled_compare(wl, dwl, n_rows=96, seed=2)
     print(reps)
     check(reps)
+    reps = layer_compare(wl, dwl, 0)                  # every element of layer 0: 8 chunks x 2048 tokens
+    print("layer 0:", reps)
+    check(reps)
     del dwl
     torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("rank", [32, 0])
 def test_config3_deepseek_mla(rank):
-    from gpu_util import sampled_compare
+    from gpu_util import layer_compare, sampled_compare
     wl = W.config(3)
     if rank == 0:
         wl.chunks = [W.Chunk(c.src_row0, c.n_tokens, c.delta, 0, c.seq, c.dst_start) for c in wl.chunks]
@@ -85,6 +89,9 @@ def test_config3_deepseek_mla(rank):
         assert k == expected_untouched(wl), n
     reps = sampled_compare(wl, dwl, n_rows=96, seed=3)
     print(reps)
+    check(reps)
+    reps = layer_compare(wl, dwl, 59)                 # every element of the last layer
+    print("layer 59:", reps)
     check(reps)
     if rank == 0:
         # c_KV copied byte for byte: gather every destination row through the block table
@@ -101,7 +108,7 @@ def test_config3_deepseek_mla(rank):
 
 
 def test_config4_window_survival_and_recall_batch():
-    from gpu_util import sampled_compare
+    from gpu_util import layer_compare, sampled_compare
     wl = W.config(4)
     dwl = harness.DeviceWorkload(wl)
     dwl.run()
@@ -111,6 +118,9 @@ def test_config4_window_survival_and_recall_batch():
         assert k == expected_untouched(wl), n
     reps = sampled_compare(wl, dwl, n_rows=128, seed=4)
     print(reps)
+    check(reps)
+    reps = layer_compare(wl, dwl, 0)                  # every element of layer 0: 256 chunks x 1024 tokens
+    print("layer 0:", reps)
     check(reps)
     # values of the 224 surviving (unpatched) chunks are byte copies
     surv = [c for c in wl.chunks if c.rank == 0]

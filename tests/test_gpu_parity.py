@@ -54,6 +54,10 @@ def test_config0_single_chunk_contiguous():
     (2, 3, 128, 256, 999, 48, 0, False, 1),       # contiguous, whole tiles, rank 48
     (1, 2, 128, 77, -123, 0, 3, False, 0),        # contiguous with an offset
     (2, 8, 128, 513, 32768, 64, 31, True, 4),     # several tiles, rank 64, D = 1024
+    (2, 2, 128, 131, -555, 8, 3, True, 2),        # rank 8: half of one 16-rank MMA step
+    (2, 3, 64, 77, 4321, 8, 0, False, 0),         # rank 8 with head_dim 64, an odd D / 64 = 3
+    (1, 4, 128, 300, 1000, 24, 5, True, 1),       # rank 24: one full step and a half
+    (1, 2, 128, 140, -98765, 120, 0, True, 0),    # rank 120: the largest rank below 128
 ], ids=lambda s: "L{}H{}d{}T{}m{}s{}{}".format(s[0], s[1], s[2], s[3], s[5], s[6], "p" if s[7] else "c"))
 def test_gqa_small(spec):
     from gpu_util import run_and_compare
@@ -68,7 +72,7 @@ def test_gqa_small(spec):
     assert dwl.status_value() == 0
 
 
-@pytest.mark.parametrize("rank,start,T", [(32, 0, 150), (0, 7, 150), (16, 9, 300)])
+@pytest.mark.parametrize("rank,start,T", [(32, 0, 150), (0, 7, 150), (16, 9, 300), (8, 1, 133), (40, 0, 64)])
 def test_mla_small(rank, start, T):
     from gpu_util import run_and_compare
     wl = W.small_mla(seed=300 + rank, n_layers=2, n_tokens=T, delta=-40000, rank=rank, dst_start=start,
@@ -199,4 +203,50 @@ def test_mrope_small(head_dim, sections, delta, rank, T):
     reps, got, want, dwl = run_and_compare(wl)
     print(reps)
     assert_parity(reps, strict=(rank == 0))
+    assert dwl.status_value() == 0
+
+
+def test_mla_batch_mixed_ranks_and_sequences():
+    """kv_relocate_batch_mla: MLA chunks with their own shifts and ranks (survivors
+    at rank 0, recalled chunks patched) across two sequences, in one launch."""
+    from gpu_util import run_and_compare
+    spec = ((150, -1024, 0, 0), (77, 31000, 32, 0), (200, -3072, 0, 1), (33, -5, 8, 1), (129, 65536, 16, 1))
+    wl = W.small_mla(seed=310, n_layers=3, chunks_spec=spec, dst_start=3, extra_pages=4)
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps)
+    assert dwl.status_value() == 0
+    # c_KV of the unpatched chunks is reused byte for byte
+    from oracle import placement
+    for c in wl.chunks:
+        if c.rank == 0:
+            pages, slots = placement(wl, c)
+            src = dwl.host["rows"]["kv"][:, c.src_row0:c.src_row0 + c.n_tokens, :512]
+            assert np.array_equal(got["kv"][:, pages, slots, :512], src)
+
+
+def test_mrope_batch_video_window():
+    """kv_relocate_batch_mrope: a window of video chunks, each moved by its own
+    (temporal, height, width) shift, some patched, in one launch."""
+    from gpu_util import run_and_compare
+    spec = ((256, (-1024, 0, 0), 0, 0), (130, (-2048, 333, 333), 32, 0), (77, (4096, -7, 12), 8, 1),
+            (300, (0, 0, 0), 0, 1), (64, (65000, -65000, 1), 16, 1))
+    wl = W.small_gqa(seed=960, n_layers=2, n_heads=2, head_dim=128, chunks_spec=spec, extra_pages=3,
+                     mrope_sections=(16, 24, 24))
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps)
+    assert dwl.status_value() == 0
+
+
+def test_batch_of_many_chunks_spans_several_plan_pieces():
+    """A 300-chunk batch: its launch plan is several times larger than one
+    parameter-block piece, so the plan reaches the device in several copy
+    launches; every chunk must still land exactly."""
+    from gpu_util import run_and_compare
+    spec = tuple((9 + (7 * i) % 41, (-1) ** i * (977 * i), (0, 8, 16, 0, 32)[i % 5], i % 4) for i in range(300))
+    wl = W.small_gqa(seed=970, n_layers=2, n_heads=1, head_dim=128, chunks_spec=spec, extra_pages=2)
+    reps, got, want, dwl = run_and_compare(wl)
+    print(reps)
+    assert_parity(reps)
     assert dwl.status_value() == 0

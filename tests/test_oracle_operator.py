@@ -51,6 +51,25 @@ def test_golden_placement():
     assert list(pages) == g["expect_pages"] and list(slots) == g["expect_slots"]
 
 
+def test_golden_conditioning():
+    """The conditioning sum S that widens the parity bar, against hand values:
+    too large an S would silently loosen every parity test, too small would
+    fail them, so both sides are pinned here."""
+    g = GOLD["conditioning"]
+    x, u, w = bits_of([g["x"]]), bits_of(g["u"]), bits_of(g["w"])
+    assert np.array_equal(bf16_bits_to_f64(x), np.array([g["x"]]))      # the hand inputs are exact in bf16
+    for tensor, key in (("k", "expect_k"), ("v", "expect_v")):
+        lay = row_layout("gqa", tensor, n_heads=1, head_dim=g["head_dim"])
+        s = conditioning(x, u, w, g["delta"], g["theta"], lay)
+        assert s.shape == (1, 4)
+        np.testing.assert_allclose(s[0], g[key], rtol=1e-13, atol=0)
+    # without a patch the sum keeps only the rotation terms
+    lay = row_layout("gqa", "k", n_heads=1, head_dim=g["head_dim"])
+    s0 = conditioning(x, None, None, g["delta"], g["theta"], lay)
+    patch = np.abs(np.array(g["u"])) @ np.abs(np.array(g["w"])).T
+    np.testing.assert_allclose(s0[0], np.array(g["expect_k"]) - patch[0], rtol=1e-13, atol=0)
+
+
 def _rand_bits(rng, shape, std=1.0):
     return bits_of(rng.standard_normal(shape) * std)
 

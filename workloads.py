@@ -202,14 +202,31 @@ def small_gqa(*, seed: int, n_layers=2, n_heads=2, head_dim=128, chunks_spec=((2
 
 
 def small_mla(*, seed: int, n_layers=2, n_tokens=150, delta=-999, rank=32, paged=True,
-              dst_start=0, theta=1e4, kv_lora_dim=512, rope_dim=64, extra_pages=0) -> Workload:
+              dst_start=0, theta=1e4, kv_lora_dim=512, rope_dim=64, extra_pages=0, chunks_spec=None) -> Workload:
+    """A host-sized MLA workload: one chunk (n_tokens, delta, rank at dst_start),
+    or, with chunks_spec = ((n_tokens, delta, rank, seq), ...), several chunks
+    packed one after another in each sequence."""
     rng = np.random.default_rng(seed)
-    pages = (dst_start + n_tokens + PAGE - 1) // PAGE
-    num_pages = pages + extra_pages
-    bt = rng.permutation(num_pages)[:pages].astype(np.int32)[None, :] if paged else None
+    if chunks_spec is None:
+        chunks_spec, starts = ((n_tokens, delta, rank, 0),), [dst_start]
+    else:
+        starts, pos = [], {}
+        for T, _, _, seq in chunks_spec:
+            starts.append(pos.get(seq, dst_start))
+            pos[seq] = starts[-1] + T
+    chunks, row = [], 0
+    for (T, d, m, seq), start in zip(chunks_spec, starts):
+        chunks.append(Chunk(row, T, d, m, seq, start))
+        row += T
+    n_seq = max(c.seq for c in chunks) + 1
+    pages = max((c.dst_start + c.n_tokens + PAGE - 1) // PAGE for c in chunks)
+    if paged:
+        num_pages = n_seq * pages + extra_pages
+        bt = rng.permutation(num_pages)[: n_seq * pages].astype(np.int32).reshape(n_seq, pages)
+    else:
+        num_pages, bt = pages + extra_pages, None
     return Workload("small_mla", "mla", n_layers, 1, rope_dim, kv_lora_dim, rope_dim, theta,
-                    n_tokens, num_pages, paged, [Chunk(0, n_tokens, delta, rank, 0, dst_start)],
-                    bt, seed, "numpy")
+                    row, num_pages, paged, chunks, bt, seed, "numpy")
 
 
 # --------------------------------------------------------------------------- #
