@@ -377,9 +377,21 @@ class PlanBuilder {
       tr.n_tblk = c.n_tokens > 0 ? (lead + c.n_tokens + kTileRows - 1) / kTileRows : 0;
       if (c.n_tokens == 0) continue;
       const uint64_t sls = c.src_layer_stride ? c.src_layer_stride : T * sh_.D;
-      kvrp_status st = map(ti.src, sh_.D, T, L, sh_.D, sls, kBoxCols, kTileRows,
-                           CU_TENSOR_MAP_SWIZZLE_128B, &tr.map_x);
-      if (st != KVRP_OK) return st;
+      // join the previous chunk's source group when these rows continue it
+      XGroup* g = groups_[t].empty() ? nullptr : &groups_[t].back();
+      const unsigned char* src = static_cast<const unsigned char*>(ti.src);
+      // (the group's rows of one layer must stay within one layer stride, so
+      // that every row the map spans belongs to one of its chunks)
+      if (g && src == g->base + g->rows * sh_.D * 2 && g->rows + T <= (1ull << 30) &&
+          (sh_.n_layers == 1 || (g->sls == sls && (g->rows + T) * sh_.D <= sls))) {
+        tr.x_row0 = static_cast<int32_t>(g->rows);
+        g->rows += T;
+      } else {
+        groups_[t].push_back(XGroup{src, sls, T});
+        tr.x_row0 = 0;
+      }
+      tr.map_x = static_cast<int32_t>(groups_[t].size() - 1);   // a group index until finish()
+      kvrp_status st;
       const uint64_t rows = static_cast<uint64_t>(ti.dst.num_pages) * kPage;
       const uint64_t dls = ti.dst.layer_stride ? ti.dst.layer_stride : rows * sh_.D;
       st = map(ti.dst.base, sh_.D, rows, L, sh_.D, dls, kBoxCols, kPage, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -406,6 +418,20 @@ class PlanBuilder {
   // Chooses the item granularity and pipeline depth and serialises the plan.
   kvrp_status finish(int sms, int smem_optin, uint32_t* status, std::vector<unsigned char>* out,
                      int* grid, int* smem_bytes) {
+    // one source map per group of consecutive chunks (see TensorRec::x_row0)
+    for (int t = 0; t < 2; ++t) {
+      std::vector<int32_t> gmap(groups_[t].size());
+      for (size_t i = 0; i < groups_[t].size(); ++i) {
+        const XGroup& g = groups_[t][i];
+        // one layer: the stride is never followed; keep it at least one layer of the group's rows
+        const uint64_t sls = sh_.n_layers == 1 ? std::max<uint64_t>(g.sls, g.rows * sh_.D) : g.sls;
+        const kvrp_status st = map(g.base, sh_.D, g.rows, static_cast<uint64_t>(sh_.n_layers), sh_.D, sls,
+                                   kBoxCols, kTileRows, CU_TENSOR_MAP_SWIZZLE_128B, &gmap[i]);
+        if (st != KVRP_OK) return st;
+      }
+      for (ChunkRec& r : chunks_)
+        if (t < r.n_tensors && r.n_tokens > 0) r.t[t].map_x = gmap[r.t[t].map_x];
+    }
     PlanHdr h;
     std::memset(&h, 0, sizeof(h));
     h.n_chunks = static_cast<int32_t>(chunks_.size());
@@ -503,6 +529,12 @@ class PlanBuilder {
   std::vector<float4> tabs_;
   std::map<TableKey, int32_t> tab_index_;
   std::vector<ChunkRec> chunks_;
+  struct XGroup {
+    const unsigned char* base;   // first row of the group's first chunk (layer 0)
+    uint64_t sls;                // layer stride, elements
+    uint64_t rows;               // rows of all the group's chunks
+  };
+  std::vector<XGroup> groups_[2];   // per tensor, in chunk order
 };
 
 // Builds the plan for `chunks` and launches it: as a kernel parameter when it

@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       bars.full(st));
           for (int j = 0; j < nbox; ++j)
             tma_load_3d(x_buf(st) + (uint32_t)j * (kTileRows * kBoxCols * 2), mx, bars.full(st),
-                        kSubCols * s + kBoxCols * j, I.t0, I.layer);
+                        kSubCols * s + kBoxCols * j, I.t->x_row0 + I.t0, I.layer);
           for (int k = 0; k < nkb; ++k)
             for (int j = 0; j < nbox; ++j)
               tma_load_3d(w_buf(st) + (uint32_t)k * (uint32_t)width * 32u + (uint32_t)j * (kBoxCols * 32),

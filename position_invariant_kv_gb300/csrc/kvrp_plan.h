@@ -54,8 +54,14 @@ struct TensorRec {             // one (chunk, tensor)
   int32_t rot_kind;
   int32_t rot_from;                       // first rotated feature (kRotHalf64)
   int32_t n_tblk;                         // token tiles of this tensor
-  int32_t pad_[2];
+  int32_t x_row0;                         // row of the chunk's token 0 in its source map (see below)
+  int32_t pad_;
 };
+// Source maps: chunks whose canonical rows follow one another in memory (same
+// layer stride, each starting where the previous one ends) share one tensor
+// map over all their rows, and a chunk addresses its rows from x_row0.  Tile
+// rows outside the chunk then read its neighbours' rows (or the map's zero
+// fill at the group's ends); they are loaded but never stored.
 
 struct ChunkRec {
   TensorRec t[2];
