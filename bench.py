@@ -433,19 +433,17 @@ def bench_ours(args) -> dict:
         if world > 1:
             torch.distributed.barrier()
 
-    # warm-up
-    for _ in range(args.warmup):
-        dwl.run(stream=stream)
-    torch.cuda.synchronize()
-    # the timed launches alone write the pools checked below
-    dwl.reset_pools()
-    dwl.status.zero_()
-    torch.cuda.synchronize()
-
     # One event pair brackets the timed region; the launches inside it run back
     # to back, as a caller's loop would issue them (an event recorded between two
     # launches would stop the next one's set-up from overlapping the previous one).
+    # The warm-up launches run right before it, once the clock sampler is up, so
+    # the GPU does not sit idle between them and the timed launches.
     with ClockSampler(local) as clocks:
+        for _ in range(args.warmup):
+            dwl.run(stream=stream)
+        # the timed launches alone write the pools checked below
+        dwl.reset_pools()
+        dwl.status.zero_()
         barrier()
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
@@ -475,7 +473,8 @@ def bench_ours(args) -> dict:
 
     # end to end through the C ABI with host buffers: copy the step's inputs in
     # from pinned memory, run, copy the destination pools out, every step
-    e2e = bench_e2e(dwl, wl, args, stream)
+    # (--e2e-steps 0 leaves it out: profiler captures only)
+    e2e = bench_e2e(dwl, wl, args, stream) if args.e2e_steps > 0 else None
 
     achieved = nbytes["total"] / (mean_launch_ms / 1e3) / 1e9
     traffic = profiled_traffic(wl.name)
@@ -989,7 +988,8 @@ def main():
     ap.add_argument("--config", type=int, default=4,
                     help="workload: 4 (default) is the sliding-window survival + recall batch, the largest")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="end-to-end steps (host copies in the loop); 0 skips that leg (profiler captures only)")
     ap.add_argument("--layers", type=int, default=0, help="use only the first N layers (profiling captures)")
     ap.add_argument("--budget", type=float, default=15.0, help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -648,10 +648,15 @@ constexpr uint32_t kPieceBytes = 31 * 1024;
 struct alignas(16) PlanPiece {
   unsigned char bytes[kPieceBytes];
 };
-__global__ void __launch_bounds__(256) plan_copy_kernel(const __grid_constant__ PlanPiece piece,
-                                                         unsigned char* __restrict__ dst, uint32_t n_bytes) {
-  for (uint32_t i = threadIdx.x * 16u; i < n_bytes; i += blockDim.x * 16u)
-    *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(piece.bytes + i);
+// The parameter block is read through the constant cache, which serves the
+// distinct addresses of a warp one after another; spreading a piece over
+// several CTAs (SMs) reads it in parallel.
+constexpr int kCopyCtas = 16, kCopyThreads = 128;
+static_assert(kCopyCtas * kCopyThreads * 16 >= (int)kPieceBytes, "one 16-byte word per thread");
+__global__ void __launch_bounds__(kCopyThreads) plan_copy_kernel(const __grid_constant__ PlanPiece piece,
+                                                                  unsigned char* __restrict__ dst, uint32_t n_bytes) {
+  const uint32_t i = (blockIdx.x * kCopyThreads + threadIdx.x) * 16u;
+  if (i < n_bytes) *reinterpret_cast<uint4*>(dst + i) = *reinterpret_cast<const uint4*>(piece.bytes + i);
 }
 }  // namespace dev
 
@@ -664,7 +669,8 @@ cudaError_t upload_plan(const void* host_bytes, size_t n_bytes, void* dev_plan, 
   for (size_t off = 0; off < n_bytes && e == cudaSuccess; off += dev::kPieceBytes) {
     const uint32_t n = (uint32_t)std::min<size_t>(dev::kPieceBytes, n_bytes - off);
     memcpy(piece->bytes, src + off, n);
-    dev::plan_copy_kernel<<<1, 256, 0, stream>>>(*piece, dst + off, n);
+    const int ctas = (int)((n + 16u * dev::kCopyThreads - 1) / (16u * dev::kCopyThreads));
+    dev::plan_copy_kernel<<<ctas, dev::kCopyThreads, 0, stream>>>(*piece, dst + off, n);
     e = cudaGetLastError();
   }
   delete piece;
