@@ -717,77 +717,111 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
 //    R^T R = G + s I (s = rel * trace G); out = R with its diagonal stored as
 //    1 / R_jj, zero outside the leading k x k block (apply_kernel's solve mode
 //    then forms X R^-1 by substitution, so R is never inverted).
-//    Right-looking, one barrier per column j; threads form a 16 x 16 grid over
-//    the trailing block and load everything they need for the step before they
-//    store (no load waits behind a store).  Row j of R goes to Rt (transposed),
-//    which nothing reads during the factorisation.
+//    Blocked right-looking factorisation over 16 x 16 blocks, in place in
+//    shared memory (entries past k hold the identity, which never couples to
+//    the leading block): warp 0 factors the diagonal block warp-synchronously,
+//    one thread per column solves the block row of R from it, and all threads
+//    apply the rank-16 update to the trailing matrix in 2 x 2 register tiles.
+//    Three CTA barriers per block instead of one per column.
 // ---------------------------------------------------------------------------
 template <int KP>
 __global__ void __launch_bounds__(kThreads) chol_kernel(float* G, int64_t sG, float* Rf, int64_t sR,
                                                                  int k, float rel) {
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
-  constexpr int kp = KP;
-  constexpr int kCholSpan = KP / 16;    // rows (and columns) of the trailing block per thread
-  extern __shared__ __align__(16) float smc[];
-  constexpr int P = kp + 1;
-  float* A = smc;              // trailing matrix
-  float* Rt = smc + kp * P;    // R transposed: Rt[c][j] = R[j][c]
+  constexpr int P = KP + 1;    // row pitch: neighbouring rows start in different banks
+  constexpr int NB = KP / 16;
+  __shared__ float A[KP * P];
   __shared__ float scratch[kThreads / 32];
-  __shared__ float rdiag[kMaxK];
+  __shared__ float rdiag[KP];
   float* g = G + (int64_t)blockIdx.x * sG;
   float* out = Rf + (int64_t)blockIdx.x * sR;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   float tr = 0.f;
-  for (int i = ty; i < kp; i += 16)
-    for (int j = tx; j < kp; j += 16) {
-      const float v = (i < k && j < k) ? 0.5f * (g[i * kp + j] + g[j * kp + i]) : 0.f;
-      A[i * P + j] = v;
-      Rt[i * P + j] = 0.f;
-      if (i == j) tr += v;
-    }
+  for (int e = tid; e < KP * KP; e += kThreads) {
+    const int i = e / KP, j = e - i * KP;
+    const float v = (i < k && j < k) ? 0.5f * (g[i * KP + j] + g[j * KP + i]) : (i == j ? 1.f : 0.f);
+    A[i * P + j] = v;
+    if (i == j && i < k) tr += v;
+  }
   tr = block_sum(tr, scratch);   // (its barriers: every thread has read G)
-  for (int e = tid; e < kp * kp; e += kThreads) g[e] = 0.f;   // zeroed for the next Gram
+  for (int e = tid; e < KP * KP; e += kThreads) g[e] = 0.f;   // zeroed for the next Gram
   const float shift = tr > 0.f ? rel * tr : 1e-30f;
   if (tid < k) A[tid * P + tid] += shift;
   __syncthreads();
-  for (int j = 0; j < k; ++j) {
-    const float d = fmaxf(A[j * P + j], shift);   // row j of A is final after the previous step
-    const float rs = rsqrtf(d);                   // 1 / R_jj
-    const float inv2 = rs * rs;
-    if (tid < k - j) {
-      const float v = tid == 0 ? d * rs : A[j * P + j + tid] * rs;
-      Rt[(j + tid) * P + j] = v;
-      if (tid == 0) rdiag[j] = rs;
-    }
-    float ajr[kCholSpan], ajc[kCholSpan], old[kCholSpan][kCholSpan];
+  for (int b = 0; b < NB; ++b) {
+    const int o = 16 * b;
+    if (warp == 0) {
+      // diagonal block in registers: lane l holds column l of the block (lanes
+      // 16 .. 31 repeat lanes 0 .. 15 and store nothing); its upper triangle
+      // becomes R_bb, row j of R coming from lane j's column by shuffles
+      const int l = lane & 15;
+      float col[16];
 #pragma unroll
-    for (int a = 0; a < kCholSpan; ++a) {
-      const int r = j + 1 + ty + 16 * a, c = j + 1 + tx + 16 * a;
-      ajr[a] = r < k ? A[j * P + r] * inv2 : 0.f;
-      ajc[a] = c < k ? A[j * P + c] : 0.f;
-    }
+      for (int r = 0; r < 16; ++r) col[r] = A[(o + r) * P + o + l];
 #pragma unroll
-    for (int a = 0; a < kCholSpan; ++a)
+      for (int j = 0; j < 16; ++j) {
+        const float d = fmaxf(__shfl_sync(0xffffffffu, col[j], j), shift);
+        const float rs = rsqrtf(d);
+        col[j] = l > j ? col[j] * rs : (l == j ? d * rs : col[j]);   // R[j][l]
 #pragma unroll
-      for (int b = 0; b < kCholSpan; ++b) {
-        const int r = j + 1 + ty + 16 * a, c = j + 1 + tx + 16 * b;
-        old[a][b] = (r < k && c < k && c >= r) ? A[r * P + c] : 0.f;
+        for (int r = 1; r < 16; ++r) {   // r > j; a fixed trip count keeps col[] in registers
+          if (r <= j) continue;
+          const float rjr = __shfl_sync(0xffffffffu, col[j], r);     // R[j][r], from lane r
+          if (l >= r) col[r] = fmaf(-rjr, col[j], col[r]);
+        }
+        if (lane == j) rdiag[o + j] = rs;
       }
 #pragma unroll
-    for (int a = 0; a < kCholSpan; ++a)
+      for (int r = 0; r < 16; ++r)
+        if (lane < 16 && l >= r) A[(o + r) * P + o + l] = col[r];
+    }
+    __syncthreads();
+    const int nt = KP - o - 16;                              // columns right of the block
+    if (tid < nt) {
+      // block row of R: R_bb^T x = A[o .. o + 16)[c], forward substitution
+      const int c = o + 16 + tid;
+      float x[16];
 #pragma unroll
-      for (int b = 0; b < kCholSpan; ++b) {
-        const int r = j + 1 + ty + 16 * a, c = j + 1 + tx + 16 * b;
-        if (r < k && c < k && c >= r) A[r * P + c] = old[a][b] - ajr[a] * ajc[b];
+      for (int i = 0; i < 16; ++i) x[i] = A[(o + i) * P + c];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float v = x[i];
+#pragma unroll
+        for (int j = 0; j < 15; ++j)
+          if (j < i) v = fmaf(-A[(o + j) * P + o + i], x[j], v);
+        x[i] = v * rdiag[o + i];
       }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) A[(o + i) * P + c] = x[i];
+    }
+    __syncthreads();
+    // trailing update A[r][c] -= sum_i R[o+i][r] R[o+i][c], r, c >= o + 16 (both triangles)
+    const int h = nt / 2;
+    for (int t = tid; t < h * h; t += kThreads) {
+      const int r = o + 16 + 2 * (t / h), c = o + 16 + 2 * (t % h);
+      float a00 = A[r * P + c], a01 = A[r * P + c + 1], a10 = A[(r + 1) * P + c], a11 = A[(r + 1) * P + c + 1];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float* row = A + (o + i) * P;
+        const float u0 = row[r], u1 = row[r + 1], v0 = row[c], v1 = row[c + 1];
+        a00 = fmaf(-u0, v0, a00);
+        a01 = fmaf(-u0, v1, a01);
+        a10 = fmaf(-u1, v0, a10);
+        a11 = fmaf(-u1, v1, a11);
+      }
+      A[r * P + c] = a00;
+      A[r * P + c + 1] = a01;
+      A[(r + 1) * P + c] = a10;
+      A[(r + 1) * P + c + 1] = a11;
+    }
     __syncthreads();
   }
-  __syncthreads();
   // R row by row, its diagonal stored as 1 / R_jj (zero outside the leading k x k block)
-  for (int i = ty; i < kp; i += 16)
-    for (int j = tx; j < kp; j += 16)
-      out[i * kp + j] = (i < k && j < k && j >= i) ? (i == j ? rdiag[i] : Rt[j * P + i]) : 0.f;
+  for (int e = tid; e < KP * KP; e += kThreads) {
+    const int i = e / KP, j = e - i * KP;
+    out[e] = (i < k && j < k && j >= i) ? (i == j ? rdiag[i] : A[i * P + j]) : 0.f;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1208,7 +1242,7 @@ class Runner {
     }
   }
 
-  size_t chol_smem() const { return sizeof(float) * 2 * (size_t)kp_ * (kp_ + 1); }
+  size_t chol_smem() const { return 0; }   // chol_kernel's shared memory is static
 
   void chol(float* g, float* rfac, int k, float rel) {
     if (err != cudaSuccess) return;
@@ -1228,14 +1262,7 @@ class Runner {
 
   static cudaError_t configure() {
     cudaError_t e = cudaSuccess;
-    const int chol = (int)(sizeof(float) * 2 * kMaxK * (kMaxK + 1));
     const int jac = (int)(sizeof(float) * 2 * kMaxK * (kMaxK + 1));
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<48>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<80>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(chol_kernel<96>, cudaFuncAttributeMaxDynamicSharedMemorySize, chol);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(jacobi_kernel<kJacThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, jac);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem_bytes(kMaxK));
