@@ -435,6 +435,12 @@ const char* kvrp_status_string(kvrp_status status);
 /* Text of the last error seen by this host thread (static per thread). */
 const char* kvrp_last_error(void);
 
+/* Kernel launches that this host thread's last relocation call (kv_relocate_*)
+ * enqueued: the relocation kernel, plus for a batch the small copy launches
+ * that carry its launch plan to the device (31 KB of plan each).  0 when the
+ * call returned an error or had nothing to move. */
+int32_t kvrp_last_launch_count(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 int32_t kvrp_version(void);
 

@@ -27,7 +27,7 @@ from ._abi import (  # noqa: F401
     KVRP_ERR_UNSUPPORTED, KVRP_ERR_CUDA, KVRP_ERR_WORKSPACE,
     Dst, Chunk, KvrpError, lib, lib_path,
     kv_relocate_patch, kv_relocate_patch_mrope, kv_relocate_patch_mla, kv_relocate_batch, kv_relocate_batch_workspace_size,
-    kvrp_status_string, kvrp_version, EXPORTED_SYMBOLS,
+    kvrp_status_string, kvrp_version, kvrp_last_launch_count, EXPORTED_SYMBOLS,
     kv_relocate_batch_noalloc, KVRP_NOALLOC_MAX_CHUNKS, chunk_array,
     kv_relocate_batch_mrope, kv_relocate_batch_mla, MlaChunk, mla_chunk_array, kvrp_test_set_wait_limit,
     kv_patch_form, kv_patch_form_orbit, kv_patch_form_workspace_size,

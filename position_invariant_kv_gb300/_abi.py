@@ -24,7 +24,7 @@ EXPORTED_SYMBOLS = (
     "kv_relocate_batch_mla", "kvrp_test_set_wait_limit", "kv_patch_form_workspace_size",
     "kv_patch_form", "kv_patch_form_orbit", "kv_attend_relocated_workspace_size", "kv_attend_relocated",
     "kvrp_status_string",
-    "kvrp_last_error", "kvrp_version",
+    "kvrp_last_error", "kvrp_last_launch_count", "kvrp_version",
 )
 KVRP_NOALLOC_MAX_CHUNKS = 256
 KVRP_ROPE_NONE = 0
@@ -125,6 +125,8 @@ def _load_library():
     L.kvrp_status_string.argtypes = [C.c_int]
     L.kvrp_last_error.restype = C.c_char_p
     L.kvrp_last_error.argtypes = []
+    L.kvrp_last_launch_count.restype = C.c_int32
+    L.kvrp_last_launch_count.argtypes = []
     L.kvrp_version.restype = C.c_int32
     L.kvrp_version.argtypes = []
     return L
@@ -152,6 +154,11 @@ class KvrpError(RuntimeError):
 
 def kvrp_status_string(status: int) -> str:
     return lib().kvrp_status_string(status).decode()
+
+
+def kvrp_last_launch_count() -> int:
+    """Kernel launches of this thread's last relocation call (1 + plan-upload copies for a batch)."""
+    return int(lib().kvrp_last_launch_count())
 
 
 def kvrp_version() -> int:

@@ -27,6 +27,7 @@
 namespace kvrp {
 
 thread_local char g_last_error[512] = "";
+thread_local int32_t g_last_launches = 0;   // kernel launches of this thread's last relocation call
 
 kvrp_status fail(kvrp_status st, const char* fmt, ...) {
   va_list ap;
@@ -569,6 +570,7 @@ kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d
   }
   std::vector<unsigned char> bytes;
   int grid = 0, smem = 0;
+  g_last_launches = 0;
   st = pb.finish(di->sms, di->smem_optin, d_status, &bytes, &grid, &smem);
   if (st != KVRP_OK) return st;
   if (grid == 0) return KVRP_OK;  // nothing to move
@@ -593,9 +595,11 @@ kvrp_status run(const Shape& sh, const std::vector<ChunkIn>& chunks, uint32_t* d
                   bytes.size());
     e = upload_plan(bytes.data(), bytes.size(), workspace, stream);
     if (e != cudaSuccess) return cuda_fail(e, "plan upload");
+    g_last_launches = upload_launches(bytes.size());
     e = launch_relocate(nullptr, workspace, grid, smem, stream);
   }
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  g_last_launches += 1;
   return KVRP_OK;
 }
 
@@ -634,6 +638,7 @@ kvrp_status run_noalloc(const Shape& sh, const std::vector<ChunkIn>& chunks, uin
   }
   std::vector<unsigned char> bytes;
   int grid = 0, smem = 0;
+  g_last_launches = 0;
   st = pb.finish(di->sms, di->smem_optin, d_status, &bytes, &grid, &smem);
   if (st != KVRP_OK) return st;
   if (grid == 0) return KVRP_OK;
@@ -653,8 +658,10 @@ kvrp_status run_noalloc(const Shape& sh, const std::vector<ChunkIn>& chunks, uin
   }
   e = upload_plan(bytes.data(), bytes.size(), scratch, stream);
   if (e != cudaSuccess) return cuda_fail(e, "plan upload to the fixed array");
+  g_last_launches = upload_launches(bytes.size());
   e = launch_relocate(nullptr, scratch, grid, smem, stream);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  g_last_launches += 1;
   return KVRP_OK;
 }
 
@@ -927,6 +934,8 @@ const char* kvrp_status_string(kvrp_status status) {
 }
 
 const char* kvrp_last_error(void) { return g_last_error; }
+
+int32_t kvrp_last_launch_count(void) { return g_last_launches; }
 
 int32_t kvrp_version(void) { return 100; }
 

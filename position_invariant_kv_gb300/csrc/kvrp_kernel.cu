@@ -677,6 +677,8 @@ cudaError_t upload_plan(const void* host_bytes, size_t n_bytes, void* dev_plan, 
   return e;
 }
 
+int32_t upload_launches(size_t n_bytes) { return (int32_t)((n_bytes + dev::kPieceBytes - 1) / dev::kPieceBytes); }
+
 cudaError_t prepare_kernel(int smem_bytes) {
   cudaError_t e = cudaFuncSetAttribute(dev::relocate_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);

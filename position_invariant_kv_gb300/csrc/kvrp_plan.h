@@ -153,6 +153,8 @@ cudaError_t launch_relocate(const void* param_plan, const void* dev_plan, int gr
 // `stream` by small copy kernels whose parameter blocks carry the bytes, so no
 // host buffer has to outlive the call and nothing is staged or pinned.
 cudaError_t upload_plan(const void* host_bytes, size_t n_bytes, void* dev_plan, cudaStream_t stream);
+// Copy launches upload_plan makes for a plan of n_bytes.
+int32_t upload_launches(size_t n_bytes);
 
 // Host helpers shared by the library's translation units.
 kvrp_status fail(kvrp_status st, const char* fmt, ...);

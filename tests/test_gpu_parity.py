@@ -250,3 +250,49 @@ def test_batch_of_many_chunks_spans_several_plan_pieces():
     print(reps)
     assert_parity(reps)
     assert dwl.status_value() == 0
+
+
+def test_launch_count_of_single_and_batch_calls():
+    """kvrp_last_launch_count: one relocation launch for a single chunk; a batch
+    adds the copy launches that carry its plan (31 KB each)."""
+    import harness
+    import position_invariant_kv_gb300 as kvrp
+    one = harness.DeviceWorkload(W.small_gqa(seed=980, chunks_spec=((50, 3, 16, 0),)))
+    one.run()
+    assert kvrp.kvrp_last_launch_count() == 1
+    spec = tuple((20, 7 * i, 16, 0) for i in range(200))
+    many = harness.DeviceWorkload(W.small_gqa(seed=981, n_layers=1, n_heads=1, chunks_spec=spec))
+    many.run()
+    n = kvrp.kvrp_last_launch_count()
+    assert 3 <= n <= 1 + -(-kvrp.kv_relocate_batch_workspace_size(200) // (31 * 1024)), n
+    torch.cuda.synchronize()
+
+
+def test_batch_call_captured_in_a_cuda_graph():
+    """A kv_relocate_batch call recorded into a CUDA graph and replayed writes
+    what the direct call writes: its plan reaches the device through kernel
+    parameters, which the graph keeps, so nothing refers to host memory of the
+    call after it returns."""
+    import harness
+    spec = ((150, -3000, 32, 0), (77, 12, 0, 0), (200, 999, 16, 1))
+    wl = W.small_gqa(seed=985, n_layers=2, n_heads=2, head_dim=128, chunks_spec=spec, extra_pages=2)
+    dwl = harness.DeviceWorkload(wl)
+    dwl.run()
+    torch.cuda.synchronize()
+    want = dwl.pools_host()
+    dwl.reset_pools()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            dwl.run(stream=s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        dwl.reset_pools()
+        g.replay()
+        torch.cuda.synchronize()
+        got = dwl.pools_host()
+        for n in wl.tensors:
+            assert np.array_equal(got[n], want[n]), n
+    assert dwl.status_value() == 0
