@@ -41,9 +41,10 @@ def layout_of(kind, D, rot_dim):
     return row_layout("gqa", "v", n_heads=1, head_dim=D)
 
 
-def make_case(seed, L, T, D, kind, rot_dim, delta, theta, true_rank, noise=1e-3, scale=0.05):
+def make_case(seed, L, T, D, kind, rot_dim, delta, theta, true_rank, noise=1e-3, scale=0.05, decay=12.0):
     """bf16 canonical and conditioned caches whose deficit is low rank + noise:
-    cond = bf16(R(delta) canon + sum_i s_i a_i b_i^T + noise), s_i decaying."""
+    cond = bf16(R(delta) canon + sum_i s_i a_i b_i^T + noise), s_i = s_0 10^(-i / decay)
+    (decay None: a flat spectrum, every s_i equal)."""
     from oracle import bf16_bits_to_f64, round_to_bf16_bits
     from oracle.kamera import apply_relocation
     rng = np.random.default_rng(seed)
@@ -54,7 +55,7 @@ def make_case(seed, L, T, D, kind, rot_dim, delta, theta, true_rank, noise=1e-3,
         y = apply_relocation(bf16_bits_to_f64(canon[l]), delta, theta, lay)
         u0 = np.linalg.qr(rng.standard_normal((T, true_rank)))[0]
         v0 = np.linalg.qr(rng.standard_normal((D, true_rank)))[0]
-        s0 = 3.0 * np.sqrt(T) * 10.0 ** (-np.arange(true_rank) / 12)
+        s0 = 3.0 * np.sqrt(T) * (np.ones(true_rank) if decay is None else 10.0 ** (-np.arange(true_rank) / decay))
         deficit = (u0 * s0) @ v0.T * scale + noise * rng.standard_normal((T, D))
         cond[l] = round_to_bf16_bits(y + deficit)
     return canon, cond
@@ -86,10 +87,10 @@ def form_on_gpu(canon, cond, kind, rot_dim, delta, theta, m, p, q, seed=0):
     return _bits(u), _bits(v)
 
 
-def residuals(delta_f64, u_bits, v_bits, m):
+def residuals(delta_f64, u_bits, v_bits, m, layers=None):
     from oracle import bf16_bits_to_f64, round_to_bf16_bits, svd_patch, eckart_young_tail
     out = []
-    for l in range(delta_f64.shape[0]):
+    for l in (range(delta_f64.shape[0]) if layers is None else layers):
         dl = delta_f64[l]
         got = np.sum((dl - bf16_bits_to_f64(u_bits[l]) @ bf16_bits_to_f64(v_bits[l]).T) ** 2)
         uo, vo = svd_patch(dl, m)
@@ -115,6 +116,30 @@ def test_patch_form_matches_exact_svd(kind, L, T, D, rot, m, p, q, true_rank):
         print(f"residual gpu {got:.4e} exact-bf16 {ref:.4e} tail {tail:.4e} total {total:.4e}")
         assert got <= 1.05 * ref + 1e-9 * total, (got, ref, tail)
         assert got < 0.1 * total           # the patch removes most of the deficit
+
+
+@pytest.mark.parametrize("name,kind,L,T,D,rot,m,p,true_rank,decay,check", [
+    # the bench's own sizes: c1's chunk (28 x 4096 x 512 keys, k = 48) and c2's per-layer
+    # shape (2048 x 4096, k = 80, the widest Jacobi of the bench), with the bench's q = 2
+    ("c1 keys", "heads", 28, 4096, 512, 128, 32, 16, 48, 12.0, (0, 13, 27)),
+    ("c2 values", "none", 2, 2048, 4096, 0, 64, 16, 96, 12.0, (0, 1)),
+    # spectra that make the k x k eigenproblem hard: flat (the top-m choice is free, any
+    # m-subspace of the planted one is optimal) and slowly decaying (lambda_m / lambda_m+1 ~ 0.95)
+    ("flat", "heads", 2, 1024, 512, 128, 32, 16, 48, None, (0, 1)),
+    ("slow decay", "heads", 2, 1024, 512, 128, 32, 16, 64, 96.0, (0, 1)),
+])
+def test_patch_form_at_bench_sizes_and_hard_spectra(name, kind, L, T, D, rot, m, p, true_rank, decay, check):
+    """The two Jacobi sweeps of the k x k eigenproblem (and everything around them) at
+    the sizes bench.py times and on spectra where the sweeps have the least to go on:
+    the residual stays within 5% of the exact truncated SVD's."""
+    delta, theta = -12345, 1e6
+    canon, cond = make_case(71 + T + D, L, T, D, kind, rot, delta, theta, true_rank, decay=decay)
+    u, v = form_on_gpu(canon, cond, kind, rot, delta, theta, m, p, 2)
+    dl = oracle_delta(canon[list(check)], cond[list(check)], kind, rot, delta, theta)
+    for (got, ref, tail, total), l in zip(residuals(dl, u[list(check)], v[list(check)], m), check):
+        print(f"{name} layer {l}: residual gpu {got:.4e} exact-bf16 {ref:.4e} ratio {got / ref:.4f} "
+              f"tail {tail:.4e} total {total:.4e}")
+        assert got <= 1.05 * ref + 1e-9 * total, (name, l, got, ref, tail)
 
 
 def test_formed_patch_recovers_the_conditioned_cache():
