@@ -135,13 +135,26 @@ __device__ __forceinline__ uint4 f_to_bf16x8(const float (&v)[8]) {
                     f2_to_bf16x2(v[6], v[7]));
 }
 
+// The transposed tile: 128 feature rows of 64 tokens (128 bytes), the 4-byte
+// word index of a row XOR-ed with a multiple of 4 that depends on the row.  A
+// warp's 2-byte stores (8 units of 8 or 16 features x 4 tokens) then fall in
+// distinct banks, and 8 consecutive tokens of one row stay one aligned 16-byte
+// group for the transposed read.
+__device__ __forceinline__ int tile_word_swz(int row) { return (((row >> 3) ^ (row >> 6)) & 7) << 2; }
+__device__ __forceinline__ int tile_at(int row, int tl) {   // index in halves
+  return row * kDeltaTokens + ((((tl >> 1) ^ tile_word_swz(row))) << 1) + (tl & 1);
+}
+
 __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constant__ DeltaArgs a,
                                                           const __grid_constant__ TableParam tab) {
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
-  __shared__ float4 tb[kTablePairs];
-  __shared__ uint16_t tile[128][kDeltaTokens + 2];   // bf16 of the deficit, for the transposed rows
-  for (int i = threadIdx.x; i < kTablePairs; i += blockDim.x) tb[i] = tab.v[i];
+  static_assert(kDeltaTokens == 64, "the tile swizzle assumes 32 words per row");
+  // phase table, entry i at i + i / 8: the 8 lanes of a 16-byte read phase take
+  // entries 8 apart, which would otherwise share one bank group
+  __shared__ float4 tb[kTablePairs + kTablePairs / 8];
+  __shared__ __align__(16) uint16_t tile[128 * kDeltaTokens];   // bf16 of the deficit, for the transposed rows
+  for (int i = threadIdx.x; i < kTablePairs; i += blockDim.x) tb[i + (i >> 3)] = tab.v[i];
   {
     const int64_t cta = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
     const int64_t n_threads = (int64_t)gridDim.x * gridDim.y * gridDim.z * blockDim.x;
@@ -218,7 +231,8 @@ __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constan
         if (sg.turns) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {   // pairs e0 + 2q, e0 + 2q + 1
-            const float4 hd = tb[e0 + 2 * q], tl4 = tb[e0 + 2 * q + 1];
+            const int ti = e0 + 2 * q;
+            const float4 hd = tb[ti + (ti >> 3)], tl4 = tb[ti + 1 + ((ti + 1) >> 3)];
             const float a0 = x0[2 * q], a1 = x0[2 * q + 1], b0 = x1[2 * q], b1 = x1[2 * q + 1];
             const float y00 = fmaf(a0, hd.x, -(b0 * hd.z)) + fmaf(a0, tl4.x, -(b0 * tl4.z));
             const float y01 = fmaf(a1, hd.y, -(b1 * hd.w)) + fmaf(a1, tl4.y, -(b1 * tl4.w));
@@ -237,7 +251,10 @@ __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constan
         *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0);
         *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) { tile[e0 + i][tl] = f_to_bf16(d0[i]); tile[e1 + i][tl] = f_to_bf16(d1[i]); }
+        for (int i = 0; i < 8; ++i) {
+          tile[tile_at(e0 + i, tl)] = f_to_bf16(d0[i]);
+          tile[tile_at(e1 + i, tl)] = f_to_bf16(d1[i]);
+        }
       }
     }
   } else {
@@ -274,7 +291,8 @@ __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constan
         const int e0 = e0s[b], e1 = e1s[b];
         float2 y0 = x0[b], y1 = x1[b];
         if (sg.turns) {
-          const float4 hd = tb[e0], tl4 = tb[e0 + 1];   // pairs i, i+1 (i = e0): {C_i, C_i+1, S_i, S_i+1}, then tails
+          // pairs i, i+1 (i = e0): {C_i, C_i+1, S_i, S_i+1}, then tails
+          const float4 hd = tb[e0 + (e0 >> 3)], tl4 = tb[e0 + 1 + ((e0 + 1) >> 3)];
           y0.x = fmaf(x0[b].x, hd.x, -(x1[b].x * hd.z)) + fmaf(x0[b].x, tl4.x, -(x1[b].x * tl4.z));
           y0.y = fmaf(x0[b].y, hd.y, -(x1[b].y * hd.w)) + fmaf(x0[b].y, tl4.y, -(x1[b].y * tl4.w));
           y1.x = fmaf(x1[b].x, hd.x, x0[b].x * hd.z) + fmaf(x1[b].x, tl4.x, x0[b].x * tl4.z);
@@ -285,8 +303,8 @@ __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constan
         uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
         *reinterpret_cast<uint32_t*>(o + e0) = f2_to_bf16x2(d00, d01);
         *reinterpret_cast<uint32_t*>(o + e1) = f2_to_bf16x2(d10, d11);
-        tile[e0][tl] = f_to_bf16(d00); tile[e0 + 1][tl] = f_to_bf16(d01);
-        tile[e1][tl] = f_to_bf16(d10); tile[e1 + 1][tl] = f_to_bf16(d11);
+        tile[tile_at(e0, tl)] = f_to_bf16(d00); tile[tile_at(e0 + 1, tl)] = f_to_bf16(d01);
+        tile[tile_at(e1, tl)] = f_to_bf16(d10); tile[tile_at(e1 + 1, tl)] = f_to_bf16(d11);
       }
     }
   }
@@ -297,10 +315,9 @@ __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constan
     const int f = it / (kDeltaTokens / 8), t8 = 8 * (it - (it / (kDeltaTokens / 8)) * (kDeltaTokens / 8));
     const int t = t0 + t8;
     if (t >= a.T) continue;
-    uint4 w;
-    uint32_t* wp = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) wp[i] = (uint32_t)tile[f][t8 + 2 * i] | ((uint32_t)tile[f][t8 + 2 * i + 1] << 16);
+    // tokens t8 .. t8 + 7 of row f: one 16-byte group (t8 is a multiple of 8, the
+    // swizzle a multiple of 4 words)
+    const uint4 w = *reinterpret_cast<const uint4*>(&tile[f * kDeltaTokens + (((t8 >> 1) ^ tile_word_swz(f)) << 1)]);
     *reinterpret_cast<uint4*>(out_t + (int64_t)(sg.f0 + f) * a.Tp + t) = w;
   }
 }
