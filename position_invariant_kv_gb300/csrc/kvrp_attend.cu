@@ -287,10 +287,32 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
     // ---------------- producer ----------------
     const int64_t row = (int64_t)p.Hkv * D;
     const uint32_t row_bytes = (uint32_t)p.hg * D * 2;
+    // Page numbers of paged chunks: lane l holds page l % pps of stage batch_f + l / pps
+    // (pps pages of 16 tokens per stage), loaded in one batch every 32 / pps stages, so a
+    // stage's copies do not wait behind a dependent block-table load of their own.
+    const int pps = p.ts / 16;
+    const int spb = 32 / pps;
+    int64_t batch_f = f1;   // no batch loaded yet
+    int32_t pg_lane = 0;
     int s = 0, n_issued = 0;
     uint32_t par = 0;
     for (int64_t f = f0; f < f1; ++f) {
-      if (!wait_phase(empty(s), par ^ 1u, abort_p, p.status)) break;
+      // the whole warp goes on or stops together (the shuffles below are warp-wide)
+      if (!__all_sync(0xffffffffu, wait_phase(empty(s), par ^ 1u, abort_p, p.status))) break;
+      if (f >= batch_f + spb || batch_f == f1) {
+        batch_f = f;
+        const int64_t gf = f + lane / pps;
+        pg_lane = 0;
+        if (gf < f1) {
+          const Cursor cl = cursor_at(p, gf);
+          const ChunkRec& cc = p.c[cl.c];
+          const int pi = cl.k * pps + lane % pps;   // page index within the chunk
+          if (cc.table && pi * 16 < cc.n_tokens) pg_lane = __ldg(cc.table + pi);
+        }
+      }
+      const int sbase = (int)(f - batch_f) * pps;
+      const int pg_a = __shfl_sync(0xffffffffu, pg_lane, (sbase + (lane >> 4)) & 31);       // token lane
+      const int pg_b = __shfl_sync(0xffffffffu, pg_lane, (sbase + 2 + (lane >> 4)) & 31);   // token lane + 32
       const ChunkRec& c = p.c[r.c];
       const int t0 = r.k * p.ts;
       const int n = min(p.ts, c.n_tokens - t0);
@@ -302,7 +324,7 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
       for (int t = lane; t < n; t += 32) {
         int64_t tok = t0 + t;   // the row of this token: contiguous, or page table[tok / 16], slot tok % 16
         if (c.table) {
-          int pg = __ldg(c.table + (tok >> 4));
+          int pg = t < 32 ? pg_a : pg_b;
           if (pg < 0 || pg >= c.num_pages) {
             if (p.status) atomicOr(p.status, KVRP_DEV_BAD_PAGE);
             pg = 0;
