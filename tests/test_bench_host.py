@@ -88,3 +88,15 @@ def test_parity_worker_reports_the_sampled_rows(tmp_path):
     path.write_bytes(pickle.dumps([g]))
     r = bench.parity_worker(str(path))
     assert r["mismatches"] == 1 and r["violations"] == 1 and r["max_ulp"] == 3
+
+
+def test_e2e_leg_fits_host_memory():
+    """The end-to-end leg moves every layer when the pinned buffers fit, and
+    fewer (at least one) when they would not."""
+    import workloads as W
+    wl = W.config(4)
+    per_layer = (wl.algorithmic_bytes()["total"] + wl.n_layers * wl.num_pages * 16 * wl.row_width * 2 * 2) / wl.n_layers
+    assert bench.e2e_layers(wl, 1 << 62) == wl.n_layers
+    assert bench.e2e_layers(wl, int(per_layer * 10.5)) == 10
+    assert bench.e2e_layers(wl, 1) == 1
+    assert bench.host_budget_bytes() > 0
