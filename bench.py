@@ -722,7 +722,8 @@ def bench_patch_form(args) -> dict:
     fac = {n: (torch.empty((L, T, m), dtype=torch.bfloat16, device=device),
                torch.empty((L, D, m), dtype=torch.bfloat16, device=device)) for n in wl.tensors}
     d_status = torch.zeros(1, dtype=torch.int32, device=device)
-    stream = torch.cuda.current_stream()
+    # a graph is captured on a stream of its own (never the legacy default stream)
+    stream = torch.cuda.Stream(device=device) if args.graph else torch.cuda.current_stream()
     if wl.family == "mla":
         kinds = {"kv": (kvrp.KVRP_ROPE_MLA_TAIL, wl.rope_dim)}
     else:
@@ -769,16 +770,35 @@ def bench_patch_form(args) -> dict:
         step()
     join_all()
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # one step (its calls on their streams, forked from and joined to the capture stream)
+        # recorded once into a CUDA graph and replayed: the library calls are capturable
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fork_all()
+            step()
+            join_all()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                graph.replay()
+        torch.cuda.synchronize()
     steps = args.steps
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
-        fork_all()
-        for _ in range(steps):
-            step()
-        join_all()
+        if graph is not None:
+            with torch.cuda.stream(stream):
+                for _ in range(steps):
+                    graph.replay()
+        else:
+            fork_all()
+            for _ in range(steps):
+                step()
+            join_all()
         t1.record(stream)
         torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / steps
@@ -794,7 +814,8 @@ def bench_patch_form(args) -> dict:
                                f"orbit of {orbit} ordering(s), "
                                f"{len(jobs)} call(s) per step ({per} layer range(s) per tensor), "
                                f"{'each on its own stream' if args.streams > 1 else 'in turn on one stream'}"
-                               f"{', every step joined' if args.join_steps else ''}",
+                               f"{', every step joined' if args.join_steps else ''}"
+                               f"{', the step replayed from a CUDA graph' if args.graph else ''}",
                    "tokens_per_step": T, "method_bytes_per_step": nb,
                    "l2": f"inputs larger than L2 ({nb / 1e6:.0f} MB moved per step vs 129 MB L2)"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -1038,6 +1059,8 @@ def main():
     ap.add_argument("--power-iters", type=int, default=2, help="patch_form: subspace iterations")
     ap.add_argument("--join-steps", type=int, default=0,
                     help="patch_form: 1 makes each step wait for the previous one on every stream")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="patch_form: 1 records one step into a CUDA graph and times its replays")
     ap.add_argument("--streams", type=int, default=4,
                     help="patch_form: concurrent calls per step, one stream each (tensors first, then layer "
                          "ranges of each tensor); 1 runs the tensors in turn on one stream")
