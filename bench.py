@@ -982,10 +982,10 @@ def bench_attend(args) -> dict:
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": profiled_traffic("attend", "attend_dram.json", ATTEND_SOURCES),
-                     "kernel": "kv_attend_relocated, whole call (prep, block and combine kernels); traffic is "
+                     "kernel": "kv_attend_relocated, whole call (block and combine kernels); traffic is "
                                "block_kernel's DRAM bytes per launch",
                      "peak_source": peaks["source"]},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": kvrp.kvrp_last_launch_count() * args.steps,
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:

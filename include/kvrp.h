@@ -381,7 +381,7 @@ kvrp_status kv_patch_form_orbit(
  *   out         device bf16 [n_seqs][n_q_heads][head_dim]; a sequence with no
  *               tokens gets zeros.
  *   workspace   device scratch of kv_attend_relocated_workspace_size(...) bytes
- *               (the rotated queries and fp32 partial results); the size depends
+ *               (fp32 partial results); the size depends
  *               on the current device's SM count, and the call returns WORKSPACE
  *               if it is smaller than the size for the device it runs on.
  *   d_status    optional device word; KVRP_DEV_TIMEOUT is OR-ed in if an internal
@@ -436,9 +436,12 @@ const char* kvrp_status_string(kvrp_status status);
 const char* kvrp_last_error(void);
 
 /* Kernel launches that this host thread's last relocation call (kv_relocate_*)
- * enqueued: the relocation kernel, plus for a batch the small copy launches
- * that carry its launch plan to the device (31 KB of plan each).  0 when the
- * call returned an error or had nothing to move. */
+ * or attention call (kv_attend_relocated) enqueued.  Relocation: the relocation
+ * kernel, plus for a batch the small copy launches that carry its launch plan to
+ * the device (31 KB of plan each).  Attention: the block and combine kernels,
+ * plus the query-preparation kernel when some chunk's work starts late in a
+ * block's share (2 or 3).  0 when the call returned an error or had nothing to
+ * move. */
 int32_t kvrp_last_launch_count(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */

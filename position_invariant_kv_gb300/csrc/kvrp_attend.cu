@@ -13,30 +13,33 @@
 // rows u_k,t, u_v,t -- the bytes of the canonical cache plus the factors.
 //
 // Kernels:
-//   prep_kernel    one CTA per (chunk, KV head): the rotated, scaled queries
-//                  scale * R(-delta) q (angles in fp64, shared by the group's
-//                  query heads) and w = scale V_k,h^T q, each split into a bf16
-//                  high and low part (their sum carries ~16 significant bits);
 //   block_kernel   persistent, two CTAs per SM.  The work is a sequence of
 //                  stages -- (head group, chunk, 16 * 4 / hg tokens) -- and each
 //                  CTA takes an equal contiguous share of it (stream-K), so
-//                  every SM streams the same number of bytes.  A producer warp
-//                  fills a ring of shared-memory stages with bulk copies (the
-//                  TMA engine; one copy per token row of the head group's K and
-//                  V -- contiguous rows, or rows of a paged pool through the
-//                  chunk's block table -- and one per factor block of U_k and
-//                  U_v, which the group's heads share); four consumer warps, one (KV head, 16-token
-//                  slice) each, compute S = K Q^T + U_k W^T with the tokens as
-//                  the MMA's rows, an online softmax in registers, and
-//                  O^T += [V | U_v]^T P^T with P^T transposed in registers
-//                  (movmatrix) -- warp-level tensor-core MMAs (mma.sync
-//                  m16n8k16 bf16 -> fp32; q, w and P enter as high + low bf16
-//                  parts, two products each).  At a chunk or share boundary a
-//                  warp applies the value patch, O^T += V_v,h (P U_v)^T (tensor
-//                  cores; P U_v as high + low bf16 parts), and writes its
-//                  (O, max, sum) as one fp32 partial;
+//                  every SM streams the same number of bytes; a chunk, or its
+//                  part inside one share, is a segment.  A producer warp fills a
+//                  ring of shared-memory slots with bulk copies (the TMA engine):
+//                  per segment, first V_k,h and the group's query rows, then the
+//                  token stages -- K and V rows (two tokens per copy when one head
+//                  group spans the whole row; contiguous rows, or rows of a paged
+//                  pool through the chunk's block table) and the U_k, U_v factor
+//                  rows, which the group's heads share -- then V_v,h.  Four
+//                  consumer warps, one (KV head, 16-token slice) each, turn the
+//                  first slots into the rotated, scaled query scale R(-delta) q
+//                  (angles in fp64) and w = scale V_k,h^T q, each as a bf16 high
+//                  and low part (their sum carries ~16 significant bits); compute
+//                  S = K Q^T + U_k W^T with the tokens as the MMA's rows, an online
+//                  softmax in registers, and O^T += [V | U_v]^T P^T with P^T
+//                  transposed in registers (movmatrix) -- warp-level tensor-core
+//                  MMAs (mma.sync m16n8k16 bf16 -> fp32; q, w and P enter as high
+//                  + low parts, two products each); and at the segment's end apply
+//                  the value patch, O^T += V_v,h (P U_v)^T, from the last slots and
+//                  write (O, max, sum) as one fp32 partial.  A consumer never
+//                  waits on a global load: everything it reads arrives through
+//                  the ring;
 //   combine_kernel one CTA per (sequence, query head): merges the partials of
-//                  the sequence's chunks by their maxima, rounds to bf16.
+//                  the sequence's chunks in one pass (running max, rescaled
+//                  sums), rounds to bf16.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -77,8 +80,6 @@ struct Params {
   const uint16_t* q;
   uint16_t* out;
   float* partial;      // [slot][slice][hg * g][d + 2]: O (value patch included), max, sum
-  uint16_t* qhl;       // [n_chunks][2][Hq][d]: high, low bf16 parts of scale * R(-delta) q
-  uint16_t* whl;       // [n_chunks][2][Hq][m_max]: high, low parts of scale * V_k,h^T q
   uint32_t* status;
   int n_chunks, n_seqs, Hq, Hkv, d, g, m_max;
   int hg;              // KV heads per head group: a power of two dividing Hkv, at most kConsumers
@@ -86,10 +87,13 @@ struct Params {
   int ns;              // token slices per stage (kConsumers / hg)
   int ts;              // tokens per stage (kSlice * ns)
   int stages;          // ring depth
-  int k_pitch;         // elements per staged K (and V) row: hg * d + 8
-  int kv_bytes;        // bytes of a stage's K (and of its V)
+  int row_bytes;       // bytes of one token's head-group row of K (or V): hg * d * 2
+  int pair_pitch;      // staged rows go in pairs: token t at (t / 2) * pair_pitch + (t % 2) * row_bytes
+  int kv_bytes;        // bytes of a stage's K (and of its V): ts / 2 pairs
   int u_bytes;         // bytes of a stage's U_k (and of its U_v): ts * m_max * 2
   int stage_bytes;
+  int hp;              // KV heads per P slot (V_k,h and query rows)
+  int hv;              // KV heads per V slot (V_v,h)
   int n_cta;
   int64_t s_hg;        // stages per head group
   float scale;
@@ -105,84 +109,31 @@ __device__ __forceinline__ uint16_t to_bf(float v) {
   return *reinterpret_cast<const uint16_t*>(&b);
 }
 __device__ __forceinline__ uint32_t pack_bf(uint16_t lo, uint16_t hi) { return (uint32_t)lo | ((uint32_t)hi << 16); }
-__device__ __forceinline__ uint32_t ldg32(const uint16_t* p) { return __ldg(reinterpret_cast<const uint32_t*>(p)); }
 
-// Shared memory is kept small (V_k,h, the queries and the angle table: 14 KB
-// for d = 128, rank 32) so that the block kernel's two CTAs per SM fit beside a
-// running prep CTA.
-__global__ void __launch_bounds__(256) prep_kernel(const __grid_constant__ Params p) {
-  extern __shared__ __align__(16) uint8_t psm[];   // V_k,h [d][m + 8] bf16, then the queries [g][d] fp32
-  __shared__ float2 rot[64];                        // (cos, sin) of -delta * theta^(-2i/d)
-  // the block kernel may launch now: its producer streams K, V and U (inputs) while
-  // this kernel prepares the queries, which its consumers wait for
-  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int ci = blockIdx.x, h = blockIdx.y;
-  const ChunkRec& c = p.c[ci];
-  const int d = p.d, half = d / 2, g = p.g, m = c.rank, Hq = p.Hq, vp = m + 8;
-  uint16_t* vks = reinterpret_cast<uint16_t*>(psm);
-  float* qs = reinterpret_cast<float*>(psm + (size_t)d * (p.m_max + 8) * 2);
-  const uint16_t* q = p.q + ((int64_t)c.seq * Hq + (int64_t)h * g) * d;
-  uint16_t* qh = p.qhl + ((int64_t)ci * 2 * Hq + (int64_t)h * g) * d;
-  uint16_t* ql = qh + (int64_t)Hq * d;
-  if (m > 0) {
-    const uint4* src = reinterpret_cast<const uint4*>(c.vk + (int64_t)h * d * m);
-    for (int e = threadIdx.x; e < d * m / 8; e += blockDim.x) {
-      const int f = e / (m / 8), r8 = e - f * (m / 8);
-      *reinterpret_cast<uint4*>(vks + f * vp + 8 * r8) = __ldg(src + e);
-    }
-  }
-  for (int e = threadIdx.x; e < g * d; e += blockDim.x) qs[e] = bf(q[e]);
-  if (threadIdx.x < half) {
-    // phi = -delta theta^(-2i/d) reduced to [-pi, pi] in fp64 (Cody and Waite: 2 pi as a
-    // double plus its remainder, each product fused), then sine and cosine in fp32
-    const double two_pi_hi = 6.283185307179586, two_pi_lo = 2.4492935982947064e-16;
-    const double phi = -static_cast<double>(p.delta[ci]) * p.inv_freq[threadIdx.x];
-    const double k = rint(phi * (1.0 / 6.283185307179586));
-    const double red = fma(-k, two_pi_lo, fma(-k, two_pi_hi, phi));
-    float sn, cs;
-    sincosf(static_cast<float>(red), &sn, &cs);
-    rot[threadIdx.x] = make_float2(cs, sn);
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < g * half; e += blockDim.x) {
-    const int j = e / half, i = e - j * half;
-    const float cs = rot[i].x, sn = rot[i].y;
-    const float a = qs[j * d + i], b = qs[j * d + i + half];
-    const float r0 = (a * cs - b * sn) * p.scale, r1 = (b * cs + a * sn) * p.scale;
-    const uint16_t h0 = to_bf(r0), h1 = to_bf(r1);
-    qh[j * d + i] = h0;
-    qh[j * d + i + half] = h1;
-    ql[j * d + i] = to_bf(r0 - bf(h0));
-    ql[j * d + i + half] = to_bf(r1 - bf(h1));
-  }
-  if (m == 0) return;
-  // W^T [m][g] = V_k,h^T Q^T on tensor cores (bf16 products, exact; fp32 sums): warp ->
-  // rank m-tiles; A = V_k,h^T by transposed ldmatrix of the [d][m] rows, B = Q^T from q
-  uint16_t* wh = p.whl + ((int64_t)ci * 2 * Hq + (int64_t)h * g) * p.m_max;
-  uint16_t* wl = wh + (int64_t)Hq * p.m_max;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
-  const int t_row = (lane & 7) + ((lane >> 4) << 3), t_col = ((lane >> 3) & 1) * 8;
-  for (int t = warp; t < (m / 16) * ((g + 7) / 8); t += blockDim.x / 32) {
-    const int mt = t % (m / 16), nt = t / (m / 16), j = nt * 8 + gid;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k0 = 0; k0 < d; k0 += 16) {
-      uint32_t a[4];
-      ldsm_x4_trans(a, smem_u32(vks + (k0 + t_row) * vp + mt * 16 + t_col));
-      const uint32_t b0 = j < g ? ldg32(q + j * d + k0 + 2 * tig) : 0u;
-      const uint32_t b1 = j < g ? ldg32(q + j * d + k0 + 8 + 2 * tig) : 0u;
-      mma16816(acc, a, b0, b1);
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {   // (rank mt 16 + gid + 8 (e / 2), head nt 8 + 2 tig + e % 2)
-      const int r = mt * 16 + gid + (e >> 1) * 8, jj = nt * 8 + 2 * tig + (e & 1);
-      if (jj < g) {
-        const float w = acc[e] * p.scale;
-        const uint16_t hw = to_bf(w);
-        wh[jj * p.m_max + r] = hw;
-        wl[jj * p.m_max + r] = to_bf(w - bf(hw));
-      }
-    }
-  }
+// The query preparation, with every rounding pinned (explicit products and fma, no
+// contraction left to the compiler).
+//
+// (cos, sin) of phi = -delta theta^(-2i/d): phi reduced to [-pi, pi] in fp64 (Cody and
+// Waite: 2 pi as a double plus its remainder, each product fused), then sine and
+// cosine in fp32.
+__device__ __forceinline__ float2 turn_angle(int64_t delta, double inv_freq) {
+  const double two_pi_hi = 6.283185307179586, two_pi_lo = 2.4492935982947064e-16;
+  const double phi = -static_cast<double>(delta) * inv_freq;
+  const double k = rint(phi * (1.0 / 6.283185307179586));
+  const double red = fma(-k, two_pi_lo, fma(-k, two_pi_hi, phi));
+  float sn, cs;
+  sincosf(static_cast<float>(red), &sn, &cs);
+  return make_float2(cs, sn);
+}
+// scale * R(-delta) applied to one frequency pair (a, b) = (q_i, q_{i + d/2}).
+__device__ __forceinline__ float2 turn_pair(float a, float b, float2 cs_sn, float scale) {
+  return make_float2(__fmul_rn(__fmaf_rn(a, cs_sn.x, -__fmul_rn(b, cs_sn.y)), scale),
+                     __fmul_rn(__fmaf_rn(b, cs_sn.x, __fmul_rn(a, cs_sn.y)), scale));
+}
+// v = high + low, both bf16 (their sum carries ~16 significant bits of v).
+__device__ __forceinline__ void split_hl(float v, uint16_t& hi, uint16_t& lo) {
+  hi = to_bf(v);
+  lo = to_bf(__fsub_rn(v, bf(hi)));
 }
 
 // --- the stage sequence ------------------------------------------------------
@@ -237,6 +188,109 @@ __host__ __device__ __forceinline__ int64_t slot_of(int i, int hg, int c, int n_
   return (int64_t)i + (int64_t)hg * n_chunks + c;
 }
 
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// The ring slots of one segment (a head group's chunk, or its part inside one CTA's
+// share), in order:
+//   P slots       V_k,h [d][m] and the query rows [g][d] of p.hp KV heads each (hg / hp
+//                 slots): the consumer warps of those heads turn them into the score
+//                 product's B fragments;
+//   token stages  the K and V rows and the U_k, U_v factor rows of ts tokens;
+//   V slots       V_v,h [d][m] of p.hv KV heads each (hg / hv slots; none at rank 0), for
+//                 the value patch at the segment's end.
+// Everything a consumer reads comes through the ring, issued ahead of its use: under a
+// full-bandwidth stream a dependent global load waits microseconds, a ring slot does not.
+
+// From a P slot: this warp's query heads (pairs read from the staged [g][d] rows) and
+// V_k,h (staged [d][m]) into the B fragments of the score product -- the rotated, scaled
+// query and w = scale V_k,h^T q as high + low bf16 parts, heads >= g zero.  W^T =
+// V_k,h^T Q^T on tensor cores (A = V_k,h^T by transposed ldmatrix, B = the raw query
+// pairs); angles in fp64, two per lane, handed to the lanes that hold each frequency
+// pair by shuffles.  Feature i < d/2 pairs with i + d/2, which sits in k-step
+// kk + KT/2 of the same lane, so the rotation is lane-local.
+template <int D, int NT, int MCAP>
+__device__ __forceinline__ void prepare(const Params& p, uint32_t vks, uint32_t qs, int m, int64_t delta,
+                                        uint32_t (&qb)[D / 16][NT][2][2], uint32_t (&wb)[MCAP / 16][NT][2][2]) {
+  constexpr int KT = D / 16, RT = MCAP / 16;
+  const int lane = threadIdx.x & 31, gid = lane >> 2, tig = lane & 3;
+  const int t_row = (lane & 7) + ((lane >> 4) << 3), t_col = ((lane >> 3) & 1) * 8;
+  const int g = p.g;
+  uint32_t raw[KT][NT][2];   // query pairs (head nt 8 + gid; features kk 16 + 2 tig (+ 8) + {0, 1})
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int j = nt * 8 + gid;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      raw[kk][nt][0] = j < g ? lds32(qs + (uint32_t)(j * D + kk * 16 + 2 * tig) * 2) : 0u;
+      raw[kk][nt][1] = j < g ? lds32(qs + (uint32_t)(j * D + kk * 16 + 8 + 2 * tig) * 2) : 0u;
+    }
+  }
+  const float2 t0 = turn_angle(delta, p.inv_freq[lane]);   // angles lane and lane + 32
+  const float2 t1 = D / 2 > 32 ? turn_angle(delta, p.inv_freq[lane + 32]) : t0;
+#pragma unroll
+  for (int mt = 0; mt < RT; ++mt) {
+    if (mt * 16 >= m) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) wb[mt][nt][0][0] = wb[mt][nt][0][1] = wb[mt][nt][1][0] = wb[mt][nt][1][1] = 0u;
+      continue;
+    }
+    float acc[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KT; ++kk) {
+      uint32_t a[4];
+      ldsm_x4_trans(a, vks + (uint32_t)((kk * 16 + t_row) * m + mt * 16 + t_col) * 2);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt], a, raw[kk][nt][0], raw[kk][nt][1]);
+    }
+    // acc = W^T (rank gid (+ 8), heads 2 tig + {0, 1}); its transpose is the B fragment
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      uint16_t h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) split_hl(__fmul_rn(acc[nt][e], p.scale), h[e], l[e]);
+      wb[mt][nt][0][0] = movmatrix_trans(pack_bf(h[0], h[1]));
+      wb[mt][nt][0][1] = movmatrix_trans(pack_bf(h[2], h[3]));
+      wb[mt][nt][1][0] = movmatrix_trans(pack_bf(l[0], l[1]));
+      wb[mt][nt][1][1] = movmatrix_trans(pack_bf(l[2], l[3]));
+    }
+  }
+#pragma unroll
+  for (int kk = 0; kk < KT / 2; ++kk) {
+    float2 cs[2][2];   // [b0 / b1][element]: angle kk 16 + 8 b + 2 tig + e, held by lane (that) mod 32
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = kk * 16 + 8 * b + 2 * tig + e;
+        const float2 t = (kk >> 1) ? t1 : t0;
+        cs[b][e] = make_float2(__shfl_sync(0xffffffffu, t.x, i & 31), __shfl_sync(0xffffffffu, t.y, i & 31));
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t lo = raw[kk][nt][b], hi = raw[kk + KT / 2][nt][b];
+        uint16_t h0[2], l0[2], h1[2], l1[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float2 r = turn_pair(bf((uint16_t)(lo >> (16 * e))), bf((uint16_t)(hi >> (16 * e))), cs[b][e], p.scale);
+          split_hl(r.x, h0[e], l0[e]);
+          split_hl(r.y, h1[e], l1[e]);
+        }
+        qb[kk][nt][0][b] = pack_bf(h0[0], h0[1]);
+        qb[kk][nt][1][b] = pack_bf(l0[0], l0[1]);
+        qb[kk + KT / 2][nt][0][b] = pack_bf(h1[0], h1[1]);
+        qb[kk + KT / 2][nt][1][b] = pack_bf(l1[0], l1[1]);
+      }
+  }
+}
+
 // Bounded wait that ignores the abort flag: used to let this CTA's own copies land before it exits.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
   const long long t0 = clock64();
@@ -278,7 +332,7 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
   }
   __syncthreads();
   // the combine kernel may launch (and wait, resident) while this grid runs
-  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) pdl_launch_dependents();
   volatile int* abort_p = &abort_flag;
   if (f0 >= f1) return;
   Cursor r = cursor_at(p, f0);
@@ -286,7 +340,10 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
   if (warp == kConsumers) {
     // ---------------- producer ----------------
     const int64_t row = (int64_t)p.Hkv * D;
-    const uint32_t row_bytes = (uint32_t)p.hg * D * 2;
+    const uint32_t row_bytes = (uint32_t)p.row_bytes;
+    // one head group covering the whole row: two consecutive tokens (of one page) are one
+    // contiguous 2-row source, moved by one copy; otherwise one copy per token row
+    const bool pairs = p.n_hg == 1;
     // Page numbers of paged chunks: lane l holds page l % pps of stage batch_f + l / pps
     // (pps pages of 16 tokens per stage), loaded in one batch every 32 / pps stages, so a
     // stage's copies do not wait behind a dependent block-table load of their own.
@@ -296,54 +353,102 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
     int32_t pg_lane = 0;
     int s = 0, n_issued = 0;
     uint32_t par = 0;
-    for (int64_t f = f0; f < f1; ++f) {
-      // the whole warp goes on or stops together (the shuffles below are warp-wide)
-      if (!__all_sync(0xffffffffu, wait_phase(empty(s), par ^ 1u, abort_p, p.status))) break;
-      if (f >= batch_f + spb || batch_f == f1) {
-        batch_f = f;
-        const int64_t gf = f + lane / pps;
-        pg_lane = 0;
-        if (gf < f1) {
-          const Cursor cl = cursor_at(p, gf);
-          const ChunkRec& cc = p.c[cl.c];
-          const int pi = cl.k * pps + lane % pps;   // page index within the chunk
-          if (cc.table && pi * 16 < cc.n_tokens) pg_lane = __ldg(cc.table + pi);
-        }
-      }
-      const int sbase = (int)(f - batch_f) * pps;
-      const int pg_a = __shfl_sync(0xffffffffu, pg_lane, (sbase + (lane >> 4)) & 31);       // token lane
-      const int pg_b = __shfl_sync(0xffffffffu, pg_lane, (sbase + 2 + (lane >> 4)) & 31);   // token lane + 32
-      const ChunkRec& c = p.c[r.c];
-      const int t0 = r.k * p.ts;
-      const int n = min(p.ts, c.n_tokens - t0);
-      const uint32_t ub = (uint32_t)n * c.rank * 2;
-      if (lane == 0) mbar_expect_tx(full(s), (uint32_t)n * 2 * row_bytes + 2 * ub);
-      __syncwarp();
-      const uint32_t st = ring + (uint32_t)s * p.stage_bytes;
-      const int64_t col = (int64_t)r.hg * p.hg * D;
-      for (int t = lane; t < n; t += 32) {
-        int64_t tok = t0 + t;   // the row of this token: contiguous, or page table[tok / 16], slot tok % 16
-        if (c.table) {
-          int pg = t < 32 ? pg_a : pg_b;
-          if (pg < 0 || pg >= c.num_pages) {
-            if (p.status) atomicOr(p.status, KVRP_DEV_BAD_PAGE);
-            pg = 0;
-          }
-          tok = (int64_t)pg * 16 + (tok & 15);
-        }
-        bulk_load(st + (uint32_t)t * p.k_pitch * 2, c.k + tok * row + col, row_bytes, full(s));
-        bulk_load(st + p.kv_bytes + (uint32_t)t * p.k_pitch * 2, c.v + tok * row + col, row_bytes, full(s));
-      }
-      if (lane == 0 && ub > 0) {
-        bulk_load(st + 2 * p.kv_bytes, c.uk + (int64_t)t0 * c.rank, ub, full(s));
-        bulk_load(st + 2 * p.kv_bytes + p.u_bytes, c.uv + (int64_t)t0 * c.rank, ub, full(s));
-      }
+    // the next slot, once every consumer has released it (the whole warp goes on or stops
+    // together: the shuffles below are warp-wide); its shared address, or 0 on an abort
+    auto acquire = [&]() -> uint32_t {
+      if (!__all_sync(0xffffffffu, wait_phase(empty(s), par ^ 1u, abort_p, p.status))) return 0u;
+      return ring + (uint32_t)s * p.stage_bytes;
+    };
+    auto release = [&]() {
       ++n_issued;
       if (++s == p.stages) {
         s = 0;
         par ^= 1u;
       }
-      if (f + 1 < f1) advance(p, r);
+    };
+    bool ok = true;
+    for (int64_t f = f0; f < f1 && ok;) {
+      const ChunkRec& c = p.c[r.c];
+      const int m = c.rank;
+      const int kv0 = r.hg * p.hg;   // the head group's first KV head
+      const int n_tok = (int)min((int64_t)(r.nst - r.k), f1 - f);
+      // P slots
+      for (int j = 0; j < p.hg && ok; j += p.hp) {
+        const uint32_t st = acquire();
+        ok = st != 0u;
+        if (!ok) break;
+        const uint32_t vk_bytes = (uint32_t)(p.hp * D * m * 2), q_bytes = (uint32_t)(p.hp * p.g * D * 2);
+        if (lane == 0) {
+          mbar_expect_tx(full(s), vk_bytes + q_bytes);
+          if (m > 0) bulk_load(st, c.vk + (int64_t)(kv0 + j) * D * m, vk_bytes, full(s));
+          bulk_load(st + vk_bytes, p.q + ((int64_t)c.seq * p.Hq + (int64_t)(kv0 + j) * p.g) * D, q_bytes, full(s));
+        }
+        release();
+      }
+      // token stages
+      for (int k = 0; k < n_tok && ok; ++k, ++f) {
+        const uint32_t st = acquire();
+        ok = st != 0u;
+        if (!ok) break;
+        if (f >= batch_f + spb || batch_f == f1) {
+          batch_f = f;
+          const int64_t gf = f + lane / pps;
+          pg_lane = 0;
+          if (gf < f1) {
+            const Cursor cl = cursor_at(p, gf);
+            const ChunkRec& cc = p.c[cl.c];
+            const int pi = cl.k * pps + lane % pps;   // page index within the chunk
+            if (cc.table && pi * 16 < cc.n_tokens) pg_lane = __ldg(cc.table + pi);
+          }
+        }
+        const int sbase = (int)(f - batch_f) * pps;
+        const int pg_a = __shfl_sync(0xffffffffu, pg_lane, (sbase + (lane >> 4)) & 31);       // token lane
+        const int pg_b = __shfl_sync(0xffffffffu, pg_lane, (sbase + 2 + (lane >> 4)) & 31);   // token lane + 32
+        const int pg_p = __shfl_sync(0xffffffffu, pg_lane, (sbase + (lane >> 3)) & 31);       // tokens 2 lane, + 1
+        const int t0 = r.k * p.ts;
+        const int n = min(p.ts, c.n_tokens - t0);
+        const uint32_t ub = (uint32_t)n * m * 2;
+        if (lane == 0) mbar_expect_tx(full(s), (uint32_t)n * 2 * row_bytes + 2 * ub);
+        __syncwarp();
+        const int64_t col = (int64_t)kv0 * D;
+        // token t of the stage (rows t, t + 1 for a pair; pairs never straddle a page: t0
+        // and t are even, pages 16 tokens) lands at (t / 2) pair_pitch
+        const int step = pairs ? 2 : 1;
+        for (int t = step * lane; t < n; t += 32 * step) {
+          int64_t tok = t0 + t;   // the row of this token: contiguous, or page table[tok / 16], slot tok % 16
+          if (c.table) {
+            int pg = pairs ? pg_p : t < 32 ? pg_a : pg_b;
+            if (pg < 0 || pg >= c.num_pages) {
+              if (p.status) atomicOr(p.status, KVRP_DEV_BAD_PAGE);
+              pg = 0;
+            }
+            tok = (int64_t)pg * 16 + (tok & 15);
+          }
+          const uint32_t dst = st + (uint32_t)(t >> 1) * p.pair_pitch + (uint32_t)(t & 1) * row_bytes;
+          const uint32_t bytes = (uint32_t)min(step, n - t) * row_bytes;
+          bulk_load(dst, c.k + tok * row + col, bytes, full(s));
+          bulk_load(dst + p.kv_bytes, c.v + tok * row + col, bytes, full(s));
+        }
+        if (lane == 0 && ub > 0) {
+          bulk_load(st + 2 * p.kv_bytes, c.uk + (int64_t)t0 * m, ub, full(s));
+          bulk_load(st + 2 * p.kv_bytes + p.u_bytes, c.uv + (int64_t)t0 * m, ub, full(s));
+        }
+        release();
+        if (f + 1 < f1) advance(p, r);
+      }
+      // V slots
+      if (m > 0)
+        for (int j = 0; j < p.hg && ok; j += p.hv) {
+          const uint32_t st = acquire();
+          ok = st != 0u;
+        if (!ok) break;
+          const uint32_t vv_bytes = (uint32_t)(p.hv * D * m * 2);
+          if (lane == 0) {
+            mbar_expect_tx(full(s), vv_bytes);
+            bulk_load(st, c.vv + (int64_t)(kv0 + j) * D * m, vv_bytes, full(s));
+          }
+          release();
+        }
     }
     // no copy of this CTA may still be landing when it exits: wait for the last phase issued on each stage
     if (lane == 0)
@@ -364,6 +469,10 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
   // ldmatrix lane offsets (elements): A from [token][feature] rows; A^T (transposed load) likewise
   const int a_row = lane & 15, a_col = (lane >> 4) * 8;
   const int t_row = (lane & 7) + ((lane >> 4) << 3), t_col = ((lane >> 3) & 1) * 8;
+  // this lane's ldmatrix row within a token stage: K rows (A), V rows (A^T, transposed load)
+  auto staged = [&](int t) { return (uint32_t)(t >> 1) * p.pair_pitch + (uint32_t)(t & 1) * p.row_bytes; };
+  const uint32_t k_lane = staged(sw * kSlice + a_row) + (uint32_t)(hw * D + a_col) * 2;
+  const uint32_t v_lane = p.kv_bytes + staged(sw * kSlice + t_row) + (uint32_t)(hw * D + t_col) * 2;
 
   float o[KT + RT][NT][4];                 // O^T: feature m-tiles, then rank m-tiles (P U_v)
   float mcol[NT][2], lcol[NT][2];
@@ -381,248 +490,234 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
     lcol[nt][0] = lcol[nt][1] = 0.f;
   }
 
-  // the rotated queries come from prep_kernel, which may still be running (dependent launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   int s = 0;
   uint32_t par = 0;
-  bool seg_start = true;
-  for (int64_t f = f0; f < f1; ++f) {
-    const ChunkRec& c = p.c[r.c];
-    const int m = c.rank;
-    const int kvh = r.hg * p.hg + hw;   // this warp's KV head
-    const int head0 = kvh * g;          // its first query head
-    if (seg_start) {
-      // a new segment: this chunk's rotated query and w as B fragments (heads >= g zero)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const int j = nt * 8 + gid;
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-          const uint16_t* qs = p.qhl + (((int64_t)r.c * 2 + part) * p.Hq + head0 + j) * D + 2 * tig;
-          const uint16_t* ws = p.whl + (((int64_t)r.c * 2 + part) * p.Hq + head0 + j) * p.m_max + 2 * tig;
-#pragma unroll
-          for (int kk = 0; kk < KT; ++kk) {
-            qb[kk][nt][part][0] = j < g ? ldg32(qs + kk * 16) : 0u;
-            qb[kk][nt][part][1] = j < g ? ldg32(qs + kk * 16 + 8) : 0u;
-          }
-#pragma unroll
-          for (int kk = 0; kk < RT; ++kk) {
-            const bool ok = j < g && kk * 16 < m;
-            wb[kk][nt][part][0] = ok ? ldg32(ws + kk * 16) : 0u;
-            wb[kk][nt][part][1] = ok ? ldg32(ws + kk * 16 + 8) : 0u;
-          }
-        }
-      }
-      // the value patch rows V_v,h are used when the segment ends: start them towards L2
-      if (m > 0)
-        for (int e = lane; e < D * m / 64; e += 32)
-          asm volatile("prefetch.global.L2 [%0];" ::"l"(c.vv + (int64_t)kvh * D * m + e * 64));
-      seg_start = false;
-    }
-    if (!wait_phase(full(s), par, abort_p, p.status)) break;
-    const int nv = min(kSlice, c.n_tokens - (r.k * p.ts + sw * kSlice));   // valid tokens of this slice
-    if (nv > 0) {
-      const uint32_t st = ring + (uint32_t)s * p.stage_bytes;
-      const uint32_t kb = st + (uint32_t)((sw * kSlice) * p.k_pitch + hw * D) * 2;
-      const uint32_t vb = kb + p.kv_bytes;
-      const uint32_t ukb = st + 2 * p.kv_bytes + (uint32_t)(sw * kSlice * m) * 2;
-      const uint32_t uvb = ukb + p.u_bytes;
-
-      // S (16 tokens x 8 NT heads) = K Q^T + U_k W^T, high and low parts in separate chains
-      float sh[NT][4], sl[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < KT; ++kk) {
-        uint32_t a[4];
-        ldsm_x4(a, kb + (uint32_t)(a_row * p.k_pitch + a_col + kk * 16) * 2);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma16816(sh[nt], a, qb[kk][nt][0][0], qb[kk][nt][0][1]);
-          mma16816(sl[nt], a, qb[kk][nt][1][0], qb[kk][nt][1][1]);
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < RT; ++kk) {
-        if (kk * 16 >= m) break;
-        uint32_t a[4];
-        ldsm_x4(a, ukb + (uint32_t)(a_row * m + a_col + kk * 16) * 2);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma16816(sh[nt], a, wb[kk][nt][0][0], wb[kk][nt][0][1]);
-          mma16816(sl[nt], a, wb[kk][nt][1][0], wb[kk][nt][1][1]);
-        }
-      }
-
-      // online softmax per head (column): rows are tokens gid (e = 0, 1) and gid + 8 (e = 2, 3)
-      float alpha[NT][2];
-      uint32_t pb[NT][2][2];   // B fragments of P^T: [n-tile][high, low][tokens 0-7, tokens 8-15]
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float sc[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[e] = sh[nt][e] + sl[nt][e];
-        if (gid >= nv) sc[0] = sc[1] = -INFINITY;
-        if (gid + 8 >= nv) sc[2] = sc[3] = -INFINITY;
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          float mx = fmaxf(sc[e2], sc[e2 + 2]);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(mcol[nt][e2], mx);   // finite: token 0 of the slice is valid
-          alpha[nt][e2] = expf(mcol[nt][e2] - mn);     // 0 while nothing was accumulated
-          mcol[nt][e2] = mn;
-          sc[e2] = expf(sc[e2] - mn);
-          sc[e2 + 2] = expf(sc[e2 + 2] - mn);
-          lcol[nt][e2] = lcol[nt][e2] * alpha[nt][e2] + (sc[e2] + sc[e2 + 2]);
-        }
-        uint16_t hb[4], lb[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          hb[e] = to_bf(sc[e]);
-          lb[e] = to_bf(sc[e] - bf(hb[e]));
-        }
-        // (token, head) pairs in fragment layout, transposed to (head, token): the B operand
-        pb[nt][0][0] = movmatrix_trans(pack_bf(hb[0], hb[1]));
-        pb[nt][0][1] = movmatrix_trans(pack_bf(hb[2], hb[3]));
-        pb[nt][1][0] = movmatrix_trans(pack_bf(lb[0], lb[1]));
-        pb[nt][1][1] = movmatrix_trans(pack_bf(lb[2], lb[3]));
-      }
-
-      // O^T = O^T * alpha + [V | U_v]^T P^T: rows features (then rank columns), columns heads
-#pragma unroll
-      for (int mt = 0; mt < KT + RT; ++mt) {
-        if (mt >= KT && (mt - KT) * 16 >= m) break;
-        uint32_t a[4];
-        if (mt < KT) ldsm_x4_trans(a, vb + (uint32_t)(t_row * p.k_pitch + t_col + mt * 16) * 2);
-        else ldsm_x4_trans(a, uvb + (uint32_t)(t_row * m + t_col + (mt - KT) * 16) * 2);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          o[mt][nt][0] *= alpha[nt][0];
-          o[mt][nt][1] *= alpha[nt][1];
-          o[mt][nt][2] *= alpha[nt][0];
-          o[mt][nt][3] *= alpha[nt][1];
-          mma16816(o[mt][nt], a, pb[nt][0][0], pb[nt][0][1]);
-          mma16816(o[mt][nt], a, pb[nt][1][0], pb[nt][1][1]);
-        }
-      }
-    }
+  auto slot = [&]() { return ring + (uint32_t)s * p.stage_bytes; };
+  auto release = [&]() {
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(s));
     if (++s == p.stages) {
       s = 0;
       par ^= 1u;
     }
+  };
+  bool ok = true;
+  for (int64_t f = f0; f < f1 && ok;) {
+    const int ci = r.c, hgi = r.hg;
+    const ChunkRec& c = p.c[ci];
+    const int m = c.rank;
+    const int n_tok = (int)min((int64_t)(r.nst - r.k), f1 - f);
+    // P slots: this segment's rotated query and w
+    for (int j = 0; j < p.hg; j += p.hp) {
+      ok = wait_phase(full(s), par, abort_p, p.status);
+      if (!ok) break;
+      if (hw >= j && hw < j + p.hp)
+        prepare<D, NT, MCAP>(p, slot() + (uint32_t)((hw - j) * D * m) * 2,
+                             slot() + (uint32_t)(p.hp * D * m + (hw - j) * g * D) * 2, m, p.delta[ci], qb, wb);
+      release();
+    }
+    // token stages
+    for (int k = 0; k < n_tok && ok; ++k, ++f) {
+      ok = wait_phase(full(s), par, abort_p, p.status);
+      if (!ok) break;
+      const int nv = min(kSlice, c.n_tokens - (r.k * p.ts + sw * kSlice));   // valid tokens of this slice
+      if (nv > 0) {
+        const uint32_t st = slot();
+        const uint32_t kb = st + k_lane, vb = st + v_lane;
+        const uint32_t ukb = st + 2 * p.kv_bytes + (uint32_t)(sw * kSlice * m) * 2;
+        const uint32_t uvb = ukb + p.u_bytes;
 
-    if (f + 1 == f1 || r.k + 1 == r.nst) {
-      // segment end.  The value patch: O^T += V_v,h (P U_v)^T, with the rank rows of O^T
-      // as the B operand (fp32 -> high + low bf16, transposed in registers) and
-      // V_v,h [d][m] rows as A, read from global memory.
-      if (m > 0) {
-        const uint16_t* vv = c.vv + (int64_t)kvh * D * m;
+        // S (16 tokens x 8 NT heads) = K Q^T + U_k W^T, high and low parts in separate chains
+        float sh[NT][4], sl[NT][4];
 #pragma unroll
-        for (int rt = 0; rt < RT; ++rt) {
-          if (rt * 16 >= m) break;
-          uint32_t ub[NT][2][2];
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sh[nt][e] = sl[nt][e] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KT; ++kk) {
+          uint32_t a[4];
+          ldsm_x4(a, kb + kk * 32);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const float* u = o[KT + rt][nt];
-            uint16_t hb[4], lb[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              hb[e] = to_bf(u[e]);
-              lb[e] = to_bf(u[e] - bf(hb[e]));
-            }
-            ub[nt][0][0] = movmatrix_trans(pack_bf(hb[0], hb[1]));
-            ub[nt][0][1] = movmatrix_trans(pack_bf(hb[2], hb[3]));
-            ub[nt][1][0] = movmatrix_trans(pack_bf(lb[0], lb[1]));
-            ub[nt][1][1] = movmatrix_trans(pack_bf(lb[2], lb[3]));
+            mma16816(sh[nt], a, qb[kk][nt][0][0], qb[kk][nt][0][1]);
+            mma16816(sl[nt], a, qb[kk][nt][1][0], qb[kk][nt][1][1]);
           }
+        }
 #pragma unroll
-          for (int ft = 0; ft < KT; ++ft) {
-            const uint16_t* va = vv + (int64_t)(ft * 16 + gid) * m + rt * 16 + 2 * tig;
-            uint32_t a[4];
-            a[0] = ldg32(va);
-            a[1] = ldg32(va + 8 * m);
-            a[2] = ldg32(va + 8);
-            a[3] = ldg32(va + 8 * m + 8);
+        for (int kk = 0; kk < RT; ++kk) {
+          if (kk * 16 >= m) break;
+          uint32_t a[4];
+          ldsm_x4(a, ukb + (uint32_t)(a_row * m + a_col + kk * 16) * 2);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              mma16816(o[ft][nt], a, ub[nt][0][0], ub[nt][0][1]);
-              mma16816(o[ft][nt], a, ub[nt][1][0], ub[nt][1][1]);
-            }
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816(sh[nt], a, wb[kk][nt][0][0], wb[kk][nt][0][1]);
+            mma16816(sl[nt], a, wb[kk][nt][1][0], wb[kk][nt][1][1]);
+          }
+        }
+
+        // online softmax per head (column): rows are tokens gid (e = 0, 1) and gid + 8 (e = 2, 3)
+        float alpha[NT][2];
+        uint32_t pb[NT][2][2];   // B fragments of P^T: [n-tile][high, low][tokens 0-7, tokens 8-15]
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float sc[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sc[e] = sh[nt][e] + sl[nt][e];
+          if (gid >= nv) sc[0] = sc[1] = -INFINITY;
+          if (gid + 8 >= nv) sc[2] = sc[3] = -INFINITY;
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            float mx = fmaxf(sc[e2], sc[e2 + 2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(mcol[nt][e2], mx);   // finite: token 0 of the slice is valid
+            alpha[nt][e2] = expf(mcol[nt][e2] - mn);     // 0 while nothing was accumulated
+            mcol[nt][e2] = mn;
+            sc[e2] = expf(sc[e2] - mn);
+            sc[e2 + 2] = expf(sc[e2 + 2] - mn);
+            lcol[nt][e2] = lcol[nt][e2] * alpha[nt][e2] + (sc[e2] + sc[e2 + 2]);
+          }
+          uint16_t hb[4], lb[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hb[e] = to_bf(sc[e]);
+            lb[e] = to_bf(sc[e] - bf(hb[e]));
+          }
+          // (token, head) pairs in fragment layout, transposed to (head, token): the B operand
+          pb[nt][0][0] = movmatrix_trans(pack_bf(hb[0], hb[1]));
+          pb[nt][0][1] = movmatrix_trans(pack_bf(hb[2], hb[3]));
+          pb[nt][1][0] = movmatrix_trans(pack_bf(lb[0], lb[1]));
+          pb[nt][1][1] = movmatrix_trans(pack_bf(lb[2], lb[3]));
+        }
+
+        // O^T = O^T * alpha + [V | U_v]^T P^T: rows features (then rank columns), columns heads
+#pragma unroll
+        for (int mt = 0; mt < KT + RT; ++mt) {
+          if (mt >= KT && (mt - KT) * 16 >= m) break;
+          uint32_t a[4];
+          if (mt < KT) ldsm_x4_trans(a, vb + mt * 32);
+          else ldsm_x4_trans(a, uvb + (uint32_t)(t_row * m + t_col + (mt - KT) * 16) * 2);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            o[mt][nt][0] *= alpha[nt][0];
+            o[mt][nt][1] *= alpha[nt][1];
+            o[mt][nt][2] *= alpha[nt][0];
+            o[mt][nt][3] *= alpha[nt][1];
+            mma16816(o[mt][nt], a, pb[nt][0][0], pb[nt][0][1]);
+            mma16816(o[mt][nt], a, pb[nt][1][0], pb[nt][1][1]);
           }
         }
       }
+      release();
+      if (f + 1 < f1) advance(p, r);
+    }
+    // V slots: the value patch, O^T += V_v,h (P U_v)^T, with the rank rows of O^T as the
+    // B operand (fp32 -> high + low bf16, transposed in registers) and the staged V_v,h
+    // [d][m] rows as A
+    if (m > 0)
+      for (int j = 0; j < p.hg && ok; j += p.hv) {
+        ok = wait_phase(full(s), par, abort_p, p.status);
+      if (!ok) break;
+        if (hw >= j && hw < j + p.hv) {
+          const uint32_t vvs = slot() + (uint32_t)((hw - j) * D * m) * 2;
+#pragma unroll
+          for (int rt = 0; rt < RT; ++rt) {
+            if (rt * 16 >= m) break;
+            uint32_t ub[NT][2][2];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float* u = o[KT + rt][nt];
+              uint16_t hb[4], lb[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                hb[e] = to_bf(u[e]);
+                lb[e] = to_bf(u[e] - bf(hb[e]));
+              }
+              ub[nt][0][0] = movmatrix_trans(pack_bf(hb[0], hb[1]));
+              ub[nt][0][1] = movmatrix_trans(pack_bf(hb[2], hb[3]));
+              ub[nt][1][0] = movmatrix_trans(pack_bf(lb[0], lb[1]));
+              ub[nt][1][1] = movmatrix_trans(pack_bf(lb[2], lb[3]));
+            }
+#pragma unroll
+            for (int ft = 0; ft < KT; ++ft) {
+              uint32_t a[4];
+              ldsm_x4(a, vvs + (uint32_t)((ft * 16 + a_row) * m + rt * 16 + a_col) * 2);
+#pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                mma16816(o[ft][nt], a, ub[nt][0][0], ub[nt][0][1]);
+                mma16816(o[ft][nt], a, ub[nt][1][0], ub[nt][1][1]);
+              }
+            }
+          }
+        }
+        release();
+      }
+    if (!ok) break;
+    // the segment's partial
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        float l = lcol[nt][e2];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        lcol[nt][e2] = l;
+      }
+    // this warp's partial (its KV head's g query heads) to slot (cta, hg, chunk), slice sw
+    float* base = p.partial + ((slot_of(cta, hgi, ci, p.n_chunks) * p.ns + sw) * (p.hg * g) + (int64_t)hw * g) * pw;
+#pragma unroll
+    for (int ft = 0; ft < KT; ++ft)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = nt * 8 + 2 * tig + (e & 1);
+          if (j < g) base[(int64_t)j * pw + ft * 16 + gid + (e >> 1) * 8] = o[ft][nt][e];
+        }
+    if (gid == 0)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
-          float l = lcol[nt][e2];
-          l += __shfl_xor_sync(0xffffffffu, l, 4);
-          l += __shfl_xor_sync(0xffffffffu, l, 8);
-          l += __shfl_xor_sync(0xffffffffu, l, 16);
-          lcol[nt][e2] = l;
+          const int j = nt * 8 + 2 * tig + e2;
+          if (j < g) {
+            base[(int64_t)j * pw + D] = mcol[nt][e2];
+            base[(int64_t)j * pw + D + 1] = lcol[nt][e2];
+          }
         }
-      // this warp's partial (its KV head's g query heads) to slot (cta, hg, chunk), slice sw
-      float* base = p.partial + ((slot_of(cta, r.hg, r.c, p.n_chunks) * p.ns + sw) * (p.hg * g) + (int64_t)hw * g) * pw;
 #pragma unroll
-      for (int ft = 0; ft < KT; ++ft)
+    for (int mt = 0; mt < KT + RT; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = nt * 8 + 2 * tig + (e & 1);
-            if (j < g) base[(int64_t)j * pw + ft * 16 + gid + (e >> 1) * 8] = o[ft][nt][e];
-          }
-      if (gid == 0)
+        for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int j = nt * 8 + 2 * tig + e2;
-            if (j < g) {
-              base[(int64_t)j * pw + D] = mcol[nt][e2];
-              base[(int64_t)j * pw + D + 1] = lcol[nt][e2];
-            }
-          }
-#pragma unroll
-      for (int mt = 0; mt < KT + RT; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[mt][nt][e] = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        mcol[nt][0] = mcol[nt][1] = -INFINITY;
-        lcol[nt][0] = lcol[nt][1] = 0.f;
-      }
-      seg_start = true;
+    for (int nt = 0; nt < NT; ++nt) {
+      mcol[nt][0] = mcol[nt][1] = -INFINITY;
+      lcol[nt][0] = lcol[nt][1] = 0.f;
     }
-    if (f + 1 < f1) advance(p, r);
   }
 }
 
 // One CTA per (sequence, query head).  Merges the partials of the sequence's
-// chunks by their maxima (a partial with no tokens has max -inf and weight 0)
-// and rounds to bf16.  The partials of all the sequence's chunks form one list,
-// taken in groups of kCombineThreads: thread t locates entry t of a group
-// (arithmetic only) and loads its max and sum; the weighted features are then
-// summed with thread -> feature (d = 128) or feature and entry parity (d = 64),
-// up to 32 entries' loads in flight.
+// chunks (a partial with no tokens has max -inf and weight 0) and rounds to bf16.
+// The partials of all the sequence's chunks form one list, taken in groups of
+// kCombineThreads: thread t locates entry t of a group (arithmetic only) and
+// posts its address; then thread -> feature (d = 128) or feature and entry parity
+// (d = 64) loads, for up to kBatch entries at once, each entry's max, sum and
+// feature, and folds them into a running (max, weighted sum, weighted count):
+// one round trip to memory per kBatch entries, no block-wide reduction.
 constexpr int kCombineThreads = 128;
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ Params p) {
   constexpr int G = kCombineThreads / D;   // thread groups, each covering the D features
+  constexpr int kBatch = 32;
   __shared__ const float* ent[kCombineThreads];
-  __shared__ float wts[kCombineThreads];
-  __shared__ float red[kCombineThreads / 32];
-  __shared__ float part[kCombineThreads];
-  asm volatile("griddepcontrol.wait;" ::: "memory");   // the block kernel's partials
-  const int s = blockIdx.x, jq = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ float part[3][kCombineThreads];
+  pdl_wait();   // the block kernel's partials
+  const int s = blockIdx.x, jq = blockIdx.y, tid = threadIdx.x;
   const int g = p.g, pw = D + 2;
   const int h = jq / g, hg = h / p.hg, row = (h % p.hg) * g + jq % g;
   const int64_t total = (int64_t)p.n_hg * p.s_hg;
@@ -643,85 +738,81 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     }
     return n;
   };
-  auto block_reduce = [&](float v, bool is_max) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float o = __shfl_xor_sync(0xffffffffu, v, off);
-      v = is_max ? fmaxf(v, o) : v + o;
-    }
-    __syncthreads();
-    if (lane == 0) red[warp] = v;
-    __syncthreads();
-    v = red[0];
-#pragma unroll
-    for (int w = 1; w < kCombineThreads / 32; ++w) v = is_max ? fmaxf(v, red[w]) : v + red[w];
-    return v;
-  };
-  // the first group's entry, max and sum stay in registers; later groups reload theirs
-  const float* pe0;
-  const int n_list = locate(tid, pe0);
-  const float mx0 = pe0 ? pe0[D] : -INFINITY, l0 = pe0 ? pe0[D + 1] : 0.f;
-  float M = mx0;
-  for (int L0 = kCombineThreads; L0 < n_list; L0 += kCombineThreads) {
-    const float* q;
-    locate(L0 + tid, q);
-    if (q) M = fmaxf(M, q[D]);
-  }
-  M = block_reduce(M, true);
   const int f = tid % D, grp = tid / D;
-  float acc = 0.f, den = 0.f;
-  for (int L0 = 0; L0 < n_list; L0 += kCombineThreads) {
-    const float* pe = pe0;
-    float mx = mx0, lt = l0;
-    if (L0 > 0) {
-      locate(L0 + tid, pe);
-      mx = pe ? pe[D] : -INFINITY;
-      lt = pe ? pe[D + 1] : 0.f;
-    }
-    const float wt = mx == -INFINITY ? 0.f : expf(mx - M);
-    den += wt * lt;
-    __syncthreads();   // the previous group's entries have been read
+  float M = -INFINITY, acc = 0.f, den = 0.f;
+  for (int L0 = 0, n_list = 1; L0 < n_list; L0 += kCombineThreads) {
+    const float* pe;
+    n_list = locate(L0 + tid, pe);
+    __syncthreads();   // the previous group's addresses have been read
     ent[tid] = pe;
-    wts[tid] = wt;
     __syncthreads();
     const int nx = min(kCombineThreads, n_list - L0);
-    for (int x = grp; x < nx; x += 32 * G) {
-      float v[32], w[32];
+    for (int x = grp; x < nx; x += kBatch * G) {
+      float v[kBatch], mx[kBatch], lt[kBatch];
 #pragma unroll
-      for (int y = 0; y < 32; ++y) {
+      for (int y = 0; y < kBatch; ++y) {
         const int xy = x + y * G;
-        w[y] = xy < nx ? wts[xy] : 0.f;
-        v[y] = xy < nx ? ent[xy][f] : 0.f;
+        const float* e = xy < nx ? ent[xy] : nullptr;
+        mx[y] = e ? e[D] : -INFINITY;
+        lt[y] = e ? e[D + 1] : 0.f;
+        v[y] = e ? e[f] : 0.f;
       }
+      float mb = M;
 #pragma unroll
-      for (int y = 0; y < 32; ++y) acc = fmaf(w[y], v[y], acc);
+      for (int y = 0; y < kBatch; ++y) mb = fmaxf(mb, mx[y]);
+      if (mb == -INFINITY) continue;   // nothing accumulated yet, nothing in this batch
+      const float a = expf(M - mb);    // 0 while nothing was accumulated
+      acc *= a;
+      den *= a;
+#pragma unroll
+      for (int y = 0; y < kBatch; ++y) {
+        const float w = expf(mx[y] - mb);   // 0 for an empty partial
+        acc = fmaf(w, v[y], acc);
+        den = fmaf(w, lt[y], den);
+      }
+      M = mb;
     }
   }
-  den = block_reduce(den, false);
-  if (G > 1) {
-    part[tid] = acc;
+  if (G > 1) {   // the groups' running sums, merged by group 0
+    part[0][tid] = M;
+    part[1][tid] = acc;
+    part[2][tid] = den;
     __syncthreads();
     if (grp == 0)
-      for (int k = 1; k < G; ++k) acc += part[k * D + f];
+      for (int k = 1; k < G; ++k) {
+        const float mk = part[0][k * D + f], mb = fmaxf(M, mk);
+        if (mb == -INFINITY) continue;
+        const float a = expf(M - mb), b = expf(mk - mb);
+        acc = acc * a + part[1][k * D + f] * b;
+        den = den * a + part[2][k * D + f] * b;
+        M = mb;
+      }
   }
   if (grp == 0) p.out[((int64_t)s * p.Hq + jq) * D + f] = to_bf(den > 0.f ? acc / den : 0.f);
 }
 
 // ---- host-side planning -----------------------------------------------------
 struct Plan {
-  int hg, n_hg, ns, ts, k_pitch, kv_bytes, u_bytes, stage_bytes, stages;
+  int hg, n_hg, ns, ts, row_bytes, pair_pitch, kv_bytes, u_bytes, stage_bytes, stages, hp, hv;
 };
-Plan make_plan(int n_kv_heads, int head_dim, int m_max) {
+Plan make_plan(int n_kv_heads, int head_dim, int m_max, int g) {
   Plan pl;
   pl.hg = 1;
   while (pl.hg * 2 <= kConsumers && n_kv_heads % (pl.hg * 2) == 0) pl.hg *= 2;
   pl.n_hg = n_kv_heads / pl.hg;
   pl.ns = kConsumers / pl.hg;
   pl.ts = kSlice * pl.ns;
-  pl.k_pitch = pl.hg * head_dim + 8;   // +16 bytes: ldmatrix rows fall in distinct banks
-  pl.kv_bytes = pl.ts * pl.k_pitch * 2;
+  pl.row_bytes = pl.hg * head_dim * 2;
+  pl.pair_pitch = 2 * pl.row_bytes + 16;   // +16 bytes a pair: the 8 rows of an ldmatrix phase span 4 bank groups
+  pl.kv_bytes = pl.ts / 2 * pl.pair_pitch;
   pl.u_bytes = pl.ts * m_max * 2;
-  pl.stage_bytes = (2 * pl.kv_bytes + 2 * pl.u_bytes + 127) / 128 * 128;
+  // a slot holds a token stage, or the P slot (V_k,h and the query rows) or V slot (V_v,h)
+  // of at least one KV head; hp, hv: the most KV heads (a power of two) whose P, V slot fits
+  const int p_head = head_dim * m_max * 2 + g * head_dim * 2, v_head = head_dim * m_max * 2;
+  pl.stage_bytes = (std::max(2 * pl.kv_bytes + 2 * pl.u_bytes, p_head) + 127) / 128 * 128;
+  pl.hp = pl.hv = 1;
+  while (pl.hp * 2 <= pl.hg && pl.hp * 2 * p_head <= pl.stage_bytes) pl.hp *= 2;
+  while (pl.hv * 2 <= pl.hg && pl.hv * 2 * v_head <= pl.stage_bytes) pl.hv *= 2;
   const int budget = kSmemPerSm / kCtasPerSm - 1024 - 256;   // per CTA: reserved and static shared memory
   pl.stages = std::max(2, std::min(kMaxStages, budget / pl.stage_bytes));
   return pl;
@@ -738,7 +829,7 @@ int sm_count() {
 }
 
 size_t partial_bytes(int n_cta_max, int n_chunks, int Hq, int Hkv, int head_dim) {
-  const Plan pl = make_plan(Hkv, head_dim, 0);
+  const Plan pl = make_plan(Hkv, head_dim, 0, Hq / Hkv);
   const int64_t slots = n_cta_max + (int64_t)pl.n_hg * n_chunks;
   return sizeof(float) * (size_t)slots * kConsumers * (Hq / Hkv) * (head_dim + 2);
 }
@@ -756,15 +847,14 @@ size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk
     return 0;
   const int n_cta_max = std::min(attn::kMaxCtas, attn::kCtasPerSm * attn::sm_count());
   const size_t part = attn::partial_bytes(n_cta_max, n_chunks, n_q_heads, n_kv_heads, head_dim);
-  const size_t qhl = (2 * 2 * (size_t)n_chunks * n_q_heads * head_dim + 255) / 256 * 256;
-  const size_t whl = (2 * 2 * (size_t)n_chunks * n_q_heads * attn::kMaxRank + 255) / 256 * 256;
-  return part + qhl + whl + 256;
+  return part + 256;
 }
 
 kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, int32_t n_chunks,
                                 const int32_t* seq_chunks, int32_t n_seqs, int32_t n_q_heads, int32_t n_kv_heads,
                                 int32_t head_dim, double rope_theta, float softmax_scale, void* out,
                                 void* workspace, size_t workspace_bytes, uint32_t* d_status, kvrp_stream_t stream) {
+  g_last_launches = 0;
   if (!q || !chunks || !seq_chunks || !out) return fail(KVRP_ERR_INVALID_ARG, "kv_attend_relocated: NULL argument");
   if (n_chunks <= 0 || n_chunks > attn::kMaxChunks)
     return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: 1 <= n_chunks <= %d", attn::kMaxChunks);
@@ -811,7 +901,7 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   if (!workspace || workspace_bytes < need)
     return fail(KVRP_ERR_WORKSPACE, "kv_attend_relocated: workspace of %zu bytes needed", need);
 
-  const attn::Plan pl = attn::make_plan(n_kv_heads, head_dim, m_max);
+  const attn::Plan pl = attn::make_plan(n_kv_heads, head_dim, m_max, n_q_heads / n_kv_heads);
   static_assert(sizeof(attn::Params) <= 32000, "kernel parameter block too large");
   attn::Params* pp = new attn::Params;   // ~20 KB: off the stack
   std::memset(pp, 0, sizeof(attn::Params));
@@ -820,11 +910,7 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   p.out = static_cast<uint16_t*>(out);
   p.status = d_status;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
-  const size_t qhl_bytes = (2 * 2 * (size_t)n_chunks * n_q_heads * head_dim + 255) / 256 * 256;
-  const size_t whl_bytes = (2 * 2 * (size_t)n_chunks * n_q_heads * attn::kMaxRank + 255) / 256 * 256;
-  p.qhl = reinterpret_cast<uint16_t*>(base);
-  p.whl = reinterpret_cast<uint16_t*>(base + qhl_bytes);
-  p.partial = reinterpret_cast<float*>(base + qhl_bytes + whl_bytes);
+  p.partial = reinterpret_cast<float*>(base);
   p.n_chunks = n_chunks;
   p.n_seqs = n_seqs;
   p.Hq = n_q_heads;
@@ -837,10 +923,13 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   p.ns = pl.ns;
   p.ts = pl.ts;
   p.stages = pl.stages;
-  p.k_pitch = pl.k_pitch;
+  p.row_bytes = pl.row_bytes;
+  p.pair_pitch = pl.pair_pitch;
   p.kv_bytes = pl.kv_bytes;
   p.u_bytes = pl.u_bytes;
   p.stage_bytes = pl.stage_bytes;
+  p.hp = pl.hp;
+  p.hv = pl.hv;
   p.scale = softmax_scale;
   for (int i = 0; i < head_dim / 2; ++i) p.inv_freq[i] = std::pow(rope_theta, -2.0 * i / head_dim);
   int64_t st0 = 0;
@@ -882,33 +971,32 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   const int n_cta_max = std::min(attn::kMaxCtas, attn::kCtasPerSm * attn::sm_count());
   p.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)std::max(per_sm, 1) * attn::sm_count(), (int64_t)n_cta_max,
                                                          (int64_t)p.n_hg * p.s_hg}));
-  if (e == cudaSuccess) {
-    const size_t prep_smem = (size_t)head_dim * (m_max + 8) * 2 + sizeof(float) * p.g * head_dim;
-    e = cudaFuncSetAttribute(attn::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
-    if (e == cudaSuccess) attn::prep_kernel<<<dim3(n_chunks, n_kv_heads), 256, prep_smem, st>>>(p);
-    e = cudaGetLastError();
-  }
-  // prep -> block -> combine as programmatic dependent launches: each may start while
-  // the previous one runs, and waits (griddepcontrol.wait) before it reads that one's results
+  // block -> combine: the combine is a programmatic dependent launch that may start while
+  // the block kernel runs, and waits (griddepcontrol.wait) before it reads the partials
+  int launches = 0;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = st;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
   if (e == cudaSuccess && p.s_hg > 0) {
     cfg.gridDim = dim3(p.n_cta);
     cfg.blockDim = dim3(attn::kThreads);
     cfg.dynamicSmemBytes = smem;
+    cfg.numAttrs = 0;   // plain stream order: it overwrites partials an earlier call's combine may read
     e = cudaLaunchKernelEx(&cfg, blk_fn, p);
+    ++launches;
   }
   if (e == cudaSuccess) {
     cfg.gridDim = dim3(n_seqs, n_q_heads);
     cfg.blockDim = dim3(attn::kCombineThreads);
     cfg.dynamicSmemBytes = 0;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, head_dim == 64 ? attn::combine_kernel<64> : attn::combine_kernel<128>, p);
+    ++launches;
   }
+  g_last_launches = e == cudaSuccess ? launches : 0;
   delete pp;
   if (e != cudaSuccess) return fail(KVRP_ERR_CUDA, "kv_attend_relocated: %s", cudaGetErrorString(e));
   return KVRP_OK;

@@ -27,7 +27,7 @@
 namespace kvrp {
 
 thread_local char g_last_error[512] = "";
-thread_local int32_t g_last_launches = 0;   // kernel launches of this thread's last relocation call
+thread_local int32_t g_last_launches = 0;
 
 kvrp_status fail(kvrp_status st, const char* fmt, ...) {
   va_list ap;

@@ -158,6 +158,8 @@ int32_t upload_launches(size_t n_bytes);
 
 // Host helpers shared by the library's translation units.
 kvrp_status fail(kvrp_status st, const char* fmt, ...);
+// Kernel launches of this host thread's last relocation or attention call.
+extern thread_local int32_t g_last_launches;
 bool aligned16(const void* p);
 // Split phase table of one shift: sections = frequency pairs per (t, h, w)
 // section (plain RoPE: {rot_dim / 2, 0, 0}); layout as the kernel reads it.

@@ -131,11 +131,15 @@ def check(got, q, chunks, seq_chunks, Hq, Hkv, d, theta, scale):
     ([[(9000, 32), (7000, 16)], [(12000, 0)]], 16, 4, 128),                               # long: several stages per CTA
     ([[(300, 64), (129, 128)], [(77, 96)]], 28, 4, 128),                                   # ranks above 32 at head_dim 128
     ([[(200, 128), (33, 64)], [(150, 0)]], 32, 2, 128),                                    # 16 heads per KV head, rank 128
+    # ~16-stage shares on 152 SMs, chunks starting inside shares (mid-share segment changes)
+    ([[(19000, 16), (23000, 32)], [(17000, 0), (21000, 16)]], 8, 4, 64),
 ])
 def test_attention_matches_oracle(seqs, Hq, Hkv, d):
+    import position_invariant_kv_gb300 as kvrp
     theta, scale = 1e6, d ** -0.5
     q, chunks, sc = make_case(7 + Hq, seqs, Hq, Hkv, d)
     got = run_gpu(q, chunks, sc, Hq, Hkv, d, theta, scale)
+    assert kvrp.kvrp_last_launch_count() == 2   # block and combine kernels
     worst = check(got, q, chunks, sc, Hq, Hkv, d, theta, scale)
     print("worst ulp distance", worst)
     # the same chunks read from paged pools (shuffled pages, unused pages NaN): the same bits
@@ -201,6 +205,7 @@ def test_bench_workload_on_sampled_sequences():
     scale = a["d"] ** -0.5
     kvrp.kv_attend_relocated(q, chunks, sc, n_q_heads=a["Hq"], n_kv_heads=a["Hkv"], head_dim=a["d"],
                              rope_theta=a["theta"], softmax_scale=scale, out=out, workspace=ws, d_status=status)
+    assert kvrp.kvrp_last_launch_count() == 2   # block and combine kernels
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     got = _bits(out)
