@@ -80,6 +80,8 @@ struct Params {
   const uint16_t* q;
   uint16_t* out;
   float* partial;      // [slot][slice][hg * g][d + 2]: O (value patch included), max, sum
+  int32_t* seg_cta;    // [2][n_hg][n_chunks]: the first and the last CTA whose share holds
+                       // stages of (head group, chunk), written by the block kernel
   uint32_t* status;
   int n_chunks, n_seqs, Hq, Hkv, d, g, m_max;
   int hg;              // KV heads per head group: a power of two dividing Hkv, at most kConsumers
@@ -101,6 +103,8 @@ struct Params {
   ChunkRec c[kMaxChunks];
   int64_t delta[kMaxChunks];
   int32_t seq_chunk[kMaxChunks + 1];
+  int32_t share0[kMaxCtas + 1];   // CTA i takes stages [share0[i], share0[i + 1])
+  int32_t n_tok[kMaxChunks];      // tokens of each chunk, packed: the combine reads them lane by lane
 };
 
 __device__ __forceinline__ float bf(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -139,16 +143,17 @@ __device__ __forceinline__ void split_hl(float v, uint16_t& hi, uint16_t& lo) {
 // --- the stage sequence ------------------------------------------------------
 // Stage f of the whole job is stage (f mod s_hg) of head group f / s_hg; inside a
 // head group the chunks follow each other, chunk c owning stages
-// [st0, st0 + ceil(n_tokens / ts)).  CTA i takes stages [begin(i), begin(i + 1)).
-__host__ __device__ __forceinline__ int64_t share_begin(int64_t total, int n_cta, int i) {
-  return (int64_t)i * total / n_cta;
-}
-// The CTA whose share holds stage f: the largest i with begin(i) <= f (32-bit division
-// when the product fits, as it does below ~2M stages).
-__host__ __device__ __forceinline__ int share_of(int64_t total, int n_cta, int64_t f) {
-  const int64_t num = (f + 1) * n_cta - 1;
-  if (num < 0x7fffffffLL && total < 0x7fffffffLL) return (int)((uint32_t)num / (uint32_t)total);
-  return (int)(num / total);
+// [st0, st0 + ceil(n_tokens / ts)).  CTA i takes stages [share0[i], share0[i + 1]),
+// boundaries the host places so that every CTA moves about the same bytes.
+// The CTA whose share holds stage f: the largest i with share0[i] <= f.
+__device__ __forceinline__ int share_of(const Params& p, int64_t f) {
+  int lo = 0, hi = p.n_cta - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.share0[mid] <= f) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 // Position in the stage sequence: head group, chunk, stage within the chunk,
 // and the chunk's stage count.  Decoded once per CTA, then advanced.
@@ -311,8 +316,7 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
   __shared__ int abort_flag;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
-  const int64_t total = (int64_t)p.n_hg * p.s_hg;
-  const int64_t f0 = share_begin(total, p.n_cta, cta), f1 = share_begin(total, p.n_cta, cta + 1);
+  const int64_t f0 = p.share0[cta], f1 = p.share0[cta + 1];
   const uint32_t ring = smem_u32(sm);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -372,6 +376,11 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
       const int m = c.rank;
       const int kv0 = r.hg * p.hg;   // the head group's first KV head
       const int n_tok = (int)min((int64_t)(r.nst - r.k), f1 - f);
+      if (lane == 0) {   // for the combine: which CTAs hold this chunk's partials
+        const int64_t cell = (int64_t)r.hg * p.n_chunks + r.c;
+        if (r.k == 0) p.seg_cta[cell] = cta;
+        if (r.k + n_tok == r.nst) p.seg_cta[(int64_t)p.n_hg * p.n_chunks + cell] = cta;
+      }
       // P slots
       for (int j = 0; j < p.hg && ok; j += p.hp) {
         const uint32_t st = acquire();
@@ -703,12 +712,14 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
 
 // One CTA per (sequence, query head).  Merges the partials of the sequence's
 // chunks (a partial with no tokens has max -inf and weight 0) and rounds to bf16.
-// The partials of all the sequence's chunks form one list, taken in groups of
-// kCombineThreads: thread t locates entry t of a group (arithmetic only) and
-// posts its address; then thread -> feature (d = 128) or feature and entry parity
-// (d = 64) loads, for up to kBatch entries at once, each entry's max, sum and
-// feature, and folds them into a running (max, weighted sum, weighted count):
-// one round trip to memory per kBatch entries, no block-wide reduction.
+// The partials of all the sequence's chunks form one list: chunk c contributes one
+// entry per token slice for each CTA from the first to the last that holds its stages
+// (recorded by the block kernel), so the list is laid out from one round trip to
+// memory and a prefix sum in shared memory.  It is then taken in groups of
+// kCombineThreads: thread t locates entry t of a group and posts its address; then
+// thread -> feature (d = 128) or feature and entry parity (d = 64) loads, for up to
+// kBatch entries at once, each entry's max, sum and feature, and folds them into a
+// running (max, weighted sum, weighted count): one round trip per kBatch entries.
 constexpr int kCombineThreads = 128;
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ Params p) {
@@ -716,33 +727,56 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   constexpr int kBatch = 32;
   __shared__ const float* ent[kCombineThreads];
   __shared__ float part[3][kCombineThreads];
-  pdl_wait();   // the block kernel's partials
+  __shared__ int first_cta[kMaxChunks], prefix[kMaxChunks + 1];
+  pdl_wait();   // the block kernel's partials and CTA records
   const int s = blockIdx.x, jq = blockIdx.y, tid = threadIdx.x;
   const int g = p.g, pw = D + 2;
   const int h = jq / g, hg = h / p.hg, row = (h % p.hg) * g + jq % g;
-  const int64_t total = (int64_t)p.n_hg * p.s_hg;
-  // list entry L: its partial (null past the end); returns the list's length
-  auto locate = [&](int L, const float*& pe) {
+  const int c0 = p.seq_chunk[s], nch = p.seq_chunk[s + 1] - c0;
+  // entries of each chunk, then their prefix sum (Hillis and Steele, two values a thread)
+  for (int t = tid; t < kMaxChunks; t += kCombineThreads) {
     int n = 0;
-    pe = nullptr;
-    for (int ci = p.seq_chunk[s]; ci < p.seq_chunk[s + 1]; ++ci) {
-      if (p.c[ci].n_tokens <= 0) continue;
-      const int64_t F0 = (int64_t)hg * p.s_hg + p.c[ci].st0;
-      const int i0 = share_of(total, p.n_cta, F0);
-      const int ne = (share_of(total, p.n_cta, F0 + (p.c[ci].n_tokens + p.ts - 1) / p.ts - 1) - i0 + 1) * p.ns;
-      if (L >= n && L < n + ne) {
-        const int e = L - n;
-        pe = p.partial + ((slot_of(i0 + e / p.ns, hg, ci, p.n_chunks) * p.ns + e % p.ns) * (p.hg * g) + row) * pw;
-      }
-      n += ne;
+    if (t < nch && p.n_tok[c0 + t] > 0) {
+      const int64_t cell = (int64_t)hg * p.n_chunks + c0 + t;
+      const int i0 = p.seg_cta[cell], i1 = p.seg_cta[(int64_t)p.n_hg * p.n_chunks + cell];
+      first_cta[t] = i0;
+      n = (i1 - i0 + 1) * p.ns;
     }
-    return n;
+    prefix[t + 1] = n;
+  }
+  if (tid == 0) prefix[0] = 0;
+  __syncthreads();
+  for (int off = 1; off < kMaxChunks; off <<= 1) {
+    int v[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int t = tid + k * kCombineThreads + 1;
+      v[k] = t > off ? prefix[t - off] : 0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) prefix[tid + k * kCombineThreads + 1] += v[k];
+    __syncthreads();
+  }
+  const int n_list = prefix[nch];
+  // list entry L: its partial (null past the end)
+  auto locate = [&](int L, const float*& pe) {
+    pe = nullptr;
+    if (L >= n_list) return;
+    int lo = 0, hi = nch - 1;   // the chunk: the last k with prefix[k] <= L
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= L) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = L - prefix[lo];
+    pe = p.partial + ((slot_of(first_cta[lo] + e / p.ns, hg, c0 + lo, p.n_chunks) * p.ns + e % p.ns) * (p.hg * g) + row) * pw;
   };
   const int f = tid % D, grp = tid / D;
   float M = -INFINITY, acc = 0.f, den = 0.f;
-  for (int L0 = 0, n_list = 1; L0 < n_list; L0 += kCombineThreads) {
+  for (int L0 = 0; L0 < n_list; L0 += kCombineThreads) {
     const float* pe;
-    n_list = locate(L0 + tid, pe);
+    locate(L0 + tid, pe);
     __syncthreads();   // the previous group's addresses have been read
     ent[tid] = pe;
     __syncthreads();
@@ -818,6 +852,71 @@ Plan make_plan(int n_kv_heads, int head_dim, int m_max, int g) {
   return pl;
 }
 
+// Share boundaries over the stage sequence, every CTA's share costing about the same
+// bytes: a token stage its K, V and factor rows; every segment a share holds (a chunk,
+// or the part of it inside the share) its P and V slots plus kSegmentBytes for the
+// partial it writes and the pipeline's turn.  A greedy walk cuts a share once it reaches
+// the budget T; bisection finds the smallest T that needs at most n_cta shares.  Writes
+// share0[0..count] and returns the count (<= n_cta; every share holds a stage).
+constexpr double kSegmentBytes = 16384.0;
+int split_shares(const Params& p, int n_cta, int head_dim, int32_t* share0) {
+  const int nc = p.n_chunks, D = head_dim;
+  std::vector<double> sc(nc), oc(nc);
+  std::vector<int> nst(nc);
+  double all = 0.0;
+  for (int c = 0; c < nc; ++c) {
+    const double m = p.c[c].rank;
+    nst[c] = (p.c[c].n_tokens + p.ts - 1) / p.ts;
+    sc[c] = p.ts * (4.0 * p.hg * D + 4.0 * m);
+    oc[c] = p.hg * (2.0 * D * m + 2.0 * p.g * D) + (m > 0 ? 2.0 * p.hg * D * m : 0.0) + kSegmentBytes;
+    if (nst[c] > 0) all += p.n_hg * (nst[c] * sc[c] + oc[c]);
+  }
+  const int64_t total = (int64_t)p.n_hg * p.s_hg;
+  auto walk = [&](double T, int32_t* out) {
+    int n = 1;
+    int64_t f = 0, last = 0;
+    double acc = 0.0;
+    if (out) out[0] = 0;
+    auto cut = [&]() {
+      if (out) out[n] = (int32_t)f;
+      ++n;
+      acc = 0.0;
+      last = f;
+    };
+    for (int hg = 0; hg < p.n_hg; ++hg)
+      for (int c = 0; c < nc; ++c) {
+        int left = nst[c];
+        bool charged = false;
+        while (left > 0) {
+          if (!charged) {
+            // entering the chunk: cut first if that ends this share nearer the budget
+            if (f > last && acc + oc[c] + sc[c] - T > T - acc) cut();
+            acc += oc[c];
+            charged = true;
+          }
+          int k = left;   // the chunk's remaining stages, or as many as bring the share nearest T
+          if (T - acc < k * sc[c]) k = std::max(1, std::min(left, (int)std::floor((T - acc) / sc[c] + 0.5)));
+          acc += k * sc[c];
+          left -= k;
+          f += k;
+          if (acc >= T - 0.5 * sc[c] && f < total) {
+            cut();
+            charged = false;
+          }
+        }
+      }
+    if (out) out[n] = (int32_t)total;
+    return n;
+  };
+  double lo = 0.0, hi = all + 1.0;
+  for (int it = 0; it < 64 && hi - lo > 1.0; ++it) {
+    const double mid = 0.5 * (lo + hi);
+    if (walk(mid, nullptr) <= n_cta) hi = mid;
+    else lo = mid;
+  }
+  return walk(hi, share0);
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -846,8 +945,8 @@ size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk
   if (n_chunks <= 0 || !chunk_tokens || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads || head_dim <= 0)
     return 0;
   const int n_cta_max = std::min(attn::kMaxCtas, attn::kCtasPerSm * attn::sm_count());
-  const size_t part = attn::partial_bytes(n_cta_max, n_chunks, n_q_heads, n_kv_heads, head_dim);
-  return part + 256;
+  const size_t part = (attn::partial_bytes(n_cta_max, n_chunks, n_q_heads, n_kv_heads, head_dim) + 255) / 256 * 256;
+  return part + 2 * sizeof(int32_t) * (size_t)n_kv_heads * n_chunks + 256;
 }
 
 kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, int32_t n_chunks,
@@ -911,6 +1010,11 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   p.status = d_status;
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255));
   p.partial = reinterpret_cast<float*>(base);
+  {
+    const int n_cta_max = std::min(attn::kMaxCtas, attn::kCtasPerSm * attn::sm_count());
+    const size_t part = (attn::partial_bytes(n_cta_max, n_chunks, n_q_heads, n_kv_heads, head_dim) + 255) / 256 * 256;
+    p.seg_cta = reinterpret_cast<int32_t*>(base + part);
+  }
   p.n_chunks = n_chunks;
   p.n_seqs = n_seqs;
   p.Hq = n_q_heads;
@@ -946,6 +1050,7 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
       r.table = c.block_table;
       r.num_pages = c.block_table ? c.num_pages : 0;
       r.n_tokens = c.n_tokens;
+      p.n_tok[i] = c.n_tokens;
       r.rank = c.rank;
       r.seq = s;
       r.st0 = (int32_t)st0;
@@ -953,6 +1058,10 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
       st0 += (c.n_tokens + pl.ts - 1) / pl.ts;
     }
   p.s_hg = st0;
+  if ((int64_t)p.n_hg * p.s_hg > INT32_MAX) {
+    delete pp;
+    return fail(KVRP_ERR_UNSUPPORTED, "kv_attend_relocated: at most 2^31 - 1 stages per call");
+  }
   for (int s = 0; s <= n_seqs; ++s) p.seq_chunk[s] = seq_chunks[s];
 
   cudaStream_t st = stream;
@@ -971,6 +1080,7 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   const int n_cta_max = std::min(attn::kMaxCtas, attn::kCtasPerSm * attn::sm_count());
   p.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)std::max(per_sm, 1) * attn::sm_count(), (int64_t)n_cta_max,
                                                          (int64_t)p.n_hg * p.s_hg}));
+  if (p.s_hg > 0) p.n_cta = attn::split_shares(p, p.n_cta, head_dim, p.share0);
   // block -> combine: the combine is a programmatic dependent launch that may start while
   // the block kernel runs, and waits (griddepcontrol.wait) before it reads the partials
   int launches = 0;
