@@ -322,10 +322,6 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kMaxStages + s); };
 
-  // zero the ring: rows past a chunk's end then always hold finite values
-  for (int e = tid; e < p.stages * p.stage_bytes / 16; e += kThreads)
-    reinterpret_cast<uint4*>(sm)[e] = make_uint4(0u, 0u, 0u, 0u);
-  fence_proxy_async_smem();
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(full(s), 1);
@@ -343,6 +339,10 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
 
   if (warp == kConsumers) {
     // ---------------- producer ----------------
+    // This grid may start while the stream's previous kernel still runs (a programmatic
+    // dependent launch): the producer waits for it to complete before its first global
+    // access.  Everything the consumers read or write comes after, through the ring.
+    pdl_wait();
     const int64_t row = (int64_t)p.Hkv * D;
     const uint32_t row_bytes = (uint32_t)p.row_bytes;
     // one head group covering the whole row: two consecutive tokens (of one page) are one
@@ -600,13 +600,24 @@ __global__ void __launch_bounds__(kThreads) block_kernel(const __grid_constant__
           pb[nt][1][1] = movmatrix_trans(pack_bf(lb[2], lb[3]));
         }
 
-        // O^T = O^T * alpha + [V | U_v]^T P^T: rows features (then rank columns), columns heads
+        // O^T = O^T * alpha + [V | U_v]^T P^T: rows features (then rank columns), columns
+        // heads.  Past a ragged slice's end the staged rows are whatever a slot last held
+        // (never written there this stage): their P is 0 and their V, U_v are masked to 0,
+        // so no stale Inf or NaN reaches the sums.
+        const uint32_t keep0 = (2 * tig < nv ? 0xffffu : 0u) | (2 * tig + 1 < nv ? 0xffff0000u : 0u);
+        const uint32_t keep1 = (8 + 2 * tig < nv ? 0xffffu : 0u) | (9 + 2 * tig < nv ? 0xffff0000u : 0u);
 #pragma unroll
         for (int mt = 0; mt < KT + RT; ++mt) {
           if (mt >= KT && (mt - KT) * 16 >= m) break;
-          uint32_t a[4];
+          uint32_t a[4];   // A = [V | U_v]^T: a[0], a[1] tokens 2 tig + {0, 1}; a[2], a[3] tokens 8 + 2 tig + {0, 1}
           if (mt < KT) ldsm_x4_trans(a, vb + mt * 32);
           else ldsm_x4_trans(a, uvb + (uint32_t)(t_row * m + t_col + (mt - KT) * 16) * 2);
+          if (nv < kSlice) {
+            a[0] &= keep0;
+            a[1] &= keep0;
+            a[2] &= keep1;
+            a[3] &= keep1;
+          }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             o[mt][nt][0] *= alpha[nt][0];
@@ -729,6 +740,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
   __shared__ float part[3][kCombineThreads];
   __shared__ int first_cta[kMaxChunks], prefix[kMaxChunks + 1];
   pdl_wait();   // the block kernel's partials and CTA records
+  // the next call's block kernel may start launching: its producer waits for this grid
+  if (threadIdx.x == 0) pdl_launch_dependents();
   const int s = blockIdx.x, jq = blockIdx.y, tid = threadIdx.x;
   const int g = p.g, pw = D + 2;
   const int h = jq / g, hg = h / p.hg, row = (h % p.hg) * g + jq % g;
@@ -1081,8 +1094,10 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
   p.n_cta = (int)std::max<int64_t>(1, std::min<int64_t>({(int64_t)std::max(per_sm, 1) * attn::sm_count(), (int64_t)n_cta_max,
                                                          (int64_t)p.n_hg * p.s_hg}));
   if (p.s_hg > 0) p.n_cta = attn::split_shares(p, p.n_cta, head_dim, p.share0);
-  // block -> combine: the combine is a programmatic dependent launch that may start while
-  // the block kernel runs, and waits (griddepcontrol.wait) before it reads the partials
+  // Both kernels are programmatic dependent launches: each may start while the kernel
+  // before it on the stream runs, and waits (griddepcontrol.wait) for that kernel to
+  // complete before it touches global memory -- the block kernel in its producer, the
+  // combine before it reads the partials.
   int launches = 0;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1094,7 +1109,7 @@ kvrp_status kv_attend_relocated(const void* q, const kvrp_attn_chunk* chunks, in
     cfg.gridDim = dim3(p.n_cta);
     cfg.blockDim = dim3(attn::kThreads);
     cfg.dynamicSmemBytes = smem;
-    cfg.numAttrs = 0;   // plain stream order: it overwrites partials an earlier call's combine may read
+    cfg.numAttrs = 1;   // its producer waits (griddepcontrol.wait) before any global access
     e = cudaLaunchKernelEx(&cfg, blk_fn, p);
     ++launches;
   }
