@@ -52,7 +52,7 @@ constexpr int kMaxK = 96;          // rank + oversampling bound (k x k solves li
 constexpr int kMaxOrbit = 64;      // conditioned caches averaged by one call
 constexpr int kJacobiSweeps = 2;   // the top-m subspace has settled by then (V_m is re-orthonormalised)
 constexpr int kThreads = 256;
-constexpr int kJacThreads = 512;   // jacobi_kernel: at most one 2 x 2 block per thread for k <= 48
+constexpr int kJacThreads = 320;   // jacobi_kernel: one 2 x 2 block of A and one row chunk of V^T per thread for k <= 48
 constexpr int kTile = 128;         // output rows per pass_kernel CTA
 constexpr int kPassStages = 4;     // pass_kernel pipeline depth
 constexpr int kPassK = 64;         // pass_kernel: contraction per stage (one 128-byte swizzle row of bf16)
@@ -145,7 +145,7 @@ __device__ __forceinline__ int tile_at(int row, int tl) {   // index in halves
   return row * kDeltaTokens + ((((tl >> 1) ^ tile_word_swz(row))) << 1) + (tl & 1);
 }
 
-__global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constant__ DeltaArgs a,
+__global__ void __launch_bounds__(kThreads, 2) delta_kernel(const __grid_constant__ DeltaArgs a,
                                                           const __grid_constant__ TableParam tab) {
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
@@ -176,58 +176,56 @@ __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constan
   const bool wide = (sg.turns ? half % 8 == 0 : sg.W % 16 == 0) && a.D % 8 == 0 && sg.f0 % 8 == 0 &&
                     a.canon_stride % 8 == 0 && a.cond_stride % 8 == 0;
   if (wide) {
-    // a thread's units (at most kDeltaWide of them) load everything first, then compute
-    constexpr int kDeltaWide = 2;
-    const int upt = sg.W / 16;
-    const int n_units = kDeltaTokens * upt;
-    for (int u0 = 0; u0 < n_units; u0 += kDeltaWide * kThreads) {
-      uint4 xa[kDeltaWide], xb[kDeltaWide], ca[kDeltaWide], cb[kDeltaWide];
-      int tls[kDeltaWide], e0s[kDeltaWide], e1s[kDeltaWide];
+    // A thread's item: two consecutive tokens x one unit, all eight 16-byte loads issued
+    // first.  The transposed tile then takes one 4-byte word (the token pair) per
+    // feature: with the row swizzle, a warp's 32 stores of one feature offset fall in
+    // distinct banks.
+    const int upt = sg.turns ? half / 8 : sg.W / 16;   // units per token (<= 8)
+    const int it = threadIdx.x;
+    if (it < (kDeltaTokens / 2) * upt) {
+      const int w = it % upt, j = it / upt;            // unit, token pair
+      const int e0 = sg.turns ? 8 * w : 16 * w;
+      const int e1 = sg.turns ? 8 * w + half : 16 * w + 8;
+      uint4 xa[2], xb[2], ca[2], cb[2];
+      bool live[2];
 #pragma unroll
-      for (int b = 0; b < kDeltaWide; ++b) {
-        const int u = u0 + b * kThreads + threadIdx.x;
-        const int tl = u / upt, w = u - (u / upt) * upt;
-        const int t = t0 + tl;
-        const bool live = u < n_units && t < a.T;
-        tls[b] = live ? tl : -1;
-        e0s[b] = sg.turns ? 8 * w : 16 * w;
-        e1s[b] = sg.turns ? 8 * w + half : 16 * w + 8;
-        xa[b] = xb[b] = ca[b] = cb[b] = make_uint4(0u, 0u, 0u, 0u);
-        if (!live) continue;
+      for (int h = 0; h < 2; ++h) {
+        const int t = t0 + 2 * j + h;
+        live[h] = t < a.T;
+        xa[h] = xb[h] = ca[h] = cb[h] = make_uint4(0u, 0u, 0u, 0u);
+        if (!live[h]) continue;
         const int64_t row = (int64_t)t * a.D + sg.f0;
-        xa[b] = *reinterpret_cast<const uint4*>(canon + row + e0s[b]);
-        xb[b] = *reinterpret_cast<const uint4*>(canon + row + e1s[b]);
+        xa[h] = *reinterpret_cast<const uint4*>(canon + row + e0);
+        xb[h] = *reinterpret_cast<const uint4*>(canon + row + e1);
         if (a.n_cond == 1) {
           const uint16_t* c = a.cond[0] + (int64_t)l * a.cond_stride + row;
-          ca[b] = *reinterpret_cast<const uint4*>(c + e0s[b]);
-          cb[b] = *reinterpret_cast<const uint4*>(c + e1s[b]);
+          ca[h] = *reinterpret_cast<const uint4*>(c + e0);
+          cb[h] = *reinterpret_cast<const uint4*>(c + e1);
         }
       }
+      float d0[2][8], d1[2][8];
 #pragma unroll
-      for (int b = 0; b < kDeltaWide; ++b) {
-        const int tl = tls[b];
-        if (tl < 0) continue;
-        const int e0 = e0s[b], e1 = e1s[b];
-        const int64_t row = (int64_t)(t0 + tl) * a.D + sg.f0;
+      for (int h = 0; h < 2; ++h) {
+        const int64_t row = (int64_t)(t0 + 2 * j + h) * a.D + sg.f0;
         float x0[8], x1[8], c0[8], c1[8];
-        bf16x8_to_f(xa[b], x0);
-        bf16x8_to_f(xb[b], x1);
+        bf16x8_to_f(xa[h], x0);
+        bf16x8_to_f(xb[h], x1);
         if (a.n_cond == 1) {
-          bf16x8_to_f(ca[b], c0);
-          bf16x8_to_f(cb[b], c1);
+          bf16x8_to_f(ca[h], c0);
+          bf16x8_to_f(cb[h], c1);
         } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) c0[i] = c1[i] = 0.f;
-          for (int p = 0; p < a.n_cond; ++p) {
-            const uint16_t* c = a.cond[p] + (int64_t)l * a.cond_stride + row;
-            float v0[8], v1[8];
-            bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e0), v0);
-            bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e1), v1);
+          if (live[h])
+            for (int q = 0; q < a.n_cond; ++q) {
+              const uint16_t* c = a.cond[q] + (int64_t)l * a.cond_stride + row;
+              float v0[8], v1[8];
+              bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e0), v0);
+              bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e1), v1);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) { c0[i] += v0[i]; c1[i] += v1[i]; }
-          }
+              for (int i = 0; i < 8; ++i) { c0[i] += v0[i]; c1[i] += v1[i]; }
+            }
         }
-        float d0[8], d1[8];
         if (sg.turns) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {   // pairs e0 + 2q, e0 + 2q + 1
@@ -238,23 +236,26 @@ __global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constan
             const float y01 = fmaf(a1, hd.y, -(b1 * hd.w)) + fmaf(a1, tl4.y, -(b1 * tl4.w));
             const float y10 = fmaf(b0, hd.x, a0 * hd.z) + fmaf(b0, tl4.x, a0 * tl4.z);
             const float y11 = fmaf(b1, hd.y, a1 * hd.w) + fmaf(b1, tl4.y, a1 * tl4.w);
-            d0[2 * q] = c0[2 * q] * a.inv_n - y00;
-            d0[2 * q + 1] = c0[2 * q + 1] * a.inv_n - y01;
-            d1[2 * q] = c1[2 * q] * a.inv_n - y10;
-            d1[2 * q + 1] = c1[2 * q + 1] * a.inv_n - y11;
+            d0[h][2 * q] = c0[2 * q] * a.inv_n - y00;
+            d0[h][2 * q + 1] = c0[2 * q + 1] * a.inv_n - y01;
+            d1[h][2 * q] = c1[2 * q] * a.inv_n - y10;
+            d1[h][2 * q + 1] = c1[2 * q + 1] * a.inv_n - y11;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) { d0[i] = c0[i] * a.inv_n - x0[i]; d1[i] = c1[i] * a.inv_n - x1[i]; }
+          for (int i = 0; i < 8; ++i) { d0[h][i] = c0[i] * a.inv_n - x0[i]; d1[h][i] = c1[i] * a.inv_n - x1[i]; }
         }
-        uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
-        *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0);
-        *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1);
+        if (live[h]) {
+          uint16_t* o = out + (int64_t)(t0 + 2 * j + h) * a.Dp + sg.f0;
+          *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0[h]);
+          *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1[h]);
+        }
+      }
+      uint32_t* tw = reinterpret_cast<uint32_t*>(tile);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          tile[tile_at(e0 + i, tl)] = f_to_bf16(d0[i]);
-          tile[tile_at(e1 + i, tl)] = f_to_bf16(d1[i]);
-        }
+      for (int i = 0; i < 8; ++i) {
+        tw[(e0 + i) * (kDeltaTokens / 2) + (j ^ tile_word_swz(e0 + i))] = f2_to_bf16x2(d0[0][i], d0[1][i]);
+        tw[(e1 + i) * (kDeltaTokens / 2) + (j ^ tile_word_swz(e1 + i))] = f2_to_bf16x2(d1[0][i], d1[1][i]);
       }
     }
   } else {
@@ -857,9 +858,10 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
   extern __shared__ __align__(16) float smj[];
-  const int P = kp + 1;
+  const int P = kp + 1;     // A's row pitch: neighbouring rows start in different banks
+  const int PV = kp + 4;    // V^T's row pitch: rows 16-byte aligned for float4 access
   float* A = smj;
-  float* V = smj + kp * P;
+  float* VT = smj + (kp * P + 3) / 4 * 4;   // V^T: row r is column r of the accumulated rotations
   __shared__ int4 rot[kMaxK / 2];      // {p, q, cos, sin} of each pair of the step
   __shared__ int order[kMaxK];
   __shared__ float scratch[NT / 32];
@@ -872,7 +874,7 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
     const int i = e / kp, j = e - (e / kp) * kp;
     const float v = (i < k && j < k) ? 0.5f * (c[i * kp + j] + c[j * kp + i]) : 0.f;
     A[i * P + j] = v;
-    V[i * P + j] = i == j ? 1.f : 0.f;
+    VT[i * PV + j] = i == j ? 1.f : 0.f;
     ss += v * v;
   }
   // entries below floor_abs are rounding noise of the fp32 input
@@ -890,9 +892,13 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
       for (int t2 = t1; t2 < np; ++t2, ++idx)
         if (idx % NT == tid && nb < kMaxBlk) blk[nb++] = (t1 << 8) | t2;
   }
-  // eigenvector rows: thread -> row vj, pairs vh, vh + H, ...
-  const int H = max(1, NT / k);
-  const int vj = tid % k, vh = tid / k;
+  // V <- V J is V^T <- J^T V^T: rows p and q of V^T, in float4 chunks; this thread's
+  // (pair, chunk) items, the same at every step
+  const int nch = (k + 3) / 4;
+  constexpr int kMaxVit = ((kMaxK / 2) * (kMaxK / 4) + NT - 1) / NT;
+  int vit[kMaxVit];
+  int nv = 0;
+  for (int it = tid; it < np * nch && nv < kMaxVit; it += NT) vit[nv++] = ((it / nch) << 8) | (4 * (it % nch));
   for (int sweep = 0; sweep < kJacobiSweeps; ++sweep) {
     if (tid == 0) rotated = 0;
     __syncthreads();
@@ -952,16 +958,19 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
           A[p2 * P + p1] = na; A[q2 * P + p1] = nb2; A[p2 * P + q1] = nc; A[q2 * P + q1] = nd;
         }
       }
-      if (vh < H) {   // V <- V J on row vj
-        for (int t = vh; t < np; t += H) {
-          const int4 r = rot[t];
-          const float s = __int_as_float(r.w);
-          if (s == 0.f) continue;
-          const float cc = __int_as_float(r.z);
-          const float vp = V[vj * P + r.x], vq = V[vj * P + r.y];
-          V[vj * P + r.x] = cc * vp - s * vq;
-          V[vj * P + r.y] = s * vp + cc * vq;
-        }
+#pragma unroll
+      for (int u = 0; u < kMaxVit; ++u) {
+        if (u >= nv) break;
+        const int4 r = rot[vit[u] >> 8];
+        const float s = __int_as_float(r.w);
+        if (s == 0.f) continue;
+        const float cc = __int_as_float(r.z);
+        const int c4 = vit[u] & 0xFF;
+        float4* vp = reinterpret_cast<float4*>(VT + r.x * PV + c4);
+        float4* vq = reinterpret_cast<float4*>(VT + r.y * PV + c4);
+        const float4 a = *vp, b = *vq;
+        *vp = make_float4(cc * a.x - s * b.x, cc * a.y - s * b.y, cc * a.z - s * b.z, cc * a.w - s * b.w);
+        *vq = make_float4(s * a.x + cc * b.x, s * a.y + cc * b.y, s * a.z + cc * b.z, s * a.w + cc * b.w);
       }
       __syncthreads();
     }
@@ -986,7 +995,7 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
     if (i < k && r < m && r < k) {
       const int o = order[r];
       const float lam = A[o * P + o];
-      if (lam > 1e-10f * lmax && lam > 0.f) v = V[i * P + o] * rsqrtf(lam);
+      if (lam > 1e-10f * lmax && lam > 0.f) v = VT[o * PV + i] * rsqrtf(lam);
     }
     w[e] = v;
   }
@@ -1275,11 +1284,11 @@ class Runner {
     }
     err = cudaGetLastError();
   }
-  size_t jacobi_smem() const { return sizeof(float) * 2 * (size_t)kp_ * (kp_ + 1); }
+  size_t jacobi_smem() const { return sizeof(float) * ((size_t)(kp_ * (kp_ + 1) + 3) / 4 * 4 + (size_t)kp_ * (kp_ + 4)); }
 
   static cudaError_t configure() {
     cudaError_t e = cudaSuccess;
-    const int jac = (int)(sizeof(float) * 2 * kMaxK * (kMaxK + 1));
+    const int jac = (int)(sizeof(float) * ((kMaxK * (kMaxK + 1) + 3) / 4 * 4 + kMaxK * (kMaxK + 4)));
     if (e == cudaSuccess) e = cudaFuncSetAttribute(jacobi_kernel<kJacThreads>, cudaFuncAttributeMaxDynamicSharedMemorySize, jac);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(pass_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pass_smem_bytes(kMaxK));
