@@ -145,7 +145,7 @@ __device__ __forceinline__ int tile_at(int row, int tl) {   // index in halves
   return row * kDeltaTokens + ((((tl >> 1) ^ tile_word_swz(row))) << 1) + (tl & 1);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) delta_kernel(const __grid_constant__ DeltaArgs a,
+__global__ void __launch_bounds__(kThreads, 3) delta_kernel(const __grid_constant__ DeltaArgs a,
                                                           const __grid_constant__ TableParam tab) {
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
@@ -176,56 +176,58 @@ __global__ void __launch_bounds__(kThreads, 2) delta_kernel(const __grid_constan
   const bool wide = (sg.turns ? half % 8 == 0 : sg.W % 16 == 0) && a.D % 8 == 0 && sg.f0 % 8 == 0 &&
                     a.canon_stride % 8 == 0 && a.cond_stride % 8 == 0;
   if (wide) {
-    // A thread's item: two consecutive tokens x one unit, all eight 16-byte loads issued
-    // first.  The transposed tile then takes one 4-byte word (the token pair) per
-    // feature: with the row swizzle, a warp's 32 stores of one feature offset fall in
-    // distinct banks.
-    const int upt = sg.turns ? half / 8 : sg.W / 16;   // units per token (<= 8)
-    const int it = threadIdx.x;
-    if (it < (kDeltaTokens / 2) * upt) {
-      const int w = it % upt, j = it / upt;            // unit, token pair
-      const int e0 = sg.turns ? 8 * w : 16 * w;
-      const int e1 = sg.turns ? 8 * w + half : 16 * w + 8;
-      uint4 xa[2], xb[2], ca[2], cb[2];
-      bool live[2];
+    // a thread's units (at most kDeltaWide of them) load everything first, then compute
+    constexpr int kDeltaWide = 2;
+    const int upt = sg.W / 16;
+    const int n_units = kDeltaTokens * upt;
+    for (int u0 = 0; u0 < n_units; u0 += kDeltaWide * kThreads) {
+      uint4 xa[kDeltaWide], xb[kDeltaWide], ca[kDeltaWide], cb[kDeltaWide];
+      int tls[kDeltaWide], e0s[kDeltaWide], e1s[kDeltaWide];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int t = t0 + 2 * j + h;
-        live[h] = t < a.T;
-        xa[h] = xb[h] = ca[h] = cb[h] = make_uint4(0u, 0u, 0u, 0u);
-        if (!live[h]) continue;
+      for (int b = 0; b < kDeltaWide; ++b) {
+        const int u = u0 + b * kThreads + threadIdx.x;
+        const int tl = u / upt, w = u - (u / upt) * upt;
+        const int t = t0 + tl;
+        const bool live = u < n_units && t < a.T;
+        tls[b] = live ? tl : -1;
+        e0s[b] = sg.turns ? 8 * w : 16 * w;
+        e1s[b] = sg.turns ? 8 * w + half : 16 * w + 8;
+        xa[b] = xb[b] = ca[b] = cb[b] = make_uint4(0u, 0u, 0u, 0u);
+        if (!live) continue;
         const int64_t row = (int64_t)t * a.D + sg.f0;
-        xa[h] = *reinterpret_cast<const uint4*>(canon + row + e0);
-        xb[h] = *reinterpret_cast<const uint4*>(canon + row + e1);
+        xa[b] = *reinterpret_cast<const uint4*>(canon + row + e0s[b]);
+        xb[b] = *reinterpret_cast<const uint4*>(canon + row + e1s[b]);
         if (a.n_cond == 1) {
           const uint16_t* c = a.cond[0] + (int64_t)l * a.cond_stride + row;
-          ca[h] = *reinterpret_cast<const uint4*>(c + e0);
-          cb[h] = *reinterpret_cast<const uint4*>(c + e1);
+          ca[b] = *reinterpret_cast<const uint4*>(c + e0s[b]);
+          cb[b] = *reinterpret_cast<const uint4*>(c + e1s[b]);
         }
       }
-      float d0[2][8], d1[2][8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t row = (int64_t)(t0 + 2 * j + h) * a.D + sg.f0;
+      for (int b = 0; b < kDeltaWide; ++b) {
+        const int tl = tls[b];
+        if (tl < 0) continue;
+        const int e0 = e0s[b], e1 = e1s[b];
+        const int64_t row = (int64_t)(t0 + tl) * a.D + sg.f0;
         float x0[8], x1[8], c0[8], c1[8];
-        bf16x8_to_f(xa[h], x0);
-        bf16x8_to_f(xb[h], x1);
+        bf16x8_to_f(xa[b], x0);
+        bf16x8_to_f(xb[b], x1);
         if (a.n_cond == 1) {
-          bf16x8_to_f(ca[h], c0);
-          bf16x8_to_f(cb[h], c1);
+          bf16x8_to_f(ca[b], c0);
+          bf16x8_to_f(cb[b], c1);
         } else {
 #pragma unroll
           for (int i = 0; i < 8; ++i) c0[i] = c1[i] = 0.f;
-          if (live[h])
-            for (int q = 0; q < a.n_cond; ++q) {
-              const uint16_t* c = a.cond[q] + (int64_t)l * a.cond_stride + row;
-              float v0[8], v1[8];
-              bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e0), v0);
-              bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e1), v1);
+          for (int p = 0; p < a.n_cond; ++p) {
+            const uint16_t* c = a.cond[p] + (int64_t)l * a.cond_stride + row;
+            float v0[8], v1[8];
+            bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e0), v0);
+            bf16x8_to_f(*reinterpret_cast<const uint4*>(c + e1), v1);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) { c0[i] += v0[i]; c1[i] += v1[i]; }
-            }
+            for (int i = 0; i < 8; ++i) { c0[i] += v0[i]; c1[i] += v1[i]; }
+          }
         }
+        float d0[8], d1[8];
         if (sg.turns) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {   // pairs e0 + 2q, e0 + 2q + 1
@@ -236,26 +238,23 @@ __global__ void __launch_bounds__(kThreads, 2) delta_kernel(const __grid_constan
             const float y01 = fmaf(a1, hd.y, -(b1 * hd.w)) + fmaf(a1, tl4.y, -(b1 * tl4.w));
             const float y10 = fmaf(b0, hd.x, a0 * hd.z) + fmaf(b0, tl4.x, a0 * tl4.z);
             const float y11 = fmaf(b1, hd.y, a1 * hd.w) + fmaf(b1, tl4.y, a1 * tl4.w);
-            d0[h][2 * q] = c0[2 * q] * a.inv_n - y00;
-            d0[h][2 * q + 1] = c0[2 * q + 1] * a.inv_n - y01;
-            d1[h][2 * q] = c1[2 * q] * a.inv_n - y10;
-            d1[h][2 * q + 1] = c1[2 * q + 1] * a.inv_n - y11;
+            d0[2 * q] = c0[2 * q] * a.inv_n - y00;
+            d0[2 * q + 1] = c0[2 * q + 1] * a.inv_n - y01;
+            d1[2 * q] = c1[2 * q] * a.inv_n - y10;
+            d1[2 * q + 1] = c1[2 * q + 1] * a.inv_n - y11;
           }
         } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) { d0[h][i] = c0[i] * a.inv_n - x0[i]; d1[h][i] = c1[i] * a.inv_n - x1[i]; }
+          for (int i = 0; i < 8; ++i) { d0[i] = c0[i] * a.inv_n - x0[i]; d1[i] = c1[i] * a.inv_n - x1[i]; }
         }
-        if (live[h]) {
-          uint16_t* o = out + (int64_t)(t0 + 2 * j + h) * a.Dp + sg.f0;
-          *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0[h]);
-          *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1[h]);
-        }
-      }
-      uint32_t* tw = reinterpret_cast<uint32_t*>(tile);
+        uint16_t* o = out + (int64_t)(t0 + tl) * a.Dp + sg.f0;
+        *reinterpret_cast<uint4*>(o + e0) = f_to_bf16x8(d0);
+        *reinterpret_cast<uint4*>(o + e1) = f_to_bf16x8(d1);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        tw[(e0 + i) * (kDeltaTokens / 2) + (j ^ tile_word_swz(e0 + i))] = f2_to_bf16x2(d0[0][i], d0[1][i]);
-        tw[(e1 + i) * (kDeltaTokens / 2) + (j ^ tile_word_swz(e1 + i))] = f2_to_bf16x2(d1[0][i], d1[1][i]);
+        for (int i = 0; i < 8; ++i) {
+          tile[tile_at(e0 + i, tl)] = f_to_bf16(d0[i]);
+          tile[tile_at(e1 + i, tl)] = f_to_bf16(d1[i]);
+        }
       }
     }
   } else {
