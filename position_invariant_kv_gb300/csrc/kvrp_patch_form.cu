@@ -976,12 +976,16 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
     if (!rotated) break;
     __syncthreads();
   }
-  // descending order by rank counting (ties by index)
+  // descending order by rank counting (ties by index).  A NaN diagonal (NaN in the caller's
+  // caches) ranks below every number: the comparison stays a strict total order, so the
+  // ranks are a permutation of 0 .. k - 1 and every order[] entry read below is set.
   if (tid < k) {
-    const float li = A[tid * P + tid];
+    const float di = A[tid * P + tid];
+    const float li = isnan(di) ? -INFINITY : di;
     int rank = 0;
     for (int j = 0; j < k; ++j) {
-      const float lj = A[j * P + j];
+      const float dj = A[j * P + j];
+      const float lj = isnan(dj) ? -INFINITY : dj;
       rank += (lj > li) || (lj == li && j < tid);
     }
     order[rank] = tid;

@@ -212,6 +212,28 @@ def test_zero_deficit_gives_a_zero_patch():
     assert np.max(np.abs(bf16_bits_to_f64(u)[0] @ bf16_bits_to_f64(v)[0].T)) < 1e-6
 
 
+def test_nan_in_one_layer_stays_in_that_layer():
+    """A NaN in one layer's conditioned cache (a caller's bad input) must neither fault nor
+    leak: the call completes, that layer's factors come out NaN or zero, and every other
+    layer's factors are as good as without the NaN.  The eigen-solve ranks NaN eigenvalue
+    estimates below every number, so its ordering stays a permutation.  The other layers
+    are compared by residual: the split-K passes sum in a free order."""
+    from oracle import bf16_bits_to_f64
+    canon, cond = make_case(41, 3, 300, 256, "heads", 128, 777, 1e4, 12)
+    bad = cond.copy()
+    bad[1, 17, 5] = 0x7FC0   # a quiet NaN in layer 1
+    u0, v0 = form_on_gpu(canon, cond, "heads", 128, 777, 1e4, 16, 8, 2)
+    u1, v1 = form_on_gpu(canon, bad, "heads", 128, 777, 1e4, 16, 8, 2)
+    f1 = bf16_bits_to_f64(u1[1]) @ bf16_bits_to_f64(v1[1]).T
+    assert np.all(~np.isfinite(f1) | (f1 == 0.0))
+    d = oracle_delta(canon, cond, "heads", 128, 777, 1e4)
+    for l in (0, 2):
+        assert np.all(np.isfinite(bf16_bits_to_f64(u1[l]))) and np.all(np.isfinite(bf16_bits_to_f64(v1[l])))
+        (g0, ref, _, _), = residuals(d, u0, v0, 16, layers=[l])
+        (g1, _, _, _), = residuals(d, u1, v1, 16, layers=[l])
+        assert abs(g1 - g0) <= 1e-3 * g0 and g1 <= 1.05 * ref, (l, g0, g1, ref)
+
+
 def make_orbit_case(seed, L, T, D, kind, rot_dim, deltas, theta, shared_rank=8, own_rank=4, noise=1e-3):
     """Canonical cache and one conditioned cache per ordering pi:
     cond_pi = bf16(R(delta_pi) canon + S + P_pi + noise), S shared by every
