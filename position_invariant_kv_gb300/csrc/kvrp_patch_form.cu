@@ -1209,8 +1209,13 @@ class Runner {
       if (err != cudaSuccess) return;
     }
     PassArgs pa{out, sO, M, K, kp_, b_layered ? 1 : 0, per, splits, L_, status_};
+    // as many CTAs as keep the item rounds the same, each taking an equal number of items:
+    // 448 items on 304 slots still take two rounds, so 224 CTAs do them and the other SMs
+    // stay free for concurrent work (another call's solves)
     const int items = tiles * splits * L_;
-    err = launch_pdl(pass_kernel, dim3(std::min(items, cap)), dim3(kPassThreads), pass_smem_bytes(kp_), st_, ma, mb, pa);
+    const int rounds = (items + cap - 1) / cap;
+    err = launch_pdl(pass_kernel, dim3((items + rounds - 1) / rounds), dim3(kPassThreads), pass_smem_bytes(kp_), st_, ma,
+                     mb, pa);
   }
 
   // G[L][kp][kp] = X^T X for X [L][R][kp]
