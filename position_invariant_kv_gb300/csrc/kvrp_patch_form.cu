@@ -575,14 +575,27 @@ __device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], 
 
 // G = X^T X on the tensor cores: each fp32 value splits into a tf32 high part and
 // a tf32 remainder, and G takes hi.hi + hi.lo + lo.hi (the lo.lo term is below
-// fp32 rounding of the sum).  Warp w owns output tiles (16 x 8) w, w + 8, ...,
-// and runs every staged row through them.
+// fp32 rounding of the sum).  G is symmetric, so only the 16 x 8 output tiles that
+// reach the upper triangle are formed (tile (mt, nt) with nt >= 2 mt: 12 of 18 at
+// KP = 48); its readers take entry (min(i, j), max(i, j)).  Warp w owns tiles
+// w, w + 8, ... of that list and runs every staged row through them.
 template <int KP>
 __global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t sX, float* G, int64_t sG, int R,
                                                         int rows_per_cta) {
   pdl_wait();               // the previous kernel's results are visible
   pdl_launch_dependents();  // the next kernel may start launching
-  constexpr int MT = KP / 16, NT = KP / 8, TILES = MT * NT, TPW = (TILES + 7) / 8;   // tiles per warp
+  constexpr int MT = KP / 16, NT = KP / 8;
+  constexpr int TILES = MT * NT - MT * (MT - 1);   // row mt holds the NT - 2 mt tiles nt >= 2 mt
+  constexpr int TPW = (TILES + 7) / 8;             // tiles per warp
+  // tile t of the list: its row mt, the first tile of that row S(mt) = mt NT - mt (mt - 1)
+  auto tile_of = [](int t, int& m0, int& n0) {
+    int mt = 0;
+#pragma unroll
+    for (int r = 1; r < MT; ++r)
+      if (r * NT - r * (r - 1) <= t) mt = r;
+    m0 = 16 * mt;
+    n0 = 8 * (2 * mt + t - (mt * NT - mt * (mt - 1)));
+  };
   constexpr int XP = KP + 8;   // staged row pitch: fragment reads fall in distinct banks
   constexpr int CH = KP <= 48 ? 32 : 16;   // rows per stage (static shared memory < 48 KB)
   __shared__ __align__(16) float xs[2][CH][XP];         // fp32 rows, by cp.async
@@ -626,7 +639,8 @@ __global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t 
       for (int i = 0; i < TPW; ++i) {
         const int t = warp + 8 * i;
         if (t >= TILES) break;
-        const int m0 = (t / NT) * 16, n0 = (t % NT) * 8;
+        int m0, n0;
+        tile_of(t, m0, n0);
         // A = X^T (rows m, columns k), B = X (rows k, columns n)
         const uint32_t ah[4] = {xh[k0 + tig][m0 + gid], xh[k0 + tig][m0 + gid + 8], xh[k0 + tig + 4][m0 + gid],
                                 xh[k0 + tig + 4][m0 + gid + 8]};
@@ -644,7 +658,8 @@ __global__ void __launch_bounds__(kThreads) gram_kernel(const float* X, int64_t 
   for (int i = 0; i < TPW; ++i) {
     const int t = warp + 8 * i;
     if (t >= TILES) break;
-    const int m0 = (t / NT) * 16, n0 = (t % NT) * 8;
+    int m0, n0;
+    tile_of(t, m0, n0);
 #pragma unroll
     for (int e = 0; e < 4; ++e) atomicAdd(&g[(m0 + gid + (e >> 1) * 8) * KP + n0 + 2 * tig + (e & 1)], acc[i][e]);
   }
@@ -757,7 +772,7 @@ __global__ void __launch_bounds__(kThreads) chol_kernel(float* G, int64_t sG, fl
   float tr = 0.f;
   for (int e = tid; e < KP * KP; e += kThreads) {
     const int i = e / KP, j = e - i * KP;
-    const float v = (i < k && j < k) ? 0.5f * (g[i * KP + j] + g[j * KP + i]) : (i == j ? 1.f : 0.f);
+    const float v = (i < k && j < k) ? g[min(i, j) * KP + max(i, j)] : (i == j ? 1.f : 0.f);   // the upper triangle
     A[i * P + j] = v;
     if (i == j && i < k) tr += v;
   }
@@ -871,7 +886,7 @@ __global__ void __launch_bounds__(NT) jacobi_kernel(float* Cm, int64_t sC, float
   float ss = 0.f;
   for (int e = tid; e < kp * kp; e += NT) {
     const int i = e / kp, j = e - (e / kp) * kp;
-    const float v = (i < k && j < k) ? 0.5f * (c[i * kp + j] + c[j * kp + i]) : 0.f;
+    const float v = (i < k && j < k) ? c[min(i, j) * kp + max(i, j)] : 0.f;   // the upper triangle
     A[i * P + j] = v;
     VT[i * PV + j] = i == j ? 1.f : 0.f;
     ss += v * v;
