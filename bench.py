@@ -680,11 +680,14 @@ def patch_form_setup(wl, orbit: int, device):
 def patch_bytes(L, T, D, m, p, q, orbit) -> int:
     """Bytes this method moves per tensor: read the caches (bf16), write the
     deficit twice (bf16 rows and transposed rows), 2q + 3 tensor-core passes
-    over it (bf16), and the small fp32 / bf16 operands and factors."""
+    over it (bf16), the small fp32 operands (each pass's output, and the Gram's
+    and the apply's reads in each of the 2q + 2 orthonormalisation rounds), and
+    the factors."""
     kp = (m + p + 15) // 16 * 16
     n = L * T * D
     skinny = L * (T + D) * kp * 4
-    return n * 2 * (1 + orbit) + n * 4 + (2 * q + 3) * n * 2 + (2 * q + 3) * 3 * skinny + L * (T + D) * m * 2
+    return (n * 2 * (1 + orbit) + n * 4 + (2 * q + 3) * n * 2 + ((2 * q + 3) + 2 * (2 * q + 2)) * skinny
+            + L * (T + D) * m * 2)
 
 
 def patch_form_jobs(tensors, n_layers: int, streams: int):
@@ -822,9 +825,9 @@ def bench_patch_form(args) -> dict:
                      "frac": achieved / peaks["hbm_gbs"], "traffic": None,
                      "kernel": "kv_patch_form_orbit, whole call (delta, tensor-core passes, k x k solves)",
                      "peak_source": peaks["source"]},
-        # per call: deficit, Omega transpose, 2q + 3 passes over the deficit, 2q + 3 orthonormalisation
+        # per call: deficit, Omega transpose, 2q + 3 passes over the deficit, 2q + 2 orthonormalisation
         # rounds of (Gram, Cholesky, apply), the projected Gram, Jacobi, the B^T W apply, U and V writers
-        "gpu_launches": steps * len(jobs) * (2 + (2 * q + 3) + 3 * (2 * q + 3) + 5),
+        "gpu_launches": steps * len(jobs) * (2 + (2 * q + 3) + 3 * (2 * q + 2) + 5),
         "clocks": clocks.summary(),
         "device_status": int(d_status.item()),
     }

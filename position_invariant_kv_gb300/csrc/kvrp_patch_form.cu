@@ -21,8 +21,10 @@
 //   4. C = U_B Lambda U_B^T by parallel cyclic Jacobi; W = U_B[:, :m] Lambda_m^(-1/2);
 //   5. V_m = orth(B^T W) (orthonormal right factors), U_m = Delta V_m.
 // orth() is shifted Cholesky QR: X <- X R^-1 with R^T R = X^T X + s I, the
-// shift s a small multiple of trace(X^T X) (one round inside the subspace
-// iterations, two for the final basis).
+// shift s a small multiple of trace(X^T X), one round each time.  After the
+// subspace iterations the final Y is conditioned like Delta's top singular values
+// (one product past an orthonormal basis), and V_m is orthonormalised again at the
+// end, so a second round on Q changes no residual measurably.
 //
 // The passes over Delta (steps 2, 3 and 5: 2q + 3 of them) are the bulk of the
 // work: tall-skinny products with k <= 96 columns, run on the tensor cores by
@@ -1442,7 +1444,7 @@ kvrp_status kv_patch_form_orbit(const void* const* conditioned, const int64_t* d
     run.pass(b.delta, b.Dp, b.s_delta, b.st_d, b.Dp, b.s_st_d, true, y, b.s_tk, T, D);              // Y = Delta Zq
   }
   // 3. Q = orth(Y); B^T = Delta^T Q; C = B B^T
-  run.orth(y, y2, b.s_tk, T, k, 2, pf::kShiftFirst, b.g, b.rfac, b.st_t, b.s_st_t, (int)b.Tp);
+  run.orth(y, y2, b.s_tk, T, k, 1, pf::kShiftFirst, b.g, b.rfac, b.st_t, b.s_st_t, (int)b.Tp);
   run.pass(b.delta_t, b.Tp, b.s_delta_t, b.st_t, b.Tp, b.s_st_t, true, z, b.s_dk, D, T);
   run.gram(z, b.s_dk, b.g, D);
   // 4. eigenvectors of the m largest eigenvalues, scaled by lambda^-1/2
