@@ -438,10 +438,9 @@ const char* kvrp_last_error(void);
 /* Kernel launches that this host thread's last relocation call (kv_relocate_*)
  * or attention call (kv_attend_relocated) enqueued.  Relocation: the relocation
  * kernel, plus for a batch the small copy launches that carry its launch plan to
- * the device (31 KB of plan each).  Attention: the block and combine kernels,
- * plus the query-preparation kernel when some chunk's work starts late in a
- * block's share (2 or 3).  0 when the call returned an error or had nothing to
- * move. */
+ * the device (31 KB of plan each).  Attention: the block and combine kernels (2;
+ * the combine alone when no chunk has tokens).  0 when the call returned an
+ * error or had nothing to move. */
 int32_t kvrp_last_launch_count(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
