@@ -381,9 +381,10 @@ kvrp_status kv_patch_form_orbit(
  *   out         device bf16 [n_seqs][n_q_heads][head_dim]; a sequence with no
  *               tokens gets zeros.
  *   workspace   device scratch of kv_attend_relocated_workspace_size(...) bytes
- *               (fp32 partial results); the size depends
- *               on the current device's SM count, and the call returns WORKSPACE
- *               if it is smaller than the size for the device it runs on.
+ *               (fp32 partial results and which blocks hold them); its contents
+ *               need not survive between calls.  The size depends on the current
+ *               device's SM count, and the call returns WORKSPACE if it is smaller
+ *               than the size for the device it runs on.
  *   d_status    optional device word; KVRP_DEV_TIMEOUT is OR-ed in if an internal
  *               pipeline wait gave up (the output is then undefined).
  * Pointers 16-byte aligned.  Arithmetic fp32 on the bf16 inputs (rotation
