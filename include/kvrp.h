@@ -430,6 +430,21 @@ kvrp_status kv_attend_relocated(
  */
 void kvrp_test_set_wait_limit(uint32_t cycles);
 
+/*
+ * kvrp_test_attend_split -- for tests of the host-side planning only; no CUDA
+ * call.  The work split kv_attend_relocated gives n_cta blocks for chunks of
+ * these token counts and ranks (host arrays of n_chunks): the stage sequence
+ * (head group, chunk, stage) cut into contiguous shares of about equal bytes,
+ * counting each stage's K, V and factor rows and each segment's V_k, query and
+ * V_v slots.  Writes the boundaries share0[0 .. count] (share0 holds n_cta + 1
+ * entries) and returns count (<= n_cta, every share non-empty), 0 when no chunk
+ * has tokens, -1 on an invalid argument.  The other arguments are those of
+ * kv_attend_relocated.
+ */
+int32_t kvrp_test_attend_split(const int32_t* chunk_tokens, const int32_t* chunk_ranks, int32_t n_chunks,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t n_cta,
+                               int32_t* share0);
+
 /* Human-readable name of a status code (static string). */
 const char* kvrp_status_string(kvrp_status status);
 

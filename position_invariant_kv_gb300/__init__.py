@@ -30,6 +30,7 @@ from ._abi import (  # noqa: F401
     kvrp_status_string, kvrp_version, kvrp_last_launch_count, EXPORTED_SYMBOLS,
     kv_relocate_batch_noalloc, KVRP_NOALLOC_MAX_CHUNKS, chunk_array,
     kv_relocate_batch_mrope, kv_relocate_batch_mla, MlaChunk, mla_chunk_array, kvrp_test_set_wait_limit,
+    kvrp_test_attend_split,
     kv_patch_form, kv_patch_form_orbit, kv_patch_form_workspace_size,
     kv_attend_relocated, kv_attend_relocated_workspace_size, AttnChunk, attn_chunk_array, KVRP_ATTN_MAX_CHUNKS,
     KVRP_ROPE_NONE, KVRP_ROPE_HEADS, KVRP_ROPE_MLA_TAIL,

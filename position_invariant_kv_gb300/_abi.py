@@ -21,7 +21,7 @@ KVRP_DEV_TIMEOUT = 0x2
 EXPORTED_SYMBOLS = (
     "kv_relocate_patch", "kv_relocate_patch_mrope", "kv_relocate_patch_mla", "kv_relocate_batch",
     "kv_relocate_batch_workspace_size", "kv_relocate_batch_noalloc", "kv_relocate_batch_mrope",
-    "kv_relocate_batch_mla", "kvrp_test_set_wait_limit", "kv_patch_form_workspace_size",
+    "kv_relocate_batch_mla", "kvrp_test_set_wait_limit", "kvrp_test_attend_split", "kv_patch_form_workspace_size",
     "kv_patch_form", "kv_patch_form_orbit", "kv_attend_relocated_workspace_size", "kv_attend_relocated",
     "kvrp_status_string",
     "kvrp_last_error", "kvrp_last_launch_count", "kvrp_version",
@@ -99,6 +99,9 @@ def _load_library():
         C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
     L.kvrp_test_set_wait_limit.restype = None
     L.kvrp_test_set_wait_limit.argtypes = [C.c_uint32]
+    L.kvrp_test_attend_split.restype = C.c_int32
+    L.kvrp_test_attend_split.argtypes = [C.POINTER(C.c_int32), C.POINTER(C.c_int32), C.c_int32, C.c_int32,
+                                         C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_int32)]
     L.kv_relocate_batch_noalloc.restype = st
     L.kv_relocate_batch_noalloc.argtypes = [
         C.POINTER(kvrp_chunk), C.c_int32, C.c_int32, C.c_int32, C.c_int32, C.c_double, C.c_void_p,
@@ -355,6 +358,20 @@ def kvrp_test_set_wait_limit(cycles: int) -> None:
     """Testing hook: the relocation kernel's pipeline wait limit in cycles for
     plans built from now on (0 = the default, about one second)."""
     lib().kvrp_test_set_wait_limit(int(cycles))
+
+
+def kvrp_test_attend_split(tokens, ranks, *, n_q_heads: int, n_kv_heads: int, head_dim: int, n_cta: int):
+    """Testing hook: the share boundaries kv_attend_relocated would give n_cta
+    blocks for chunks of these token counts and ranks (a list of count + 1
+    stage indices), [] when no chunk has tokens; ValueError on invalid input."""
+    n = len(tokens)
+    t = (C.c_int32 * n)(*[int(x) for x in tokens])
+    r = (C.c_int32 * n)(*[int(x) for x in ranks])
+    out = (C.c_int32 * (int(n_cta) + 1))()
+    cnt = lib().kvrp_test_attend_split(t, r, n, int(n_q_heads), int(n_kv_heads), int(head_dim), int(n_cta), out)
+    if cnt < 0:
+        raise ValueError("kvrp_test_attend_split: invalid arguments")
+    return [out[i] for i in range(cnt + 1)] if cnt > 0 else []
 
 
 def kv_relocate_batch_noalloc(chunks, *, n_layers: int, n_kv_heads: int, head_dim: int,

@@ -953,6 +953,40 @@ using namespace kvrp;
 
 extern "C" {
 
+int32_t kvrp_test_attend_split(const int32_t* chunk_tokens, const int32_t* chunk_ranks, int32_t n_chunks,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t n_cta,
+                               int32_t* share0) {
+  if (!chunk_tokens || !chunk_ranks || !share0 || n_chunks <= 0 || n_chunks > attn::kMaxChunks || n_kv_heads <= 0 ||
+      n_q_heads <= 0 || n_q_heads % n_kv_heads || (head_dim != 64 && head_dim != 128) || n_cta <= 0 ||
+      n_cta > attn::kMaxCtas)
+    return -1;
+  int m_max = 0;
+  for (int i = 0; i < n_chunks; ++i) {
+    if (chunk_tokens[i] < 0 || chunk_ranks[i] < 0 || chunk_ranks[i] > attn::kMaxRank) return -1;
+    m_max = std::max(m_max, (int)chunk_ranks[i]);
+  }
+  const attn::Plan pl = attn::make_plan(n_kv_heads, head_dim, m_max, n_q_heads / n_kv_heads);
+  std::vector<uint8_t> mem(sizeof(attn::Params), 0);   // ~29 KB: off the stack
+  attn::Params& p = *reinterpret_cast<attn::Params*>(mem.data());
+  p.n_chunks = n_chunks;
+  p.g = n_q_heads / n_kv_heads;
+  p.hg = pl.hg;
+  p.n_hg = pl.n_hg;
+  p.ts = pl.ts;
+  int64_t st0 = 0;
+  for (int i = 0; i < n_chunks; ++i) {
+    p.c[i].n_tokens = chunk_tokens[i];
+    p.c[i].rank = chunk_ranks[i];
+    p.c[i].st0 = (int32_t)st0;
+    st0 += (chunk_tokens[i] + pl.ts - 1) / pl.ts;
+  }
+  p.s_hg = st0;
+  const int64_t total = (int64_t)p.n_hg * p.s_hg;
+  if (total == 0) return 0;
+  if (total > INT32_MAX) return -1;
+  return attn::split_shares(p, (int)std::min<int64_t>(n_cta, total), head_dim, share0);
+}
+
 size_t kv_attend_relocated_workspace_size(int32_t n_chunks, const int32_t* chunk_tokens, int32_t n_q_heads,
                                           int32_t n_kv_heads, int32_t head_dim) {
   if (n_chunks <= 0 || !chunk_tokens || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads || head_dim <= 0)
