@@ -12,6 +12,12 @@ import pytest
 SEGMENT_ALLOWANCE = 16384   # bytes a segment is charged beyond its slots (partial, pipeline turn)
 
 
+@pytest.fixture(scope="module", autouse=True)
+def library():
+    from position_invariant_kv_gb300.build import build
+    build()
+
+
 def plan(n_q_heads, n_kv_heads, head_dim):
     hg = 4 if n_kv_heads % 4 == 0 else 2 if n_kv_heads % 2 == 0 else 1
     return hg, n_kv_heads // hg, 64 // hg, n_q_heads // n_kv_heads
