@@ -957,8 +957,8 @@ int32_t kvrp_test_attend_split(const int32_t* chunk_tokens, const int32_t* chunk
                                int32_t n_q_heads, int32_t n_kv_heads, int32_t head_dim, int32_t n_cta,
                                int32_t* share0) {
   if (!chunk_tokens || !chunk_ranks || !share0 || n_chunks <= 0 || n_chunks > attn::kMaxChunks || n_kv_heads <= 0 ||
-      n_q_heads <= 0 || n_q_heads % n_kv_heads || (head_dim != 64 && head_dim != 128) || n_cta <= 0 ||
-      n_cta > attn::kMaxCtas)
+      n_q_heads <= 0 || n_q_heads % n_kv_heads || n_q_heads / n_kv_heads > attn::kMaxGroup ||
+      (head_dim != 64 && head_dim != 128) || n_cta <= 0 || n_cta > attn::kMaxCtas)
     return -1;
   int m_max = 0;
   for (int i = 0; i < n_chunks; ++i) {

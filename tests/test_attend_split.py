@@ -120,3 +120,5 @@ def test_no_tokens_and_bad_arguments():
         split([100], [16], 8, 4, 96, 304)     # head_dim 96
     with pytest.raises(ValueError):
         split([100], [16], 8, 4, 128, 0)      # no blocks
+    with pytest.raises(ValueError):
+        split([100], [16], 34, 2, 128, 304)   # 17 query heads per KV head
