@@ -100,3 +100,27 @@ def test_e2e_leg_fits_host_memory():
     assert bench.e2e_layers(wl, int(per_layer * 10.5)) == 10
     assert bench.e2e_layers(wl, 1) == 1
     assert bench.host_budget_bytes() > 0
+
+
+def test_method_bytes_of_patch_formation_and_attention():
+    """The bytes the roofline fractions divide by, counted by hand for small shapes.
+    Patch formation, per tensor: the caches read once (the conditioned ones orbit times),
+    the bf16 deficit written twice, read by each of the 2q + 3 tensor-core passes, each
+    pass's fp32 output, the Gram's and the apply's reads in each of the 2q + 2
+    orthonormalisation rounds, and the bf16 factors.  Decode attention: every chunk's K,
+    V and factor rows, V_k and V_v, and the queries in and the output out."""
+    import bench
+    L, T, D, m, p, q, orbit = 2, 100, 64, 16, 8, 1, 1
+    kp = 32                                     # m + p padded to 16
+    n = L * T * D
+    skinny = L * (T + D) * kp * 4
+    want = (2 * n * 2                           # canonical and one conditioned cache, bf16
+            + 2 * n * 2                         # the deficit written as rows and as transposed rows
+            + 5 * n * 2                         # 2q + 3 passes read it
+            + 5 * skinny                        # each pass writes its fp32 output
+            + 4 * 2 * skinny                    # 2q + 2 rounds: the Gram's and the apply's reads
+            + L * (T + D) * m * 2)              # the factors U, V in bf16
+    assert bench.patch_bytes(L, T, D, m, p, q, orbit) == want
+    a = dict(seqs=2, chunks=3, tokens=100, Hq=8, Hkv=2, d=64, rank=16)
+    per_chunk = 100 * 128 * 2 * 2 + 100 * 16 * 2 * 2 + 128 * 16 * 2 * 2
+    assert bench.attn_bytes(a) == 6 * per_chunk + 2 * 8 * 64 * 2 * 2
