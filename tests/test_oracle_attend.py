@@ -120,3 +120,30 @@ def test_chunks_concatenate_along_the_context():
     k2, v2 = relocated_chunk(c2["k"], c2["v"], -9, 1e4, H, d)
     want = attention(bf16_bits_to_f64(q), np.concatenate([k1, k2]), np.concatenate([v1, v2]), Hq, H, d, 0.5)
     assert np.allclose(both, want, atol=1e-14)
+
+
+def test_conditioning_sum_against_hand_values():
+    """The magnitude term of the attention parity bar, sum_t p_t |v^_t| per output element
+    (oracle.attend_conditioning), pinned on both sides with hand values.
+    - Two tokens whose scores differ by ln 3 give weights 3/4 and 1/4.
+    - Their values have opposite signs, so |sum p v| (a plausible slip) differs from
+      sum p |v|.
+    - Unnormalised or uniform weights differ too.
+    - A rank-1 value patch that moves token 1's first element from 1 to -3 changes that
+      element's term to 3/4 * 3 + 1/4 * 3."""
+    from oracle import attend_conditioning
+    k = _bits([[1.0, 0.0, 0.0, 0.0], [0.0, 0.0, 0.0, 0.0]])
+    v = _bits([[1.0, -2.0, 0.5, 4.0], [-3.0, 2.0, 0.5, -4.0]])
+    q = _bits([1.0, 0.0, 0.0, 0.0])
+    scale = math.log(3.0)                       # scores ln 3 and 0
+    got = attend_conditioning(q, [{"k": k, "v": v, "delta": 0}], 1, 1, 4, 1e4, scale)
+    want = 0.75 * np.abs([1.0, -2.0, 0.5, 4.0]) + 0.25 * np.abs([-3.0, 2.0, 0.5, -4.0])
+    assert np.allclose(got, want, rtol=1e-14, atol=0)          # [1.5, 2.0, 0.5, 4.0]
+    assert not np.allclose(got, np.abs(0.75 * np.array([1.0, -2.0, 0.5, 4.0]) + 0.25 * np.array([-3.0, 2.0, 0.5, -4.0])))
+    uv = _bits([[1.0], [0.0]])                  # token 1 only
+    vv = _bits([[-4.0], [0.0], [0.0], [0.0]])   # feature 0 only
+    got2 = attend_conditioning(q, [{"k": k, "v": v, "delta": 0, "rank": 1, "uk": None, "vk": None, "uv": uv,
+                                    "vv": vv}], 1, 1, 4, 1e4, scale)
+    want2 = want.copy()
+    want2[0] = 0.75 * 3.0 + 0.25 * 3.0
+    assert np.allclose(got2, want2, rtol=1e-14, atol=0)
