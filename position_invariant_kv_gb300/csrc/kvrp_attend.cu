@@ -160,7 +160,6 @@ __device__ __forceinline__ int share_of(const Params& p, int64_t f) {
 struct Cursor {
   int hg, c, k, nst;
 };
-__device__ __forceinline__ int chunk_stages(const Params& p, int ci) { return (p.c[ci].n_tokens + p.ts - 1) / p.ts; }
 __device__ __forceinline__ Cursor cursor_at(const Params& p, int64_t f) {
   Cursor r;
   r.hg = (int)(f / p.s_hg);
