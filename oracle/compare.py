@@ -1,4 +1,4 @@
-"""The parity rule used to judge a bf16 result against the fp64 oracle
+"""The parity rule that decides whether a bf16 result agrees with the fp64 oracle
 (test infrastructure only).
 
 An element passes when its bf16 value is within 1 bf16 ulp of the oracle

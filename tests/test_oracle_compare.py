@@ -1,4 +1,4 @@
-"""Pins for the two acceptance helpers the GPU tests judge with: the parity
+"""Pins for the two acceptance helpers the GPU tests decide with: the parity
 rule of oracle.compare (within 1 bf16 ulp of the fp64 result rounded to bf16,
 or a counted mismatch inside the conditioned bound) and the attention
 conditioning sum of oracle.attend (sum over tokens of p_t |V^_t|).  They are
